@@ -1,0 +1,178 @@
+/*
+ * flamia.h — C ABI of the block-scaled causal attention training call
+ * (FLAMIA-style MXFP8 and mixed NVFP4/FP8 paths) for one GB300 (sm_103a).
+ *
+ * Sources, by page title and section:
+ *   [SUM]  "FLAMIA: FLAsh MIcroscaling Attention for Fast and Causally Safe
+ *          Training on Blackwell" (paper summary), bullets under §3.1–§3.7,
+ *          §4.1–§4.6.
+ *   [READ] "因果安全的低精度注意力——FLAMIA Blackwell 训练内核精读"
+ *          (close reading), 四 4.1–4.6 and 五 5.1–5.3.
+ *
+ * One training call is, in this order, on one CUDA stream:
+ *   flamia_plan        -> work lists and document tables (once per cu_seqlens)
+ *   flamia_quantize    -> role QKV: Q^, K^, V^ codes and scales
+ *   flamia_fwd         -> O, per-row (m, l)
+ *   flamia_quantize    -> role DO: dO^ codes and scales, D = rowsum(dO^ * O)
+ *   flamia_bwd         -> dQ, dK, dV
+ * ([READ] 五 5.1: the training call is forward + backward + quantization.)
+ *
+ * Conventions for every entry point:
+ *   - Every pointer named "device" is a CUDA device pointer owned by the
+ *     caller; the library never allocates, frees or synchronises inside
+ *     plan/quantize/fwd/bwd, so the sequence can be captured in a CUDA graph.
+ *   - Packed token-major layouts: activations [T][heads][d] (row-major, d
+ *     contiguous); per-token metadata [heads][T].
+ *   - All device pointers must be 16-byte aligned; tensors are contiguous.
+ *   - Arguments are validated on the host before any launch; a violation
+ *     returns FLAMIA_ERR_INVALID_ARG or FLAMIA_ERR_UNSUPPORTED and launches
+ *     nothing.  Launch failures return FLAMIA_ERR_CUDA.  Device-side
+ *     conditions (a bounded wait that expired, an inconsistent cu_seqlens
+ *     seen by a kernel) set the device status word in the workspace, read
+ *     with flamia_get_device_status().
+ *   - The workspace `ws` (size from flamia_workspace_size) holds the plan,
+ *     the fp32 dQ accumulator and the status word.  It must stay the same
+ *     buffer from flamia_plan through flamia_bwd of one call.
+ */
+#ifndef FLAMIA_H_
+#define FLAMIA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FLAMIA_OK = 0,
+  FLAMIA_ERR_INVALID_ARG = 1,
+  FLAMIA_ERR_UNSUPPORTED = 2,
+  FLAMIA_ERR_WORKSPACE_TOO_SMALL = 3,
+  FLAMIA_ERR_CUDA = 4,
+  FLAMIA_ERR_TIMEOUT = 5,
+  FLAMIA_ERR_BAD_SEQLENS = 6
+} flamia_status_t;
+
+/* [SUM] §3.4: the two default training paths. */
+typedef enum { FLAMIA_PATH_MXFP8 = 0, FLAMIA_PATH_NVFP4_FP8 = 1 } flamia_path_t;
+
+typedef enum { FLAMIA_F32 = 0, FLAMIA_BF16 = 1 } flamia_dtype_t;
+
+typedef enum { FLAMIA_ROLE_QKV = 0, FLAMIA_ROLE_DO = 1 } flamia_role_t;
+
+/* Problem description (host struct; cu_seqlens is a device pointer).
+ *   T            total packed tokens (>= 1)
+ *   H, Hkv       query heads and key/value heads; H % Hkv == 0 (GQA)
+ *   d            head dimension: 64 or 128
+ *   n_seq        documents; cu_seqlens[0] = 0, cu_seqlens[n_seq] = T,
+ *                non-decreasing (device int32 [n_seq + 1]); an empty document
+ *                is allowed.  Batched equal-length input is
+ *                {0, L, 2L, ...} ([SUM] §3.6.2: packed documents in place).
+ *   causal       1: query i sees keys j <= i of its own document; 0: the whole
+ *                document.
+ *   exact        1: the exact option ([SUM] §4.5): per-token Q, K and dO
+ *                scales, per-(row, 32-key) dS exponents for dQ, deterministic
+ *                dQ.  0: token-block scales over 32 document-local tokens.
+ *   causal_dq_scale  accepted; with fp32 dQ accumulation it changes nothing
+ *                ([SUM] §4.5 introduces it for FP16 accumulators).
+ *   deterministic 1: dQ reduced in a fixed order (no atomics).
+ *   softmax_scale  0 selects 1/sqrt(d).
+ *   path         flamia_path_t.
+ *   in_dtype     dtype of Q, K, V, dO, O inputs (FLAMIA_BF16 or FLAMIA_F32).
+ *   out_dtype    dtype of O, dQ, dK, dV outputs.
+ */
+typedef struct {
+  int32_t T, H, Hkv, d, n_seq;
+  const int32_t* cu_seqlens;
+  int32_t causal, exact, causal_dq_scale, deterministic;
+  float softmax_scale;
+  int32_t path, in_dtype, out_dtype;
+} flamia_problem_t;
+
+/* A quantized operand (device pointers, caller-owned).
+ *   codes    uint8 [T][heads][d] E4M3FN codes.  One payload serves both MMA
+ *            orientations ([SUM] §3.1).
+ *   scales   uint8 [heads][T] UE8M0 exponent byte (e + 127) of each token's
+ *            block, replicated per token ([SUM] §3.6.2: per-token scale
+ *            metadata).  V always has one exponent per key ([SUM] abstract).
+ *   codes4   mixed path, Q and K only: uint8 [T][heads][d/2], two E2M1 codes
+ *            per byte, element 2k in the low nibble.
+ *   scales4  mixed path, Q and K only: uint8 [T][heads][d/16] E4M3 block scales.
+ *   gscale4  mixed path, Q and K only: float [heads][T] per-token fp32 scale.
+ * Unused members may be NULL. */
+typedef struct {
+  void* codes;
+  void* scales;
+  void* codes4;
+  void* scales4;
+  void* gscale4;
+} flamia_operand_t;
+
+/* Bytes of device workspace needed by plan/quantize/fwd/bwd for `p`
+ * (0 if `p` is invalid). */
+size_t flamia_workspace_size(const flamia_problem_t* p);
+
+/* Builds, on the GPU, the document tables and the longest-first work lists
+ * ([SUM] §3.6.2 and [READ] 4.4: a fixed-pass merge sort on the GPU, once per
+ * microbatch, items issued to a persistent grid in descending cost).
+ * Forward items are (document, 128-query tile) with cost = key tiles visited;
+ * backward items are (document, 128-key tile) with cost = query tiles
+ * visited; ties keep document order.  Reads cu_seqlens on the device only. */
+flamia_status_t flamia_plan(const flamia_problem_t* p, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Fused quantizer ([SUM] §3.1, §3.2; [READ] 4.4 fused quantization).
+ * role FLAMIA_ROLE_QKV: in = {Q [T][H][d], K [T][Hkv][d], V [T][Hkv][d]},
+ *   out = {Q^, K^, V^} operands.  Q and K: token-block exponent over 32
+ *   document-local tokens x d (per token in the exact option); V: per key.
+ *   Exponent = smallest e with max|x| <= 448 * 2^e (nothing clamps), clamped
+ *   to [-127, 127]; all-zero blocks take e = 0; codes RNE(x * 2^-e).
+ *   Mixed path: Q and K also get the NVFP4 payload (codes4/scales4/gscale4).
+ * role FLAMIA_ROLE_DO: in = {dO [T][H][d]}, O = the forward output as stored
+ *   (out_dtype), out = {dO^}; also writes D (device float [H][T]),
+ *   D_i = sum_d dO^_id * O_id from the same dO^ that feeds dP ([SUM] §3.3).
+ * Requires flamia_plan on the same workspace. */
+flamia_status_t flamia_quantize(const flamia_problem_t* p, int32_t role, const void* const* in, const void* O,
+                                const flamia_operand_t* out, float* D, void* ws, size_t ws_bytes,
+                                cudaStream_t stream);
+
+/* Forward ([SUM] §3.1–§3.3; [READ] 4.1–4.4): S = Q^ K^T, online softmax over
+ * key tiles with an integer row reference, P^ quantized to E4M3 with one
+ * exponent per (row, 32-key block) after the per-key V factor is folded in,
+ * O += P^ V^ by a block-scaled MMA, O = acc / l.
+ *   O  device [T][H][d] out_dtype
+ *   m  device int32 [H][T]: the row's integer reference exponent
+ *   l  device float [H][T]: sum_j 2^(x_ij - m_i), x = S * softmax_scale * log2(e)
+ * Requires flamia_plan on the same workspace. */
+flamia_status_t flamia_fwd(const flamia_problem_t* p, const flamia_operand_t* q, const flamia_operand_t* k,
+                           const flamia_operand_t* v, void* O, int32_t* m, float* l, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
+
+/* Backward ([SUM] §3.3; [READ] 4.3): recomputes S and P^ from the same Q^/K^
+ * with the forward's tiling and exponent evaluation, dP = dO^ V^T,
+ * dS = P (dP - D), dS quantized with one exponent per 32x32 block (the exact
+ * option: per (row, 32 keys) for dQ), dV += P~^T dO^, dK += dS^T Q^,
+ * dQ += dS K^, all accumulated in fp32; GQA sums dK/dV over the group.
+ *   dQ device [T][H][d], dK/dV device [T][Hkv][d], out_dtype.
+ * D, m, l as produced by flamia_quantize(DO) and flamia_fwd. */
+flamia_status_t flamia_bwd(const flamia_problem_t* p, const flamia_operand_t* q, const flamia_operand_t* k,
+                           const flamia_operand_t* v, const flamia_operand_t* dO, const float* D, const int32_t* m,
+                           const float* l, void* dQ, void* dK, void* dV, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
+
+/* Reads and returns the device status word of `ws` (FLAMIA_OK,
+ * FLAMIA_ERR_TIMEOUT or FLAMIA_ERR_BAD_SEQLENS).  Synchronises `stream`:
+ * for tests and diagnostics, not for the hot path. */
+flamia_status_t flamia_get_device_status(const void* ws, cudaStream_t stream);
+
+/* Clears the device status word (stream-ordered, no synchronisation). */
+flamia_status_t flamia_clear_device_status(void* ws, cudaStream_t stream);
+
+/* Static description of a status code. */
+const char* flamia_status_string(flamia_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FLAMIA_H_ */

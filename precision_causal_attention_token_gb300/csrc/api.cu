@@ -1,0 +1,255 @@
+// api.cu — the C ABI (include/flamia.h): host-side validation, workspace
+// layout, TMA descriptors and kernel launches.  No allocation, no host
+// synchronisation on the plan/quantize/fwd/bwd paths.
+#include <cmath>
+#include <cstring>
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+
+using namespace flamia;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+flamia_status_t validate(const flamia_problem_t* p) {
+  if (!p) return FLAMIA_ERR_INVALID_ARG;
+  if (p->T < 1 || p->H < 1 || p->Hkv < 1 || p->n_seq < 1 || !p->cu_seqlens) return FLAMIA_ERR_INVALID_ARG;
+  if (p->H % p->Hkv != 0) return FLAMIA_ERR_INVALID_ARG;
+  if (p->d != 64 && p->d != 128) return FLAMIA_ERR_UNSUPPORTED;
+  if ((int64_t)p->T * p->H * p->d >= (int64_t)1 << 40) return FLAMIA_ERR_UNSUPPORTED;
+  if (p->T > (1 << 30) || p->n_seq > p->T + 1) return FLAMIA_ERR_INVALID_ARG;
+  if (p->path != FLAMIA_PATH_MXFP8 && p->path != FLAMIA_PATH_NVFP4_FP8) return FLAMIA_ERR_UNSUPPORTED;
+  if ((p->in_dtype != FLAMIA_F32 && p->in_dtype != FLAMIA_BF16) ||
+      (p->out_dtype != FLAMIA_F32 && p->out_dtype != FLAMIA_BF16))
+    return FLAMIA_ERR_UNSUPPORTED;
+  if (!(p->softmax_scale >= 0.f) || std::isinf(p->softmax_scale)) return FLAMIA_ERR_INVALID_ARG;
+  if (!aligned16(p->cu_seqlens) && (reinterpret_cast<uintptr_t>(p->cu_seqlens) & 3u)) return FLAMIA_ERR_INVALID_ARG;
+  return FLAMIA_OK;
+}
+
+flamia_status_t check_ws(const flamia_problem_t* p, void* ws, size_t ws_bytes, WsLayout* L) {
+  *L = ws_layout(*p);
+  if (!ws || !aligned16(ws)) return FLAMIA_ERR_INVALID_ARG;
+  if (ws_bytes < L->total) return FLAMIA_ERR_WORKSPACE_TOO_SMALL;
+  return FLAMIA_OK;
+}
+
+float softmax_scale_of(const flamia_problem_t* p) {
+  return p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / std::sqrt((float)p->d);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// 3-D map over E4M3 codes [T][heads][d]: box = 128 tokens x 1 head x d bytes,
+// swizzle = d bytes (128B or 64B), out-of-range rows read as zero.
+bool make_codes_map(CUtensorMap* m, const void* ptr, int d, int heads, int T) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)heads * d};
+  cuuint32_t box[3] = {(cuuint32_t)d, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool operand_ok(const flamia_operand_t* o) { return o && o->codes && o->scales && aligned16(o->codes); }
+
+}  // namespace
+
+extern "C" {
+
+size_t flamia_workspace_size(const flamia_problem_t* p) {
+  if (validate(p) != FLAMIA_OK) return 0;
+  return ws_layout(*p).total;
+}
+
+const char* flamia_status_string(flamia_status_t s) {
+  switch (s) {
+    case FLAMIA_OK: return "ok";
+    case FLAMIA_ERR_INVALID_ARG: return "invalid argument";
+    case FLAMIA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FLAMIA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case FLAMIA_ERR_CUDA: return "CUDA launch error";
+    case FLAMIA_ERR_TIMEOUT: return "device wait timed out";
+    case FLAMIA_ERR_BAD_SEQLENS: return "cu_seqlens inconsistent with T";
+  }
+  return "unknown status";
+}
+
+flamia_status_t flamia_plan(const flamia_problem_t* p, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  flamia_status_t s = validate(p);
+  if (s != FLAMIA_OK) return s;
+  WsLayout L;
+  if ((s = check_ws(p, ws, ws_bytes, &L)) != FLAMIA_OK) return s;
+  return launch_plan(*p, L, static_cast<uint8_t*>(ws), stream) == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+}
+
+flamia_status_t flamia_quantize(const flamia_problem_t* p, int32_t role, const void* const* in, const void* O,
+                                const flamia_operand_t* out, float* D, void* ws, size_t ws_bytes,
+                                cudaStream_t stream) {
+  flamia_status_t s = validate(p);
+  if (s != FLAMIA_OK) return s;
+  WsLayout L;
+  if ((s = check_ws(p, ws, ws_bytes, &L)) != FLAMIA_OK) return s;
+  if (!in || !out) return FLAMIA_ERR_INVALID_ARG;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(w + L.header);
+  const int32_t* blk = reinterpret_cast<const int32_t*>(w + L.blk32_prefix);
+  const int max_blk = (p->T + 31) / 32 + p->n_seq;
+  const int in_bf16 = p->in_dtype == FLAMIA_BF16, o_bf16 = p->out_dtype == FLAMIA_BF16;
+  if (role == FLAMIA_ROLE_QKV) {
+    for (int i = 0; i < 3; ++i) {
+      if (!in[i] || !aligned16(in[i]) || !operand_ok(&out[i])) return FLAMIA_ERR_INVALID_ARG;
+    }
+    const bool nv = p->path == FLAMIA_PATH_NVFP4_FP8;
+    for (int i = 0; i < 3; ++i) {
+      QuantArgs a{};
+      a.x = in[i];
+      a.codes = static_cast<uint8_t*>(out[i].codes);
+      a.scales = static_cast<uint8_t*>(out[i].scales);
+      a.heads = i == 0 ? p->H : p->Hkv;
+      a.T = p->T;
+      a.per_token = (i == 2 || p->exact) ? 1 : 0;
+      const bool nv_i = nv && i < 2;
+      if (nv_i) {
+        if (!out[i].codes4 || !out[i].scales4 || !out[i].gscale4) return FLAMIA_ERR_INVALID_ARG;
+        a.codes4 = static_cast<uint8_t*>(out[i].codes4);
+        a.scales4 = static_cast<uint8_t*>(out[i].scales4);
+        a.gscale4 = static_cast<float*>(out[i].gscale4);
+      }
+      if (launch_quantize(a, p->d, in_bf16, o_bf16, false, nv_i, p->cu_seqlens, blk, p->n_seq, hdr,
+                          max_blk * a.heads, stream) != cudaSuccess)
+        return FLAMIA_ERR_CUDA;
+    }
+    return FLAMIA_OK;
+  }
+  if (role == FLAMIA_ROLE_DO) {
+    if (!in[0] || !aligned16(in[0]) || !O || !aligned16(O) || !D || !operand_ok(&out[0]))
+      return FLAMIA_ERR_INVALID_ARG;
+    QuantArgs a{};
+    a.x = in[0];
+    a.codes = static_cast<uint8_t*>(out[0].codes);
+    a.scales = static_cast<uint8_t*>(out[0].scales);
+    a.O = O;
+    a.D = D;
+    a.heads = p->H;
+    a.T = p->T;
+    a.per_token = p->exact ? 1 : 0;
+    return launch_quantize(a, p->d, in_bf16, o_bf16, true, false, p->cu_seqlens, blk, p->n_seq, hdr,
+                           max_blk * p->H, stream) == cudaSuccess
+               ? FLAMIA_OK
+               : FLAMIA_ERR_CUDA;
+  }
+  return FLAMIA_ERR_INVALID_ARG;
+}
+
+static flamia_status_t fill_params(const flamia_problem_t* p, const WsLayout& L, void* ws, AttnParams* a) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  std::memset(a, 0, sizeof(*a));
+  a->T = p->T; a->H = p->H; a->Hkv = p->Hkv; a->d = p->d; a->n_seq = p->n_seq;
+  a->causal = p->causal ? 1 : 0;
+  a->exact = p->exact ? 1 : 0;
+  a->out_bf16 = p->out_dtype == FLAMIA_BF16;
+  a->max_items = L.max_items;
+  a->softmax_scale = softmax_scale_of(p);
+  a->c_log2 = (float)((double)a->softmax_scale * 1.4426950408889634);
+  a->cu = p->cu_seqlens;
+  a->tile_prefix = reinterpret_cast<const int32_t*>(w + L.tile_prefix);
+  a->fwd_items = reinterpret_cast<const int2*>(w + L.fwd_items);
+  a->bwd_items = reinterpret_cast<const int2*>(w + L.bwd_items);
+  a->hdr = reinterpret_cast<WsHeader*>(w + L.header);
+  a->dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
+  return FLAMIA_OK;
+}
+
+flamia_status_t flamia_fwd(const flamia_problem_t* p, const flamia_operand_t* q, const flamia_operand_t* k,
+                           const flamia_operand_t* v, void* O, int32_t* m, float* l, void* ws, size_t ws_bytes,
+                           cudaStream_t stream) {
+  flamia_status_t s = validate(p);
+  if (s != FLAMIA_OK) return s;
+  WsLayout L;
+  if ((s = check_ws(p, ws, ws_bytes, &L)) != FLAMIA_OK) return s;
+  if (!operand_ok(q) || !operand_ok(k) || !operand_ok(v) || !O || !aligned16(O) || !m || !l)
+    return FLAMIA_ERR_INVALID_ARG;
+  if (p->path == FLAMIA_PATH_NVFP4_FP8 && (!q->codes4 || !q->scales4 || !q->gscale4 || !k->codes4 ||
+                                           !k->scales4 || !k->gscale4))
+    return FLAMIA_ERR_INVALID_ARG;
+  if (p->path == FLAMIA_PATH_NVFP4_FP8) return FLAMIA_ERR_UNSUPPORTED;  // scores in NVFP4: not built yet
+  AttnParams a;
+  fill_params(p, L, ws, &a);
+  a.q_sc = static_cast<const uint8_t*>(q->scales);
+  a.k_sc = static_cast<const uint8_t*>(k->scales);
+  a.v_sc = static_cast<const uint8_t*>(v->scales);
+  a.O = O; a.m = m; a.l = l;
+  AttnMaps maps;
+  if (!make_codes_map(&maps.q, q->codes, p->d, p->H, p->T) || !make_codes_map(&maps.k, k->codes, p->d, p->Hkv, p->T) ||
+      !make_codes_map(&maps.v, v->codes, p->d, p->Hkv, p->T))
+    return FLAMIA_ERR_CUDA;
+  maps.dO = maps.q;
+  return launch_fwd(a, maps, stream) == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+}
+
+flamia_status_t flamia_bwd(const flamia_problem_t* p, const flamia_operand_t* q, const flamia_operand_t* k,
+                           const flamia_operand_t* v, const flamia_operand_t* dO, const float* D, const int32_t* m,
+                           const float* l, void* dQ, void* dK, void* dV, void* ws, size_t ws_bytes,
+                           cudaStream_t stream) {
+  flamia_status_t s = validate(p);
+  if (s != FLAMIA_OK) return s;
+  WsLayout L;
+  if ((s = check_ws(p, ws, ws_bytes, &L)) != FLAMIA_OK) return s;
+  if (!operand_ok(q) || !operand_ok(k) || !operand_ok(v) || !operand_ok(dO) || !D || !m || !l || !dQ || !dK ||
+      !dV || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
+    return FLAMIA_ERR_INVALID_ARG;
+  if (p->path == FLAMIA_PATH_NVFP4_FP8) return FLAMIA_ERR_UNSUPPORTED;
+  AttnParams a;
+  fill_params(p, L, ws, &a);
+  a.q_sc = static_cast<const uint8_t*>(q->scales);
+  a.k_sc = static_cast<const uint8_t*>(k->scales);
+  a.v_sc = static_cast<const uint8_t*>(v->scales);
+  a.do_sc = static_cast<const uint8_t*>(dO->scales);
+  a.D = D;
+  a.m = const_cast<int32_t*>(m);
+  a.l = const_cast<float*>(l);
+  a.dQ = dQ; a.dK = dK; a.dV = dV;
+  AttnMaps maps;
+  if (!make_codes_map(&maps.q, q->codes, p->d, p->H, p->T) || !make_codes_map(&maps.k, k->codes, p->d, p->Hkv, p->T) ||
+      !make_codes_map(&maps.v, v->codes, p->d, p->Hkv, p->T) || !make_codes_map(&maps.dO, dO->codes, p->d, p->H, p->T))
+    return FLAMIA_ERR_CUDA;
+  if (cudaMemsetAsync(a.dq_acc, 0, sizeof(float) * (size_t)p->T * p->H * p->d, stream) != cudaSuccess)
+    return FLAMIA_ERR_CUDA;
+  if (launch_bwd(a, maps, stream) != cudaSuccess) return FLAMIA_ERR_CUDA;
+  return launch_dq_convert(a, stream) == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+}
+
+flamia_status_t flamia_get_device_status(const void* ws, cudaStream_t stream) {
+  if (!ws) return FLAMIA_ERR_INVALID_ARG;
+  uint32_t st = 0;
+  if (cudaMemcpyAsync(&st, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return FLAMIA_ERR_CUDA;
+  return static_cast<flamia_status_t>(st);
+}
+
+flamia_status_t flamia_clear_device_status(void* ws, cudaStream_t stream) {
+  if (!ws) return FLAMIA_ERR_INVALID_ARG;
+  return cudaMemsetAsync(ws, 0, 2 * sizeof(uint32_t), stream) == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,315 @@
+// common.cuh — device helpers shared by the kernels: workspace layout,
+// status word, fp8/fp4 conversions, mbarrier, TMA and tcgen05 wrappers.
+// Everything is sm_103a inline PTX written against the PTX ISA (CUDA 13.0).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda.h>
+
+#include "../../include/flamia.h"
+
+namespace flamia {
+
+// ---------------------------------------------------------------------------
+// Workspace layout (device bytes, all offsets 256-aligned).
+// ---------------------------------------------------------------------------
+struct WsHeader {
+  uint32_t status;         // flamia_status_t of the first device-side failure
+  uint32_t status_where;   // kernel tag + site of that failure
+  int32_t n_items;         // tiles (document, 128-token tile) in the plan
+  int32_t n_blk32;         // document-local 32-token blocks
+  uint32_t fwd_counter;    // persistent-grid work counters (reset per launch)
+  uint32_t bwd_counter;
+  uint32_t dq_counter;
+  uint32_t pad[57];
+};
+static_assert(sizeof(WsHeader) == 256, "header");
+
+struct WsLayout {
+  size_t header, tile_prefix, blk32_prefix, fwd_items, bwd_items, keys_a, keys_b, dq_acc, total;
+  int32_t max_items;       // upper bound of tiles: ceil(T/128) + n_seq
+  int32_t sort_n;          // max_items rounded up to the block-sort size
+};
+
+constexpr int kSortBlock = 2048;
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline WsLayout ws_layout(const flamia_problem_t& p) {
+  WsLayout L{};
+  L.max_items = (p.T + 127) / 128 + p.n_seq;
+  L.sort_n = ((L.max_items + kSortBlock - 1) / kSortBlock) * kSortBlock;
+  size_t o = 0;
+  L.header = o; o = align256(o + sizeof(WsHeader));
+  L.tile_prefix = o; o = align256(o + sizeof(int32_t) * (p.n_seq + 1));
+  L.blk32_prefix = o; o = align256(o + sizeof(int32_t) * (p.n_seq + 1));
+  L.fwd_items = o; o = align256(o + sizeof(int2) * L.max_items);
+  L.bwd_items = o; o = align256(o + sizeof(int2) * L.max_items);
+  L.keys_a = o; o = align256(o + sizeof(uint64_t) * L.sort_n * 2);
+  L.keys_b = o; o = align256(o + sizeof(uint64_t) * L.sort_n * 2);
+  L.dq_acc = o; o = align256(o + sizeof(float) * (size_t)p.T * p.H * p.d);
+  L.total = o;
+  return L;
+}
+
+// Device-side failure report: first writer wins.
+__device__ __forceinline__ void report(WsHeader* hdr, uint32_t code, uint32_t where) {
+  if (atomicCAS(&hdr->status, 0u, code) == 0u) hdr->status_where = where;
+}
+
+// ---------------------------------------------------------------------------
+// Numeric helpers.
+// ---------------------------------------------------------------------------
+// 2^e as fp32 for e in [-126, 127] (built from the exponent field).
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// The no-clamp exponent of a non-negative fp32 amax: the smallest integer e
+// with amax <= 448 * 2^e, clamped to [-127, 127]; 0 for amax == 0.
+// amax = 1.m * 2^(E-127) = (1.m / 2) * 2^(E-126): e = E-135 when 1.m <= 1.75,
+// else E-134.  Subnormal amax lies far below 448 * 2^-127 and clamps to -127.
+__device__ __forceinline__ int noclamp_exp_clamped(float amax) {
+  uint32_t b = __float_as_uint(amax);
+  if (b == 0u) return 0;
+  int E = (int)(b >> 23);
+  if (E == 0) return -127;
+  int e = ((b & 0x7FFFFFu) <= 0x600000u) ? E - 135 : E - 134;
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// Two fp32 -> two E4M3FN codes (RNE, saturating), `lo` in the low byte.
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  return (uint32_t)pack_e4m3x2(a, b) | ((uint32_t)pack_e4m3x2(c, d) << 16);
+}
+// Two E4M3FN codes (low byte first) -> two fp32 values (exact).
+__device__ __forceinline__ float2 unpack_e4m3x2(uint16_t v) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
+}
+// Two fp32 -> two E2M1 codes in one byte (RNE, saturating), `lo` in the low nibble.
+__device__ __forceinline__ uint32_t pack_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return r & 0xFFu;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// ---------------------------------------------------------------------------
+// Shared-memory addresses, mbarriers (bounded waits), TMA.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait.  Every wait in these kernels goes through here: after about
+// two seconds without progress it records FLAMIA_ERR_TIMEOUT, raises the
+// CTA's abort flag and returns false; a wait that finds the abort flag raised
+// returns false at once, so every role leaves its loop and the CTA reaches
+// its teardown (TMEM release) normally.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          WsHeader* hdr, uint32_t where) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u) {
+      if (*abort_flag) return false;
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        report(hdr, FLAMIA_ERR_TIMEOUT, where);
+        return false;
+      }
+    }
+  }
+}
+
+// After an abort, give TMA copies already issued by this CTA time to land
+// before the CTA exits (bounded: about 50 microseconds).
+__device__ __forceinline__ void drain_after_abort(volatile int* abort_flag) {
+  if (*abort_flag) {
+    for (int i = 0; i < 100; ++i) __nanosleep(500);
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2),
+        "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+// Generic-proxy shared-memory writes -> visible to the async proxy (MMA, TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05: tensor memory, MMA, loads/stores.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Arrive (once) on `bar` when every tcgen05 op issued so far by this thread completes.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 form): start >> 4 in bits 0-13,
+// leading-dimension byte offset >> 4 in 16-29, stride-dimension byte offset
+// >> 4 in 32-45, the fixed version value 1 in bits 46-47, base offset 0,
+// swizzle mode in bits 61-63 (2 = 128B, 4 = 64B, 6 = 32B, 0 = none).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)(swz & 7u) << 61;
+  return d;
+}
+constexpr uint32_t kSwz128 = 2, kSwz64 = 4;
+
+// Instruction descriptor, kind::f8f6f4 (E4M3 x E4M3 -> fp32):
+// c_format(4-5)=1 (F32), a_format(7-9)=0 (E4M3), b_format(10-12)=0,
+// a_major(15), b_major(16) (0 K-major, 1 MN-major), N>>3 in 17-22, M>>4 in 24-28.
+__host__ __device__ constexpr uint32_t idesc_f8(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn) {
+  return (1u << 4) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+// Instruction descriptor, kind::mxf8f6f4 block-scaled (E4M3, UE8M0 scales):
+// b_sf_id in 4-5, a/b formats 0, majors 15/16, N>>3 in 17-22, scale_format
+// (bit 23) = 1 (UE8M0), M>>4 in 24-28, a_sf_id in 29-30.
+__host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn,
+                                                  uint32_t a_sf_id, uint32_t b_sf_id) {
+  return (b_sf_id << 4) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
+         (a_sf_id << 29);
+}
+
+// D[tmem] (+)= A[smem] * B[smem], E4M3 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// Block-scaled form: one UE8M0 scale per 32 K-elements for each row of A
+// (scale-A in tensor memory) and each column of B (scale-B in tensor memory).
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit: thread t of the warp gets lane (quarter*32+t).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
+               "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Tensor-memory address of (lane, column).
+__device__ __forceinline__ uint32_t taddr(uint32_t base, uint32_t lane, uint32_t col) {
+  return base + (lane << 16) + col;
+}
+
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(pred));
+  return pred;
+}
+
+// Offset of 16-byte chunk `c` of row `r` in a 128B-swizzled tile (rows of
+// 128 bytes, 8-row atoms of 1024 bytes, tile base 1024-aligned).
+__device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
+
+}  // namespace flamia

@@ -1,0 +1,412 @@
+// fwd.cu — forward of the block-scaled causal attention (MXFP8 path).
+//
+// FLAMIA (paper summary), abstract and §3.1–§3.3; close reading 4.1 (scale
+// factorisation S_ij = 2^(eQ(i)+eK(j)) * <codes>), 4.4 (warp specialisation
+// after FlashAttention-4, tiles on chip, tensor cores kept busy).
+//
+// Persistent grid over the longest-first work list (document, 128-query tile)
+// x query heads.  Warp roles:
+//   warps 0-3  softmax: thread r owns query row r of the tile = TMEM lane r.
+//              Reads S from TMEM, forms y = x + eV(j) (the per-key V factor
+//              folded into P along the contraction axis), quantizes P^ with
+//              one no-clamp exponent per (row, 32-key block), keeps the
+//              row's integer reference m and normaliser l, writes P^ codes to
+//              shared memory and the block exponents (relative to m) to TMEM
+//              as the A-operand scale factors of the P^V MMA.
+//   warp 4     producer: TMA loads of Q, K, V code tiles (128 x d, swizzled)
+//              and the per-key scale vectors of each K/V stage.
+//   warp 5     MMA issuer: S = Q^ K^T (kind::f8f6f4, fp32 in TMEM, double
+//              buffered) and O += P^ V^ (kind::mxf8f6f4 block-scaled, scale A
+//              = P^ block exponents, scale B = 1: V's own scale is folded).
+// The next tile's S is issued before the current tile's P^V so the tensor
+// core works while the softmax warps quantize.
+#include "kernels.h"
+#include "attn_common.cuh"
+
+namespace flamia {
+
+constexpr int kFwdStages = 3;
+constexpr int kFwdThreads = 192;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColSFA0 = 384, kColSFA1 = 392, kColSFB = 400;
+
+template <int HD>
+struct __align__(1024) FwdTiles {
+  uint8_t q[kTile * HD];
+  uint8_t k[kFwdStages][kTile * HD];
+  uint8_t v[kFwdStages][kTile * HD];
+  uint8_t p[2][kTile * kTile];
+};
+
+struct FwdCtl {
+  float kf[kFwdStages][kTile];    // 2^eK(j)
+  float vf[kFwdStages][kTile];    // eV(j)
+  float vinv[kFwdStages][kTile];  // 2^-eV(j)
+  uint64_t q_full, q_empty;
+  uint64_t k_full[kFwdStages], k_empty[kFwdStages], v_full[kFwdStages], v_empty[kFwdStages];
+  uint64_t s_full[2], s_free[2], p_full[2], p_free[2], o_full, o_free;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int HD>
+constexpr size_t fwd_smem_bytes() {
+  return sizeof(FwdTiles<HD>) + sizeof(FwdCtl) + 1024;
+}
+
+// K-major operand with rows of `row_bytes` (128 or 64), swizzle = row size.
+__device__ __forceinline__ uint64_t desc_kmajor(const uint8_t* tile, uint32_t byte_off, uint32_t row_bytes) {
+  return smem_desc(smem_u32(tile) + byte_off, 16, 8 * row_bytes, row_bytes == 128 ? kSwz128 : kSwz64);
+}
+// MN-major operand: rows are K indices, `row_bytes` of M/N per row.
+__device__ __forceinline__ uint64_t desc_mnmajor(const uint8_t* tile, uint32_t byte_off, uint32_t row_bytes) {
+  return smem_desc(smem_u32(tile) + byte_off, 8 * row_bytes, 8 * row_bytes, row_bytes == 128 ? kSwz128 : kSwz64);
+}
+
+template <int HD, bool OUT_BF16>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    fwd_kernel(const AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+               const __grid_constant__ CUtensorMap map_v) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  FwdTiles<HD>& tl = *reinterpret_cast<FwdTiles<HD>*>(base);
+  FwdCtl& c = *reinterpret_cast<FwdCtl*>(base + sizeof(FwdTiles<HD>));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = p.H / p.Hkv;
+  const int n_work = p.hdr->n_items * p.H;
+  volatile int* abort_flag = &c.abort_flag;
+  WsHeader* hdr = p.hdr;
+
+  if (tid == 0) {
+    mbar_init(&c.q_full, 1);
+    mbar_init(&c.q_empty, 1);
+    for (int s = 0; s < kFwdStages; ++s) {
+      mbar_init(&c.k_full[s], 32);
+      mbar_init(&c.k_empty[s], 1 + 128);
+      mbar_init(&c.v_full[s], 1);
+      mbar_init(&c.v_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&c.s_full[b], 1);
+      mbar_init(&c.s_free[b], 128);
+      mbar_init(&c.p_full[b], 128);
+      mbar_init(&c.p_free[b], 1);
+    }
+    mbar_init(&c.o_full, 1);
+    mbar_init(&c.o_free, 128);
+    c.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) tmem_alloc(&c.tmem_base, 512);
+  if (warp == 4 && lane == 0) {
+    prefetch_tensormap(&map_q);
+    prefetch_tensormap(&map_k);
+    prefetch_tensormap(&map_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = c.tmem_base;
+  if (warp < 4) {  // scale factors of V in the P^V MMA: 2^0 (V's factor is folded into P)
+    tmem_st4(taddr(tb, warp * 32, kColSFB), 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    uint32_t kv = 0, qc = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+      const int pair = w / p.H, h = w - pair * p.H, hk = h / G;
+      const int2 it = p.fwd_items[pair];
+      const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
+      const int q0 = ds + kTile * it.y;
+      const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
+      if (!(ok = mbar_wait(&c.q_empty, (qc & 1) ^ 1, abort_flag, hdr, 0x201))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&c.q_full, kTile * HD);
+        tma_load_3d(tl.q, &map_q, &c.q_full, 0, h, q0);
+      }
+      ++qc;
+      for (int kt = 0; kt < n_kt; ++kt, ++kv) {
+        const int st = kv % kFwdStages;
+        const uint32_t ph = (kv / kFwdStages) & 1;
+        if (!(ok = mbar_wait(&c.k_empty[st], ph ^ 1, abort_flag, hdr, 0x202))) break;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = lane * 4 + jj, key = kTile * kt + j;
+          int ek = 0, ev = 0;
+          if (key < len) {
+            ek = (int)__ldg(p.k_sc + (size_t)hk * p.T + ds + key) - 127;
+            ev = (int)__ldg(p.v_sc + (size_t)hk * p.T + ds + key) - 127;
+          }
+          c.kf[st][j] = pow2_127(ek);
+          c.vf[st][j] = (float)ev;
+          c.vinv[st][j] = pow2_127(-ev);
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&c.k_full[st], kTile * HD);
+          tma_load_3d(tl.k[st], &map_k, &c.k_full[st], 0, hk, ds + kTile * kt);
+        } else {
+          mbar_arrive(&c.k_full[st]);
+        }
+        if (!(ok = mbar_wait(&c.v_empty[st], ph ^ 1, abort_flag, hdr, 0x203))) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&c.v_full[st], kTile * HD);
+          tma_load_3d(tl.v[st], &map_v, &c.v_full[st], 0, hk, ds + kTile * kt);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      uint32_t kv = 0, qc = 0, sc = 0, pc = 0, ic = 0;
+      bool ok = true;
+      const uint32_t id_s = idesc_f8(128, 128, 0, 0);
+      for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+        const int pair = w / p.H;
+        const int2 it = p.fwd_items[pair];
+        const int len = __ldg(p.cu + it.x + 1) - __ldg(p.cu + it.x);
+        const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
+        if (!(ok = mbar_wait(&c.q_full, qc & 1, abort_flag, hdr, 0x211))) break;
+        const uint32_t kv_base = kv;
+        for (int kt = 0; ok && kt <= n_kt; ++kt) {
+          if (kt < n_kt) {
+            const int st = kv % kFwdStages;
+            const uint32_t ph = (kv / kFwdStages) & 1;
+            const uint32_t sb = sc & 1, sph = (sc >> 1) & 1;
+            if (!(ok = mbar_wait(&c.k_full[st], ph, abort_flag, hdr, 0x212))) break;
+            if (!(ok = mbar_wait(&c.s_free[sb], sph ^ 1, abort_flag, hdr, 0x213))) break;
+            tc_fence_after();
+            const uint32_t d_s = tb + (sb ? kColS1 : kColS0);
+#pragma unroll
+            for (int kk = 0; kk < HD / 32; ++kk)
+              mma_f8(d_s, desc_kmajor(tl.q, 32 * kk, HD), desc_kmajor(tl.k[st], 32 * kk, HD), id_s, kk > 0);
+            tc_commit(&c.s_full[sb]);
+            tc_commit(&c.k_empty[st]);
+            if (kt == n_kt - 1) tc_commit(&c.q_empty);
+            ++sc;
+            ++kv;
+          }
+          if (kt >= 1) {
+            const uint32_t j = kt - 1, vidx = kv_base + j;
+            const int vst = vidx % kFwdStages;
+            const uint32_t vph = (vidx / kFwdStages) & 1;
+            const uint32_t pb = pc & 1, pph = (pc >> 1) & 1;
+            if (!(ok = mbar_wait(&c.p_full[pb], pph, abort_flag, hdr, 0x214))) break;
+            if (!(ok = mbar_wait(&c.v_full[vst], vph, abort_flag, hdr, 0x215))) break;
+            if (j == 0 && !(ok = mbar_wait(&c.o_free, (ic & 1) ^ 1, abort_flag, hdr, 0x216))) break;
+            tc_fence_after();
+            const uint32_t sfa = tb + (pb ? kColSFA1 : kColSFA0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_mxf8(tb + kColO, desc_kmajor(tl.p[pb], 32 * kk, 128), desc_mnmajor(tl.v[vst], 32 * kk * HD, HD),
+                       idesc_mxf8(128, HD, 0, 1, kk, kk), sfa, tb + kColSFB, (j > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(&c.p_free[pb]);
+            tc_commit(&c.v_empty[vst]);
+            if ((int)j == n_kt - 1) tc_commit(&c.o_full);
+            ++pc;
+          }
+        }
+        ++qc;
+        ++ic;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int r = tid;
+    uint32_t kv = 0, sc = 0, pc = 0, ic = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+      const int pair = w / p.H, h = w - pair * p.H;
+      const int2 it = p.fwd_items[pair];
+      const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
+      const int q0 = ds + kTile * it.y;
+      const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
+      const int i_loc = kTile * it.y + r;
+      const bool row_ok = i_loc < len;
+      const int eq = row_ok ? (int)__ldg(p.q_sc + (size_t)h * p.T + q0 + r) - 127 : 0;
+      const float rowc = p.c_log2 * pow2_127(eq);
+      int m_ref = kEmptyBlock;
+      float l_run = 0.f;
+      for (int kt = 0; ok && kt < n_kt; ++kt, ++kv, ++sc, ++pc) {
+        const int st = kv % kFwdStages;
+        const uint32_t kph = (kv / kFwdStages) & 1;
+        const uint32_t sb = sc & 1, sph = (sc >> 1) & 1;
+        if (!(ok = mbar_wait(&c.k_full[st], kph, abort_flag, hdr, 0x221))) break;
+        if (!(ok = mbar_wait(&c.s_full[sb], sph, abort_flag, hdr, 0x222))) break;
+        tc_fence_after();
+        float acc[128];
+        {
+          uint32_t rr[32];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            tmem_ld32(taddr(tb, warp * 32, (sb ? kColS1 : kColS0) + 32 * b), rr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[32 * b + j] = __uint_as_float(rr[j]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&c.s_free[sb]);
+        const int key0 = kTile * kt;
+        int Eb[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          float M = -INFINITY;
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int j = 32 * b + jj;
+            const float y = visible(i_loc, key0 + j, len, p.causal)
+                                ? score_to_y(acc[j], rowc, c.kf[st][j], c.vf[st][j])
+                                : -INFINITY;
+            acc[j] = y;
+            M = fmaxf(M, y);
+          }
+          Eb[b] = (M == -INFINITY) ? kEmptyBlock : phat_block_exp(M);
+        }
+        const int Emax = max(max(Eb[0], Eb[1]), max(Eb[2], Eb[3]));
+        int m_new = m_ref;
+        if (Emax != kEmptyBlock && (m_ref == kEmptyBlock || Emax > m_ref + 8)) m_new = Emax;
+        uint32_t codes[32];
+        float lsum = 0.f;
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          float lb = 0.f;
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            float pv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = 32 * b + 4 * q4 + e;
+              pv[e] = (Eb[b] == kEmptyBlock) ? 0.f : phat_value(acc[j], Eb[b]);
+              lb = fmaf(pv[e], c.vinv[st][j], lb);
+            }
+            codes[8 * b + q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
+          }
+          if (Eb[b] != kEmptyBlock) {
+            lsum += ldexp_f(lb, Eb[b] - m_new);
+            const int byte = min(max(Eb[b] - m_new + 127, 0), 254);
+            word |= (uint32_t)byte << (8 * b);
+          }
+        }
+        mbar_arrive(&c.k_empty[st]);
+        l_run = (m_ref == kEmptyBlock) ? lsum : ldexp_f(l_run, m_ref - m_new) + lsum;
+        if (kt > 0 && m_new != m_ref) {
+          // rescale the O accumulator row once the previous P^V has landed
+          const uint32_t pp = pc - 1;
+          if (!(ok = mbar_wait(&c.p_free[pp & 1], (pp >> 1) & 1, abort_flag, hdr, 0x223))) break;
+          tc_fence_after();
+          const float f = ldexp_f(1.0f, m_ref - m_new);
+#pragma unroll
+          for (int cb = 0; cb < HD / 32; ++cb) {
+            uint32_t rr[32];
+            tmem_ld32(taddr(tb, warp * 32, kColO + 32 * cb), rr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * f);
+            tmem_st32(taddr(tb, warp * 32, kColO + 32 * cb), rr);
+          }
+          tmem_st_wait();
+        }
+        m_ref = m_new;
+        const uint32_t pb = pc & 1;
+        if (!(ok = mbar_wait(&c.p_free[pb], ((pc >> 1) & 1) ^ 1, abort_flag, hdr, 0x224))) break;
+        uint8_t* prow = tl.p[pb];
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint4 v4 = make_uint4(codes[4 * ch], codes[4 * ch + 1], codes[4 * ch + 2], codes[4 * ch + 3]);
+          *reinterpret_cast<uint4*>(prow + sw128_off(r, ch)) = v4;
+        }
+        tmem_st4(taddr(tb, warp * 32, pb ? kColSFA1 : kColSFA0), word, word, word, word);
+        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&c.p_full[pb]);
+      }
+      if (!ok) break;
+      // epilogue: O = acc / l
+      if (!(ok = mbar_wait(&c.o_full, ic & 1, abort_flag, hdr, 0x225))) break;
+      tc_fence_after();
+      float o[HD];
+#pragma unroll
+      for (int cb = 0; cb < HD / 32; ++cb) {
+        uint32_t rr[32];
+        tmem_ld32(taddr(tb, warp * 32, kColO + 32 * cb), rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[32 * cb + j] = __uint_as_float(rr[j]);
+      }
+      tc_fence_before();
+      mbar_arrive(&c.o_free);
+      if (row_ok) {
+        const float inv = 1.0f / l_run;
+        const size_t off = ((size_t)(q0 + r) * p.H + h) * HD;
+        if constexpr (OUT_BF16) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O) + off);
+#pragma unroll
+          for (int c8 = 0; c8 < HD / 8; ++c8) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(o[8 * c8 + 2 * e] * inv, o[8 * c8 + 2 * e + 1] * inv);
+              wv[e] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            dst[c8] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.O) + off);
+#pragma unroll
+          for (int c4 = 0; c4 < HD / 4; ++c4)
+            dst[c4] = make_float4(o[4 * c4] * inv, o[4 * c4 + 1] * inv, o[4 * c4 + 2] * inv, o[4 * c4 + 3] * inv);
+        }
+        p.m[(size_t)h * p.T + q0 + r] = m_ref;
+        p.l[(size_t)h * p.T + q0 + r] = l_run;
+      }
+      ++ic;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  drain_after_abort(abort_flag);
+  if (warp == 5) tmem_dealloc(tb, 512);
+}
+
+static int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+template <int HD, bool OB>
+static cudaError_t launch_fwd_t(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
+  const size_t smem = fwd_smem_bytes<HD>();
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<HD, OB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  long work = (long)p.max_items * p.H;
+  int grid = (int)(work < num_sms() ? work : num_sms());
+  fwd_kernel<HD, OB><<<grid, kFwdThreads, smem, st>>>(p, m.q, m.k, m.v);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
+  if (p.d == 128) return p.out_bf16 ? launch_fwd_t<128, true>(p, m, st) : launch_fwd_t<128, false>(p, m, st);
+  return p.out_bf16 ? launch_fwd_t<64, true>(p, m, st) : launch_fwd_t<64, false>(p, m, st);
+}
+
+int sm_count() { return num_sms(); }
+
+}  // namespace flamia

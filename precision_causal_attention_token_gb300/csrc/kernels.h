@@ -1,0 +1,57 @@
+// kernels.h — host-side launch interfaces between api.cu and the kernels.
+#pragma once
+#include "common.cuh"
+
+namespace flamia {
+
+struct QuantArgs {
+  const void* x;     // [T][heads][d]
+  uint8_t* codes;    // [T][heads][d]
+  uint8_t* scales;   // [heads][T]
+  uint8_t* codes4;   // [T][heads][d/2]   (NVFP4 operand)
+  uint8_t* scales4;  // [T][heads][d/16]
+  float* gscale4;    // [heads][T]
+  const void* O;     // [T][heads][d]     (dO role)
+  float* D;          // [heads][T]
+  int T, heads;
+  int per_token;
+};
+
+cudaError_t launch_quantize(const QuantArgs& a, int d, int in_bf16, int o_bf16, bool with_D, bool nvfp4,
+                            const int32_t* cu, const int32_t* blk_prefix, int n_seq, WsHeader* hdr, int max_units,
+                            cudaStream_t st);
+cudaError_t launch_plan(const flamia_problem_t& p, const WsLayout& L, uint8_t* ws, cudaStream_t st);
+
+// Everything the attention kernels need for one call (host-built).
+struct AttnParams {
+  int T, H, Hkv, d, n_seq, causal, exact, out_bf16, max_items;
+  float softmax_scale;  // c' (scores)
+  float c_log2;         // softmax_scale * log2(e)
+  const int32_t* cu;
+  const int32_t* tile_prefix;
+  const int2* fwd_items;
+  const int2* bwd_items;
+  WsHeader* hdr;
+  const uint8_t* q_sc;  // [H][T]
+  const uint8_t* k_sc;  // [Hkv][T]
+  const uint8_t* v_sc;  // [Hkv][T]
+  const uint8_t* do_sc; // [H][T]
+  const float* D;       // [H][T]
+  int32_t* m;           // [H][T]
+  float* l;             // [H][T]
+  void* O;              // [T][H][d]
+  float* dq_acc;        // [T][H][d] fp32
+  void* dQ;             // [T][H][d]
+  void* dK;             // [T][Hkv][d]
+  void* dV;             // [T][Hkv][d]
+};
+
+struct AttnMaps {
+  CUtensorMap q, k, v, dO;
+};
+
+cudaError_t launch_fwd(const AttnParams& p, const AttnMaps& maps, cudaStream_t st);
+cudaError_t launch_bwd(const AttnParams& p, const AttnMaps& maps, cudaStream_t st);
+cudaError_t launch_dq_convert(const AttnParams& p, cudaStream_t st);
+
+}  // namespace flamia

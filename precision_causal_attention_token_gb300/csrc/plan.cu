@@ -1,0 +1,188 @@
+// plan.cu — document tables and the longest-first work lists, built on the
+// GPU once per microbatch with no host read-back.
+//
+// FLAMIA (paper summary), §3.6.2 Load-Balanced Scheduling and the close
+// reading 4.4 (GPU-side scheduling): the schedule is built on the GPU with a
+// fixed number of merge-sort passes and handed to a persistent grid in
+// descending cost.  Here a work item is a (document, 128-token tile); its cost
+// is the number of tiles the kernel visits for it: key tiles for a forward
+// query tile, query tiles for a backward key tile.  Sort keys are
+// (cost descending, item index ascending), unique, so the order is
+// deterministic.  The pass count depends only on a host-side bound of the item
+// count (ceil(T/128) + n_seq), so the whole plan can be captured in a graph.
+#include "common.cuh"
+
+namespace flamia {
+
+// One CTA: validate cu_seqlens, per-document 128-tile and 32-block counts,
+// exclusive scans into tile_prefix / blk32_prefix, totals into the header.
+__global__ void __launch_bounds__(1024) plan_prefix_kernel(const int32_t* __restrict__ cu, int n_seq, int T,
+                                                           int32_t* tile_prefix, int32_t* blk32_prefix,
+                                                           WsHeader* hdr) {
+  __shared__ int32_t s_t[1024], s_b[1024];
+  __shared__ int32_t carry_t, carry_b, bad;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    carry_t = 0;
+    carry_b = 0;
+    bad = (__ldg(cu) != 0 || __ldg(cu + n_seq) != T) ? 1 : 0;
+    hdr->fwd_counter = 0;
+    hdr->bwd_counter = 0;
+    hdr->dq_counter = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < n_seq; base += 1024) {
+    const int i = base + tid;
+    int nt = 0, nb = 0;
+    if (i < n_seq) {
+      const int len = __ldg(cu + i + 1) - __ldg(cu + i);
+      if (len < 0) bad = 1;
+      const int l = len < 0 ? 0 : len;
+      nt = (l + 127) / 128;
+      nb = (l + 31) / 32;
+    }
+    s_t[tid] = nt;
+    s_b[tid] = nb;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {  // Hillis-Steele inclusive scan
+      int at = tid >= off ? s_t[tid - off] : 0;
+      int ab = tid >= off ? s_b[tid - off] : 0;
+      __syncthreads();
+      s_t[tid] += at;
+      s_b[tid] += ab;
+      __syncthreads();
+    }
+    if (i < n_seq) {
+      tile_prefix[i] = carry_t + s_t[tid] - nt;
+      blk32_prefix[i] = carry_b + s_b[tid] - nb;
+    }
+    __syncthreads();
+    if (tid == 1023) {
+      carry_t += s_t[1023];
+      carry_b += s_b[1023];
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    tile_prefix[n_seq] = carry_t;
+    blk32_prefix[n_seq] = carry_b;
+    hdr->n_items = bad ? 0 : carry_t;
+    hdr->n_blk32 = bad ? 0 : carry_b;
+    if (bad) report(hdr, FLAMIA_ERR_BAD_SEQLENS, 0x100u);
+  }
+}
+
+__device__ __forceinline__ int doc_of_tile(const int32_t* __restrict__ tile_prefix, int n_seq, int g) {
+  int lo = 0, hi = n_seq;  // tile_prefix[lo] <= g < tile_prefix[hi]
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (__ldg(tile_prefix + mid) <= g) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// keys[0 .. sort_n) forward list, keys[sort_n .. 2 sort_n) backward list.
+__global__ void plan_keys_kernel(const int32_t* __restrict__ tile_prefix, int n_seq, int causal, int sort_n,
+                                 const WsHeader* hdr, uint64_t* keys) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= sort_n) return;
+  const int n_items = hdr->n_items;
+  uint64_t kf = ~0ull, kb = ~0ull;
+  if (g < n_items) {
+    const int doc = doc_of_tile(tile_prefix, n_seq, g);
+    const int tile = g - __ldg(tile_prefix + doc);
+    const int nt = __ldg(tile_prefix + doc + 1) - __ldg(tile_prefix + doc);
+    const uint32_t cf = causal ? (uint32_t)(tile + 1) : (uint32_t)nt;
+    const uint32_t cb = causal ? (uint32_t)(nt - tile) : (uint32_t)nt;
+    kf = ((uint64_t)(0xFFFFFFFFu - cf) << 32) | (uint32_t)g;
+    kb = ((uint64_t)(0xFFFFFFFFu - cb) << 32) | (uint32_t)g;
+  }
+  keys[g] = kf;
+  keys[sort_n + g] = kb;
+}
+
+// Bitonic sort of kSortBlock keys per CTA (ascending).
+__global__ void __launch_bounds__(1024) block_sort_kernel(uint64_t* keys) {
+  __shared__ uint64_t s[kSortBlock];
+  uint64_t* k = keys + (size_t)blockIdx.x * kSortBlock;
+  const int tid = threadIdx.x;
+  s[tid] = k[tid];
+  s[tid + 1024] = k[tid + 1024];
+  __syncthreads();
+  for (int size = 2; size <= kSortBlock; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const int i = 2 * tid - (tid & (stride - 1));  // lower index of the pair
+      const int j = i + stride;
+      const bool up = ((i & size) == 0);
+      const uint64_t a = s[i], b = s[j];
+      if ((a > b) == up) { s[i] = b; s[j] = a; }
+      __syncthreads();
+    }
+  }
+  k[tid] = s[tid];
+  k[tid + 1024] = s[tid + 1024];
+}
+
+// One merge pass: sorted runs of `width` keys are merged pairwise.  Each key
+// finds its output slot as (own rank) + (number of smaller keys in the
+// sibling run), by binary search; keys are unique.  Two lists of sort_n keys.
+__global__ void merge_pass_kernel(const uint64_t* __restrict__ src, uint64_t* __restrict__ dst, int sort_n,
+                                  int width) {
+  const int gi = blockIdx.x * blockDim.x + threadIdx.x;
+  if (gi >= 2 * sort_n) return;
+  const int seg = gi / sort_n, i = gi - seg * sort_n;
+  const uint64_t* s = src + (size_t)seg * sort_n;
+  uint64_t* d = dst + (size_t)seg * sort_n;
+  const int pair = i / (2 * width);
+  const int a0 = pair * 2 * width;
+  const int b0 = a0 + width;
+  const int a_len = min(width, sort_n - a0);
+  const int b_len = max(0, min(width, sort_n - b0));
+  const uint64_t key = s[i];
+  const bool in_a = i < b0;
+  const int own = in_a ? i - a0 : i - b0;
+  const uint64_t* other = in_a ? s + b0 : s + a0;
+  int lo = 0, hi = in_a ? b_len : a_len;  // count of keys in `other` smaller than key
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (other[mid] < key) lo = mid + 1; else hi = mid;
+  }
+  d[a0 + own + lo] = key;
+  (void)a_len;
+}
+
+__global__ void plan_items_kernel(const uint64_t* __restrict__ keys, const int32_t* __restrict__ tile_prefix,
+                                  int n_seq, int sort_n, const WsHeader* hdr, int2* fwd_items, int2* bwd_items) {
+  const int gi = blockIdx.x * blockDim.x + threadIdx.x;
+  const int n_items = hdr->n_items;
+  if (gi >= 2 * sort_n) return;
+  const int seg = gi / sort_n, r = gi - seg * sort_n;
+  if (r >= n_items) return;
+  const int g = (int)(uint32_t)(keys[gi] & 0xFFFFFFFFull);
+  const int doc = doc_of_tile(tile_prefix, n_seq, g);
+  const int2 it = make_int2(doc, g - __ldg(tile_prefix + doc));
+  (seg == 0 ? fwd_items : bwd_items)[r] = it;
+}
+
+cudaError_t launch_plan(const flamia_problem_t& p, const WsLayout& L, uint8_t* ws, cudaStream_t st) {
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + L.header);
+  int32_t* tile_prefix = reinterpret_cast<int32_t*>(ws + L.tile_prefix);
+  int32_t* blk_prefix = reinterpret_cast<int32_t*>(ws + L.blk32_prefix);
+  uint64_t* ka = reinterpret_cast<uint64_t*>(ws + L.keys_a);
+  uint64_t* kb = reinterpret_cast<uint64_t*>(ws + L.keys_b);
+  plan_prefix_kernel<<<1, 1024, 0, st>>>(p.cu_seqlens, p.n_seq, p.T, tile_prefix, blk_prefix, hdr);
+  const int n = L.sort_n;
+  plan_keys_kernel<<<(n + 255) / 256, 256, 0, st>>>(tile_prefix, p.n_seq, p.causal, n, hdr, ka);
+  block_sort_kernel<<<2 * n / kSortBlock, 1024, 0, st>>>(ka);
+  uint64_t *src = ka, *dst = kb;
+  for (int w = kSortBlock; w < n; w *= 2) {
+    merge_pass_kernel<<<(2 * n + 255) / 256, 256, 0, st>>>(src, dst, n, w);
+    uint64_t* t = src; src = dst; dst = t;
+  }
+  plan_items_kernel<<<(2 * n + 255) / 256, 256, 0, st>>>(src, tile_prefix, p.n_seq, n, hdr,
+                                                         reinterpret_cast<int2*>(ws + L.fwd_items),
+                                                         reinterpret_cast<int2*>(ws + L.bwd_items));
+  return cudaGetLastError();
+}
+
+}  // namespace flamia

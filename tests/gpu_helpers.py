@@ -1,0 +1,75 @@
+"""Shared helpers for the GPU parity tests: run one training call through the
+C ABI on seeded inputs, run the oracle on the same inputs, compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import precision_causal_attention_token_gb300 as fl
+
+# Tolerances for floating-point outputs against the oracle's result of the
+# same quantization: max |err| <= 2e-2 of the row's max-abs, cosine >= 0.9999.
+ROW_TOL = 2e-2
+COS_TOL = 0.9999
+
+
+def to_dev(a: np.ndarray, dtype: str, dev="cuda"):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.to(dev, torch.bfloat16 if dtype == "bf16" else torch.float32)
+
+
+def run_gpu(w, *, causal=True, exact=False, path=fl.PATH_MXFP8, deterministic=False, inputs=None,
+            backward=True):
+    dev = torch.device("cuda:0")
+    q, k, v, do = inputs if inputs is not None else (w.tensor(n) for n in ("q", "k", "v", "do"))
+    cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
+    dt = fl.BF16 if w.dtype == "bf16" else fl.F32
+    tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu, causal=causal, exact=exact, path=path, in_dtype=dt,
+                      out_dtype=dt, deterministic=deterministic)
+    tc.plan()
+    tc.forward(to_dev(q, w.dtype), to_dev(k, w.dtype), to_dev(v, w.dtype))
+    if backward:
+        tc.backward(to_dev(do, w.dtype))
+    torch.cuda.synchronize()
+    st = fl.flamia_get_device_status(tc.ws)
+    assert st == fl.OK, fl.status_string(st)
+    tc._keep = cu
+    return tc
+
+
+def run_oracle(w, *, causal=True, exact=False, path=oracle.PATH_MXFP8, inputs=None, backward=True):
+    q, k, v, do = inputs if inputs is not None else (w.tensor(n) for n in ("q", "k", "v", "do"))
+    return oracle.train_call(q, k, v, do if backward else None, w.cu_seqlens, causal=causal, exact=exact,
+                             path=path, out_dtype=w.dtype)
+
+
+def np_of(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def compare(name, got, want, row_tol=ROW_TOL, cos_tol=COS_TOL, rows=None):
+    """Per-row (last axis) max-error bound and whole-tensor cosine."""
+    g = np_of(got) if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
+    r = np.asarray(want, np.float64)
+    if rows is not None:
+        g, r = g[rows], r[rows]
+    assert g.shape == r.shape, (name, g.shape, r.shape)
+    assert np.isfinite(g).all(), f"{name}: non-finite values"
+    rowmax = np.abs(r).max(axis=-1, keepdims=True)
+    floor = 1e-6 * max(np.abs(r).max(), 1e-30)
+    err = np.abs(g - r)
+    ratio = err / np.maximum(rowmax, floor)
+    worst = float(ratio.max()) if ratio.size else 0.0
+    gg, rr = g.ravel(), r.ravel()
+    denom = np.sqrt((gg @ gg) * (rr @ rr))
+    cos = float(gg @ rr / denom) if denom > 0 else 1.0
+    assert worst <= row_tol, f"{name}: max |err| / row max-abs = {worst:.3e} > {row_tol}"
+    assert cos >= cos_tol, f"{name}: cosine {cos:.7f} < {cos_tol}"
+    return worst, cos
+
+
+def cosine(a, b):
+    a = np.asarray(a, np.float64).ravel()
+    b = np.asarray(b, np.float64).ravel()
+    return float(a @ b / np.sqrt((a @ a) * (b @ b)))

@@ -1,0 +1,92 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+that include/flamia.h declares, and rejects bad arguments on the host before
+any launch."""
+import os
+import re
+
+import pytest
+import torch
+
+import precision_causal_attention_token_gb300 as fl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "flamia.h")).read()
+    return sorted(set(re.findall(r"\b(flamia_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return fl.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(fl.EXPORTED) <= set(names)
+
+
+def _prob(**kw):
+    cu = torch.tensor([0, 100, 228], dtype=torch.int32)
+    base = dict(T=228, H=4, Hkv=2, d=128)
+    base.update(kw)
+    p = fl.make_problem(base["T"], base["H"], base["Hkv"], base["d"], cu)
+    for k, v in kw.items():
+        if k not in base or k in ("path", "in_dtype", "out_dtype"):
+            setattr(p, k, v)
+    return p, cu
+
+
+def test_workspace_size_valid_and_invalid(lib):
+    p, _ = _prob()
+    n = fl.flamia_workspace_size(p)
+    assert n > 228 * 4 * 128 * 4  # holds the fp32 dQ accumulator
+    for bad in (dict(d=96), dict(H=3), dict(T=0), dict(Hkv=0)):
+        q, _ = _prob(**bad)
+        assert fl.flamia_workspace_size(q) == 0, bad
+    q, _ = _prob()
+    q.path = 7
+    assert fl.flamia_workspace_size(q) == 0
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert fl.status_string(s)
+    assert fl.status_string(fl.ERR_TIMEOUT) == "device wait timed out"
+
+
+def test_host_validation_rejects_before_launch(lib):
+    p, cu = _prob()
+    ws = torch.empty(16, dtype=torch.uint8)
+    # workspace too small -> reported without touching the device
+    st = lib.flamia_plan(p, ws.data_ptr(), 16, None)
+    assert st == fl.ERR_WORKSPACE_TOO_SMALL
+    q, _ = _prob(d=80)
+    assert lib.flamia_plan(q, ws.data_ptr(), 1 << 30, None) == fl.ERR_UNSUPPORTED
+    q, _ = _prob(H=5)
+    assert lib.flamia_plan(q, ws.data_ptr(), 1 << 30, None) == fl.ERR_INVALID_ARG
+    # misaligned workspace pointer
+    assert lib.flamia_plan(p, ws.data_ptr() + 1, 1 << 30, None) == fl.ERR_INVALID_ARG
+    # null operands
+    big = 1 << 40
+    op = fl.Operand()
+    assert lib.flamia_fwd(p, op, op, op, None, None, None, ws.data_ptr(), big, None) == fl.ERR_INVALID_ARG
+    assert lib.flamia_get_device_status(None, None) == fl.ERR_INVALID_ARG
+
+
+def test_binding_raises_without_library(tmp_path):
+    import importlib
+    mod = importlib.import_module("precision_causal_attention_token_gb300")
+    saved = mod._lib
+    try:
+        mod._lib = None
+        with pytest.raises(RuntimeError):
+            mod.load_library(str(tmp_path / "missing.so"))
+    finally:
+        mod._lib = saved
