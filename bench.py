@@ -1,0 +1,319 @@
+"""Benchmark of the block-scaled causal attention training call on GB300.
+
+One step = the whole hot path on one batch of synthetic input: work-list plan,
+quantize Q/K/V, forward, quantize dO (+ D), backward.  Workload: 4 rows x 4096
+tokens, 16 heads, d = 128, bf16, causal (equal-length documents).  The metric is
+the algorithmic causal FLOP rate including quantization: 14 d H sum_docs
+l(l+1)/2 FLOPs per step (4d forward + 10d backward per unmasked pair).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs one independent replica per GPU (torchrun), weak scaling.  The
+reference arm times the fp64 oracle on the host cores on a bounded sample of
+the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal fwd+bwd attn TFLOP/s incl. quant, MXFP8 d=128; % of dense FP8 peak"
+WORKLOAD = "batched causal 4 rows x 4096 tokens, H=16, d=128, bf16 N(0,1), MXFP8"
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample-tokens", type=int, default=1536,
+                    help="causal prefix length of the oracle sample (cpu_baseline leg)")
+    ap.add_argument("--ref-sample-tokens", type=int, default=1024,
+                    help="causal prefix length per step of the reference (oracle) arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return p, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _workload():
+    import synth
+    return synth.workload(2)
+
+
+_SAMPLE_CACHE: dict = {}
+
+
+def _oracle_sample(w, n_tokens: int):
+    """Oracle on a bounded sample: the causal prefix of the first document for head 0
+    (its rows see only keys inside the prefix, so it is an exact part of the workload)."""
+    import oracle
+    if "x" not in _SAMPLE_CACHE:
+        _SAMPLE_CACHE["x"] = [np.ascontiguousarray(w.tensor(n)[:4096, 0:1]) for n in ("q", "k", "v", "do")]
+    q, k, v, do = (x[:n_tokens] for x in _SAMPLE_CACHE["x"])
+    cu = np.array([0, n_tokens], np.int32)
+    t0 = time.perf_counter()
+    oracle.train_call(q, k, v, do, cu, out_dtype="bf16")
+    dt = time.perf_counter() - t0
+    flops = 14.0 * w.d * 1 * n_tokens * (n_tokens + 1) / 2
+    return flops, dt
+
+
+def run_reference(a):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return 0
+    w = _workload()
+    import oracle
+    oracle.build()
+    for _ in range(max(0, a.warmup)):
+        _oracle_sample(w, 256)
+    times, flops = [], 0.0
+    for _ in range(a.steps):
+        f, dt = _oracle_sample(w, a.ref_sample_tokens)
+        times.append(dt)
+        flops = f
+    tot = sum(times)
+    val = flops * a.steps / tot / 1e12
+    sample = (f"causal prefix of {a.ref_sample_tokens} tokens of document 0, head 0 of the workload "
+              f"(single-threaded fp64 oracle, full quantized call)")
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": a.gpus,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1e3 * tot / a.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(a):
+    import torch
+    import precision_causal_attention_token_gb300 as fl
+    import __graft_entry__
+
+    rank, world, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    __graft_entry__.build()
+
+    w = _workload()
+    q, k, v, do = (torch.from_numpy(w.tensor(n)).to(dev, torch.bfloat16) for n in ("q", "k", "v", "do"))
+    cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
+    tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu)
+    flops = w.flops()
+    pairs = w.causal_pairs
+    fwd_flops, bwd_flops = 4.0 * w.d * w.H * pairs, 10.0 * w.d * w.H * pairs
+    stream = torch.cuda.current_stream()
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        tc.plan(stream)
+        fl.flamia_quantize(tc.prob, fl.ROLE_QKV, [q, k, v], None, [tc.opq, tc.opk, tc.opv], None, tc.ws, stream)
+        if evs:
+            evs[1].record(stream)
+        fl.flamia_fwd(tc.prob, tc.opq, tc.opk, tc.opv, tc.O, tc.m, tc.l, tc.ws, stream)
+        if evs:
+            evs[2].record(stream)
+        fl.flamia_quantize(tc.prob, fl.ROLE_DO, [do], tc.O, [tc.opdo], tc.D, tc.ws, stream)
+        if evs:
+            evs[3].record(stream)
+        fl.flamia_bwd(tc.prob, tc.opq, tc.opk, tc.opv, tc.opdo, tc.D, tc.m, tc.l, tc.dQ, tc.dK, tc.dV, tc.ws,
+                      stream)
+        if evs:
+            evs[4].record(stream)
+
+    for _ in range(max(3, a.warmup)):
+        step()
+    torch.cuda.synchronize()
+    st = fl.flamia_get_device_status(tc.ws)
+    if st != fl.OK:
+        raise RuntimeError(f"device status after warm-up: {fl.status_string(st)}")
+
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    evs = [[ev() for _ in range(5)] for _ in range(a.steps)]
+    t_start, t_end = ev(), ev()
+    t_start.record(stream)
+    for i in range(a.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if rank == 0 else None
+    ms = t_start.elapsed_time(t_end) / a.steps
+    ph = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])  # ms
+    quant_ms, fwd_ms, dquant_ms, bwd_ms = ph.mean(axis=0)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = flops * world / (ms * 1e-3) / 1e12
+
+    # e2e: host (pinned) inputs copied in, results (O, dQ, dK, dV) copied out, every step
+    hq, hk, hv, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
+    outs = [torch.empty_like(x, device="cpu").pin_memory() for x in (tc.O, tc.dQ, tc.dK, tc.dV)]
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
+    d2h = sum(x.numel() * x.element_size() for x in outs)
+    e2e_steps = max(3, a.steps // 2)
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        do.copy_(hdo, non_blocking=True)
+        step()
+        for o, src in zip(outs, (tc.O, tc.dQ, tc.dK, tc.dV)):
+            o.copy_(src, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_val = flops * world / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    peaks, kind = _peaks()
+    fp8_sustained = 2.0 * float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    bwd_tflops = bwd_flops / (bwd_ms * 1e-3) / 1e12
+    n_items = int(sum((l + 127) // 128 for l in w.seqlens))
+    launches_per_step = 4 + 3 + 1 + 1 + 2  # plan(4) quantize(3) fwd dO-quantize bwd dq-convert
+    cpu = None
+    if not a.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        f, dt = _oracle_sample(w, a.cpu_sample_tokens)
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"causal prefix of {a.cpu_sample_tokens} tokens of document 0, head 0 "
+                         f"(single-threaded fp64 oracle, full quantized call), {dt:.1f} s"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 (MXFP8 operands, fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": w.T, "heads": w.H, "head_dim": w.d, "documents": len(w.seqlens),
+                   "flops_per_step": flops, "l2": "inputs larger than L2 (256 MiB of bf16 Q/K/V/dO)",
+                   "fraction_of_fp8_peak": value / world / fp8_sustained,
+                   "phase_ms": {"plan+quantize_qkv": quant_ms, "fwd": fwd_ms, "quantize_do": dquant_ms,
+                                "bwd+dq_convert": bwd_ms},
+                   "fwd_tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": bwd_tflops},
+        "roofline": {"bound": "tensor", "kernel": "bwd_kernel (+dq convert)", "achieved": bwd_tflops,
+                     "peak": fp8_sustained, "unit": "TFLOP/s", "frac": bwd_tflops / fp8_sustained,
+                     "traffic": None,
+                     "peak_source": f"{kind}: 2 x bf16_tflops_sustained (dense FP8 = 2x bf16)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * a.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    a = _args()
+    if a.impl == "reference":
+        return run_reference(a)
+    return run_ours(a)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

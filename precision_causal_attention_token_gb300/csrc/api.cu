@@ -166,6 +166,7 @@ static flamia_status_t fill_params(const flamia_problem_t* p, const WsLayout& L,
   a->T = p->T; a->H = p->H; a->Hkv = p->Hkv; a->d = p->d; a->n_seq = p->n_seq;
   a->causal = p->causal ? 1 : 0;
   a->exact = p->exact ? 1 : 0;
+  a->deterministic = p->deterministic ? 1 : 0;
   a->out_bf16 = p->out_dtype == FLAMIA_BF16;
   a->max_items = L.max_items;
   a->softmax_scale = softmax_scale_of(p);
@@ -232,10 +233,7 @@ flamia_status_t flamia_bwd(const flamia_problem_t* p, const flamia_operand_t* q,
   if (!make_codes_map(&maps.q, q->codes, p->d, p->H, p->T) || !make_codes_map(&maps.k, k->codes, p->d, p->Hkv, p->T) ||
       !make_codes_map(&maps.v, v->codes, p->d, p->Hkv, p->T) || !make_codes_map(&maps.dO, dO->codes, p->d, p->H, p->T))
     return FLAMIA_ERR_CUDA;
-  if (cudaMemsetAsync(a.dq_acc, 0, sizeof(float) * (size_t)p->T * p->H * p->d, stream) != cudaSuccess)
-    return FLAMIA_ERR_CUDA;
-  if (launch_bwd(a, maps, stream) != cudaSuccess) return FLAMIA_ERR_CUDA;
-  return launch_dq_convert(a, stream) == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+  return launch_bwd(a, maps, stream) == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
 }
 
 flamia_status_t flamia_get_device_status(const void* ws, cudaStream_t stream) {

@@ -83,7 +83,160 @@ __device__ __forceinline__ float warp_max(float v) {
 
 __device__ __forceinline__ uint32_t sf_byte(int e) { return (uint32_t)min(max(e + 127, 0), 254); }
 
-template <int HD, bool OUT_BF16, bool EXACT>
+// Recompute this thread's P^ codes for one 128-key tile from S in TMEM, with
+// the forward's arithmetic (score_to_y, visible, phat_block_exp, phat_value):
+// the same inputs give the same codes and block exponents.
+__device__ __forceinline__ void recompute_phat(uint32_t t_s, float rowc, const float* kf, const float* vf, int i_loc,
+                                               int key0, int len, int causal, bool row_ok, uint32_t (&pcode)[32],
+                                               int (&Eb)[4]) {
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    uint32_t rr[32];
+    tmem_ld32(t_s + 32 * b, rr);
+    tmem_ld_wait();
+    float yv[32];
+    float M = -INFINITY;
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      const int j = 32 * b + jj;
+      yv[jj] = (row_ok && visible(i_loc, key0 + j, len, causal)) ? score_to_y(__uint_as_float(rr[jj]), rowc, kf[j], vf[j])
+                                                                 : -INFINITY;
+      M = fmaxf(M, yv[jj]);
+    }
+    Eb[b] = (M == -INFINITY) ? kEmptyBlock : phat_block_exp(M);
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4) {
+      float pv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pv[e] = (Eb[b] == kEmptyBlock) ? 0.f : phat_value(yv[4 * q4 + e], Eb[b]);
+      pcode[8 * b + q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
+    }
+  }
+}
+
+// dS and the P~ input of one 32-key block b of this thread's row, from dP in
+// TMEM (32 columns at t_dp):  Pn = P^ 2^-eV / l = code 2^(Eb - m) / l 2^-eV,
+// dS = Pn (dP - D) = code 2^(Eb - m) / l (accdP 2^edO - D 2^-eV), P~ input
+// = Pn 2^edO (the dO factor folded in).  Rows outside the document give 0.
+__device__ __forceinline__ void ds_block(uint32_t t_dp, const uint32_t* pcode_b, int Eb_b, int mi, float inv_l,
+                                         float hdo, float Di, const float* vinv_b, bool row_ok, float (&dsv)[32],
+                                         float (&ptv)[32], float& amax_ds, float& amax_pt) {
+  uint32_t rr[32];
+  tmem_ld32(t_dp, rr);
+  tmem_ld_wait();
+  const float gb = (Eb_b == kEmptyBlock) ? 0.f : ldexp_f(inv_l, Eb_b - mi);
+  amax_ds = 0.f;
+  amax_pt = 0.f;
+#pragma unroll
+  for (int q4 = 0; q4 < 8; ++q4) {
+    const uint32_t cw = pcode_b[q4];
+    const float2 p01 = unpack_e4m3x2((uint16_t)(cw & 0xFFFFu));
+    const float2 p23 = unpack_e4m3x2((uint16_t)(cw >> 16));
+    const float pd[4] = {p01.x, p01.y, p23.x, p23.y};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int jj = 4 * q4 + e;
+      const float pg = pd[e] * gb;
+      const float d_s = pg * (__uint_as_float(rr[jj]) * hdo - Di * vinv_b[jj]);
+      dsv[jj] = row_ok ? d_s : 0.f;
+      ptv[jj] = row_ok ? pg * vinv_b[jj] * hdo : 0.f;
+      amax_ds = fmaxf(amax_ds, fabsf(dsv[jj]));
+      amax_pt = fmaxf(amax_pt, ptv[jj]);
+    }
+  }
+}
+
+// Codes of 32 values scaled by 2^-e, as 8 words of 4 E4M3 bytes.
+__device__ __forceinline__ void encode32(const float (&v)[32], int e, uint32_t (&out)[8]) {
+#pragma unroll
+  for (int q4 = 0; q4 < 8; ++q4)
+    out[q4] = pack_e4m3x4(ldexp_f(v[4 * q4], -e), ldexp_f(v[4 * q4 + 1], -e), ldexp_f(v[4 * q4 + 2], -e),
+                          ldexp_f(v[4 * q4 + 3], -e));
+}
+
+// Store 32 codes (keys 32b..32b+31) of row r into a 128B-swizzled [128][128] tile.
+__device__ __forceinline__ void store_row_block(uint8_t* tile, int r, int b, const uint32_t (&w)[8]) {
+  *reinterpret_cast<uint4*>(tile + sw128_off(r, 2 * b)) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4*>(tile + sw128_off(r, 2 * b + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+
+// Store 32 fp32 values (times f) of one row at out + off, in the output dtype.
+template <bool OUT_BF16>
+__device__ __forceinline__ void store_row32(void* out, size_t off, const uint32_t (&rr)[32], float f) {
+  if constexpr (OUT_BF16) {
+    uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + off);
+#pragma unroll
+    for (int c8 = 0; c8 < 4; ++c8) {
+      uint32_t wv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 b2 =
+            __floats2bfloat162_rn(__uint_as_float(rr[8 * c8 + 2 * e]) * f, __uint_as_float(rr[8 * c8 + 2 * e + 1]) * f);
+        wv[e] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+      d4[c8] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    }
+  } else {
+    float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(out) + off);
+#pragma unroll
+    for (int c4 = 0; c4 < 8; ++c4)
+      d4[c4] = make_float4(__uint_as_float(rr[4 * c4]) * f, __uint_as_float(rr[4 * c4 + 1]) * f,
+                           __uint_as_float(rr[4 * c4 + 2]) * f, __uint_as_float(rr[4 * c4 + 3]) * f);
+  }
+}
+
+// Per-row values the backward needs for query row i of head h.
+struct RowVals {
+  int eq, edo, mi;
+  float li, Di, rowc, hdo;
+};
+__device__ __forceinline__ RowVals load_row(const AttnParams& p, int h, int tok, bool row_ok) {
+  RowVals v{0, 0, 0, 1.f, 0.f, 0.f, 1.f};
+  if (row_ok) {
+    const size_t mt = (size_t)h * p.T + tok;
+    v.eq = (int)__ldg(p.q_sc + mt) - 127;
+    v.edo = (int)__ldg(p.do_sc + mt) - 127;
+    v.mi = __ldg(p.m + mt);
+    v.li = __ldg(p.l + mt);
+    v.Di = __ldg(p.D + mt);
+  }
+  v.rowc = p.c_log2 * pow2_127(v.eq);
+  v.hdo = pow2_127(v.edo);
+  return v;
+}
+
+// The dQ operand of key block b.  Default option: one exponent per 32x32
+// block (reduced over the warp's 32 rows) and scale byte e + eK(block).  Exact
+// option: one exponent per (row, 32 keys) of dS * 2^eK(j), scale byte e.
+// Returns the default option's block exponent (reused for dK) in e_blk.
+template <bool EXACT>
+__device__ __forceinline__ uint32_t dq_operand(const float (&dsv)[32], float amax_ds, const float* kf_b, int ekb,
+                                               uint32_t (&codes)[8], int& e_blk) {
+  if constexpr (!EXACT) {
+    e_blk = noclamp_exp_clamped(warp_max(amax_ds));
+    encode32(dsv, e_blk, codes);
+    return sf_byte(e_blk + ekb);
+  } else {
+    float f[32];
+    float am = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      f[jj] = dsv[jj] * kf_b[jj];
+      am = fmaxf(am, fabsf(f[jj]));
+    }
+    const int e = noclamp_exp_clamped(am);
+    encode32(f, e, codes);
+    e_blk = 0;
+    return sf_byte(e);
+  }
+}
+
+// ============================================================================
+// dK/dV kernel (and dQ by fp32 reductions when DQ): one CTA per (document,
+// 128-key tile, KV head), looping over the group's query heads and tiles.
+// ============================================================================
+template <int HD, bool OUT_BF16, bool EXACT, bool DQ>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do) {
@@ -126,12 +279,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tb = c.tmem_base;
 
-  // number of query tiles a (document, key tile) item visits, per query head
-  auto q_range = [&](int kt, int len, int& q_first, int& n_t) {
-    n_t = (len + kTile - 1) / kTile;
-    q_first = p.causal ? kt : 0;
-  };
-
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     uint32_t ic = 0, ii = 0;
@@ -141,8 +288,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int2 it = p.bwd_items[pair];
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
       const int k0 = ds + kTile * it.y;
-      int q_first, n_t;
-      q_range(it.y, len, q_first, n_t);
+      const int n_t = (len + kTile - 1) / kTile, q_first = p.causal ? it.y : 0;
       if (!(ok = mbar_wait(&c.kv_empty, (ic & 1) ^ 1, abort_flag, hdr, 0x301))) break;
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
@@ -187,14 +333,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int pair = w / p.Hkv;
         const int2 it = p.bwd_items[pair];
         const int len = __ldg(p.cu + it.x + 1) - __ldg(p.cu + it.x);
-        int q_first, n_t;
-        q_range(it.y, len, q_first, n_t);
+        const int n_t = (len + kTile - 1) / kTile, q_first = p.causal ? it.y : 0;
         const int n_iter = G * (n_t - q_first);
         if (!(ok = mbar_wait(&c.kv_full, ic & 1, abort_flag, hdr, 0x311))) break;
         for (int t = 0; ok && t < n_iter; ++t, ++ii) {
           const int qs = ii & 1;
           if (!(ok = mbar_wait(&c.qd_full[qs], (ii >> 1) & 1, abort_flag, hdr, 0x312))) break;
-          // X0 still holds the previous iteration's scale factors until its MMAs finish
+          // X0 holds the previous iteration's scale factors until its MMAs finish
           if (ii > 0 && !(ok = mbar_wait(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x313))) break;
           tc_fence_after();
 #pragma unroll
@@ -219,10 +364,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_mxf8(tb + kColDK, bdesc_mn(dsk, kk * 32 * 128, 128), bdesc_mn(tl.q[qs], kk * 32 * HD, HD),
                      idesc_mxf8(128, HD, 1, 1, kk, kk), tb + kColSfDK, tb + kColSfOne, acc);
           }
+          if constexpr (DQ) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // contraction over the 128 keys
-            mma_mxf8(tb + kColX1, bdesc_k(tl.ds, 32 * kk, 128), bdesc_mn(tl.k, kk * 32 * HD, HD),
-                     idesc_mxf8(128, HD, 0, 1, kk, kk), tb + kColSfDQ, tb + kColSfOne, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)  // contraction over the 128 keys
+              mma_mxf8(tb + kColX1, bdesc_k(tl.ds, 32 * kk, 128), bdesc_mn(tl.k, kk * 32 * HD, HD),
+                       idesc_mxf8(128, HD, 0, 1, kk, kk), tb + kColSfDQ, tb + kColSfOne, kk > 0 ? 1u : 0u);
+          }
           tc_commit(&c.mm_done);
           tc_commit(&c.qd_empty[qs]);
           if (t == n_iter - 1) {
@@ -243,8 +390,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int pair = w / p.Hkv, hk = w - pair * p.Hkv;
       const int2 it = p.bwd_items[pair];
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
-      int q_first, n_t;
-      q_range(it.y, len, q_first, n_t);
+      const int n_t = (len + kTile - 1) / kTile, q_first = p.causal ? it.y : 0;
       if (!(ok = mbar_wait(&c.kv_full, ic & 1, abort_flag, hdr, 0x321))) break;
       const int key0 = kTile * it.y;
       for (int g = 0; ok && g < G; ++g) {
@@ -252,137 +398,61 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int qt = q_first; ok && qt < n_t; ++qt, ++ii) {
           const int i_loc = kTile * qt + r;
           const bool row_ok = i_loc < len;
-          const size_t mt = (size_t)h * p.T + ds + i_loc;
-          int eq = 0, edo = 0, mi = 0;
-          float li = 1.f, Di = 0.f;
-          if (row_ok) {
-            eq = (int)__ldg(p.q_sc + mt) - 127;
-            edo = (int)__ldg(p.do_sc + mt) - 127;
-            mi = __ldg(p.m + mt);
-            li = __ldg(p.l + mt);
-            Di = __ldg(p.D + mt);
-          }
-          const float rowc = p.c_log2 * pow2_127(eq);
-          const float hdo = pow2_127(edo);
-          // ---- recompute P^ exactly as the forward does
+          const RowVals rv = load_row(p, h, ds + i_loc, row_ok);
           if (!(ok = mbar_wait(&c.s_full, ii & 1, abort_flag, hdr, 0x322))) break;
           tc_fence_after();
           uint32_t pcode[32];
           int Eb[4];
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            uint32_t rr[32];
-            tmem_ld32(taddr(tb, warp * 32, kColX0 + 32 * b), rr);
-            tmem_ld_wait();
-            float yv[32];
-            float M = -INFINITY;
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              const int j = 32 * b + jj;
-              yv[jj] = (row_ok && visible(i_loc, key0 + j, len, p.causal))
-                           ? score_to_y(__uint_as_float(rr[jj]), rowc, c.kf[j], c.vf[j])
-                           : -INFINITY;
-              M = fmaxf(M, yv[jj]);
-            }
-            Eb[b] = (M == -INFINITY) ? kEmptyBlock : phat_block_exp(M);
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              float pv[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) pv[e] = (Eb[b] == kEmptyBlock) ? 0.f : phat_value(yv[4 * q4 + e], Eb[b]);
-              pcode[8 * b + q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
-            }
-          }
-          // ---- dS, P~ per 32-key block
+          recompute_phat(taddr(tb, warp * 32, kColX0), rv.rowc, c.kf, c.vf, i_loc, key0, len, p.causal, row_ok, pcode,
+                         Eb);
           if (!(ok = mbar_wait(&c.dp_full, ii & 1, abort_flag, hdr, 0x323))) break;
+          // the previous iteration's MMAs must be done with the P~ / dS tiles
+          if (ii > 0 && !(ok = mbar_wait(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x326))) break;
           tc_fence_after();
-          const float inv_l = 1.0f / li;
+          const float inv_l = 1.0f / rv.li;
           uint32_t word_dq = 0;
           const int par = ii & 1;
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
-            uint32_t rr[32];
-            tmem_ld32(taddr(tb, warp * 32, kColX1 + 32 * b), rr);
-            tmem_ld_wait();
-            // Pn = P^ 2^-eV / l = code * 2^(Eb - m) / l * 2^-eV ; dS = Pn (dP - D)
-            const float gb = (Eb[b] == kEmptyBlock) ? 0.f : ldexp_f(inv_l, Eb[b] - mi);
             float dsv[32], ptv[32];
-            float amax_ds = 0.f, amax_pt = 0.f;
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              const uint32_t cw = pcode[8 * b + q4];
-              const float2 p01 = unpack_e4m3x2((uint16_t)(cw & 0xFFFFu));
-              const float2 p23 = unpack_e4m3x2((uint16_t)(cw >> 16));
-              const float pd[4] = {p01.x, p01.y, p23.x, p23.y};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int jj = 4 * q4 + e, j = 32 * b + jj;
-                const float pn = pd[e] * gb * c.vinv[j];
-                const float dpv = __uint_as_float(rr[jj]) * hdo;  // dP * 2^-eV(j)
-                const float d_s = (pd[e] * gb) * (dpv - Di * c.vinv[j]);
-                dsv[jj] = row_ok ? d_s : 0.f;
-                ptv[jj] = row_ok ? pn * hdo : 0.f;
-                amax_ds = fmaxf(amax_ds, fabsf(dsv[jj]));
-                amax_pt = fmaxf(amax_pt, ptv[jj]);
-              }
-            }
-            // 32 x 32 block exponents (this warp's 32 queries x key block b)
+            float amax_ds, amax_pt;
+            ds_block(taddr(tb, warp * 32, kColX1 + 32 * b), pcode + 8 * b, Eb[b], rv.mi, inv_l, rv.hdo, rv.Di,
+                     c.vinv + 32 * b, row_ok, dsv, ptv, amax_ds, amax_pt);
+            // P~: 32 x 32 block (this warp's 32 queries x key block b)
             const int e_pt = noclamp_exp_clamped(warp_max(amax_pt));
-            uint32_t ptc[8], dsc[8];
+            uint32_t codes[8];
+            encode32(ptv, e_pt, codes);
+            store_row_block(tl.pt, r, b, codes);
+            uint32_t kbyte;
             if constexpr (!EXACT) {
-              const int e_ds = noclamp_exp_clamped(warp_max(amax_ds));
-#pragma unroll
-              for (int q4 = 0; q4 < 8; ++q4) {
-                ptc[q4] = pack_e4m3x4(ldexp_f(ptv[4 * q4], -e_pt), ldexp_f(ptv[4 * q4 + 1], -e_pt),
-                                      ldexp_f(ptv[4 * q4 + 2], -e_pt), ldexp_f(ptv[4 * q4 + 3], -e_pt));
-                dsc[q4] = pack_e4m3x4(ldexp_f(dsv[4 * q4], -e_ds), ldexp_f(dsv[4 * q4 + 1], -e_ds),
-                                      ldexp_f(dsv[4 * q4 + 2], -e_ds), ldexp_f(dsv[4 * q4 + 3], -e_ds));
-              }
-              word_dq |= sf_byte(e_ds + c.ekb[b]) << (8 * b);
-              if (lane == 0) {
-                c.xch[par][0][warp] = (c.xch[par][0][warp] & ~(0xFFu << (8 * b))) | (sf_byte(e_pt) << (8 * b));
-                c.xch[par][1][warp] = (c.xch[par][1][warp] & ~(0xFFu << (8 * b))) | (sf_byte(e_ds + eq) << (8 * b));
-              }
+              int e_ds;
+              word_dq |= dq_operand<false>(dsv, amax_ds, c.kf + 32 * b, c.ekb[b], codes, e_ds) << (8 * b);
+              store_row_block(tl.ds, r, b, codes);
+              kbyte = sf_byte(e_ds + rv.eq);  // dK operand: the same codes, Q's block exponent folded in
             } else {
-              // dQ payload: per (row, 32 keys) on dS * 2^eK(j); dK payload: 32x32 on dS * 2^eQ(i)
-              float amq = 0.f;
+              if constexpr (DQ) {
+                int unused;
+                word_dq |= dq_operand<true>(dsv, amax_ds, c.kf + 32 * b, c.ekb[b], codes, unused) << (8 * b);
+                store_row_block(tl.ds, r, b, codes);
+              }
+              // dK operand: 32 x 32 block of dS * 2^eQ(i)
+              const float feq = pow2_127(rv.eq);
+              float f[32];
 #pragma unroll
-              for (int jj = 0; jj < 32; ++jj) amq = fmaxf(amq, fabsf(dsv[jj] * c.kf[32 * b + jj]));
-              const int e_q = noclamp_exp_clamped(amq);
-              const float feq = pow2_127(eq);
+              for (int jj = 0; jj < 32; ++jj) f[jj] = dsv[jj] * feq;
               const int e_k = noclamp_exp_clamped(warp_max(amax_ds * feq));
-              uint32_t dkc[8];
-#pragma unroll
-              for (int q4 = 0; q4 < 8; ++q4) {
-                float a4[4], b4[4], p4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int jj = 4 * q4 + e;
-                  a4[e] = ldexp_f(dsv[jj] * c.kf[32 * b + jj], -e_q);
-                  b4[e] = ldexp_f(dsv[jj] * feq, -e_k);
-                  p4[e] = ldexp_f(ptv[jj], -e_pt);
-                }
-                dsc[q4] = pack_e4m3x4(a4[0], a4[1], a4[2], a4[3]);
-                dkc[q4] = pack_e4m3x4(b4[0], b4[1], b4[2], b4[3]);
-                ptc[q4] = pack_e4m3x4(p4[0], p4[1], p4[2], p4[3]);
-              }
-              word_dq |= sf_byte(e_q) << (8 * b);
-              if (lane == 0) {
-                c.xch[par][0][warp] = (c.xch[par][0][warp] & ~(0xFFu << (8 * b))) | (sf_byte(e_pt) << (8 * b));
-                c.xch[par][1][warp] = (c.xch[par][1][warp] & ~(0xFFu << (8 * b))) | (sf_byte(e_k) << (8 * b));
-              }
-#pragma unroll
-              for (int h16 = 0; h16 < 2; ++h16)
-                *reinterpret_cast<uint4*>(tl.dsk + sw128_off(r, 2 * b + h16)) =
-                    make_uint4(dkc[4 * h16], dkc[4 * h16 + 1], dkc[4 * h16 + 2], dkc[4 * h16 + 3]);
+              encode32(f, e_k, codes);
+              store_row_block(tl.dsk, r, b, codes);
+              kbyte = sf_byte(e_k);
             }
-#pragma unroll
-            for (int h16 = 0; h16 < 2; ++h16) {
-              *reinterpret_cast<uint4*>(tl.pt + sw128_off(r, 2 * b + h16)) =
-                  make_uint4(ptc[4 * h16], ptc[4 * h16 + 1], ptc[4 * h16 + 2], ptc[4 * h16 + 3]);
-              *reinterpret_cast<uint4*>(tl.ds + sw128_off(r, 2 * b + h16)) =
-                  make_uint4(dsc[4 * h16], dsc[4 * h16 + 1], dsc[4 * h16 + 2], dsc[4 * h16 + 3]);
+            if (lane == 0) {
+              c.xch[par][0][warp] = (c.xch[par][0][warp] & ~(0xFFu << (8 * b))) | (sf_byte(e_pt) << (8 * b));
+              c.xch[par][1][warp] = (c.xch[par][1][warp] & ~(0xFFu << (8 * b))) | (kbyte << (8 * b));
             }
+          }
+          if constexpr (!DQ) {  // dP has been read: X1 may take the next dP
+            tc_fence_before();
+            mbar_arrive(&c.x1_free);
           }
           // scale-factor words: dV / dK rows are keys (key block = this warp),
           // one byte per query block; dQ rows are queries (this thread's row)
@@ -401,24 +471,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(&c.ds_full);
-          // ---- dQ tile -> fp32 buffer
-          if (!(ok = mbar_wait(&c.mm_done, ii & 1, abort_flag, hdr, 0x324))) break;
-          tc_fence_after();
-          float* dst = p.dq_acc + ((size_t)(ds + i_loc) * p.H + h) * HD;
+          if constexpr (DQ) {
+            // ---- dQ tile -> fp32 buffer
+            if (!(ok = mbar_wait(&c.mm_done, ii & 1, abort_flag, hdr, 0x324))) break;
+            tc_fence_after();
+            float* dst = p.dq_acc + ((size_t)(ds + i_loc) * p.H + h) * HD;
 #pragma unroll
-          for (int cb = 0; cb < HD / 32; ++cb) {
-            uint32_t rr[32];
-            tmem_ld32(taddr(tb, warp * 32, kColX1 + 32 * cb), rr);
-            tmem_ld_wait();
-            if (row_ok) {
+            for (int cb = 0; cb < HD / 32; ++cb) {
+              uint32_t rr[32];
+              tmem_ld32(taddr(tb, warp * 32, kColX1 + 32 * cb), rr);
+              tmem_ld_wait();
+              if (row_ok) {
 #pragma unroll
-              for (int e = 0; e < 32; e += 4)
-                red_add_v4(dst + 32 * cb + e, __uint_as_float(rr[e]) * sm_scale, __uint_as_float(rr[e + 1]) * sm_scale,
-                           __uint_as_float(rr[e + 2]) * sm_scale, __uint_as_float(rr[e + 3]) * sm_scale);
+                for (int e = 0; e < 32; e += 4)
+                  red_add_v4(dst + 32 * cb + e, __uint_as_float(rr[e]) * sm_scale,
+                             __uint_as_float(rr[e + 1]) * sm_scale, __uint_as_float(rr[e + 2]) * sm_scale,
+                             __uint_as_float(rr[e + 3]) * sm_scale);
+              }
             }
+            tc_fence_before();
+            mbar_arrive(&c.x1_free);
           }
-          tc_fence_before();
-          mbar_arrive(&c.x1_free);
         }
       }
       if (!ok) break;
@@ -439,32 +512,233 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t rr[32];
           tmem_ld32(taddr(tb, warp * 32, col + 32 * cb), rr);
           tmem_ld_wait();
-          if (key_ok) {
-            if constexpr (OUT_BF16) {
-              uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(outp) + koff + 32 * cb);
-#pragma unroll
-              for (int c8 = 0; c8 < 4; ++c8) {
-                uint32_t wv[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(rr[8 * c8 + 2 * e]) * f,
-                                                            __uint_as_float(rr[8 * c8 + 2 * e + 1]) * f);
-                  wv[e] = *reinterpret_cast<uint32_t*>(&b2);
-                }
-                d4[c8] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-              }
-            } else {
-              float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(outp) + koff + 32 * cb);
-#pragma unroll
-              for (int c4 = 0; c4 < 8; ++c4)
-                d4[c4] = make_float4(__uint_as_float(rr[4 * c4]) * f, __uint_as_float(rr[4 * c4 + 1]) * f,
-                                     __uint_as_float(rr[4 * c4 + 2]) * f, __uint_as_float(rr[4 * c4 + 3]) * f);
-            }
-          }
+          if (key_ok) store_row32<OUT_BF16>(outp, koff + 32 * cb, rr, f);
         }
       }
       tc_fence_before();
       mbar_arrive(&c.acc_free);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  drain_after_abort(abort_flag);
+  if (warp == 5) tmem_dealloc(tb, 512);
+}
+
+// ============================================================================
+// Deterministic dQ kernel: one CTA per (document, 128-query tile, head) from
+// the forward's work list; dQ accumulates in TMEM over the key tiles in a
+// fixed order and is written once (no atomics).  Recomputes S, P^, dP and dS
+// with the same functions as the dK/dV kernel.
+// ============================================================================
+constexpr int kDqStages = 2;
+constexpr uint32_t kDqColAcc = 0, kDqColX0 = 128, kDqColX1 = 256;
+constexpr uint32_t kDqColSf = kDqColX0 + 0, kDqColSfOne = kDqColX0 + 4;
+
+template <int HD>
+struct __align__(1024) DqTiles {
+  uint8_t q[kTile * HD];
+  uint8_t dO[kTile * HD];
+  uint8_t k[kDqStages][kTile * HD];
+  uint8_t v[kDqStages][kTile * HD];
+  uint8_t ds[kTile * kTile];
+};
+
+struct DqCtl {
+  float kf[kDqStages][kTile], vf[kDqStages][kTile], vinv[kDqStages][kTile];
+  int ekb[kDqStages][4];
+  uint64_t qd_full, qd_empty, kv_full[kDqStages], kv_empty[kDqStages];
+  uint64_t s_full, dp_full, dp_free, ds_full, mm_done, dq_full, dq_free;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int HD>
+constexpr size_t dq_smem_bytes() {
+  return sizeof(DqTiles<HD>) + sizeof(DqCtl) + 1024;
+}
+
+template <int HD, bool OUT_BF16, bool EXACT>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    dq_kernel(const AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+              const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  DqTiles<HD>& tl = *reinterpret_cast<DqTiles<HD>*>(base);
+  DqCtl& c = *reinterpret_cast<DqCtl*>(base + sizeof(DqTiles<HD>));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = p.H / p.Hkv;
+  const int n_work = p.hdr->n_items * p.H;
+  volatile int* abort_flag = &c.abort_flag;
+  WsHeader* hdr = p.hdr;
+  if (tid == 0) {
+    mbar_init(&c.qd_full, 1);
+    mbar_init(&c.qd_empty, 1);
+    for (int s = 0; s < kDqStages; ++s) {
+      mbar_init(&c.kv_full[s], 32);
+      mbar_init(&c.kv_empty[s], 1 + 128);
+    }
+    mbar_init(&c.s_full, 1);
+    mbar_init(&c.dp_full, 1);
+    mbar_init(&c.dp_free, 128);
+    mbar_init(&c.ds_full, 128);
+    mbar_init(&c.mm_done, 1);
+    mbar_init(&c.dq_full, 1);
+    mbar_init(&c.dq_free, 128);
+    c.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) tmem_alloc(&c.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = c.tmem_base;
+
+  if (warp == 4) {
+    uint32_t ic = 0, kv = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++ic) {
+      const int pair = w / p.H, h = w - pair * p.H, hk = h / G;
+      const int2 it = p.fwd_items[pair];
+      const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
+      const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
+      if (!(ok = mbar_wait(&c.qd_empty, (ic & 1) ^ 1, abort_flag, hdr, 0x401))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&c.qd_full, 2 * kTile * HD);
+        tma_load_3d(tl.q, &map_q, &c.qd_full, 0, h, ds + kTile * it.y);
+        tma_load_3d(tl.dO, &map_do, &c.qd_full, 0, h, ds + kTile * it.y);
+      }
+      for (int kt = 0; kt < n_kt; ++kt, ++kv) {
+        const int st = kv % kDqStages;
+        const uint32_t ph = (kv / kDqStages) & 1;
+        if (!(ok = mbar_wait(&c.kv_empty[st], ph ^ 1, abort_flag, hdr, 0x402))) break;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = lane * 4 + jj, key = kTile * kt + j;
+          int ek = 0, ev = 0;
+          if (key < len) {
+            ek = (int)__ldg(p.k_sc + (size_t)hk * p.T + ds + key) - 127;
+            ev = (int)__ldg(p.v_sc + (size_t)hk * p.T + ds + key) - 127;
+          }
+          c.kf[st][j] = pow2_127(ek);
+          c.vf[st][j] = (float)ev;
+          c.vinv[st][j] = pow2_127(-ev);
+          if ((j & 31) == 0) c.ekb[st][j >> 5] = ek;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&c.kv_full[st], 2 * kTile * HD);
+          tma_load_3d(tl.k[st], &map_k, &c.kv_full[st], 0, hk, ds + kTile * kt);
+          tma_load_3d(tl.v[st], &map_v, &c.kv_full[st], 0, hk, ds + kTile * kt);
+        } else {
+          mbar_arrive(&c.kv_full[st]);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    if (elect_one()) {
+      uint32_t ic = 0, kv = 0, ii = 0;
+      bool ok = true;
+      const uint32_t id_sp = idesc_f8(128, 128, 0, 0);
+      for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++ic) {
+        const int pair = w / p.H;
+        const int2 it = p.fwd_items[pair];
+        const int len = __ldg(p.cu + it.x + 1) - __ldg(p.cu + it.x);
+        const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
+        if (!(ok = mbar_wait(&c.qd_full, ic & 1, abort_flag, hdr, 0x411))) break;
+        for (int kt = 0; ok && kt < n_kt; ++kt, ++kv, ++ii) {
+          const int st = kv % kDqStages;
+          const uint32_t ph = (kv / kDqStages) & 1;
+          if (!(ok = mbar_wait(&c.kv_full[st], ph, abort_flag, hdr, 0x412))) break;
+          if (ii > 0 && !(ok = mbar_wait(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x413))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < HD / 32; ++kk)
+            mma_f8(tb + kDqColX0, bdesc_k(tl.q, 32 * kk, HD), bdesc_k(tl.k[st], 32 * kk, HD), id_sp, kk > 0);
+          tc_commit(&c.s_full);
+          if (!(ok = mbar_wait(&c.dp_free, (ii & 1) ^ 1, abort_flag, hdr, 0x414))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < HD / 32; ++kk)
+            mma_f8(tb + kDqColX1, bdesc_k(tl.dO, 32 * kk, HD), bdesc_k(tl.v[st], 32 * kk, HD), id_sp, kk > 0);
+          tc_commit(&c.dp_full);
+          if (!(ok = mbar_wait(&c.ds_full, ii & 1, abort_flag, hdr, 0x415))) break;
+          if (kt == 0 && !(ok = mbar_wait(&c.dq_free, (ic & 1) ^ 1, abort_flag, hdr, 0x416))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_mxf8(tb + kDqColAcc, bdesc_k(tl.ds, 32 * kk, 128), bdesc_mn(tl.k[st], kk * 32 * HD, HD),
+                     idesc_mxf8(128, HD, 0, 1, kk, kk), tb + kDqColSf, tb + kDqColSfOne, (kt > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&c.mm_done);
+          tc_commit(&c.kv_empty[st]);
+          if (kt == n_kt - 1) {
+            tc_commit(&c.dq_full);
+            tc_commit(&c.qd_empty);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    const int r = tid;
+    uint32_t ic = 0, kv = 0, ii = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++ic) {
+      const int pair = w / p.H, h = w - pair * p.H;
+      const int2 it = p.fwd_items[pair];
+      const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
+      const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
+      const int i_loc = kTile * it.y + r;
+      const bool row_ok = i_loc < len;
+      const RowVals rv = load_row(p, h, ds + i_loc, row_ok);
+      const float inv_l = 1.0f / rv.li;
+      for (int kt = 0; ok && kt < n_kt; ++kt, ++kv, ++ii) {
+        const int st = kv % kDqStages;
+        const uint32_t ph = (kv / kDqStages) & 1;
+        if (!(ok = mbar_wait(&c.kv_full[st], ph, abort_flag, hdr, 0x421))) break;
+        if (!(ok = mbar_wait(&c.s_full, ii & 1, abort_flag, hdr, 0x422))) break;
+        tc_fence_after();
+        uint32_t pcode[32];
+        int Eb[4];
+        recompute_phat(taddr(tb, warp * 32, kDqColX0), rv.rowc, c.kf[st], c.vf[st], i_loc, kTile * kt, len, p.causal,
+                       row_ok, pcode, Eb);
+        if (!(ok = mbar_wait(&c.dp_full, ii & 1, abort_flag, hdr, 0x423))) break;
+        if (ii > 0 && !(ok = mbar_wait(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x424))) break;
+        tc_fence_after();
+        uint32_t word_dq = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          float dsv[32], ptv[32];
+          float amax_ds, amax_pt;
+          ds_block(taddr(tb, warp * 32, kDqColX1 + 32 * b), pcode + 8 * b, Eb[b], rv.mi, inv_l, rv.hdo, rv.Di,
+                   c.vinv[st] + 32 * b, row_ok, dsv, ptv, amax_ds, amax_pt);
+          uint32_t codes[8];
+          int e_blk;
+          word_dq |= dq_operand<EXACT>(dsv, amax_ds, c.kf[st] + 32 * b, c.ekb[st][b], codes, e_blk) << (8 * b);
+          store_row_block(tl.ds, r, b, codes);
+        }
+        tc_fence_before();
+        mbar_arrive(&c.dp_free);
+        tmem_st4(taddr(tb, warp * 32, kDqColSf), word_dq, word_dq, word_dq, word_dq);
+        tmem_st4(taddr(tb, warp * 32, kDqColSfOne), 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&c.ds_full);
+        mbar_arrive(&c.kv_empty[st]);
+      }
+      if (!ok) break;
+      if (!(ok = mbar_wait(&c.dq_full, ic & 1, abort_flag, hdr, 0x425))) break;
+      tc_fence_after();
+      const size_t off = ((size_t)(ds + i_loc) * p.H + h) * HD;
+#pragma unroll
+      for (int cb = 0; cb < HD / 32; ++cb) {
+        uint32_t rr[32];
+        tmem_ld32(taddr(tb, warp * 32, kDqColAcc + 32 * cb), rr);
+        tmem_ld_wait();
+        if (row_ok) store_row32<OUT_BF16>(p.dQ, off + 32 * cb, rr, p.softmax_scale);
+      }
+      tc_fence_before();
+      mbar_arrive(&c.dq_free);
     }
   }
   tc_fence_before();
@@ -490,18 +764,39 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, void* out, size
 
 int sm_count();
 
+template <typename K>
+static cudaError_t set_smem(K kernel, size_t smem) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
 template <int HD, bool OB, bool EX>
 static cudaError_t launch_bwd_t(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
+  const bool det = p.exact || p.deterministic;
+  const int nsm = sm_count();
   const size_t smem = bwd_smem_bytes<HD>();
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_kernel<HD, OB, EX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
   long work = (long)p.max_items * p.Hkv;
-  int grid = (int)(work < sm_count() ? work : sm_count());
-  bwd_kernel<HD, OB, EX><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO);
+  int grid = (int)(work < nsm ? work : nsm);
+  cudaError_t e;
+  if (!det) {
+    if ((e = set_smem(bwd_kernel<HD, OB, EX, true>, smem)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(p.dq_acc, 0, sizeof(float) * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
+    bwd_kernel<HD, OB, EX, true><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t n4 = (size_t)p.T * p.H * HD / 4;
+    int cg = (int)((n4 + 255) / 256);
+    if (cg > nsm * 8) cg = nsm * 8;
+    if (OB) dq_convert_kernel<true><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4);
+    else dq_convert_kernel<false><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4);
+    return cudaGetLastError();
+  }
+  if ((e = set_smem(bwd_kernel<HD, OB, EX, false>, smem)) != cudaSuccess) return e;
+  bwd_kernel<HD, OB, EX, false><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const size_t dsm = dq_smem_bytes<HD>();
+  if ((e = set_smem(dq_kernel<HD, OB, EX>, dsm)) != cudaSuccess) return e;
+  long dwork = (long)p.max_items * p.H;
+  int dgrid = (int)(dwork < nsm ? dwork : nsm);
+  dq_kernel<HD, OB, EX><<<dgrid, kBwdThreads, dsm, st>>>(p, m.q, m.k, m.v, m.dO);
   return cudaGetLastError();
 }
 
@@ -512,15 +807,6 @@ cudaError_t launch_bwd(const AttnParams& p, const AttnMaps& m, cudaStream_t st) 
   }
   if (p.exact) return p.out_bf16 ? launch_bwd_t<64, true, true>(p, m, st) : launch_bwd_t<64, false, true>(p, m, st);
   return p.out_bf16 ? launch_bwd_t<64, true, false>(p, m, st) : launch_bwd_t<64, false, false>(p, m, st);
-}
-
-cudaError_t launch_dq_convert(const AttnParams& p, cudaStream_t st) {
-  const size_t n4 = (size_t)p.T * p.H * p.d / 4;
-  int grid = (int)((n4 + 255) / 256);
-  if (grid > sm_count() * 8) grid = sm_count() * 8;
-  if (p.out_bf16) dq_convert_kernel<true><<<grid, 256, 0, st>>>(p.dq_acc, p.dQ, n4);
-  else dq_convert_kernel<false><<<grid, 256, 0, st>>>(p.dq_acc, p.dQ, n4);
-  return cudaGetLastError();
 }
 
 }  // namespace flamia

@@ -24,7 +24,7 @@ cudaError_t launch_plan(const flamia_problem_t& p, const WsLayout& L, uint8_t* w
 
 // Everything the attention kernels need for one call (host-built).
 struct AttnParams {
-  int T, H, Hkv, d, n_seq, causal, exact, out_bf16, max_items;
+  int T, H, Hkv, d, n_seq, causal, exact, deterministic, out_bf16, max_items;
   float softmax_scale;  // c' (scores)
   float c_log2;         // softmax_scale * log2(e)
   const int32_t* cu;
@@ -52,6 +52,5 @@ struct AttnMaps {
 
 cudaError_t launch_fwd(const AttnParams& p, const AttnMaps& maps, cudaStream_t st);
 cudaError_t launch_bwd(const AttnParams& p, const AttnMaps& maps, cudaStream_t st);
-cudaError_t launch_dq_convert(const AttnParams& p, cudaStream_t st);
 
 }  // namespace flamia
