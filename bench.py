@@ -29,7 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "causal fwd+bwd attn TFLOP/s incl. quant, MXFP8 d=128; % of dense FP8 peak"
-WORKLOAD = "batched causal 4 rows x 4096 tokens, H=16, d=128, bf16 N(0,1), MXFP8"
+WORKLOAD = "batched causal {rows} rows x 4096 tokens, H=16, d=128, bf16 N(0,1), MXFP8"
 
 
 def _args():
@@ -43,6 +43,9 @@ def _args():
     ap.add_argument("--ref-sample-tokens", type=int, default=1024,
                     help="causal prefix length per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=4,
+                    help="4096-token rows of the batched workload (4 = the benchmark workload; fewer rows give "
+                         "a smaller case of the same kernels for profiler captures)")
     return ap.parse_args()
 
 
@@ -113,9 +116,12 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _workload():
+def _workload(rows: int = 4):
     import synth
-    return synth.workload(2)
+    w = synth.workload(2)
+    if rows != 4:
+        w = synth.custom([4096] * rows, H=16, d=128, seed=w.seed, name=f"batched {rows}x4096 H=16 d=128 bf16")
+    return w
 
 
 _SAMPLE_CACHE: dict = {}
@@ -157,7 +163,7 @@ def run_reference(a):
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": a.gpus,
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1e3 * tot / a.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample": sample},
+            "config": {"workload": WORKLOAD.format(rows=4), "sample": sample},
             "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -177,7 +183,7 @@ def run_ours(a):
     dev = torch.device("cuda", local)
     __graft_entry__.build()
 
-    w = _workload()
+    w = _workload(a.rows)
     q, k, v, do = (torch.from_numpy(w.tensor(n)).to(dev, torch.bfloat16) for n in ("q", "k", "v", "do"))
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
     tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu)
@@ -287,7 +293,7 @@ def run_ours(a):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 (MXFP8 operands, fp32 accumulate)", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens": w.T, "heads": w.H, "head_dim": w.d, "documents": len(w.seqlens),
+        "config": {"workload": WORKLOAD.format(rows=a.rows), "tokens": w.T, "heads": w.H, "head_dim": w.d, "documents": len(w.seqlens),
                    "flops_per_step": flops, "l2": "inputs larger than L2 (256 MiB of bf16 Q/K/V/dO)",
                    "fraction_of_fp8_peak": value / world / fp8_sustained,
                    "phase_ms": {"plan+quantize_qkv": quant_ms, "fwd": fwd_ms, "quantize_do": dquant_ms,

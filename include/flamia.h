@@ -119,7 +119,9 @@ size_t flamia_workspace_size(const flamia_problem_t* p);
  * microbatch, items issued to a persistent grid in descending cost).
  * Forward items are (document, 128-query tile) with cost = key tiles visited;
  * backward items are (document, 128-key tile) with cost = query tiles
- * visited; ties keep document order.  Reads cu_seqlens on the device only. */
+ * visited; ties keep document order.  Reads cu_seqlens on the device only.
+ * Also clears the workspace's device status word and test hooks: the status
+ * read after flamia_bwd covers one call, plan through backward. */
 flamia_status_t flamia_plan(const flamia_problem_t* p, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Fused quantizer ([SUM] §3.1, §3.2; [READ] 4.4 fused quantization).
@@ -168,6 +170,18 @@ flamia_status_t flamia_get_device_status(const void* ws, cudaStream_t stream);
 
 /* Clears the device status word (stream-ordered, no synchronisation). */
 flamia_status_t flamia_clear_device_status(void* ws, cudaStream_t stream);
+
+/* Test hook (not for the hot path): make the next flamia_fwd / flamia_bwd
+ * calls on workspace `ws` record, for every (query head h, query token i,
+ * key token j) they evaluate, the P^ code in codes[(h*T + i)*T + j] (device
+ * uint8 [H][T][T]) and each 32-key block's exponent in
+ * exps[(h*T + i)*T + j0] at the block's first key j0 (device int32 [H][T][T]).
+ * Both kernels write the P^ they use, so a caller can check that the backward
+ * rebuilds the forward's P^ bit for bit ([SUM] §3.3).  NULL, NULL switches the
+ * hook off.  Must be called after flamia_plan (which does not touch it) and
+ * synchronises `stream`. */
+flamia_status_t flamia_debug_set_phat_dump(void* ws, size_t ws_bytes, void* codes, int32_t* exps,
+                                           cudaStream_t stream);
 
 /* Static description of a status code. */
 const char* flamia_status_string(flamia_status_t s);

@@ -20,7 +20,8 @@ F32, BF16 = 0, 1
 ROLE_QKV, ROLE_DO = 0, 1
 
 EXPORTED = ("flamia_workspace_size", "flamia_plan", "flamia_quantize", "flamia_fwd", "flamia_bwd",
-            "flamia_get_device_status", "flamia_clear_device_status", "flamia_status_string")
+            "flamia_get_device_status", "flamia_clear_device_status", "flamia_status_string",
+            "flamia_debug_set_phat_dump")
 
 
 class FlamiaError(RuntimeError):
@@ -67,6 +68,8 @@ def load_library(path: str = LIB_PATH):
     L.flamia_get_device_status.restype, L.flamia_get_device_status.argtypes = i32, [vp, vp]
     L.flamia_clear_device_status.restype, L.flamia_clear_device_status.argtypes = i32, [vp, vp]
     L.flamia_status_string.restype, L.flamia_status_string.argtypes = ctypes.c_char_p, [i32]
+    L.flamia_debug_set_phat_dump.restype = i32
+    L.flamia_debug_set_phat_dump.argtypes = [vp, sz, vp, vp, vp]
     _lib = L
     return L
 
@@ -136,6 +139,12 @@ def flamia_get_device_status(ws, stream=None) -> int:
     return int(load_library().flamia_get_device_status(_ptr(ws), _stream(stream)))
 
 
+def flamia_debug_set_phat_dump(ws, codes, exps, stream=None):
+    """Test hook: record P^ codes / block exponents of the next fwd/bwd calls (None, None: off)."""
+    _check(load_library().flamia_debug_set_phat_dump(_ptr(ws), ws.numel() * ws.element_size(), _ptr(codes), _ptr(exps),
+                                                     _stream(stream)), "flamia_debug_set_phat_dump")
+
+
 def flamia_clear_device_status(ws, stream=None):
     _check(load_library().flamia_clear_device_status(_ptr(ws), _stream(stream)), "flamia_clear_device_status")
 
@@ -171,7 +180,7 @@ class TrainCall:
         nbytes = flamia_workspace_size(self.prob)
         if nbytes == 0:
             raise FlamiaError(ERR_INVALID_ARG, "flamia_workspace_size")
-        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
         u8 = dict(dtype=torch.uint8, device=dev)
         T, H, Hkv, d = self.T, self.H, self.Hkv, self.d
         odt = torch.bfloat16 if self.out_dtype == BF16 else torch.float32

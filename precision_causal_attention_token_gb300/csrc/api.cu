@@ -2,6 +2,7 @@
 // layout, TMA descriptors and kernel launches.  No allocation, no host
 // synchronisation on the plan/quantize/fwd/bwd paths.
 #include <cmath>
+#include <cstddef>
 #include <cstring>
 #include <cudaTypedefs.h>
 
@@ -243,6 +244,19 @@ flamia_status_t flamia_get_device_status(const void* ws, cudaStream_t stream) {
       cudaStreamSynchronize(stream) != cudaSuccess)
     return FLAMIA_ERR_CUDA;
   return static_cast<flamia_status_t>(st);
+}
+
+flamia_status_t flamia_debug_set_phat_dump(void* ws, size_t ws_bytes, void* codes, int32_t* exps,
+                                           cudaStream_t stream) {
+  if (!ws || ws_bytes < sizeof(WsHeader) || (codes == nullptr) != (exps == nullptr)) return FLAMIA_ERR_INVALID_ARG;
+  static thread_local void* ptrs[2];
+  ptrs[0] = codes;
+  ptrs[1] = exps;
+  uint8_t* dst = static_cast<uint8_t*>(ws) + offsetof(WsHeader, dbg_phat);
+  if (cudaMemcpyAsync(dst, ptrs, sizeof(ptrs), cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return FLAMIA_ERR_CUDA;
+  return FLAMIA_OK;
 }
 
 flamia_status_t flamia_clear_device_status(void* ws, cudaStream_t stream) {

@@ -15,11 +15,9 @@ constexpr float kLog2_448 = 8.807354922057604f;  // log2(448), E4M3 max
 
 // y = acc * (rowc * kf) + vf with rowc = softmax_scale * log2(e) * 2^eQ(i),
 // kf = 2^eK(j), vf = eV(j): the base-2 logit with the V fold.  rowc * kf is
-// exact (a power-of-two scaling); the two remaining ops are rounded once
-// each, never contracted into an FMA, so every kernel gets the same bits.
-__device__ __forceinline__ float score_to_y(float acc, float rowc, float kf, float vf) {
-  return __fadd_rn(__fmul_rn(acc, __fmul_rn(rowc, kf)), vf);
-}
+// exact (a power-of-two scaling); the fused multiply-add rounds once.  Every
+// kernel evaluates it through phat_block_logits, so all get the same bits.
+__device__ __forceinline__ float score_to_y(float acc, float scale, float vf) { return __fmaf_rn(acc, scale, vf); }
 
 // Visibility of doc-local key j for doc-local query i (document length len).
 __device__ __forceinline__ bool visible(int i, int j, int len, int causal) {
@@ -30,10 +28,35 @@ __device__ __forceinline__ bool visible(int i, int j, int len, int causal) {
 // smallest e with 2^M <= 448 * 2^e, i.e. ceil(M - log2 448).  No clamp.
 __device__ __forceinline__ int phat_block_exp(float M) { return (int)ceilf(__fsub_rn(M, kLog2_448)); }
 
+constexpr int kEmptyBlock = -(1 << 30);
+
+// Logits of one 32-key block of one query row, in place (a: S accumulator in,
+// y out; masked keys -> -inf), and the block's P^ exponent (kEmptyBlock when
+// every key is masked).  `kf`, `vf` point at the block's 32 per-key factors.
+// In the default option 2^eK is constant over the block (document-local
+// 32-token blocks), so one scale serves all 32 keys; the exact option has a
+// per-key scale.  The value of every visible y is the same either way.
+// Only the tile on the diagonal (and a document's last, partial tile) needs
+// the mask: `need_mask` is false on the tiles every key of which is visible.
+template <bool EXACT>
+__device__ __forceinline__ int phat_block_logits(float (&a)[32], float rowc, const float* kf, const float* vf,
+                                                 bool need_mask, int i_loc, int key, int len, int causal) {
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  const float sb = __fmul_rn(rowc, kf[0]);
+#pragma unroll
+  for (int jj = 0; jj < 32; ++jj) {
+    const float sc = EXACT ? __fmul_rn(rowc, kf[jj]) : sb;
+    float y = score_to_y(a[jj], sc, vf[jj]);
+    if (need_mask && !visible(i_loc, key + jj, len, causal)) y = -INFINITY;
+    a[jj] = y;
+    m4[jj & 3] = fmaxf(m4[jj & 3], y);
+  }
+  const float M = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+  return (M == -INFINITY) ? kEmptyBlock : phat_block_exp(M);
+}
+
 // p = 2^(y - E) (<= 448 up to the approximation of ex2; the cvt saturates).
 __device__ __forceinline__ float phat_value(float y, int E) { return ex2_approx(__fsub_rn(y, (float)E)); }
-
-constexpr int kEmptyBlock = -(1 << 30);
 
 // x * 2^e for any integer e (exact while the result stays normal).
 __device__ __forceinline__ float ldexp_f(float x, int e) {

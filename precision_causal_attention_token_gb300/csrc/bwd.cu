@@ -84,26 +84,25 @@ __device__ __forceinline__ float warp_max(float v) {
 __device__ __forceinline__ uint32_t sf_byte(int e) { return (uint32_t)min(max(e + 127, 0), 254); }
 
 // Recompute this thread's P^ codes for one 128-key tile from S in TMEM, with
-// the forward's arithmetic (score_to_y, visible, phat_block_exp, phat_value):
-// the same inputs give the same codes and block exponents.
+// the forward's arithmetic (phat_block_logits, phat_value): the same inputs
+// give the same codes and block exponents.  Rows outside the document give
+// empty blocks.
+template <bool EXACT>
 __device__ __forceinline__ void recompute_phat(uint32_t t_s, float rowc, const float* kf, const float* vf, int i_loc,
-                                               int key0, int len, int causal, bool row_ok, uint32_t (&pcode)[32],
-                                               int (&Eb)[4]) {
+                                               int key0, int len, int causal, bool need_mask, bool row_ok,
+                                               uint32_t (&pcode)[32], int (&Eb)[4]) {
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
-    uint32_t rr[32];
-    tmem_ld32(t_s + 32 * b, rr);
-    tmem_ld_wait();
     float yv[32];
-    float M = -INFINITY;
+    {
+      uint32_t rr[32];
+      tmem_ld32(t_s + 32 * b, rr);
+      tmem_ld_wait();
 #pragma unroll
-    for (int jj = 0; jj < 32; ++jj) {
-      const int j = 32 * b + jj;
-      yv[jj] = (row_ok && visible(i_loc, key0 + j, len, causal)) ? score_to_y(__uint_as_float(rr[jj]), rowc, kf[j], vf[j])
-                                                                 : -INFINITY;
-      M = fmaxf(M, yv[jj]);
+      for (int jj = 0; jj < 32; ++jj) yv[jj] = __uint_as_float(rr[jj]);
     }
-    Eb[b] = (M == -INFINITY) ? kEmptyBlock : phat_block_exp(M);
+    Eb[b] = phat_block_logits<EXACT>(yv, rowc, kf + 32 * b, vf + 32 * b, need_mask, i_loc, key0 + 32 * b, len, causal);
+    if (!row_ok) Eb[b] = kEmptyBlock;
 #pragma unroll
     for (int q4 = 0; q4 < 8; ++q4) {
       float pv[4];
@@ -403,8 +402,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
           uint32_t pcode[32];
           int Eb[4];
-          recompute_phat(taddr(tb, warp * 32, kColX0), rv.rowc, c.kf, c.vf, i_loc, key0, len, p.causal, row_ok, pcode,
-                         Eb);
+          // the diagonal tile (and a document's last key tile) needs the mask
+          const bool need_mask = p.causal ? (qt == it.y) : (it.y == n_t - 1);
+          recompute_phat<EXACT>(taddr(tb, warp * 32, kColX0), rv.rowc, c.kf, c.vf, i_loc, key0, len, p.causal, need_mask,
+                                row_ok, pcode, Eb);
+          if (row_ok) dbg_dump_phat(hdr, p.T, h, ds + i_loc, ds + key0, pcode, Eb);
           if (!(ok = mbar_wait(&c.dp_full, ii & 1, abort_flag, hdr, 0x323))) break;
           // the previous iteration's MMAs must be done with the P~ / dS tiles
           if (ii > 0 && !(ok = mbar_wait(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x326))) break;
@@ -699,8 +701,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         uint32_t pcode[32];
         int Eb[4];
-        recompute_phat(taddr(tb, warp * 32, kDqColX0), rv.rowc, c.kf[st], c.vf[st], i_loc, kTile * kt, len, p.causal,
-                       row_ok, pcode, Eb);
+        recompute_phat<EXACT>(taddr(tb, warp * 32, kDqColX0), rv.rowc, c.kf[st], c.vf[st], i_loc, kTile * kt, len,
+                              p.causal, kt == n_kt - 1, row_ok, pcode, Eb);
         if (!(ok = mbar_wait(&c.dp_full, ii & 1, abort_flag, hdr, 0x423))) break;
         if (ii > 0 && !(ok = mbar_wait(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x424))) break;
         tc_fence_after();

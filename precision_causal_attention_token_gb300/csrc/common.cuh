@@ -22,9 +22,27 @@ struct WsHeader {
   uint32_t fwd_counter;    // persistent-grid work counters (reset per launch)
   uint32_t bwd_counter;
   uint32_t dq_counter;
-  uint32_t pad[57];
+  uint32_t pad0;
+  uint8_t* dbg_phat;       // test hook: P^ codes [H][T][T] (null: off)
+  int32_t* dbg_eb;         // test hook: P^ block exponents [H][T][T] at each block's first key
+  uint32_t pad[52];
 };
 static_assert(sizeof(WsHeader) == 256, "header");
+
+// Test hook: record one row's P^ codes and block exponents for a 128-key tile.
+__device__ __forceinline__ void dbg_dump_phat(const WsHeader* hdr, int T, int h, int tok, int key_tok0,
+                                              const uint32_t (&codes)[32], const int (&Eb)[4]) {
+  uint8_t* dc = hdr->dbg_phat;
+  if (dc == nullptr) return;
+  int32_t* de = hdr->dbg_eb;
+  const size_t row = ((size_t)h * T + tok) * (size_t)T;
+#pragma unroll
+  for (int j = 0; j < 128; ++j)
+    if (key_tok0 + j < T) dc[row + key_tok0 + j] = (uint8_t)(codes[j >> 2] >> (8 * (j & 3)));
+#pragma unroll
+  for (int b = 0; b < 4; ++b)
+    if (key_tok0 + 32 * b < T) de[row + key_tok0 + 32 * b] = Eb[b];
+}
 
 struct WsLayout {
   size_t header, tile_prefix, blk32_prefix, fwd_items, bwd_items, keys_a, keys_b, dq_acc, total;

@@ -62,7 +62,7 @@ __device__ __forceinline__ uint64_t desc_mnmajor(const uint8_t* tile, uint32_t b
   return smem_desc(smem_u32(tile) + byte_off, 8 * row_bytes, 8 * row_bytes, row_bytes == 128 ? kSwz128 : kSwz64);
 }
 
-template <int HD, bool OUT_BF16>
+template <int HD, bool OUT_BF16, bool EXACT>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                const __grid_constant__ CUtensorMap map_v) {
@@ -239,62 +239,53 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (!(ok = mbar_wait(&c.k_full[st], kph, abort_flag, hdr, 0x221))) break;
         if (!(ok = mbar_wait(&c.s_full[sb], sph, abort_flag, hdr, 0x222))) break;
         tc_fence_after();
-        float acc[128];
-        {
-          uint32_t rr[32];
+        const int key0 = kTile * kt;
+        const bool need_mask = (kt == n_kt - 1);  // diagonal tile, or a document's last tile
+        int Eb[4];
+        float lb[4];
+        uint32_t codes[32];
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
+        for (int b = 0; b < 4; ++b) {
+          float a[32];
+          {
+            uint32_t rr[32];
             tmem_ld32(taddr(tb, warp * 32, (sb ? kColS1 : kColS0) + 32 * b), rr);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[32 * b + j] = __uint_as_float(rr[j]);
+            for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(rr[j]);
           }
-        }
-        tc_fence_before();
-        mbar_arrive(&c.s_free[sb]);
-        const int key0 = kTile * kt;
-        int Eb[4];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          float M = -INFINITY;
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int j = 32 * b + jj;
-            const float y = visible(i_loc, key0 + j, len, p.causal)
-                                ? score_to_y(acc[j], rowc, c.kf[st][j], c.vf[st][j])
-                                : -INFINITY;
-            acc[j] = y;
-            M = fmaxf(M, y);
-          }
-          Eb[b] = (M == -INFINITY) ? kEmptyBlock : phat_block_exp(M);
-        }
-        const int Emax = max(max(Eb[0], Eb[1]), max(Eb[2], Eb[3]));
-        int m_new = m_ref;
-        if (Emax != kEmptyBlock && (m_ref == kEmptyBlock || Emax > m_ref + 8)) m_new = Emax;
-        uint32_t codes[32];
-        float lsum = 0.f;
-        uint32_t word = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          float lb = 0.f;
+          Eb[b] = phat_block_logits<EXACT>(a, rowc, c.kf[st] + 32 * b, c.vf[st] + 32 * b, need_mask, i_loc,
+                                           key0 + 32 * b, len, p.causal);
+          float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
             float pv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int j = 32 * b + 4 * q4 + e;
-              pv[e] = (Eb[b] == kEmptyBlock) ? 0.f : phat_value(acc[j], Eb[b]);
-              lb = fmaf(pv[e], c.vinv[st][j], lb);
+              pv[e] = (Eb[b] == kEmptyBlock) ? 0.f : phat_value(a[4 * q4 + e], Eb[b]);
+              l4[e] = fmaf(pv[e], c.vinv[st][32 * b + 4 * q4 + e], l4[e]);
             }
             codes[8 * b + q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
           }
+          lb[b] = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        }
+        tc_fence_before();
+        mbar_arrive(&c.s_free[sb]);
+        const int Emax = max(max(Eb[0], Eb[1]), max(Eb[2], Eb[3]));
+        int m_new = m_ref;
+        if (Emax != kEmptyBlock && (m_ref == kEmptyBlock || Emax > m_ref + 8)) m_new = Emax;
+        float lsum = 0.f;
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
           if (Eb[b] != kEmptyBlock) {
-            lsum += ldexp_f(lb, Eb[b] - m_new);
+            lsum += ldexp_f(lb[b], Eb[b] - m_new);
             const int byte = min(max(Eb[b] - m_new + 127, 0), 254);
             word |= (uint32_t)byte << (8 * b);
           }
         }
         mbar_arrive(&c.k_empty[st]);
+        if (row_ok) dbg_dump_phat(hdr, p.T, h, q0 + r, ds + key0, codes, Eb);
         l_run = (m_ref == kEmptyBlock) ? lsum : ldexp_f(l_run, m_ref - m_new) + lsum;
         if (kt > 0 && m_new != m_ref) {
           // rescale the O accumulator row once the previous P^V has landed
@@ -387,24 +378,30 @@ static int num_sms() {
   return n;
 }
 
-template <int HD, bool OB>
+template <int HD, bool OB, bool EX>
 static cudaError_t launch_fwd_t(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
   const size_t smem = fwd_smem_bytes<HD>();
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<HD, OB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(fwd_kernel<HD, OB, EX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   long work = (long)p.max_items * p.H;
   int grid = (int)(work < num_sms() ? work : num_sms());
-  fwd_kernel<HD, OB><<<grid, kFwdThreads, smem, st>>>(p, m.q, m.k, m.v);
+  fwd_kernel<HD, OB, EX><<<grid, kFwdThreads, smem, st>>>(p, m.q, m.k, m.v);
   return cudaGetLastError();
 }
 
+template <int HD, bool OB>
+static cudaError_t launch_fwd_e(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
+  return p.exact ? launch_fwd_t<HD, OB, true>(p, m, st) : launch_fwd_t<HD, OB, false>(p, m, st);
+}
+
 cudaError_t launch_fwd(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
-  if (p.d == 128) return p.out_bf16 ? launch_fwd_t<128, true>(p, m, st) : launch_fwd_t<128, false>(p, m, st);
-  return p.out_bf16 ? launch_fwd_t<64, true>(p, m, st) : launch_fwd_t<64, false>(p, m, st);
+  if (p.d == 128) return p.out_bf16 ? launch_fwd_e<128, true>(p, m, st) : launch_fwd_e<128, false>(p, m, st);
+  return p.out_bf16 ? launch_fwd_e<64, true>(p, m, st) : launch_fwd_e<64, false>(p, m, st);
 }
 
 int sm_count() { return num_sms(); }

@@ -29,6 +29,10 @@ __global__ void __launch_bounds__(1024) plan_prefix_kernel(const int32_t* __rest
     hdr->fwd_counter = 0;
     hdr->bwd_counter = 0;
     hdr->dq_counter = 0;
+    hdr->status = 0;         // the status word covers one call, plan through backward
+    hdr->status_where = 0;
+    hdr->dbg_phat = nullptr;  // test hooks off unless set after the plan
+    hdr->dbg_eb = nullptr;
   }
   __syncthreads();
   for (int base = 0; base < n_seq; base += 1024) {

@@ -9,7 +9,7 @@ import torch
 import oracle
 import precision_causal_attention_token_gb300 as fl
 import synth
-from gpu_helpers import compare, cosine, np_of, run_gpu, run_oracle
+from gpu_helpers import compare, cosine, np_of, run_gpu, run_oracle, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -87,3 +87,89 @@ def test_full_size_sampled_against_oracle(wl, doc, head):
     ref = oracle.train_call(sl(q), sl(k), sl(v), sl(do), np.array([0, e - s], np.int32), out_dtype="bf16")
     for name in ("O", "dQ", "dK", "dV"):
         compare(f"{name} doc {doc} head {head}", getattr(tc, name)[s:e, head:head + 1], ref[name])
+
+
+def _dump_buffers(w):
+    codes = torch.zeros(w.H, w.T, w.T, dtype=torch.uint8, device="cuda")
+    exps = torch.full((w.H, w.T, w.T), -7777, dtype=torch.int32, device="cuda")
+    return codes, exps
+
+
+def test_forward_and_backward_phat_bit_identical():
+    """The backward rebuilds the forward's P^ codes and block exponents bit for bit."""
+    for kw, w in (({}, synth.custom([300, 129, 64], H=2, d=128, seed=701)),
+                  ({"causal": False}, synth.custom([200, 70], H=2, Hkv=1, d=128, seed=702)),
+                  ({"exact": True}, synth.custom([257], H=1, d=128, seed=703))):
+        q, k, v, do = (to_dev(w.tensor(n), w.dtype) for n in ("q", "k", "v", "do"))
+        cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device="cuda")
+        tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu, **kw)
+        tc.plan()
+        cf, ef = _dump_buffers(w)
+        fl.flamia_debug_set_phat_dump(tc.ws, cf, ef)
+        tc.forward(q, k, v)
+        cb, eb = _dump_buffers(w)
+        fl.flamia_debug_set_phat_dump(tc.ws, cb, eb)
+        tc.backward(do)
+        fl.flamia_debug_set_phat_dump(tc.ws, None, None)
+        torch.cuda.synchronize()
+        assert (ef != -7777).sum().item() > 0
+        assert torch.equal(ef, eb), kw
+        assert torch.equal(cf, cb), kw
+        assert (cf != 0).float().mean().item() > 0.01
+
+
+def _perturb_future(x, half, seed):
+    y = x.copy()
+    rng = np.random.default_rng(seed)
+    y[half + 1:] = rng.standard_normal(y[half + 1:].shape).astype(np.float32)
+    y[half + 1:half + 4] *= 1000.0
+    return synth.round_to_bf16(y)
+
+
+def _probe(w, exact):
+    L = w.seqlens[0]
+    half = L // 2
+    base = [w.tensor(n) for n in ("q", "k", "v", "do")]
+    pert = []
+    for i, x in enumerate(base):
+        y = x.copy()
+        for d in range(len(w.seqlens)):
+            s = d * L
+            y[s:s + L] = _perturb_future(x[s:s + L], half, 100 * d + i)
+        pert.append(y)
+    a = run_gpu(w, exact=exact, inputs=base)
+    oa, qa = np_of(a.O), np_of(a.dQ)
+    b = run_gpu(w, exact=exact, inputs=pert)
+    ob, qb = np_of(b.O), np_of(b.dQ)
+    early = np.concatenate([np.arange(d * L, d * L + half + 1) for d in range(len(w.seqlens))])
+    late = np.concatenate([np.arange(d * L + half + 1, (d + 1) * L) for d in range(len(w.seqlens))])
+    rel = lambda x, y: float(np.abs(x - y).max() / max(np.abs(x).max(), 1e-30))
+    return (rel(oa[early], ob[early]), rel(qa[early], qb[early]), np.array_equal(oa[early], ob[early]),
+            np.array_equal(qa[early], qb[early]), rel(oa[late], ob[late]))
+
+
+@pytest.mark.parametrize("full", [False, True])
+def test_leakage_probe_exact_option_gpu(full):
+    """Exact option: perturbing tokens past L/2 (raising their scale-group max)
+    leaves O and dQ of rows <= L/2 bit-identical (the pages' probe reads 0/0)."""
+    w = synth.workload(2) if full else synth.custom([1024, 1024], H=2, d=128, seed=705)
+    o_rel, q_rel, o_same, q_same, late = _probe(w, exact=True)
+    assert o_same and q_same, (o_rel, q_rel)
+    assert late > 0
+
+
+def test_leakage_probe_default_option_residue():
+    """Default token-block scales keep a within-block residue (nonzero, small)."""
+    w = synth.custom([1024, 1024], H=2, d=128, seed=706)
+    o_rel, q_rel, o_same, q_same, _ = _probe(w, exact=False)
+    assert not o_same and o_rel > 0
+
+
+def test_deterministic_dq_is_reproducible():
+    w = synth.custom([700, 300], H=2, Hkv=1, d=128, seed=707)
+    a = run_gpu(w, deterministic=True)
+    b = run_gpu(w, deterministic=True)
+    assert torch.equal(a.dQ, b.dQ) and torch.equal(a.dK, b.dK) and torch.equal(a.dV, b.dV)
+    ref = run_oracle(w)
+    for name in ("O", "dQ", "dK", "dV"):
+        compare(name, getattr(a, name), ref[name])
