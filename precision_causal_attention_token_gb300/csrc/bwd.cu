@@ -53,7 +53,7 @@ struct BwdCtl {
   int ekb[4];          // eK of each 32-key block (default option)
   uint32_t xch[2][2][4];  // [parity][dV, dK][query block]: 4 scale bytes (one per key block)
   uint64_t kv_full, kv_empty, qd_full[2], qd_empty[2];
-  uint64_t s_full, dp_full, ds_full, mm_done, x1_free, acc_full, acc_free;
+  uint64_t s_full, dp_full, ds_full, mm_done, x1_free, acc_full, acc_free, xch_bar;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -263,6 +263,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&c.x1_free, 128);
     mbar_init(&c.acc_full, 1);
     mbar_init(&c.acc_free, 128);
+    mbar_init(&c.xch_bar, 128);
     c.abort_flag = 0;
     fence_mbar_init();
   }
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
       const int k0 = ds + kTile * it.y;
       const int n_t = (len + kTile - 1) / kTile, q_first = p.causal ? it.y : 0;
-      if (!(ok = mbar_wait(&c.kv_empty, (ic & 1) ^ 1, abort_flag, hdr, 0x301))) break;
+      if (!(ok = mbar_wait_warp(&c.kv_empty, (ic & 1) ^ 1, abort_flag, hdr, 0x301))) break;
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
         const int j = lane * 4 + jj, key = kTile * it.y + j;
@@ -313,7 +314,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int h = hk * G + g;
         for (int qt = q_first; qt < n_t; ++qt, ++ii) {
           const int qs = ii & 1;
-          if (!(ok = mbar_wait(&c.qd_empty[qs], ((ii >> 1) & 1) ^ 1, abort_flag, hdr, 0x302))) break;
+          if (!(ok = mbar_wait_warp(&c.qd_empty[qs], ((ii >> 1) & 1) ^ 1, abort_flag, hdr, 0x302))) break;
           if (lane == 0) {
             mbar_arrive_expect_tx(&c.qd_full[qs], 2 * kTile * HD);
             tma_load_3d(tl.q[qs], &map_q, &c.qd_full[qs], 0, h, ds + kTile * qt);
@@ -390,7 +391,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int2 it = p.bwd_items[pair];
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
       const int n_t = (len + kTile - 1) / kTile, q_first = p.causal ? it.y : 0;
-      if (!(ok = mbar_wait(&c.kv_full, ic & 1, abort_flag, hdr, 0x321))) break;
+      if (!(ok = mbar_wait_warp(&c.kv_full, ic & 1, abort_flag, hdr, 0x321))) break;
       const int key0 = kTile * it.y;
       for (int g = 0; ok && g < G; ++g) {
         const int h = hk * G + g;
@@ -398,7 +399,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int i_loc = kTile * qt + r;
           const bool row_ok = i_loc < len;
           const RowVals rv = load_row(p, h, ds + i_loc, row_ok);
-          if (!(ok = mbar_wait(&c.s_full, ii & 1, abort_flag, hdr, 0x322))) break;
+          if (!(ok = mbar_wait_warp(&c.s_full, ii & 1, abort_flag, hdr, 0x322))) break;
           tc_fence_after();
           uint32_t pcode[32];
           int Eb[4];
@@ -407,9 +408,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           recompute_phat<EXACT>(taddr(tb, warp * 32, kColX0), rv.rowc, c.kf, c.vf, i_loc, key0, len, p.causal, need_mask,
                                 row_ok, pcode, Eb);
           if (row_ok) dbg_dump_phat(hdr, p.T, h, ds + i_loc, ds + key0, pcode, Eb);
-          if (!(ok = mbar_wait(&c.dp_full, ii & 1, abort_flag, hdr, 0x323))) break;
+          if (!(ok = mbar_wait_warp(&c.dp_full, ii & 1, abort_flag, hdr, 0x323))) break;
           // the previous iteration's MMAs must be done with the P~ / dS tiles
-          if (ii > 0 && !(ok = mbar_wait(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x326))) break;
+          if (ii > 0 && !(ok = mbar_wait_warp(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x326))) break;
           tc_fence_after();
           const float inv_l = 1.0f / rv.li;
           uint32_t word_dq = 0;
@@ -458,7 +459,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           // scale-factor words: dV / dK rows are keys (key block = this warp),
           // one byte per query block; dQ rows are queries (this thread's row)
-          named_bar_sync(1, 128);
+          // exchange the block exponents among the four compute warps
+          // (an mbarrier with a bounded wait, so an aborting warp cannot strand the others)
+          mbar_arrive(&c.xch_bar);
+          if (!(ok = mbar_wait_warp(&c.xch_bar, ii & 1, abort_flag, hdr, 0x327))) break;
           uint32_t wdv = 0, wdk = 0;
 #pragma unroll
           for (int qb = 0; qb < 4; ++qb) {
@@ -475,7 +479,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mbar_arrive(&c.ds_full);
           if constexpr (DQ) {
             // ---- dQ tile -> fp32 buffer
-            if (!(ok = mbar_wait(&c.mm_done, ii & 1, abort_flag, hdr, 0x324))) break;
+            if (!(ok = mbar_wait_warp(&c.mm_done, ii & 1, abort_flag, hdr, 0x324))) break;
             tc_fence_after();
             float* dst = p.dq_acc + ((size_t)(ds + i_loc) * p.H + h) * HD;
 #pragma unroll
@@ -499,7 +503,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       mbar_arrive(&c.kv_empty);  // key vectors no longer read
       // ---- dK, dV of this key tile (TMEM lane = key)
-      if (!(ok = mbar_wait(&c.acc_full, ic & 1, abort_flag, hdr, 0x325))) break;
+      if (!(ok = mbar_wait_warp(&c.acc_full, ic & 1, abort_flag, hdr, 0x325))) break;
       tc_fence_after();
       const int j_loc = key0 + r;
       const bool key_ok = j_loc < len;
@@ -604,7 +608,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int2 it = p.fwd_items[pair];
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
       const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
-      if (!(ok = mbar_wait(&c.qd_empty, (ic & 1) ^ 1, abort_flag, hdr, 0x401))) break;
+      if (!(ok = mbar_wait_warp(&c.qd_empty, (ic & 1) ^ 1, abort_flag, hdr, 0x401))) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&c.qd_full, 2 * kTile * HD);
         tma_load_3d(tl.q, &map_q, &c.qd_full, 0, h, ds + kTile * it.y);
@@ -613,7 +617,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int kt = 0; kt < n_kt; ++kt, ++kv) {
         const int st = kv % kDqStages;
         const uint32_t ph = (kv / kDqStages) & 1;
-        if (!(ok = mbar_wait(&c.kv_empty[st], ph ^ 1, abort_flag, hdr, 0x402))) break;
+        if (!(ok = mbar_wait_warp(&c.kv_empty[st], ph ^ 1, abort_flag, hdr, 0x402))) break;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           const int j = lane * 4 + jj, key = kTile * kt + j;
@@ -696,15 +700,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int kt = 0; ok && kt < n_kt; ++kt, ++kv, ++ii) {
         const int st = kv % kDqStages;
         const uint32_t ph = (kv / kDqStages) & 1;
-        if (!(ok = mbar_wait(&c.kv_full[st], ph, abort_flag, hdr, 0x421))) break;
-        if (!(ok = mbar_wait(&c.s_full, ii & 1, abort_flag, hdr, 0x422))) break;
+        if (!(ok = mbar_wait_warp(&c.kv_full[st], ph, abort_flag, hdr, 0x421))) break;
+        if (!(ok = mbar_wait_warp(&c.s_full, ii & 1, abort_flag, hdr, 0x422))) break;
         tc_fence_after();
         uint32_t pcode[32];
         int Eb[4];
         recompute_phat<EXACT>(taddr(tb, warp * 32, kDqColX0), rv.rowc, c.kf[st], c.vf[st], i_loc, kTile * kt, len,
                               p.causal, kt == n_kt - 1, row_ok, pcode, Eb);
-        if (!(ok = mbar_wait(&c.dp_full, ii & 1, abort_flag, hdr, 0x423))) break;
-        if (ii > 0 && !(ok = mbar_wait(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x424))) break;
+        if (!(ok = mbar_wait_warp(&c.dp_full, ii & 1, abort_flag, hdr, 0x423))) break;
+        if (ii > 0 && !(ok = mbar_wait_warp(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x424))) break;
         tc_fence_after();
         uint32_t word_dq = 0;
 #pragma unroll
@@ -729,7 +733,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(&c.kv_empty[st]);
       }
       if (!ok) break;
-      if (!(ok = mbar_wait(&c.dq_full, ic & 1, abort_flag, hdr, 0x425))) break;
+      if (!(ok = mbar_wait_warp(&c.dq_full, ic & 1, abort_flag, hdr, 0x425))) break;
       tc_fence_after();
       const size_t off = ((size_t)(ds + i_loc) * p.H + h) * HD;
 #pragma unroll

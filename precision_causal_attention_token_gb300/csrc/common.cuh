@@ -190,6 +190,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Warp-uniform bounded wait: every lane polls, and the warp continues only if
+// every lane saw the phase complete.  Warps that go on to warp-collective
+// instructions (tcgen05.ld/st are .sync.aligned) use this form, so a timeout
+// can never leave part of a warp behind.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                               WsHeader* hdr, uint32_t where) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, hdr, where);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // After an abort, give TMA copies already issued by this CTA time to land
 // before the CTA exits (bounded: about 50 microseconds).
 __device__ __forceinline__ void drain_after_abort(volatile int* abort_flag) {

@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
       const int q0 = ds + kTile * it.y;
       const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
-      if (!(ok = mbar_wait(&c.q_empty, (qc & 1) ^ 1, abort_flag, hdr, 0x201))) break;
+      if (!(ok = mbar_wait_warp(&c.q_empty, (qc & 1) ^ 1, abort_flag, hdr, 0x201))) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&c.q_full, kTile * HD);
         tma_load_3d(tl.q, &map_q, &c.q_full, 0, h, q0);
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int kt = 0; kt < n_kt; ++kt, ++kv) {
         const int st = kv % kFwdStages;
         const uint32_t ph = (kv / kFwdStages) & 1;
-        if (!(ok = mbar_wait(&c.k_empty[st], ph ^ 1, abort_flag, hdr, 0x202))) break;
+        if (!(ok = mbar_wait_warp(&c.k_empty[st], ph ^ 1, abort_flag, hdr, 0x202))) break;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           const int j = lane * 4 + jj, key = kTile * kt + j;
@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         } else {
           mbar_arrive(&c.k_full[st]);
         }
-        if (!(ok = mbar_wait(&c.v_empty[st], ph ^ 1, abort_flag, hdr, 0x203))) break;
+        if (!(ok = mbar_wait_warp(&c.v_empty[st], ph ^ 1, abort_flag, hdr, 0x203))) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(&c.v_full[st], kTile * HD);
           tma_load_3d(tl.v[st], &map_v, &c.v_full[st], 0, hk, ds + kTile * kt);
@@ -236,8 +236,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int st = kv % kFwdStages;
         const uint32_t kph = (kv / kFwdStages) & 1;
         const uint32_t sb = sc & 1, sph = (sc >> 1) & 1;
-        if (!(ok = mbar_wait(&c.k_full[st], kph, abort_flag, hdr, 0x221))) break;
-        if (!(ok = mbar_wait(&c.s_full[sb], sph, abort_flag, hdr, 0x222))) break;
+        if (!(ok = mbar_wait_warp(&c.k_full[st], kph, abort_flag, hdr, 0x221))) break;
+        if (!(ok = mbar_wait_warp(&c.s_full[sb], sph, abort_flag, hdr, 0x222))) break;
         tc_fence_after();
         const int key0 = kTile * kt;
         const bool need_mask = (kt == n_kt - 1);  // diagonal tile, or a document's last tile
@@ -287,12 +287,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_arrive(&c.k_empty[st]);
         if (row_ok) dbg_dump_phat(hdr, p.T, h, q0 + r, ds + key0, codes, Eb);
         l_run = (m_ref == kEmptyBlock) ? lsum : ldexp_f(l_run, m_ref - m_new) + lsum;
-        if (kt > 0 && m_new != m_ref) {
-          // rescale the O accumulator row once the previous P^V has landed
+        // rescale the O accumulator rows once the previous P^V has landed
+        // (warp-uniform: tcgen05.ld/st are warp-collective; lanes whose
+        // reference did not move scale by 1)
+        if (__any_sync(0xffffffffu, kt > 0 && m_new != m_ref)) {
           const uint32_t pp = pc - 1;
-          if (!(ok = mbar_wait(&c.p_free[pp & 1], (pp >> 1) & 1, abort_flag, hdr, 0x223))) break;
+          if (!(ok = mbar_wait_warp(&c.p_free[pp & 1], (pp >> 1) & 1, abort_flag, hdr, 0x223))) break;
           tc_fence_after();
-          const float f = ldexp_f(1.0f, m_ref - m_new);
+          const float f = (m_new != m_ref) ? ldexp_f(1.0f, m_ref - m_new) : 1.0f;
 #pragma unroll
           for (int cb = 0; cb < HD / 32; ++cb) {
             uint32_t rr[32];
@@ -306,7 +308,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         m_ref = m_new;
         const uint32_t pb = pc & 1;
-        if (!(ok = mbar_wait(&c.p_free[pb], ((pc >> 1) & 1) ^ 1, abort_flag, hdr, 0x224))) break;
+        if (!(ok = mbar_wait_warp(&c.p_free[pb], ((pc >> 1) & 1) ^ 1, abort_flag, hdr, 0x224))) break;
         uint8_t* prow = tl.p[pb];
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
@@ -321,7 +323,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (!ok) break;
       // epilogue: O = acc / l
-      if (!(ok = mbar_wait(&c.o_full, ic & 1, abort_flag, hdr, 0x225))) break;
+      if (!(ok = mbar_wait_warp(&c.o_full, ic & 1, abort_flag, hdr, 0x225))) break;
       tc_fence_after();
       float o[HD];
 #pragma unroll
