@@ -48,25 +48,47 @@ def np_of(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def compare(name, got, want, row_tol=ROW_TOL, cos_tol=COS_TOL, rows=None):
-    """Per-row (last axis) max-error bound and whole-tensor cosine."""
+def compare(name, got, want, row_tol=ROW_TOL, cos_tol=COS_TOL, rows=None, noise=None):
+    """Per-row (last axis) max-error bound and whole-tensor cosine.
+
+    noise: the oracle's own sensitivity of this output to how O is rounded
+    before D = <dO, O> (oracle with O stored in the output dtype minus oracle
+    with O kept in fp64), same shape as `want`.  When given, each row may in
+    addition differ by twice that row's sensitivity, and the cosine bound
+    loosens by twice the sensitivity's cosine deficit.  Both sides round their
+    own O, so where the softmax is nearly one-hot (x20 outlier channels in Q
+    and K) dS = P (dP - D) cancels down to that rounding and no tighter
+    agreement is meaningful.  All of it comes from the oracle."""
     g = np_of(got) if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
     r = np.asarray(want, np.float64)
+    nz = None if noise is None else np.asarray(noise, np.float64)
     if rows is not None:
         g, r = g[rows], r[rows]
+        nz = None if nz is None else nz[rows]
     assert g.shape == r.shape, (name, g.shape, r.shape)
     assert np.isfinite(g).all(), f"{name}: non-finite values"
     rowmax = np.abs(r).max(axis=-1, keepdims=True)
     floor = 1e-6 * max(np.abs(r).max(), 1e-30)
+    allow = row_tol * np.maximum(rowmax, floor)
+    if nz is not None:
+        allow = allow + 2.0 * np.abs(nz).max(axis=-1, keepdims=True)
+        cos_tol = min(cos_tol, 1.0 - 2.0 * (1.0 - cosine(r - nz, r)) - 1e-6) if np.abs(nz).max() > 0 else cos_tol
     err = np.abs(g - r)
-    ratio = err / np.maximum(rowmax, floor)
-    worst = float(ratio.max()) if ratio.size else 0.0
+    worst = float((err / allow).max()) if err.size else 0.0
     gg, rr = g.ravel(), r.ravel()
     denom = np.sqrt((gg @ gg) * (rr @ rr))
     cos = float(gg @ rr / denom) if denom > 0 else 1.0
-    assert worst <= row_tol, f"{name}: max |err| / row max-abs = {worst:.3e} > {row_tol}"
+    assert worst <= 1.0, f"{name}: max |err| exceeds the bound by {worst:.3f}x (row tol {row_tol})"
     assert cos >= cos_tol, f"{name}: cosine {cos:.7f} < {cos_tol}"
     return worst, cos
+
+
+def o_rounding_noise(w, *, causal=True, exact=False, inputs=None):
+    """Oracle-only sensitivity of dQ/dK/dV to rounding O before D."""
+    a = run_oracle(w, causal=causal, exact=exact, inputs=inputs)
+    q, k, v, do = inputs if inputs is not None else (w.tensor(n) for n in ("q", "k", "v", "do"))
+    b = oracle.train_call(q, k, v, do, w.cu_seqlens, causal=causal, exact=exact, out_dtype="f64")
+    return a, {n: a[n] - b[n] for n in ("dQ", "dK", "dV")}
 
 
 def cosine(a, b):

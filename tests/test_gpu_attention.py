@@ -9,15 +9,16 @@ import torch
 import oracle
 import precision_causal_attention_token_gb300 as fl
 import synth
-from gpu_helpers import compare, cosine, np_of, run_gpu, run_oracle, to_dev
+from gpu_helpers import compare, cosine, np_of, o_rounding_noise, run_gpu, run_oracle, to_dev
 
 pytestmark = pytest.mark.gpu
 
 
-def _check_all(w, tc, ref, rows=None):
+def _check_all(w, tc, ref, rows=None, noise=None):
     out = {}
     for name in ("O", "dQ", "dK", "dV"):
-        out[name] = compare(name, getattr(tc, name), ref[name], rows=rows)
+        nz = None if noise is None or name == "O" else noise[name]
+        out[name] = compare(name, getattr(tc, name), ref[name], rows=rows, noise=nz)
     # row statistics: lse2 = m + log2(l) for valid rows
     lse = np_of(tc.m) + np.log2(np_of(tc.l))
     assert np.abs(lse - ref["lse2"]).max() < 1e-3
@@ -39,10 +40,14 @@ SMALL = [
 @pytest.mark.parametrize("name,w,kw", SMALL, ids=[c[0] for c in SMALL])
 def test_parity_small(name, w, kw):
     tc = run_gpu(w, **kw)
-    ref = run_oracle(w, **kw)
+    noise = None
+    if w.outlier_channels:  # near one-hot softmax: allow the oracle's own O-rounding sensitivity
+        ref, noise = o_rounding_noise(w, **kw)
+    else:
+        ref = run_oracle(w, **kw)
     assert (tc.q_codes.cpu().numpy() == ref["q_codes"]).all()
     assert (tc.do_codes.cpu().numpy() == ref["do_codes"]).all()
-    _check_all(w, tc, ref)
+    _check_all(w, tc, ref, noise=noise)
 
 
 def test_cosine_to_unquantized_reference():
@@ -84,9 +89,15 @@ def test_full_size_sampled_against_oracle(wl, doc, head):
         doc = int(np.argsort(lens)[len(lens) // 2])
     s, e = int(w.cu_seqlens[doc]), int(w.cu_seqlens[doc + 1])
     sl = lambda a: np.ascontiguousarray(a[s:e, head:head + 1])
-    ref = oracle.train_call(sl(q), sl(k), sl(v), sl(do), np.array([0, e - s], np.int32), out_dtype="bf16")
+    cu1 = np.array([0, e - s], np.int32)
+    ref = oracle.train_call(sl(q), sl(k), sl(v), sl(do), cu1, out_dtype="bf16")
+    noise = {}
+    if w.outlier_channels:
+        r64 = oracle.train_call(sl(q), sl(k), sl(v), sl(do), cu1, out_dtype="f64")
+        noise = {n: ref[n] - r64[n] for n in ("dQ", "dK", "dV")}
     for name in ("O", "dQ", "dK", "dV"):
-        compare(f"{name} doc {doc} head {head}", getattr(tc, name)[s:e, head:head + 1], ref[name])
+        compare(f"{name} doc {doc} head {head}", getattr(tc, name)[s:e, head:head + 1], ref[name],
+                noise=noise.get(name))
 
 
 def _dump_buffers(w):
