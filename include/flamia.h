@@ -183,6 +183,29 @@ flamia_status_t flamia_clear_device_status(void* ws, cudaStream_t stream);
 flamia_status_t flamia_debug_set_phat_dump(void* ws, size_t ws_bytes, void* codes, int32_t* exps,
                                            cudaStream_t stream);
 
+/* Allocation-free work-list builder (this library's own addition; the
+ * method's pages have no counterpart).  For callers that cannot allocate
+ * device memory: code inside a CUDA graph under capture (cudaMalloc cannot be
+ * captured), embeddings without an allocator, or frameworks that forbid
+ * allocations outside their own caching allocator.  It builds the same two
+ * longest-first work lists as flamia_plan, but its scratch (document
+ * prefix tables, sort keys) lives in a file-scope device array of the library
+ * (about 2.5 MiB, held by every GPU that loads the library until the process
+ * exits) instead of a caller workspace; it calls no allocating routine.
+ *   fwd_items, bwd_items  device int32 pairs (document, 128-token tile),
+ *                         each [ceil(T/128) + n_seq] entries, caller-owned;
+ *                         the first *n_items entries are written.
+ *   n_items               device int32, receives the number of tiles (0 when
+ *                         cu_seqlens is inconsistent with T).
+ * Limits: ceil(T/128) + n_seq <= 65536 and n_seq <= 65536, else
+ * FLAMIA_ERR_UNSUPPORTED.  The first call on each device looks up the array's
+ * device address with that device current (make that first call before any
+ * stream capture).  All calls share the array and it keeps the last call's
+ * contents: calls whose kernels may overlap on the GPU race with each other
+ * and must be serialised by the caller. */
+flamia_status_t flamia_plan_noalloc(const flamia_problem_t* p, int2* fwd_items, int2* bwd_items, int32_t* n_items,
+                                    cudaStream_t stream);
+
 /* Static description of a status code. */
 const char* flamia_status_string(flamia_status_t s);
 

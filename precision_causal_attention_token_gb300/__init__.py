@@ -21,7 +21,7 @@ ROLE_QKV, ROLE_DO = 0, 1
 
 EXPORTED = ("flamia_workspace_size", "flamia_plan", "flamia_quantize", "flamia_fwd", "flamia_bwd",
             "flamia_get_device_status", "flamia_clear_device_status", "flamia_status_string",
-            "flamia_debug_set_phat_dump")
+            "flamia_debug_set_phat_dump", "flamia_plan_noalloc")
 
 
 class FlamiaError(RuntimeError):
@@ -70,6 +70,8 @@ def load_library(path: str = LIB_PATH):
     L.flamia_status_string.restype, L.flamia_status_string.argtypes = ctypes.c_char_p, [i32]
     L.flamia_debug_set_phat_dump.restype = i32
     L.flamia_debug_set_phat_dump.argtypes = [vp, sz, vp, vp, vp]
+    L.flamia_plan_noalloc.restype = i32
+    L.flamia_plan_noalloc.argtypes = [P, vp, vp, vp, vp]
     _lib = L
     return L
 
@@ -133,6 +135,13 @@ def flamia_bwd(prob: Problem, q: Operand, k: Operand, v: Operand, dO: Operand, D
     _check(load_library().flamia_bwd(ctypes.byref(prob), ctypes.byref(q), ctypes.byref(k), ctypes.byref(v),
                                      ctypes.byref(dO), _ptr(D), _ptr(m), _ptr(l), _ptr(dQ), _ptr(dK), _ptr(dV),
                                      _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "flamia_bwd")
+
+
+def flamia_plan_noalloc(prob: Problem, fwd_items, bwd_items, n_items, stream=None):
+    """Work lists without a workspace (library-held scratch; see include/flamia.h).
+    fwd_items/bwd_items: int32 device tensors [ceil(T/128) + n_seq, 2]; n_items: int32 device [1]."""
+    _check(load_library().flamia_plan_noalloc(ctypes.byref(prob), _ptr(fwd_items), _ptr(bwd_items), _ptr(n_items),
+                                              _stream(stream)), "flamia_plan_noalloc")
 
 
 def flamia_get_device_status(ws, stream=None) -> int:

@@ -10,6 +10,8 @@
 // (cost descending, item index ascending), unique, so the order is
 // deterministic.  The pass count depends only on a host-side bound of the item
 // count (ceil(T/128) + n_seq), so the whole plan can be captured in a graph.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace flamia {
@@ -190,3 +192,87 @@ cudaError_t launch_plan(const flamia_problem_t& p, const WsLayout& L, uint8_t* w
 }
 
 }  // namespace flamia
+
+// ===========================================================================
+// Allocation-free work-list builder.
+//
+// For callers that cannot allocate device memory themselves: code running
+// inside a CUDA graph that is being captured (cudaMalloc is not a stream
+// operation and cannot be captured), allocator-less embeddings of the library,
+// or a framework that forbids allocations outside its own caching allocator.
+// flamia_plan_noalloc keeps the planner's scratch (prefix tables, sort keys)
+// in the file-scope array below instead of the caller's workspace, and writes
+// only the two sorted work lists and the item count to caller-owned buffers.
+// Every GPU that loads this library holds the array (about 2.5 MiB) until the
+// process exits.  All calls share it: calls whose kernels overlap on the GPU
+// (different streams, or different threads) race and must be serialised by
+// the caller.
+// ===========================================================================
+namespace flamia {
+namespace {
+
+constexpr int kNoAllocMaxItems = 65536;  // limit on ceil(T/128) + n_seq
+constexpr int kNoAllocMaxSeq = 65536;    // limit on n_seq
+
+struct NoAllocScratch {
+  WsHeader hdr;
+  int32_t tile_prefix[kNoAllocMaxSeq + 1];
+  int32_t blk_prefix[kNoAllocMaxSeq + 1];
+  uint64_t keys_a[2 * kNoAllocMaxItems];
+  uint64_t keys_b[2 * kNoAllocMaxItems];
+};
+
+__device__ __align__(256) NoAllocScratch g_noalloc_scratch;
+
+// Device address of g_noalloc_scratch for the current device, looked up once
+// per device (the host-side symbol is a stand-in, not a device address).
+NoAllocScratch* noalloc_scratch_for_current_device() {
+  static std::mutex mu;
+  static NoAllocScratch* addr[256] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<NoAllocScratch*>(p);
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+}  // namespace flamia
+
+extern "C" flamia_status_t flamia_plan_noalloc(const flamia_problem_t* p, int2* fwd_items, int2* bwd_items,
+                                               int32_t* n_items, cudaStream_t stream) {
+  using namespace flamia;
+  if (flamia_workspace_size(p) == 0) return FLAMIA_ERR_INVALID_ARG;
+  if (!fwd_items || !bwd_items || !n_items) return FLAMIA_ERR_INVALID_ARG;
+  const int max_items = (p->T + 127) / 128 + p->n_seq;
+  if (max_items > kNoAllocMaxItems || p->n_seq > kNoAllocMaxSeq) return FLAMIA_ERR_UNSUPPORTED;
+  NoAllocScratch* sc = noalloc_scratch_for_current_device();
+  if (sc == nullptr) return FLAMIA_ERR_CUDA;
+  const int n = ((max_items + kSortBlock - 1) / kSortBlock) * kSortBlock;
+  // every scratch word a kernel reads is written earlier in this sequence
+  // (the prefix kernel writes the header and both tables, the key kernel all
+  // 2n keys), so nothing needs clearing between calls
+  plan_prefix_kernel<<<1, 1024, 0, stream>>>(p->cu_seqlens, p->n_seq, p->T, sc->tile_prefix, sc->blk_prefix,
+                                            &sc->hdr);
+  plan_keys_kernel<<<(n + 255) / 256, 256, 0, stream>>>(sc->tile_prefix, p->n_seq, p->causal, n, &sc->hdr,
+                                                        sc->keys_a);
+  block_sort_kernel<<<2 * n / kSortBlock, 1024, 0, stream>>>(sc->keys_a);
+  uint64_t *src = sc->keys_a, *dst = sc->keys_b;
+  for (int w = kSortBlock; w < n; w *= 2) {
+    merge_pass_kernel<<<(2 * n + 255) / 256, 256, 0, stream>>>(src, dst, n, w);
+    uint64_t* t = src;
+    src = dst;
+    dst = t;
+  }
+  plan_items_kernel<<<(2 * n + 255) / 256, 256, 0, stream>>>(src, sc->tile_prefix, p->n_seq, n, &sc->hdr,
+                                                             fwd_items, bwd_items);
+  if (cudaMemcpyAsync(n_items, &sc->hdr.n_items, sizeof(int32_t), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+    return FLAMIA_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+}
+
