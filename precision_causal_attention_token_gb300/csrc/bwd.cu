@@ -31,7 +31,11 @@
 
 namespace flamia {
 
-constexpr int kBwdThreads = 192;
+// Compute warps 0-7 (two per TMEM lane quarter: warp w owns query rows
+// 32(w%4)..+31 and key blocks 2(w/4), 2(w/4)+1), producer warp 8, MMA warp 9.
+constexpr int kBwdCompute = 256;
+constexpr int kBwdThreads = kBwdCompute + 64;
+constexpr int kWarpProd = 8, kWarpMma = 9;
 constexpr uint32_t kColDV = 0, kColDK = 128, kColX0 = 256, kColX1 = 384;
 constexpr uint32_t kColSfDV = kColX0 + 0, kColSfDK = kColX0 + 4, kColSfDQ = kColX0 + 8, kColSfOne = kColX0 + 12;
 
@@ -46,12 +50,21 @@ struct __align__(1024) BwdTiles {
   uint8_t dsk[kTile * kTile];  // exact option: dK payload
 };
 
+// Per-row values of one query tile, staged in shared memory by the producer
+// next to the tile's Q / dO codes (off the compute warps' critical path).
+struct RowStage {
+  float rowc, hdo, inv_l, Di;
+  int mi, eq;
+};
+
 struct BwdCtl {
+  RowStage rows[2][kTile];  // [Q/dO stage][query row]
   float kf[kTile];     // 2^eK(j)
   float vf[kTile];     // eV(j)
   float vinv[kTile];   // 2^-eV(j)
   int ekb[4];          // eK of each 32-key block (default option)
-  uint32_t xch[2][2][4];  // [parity][dV, dK][query block]: 4 scale bytes (one per key block)
+  uint8_t xch[2][2][4][4];   // [parity][dV, dK][query block][key block] scale bytes
+  uint8_t xdq[2][kTile][4];  // [parity][query row][key block] dQ scale bytes
   uint64_t kv_full, kv_empty, qd_full[2], qd_empty[2];
   uint64_t s_full, dp_full, ds_full, mm_done, x1_free, acc_full, acc_free, xch_bar;
   uint32_t tmem_base;
@@ -87,12 +100,13 @@ __device__ __forceinline__ uint32_t sf_byte(int e) { return (uint32_t)min(max(e 
 // the forward's arithmetic (phat_block_logits, phat_value): the same inputs
 // give the same codes and block exponents.  Rows outside the document give
 // empty blocks.
-template <bool EXACT>
-__device__ __forceinline__ void recompute_phat(uint32_t t_s, float rowc, const float* kf, const float* vf, int i_loc,
-                                               int key0, int len, int causal, bool need_mask, bool row_ok,
-                                               uint32_t (&pcode)[32], int (&Eb)[4]) {
+template <bool EXACT, int NB>
+__device__ __forceinline__ void recompute_phat(uint32_t t_s, int b0, float rowc, const float* kf, const float* vf,
+                                               int i_loc, int key0, int len, int causal, bool need_mask, bool row_ok,
+                                               uint32_t (&pcode)[8 * NB], int (&Eb)[NB]) {
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
+  for (int bb = 0; bb < NB; ++bb) {
+    const int b = b0 + bb;
     float yv[32];
     {
       uint32_t rr[32];
@@ -101,14 +115,14 @@ __device__ __forceinline__ void recompute_phat(uint32_t t_s, float rowc, const f
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) yv[jj] = __uint_as_float(rr[jj]);
     }
-    Eb[b] = phat_block_logits<EXACT>(yv, rowc, kf + 32 * b, vf + 32 * b, need_mask, i_loc, key0 + 32 * b, len, causal);
-    if (!row_ok) Eb[b] = kEmptyBlock;
+    Eb[bb] = phat_block_logits<EXACT>(yv, rowc, kf + 32 * b, vf + 32 * b, need_mask, i_loc, key0 + 32 * b, len, causal);
+    if (!row_ok) Eb[bb] = kEmptyBlock;
 #pragma unroll
     for (int q4 = 0; q4 < 8; ++q4) {
       float pv[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) pv[e] = (Eb[b] == kEmptyBlock) ? 0.f : phat_value(yv[4 * q4 + e], Eb[b]);
-      pcode[8 * b + q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
+      for (int e = 0; e < 4; ++e) pv[e] = (Eb[bb] == kEmptyBlock) ? 0.f : phat_value(yv[4 * q4 + e], Eb[bb]);
+      pcode[8 * bb + q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
     }
   }
 }
@@ -251,24 +265,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (tid == 0) {
     mbar_init(&c.kv_full, 32);
-    mbar_init(&c.kv_empty, 1 + 128);
+    mbar_init(&c.kv_empty, 1 + kBwdCompute);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&c.qd_full[s], 1);
+      mbar_init(&c.qd_full[s], 32);
       mbar_init(&c.qd_empty[s], 1);
     }
     mbar_init(&c.s_full, 1);
     mbar_init(&c.dp_full, 1);
-    mbar_init(&c.ds_full, 128);
+    mbar_init(&c.ds_full, kBwdCompute);
     mbar_init(&c.mm_done, 1);
-    mbar_init(&c.x1_free, 128);
+    mbar_init(&c.x1_free, kBwdCompute);
     mbar_init(&c.acc_full, 1);
-    mbar_init(&c.acc_free, 128);
-    mbar_init(&c.xch_bar, 128);
+    mbar_init(&c.acc_free, kBwdCompute);
+    mbar_init(&c.xch_bar, kBwdCompute);
     c.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) tmem_alloc(&c.tmem_base, 512);
-  if (warp == 4 && lane == 0) {
+  if (warp == kWarpMma) tmem_alloc(&c.tmem_base, 512);
+  if (warp == kWarpProd && lane == 0) {
     prefetch_tensormap(&map_q);
     prefetch_tensormap(&map_k);
     prefetch_tensormap(&map_v);
@@ -279,7 +293,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tb = c.tmem_base;
 
-  if (warp == 4) {
+  if (warp == kWarpProd) {
     // ------------------------------------------------------------ producer
     uint32_t ic = 0, ii = 0;
     bool ok = true;
@@ -315,15 +329,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int qt = q_first; qt < n_t; ++qt, ++ii) {
           const int qs = ii & 1;
           if (!(ok = mbar_wait_warp(&c.qd_empty[qs], ((ii >> 1) & 1) ^ 1, abort_flag, hdr, 0x302))) break;
+#pragma unroll
+          for (int rr4 = 0; rr4 < 4; ++rr4) {
+            const int row = lane * 4 + rr4, i_loc = kTile * qt + row;
+            const RowVals v = load_row(p, h, ds + i_loc, i_loc < len);
+            c.rows[qs][row] = RowStage{v.rowc, v.hdo, 1.0f / v.li, v.Di, v.mi, v.eq};
+          }
           if (lane == 0) {
             mbar_arrive_expect_tx(&c.qd_full[qs], 2 * kTile * HD);
             tma_load_3d(tl.q[qs], &map_q, &c.qd_full[qs], 0, h, ds + kTile * qt);
             tma_load_3d(tl.dO[qs], &map_do, &c.qd_full[qs], 0, h, ds + kTile * qt);
+          } else {
+            mbar_arrive(&c.qd_full[qs]);
           }
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
       uint32_t ic = 0, ii = 0;
@@ -382,7 +404,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ compute warps
-    const int r = tid;
+    const int q = warp & 3, hf = warp >> 2;  // lane quarter (query rows), key-block half
+    const int r = 32 * q + lane;             // query row of the tile = TMEM lane
+    const int b0 = 2 * hf;                   // first of this thread's two key blocks
+    constexpr int HC = HD / 2;               // output columns drained by this thread
     uint32_t ic = 0, ii = 0;
     bool ok = true;
     const float sm_scale = p.softmax_scale;
@@ -398,44 +423,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int qt = q_first; ok && qt < n_t; ++qt, ++ii) {
           const int i_loc = kTile * qt + r;
           const bool row_ok = i_loc < len;
-          const RowVals rv = load_row(p, h, ds + i_loc, row_ok);
+          const int qs = ii & 1;
+          if (!(ok = mbar_wait_warp(&c.qd_full[qs], (ii >> 1) & 1, abort_flag, hdr, 0x328))) break;
+          const RowStage rv = c.rows[qs][r];
           if (!(ok = mbar_wait_warp(&c.s_full, ii & 1, abort_flag, hdr, 0x322))) break;
           tc_fence_after();
-          uint32_t pcode[32];
-          int Eb[4];
+          uint32_t pcode[16];
+          int Eb[2];
           // the diagonal tile (and a document's last key tile) needs the mask
           const bool need_mask = p.causal ? (qt == it.y) : (it.y == n_t - 1);
-          recompute_phat<EXACT>(taddr(tb, warp * 32, kColX0), rv.rowc, c.kf, c.vf, i_loc, key0, len, p.causal, need_mask,
-                                row_ok, pcode, Eb);
-          if (row_ok) dbg_dump_phat(hdr, p.T, h, ds + i_loc, ds + key0, pcode, Eb);
+          recompute_phat<EXACT, 2>(taddr(tb, q * 32, kColX0), b0, rv.rowc, c.kf, c.vf, i_loc, key0, len, p.causal,
+                                   need_mask, row_ok, pcode, Eb);
+          if (row_ok) dbg_dump_phat2(hdr, p.T, h, ds + i_loc, ds + key0, b0, pcode, Eb);
           if (!(ok = mbar_wait_warp(&c.dp_full, ii & 1, abort_flag, hdr, 0x323))) break;
           // the previous iteration's MMAs must be done with the P~ / dS tiles
           if (ii > 0 && !(ok = mbar_wait_warp(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x326))) break;
           tc_fence_after();
-          const float inv_l = 1.0f / rv.li;
-          uint32_t word_dq = 0;
           const int par = ii & 1;
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
+          for (int bb = 0; bb < 2; ++bb) {
+            const int b = b0 + bb;
             float dsv[32], ptv[32];
             float amax_ds, amax_pt;
-            ds_block(taddr(tb, warp * 32, kColX1 + 32 * b), pcode + 8 * b, Eb[b], rv.mi, inv_l, rv.hdo, rv.Di,
+            ds_block(taddr(tb, q * 32, kColX1 + 32 * b), pcode + 8 * bb, Eb[bb], rv.mi, rv.inv_l, rv.hdo, rv.Di,
                      c.vinv + 32 * b, row_ok, dsv, ptv, amax_ds, amax_pt);
             // P~: 32 x 32 block (this warp's 32 queries x key block b)
             const int e_pt = noclamp_exp_clamped(warp_max(amax_pt));
             uint32_t codes[8];
             encode32(ptv, e_pt, codes);
             store_row_block(tl.pt, r, b, codes);
-            uint32_t kbyte;
+            uint32_t kbyte, qbyte = 0;
             if constexpr (!EXACT) {
               int e_ds;
-              word_dq |= dq_operand<false>(dsv, amax_ds, c.kf + 32 * b, c.ekb[b], codes, e_ds) << (8 * b);
+              qbyte = dq_operand<false>(dsv, amax_ds, c.kf + 32 * b, c.ekb[b], codes, e_ds);
               store_row_block(tl.ds, r, b, codes);
               kbyte = sf_byte(e_ds + rv.eq);  // dK operand: the same codes, Q's block exponent folded in
             } else {
               if constexpr (DQ) {
                 int unused;
-                word_dq |= dq_operand<true>(dsv, amax_ds, c.kf + 32 * b, c.ekb[b], codes, unused) << (8 * b);
+                qbyte = dq_operand<true>(dsv, amax_ds, c.kf + 32 * b, c.ekb[b], codes, unused);
                 store_row_block(tl.ds, r, b, codes);
               }
               // dK operand: 32 x 32 block of dS * 2^eQ(i)
@@ -448,44 +474,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               store_row_block(tl.dsk, r, b, codes);
               kbyte = sf_byte(e_k);
             }
+            c.xdq[par][r][b] = (uint8_t)qbyte;
             if (lane == 0) {
-              c.xch[par][0][warp] = (c.xch[par][0][warp] & ~(0xFFu << (8 * b))) | (sf_byte(e_pt) << (8 * b));
-              c.xch[par][1][warp] = (c.xch[par][1][warp] & ~(0xFFu << (8 * b))) | (kbyte << (8 * b));
+              c.xch[par][0][q][b] = (uint8_t)sf_byte(e_pt);
+              c.xch[par][1][q][b] = (uint8_t)kbyte;
             }
           }
           if constexpr (!DQ) {  // dP has been read: X1 may take the next dP
             tc_fence_before();
             mbar_arrive(&c.x1_free);
           }
-          // scale-factor words: dV / dK rows are keys (key block = this warp),
-          // one byte per query block; dQ rows are queries (this thread's row)
-          // exchange the block exponents among the four compute warps
-          // (an mbarrier with a bounded wait, so an aborting warp cannot strand the others)
+          // exchange the block exponents among the compute warps (an mbarrier
+          // with a bounded wait, so an aborting warp cannot strand the others)
           mbar_arrive(&c.xch_bar);
           if (!(ok = mbar_wait_warp(&c.xch_bar, ii & 1, abort_flag, hdr, 0x327))) break;
-          uint32_t wdv = 0, wdk = 0;
+          if (hf == 0) {
+            // dV / dK rows are keys: lane quarter q = key block q, one byte per query block
+            uint32_t wdv = 0, wdk = 0;
 #pragma unroll
-          for (int qb = 0; qb < 4; ++qb) {
-            wdv |= ((c.xch[par][0][qb] >> (8 * warp)) & 0xFFu) << (8 * qb);
-            wdk |= ((c.xch[par][1][qb] >> (8 * warp)) & 0xFFu) << (8 * qb);
+            for (int qb = 0; qb < 4; ++qb) {
+              wdv |= (uint32_t)c.xch[par][0][qb][q] << (8 * qb);
+              wdk |= (uint32_t)c.xch[par][1][qb][q] << (8 * qb);
+            }
+            tmem_st4(taddr(tb, q * 32, kColSfDV), wdv, wdv, wdv, wdv);
+            tmem_st4(taddr(tb, q * 32, kColSfDK), wdk, wdk, wdk, wdk);
+          } else {
+            // dQ rows are queries: this thread's row, one byte per key block
+            const uint32_t wdq = *reinterpret_cast<const uint32_t*>(c.xdq[par][r]);
+            tmem_st4(taddr(tb, q * 32, kColSfDQ), wdq, wdq, wdq, wdq);
+            tmem_st4(taddr(tb, q * 32, kColSfOne), 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
           }
-          tmem_st4(taddr(tb, warp * 32, kColSfDV), wdv, wdv, wdv, wdv);
-          tmem_st4(taddr(tb, warp * 32, kColSfDK), wdk, wdk, wdk, wdk);
-          tmem_st4(taddr(tb, warp * 32, kColSfDQ), word_dq, word_dq, word_dq, word_dq);
-          tmem_st4(taddr(tb, warp * 32, kColSfOne), 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
           fence_proxy_async_smem();
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(&c.ds_full);
           if constexpr (DQ) {
-            // ---- dQ tile -> fp32 buffer
+            // ---- dQ tile -> fp32 buffer (this thread: its row, half of the columns)
             if (!(ok = mbar_wait_warp(&c.mm_done, ii & 1, abort_flag, hdr, 0x324))) break;
             tc_fence_after();
-            float* dst = p.dq_acc + ((size_t)(ds + i_loc) * p.H + h) * HD;
+            float* dst = p.dq_acc + ((size_t)(ds + i_loc) * p.H + h) * HD + hf * HC;
 #pragma unroll
-            for (int cb = 0; cb < HD / 32; ++cb) {
+            for (int cb = 0; cb < HC / 32; ++cb) {
               uint32_t rr[32];
-              tmem_ld32(taddr(tb, warp * 32, kColX1 + 32 * cb), rr);
+              tmem_ld32(taddr(tb, q * 32, kColX1 + hf * HC + 32 * cb), rr);
               tmem_ld_wait();
               if (row_ok) {
 #pragma unroll
@@ -502,21 +533,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!ok) break;
       mbar_arrive(&c.kv_empty);  // key vectors no longer read
-      // ---- dK, dV of this key tile (TMEM lane = key)
+      // ---- dK, dV of this key tile (TMEM lane = key; this thread: half of the columns)
       if (!(ok = mbar_wait_warp(&c.acc_full, ic & 1, abort_flag, hdr, 0x325))) break;
       tc_fence_after();
       const int j_loc = key0 + r;
       const bool key_ok = j_loc < len;
-      const size_t koff = ((size_t)(ds + j_loc) * p.Hkv + hk) * HD;
+      const size_t koff = ((size_t)(ds + j_loc) * p.Hkv + hk) * HD + hf * HC;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const float f = which == 0 ? sm_scale : 1.0f;
         void* outp = which == 0 ? p.dK : p.dV;
-        const uint32_t col = which == 0 ? kColDK : kColDV;
+        const uint32_t col = (which == 0 ? kColDK : kColDV) + hf * HC;
 #pragma unroll
-        for (int cb = 0; cb < HD / 32; ++cb) {
+        for (int cb = 0; cb < HC / 32; ++cb) {
           uint32_t rr[32];
-          tmem_ld32(taddr(tb, warp * 32, col + 32 * cb), rr);
+          tmem_ld32(taddr(tb, q * 32, col + 32 * cb), rr);
           tmem_ld_wait();
           if (key_ok) store_row32<OUT_BF16>(outp, koff + 32 * cb, rr, f);
         }
@@ -528,7 +559,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_before();
   __syncthreads();
   drain_after_abort(abort_flag);
-  if (warp == 5) tmem_dealloc(tb, 512);
+  if (warp == kWarpMma) tmem_dealloc(tb, 512);
 }
 
 // ============================================================================
@@ -553,8 +584,9 @@ struct __align__(1024) DqTiles {
 struct DqCtl {
   float kf[kDqStages][kTile], vf[kDqStages][kTile], vinv[kDqStages][kTile];
   int ekb[kDqStages][4];
+  uint8_t xdq[2][kTile][4];  // [parity][query row][key block] dQ scale bytes
   uint64_t qd_full, qd_empty, kv_full[kDqStages], kv_empty[kDqStages];
-  uint64_t s_full, dp_full, dp_free, ds_full, mm_done, dq_full, dq_free;
+  uint64_t s_full, dp_full, dp_free, ds_full, mm_done, dq_full, dq_free, xch_bar;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -582,25 +614,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&c.qd_empty, 1);
     for (int s = 0; s < kDqStages; ++s) {
       mbar_init(&c.kv_full[s], 32);
-      mbar_init(&c.kv_empty[s], 1 + 128);
+      mbar_init(&c.kv_empty[s], 1 + kBwdCompute);
     }
     mbar_init(&c.s_full, 1);
     mbar_init(&c.dp_full, 1);
-    mbar_init(&c.dp_free, 128);
-    mbar_init(&c.ds_full, 128);
+    mbar_init(&c.dp_free, kBwdCompute);
+    mbar_init(&c.ds_full, kBwdCompute);
     mbar_init(&c.mm_done, 1);
     mbar_init(&c.dq_full, 1);
-    mbar_init(&c.dq_free, 128);
+    mbar_init(&c.dq_free, kBwdCompute);
+    mbar_init(&c.xch_bar, kBwdCompute);
     c.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) tmem_alloc(&c.tmem_base, 512);
+  if (warp == kWarpMma) tmem_alloc(&c.tmem_base, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = c.tmem_base;
 
-  if (warp == 4) {
+  if (warp == kWarpProd) {
     uint32_t ic = 0, kv = 0;
     bool ok = true;
     for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++ic) {
@@ -640,7 +673,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     if (elect_one()) {
       uint32_t ic = 0, kv = 0, ii = 0;
       bool ok = true;
@@ -685,7 +718,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     __syncwarp();
   } else {
-    const int r = tid;
+    const int q = warp & 3, hf = warp >> 2;  // lane quarter (query rows), key-block half
+    const int r = 32 * q + lane;
+    const int b0 = 2 * hf;
+    constexpr int HC = HD / 2;
     uint32_t ic = 0, kv = 0, ii = 0;
     bool ok = true;
     for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++ic) {
@@ -703,29 +739,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!(ok = mbar_wait_warp(&c.kv_full[st], ph, abort_flag, hdr, 0x421))) break;
         if (!(ok = mbar_wait_warp(&c.s_full, ii & 1, abort_flag, hdr, 0x422))) break;
         tc_fence_after();
-        uint32_t pcode[32];
-        int Eb[4];
-        recompute_phat<EXACT>(taddr(tb, warp * 32, kDqColX0), rv.rowc, c.kf[st], c.vf[st], i_loc, kTile * kt, len,
-                              p.causal, kt == n_kt - 1, row_ok, pcode, Eb);
+        uint32_t pcode[16];
+        int Eb[2];
+        recompute_phat<EXACT, 2>(taddr(tb, q * 32, kDqColX0), b0, rv.rowc, c.kf[st], c.vf[st], i_loc, kTile * kt,
+                                 len, p.causal, kt == n_kt - 1, row_ok, pcode, Eb);
         if (!(ok = mbar_wait_warp(&c.dp_full, ii & 1, abort_flag, hdr, 0x423))) break;
         if (ii > 0 && !(ok = mbar_wait_warp(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x424))) break;
         tc_fence_after();
-        uint32_t word_dq = 0;
+        const int par = ii & 1;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
+        for (int bb = 0; bb < 2; ++bb) {
+          const int b = b0 + bb;
           float dsv[32], ptv[32];
           float amax_ds, amax_pt;
-          ds_block(taddr(tb, warp * 32, kDqColX1 + 32 * b), pcode + 8 * b, Eb[b], rv.mi, inv_l, rv.hdo, rv.Di,
+          ds_block(taddr(tb, q * 32, kDqColX1 + 32 * b), pcode + 8 * bb, Eb[bb], rv.mi, inv_l, rv.hdo, rv.Di,
                    c.vinv[st] + 32 * b, row_ok, dsv, ptv, amax_ds, amax_pt);
           uint32_t codes[8];
           int e_blk;
-          word_dq |= dq_operand<EXACT>(dsv, amax_ds, c.kf[st] + 32 * b, c.ekb[st][b], codes, e_blk) << (8 * b);
+          c.xdq[par][r][b] =
+              (uint8_t)dq_operand<EXACT>(dsv, amax_ds, c.kf[st] + 32 * b, c.ekb[st][b], codes, e_blk);
           store_row_block(tl.ds, r, b, codes);
         }
         tc_fence_before();
         mbar_arrive(&c.dp_free);
-        tmem_st4(taddr(tb, warp * 32, kDqColSf), word_dq, word_dq, word_dq, word_dq);
-        tmem_st4(taddr(tb, warp * 32, kDqColSfOne), 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        mbar_arrive(&c.xch_bar);
+        if (!(ok = mbar_wait_warp(&c.xch_bar, ii & 1, abort_flag, hdr, 0x426))) break;
+        if (hf == 0) {
+          const uint32_t wdq = *reinterpret_cast<const uint32_t*>(c.xdq[par][r]);
+          tmem_st4(taddr(tb, q * 32, kDqColSf), wdq, wdq, wdq, wdq);
+          tmem_st4(taddr(tb, q * 32, kDqColSfOne), 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        }
         fence_proxy_async_smem();
         tmem_st_wait();
         tc_fence_before();
@@ -735,11 +778,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       if (!(ok = mbar_wait_warp(&c.dq_full, ic & 1, abort_flag, hdr, 0x425))) break;
       tc_fence_after();
-      const size_t off = ((size_t)(ds + i_loc) * p.H + h) * HD;
+      const size_t off = ((size_t)(ds + i_loc) * p.H + h) * HD + hf * HC;
 #pragma unroll
-      for (int cb = 0; cb < HD / 32; ++cb) {
+      for (int cb = 0; cb < HC / 32; ++cb) {
         uint32_t rr[32];
-        tmem_ld32(taddr(tb, warp * 32, kDqColAcc + 32 * cb), rr);
+        tmem_ld32(taddr(tb, q * 32, kDqColAcc + hf * HC + 32 * cb), rr);
         tmem_ld_wait();
         if (row_ok) store_row32<OUT_BF16>(p.dQ, off + 32 * cb, rr, p.softmax_scale);
       }
@@ -750,7 +793,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_before();
   __syncthreads();
   drain_after_abort(abort_flag);
-  if (warp == 5) tmem_dealloc(tb, 512);
+  if (warp == kWarpMma) tmem_dealloc(tb, 512);
 }
 
 // dQ buffer (fp32, already scaled) -> output dtype.

@@ -29,6 +29,23 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "header");
 
+// Test hook: record one row's P^ codes and block exponents for two 32-key
+// blocks (b0, b0 + 1) of a 128-key tile.
+__device__ __forceinline__ void dbg_dump_phat2(const WsHeader* hdr, int T, int h, int tok, int key_tok0, int b0,
+                                               const uint32_t (&codes)[16], const int (&Eb)[2]) {
+  uint8_t* dc = hdr->dbg_phat;
+  if (dc == nullptr) return;
+  int32_t* de = hdr->dbg_eb;
+  const size_t row = ((size_t)h * T + tok) * (size_t)T;
+  const int k0 = key_tok0 + 32 * b0;
+#pragma unroll
+  for (int j = 0; j < 64; ++j)
+    if (k0 + j < T) dc[row + k0 + j] = (uint8_t)(codes[j >> 2] >> (8 * (j & 3)));
+#pragma unroll
+  for (int b = 0; b < 2; ++b)
+    if (k0 + 32 * b < T) de[row + k0 + 32 * b] = Eb[b];
+}
+
 // Test hook: record one row's P^ codes and block exponents for a 128-key tile.
 __device__ __forceinline__ void dbg_dump_phat(const WsHeader* hdr, int T, int h, int tok, int key_tok0,
                                               const uint32_t (&codes)[32], const int (&Eb)[4]) {
@@ -149,13 +166,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes) : "memory");
 }
+// One poll.  The suspend-time hint lets the hardware park the warp until the
+// phase completes (or 1 ms passes) instead of spinning on issue slots that
+// the other warps of the same sub-partition need.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u) : "memory");
   return ok != 0;
 }
 
@@ -173,19 +193,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           WsHeader* hdr, uint32_t where) {
-  uint64_t t0 = 0;
-  for (uint32_t i = 0;; ++i) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u) {
-      if (*abort_flag) return false;
-      const uint64_t now = globaltimer_ns();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        report(hdr, FLAMIA_ERR_TIMEOUT, where);
-        return false;
-      }
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      report(hdr, FLAMIA_ERR_TIMEOUT, where);
+      return false;
     }
   }
 }
@@ -318,6 +334,9 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t a, uint32_t b) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(a), "r"(b) : "memory");
+}
 __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
                "r"(c), "r"(d) : "memory");

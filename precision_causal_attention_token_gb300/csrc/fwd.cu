@@ -6,16 +6,18 @@
 //
 // Persistent grid over the longest-first work list (document, 128-query tile)
 // x query heads.  Warp roles:
-//   warps 0-3  softmax: thread r owns query row r of the tile = TMEM lane r.
+//   warps 0-7  softmax: two warps per TMEM lane quarter; thread (warp w, lane)
+//              owns query row 32(w%4)+lane of the tile (= its TMEM lane) and
+//              key blocks 2(w/4), 2(w/4)+1 of each 128-key tile.
 //              Reads S from TMEM, forms y = x + eV(j) (the per-key V factor
 //              folded into P along the contraction axis), quantizes P^ with
 //              one no-clamp exponent per (row, 32-key block), keeps the
 //              row's integer reference m and normaliser l, writes P^ codes to
 //              shared memory and the block exponents (relative to m) to TMEM
 //              as the A-operand scale factors of the P^V MMA.
-//   warp 4     producer: TMA loads of Q, K, V code tiles (128 x d, swizzled)
+//   warp 8     producer: TMA loads of Q, K, V code tiles (128 x d, swizzled)
 //              and the per-key scale vectors of each K/V stage.
-//   warp 5     MMA issuer: S = Q^ K^T (kind::f8f6f4, fp32 in TMEM, double
+//   warp 9     MMA issuer: S = Q^ K^T (kind::f8f6f4, fp32 in TMEM, double
 //              buffered) and O += P^ V^ (kind::mxf8f6f4 block-scaled, scale A
 //              = P^ block exponents, scale B = 1: V's own scale is folded).
 // The next tile's S is issued before the current tile's P^V so the tensor
@@ -26,7 +28,9 @@
 namespace flamia {
 
 constexpr int kFwdStages = 3;
-constexpr int kFwdThreads = 192;
+constexpr int kFwdSoftmax = 256;
+constexpr int kFwdThreads = kFwdSoftmax + 64;
+constexpr int kFwdWarpProd = 8, kFwdWarpMma = 9;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColSFA0 = 384, kColSFA1 = 392, kColSFB = 400;
 
 template <int HD>
@@ -43,7 +47,9 @@ struct FwdCtl {
   float vinv[kFwdStages][kTile];  // 2^-eV(j)
   uint64_t q_full, q_empty;
   uint64_t k_full[kFwdStages], k_empty[kFwdStages], v_full[kFwdStages], v_empty[kFwdStages];
-  uint64_t s_full[2], s_free[2], p_full[2], p_free[2], o_full, o_free;
+  uint64_t s_full[2], s_free[2], p_full[2], p_free[2], o_full, o_free, eb_bar, l_bar;
+  int ebx[2][kTile][4];  // [tile parity][row][key block] P^ block exponents, shared by a row's two threads
+  float lx[kTile][2];    // [row][half] partial normalisers for the epilogue
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -81,23 +87,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     mbar_init(&c.q_empty, 1);
     for (int s = 0; s < kFwdStages; ++s) {
       mbar_init(&c.k_full[s], 32);
-      mbar_init(&c.k_empty[s], 1 + 128);
+      mbar_init(&c.k_empty[s], 1 + kFwdSoftmax);
       mbar_init(&c.v_full[s], 1);
       mbar_init(&c.v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&c.s_full[b], 1);
-      mbar_init(&c.s_free[b], 128);
-      mbar_init(&c.p_full[b], 128);
+      mbar_init(&c.s_free[b], kFwdSoftmax);
+      mbar_init(&c.p_full[b], kFwdSoftmax);
       mbar_init(&c.p_free[b], 1);
     }
     mbar_init(&c.o_full, 1);
-    mbar_init(&c.o_free, 128);
+    mbar_init(&c.o_free, kFwdSoftmax);
+    mbar_init(&c.eb_bar, kFwdSoftmax);
+    mbar_init(&c.l_bar, kFwdSoftmax);
     c.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) tmem_alloc(&c.tmem_base, 512);
-  if (warp == 4 && lane == 0) {
+  if (warp == kFwdWarpMma) tmem_alloc(&c.tmem_base, 512);
+  if (warp == kFwdWarpProd && lane == 0) {
     prefetch_tensormap(&map_q);
     prefetch_tensormap(&map_k);
     prefetch_tensormap(&map_v);
@@ -114,7 +122,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after();
 
-  if (warp == 4) {
+  if (warp == kFwdWarpProd) {
     // ------------------------------------------------------------ producer
     uint32_t kv = 0, qc = 0;
     bool ok = true;
@@ -159,7 +167,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kFwdWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
       uint32_t kv = 0, qc = 0, sc = 0, pc = 0, ic = 0;
@@ -217,7 +225,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int r = tid;
+    const int q = warp & 3, hf = warp >> 2;  // lane quarter, key-block half
+    const int r = 32 * q + lane;             // query row of the tile = TMEM lane
+    const int b0 = 2 * hf;                   // first of this thread's two key blocks
+    constexpr int HC = HD / 2;               // O columns handled by this thread
     uint32_t kv = 0, sc = 0, pc = 0, ic = 0;
     bool ok = true;
     for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
@@ -231,7 +242,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int eq = row_ok ? (int)__ldg(p.q_sc + (size_t)h * p.T + q0 + r) - 127 : 0;
       const float rowc = p.c_log2 * pow2_127(eq);
       int m_ref = kEmptyBlock;
-      float l_run = 0.f;
+      float l_run = 0.f;  // this thread's share of the normaliser (its two key blocks)
       for (int kt = 0; ok && kt < n_kt; ++kt, ++kv, ++sc, ++pc) {
         const int st = kv % kFwdStages;
         const uint32_t kph = (kv / kFwdStages) & 1;
@@ -241,68 +252,77 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_after();
         const int key0 = kTile * kt;
         const bool need_mask = (kt == n_kt - 1);  // diagonal tile, or a document's last tile
-        int Eb[4];
-        float lb[4];
-        uint32_t codes[32];
+        int Eb[2];
+        float lb[2];
+        uint32_t codes[16];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
+        for (int bb = 0; bb < 2; ++bb) {
+          const int b = b0 + bb;
           float a[32];
           {
             uint32_t rr[32];
-            tmem_ld32(taddr(tb, warp * 32, (sb ? kColS1 : kColS0) + 32 * b), rr);
+            tmem_ld32(taddr(tb, q * 32, (sb ? kColS1 : kColS0) + 32 * b), rr);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(rr[j]);
           }
-          Eb[b] = phat_block_logits<EXACT>(a, rowc, c.kf[st] + 32 * b, c.vf[st] + 32 * b, need_mask, i_loc,
-                                           key0 + 32 * b, len, p.causal);
+          Eb[bb] = phat_block_logits<EXACT>(a, rowc, c.kf[st] + 32 * b, c.vf[st] + 32 * b, need_mask, i_loc,
+                                            key0 + 32 * b, len, p.causal);
           float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
             float pv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              pv[e] = (Eb[b] == kEmptyBlock) ? 0.f : phat_value(a[4 * q4 + e], Eb[b]);
+              pv[e] = (Eb[bb] == kEmptyBlock) ? 0.f : phat_value(a[4 * q4 + e], Eb[bb]);
               l4[e] = fmaf(pv[e], c.vinv[st][32 * b + 4 * q4 + e], l4[e]);
             }
-            codes[8 * b + q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
+            codes[8 * bb + q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
           }
-          lb[b] = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+          lb[bb] = (l4[0] + l4[1]) + (l4[2] + l4[3]);
         }
         tc_fence_before();
         mbar_arrive(&c.s_free[sb]);
-        const int Emax = max(max(Eb[0], Eb[1]), max(Eb[2], Eb[3]));
+        // the row's reference needs all four block exponents: exchange with
+        // the row's other thread (an mbarrier with a bounded wait)
+        const int par = sc & 1;
+        c.ebx[par][r][b0] = Eb[0];
+        c.ebx[par][r][b0 + 1] = Eb[1];
+        mbar_arrive(&c.eb_bar);
+        if (!(ok = mbar_wait_warp(&c.eb_bar, sc & 1, abort_flag, hdr, 0x226))) break;
+        int Eall[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) Eall[b] = c.ebx[par][r][b];
+        const int Emax = max(max(Eall[0], Eall[1]), max(Eall[2], Eall[3]));
         int m_new = m_ref;
         if (Emax != kEmptyBlock && (m_ref == kEmptyBlock || Emax > m_ref + 8)) m_new = Emax;
         float lsum = 0.f;
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb)
+          if (Eb[bb] != kEmptyBlock) lsum += ldexp_f(lb[bb], Eb[bb] - m_new);
         uint32_t word = 0;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          if (Eb[b] != kEmptyBlock) {
-            lsum += ldexp_f(lb[b], Eb[b] - m_new);
-            const int byte = min(max(Eb[b] - m_new + 127, 0), 254);
-            word |= (uint32_t)byte << (8 * b);
-          }
-        }
+        for (int b = 0; b < 4; ++b)
+          if (Eall[b] != kEmptyBlock) word |= (uint32_t)min(max(Eall[b] - m_new + 127, 0), 254) << (8 * b);
         mbar_arrive(&c.k_empty[st]);
-        if (row_ok) dbg_dump_phat(hdr, p.T, h, q0 + r, ds + key0, codes, Eb);
+        if (row_ok) dbg_dump_phat2(hdr, p.T, h, q0 + r, ds + key0, b0, codes, Eb);
         l_run = (m_ref == kEmptyBlock) ? lsum : ldexp_f(l_run, m_ref - m_new) + lsum;
-        // rescale the O accumulator rows once the previous P^V has landed
-        // (warp-uniform: tcgen05.ld/st are warp-collective; lanes whose
-        // reference did not move scale by 1)
+        // rescale this thread's half of the O accumulator row once the previous
+        // P^V has landed (warp-uniform: tcgen05.ld/st are warp-collective; lanes
+        // whose reference did not move scale by 1)
         if (__any_sync(0xffffffffu, kt > 0 && m_new != m_ref)) {
           const uint32_t pp = pc - 1;
           if (!(ok = mbar_wait_warp(&c.p_free[pp & 1], (pp >> 1) & 1, abort_flag, hdr, 0x223))) break;
           tc_fence_after();
           const float f = (m_new != m_ref) ? ldexp_f(1.0f, m_ref - m_new) : 1.0f;
 #pragma unroll
-          for (int cb = 0; cb < HD / 32; ++cb) {
+          for (int cb = 0; cb < HC / 32; ++cb) {
             uint32_t rr[32];
-            tmem_ld32(taddr(tb, warp * 32, kColO + 32 * cb), rr);
+            tmem_ld32(taddr(tb, q * 32, kColO + hf * HC + 32 * cb), rr);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * f);
-            tmem_st32(taddr(tb, warp * 32, kColO + 32 * cb), rr);
+            tmem_st32(taddr(tb, q * 32, kColO + hf * HC + 32 * cb), rr);
           }
           tmem_st_wait();
         }
@@ -311,38 +331,43 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (!(ok = mbar_wait_warp(&c.p_free[pb], ((pc >> 1) & 1) ^ 1, abort_flag, hdr, 0x224))) break;
         uint8_t* prow = tl.p[pb];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int ch = 0; ch < 4; ++ch) {
           uint4 v4 = make_uint4(codes[4 * ch], codes[4 * ch + 1], codes[4 * ch + 2], codes[4 * ch + 3]);
-          *reinterpret_cast<uint4*>(prow + sw128_off(r, ch)) = v4;
+          *reinterpret_cast<uint4*>(prow + sw128_off(r, 4 * hf + ch)) = v4;
         }
-        tmem_st4(taddr(tb, warp * 32, pb ? kColSFA1 : kColSFA0), word, word, word, word);
+        // the row's scale word goes to all four columns (two per thread)
+        tmem_st2(taddr(tb, q * 32, (pb ? kColSFA1 : kColSFA0) + 2 * hf), word, word);
         fence_proxy_async_smem();
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&c.p_full[pb]);
       }
       if (!ok) break;
-      // epilogue: O = acc / l
+      // epilogue: O = acc / l (this thread: half of the row)
       if (!(ok = mbar_wait_warp(&c.o_full, ic & 1, abort_flag, hdr, 0x225))) break;
       tc_fence_after();
-      float o[HD];
+      float o[HC];
 #pragma unroll
-      for (int cb = 0; cb < HD / 32; ++cb) {
+      for (int cb = 0; cb < HC / 32; ++cb) {
         uint32_t rr[32];
-        tmem_ld32(taddr(tb, warp * 32, kColO + 32 * cb), rr);
+        tmem_ld32(taddr(tb, q * 32, kColO + hf * HC + 32 * cb), rr);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j) o[32 * cb + j] = __uint_as_float(rr[j]);
       }
       tc_fence_before();
       mbar_arrive(&c.o_free);
+      c.lx[r][hf] = l_run;
+      mbar_arrive(&c.l_bar);
+      if (!(ok = mbar_wait_warp(&c.l_bar, ic & 1, abort_flag, hdr, 0x227))) break;
+      const float l_tot = c.lx[r][0] + c.lx[r][1];
       if (row_ok) {
-        const float inv = 1.0f / l_run;
-        const size_t off = ((size_t)(q0 + r) * p.H + h) * HD;
+        const float inv = 1.0f / l_tot;
+        const size_t off = ((size_t)(q0 + r) * p.H + h) * HD + hf * HC;
         if constexpr (OUT_BF16) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O) + off);
 #pragma unroll
-          for (int c8 = 0; c8 < HD / 8; ++c8) {
+          for (int c8 = 0; c8 < HC / 8; ++c8) {
             uint32_t wv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -354,11 +379,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         } else {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.O) + off);
 #pragma unroll
-          for (int c4 = 0; c4 < HD / 4; ++c4)
+          for (int c4 = 0; c4 < HC / 4; ++c4)
             dst[c4] = make_float4(o[4 * c4] * inv, o[4 * c4 + 1] * inv, o[4 * c4 + 2] * inv, o[4 * c4 + 3] * inv);
         }
-        p.m[(size_t)h * p.T + q0 + r] = m_ref;
-        p.l[(size_t)h * p.T + q0 + r] = l_run;
+        if (hf == 0) {
+          p.m[(size_t)h * p.T + q0 + r] = m_ref;
+          p.l[(size_t)h * p.T + q0 + r] = l_tot;
+        }
       }
       ++ic;
     }
@@ -366,7 +393,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_before();
   __syncthreads();
   drain_after_abort(abort_flag);
-  if (warp == 5) tmem_dealloc(tb, 512);
+  if (warp == kFwdWarpMma) tmem_dealloc(tb, 512);
 }
 
 static int num_sms() {

@@ -65,10 +65,11 @@ def test_empty_and_single_token_documents():
     tc = run_gpu(w)
     ref = run_oracle(w)
     _check_all(w, tc, ref)
-    # a one-token document attends to itself only: O = V^ (bf16-rounded)
+    # a one-token document attends to itself only: O = V^ (P^ / P), within
+    # one E4M3 rounding of P^ (the normaliser uses the unquantized P)
     vh = oracle.dequantize_blocks(ref["v_codes"], ref["v_scales"])
     o = np_of(tc.O)
-    assert np.abs(o[0] - vh[0]).max() <= 1e-2 * np.abs(vh[0]).max()
+    assert np.abs(o[0] - vh[0]).max() <= (2.0 ** -4 + 2.0 ** -8) * np.abs(vh[0]).max()
 
 
 def _doc_slice(w, doc, heads, kv_heads):
