@@ -70,6 +70,21 @@ bool make_codes_map(CUtensorMap* m, const void* ptr, int d, int heads, int T) {
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over the fp32 dQ accumulator [T][heads][d]: box = 128 tokens x 1
+// head x 32 values (128 bytes, 128B swizzle), the target of bulk reduce-adds.
+bool make_dq_map(CUtensorMap* m, float* ptr, int d, int heads, int T) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)heads * d * 4};
+  cuuint32_t box[3] = {32, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool operand_ok(const flamia_operand_t* o) { return o && o->codes && o->scales && aligned16(o->codes); }
 
 }  // namespace
@@ -120,31 +135,36 @@ flamia_status_t flamia_quantize(const flamia_problem_t* p, int32_t role, const v
       if (!in[i] || !aligned16(in[i]) || !operand_ok(&out[i])) return FLAMIA_ERR_INVALID_ARG;
     }
     const bool nv = p->path == FLAMIA_PATH_NVFP4_FP8;
+    QuantBatch qb{};
+    qb.n = 3;
+    int units = 0;
     for (int i = 0; i < 3; ++i) {
-      QuantArgs a{};
+      QuantArgs& a = qb.a[i];
       a.x = in[i];
       a.codes = static_cast<uint8_t*>(out[i].codes);
       a.scales = static_cast<uint8_t*>(out[i].scales);
       a.heads = i == 0 ? p->H : p->Hkv;
       a.T = p->T;
       a.per_token = (i == 2 || p->exact) ? 1 : 0;
-      const bool nv_i = nv && i < 2;
-      if (nv_i) {
+      if (nv && i < 2) {
         if (!out[i].codes4 || !out[i].scales4 || !out[i].gscale4) return FLAMIA_ERR_INVALID_ARG;
         a.codes4 = static_cast<uint8_t*>(out[i].codes4);
         a.scales4 = static_cast<uint8_t*>(out[i].scales4);
         a.gscale4 = static_cast<float*>(out[i].gscale4);
       }
-      if (launch_quantize(a, p->d, in_bf16, o_bf16, false, nv_i, p->cu_seqlens, blk, p->n_seq, hdr,
-                          max_blk * a.heads, stream) != cudaSuccess)
-        return FLAMIA_ERR_CUDA;
+      units += max_blk * a.heads;
     }
-    return FLAMIA_OK;
+    return launch_quantize(qb, p->d, in_bf16, o_bf16, false, nv, p->cu_seqlens, blk, p->n_seq, hdr, units,
+                           sm_count(), stream) == cudaSuccess
+               ? FLAMIA_OK
+               : FLAMIA_ERR_CUDA;
   }
   if (role == FLAMIA_ROLE_DO) {
     if (!in[0] || !aligned16(in[0]) || !O || !aligned16(O) || !D || !operand_ok(&out[0]))
       return FLAMIA_ERR_INVALID_ARG;
-    QuantArgs a{};
+    QuantBatch qb{};
+    qb.n = 1;
+    QuantArgs& a = qb.a[0];
     a.x = in[0];
     a.codes = static_cast<uint8_t*>(out[0].codes);
     a.scales = static_cast<uint8_t*>(out[0].scales);
@@ -153,8 +173,8 @@ flamia_status_t flamia_quantize(const flamia_problem_t* p, int32_t role, const v
     a.heads = p->H;
     a.T = p->T;
     a.per_token = p->exact ? 1 : 0;
-    return launch_quantize(a, p->d, in_bf16, o_bf16, true, false, p->cu_seqlens, blk, p->n_seq, hdr,
-                           max_blk * p->H, stream) == cudaSuccess
+    return launch_quantize(qb, p->d, in_bf16, o_bf16, true, false, p->cu_seqlens, blk, p->n_seq, hdr,
+                           max_blk * p->H, sm_count(), stream) == cudaSuccess
                ? FLAMIA_OK
                : FLAMIA_ERR_CUDA;
   }
@@ -205,6 +225,7 @@ flamia_status_t flamia_fwd(const flamia_problem_t* p, const flamia_operand_t* q,
       !make_codes_map(&maps.v, v->codes, p->d, p->Hkv, p->T))
     return FLAMIA_ERR_CUDA;
   maps.dO = maps.q;
+  maps.dq = maps.q;
   return launch_fwd(a, maps, stream) == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
 }
 
@@ -232,7 +253,8 @@ flamia_status_t flamia_bwd(const flamia_problem_t* p, const flamia_operand_t* q,
   a.dQ = dQ; a.dK = dK; a.dV = dV;
   AttnMaps maps;
   if (!make_codes_map(&maps.q, q->codes, p->d, p->H, p->T) || !make_codes_map(&maps.k, k->codes, p->d, p->Hkv, p->T) ||
-      !make_codes_map(&maps.v, v->codes, p->d, p->Hkv, p->T) || !make_codes_map(&maps.dO, dO->codes, p->d, p->H, p->T))
+      !make_codes_map(&maps.v, v->codes, p->d, p->Hkv, p->T) || !make_codes_map(&maps.dO, dO->codes, p->d, p->H, p->T) ||
+      !make_dq_map(&maps.dq, a.dq_acc, p->d, p->H, p->T))
     return FLAMIA_ERR_CUDA;
   return launch_bwd(a, maps, stream) == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
 }

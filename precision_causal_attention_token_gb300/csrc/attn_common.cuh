@@ -37,17 +37,18 @@ constexpr int kEmptyBlock = -(1 << 30);
 // 32-token blocks), so one scale serves all 32 keys; the exact option has a
 // per-key scale.  The value of every visible y is the same either way.
 // Only the tile on the diagonal (and a document's last, partial tile) needs
-// the mask: `need_mask` is false on the tiles every key of which is visible.
-template <bool EXACT>
+// the mask: NEED_MASK is false on the tiles every key of which is visible,
+// and the visible logits are computed identically in both forms.
+template <bool EXACT, bool NEED_MASK>
 __device__ __forceinline__ int phat_block_logits(float (&a)[32], float rowc, const float* kf, const float* vf,
-                                                 bool need_mask, int i_loc, int key, int len, int causal) {
+                                                 int i_loc, int key, int len, int causal) {
   float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
   const float sb = __fmul_rn(rowc, kf[0]);
 #pragma unroll
   for (int jj = 0; jj < 32; ++jj) {
     const float sc = EXACT ? __fmul_rn(rowc, kf[jj]) : sb;
     float y = score_to_y(a[jj], sc, vf[jj]);
-    if (need_mask && !visible(i_loc, key + jj, len, causal)) y = -INFINITY;
+    if (NEED_MASK && !visible(i_loc, key + jj, len, causal)) y = -INFINITY;
     a[jj] = y;
     m4[jj & 3] = fmaxf(m4[jj & 3], y);
   }
@@ -57,6 +58,37 @@ __device__ __forceinline__ int phat_block_logits(float (&a)[32], float rowc, con
 
 // p = 2^(y - E) (<= 448 up to the approximation of ex2; the cvt saturates).
 __device__ __forceinline__ float phat_value(float y, int E) { return ex2_approx(__fsub_rn(y, (float)E)); }
+
+// P^ codes of one 32-key block from its logits and exponent (all zero for an
+// empty block), as 8 words of 4 E4M3 bytes.
+__device__ __forceinline__ void phat_block_codes(const float (&y)[32], int E, uint32_t (&codes)[8]) {
+#pragma unroll
+  for (int q4 = 0; q4 < 8; ++q4) {
+    float pv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pv[e] = (E == kEmptyBlock) ? 0.f : phat_value(y[4 * q4 + e], E);
+    codes[q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
+  }
+}
+
+// Two 32-key blocks of logits for one row: both S blocks are read from
+// tensor memory with one wait, then turned into logits and exponents.
+template <bool EXACT, bool NEED_MASK>
+__device__ __forceinline__ void phat_logits2(uint32_t t_s0, uint32_t t_s1, float (&y)[2][32], int (&Eb)[2],
+                                             float rowc, const float* kf, const float* vf, int i_loc, int key0,
+                                             int len, int causal) {
+  uint32_t rr[2][32];
+  tmem_ld32(t_s0, rr[0]);
+  tmem_ld32(t_s1, rr[1]);
+  tmem_ld_wait_regs(rr[0], rr[1]);
+#pragma unroll
+  for (int bb = 0; bb < 2; ++bb) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) y[bb][j] = __uint_as_float(rr[bb][j]);
+    Eb[bb] = phat_block_logits<EXACT, NEED_MASK>(y[bb], rowc, kf + 32 * bb, vf + 32 * bb, i_loc, key0 + 32 * bb,
+                                                 len, causal);
+  }
+}
 
 // x * 2^e for any integer e (exact while the result stays normal).
 __device__ __forceinline__ float ldexp_f(float x, int e) {

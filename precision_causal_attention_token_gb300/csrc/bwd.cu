@@ -34,12 +34,12 @@ namespace flamia {
 // Compute warps 0-7 (two per TMEM lane quarter: warp w owns query rows
 // 32(w%4)..+31 and key blocks 2(w/4), 2(w/4)+1), producer warp 8, MMA warp 9.
 constexpr int kBwdCompute = 256;
-constexpr int kBwdThreads = kBwdCompute + 64;
-constexpr int kWarpProd = 8, kWarpMma = 9;
+constexpr int kBwdThreads = kBwdCompute + 96;
+constexpr int kWarpProd = 8, kWarpMma = 9, kWarpRed = 10;
 constexpr uint32_t kColDV = 0, kColDK = 128, kColX0 = 256, kColX1 = 384;
 constexpr uint32_t kColSfDV = kColX0 + 0, kColSfDK = kColX0 + 4, kColSfDQ = kColX0 + 8, kColSfOne = kColX0 + 12;
 
-template <int HD>
+template <int HD, bool EXACT, bool DQ>
 struct __align__(1024) BwdTiles {
   uint8_t k[kTile * HD];
   uint8_t v[kTile * HD];
@@ -47,7 +47,9 @@ struct __align__(1024) BwdTiles {
   uint8_t dO[2][kTile * HD];
   uint8_t pt[kTile * kTile];   // P~ codes   [query][key]
   uint8_t ds[kTile * kTile];   // dS^ codes  [query][key] (dQ payload; also dK's in the default option)
-  uint8_t dsk[kTile * kTile];  // exact option: dK payload
+  uint8_t dsk[EXACT ? kTile * kTile : 1024];  // exact option: dK payload
+  // dQ tile staged for the bulk reduce-add: HD/32 boxes of [128 rows][32 fp32], 128B-swizzled
+  float dqs[DQ ? kTile * HD : 256];
 };
 
 // Per-row values of one query tile, staged in shared memory by the producer
@@ -66,14 +68,14 @@ struct BwdCtl {
   uint8_t xch[2][2][4][4];   // [parity][dV, dK][query block][key block] scale bytes
   uint8_t xdq[2][kTile][4];  // [parity][query row][key block] dQ scale bytes
   uint64_t kv_full, kv_empty, qd_full[2], qd_empty[2];
-  uint64_t s_full, dp_full, ds_full, mm_done, x1_free, acc_full, acc_free, xch_bar;
+  uint64_t s_full, dp_full, ds_full, mm_done, x1_free, acc_full, acc_free, xch_bar, dqs_full, dqs_free;
   uint32_t tmem_base;
   int abort_flag;
 };
 
-template <int HD>
+template <int HD, bool EXACT, bool DQ>
 constexpr size_t bwd_smem_bytes() {
-  return sizeof(BwdTiles<HD>) + sizeof(BwdCtl) + 1024;
+  return sizeof(BwdTiles<HD, EXACT, DQ>) + sizeof(BwdCtl) + 1024;
 }
 
 __device__ __forceinline__ uint64_t bdesc_k(const uint8_t* t, uint32_t off, uint32_t rb) {
@@ -81,11 +83,6 @@ __device__ __forceinline__ uint64_t bdesc_k(const uint8_t* t, uint32_t off, uint
 }
 __device__ __forceinline__ uint64_t bdesc_mn(const uint8_t* t, uint32_t off, uint32_t rb) {
   return smem_desc(smem_u32(t) + off, 8 * rb, 8 * rb, rb == 128 ? kSwz128 : kSwz64);
-}
-
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
-               "f"(d) : "memory");
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -96,75 +93,76 @@ __device__ __forceinline__ float warp_max(float v) {
 
 __device__ __forceinline__ uint32_t sf_byte(int e) { return (uint32_t)min(max(e + 127, 0), 254); }
 
-// Recompute this thread's P^ codes for one 128-key tile from S in TMEM, with
-// the forward's arithmetic (phat_block_logits, phat_value): the same inputs
-// give the same codes and block exponents.  Rows outside the document give
-// empty blocks.
-template <bool EXACT, int NB>
+// Recompute this thread's P^ codes for its two 32-key blocks (b0, b0 + 1) of a
+// 128-key tile from S in TMEM, with the forward's arithmetic
+// (phat_block_logits, phat_value): the same inputs give the same codes and
+// block exponents.  Rows outside the document give empty blocks (codes 0).
+template <bool EXACT>
 __device__ __forceinline__ void recompute_phat(uint32_t t_s, int b0, float rowc, const float* kf, const float* vf,
                                                int i_loc, int key0, int len, int causal, bool need_mask, bool row_ok,
-                                               uint32_t (&pcode)[8 * NB], int (&Eb)[NB]) {
-#pragma unroll
-  for (int bb = 0; bb < NB; ++bb) {
-    const int b = b0 + bb;
-    float yv[32];
-    {
-      uint32_t rr[32];
-      tmem_ld32(t_s + 32 * b, rr);
-      tmem_ld_wait();
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) yv[jj] = __uint_as_float(rr[jj]);
-    }
-    Eb[bb] = phat_block_logits<EXACT>(yv, rowc, kf + 32 * b, vf + 32 * b, need_mask, i_loc, key0 + 32 * b, len, causal);
-    if (!row_ok) Eb[bb] = kEmptyBlock;
-#pragma unroll
-    for (int q4 = 0; q4 < 8; ++q4) {
-      float pv[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) pv[e] = (Eb[bb] == kEmptyBlock) ? 0.f : phat_value(yv[4 * q4 + e], Eb[bb]);
-      pcode[8 * bb + q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
-    }
-  }
+                                               uint32_t (&pcode)[2][8], int (&Eb)[2]) {
+  float y[2][32];
+  const uint32_t t0 = t_s + 32 * b0, t1 = t0 + 32;
+  if (need_mask)
+    phat_logits2<EXACT, true>(t0, t1, y, Eb, rowc, kf + 32 * b0, vf + 32 * b0, i_loc, key0 + 32 * b0, len, causal);
+  else
+    phat_logits2<EXACT, false>(t0, t1, y, Eb, rowc, kf + 32 * b0, vf + 32 * b0, i_loc, key0 + 32 * b0, len, causal);
+  if (!row_ok) Eb[0] = Eb[1] = kEmptyBlock;
+  phat_block_codes(y[0], Eb[0], pcode[0]);
+  phat_block_codes(y[1], Eb[1], pcode[1]);
 }
 
-// dS and the P~ input of one 32-key block b of this thread's row, from dP in
-// TMEM (32 columns at t_dp):  Pn = P^ 2^-eV / l = code 2^(Eb - m) / l 2^-eV,
-// dS = Pn (dP - D) = code 2^(Eb - m) / l (accdP 2^edO - D 2^-eV), P~ input
-// = Pn 2^edO (the dO factor folded in).  Rows outside the document give 0.
-__device__ __forceinline__ void ds_block(uint32_t t_dp, const uint32_t* pcode_b, int Eb_b, int mi, float inv_l,
-                                         float hdo, float Di, const float* vinv_b, bool row_ok, float (&dsv)[32],
-                                         float (&ptv)[32], float& amax_ds, float& amax_pt) {
-  uint32_t rr[32];
-  tmem_ld32(t_dp, rr);
-  tmem_ld_wait();
+// Per-(row, key block) factors of dS and P~: with gb = 2^(Eb - m) / l (0 for
+// an empty block or a row outside the document), Pn = P^ 2^-eV / l =
+// code * gb * 2^-eV, so
+//   dS  = Pn (dP - D) = code * (accdP * gb 2^edO - gb D * 2^-eV(j))
+//   P~ input = Pn 2^edO = code * (gb 2^edO) * 2^-eV(j)   (the dO factor folded in).
+struct DsFactors {
+  float gbh;  // gb * 2^edO
+  float gbD;  // gb * D
+};
+__device__ __forceinline__ DsFactors ds_factors(int Eb_b, int mi, float inv_l, float hdo, float Di) {
   const float gb = (Eb_b == kEmptyBlock) ? 0.f : ldexp_f(inv_l, Eb_b - mi);
-  amax_ds = 0.f;
-  amax_pt = 0.f;
+  return DsFactors{gb * hdo, gb * Di};
+}
+
+// dS and the P~ input of one 32-key block of this thread's row from the dP
+// accumulator values `acc` (fp32 bits), and their max-abs.
+__device__ __forceinline__ void ds_block(const uint32_t (&acc)[32], const uint32_t (&pcode_b)[8], DsFactors f,
+                                         const float* vinv_b, float (&dsv)[32], float (&ptv)[32], float& amax_ds,
+                                         float& amax_pt) {
+  float a_ds = 0.f, a_pt = 0.f;
 #pragma unroll
   for (int q4 = 0; q4 < 8; ++q4) {
     const uint32_t cw = pcode_b[q4];
     const float2 p01 = unpack_e4m3x2((uint16_t)(cw & 0xFFFFu));
     const float2 p23 = unpack_e4m3x2((uint16_t)(cw >> 16));
     const float pd[4] = {p01.x, p01.y, p23.x, p23.y};
+    const float4 vi = *reinterpret_cast<const float4*>(vinv_b + 4 * q4);
+    const float vv[4] = {vi.x, vi.y, vi.z, vi.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int jj = 4 * q4 + e;
-      const float pg = pd[e] * gb;
-      const float d_s = pg * (__uint_as_float(rr[jj]) * hdo - Di * vinv_b[jj]);
-      dsv[jj] = row_ok ? d_s : 0.f;
-      ptv[jj] = row_ok ? pg * vinv_b[jj] * hdo : 0.f;
-      amax_ds = fmaxf(amax_ds, fabsf(dsv[jj]));
-      amax_pt = fmaxf(amax_pt, ptv[jj]);
+      const float z = fmaf(__uint_as_float(acc[jj]), f.gbh, -(f.gbD * vv[e]));
+      dsv[jj] = pd[e] * z;
+      ptv[jj] = pd[e] * (f.gbh * vv[e]);
+      a_ds = fmaxf(a_ds, fabsf(dsv[jj]));
+      a_pt = fmaxf(a_pt, ptv[jj]);
     }
   }
+  amax_ds = a_ds;
+  amax_pt = a_pt;
 }
 
-// Codes of 32 values scaled by 2^-e, as 8 words of 4 E4M3 bytes.
-__device__ __forceinline__ void encode32(const float (&v)[32], int e, uint32_t (&out)[8]) {
+// 2^-e for a block exponent e (e <= 120 for any finite max-abs, so the
+// factor is a normal fp32 and x * 2^-e is exact down to the E4M3 range).
+__device__ __forceinline__ float inv_pow2(int e) { return exp2i(-min(e, 126)); }
+
+// Codes of 32 values times s (a power of two), as 8 words of 4 E4M3 bytes.
+__device__ __forceinline__ void encode32(const float (&v)[32], float s, uint32_t (&out)[8]) {
 #pragma unroll
   for (int q4 = 0; q4 < 8; ++q4)
-    out[q4] = pack_e4m3x4(ldexp_f(v[4 * q4], -e), ldexp_f(v[4 * q4 + 1], -e), ldexp_f(v[4 * q4 + 2], -e),
-                          ldexp_f(v[4 * q4 + 3], -e));
+    out[q4] = pack_e4m3x4(v[4 * q4] * s, v[4 * q4 + 1] * s, v[4 * q4 + 2] * s, v[4 * q4 + 3] * s);
 }
 
 // Store 32 codes (keys 32b..32b+31) of row r into a 128B-swizzled [128][128] tile.
@@ -172,7 +170,6 @@ __device__ __forceinline__ void store_row_block(uint8_t* tile, int r, int b, con
   *reinterpret_cast<uint4*>(tile + sw128_off(r, 2 * b)) = make_uint4(w[0], w[1], w[2], w[3]);
   *reinterpret_cast<uint4*>(tile + sw128_off(r, 2 * b + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
 }
-
 
 // Store 32 fp32 values (times f) of one row at out + off, in the output dtype.
 template <bool OUT_BF16>
@@ -197,6 +194,14 @@ __device__ __forceinline__ void store_row32(void* out, size_t off, const uint32_
       d4[c4] = make_float4(__uint_as_float(rr[4 * c4]) * f, __uint_as_float(rr[4 * c4 + 1]) * f,
                            __uint_as_float(rr[4 * c4 + 2]) * f, __uint_as_float(rr[4 * c4 + 3]) * f);
   }
+}
+
+// Store 32 fp32 values of row r into one 128B-swizzled [128 rows][32 fp32] box.
+__device__ __forceinline__ void store_row_box(float* box, int r, const uint32_t (&rr)[32]) {
+  uint8_t* b = reinterpret_cast<uint8_t*>(box);
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4*>(b + sw128_off(r, c)) = make_uint4(rr[4 * c], rr[4 * c + 1], rr[4 * c + 2], rr[4 * c + 3]);
 }
 
 // Per-row values the backward needs for query row i of head h.
@@ -228,7 +233,7 @@ __device__ __forceinline__ uint32_t dq_operand(const float (&dsv)[32], float ama
                                                uint32_t (&codes)[8], int& e_blk) {
   if constexpr (!EXACT) {
     e_blk = noclamp_exp_clamped(warp_max(amax_ds));
-    encode32(dsv, e_blk, codes);
+    encode32(dsv, inv_pow2(e_blk), codes);
     return sf_byte(e_blk + ekb);
   } else {
     float f[32];
@@ -239,24 +244,29 @@ __device__ __forceinline__ uint32_t dq_operand(const float (&dsv)[32], float ama
       am = fmaxf(am, fabsf(f[jj]));
     }
     const int e = noclamp_exp_clamped(am);
-    encode32(f, e, codes);
+    encode32(f, inv_pow2(e), codes);
     e_blk = 0;
     return sf_byte(e);
   }
 }
 
 // ============================================================================
-// dK/dV kernel (and dQ by fp32 reductions when DQ): one CTA per (document,
-// 128-key tile, KV head), looping over the group's query heads and tiles.
+// dK/dV kernel (and dQ when DQ): one CTA per (document, 128-key tile, KV
+// head), looping over the group's query heads and tiles.  With DQ, each query
+// tile's dQ = dS^ K^ lands in TMEM, is staged in shared memory by the compute
+// warps and added to the fp32 dQ buffer by the reducer warp with bulk tensor
+// reduce-adds (whole 128-byte lines, the addition done in L2).
 // ============================================================================
 template <int HD, bool OUT_BF16, bool EXACT, bool DQ>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do) {
+               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+               const __grid_constant__ CUtensorMap map_dq) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  BwdTiles<HD>& tl = *reinterpret_cast<BwdTiles<HD>*>(base);
-  BwdCtl& c = *reinterpret_cast<BwdCtl*>(base + sizeof(BwdTiles<HD>));
+  using Tiles = BwdTiles<HD, EXACT, DQ>;
+  Tiles& tl = *reinterpret_cast<Tiles*>(base);
+  BwdCtl& c = *reinterpret_cast<BwdCtl*>(base + sizeof(Tiles));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.H / p.Hkv;
   const int n_work = p.hdr->n_items * p.Hkv;
@@ -278,6 +288,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&c.acc_full, 1);
     mbar_init(&c.acc_free, kBwdCompute);
     mbar_init(&c.xch_bar, kBwdCompute);
+    mbar_init(&c.dqs_full, kBwdCompute);
+    mbar_init(&c.dqs_free, 1);
     c.abort_flag = 0;
     fence_mbar_init();
   }
@@ -287,6 +299,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     prefetch_tensormap(&map_k);
     prefetch_tensormap(&map_v);
     prefetch_tensormap(&map_do);
+    if (DQ) prefetch_tensormap(&map_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -402,12 +415,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
     __syncwarp();
+  } else if (warp == kWarpRed) {
+    // ------------------------------------------------------------ dQ reducer
+    if (DQ && lane == 0) {
+      uint32_t ii = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+        const int pair = w / p.Hkv, hk = w - pair * p.Hkv;
+        const int2 it = p.bwd_items[pair];
+        const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
+        const int n_t = (len + kTile - 1) / kTile, q_first = p.causal ? it.y : 0;
+        for (int g = 0; ok && g < G; ++g) {
+          const int h = hk * G + g;
+          for (int qt = q_first; qt < n_t; ++qt, ++ii) {
+            if (!(ok = mbar_wait(&c.dqs_full, ii & 1, abort_flag, hdr, 0x331))) break;
+#pragma unroll
+            for (int cb = 0; cb < HD / 32; ++cb)
+              tma_reduce_add_3d(&map_dq, tl.dqs + cb * (kTile * 32), 32 * cb, h, ds + kTile * qt);
+            bulk_commit_group();
+            bulk_wait_group_read0();
+            mbar_arrive(&c.dqs_free);
+          }
+        }
+      }
+      bulk_wait_group0();
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ compute warps
     const int q = warp & 3, hf = warp >> 2;  // lane quarter (query rows), key-block half
     const int r = 32 * q + lane;             // query row of the tile = TMEM lane
     const int b0 = 2 * hf;                   // first of this thread's two key blocks
     constexpr int HC = HD / 2;               // output columns drained by this thread
+    uint8_t* const dbg_c = hdr->dbg_phat;
+    int32_t* const dbg_e = hdr->dbg_eb;
     uint32_t ic = 0, ii = 0;
     bool ok = true;
     const float sm_scale = p.softmax_scale;
@@ -428,29 +469,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const RowStage rv = c.rows[qs][r];
           if (!(ok = mbar_wait_warp(&c.s_full, ii & 1, abort_flag, hdr, 0x322))) break;
           tc_fence_after();
-          uint32_t pcode[16];
+          uint32_t pcode[2][8];
           int Eb[2];
           // the diagonal tile (and a document's last key tile) needs the mask
           const bool need_mask = p.causal ? (qt == it.y) : (it.y == n_t - 1);
-          recompute_phat<EXACT, 2>(taddr(tb, q * 32, kColX0), b0, rv.rowc, c.kf, c.vf, i_loc, key0, len, p.causal,
-                                   need_mask, row_ok, pcode, Eb);
-          if (row_ok) dbg_dump_phat2(hdr, p.T, h, ds + i_loc, ds + key0, b0, pcode, Eb);
+          recompute_phat<EXACT>(taddr(tb, q * 32, kColX0), b0, rv.rowc, c.kf, c.vf, i_loc, key0, len, p.causal,
+                                need_mask, row_ok, pcode, Eb);
+          if (row_ok) dbg_dump_phat2(dbg_c, dbg_e, p.T, h, ds + i_loc, ds + key0, b0, pcode, Eb);
           if (!(ok = mbar_wait_warp(&c.dp_full, ii & 1, abort_flag, hdr, 0x323))) break;
           // the previous iteration's MMAs must be done with the P~ / dS tiles
           if (ii > 0 && !(ok = mbar_wait_warp(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x326))) break;
           tc_fence_after();
           const int par = ii & 1;
+          uint32_t dp[2][32];
+          tmem_ld32(taddr(tb, q * 32, kColX1 + 32 * b0), dp[0]);
+          tmem_ld32(taddr(tb, q * 32, kColX1 + 32 * (b0 + 1)), dp[1]);
+          tmem_ld_wait_regs(dp[0], dp[1]);
+          if constexpr (!DQ) {  // dP has been read: X1 may take the next dP
+            tc_fence_before();
+            mbar_arrive(&c.x1_free);
+          }
 #pragma unroll
           for (int bb = 0; bb < 2; ++bb) {
             const int b = b0 + bb;
             float dsv[32], ptv[32];
             float amax_ds, amax_pt;
-            ds_block(taddr(tb, q * 32, kColX1 + 32 * b), pcode + 8 * bb, Eb[bb], rv.mi, rv.inv_l, rv.hdo, rv.Di,
-                     c.vinv + 32 * b, row_ok, dsv, ptv, amax_ds, amax_pt);
+            ds_block(dp[bb], pcode[bb], ds_factors(Eb[bb], rv.mi, rv.inv_l, rv.hdo, rv.Di), c.vinv + 32 * b, dsv,
+                     ptv, amax_ds, amax_pt);
             // P~: 32 x 32 block (this warp's 32 queries x key block b)
             const int e_pt = noclamp_exp_clamped(warp_max(amax_pt));
             uint32_t codes[8];
-            encode32(ptv, e_pt, codes);
+            encode32(ptv, inv_pow2(e_pt), codes);
             store_row_block(tl.pt, r, b, codes);
             uint32_t kbyte, qbyte = 0;
             if constexpr (!EXACT) {
@@ -470,7 +519,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
               for (int jj = 0; jj < 32; ++jj) f[jj] = dsv[jj] * feq;
               const int e_k = noclamp_exp_clamped(warp_max(amax_ds * feq));
-              encode32(f, e_k, codes);
+              encode32(f, inv_pow2(e_k), codes);
               store_row_block(tl.dsk, r, b, codes);
               kbyte = sf_byte(e_k);
             }
@@ -479,10 +528,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               c.xch[par][0][q][b] = (uint8_t)sf_byte(e_pt);
               c.xch[par][1][q][b] = (uint8_t)kbyte;
             }
-          }
-          if constexpr (!DQ) {  // dP has been read: X1 may take the next dP
-            tc_fence_before();
-            mbar_arrive(&c.x1_free);
           }
           // exchange the block exponents among the compute warps (an mbarrier
           // with a bounded wait, so an aborting warp cannot strand the others)
@@ -509,25 +554,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_before();
           mbar_arrive(&c.ds_full);
           if constexpr (DQ) {
-            // ---- dQ tile -> fp32 buffer (this thread: its row, half of the columns)
+            // ---- dQ tile -> staging boxes (this thread: its row, half of the
+            // columns).  Rows outside the document hold exact zeros (their dS
+            // row is zero), so the whole 128-row box is added.
             if (!(ok = mbar_wait_warp(&c.mm_done, ii & 1, abort_flag, hdr, 0x324))) break;
             tc_fence_after();
-            float* dst = p.dq_acc + ((size_t)(ds + i_loc) * p.H + h) * HD + hf * HC;
-#pragma unroll
-            for (int cb = 0; cb < HC / 32; ++cb) {
-              uint32_t rr[32];
-              tmem_ld32(taddr(tb, q * 32, kColX1 + hf * HC + 32 * cb), rr);
-              tmem_ld_wait();
-              if (row_ok) {
-#pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                  red_add_v4(dst + 32 * cb + e, __uint_as_float(rr[e]) * sm_scale,
-                             __uint_as_float(rr[e + 1]) * sm_scale, __uint_as_float(rr[e + 2]) * sm_scale,
-                             __uint_as_float(rr[e + 3]) * sm_scale);
-              }
+            uint32_t rq[2][32];
+            tmem_ld32(taddr(tb, q * 32, kColX1 + hf * HC), rq[0]);
+            if constexpr (HC == 64) {
+              tmem_ld32(taddr(tb, q * 32, kColX1 + hf * HC + 32), rq[1]);
+              tmem_ld_wait_regs(rq[0], rq[1]);
+            } else {
+              tmem_ld_wait_regs(rq[0]);
             }
             tc_fence_before();
             mbar_arrive(&c.x1_free);
+            if (!(ok = mbar_wait_warp(&c.dqs_free, (ii & 1) ^ 1, abort_flag, hdr, 0x329))) break;
+#pragma unroll
+            for (int cbl = 0; cbl < HC / 32; ++cbl)
+              store_row_box(tl.dqs + (hf * (HC / 32) + cbl) * (kTile * 32), r, rq[cbl]);
+            fence_proxy_async_smem();
+            mbar_arrive(&c.dqs_full);
           }
         }
       }
@@ -548,7 +595,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int cb = 0; cb < HC / 32; ++cb) {
           uint32_t rr[32];
           tmem_ld32(taddr(tb, q * 32, col + 32 * cb), rr);
-          tmem_ld_wait();
+          tmem_ld_wait_regs(rr);
           if (key_ok) store_row32<OUT_BF16>(outp, koff + 32 * cb, rr, f);
         }
       }
@@ -569,6 +616,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // with the same functions as the dK/dV kernel.
 // ============================================================================
 constexpr int kDqStages = 2;
+constexpr int kDqThreads = kBwdCompute + 64;  // compute warps 0-7, producer 8, MMA 9
 constexpr uint32_t kDqColAcc = 0, kDqColX0 = 128, kDqColX1 = 256;
 constexpr uint32_t kDqColSf = kDqColX0 + 0, kDqColSfOne = kDqColX0 + 4;
 
@@ -597,7 +645,7 @@ constexpr size_t dq_smem_bytes() {
 }
 
 template <int HD, bool OUT_BF16, bool EXACT>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
     dq_kernel(const AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do) {
   extern __shared__ uint8_t smem_raw[];
@@ -739,21 +787,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!(ok = mbar_wait_warp(&c.kv_full[st], ph, abort_flag, hdr, 0x421))) break;
         if (!(ok = mbar_wait_warp(&c.s_full, ii & 1, abort_flag, hdr, 0x422))) break;
         tc_fence_after();
-        uint32_t pcode[16];
+        uint32_t pcode[2][8];
         int Eb[2];
-        recompute_phat<EXACT, 2>(taddr(tb, q * 32, kDqColX0), b0, rv.rowc, c.kf[st], c.vf[st], i_loc, kTile * kt,
-                                 len, p.causal, kt == n_kt - 1, row_ok, pcode, Eb);
+        recompute_phat<EXACT>(taddr(tb, q * 32, kDqColX0), b0, rv.rowc, c.kf[st], c.vf[st], i_loc, kTile * kt, len,
+                              p.causal, kt == n_kt - 1, row_ok, pcode, Eb);
         if (!(ok = mbar_wait_warp(&c.dp_full, ii & 1, abort_flag, hdr, 0x423))) break;
         if (ii > 0 && !(ok = mbar_wait_warp(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x424))) break;
         tc_fence_after();
         const int par = ii & 1;
+        uint32_t dp[2][32];
+        tmem_ld32(taddr(tb, q * 32, kDqColX1 + 32 * b0), dp[0]);
+        tmem_ld32(taddr(tb, q * 32, kDqColX1 + 32 * (b0 + 1)), dp[1]);
+        tmem_ld_wait_regs(dp[0], dp[1]);
 #pragma unroll
         for (int bb = 0; bb < 2; ++bb) {
           const int b = b0 + bb;
           float dsv[32], ptv[32];
           float amax_ds, amax_pt;
-          ds_block(taddr(tb, q * 32, kDqColX1 + 32 * b), pcode + 8 * bb, Eb[bb], rv.mi, inv_l, rv.hdo, rv.Di,
-                   c.vinv[st] + 32 * b, row_ok, dsv, ptv, amax_ds, amax_pt);
+          ds_block(dp[bb], pcode[bb], ds_factors(Eb[bb], rv.mi, inv_l, rv.hdo, rv.Di), c.vinv[st] + 32 * b, dsv, ptv,
+                   amax_ds, amax_pt);
           uint32_t codes[8];
           int e_blk;
           c.xdq[par][r][b] =
@@ -783,7 +835,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int cb = 0; cb < HC / 32; ++cb) {
         uint32_t rr[32];
         tmem_ld32(taddr(tb, q * 32, kDqColAcc + hf * HC + 32 * cb), rr);
-        tmem_ld_wait();
+        tmem_ld_wait_regs(rr);
         if (row_ok) store_row32<OUT_BF16>(p.dQ, off + 32 * cb, rr, p.softmax_scale);
       }
       tc_fence_before();
@@ -796,11 +848,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == kWarpMma) tmem_dealloc(tb, 512);
 }
 
-// dQ buffer (fp32, already scaled) -> output dtype.
+// dQ buffer (fp32 sums of dS^ K^) times the softmax scale -> output dtype.
 template <bool OUT_BF16>
-__global__ void dq_convert_kernel(const float* __restrict__ acc, void* out, size_t n4) {
+__global__ void dq_convert_kernel(const float* __restrict__ acc, void* out, size_t n4, float scale) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-    const float4 v = reinterpret_cast<const float4*>(acc)[i];
+    float4 v = reinterpret_cast<const float4*>(acc)[i];
+    v.x *= scale;
+    v.y *= scale;
+    v.z *= scale;
+    v.w *= scale;
     if constexpr (OUT_BF16) {
       __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
       uint2 u = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
@@ -822,30 +878,32 @@ template <int HD, bool OB, bool EX>
 static cudaError_t launch_bwd_t(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
   const bool det = p.exact || p.deterministic;
   const int nsm = sm_count();
-  const size_t smem = bwd_smem_bytes<HD>();
   long work = (long)p.max_items * p.Hkv;
   int grid = (int)(work < nsm ? work : nsm);
   cudaError_t e;
   if (!det) {
+    const size_t smem = bwd_smem_bytes<HD, EX, true>();
     if ((e = set_smem(bwd_kernel<HD, OB, EX, true>, smem)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(p.dq_acc, 0, sizeof(float) * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
-    bwd_kernel<HD, OB, EX, true><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO);
+    bwd_kernel<HD, OB, EX, true><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.dq);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t n4 = (size_t)p.T * p.H * HD / 4;
     int cg = (int)((n4 + 255) / 256);
     if (cg > nsm * 8) cg = nsm * 8;
-    if (OB) dq_convert_kernel<true><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4);
-    else dq_convert_kernel<false><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4);
+    if (OB) dq_convert_kernel<true><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4, p.softmax_scale);
+    else dq_convert_kernel<false><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4, p.softmax_scale);
     return cudaGetLastError();
   }
+  const size_t smem = bwd_smem_bytes<HD, EX, false>();
   if ((e = set_smem(bwd_kernel<HD, OB, EX, false>, smem)) != cudaSuccess) return e;
-  bwd_kernel<HD, OB, EX, false><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO);
+  // without DQ the dQ map is not read (the q map stands in for the argument)
+  bwd_kernel<HD, OB, EX, false><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.q);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t dsm = dq_smem_bytes<HD>();
   if ((e = set_smem(dq_kernel<HD, OB, EX>, dsm)) != cudaSuccess) return e;
   long dwork = (long)p.max_items * p.H;
   int dgrid = (int)(dwork < nsm ? dwork : nsm);
-  dq_kernel<HD, OB, EX><<<dgrid, kBwdThreads, dsm, st>>>(p, m.q, m.k, m.v, m.dO);
+  dq_kernel<HD, OB, EX><<<dgrid, kDqThreads, dsm, st>>>(p, m.q, m.k, m.v, m.dO);
   return cudaGetLastError();
 }
 

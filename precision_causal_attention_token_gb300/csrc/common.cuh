@@ -30,35 +30,19 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header");
 
 // Test hook: record one row's P^ codes and block exponents for two 32-key
-// blocks (b0, b0 + 1) of a 128-key tile.
-__device__ __forceinline__ void dbg_dump_phat2(const WsHeader* hdr, int T, int h, int tok, int key_tok0, int b0,
-                                               const uint32_t (&codes)[16], const int (&Eb)[2]) {
-  uint8_t* dc = hdr->dbg_phat;
+// blocks (b0, b0 + 1) of a 128-key tile.  `dc`/`de` are the header's hook
+// pointers, read once per kernel (null: off).
+__device__ __forceinline__ void dbg_dump_phat2(uint8_t* dc, int32_t* de, int T, int h, int tok, int key_tok0,
+                                               int b0, const uint32_t (&codes)[2][8], const int (&Eb)[2]) {
   if (dc == nullptr) return;
-  int32_t* de = hdr->dbg_eb;
   const size_t row = ((size_t)h * T + tok) * (size_t)T;
   const int k0 = key_tok0 + 32 * b0;
 #pragma unroll
   for (int j = 0; j < 64; ++j)
-    if (k0 + j < T) dc[row + k0 + j] = (uint8_t)(codes[j >> 2] >> (8 * (j & 3)));
+    if (k0 + j < T) dc[row + k0 + j] = (uint8_t)(codes[j >> 5][(j >> 2) & 7] >> (8 * (j & 3)));
 #pragma unroll
   for (int b = 0; b < 2; ++b)
     if (k0 + 32 * b < T) de[row + k0 + 32 * b] = Eb[b];
-}
-
-// Test hook: record one row's P^ codes and block exponents for a 128-key tile.
-__device__ __forceinline__ void dbg_dump_phat(const WsHeader* hdr, int T, int h, int tok, int key_tok0,
-                                              const uint32_t (&codes)[32], const int (&Eb)[4]) {
-  uint8_t* dc = hdr->dbg_phat;
-  if (dc == nullptr) return;
-  int32_t* de = hdr->dbg_eb;
-  const size_t row = ((size_t)h * T + tok) * (size_t)T;
-#pragma unroll
-  for (int j = 0; j < 128; ++j)
-    if (key_tok0 + j < T) dc[row + key_tok0 + j] = (uint8_t)(codes[j >> 2] >> (8 * (j & 3)));
-#pragma unroll
-  for (int b = 0; b < 4; ++b)
-    if (key_tok0 + 32 * b < T) de[row + key_tok0 + 32 * b] = Eb[b];
 }
 
 struct WsLayout {
@@ -232,6 +216,22 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
         "r"(smem_u32(bar))
       : "memory");
 }
+// Element-wise add of a shared-memory box into global memory through a tensor
+// map (the reduction happens in L2); completion is tracked by bulk groups.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* smem_src, int c0, int c1,
+                                                  int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the shared-memory sources of every committed bulk group have been read.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until every committed bulk group has completed.
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -334,6 +334,32 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// The wait, with the loaded registers passed through it so that no use of
+// them can be scheduled before the loads have landed.
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&a)[32], uint32_t (&b)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+        "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]),
+        "+r"(a[16]), "+r"(a[17]), "+r"(a[18]), "+r"(a[19]), "+r"(a[20]), "+r"(a[21]), "+r"(a[22]), "+r"(a[23]),
+        "+r"(a[24]), "+r"(a[25]), "+r"(a[26]), "+r"(a[27]), "+r"(a[28]), "+r"(a[29]), "+r"(a[30]), "+r"(a[31]),
+        "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]),
+        "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15]),
+        "+r"(b[16]), "+r"(b[17]), "+r"(b[18]), "+r"(b[19]), "+r"(b[20]), "+r"(b[21]), "+r"(b[22]), "+r"(b[23]),
+        "+r"(b[24]), "+r"(b[25]), "+r"(b[26]), "+r"(b[27]), "+r"(b[28]), "+r"(b[29]), "+r"(b[30]), "+r"(b[31])
+      :
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&a)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+        "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]),
+        "+r"(a[16]), "+r"(a[17]), "+r"(a[18]), "+r"(a[19]), "+r"(a[20]), "+r"(a[21]), "+r"(a[22]), "+r"(a[23]),
+        "+r"(a[24]), "+r"(a[25]), "+r"(a[26]), "+r"(a[27]), "+r"(a[28]), "+r"(a[29]), "+r"(a[30]), "+r"(a[31])
+      :
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t a, uint32_t b) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(a), "r"(b) : "memory");
 }

@@ -47,7 +47,8 @@ struct FwdCtl {
   float vinv[kFwdStages][kTile];  // 2^-eV(j)
   uint64_t q_full, q_empty;
   uint64_t k_full[kFwdStages], k_empty[kFwdStages], v_full[kFwdStages], v_empty[kFwdStages];
-  uint64_t s_full[2], s_free[2], p_full[2], p_free[2], o_full, o_free, eb_bar, l_bar;
+  uint64_t s_full[2], s_free[2], p_full[2], p_free[2], o_full, o_free;
+  uint64_t eb_bar[4], l_bar[4];  // per TMEM lane quarter: the two warps that share its rows
   int ebx[2][kTile][4];  // [tile parity][row][key block] P^ block exponents, shared by a row's two threads
   float lx[kTile][2];    // [row][half] partial normalisers for the epilogue
   uint32_t tmem_base;
@@ -99,8 +100,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     mbar_init(&c.o_full, 1);
     mbar_init(&c.o_free, kFwdSoftmax);
-    mbar_init(&c.eb_bar, kFwdSoftmax);
-    mbar_init(&c.l_bar, kFwdSoftmax);
+    for (int qq = 0; qq < 4; ++qq) {
+      mbar_init(&c.eb_bar[qq], 64);
+      mbar_init(&c.l_bar[qq], 64);
+    }
     c.abort_flag = 0;
     fence_mbar_init();
   }
@@ -229,6 +232,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int r = 32 * q + lane;             // query row of the tile = TMEM lane
     const int b0 = 2 * hf;                   // first of this thread's two key blocks
     constexpr int HC = HD / 2;               // O columns handled by this thread
+    uint8_t* const dbg_c = hdr->dbg_phat;
+    int32_t* const dbg_e = hdr->dbg_eb;
     uint32_t kv = 0, sc = 0, pc = 0, ic = 0;
     bool ok = true;
     for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
@@ -254,32 +259,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const bool need_mask = (kt == n_kt - 1);  // diagonal tile, or a document's last tile
         int Eb[2];
         float lb[2];
-        uint32_t codes[16];
+        uint32_t codes[2][8];
+        {
+          float y[2][32];
+          const uint32_t t0 = taddr(tb, q * 32, (sb ? kColS1 : kColS0) + 32 * b0), t1 = t0 + 32;
+          const float* kfb = c.kf[st] + 32 * b0;
+          const float* vfb = c.vf[st] + 32 * b0;
+          if (need_mask)
+            phat_logits2<EXACT, true>(t0, t1, y, Eb, rowc, kfb, vfb, i_loc, key0 + 32 * b0, len, p.causal);
+          else
+            phat_logits2<EXACT, false>(t0, t1, y, Eb, rowc, kfb, vfb, i_loc, key0 + 32 * b0, len, p.causal);
 #pragma unroll
-        for (int bb = 0; bb < 2; ++bb) {
-          const int b = b0 + bb;
-          float a[32];
-          {
-            uint32_t rr[32];
-            tmem_ld32(taddr(tb, q * 32, (sb ? kColS1 : kColS0) + 32 * b), rr);
-            tmem_ld_wait();
+          for (int bb = 0; bb < 2; ++bb) {
+            const float* vi = c.vinv[st] + 32 * (b0 + bb);
+            float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(rr[j]);
-          }
-          Eb[bb] = phat_block_logits<EXACT>(a, rowc, c.kf[st] + 32 * b, c.vf[st] + 32 * b, need_mask, i_loc,
-                                            key0 + 32 * b, len, p.causal);
-          float l4[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const float4 v4 = *reinterpret_cast<const float4*>(vi + 4 * q4);
+              const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+              float pv[4];
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            float pv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              pv[e] = (Eb[bb] == kEmptyBlock) ? 0.f : phat_value(a[4 * q4 + e], Eb[bb]);
-              l4[e] = fmaf(pv[e], c.vinv[st][32 * b + 4 * q4 + e], l4[e]);
+              for (int e = 0; e < 4; ++e) {
+                pv[e] = (Eb[bb] == kEmptyBlock) ? 0.f : phat_value(y[bb][4 * q4 + e], Eb[bb]);
+                l4[e] = fmaf(pv[e], vv[e], l4[e]);
+              }
+              codes[bb][q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
             }
-            codes[8 * bb + q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
+            lb[bb] = (l4[0] + l4[1]) + (l4[2] + l4[3]);
           }
-          lb[bb] = (l4[0] + l4[1]) + (l4[2] + l4[3]);
         }
         tc_fence_before();
         mbar_arrive(&c.s_free[sb]);
@@ -288,8 +295,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int par = sc & 1;
         c.ebx[par][r][b0] = Eb[0];
         c.ebx[par][r][b0 + 1] = Eb[1];
-        mbar_arrive(&c.eb_bar);
-        if (!(ok = mbar_wait_warp(&c.eb_bar, sc & 1, abort_flag, hdr, 0x226))) break;
+        mbar_arrive(&c.eb_bar[q]);
+        if (!(ok = mbar_wait_warp(&c.eb_bar[q], sc & 1, abort_flag, hdr, 0x226))) break;
         int Eall[4];
 #pragma unroll
         for (int b = 0; b < 4; ++b) Eall[b] = c.ebx[par][r][b];
@@ -305,7 +312,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int b = 0; b < 4; ++b)
           if (Eall[b] != kEmptyBlock) word |= (uint32_t)min(max(Eall[b] - m_new + 127, 0), 254) << (8 * b);
         mbar_arrive(&c.k_empty[st]);
-        if (row_ok) dbg_dump_phat2(hdr, p.T, h, q0 + r, ds + key0, b0, codes, Eb);
+        if (row_ok) dbg_dump_phat2(dbg_c, dbg_e, p.T, h, q0 + r, ds + key0, b0, codes, Eb);
         l_run = (m_ref == kEmptyBlock) ? lsum : ldexp_f(l_run, m_ref - m_new) + lsum;
         // rescale this thread's half of the O accumulator row once the previous
         // P^V has landed (warp-uniform: tcgen05.ld/st are warp-collective; lanes
@@ -319,7 +326,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int cb = 0; cb < HC / 32; ++cb) {
             uint32_t rr[32];
             tmem_ld32(taddr(tb, q * 32, kColO + hf * HC + 32 * cb), rr);
-            tmem_ld_wait();
+            tmem_ld_wait_regs(rr);
 #pragma unroll
             for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * f);
             tmem_st32(taddr(tb, q * 32, kColO + hf * HC + 32 * cb), rr);
@@ -332,7 +339,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         uint8_t* prow = tl.p[pb];
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
-          uint4 v4 = make_uint4(codes[4 * ch], codes[4 * ch + 1], codes[4 * ch + 2], codes[4 * ch + 3]);
+          uint4 v4 = make_uint4(codes[ch >> 1][4 * (ch & 1)], codes[ch >> 1][4 * (ch & 1) + 1],
+                                codes[ch >> 1][4 * (ch & 1) + 2], codes[ch >> 1][4 * (ch & 1) + 3]);
           *reinterpret_cast<uint4*>(prow + sw128_off(r, 4 * hf + ch)) = v4;
         }
         // the row's scale word goes to all four columns (two per thread)
@@ -351,15 +359,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int cb = 0; cb < HC / 32; ++cb) {
         uint32_t rr[32];
         tmem_ld32(taddr(tb, q * 32, kColO + hf * HC + 32 * cb), rr);
-        tmem_ld_wait();
+        tmem_ld_wait_regs(rr);
 #pragma unroll
         for (int j = 0; j < 32; ++j) o[32 * cb + j] = __uint_as_float(rr[j]);
       }
       tc_fence_before();
       mbar_arrive(&c.o_free);
       c.lx[r][hf] = l_run;
-      mbar_arrive(&c.l_bar);
-      if (!(ok = mbar_wait_warp(&c.l_bar, ic & 1, abort_flag, hdr, 0x227))) break;
+      mbar_arrive(&c.l_bar[q]);
+      if (!(ok = mbar_wait_warp(&c.l_bar[q], ic & 1, abort_flag, hdr, 0x227))) break;
       const float l_tot = c.lx[r][0] + c.lx[r][1];
       if (row_ok) {
         const float inv = 1.0f / l_tot;

@@ -17,9 +17,16 @@ struct QuantArgs {
   int per_token;
 };
 
-cudaError_t launch_quantize(const QuantArgs& a, int d, int in_bf16, int o_bf16, bool with_D, bool nvfp4,
+// Up to three tensors quantized by one launch (Q, K, V; or dO alone).
+struct QuantBatch {
+  QuantArgs a[3];
+  int n;
+};
+
+cudaError_t launch_quantize(const QuantBatch& qb, int d, int in_bf16, int o_bf16, bool with_D, bool nvfp4,
                             const int32_t* cu, const int32_t* blk_prefix, int n_seq, WsHeader* hdr, int max_units,
-                            cudaStream_t st);
+                            int n_sms, cudaStream_t st);
+int sm_count();
 cudaError_t launch_plan(const flamia_problem_t& p, const WsLayout& L, uint8_t* ws, cudaStream_t st);
 
 // Everything the attention kernels need for one call (host-built).
@@ -48,6 +55,7 @@ struct AttnParams {
 
 struct AttnMaps {
   CUtensorMap q, k, v, dO;
+  CUtensorMap dq;  // fp32 dQ accumulator [T][H][d], boxes of 128 rows x 32 values (reduce-add target)
 };
 
 cudaError_t launch_fwd(const AttnParams& p, const AttnMaps& maps, cudaStream_t st);

@@ -7,11 +7,15 @@
 // valid in both MMA orientations; §3.2 Causally Safe Scales: the exponent is
 // rounded up so no element clamps; §3.6.2: blocks are document-local and the
 // scale is stored per token; §3.3: D comes from the same quantized dO as dP.
-// Close reading 4.4: a single fused launch produces codes and scales.
+// Close reading 4.4: a single fused launch produces codes and scales (here one
+// launch covers Q, K and V together).
 //
 // One warp handles one (document-local 32-token block, head) unit: lane l
 // holds elements [l*EPL, l*EPL + EPL) of each of the block's tokens (EPL =
-// d/32), so every token row is read and written as one contiguous segment.
+// d/32), so every token row is read with one vector load per lane (256 or 512
+// contiguous bytes per warp) and written as one contiguous 128-byte segment.
+// The block is kept as raw input words (bf16 pairs stay packed); three
+// blocks of 128 threads fit on an SM, each warp with 32 loads in flight.
 #include "kernels.h"
 
 namespace flamia {
@@ -47,143 +51,183 @@ __device__ __forceinline__ uint32_t e4m3_roundup(float r) {
   return c > 0x7Eu ? 0x7Eu : c;
 }
 
+// One lane's EPL input elements of one token, as raw 32-bit words, and their
+// fp32 values.  bf16 -> fp32 is exact (the bf16 bits are the high half).
+template <typename T, int EPL>
+struct RawRow {
+  static constexpr int kWords = (int)sizeof(T) * EPL / 4;
+  uint32_t w[kWords];
+  __device__ __forceinline__ void load(const T* p) {
+    if constexpr (kWords == 4) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+      w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+    } else if constexpr (kWords == 2) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+      w[0] = u.x; w[1] = u.y;
+    } else {
+      w[0] = __ldg(reinterpret_cast<const uint32_t*>(p));
+    }
+  }
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int i = 0; i < kWords; ++i) w[i] = 0u;
+  }
+  __device__ __forceinline__ float at(int e) const {
+    if constexpr (sizeof(T) == 4) return __uint_as_float(w[e]);
+    else return __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
+  }
+};
+
+// Quantize one (32-token block g, head h) unit of one tensor.
 template <typename TIn, typename TO, int HD, bool WITH_D, bool NVFP4>
-__global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a, const int32_t* __restrict__ cu,
-                                                       const int32_t* __restrict__ blk_prefix, int n_seq,
-                                                       WsHeader* hdr) {
+__device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, const int32_t* __restrict__ cu,
+                                              const int32_t* __restrict__ blk_prefix, int n_seq, int lane) {
   constexpr int EPL = HD / 32;  // elements per lane: 4 (d=128) or 2 (d=64)
-  const int lane = threadIdx.x & 31;
-  const int warps_total = gridDim.x * (blockDim.x >> 5);
-  const int n_units = hdr->n_blk32 * a.heads;
   const TIn* __restrict__ x = static_cast<const TIn*>(a.x);
   const size_t row = (size_t)a.heads * HD;  // elements between consecutive tokens
+  // document of block g: last doc with blk_prefix[doc] <= g
+  int lo = 0, hi = n_seq;  // blk_prefix[lo] <= g < blk_prefix[hi]
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (__ldg(blk_prefix + mid) <= g) lo = mid; else hi = mid;
+  }
+  const int doc_start = __ldg(cu + lo), doc_end = __ldg(cu + lo + 1);
+  const int t0 = doc_start + 32 * (g - __ldg(blk_prefix + lo));
+  const int ntok = min(32, doc_end - t0);
 
-  for (int unit = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); unit < n_units; unit += warps_total) {
-    const int g = unit / a.heads, h = unit - g * a.heads;
-    // document of block g: last doc with blk_prefix[doc] <= g
-    int lo = 0, hi = n_seq;  // blk_prefix[lo] <= g < blk_prefix[hi]
-    while (hi - lo > 1) {
-      int mid = (lo + hi) >> 1;
-      if (__ldg(blk_prefix + mid) <= g) lo = mid; else hi = mid;
-    }
-    const int doc_start = __ldg(cu + lo), doc_end = __ldg(cu + lo + 1);
-    const int t0 = doc_start + 32 * (g - __ldg(blk_prefix + lo));
-    const int ntok = min(32, doc_end - t0);
+  RawRow<TIn, EPL> raw[32];
+#pragma unroll
+  for (int t = 0; t < 32; ++t) {
+    if (t < ntok) raw[t].load(x + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL);
+    else raw[t].zero();
+  }
+  // per-token maxima (lane t <- token t) also feed the NVFP4 token scale
+  float pmax[32];
+#pragma unroll
+  for (int t = 0; t < 32; ++t) {
+    float m = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) m = fmaxf(m, fabsf(raw[t].at(e)));
+    pmax[t] = m;
+  }
+  float tok_amax_arr[32];
+#pragma unroll
+  for (int t = 0; t < 32; ++t) tok_amax_arr[t] = pmax[t];
+  const float my_tok_amax = transpose_reduce<true>(tok_amax_arr, lane);
+  int my_e;  // exponent of token `lane`
+  if (a.per_token) {
+    my_e = noclamp_exp_clamped(my_tok_amax);
+  } else {
+    float bmax = my_tok_amax;
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, s));
+    my_e = noclamp_exp_clamped(bmax);
+  }
+  if (lane < ntok) a.scales[(size_t)h * a.T + t0 + lane] = (uint8_t)(my_e + 127);
 
-    float v[32][EPL];
-    float pmax[32];
+  float dpart[32];
 #pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      pmax[t] = 0.f;
+  for (int t = 0; t < 32; ++t) {
+    dpart[t] = 0.f;
+    const int e_t = __shfl_sync(0xffffffffu, my_e, t);
+    if (t < ntok) {
+      float q[EPL];
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) v[t][e] = 0.f;
-      if (t < ntok) {
-        const TIn* p = x + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL;
+      for (int e = 0; e < EPL; ++e) q[e] = mul_pow2(raw[t].at(e), -e_t);
+      uint8_t* dst = a.codes + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL;
+      uint32_t cw;
+      if constexpr (EPL == 4) {
+        cw = pack_e4m3x4(q[0], q[1], q[2], q[3]);
+        *reinterpret_cast<uint32_t*>(dst) = cw;
+      } else {
+        cw = pack_e4m3x2(q[0], q[1]);
+        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)cw;
+      }
+      if constexpr (WITH_D) {
+        RawRow<TO, EPL> o;
+        o.load(static_cast<const TO*>(a.O) + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL);
+        float acc = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-          v[t][e] = to_f32(p[e]);
-          pmax[t] = fmaxf(pmax[t], fabsf(v[t][e]));
+        for (int e = 0; e < EPL; e += 2) {
+          const float2 d2 = unpack_e4m3x2((uint16_t)(cw >> (8 * e)));
+          acc = fmaf(mul_pow2(d2.x, e_t), o.at(e), acc);
+          acc = fmaf(mul_pow2(d2.y, e_t), o.at(e + 1), acc);
         }
+        dpart[t] = acc;
       }
     }
-    // per-token maxima (lane t <- token t) also feed the NVFP4 token scale
-    float tok_amax_arr[32];
-#pragma unroll
-    for (int t = 0; t < 32; ++t) tok_amax_arr[t] = pmax[t];
-    const float my_tok_amax = transpose_reduce<true>(tok_amax_arr, lane);
-    int my_e;  // exponent of token `lane`
-    if (a.per_token) {
-      my_e = noclamp_exp_clamped(my_tok_amax);
-    } else {
-      float bmax = my_tok_amax;
-#pragma unroll
-      for (int s = 16; s >= 1; s >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, s));
-      my_e = noclamp_exp_clamped(bmax);
-    }
-    if (lane < ntok) a.scales[(size_t)h * a.T + t0 + lane] = (uint8_t)(my_e + 127);
-
-    float dpart[32];
+  }
+  if constexpr (WITH_D) {
+    const float dsum = transpose_reduce<false>(dpart, lane);
+    if (lane < ntok) a.D[(size_t)h * a.T + t0 + lane] = dsum;
+  }
+  if constexpr (NVFP4) {
+    if (a.codes4 == nullptr) return;  // V has no NVFP4 operand
+    // NVFP4 operand for the mixed path's QK^T (FLAMIA summary §3.4, §3.2):
+    // per-token fp32 scale g = amax / (6 * 448), 16-element E4M3 block
+    // scales rounded up so nothing exceeds 6, E2M1 codes; IEEE fp32 ops.
+    constexpr int LPB = 16 / EPL;  // lanes per 16-element block
+    const float my_g = (my_tok_amax == 0.f) ? 1.f : __fdiv_rn(my_tok_amax, 2688.f);
+    if (lane < ntok) a.gscale4[(size_t)h * a.T + t0 + lane] = my_g;
 #pragma unroll
     for (int t = 0; t < 32; ++t) {
-      dpart[t] = 0.f;
-      const int e_t = __shfl_sync(0xffffffffu, my_e, t);
+      const float gs = __shfl_sync(0xffffffffu, my_g, t);
+      float bm = pmax[t];
+#pragma unroll
+      for (int s = 1; s < LPB; s <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, s));
       if (t < ntok) {
-        float q[EPL];
+        uint32_t sc = 0u;
+        if (bm > 0.f) sc = e4m3_roundup(__fdiv_rn(bm, __fmul_rn(6.f, gs)));
+        const float sg = __fmul_rn(unpack_e4m3x2((uint16_t)sc).x, gs);
+        uint32_t packed = 0u;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) q[e] = mul_pow2(v[t][e], -e_t);
-        uint8_t* dst = a.codes + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL;
-        if constexpr (EPL == 4) {
-          const uint32_t c4 = pack_e4m3x4(q[0], q[1], q[2], q[3]);
-          *reinterpret_cast<uint32_t*>(dst) = c4;
-          if constexpr (WITH_D) {
-            const TO* op = static_cast<const TO*>(a.O) + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL;
-            float2 d01 = unpack_e4m3x2((uint16_t)(c4 & 0xFFFFu));
-            float2 d23 = unpack_e4m3x2((uint16_t)(c4 >> 16));
-            float acc = mul_pow2(d01.x, e_t) * to_f32(op[0]);
-            acc = fmaf(mul_pow2(d01.y, e_t), to_f32(op[1]), acc);
-            acc = fmaf(mul_pow2(d23.x, e_t), to_f32(op[2]), acc);
-            acc = fmaf(mul_pow2(d23.y, e_t), to_f32(op[3]), acc);
-            dpart[t] = acc;
-          }
-        } else {
-          const uint16_t c2 = pack_e4m3x2(q[0], q[1]);
-          *reinterpret_cast<uint16_t*>(dst) = c2;
-          if constexpr (WITH_D) {
-            const TO* op = static_cast<const TO*>(a.O) + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL;
-            float2 d01 = unpack_e4m3x2(c2);
-            float acc = mul_pow2(d01.x, e_t) * to_f32(op[0]);
-            acc = fmaf(mul_pow2(d01.y, e_t), to_f32(op[1]), acc);
-            dpart[t] = acc;
-          }
+        for (int e = 0; e < EPL; e += 2) {
+          uint32_t byte = (sc == 0u) ? 0u
+                                     : pack_e2m1x2(__fdiv_rn(raw[t].at(e), sg), __fdiv_rn(raw[t].at(e + 1), sg));
+          packed |= byte << (8 * (e / 2));
         }
-      }
-    }
-    if constexpr (WITH_D) {
-      const float dsum = transpose_reduce<false>(dpart, lane);
-      if (lane < ntok) a.D[(size_t)h * a.T + t0 + lane] = dsum;
-    }
-    if constexpr (NVFP4) {
-      // NVFP4 operand for the mixed path's QK^T (FLAMIA summary §3.4, §3.2):
-      // per-token fp32 scale g = amax / (6 * 448), 16-element E4M3 block
-      // scales rounded up so nothing exceeds 6, E2M1 codes; IEEE fp32 ops.
-      constexpr int LPB = 16 / EPL;  // lanes per 16-element block
-      const float my_g = (my_tok_amax == 0.f) ? 1.f : __fdiv_rn(my_tok_amax, 2688.f);
-      if (lane < ntok) a.gscale4[(size_t)h * a.T + t0 + lane] = my_g;
-#pragma unroll
-      for (int t = 0; t < 32; ++t) {
-        const float g = __shfl_sync(0xffffffffu, my_g, t);
-        float bm = pmax[t];
-#pragma unroll
-        for (int s = 1; s < LPB; s <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, s));
-        if (t < ntok) {
-          uint32_t sc = 0u;
-          if (bm > 0.f) sc = e4m3_roundup(__fdiv_rn(bm, __fmul_rn(6.f, g)));
-          const float sg = __fmul_rn(unpack_e4m3x2((uint16_t)sc).x, g);
-          uint32_t packed = 0u;
-#pragma unroll
-          for (int e = 0; e < EPL; e += 2) {
-            uint32_t byte = (sc == 0u) ? 0u : pack_e2m1x2(__fdiv_rn(v[t][e], sg), __fdiv_rn(v[t][e + 1], sg));
-            packed |= byte << (8 * (e / 2));
-          }
-          uint8_t* dst4 = a.codes4 + (size_t)(t0 + t) * a.heads * (HD / 2) + (size_t)h * (HD / 2) + lane * (EPL / 2);
-          if constexpr (EPL == 4) *reinterpret_cast<uint16_t*>(dst4) = (uint16_t)packed;
-          else *dst4 = (uint8_t)packed;
-          if ((lane % LPB) == 0)
-            a.scales4[(size_t)(t0 + t) * a.heads * (HD / 16) + (size_t)h * (HD / 16) + lane / LPB] = (uint8_t)sc;
-        }
+        uint8_t* dst4 = a.codes4 + (size_t)(t0 + t) * a.heads * (HD / 2) + (size_t)h * (HD / 2) + lane * (EPL / 2);
+        if constexpr (EPL == 4) *reinterpret_cast<uint16_t*>(dst4) = (uint16_t)packed;
+        else *dst4 = (uint8_t)packed;
+        if ((lane % LPB) == 0)
+          a.scales4[(size_t)(t0 + t) * a.heads * (HD / 16) + (size_t)h * (HD / 16) + lane / LPB] = (uint8_t)sc;
       }
     }
   }
 }
 
+// Grid-stride over the units of up to three tensors (Q, K, V share a launch).
+template <typename TIn, typename TO, int HD, bool WITH_D, bool NVFP4>
+__global__ void __launch_bounds__(128, 3) quantize_kernel(const __grid_constant__ QuantBatch qb,
+                                                          const int32_t* __restrict__ cu,
+                                                          const int32_t* __restrict__ blk_prefix, int n_seq,
+                                                          WsHeader* hdr) {
+  const int lane = threadIdx.x & 31;
+  const int warps_total = gridDim.x * (blockDim.x >> 5);
+  const int n_blk = hdr->n_blk32;
+  int total = 0;
+  for (int r = 0; r < qb.n; ++r) total += n_blk * qb.a[r].heads;
+  for (int unit = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); unit < total; unit += warps_total) {
+    int r = 0, u = unit;
+    while (r + 1 < qb.n && u >= n_blk * qb.a[r].heads) {
+      u -= n_blk * qb.a[r].heads;
+      ++r;
+    }
+    const QuantArgs& a = qb.a[r];
+    const int g = u / a.heads, h = u - g * a.heads;
+    quantize_unit<TIn, TO, HD, WITH_D, NVFP4>(a, g, h, cu, blk_prefix, n_seq, lane);
+  }
+}
+
 // Host-side launcher (called by api.cu).
-cudaError_t launch_quantize(const QuantArgs& a, int d, int in_bf16, int o_bf16, bool with_D, bool nvfp4,
+cudaError_t launch_quantize(const QuantBatch& qb, int d, int in_bf16, int o_bf16, bool with_D, bool nvfp4,
                             const int32_t* cu, const int32_t* blk_prefix, int n_seq, WsHeader* hdr,
-                            int max_units, cudaStream_t st) {
-  int blocks = (max_units + 7) / 8;
-  blocks = blocks < 1 ? 1 : (blocks > 152 * 8 ? 152 * 8 : blocks);
+                            int max_units, int n_sms, cudaStream_t st) {
+  int blocks = (max_units + 3) / 4;  // four warps per block, one unit per warp
+  const int cap = 3 * n_sms * 4;      // three resident blocks per SM, four waves of grid stride
+  blocks = blocks < 1 ? 1 : (blocks > cap ? cap : blocks);
 #define FLAMIA_QL(TIN, TO_, HD_, WD, NV) \
-  quantize_kernel<TIN, TO_, HD_, WD, NV><<<blocks, 256, 0, st>>>(a, cu, blk_prefix, n_seq, hdr)
+  quantize_kernel<TIN, TO_, HD_, WD, NV><<<blocks, 128, 0, st>>>(qb, cu, blk_prefix, n_seq, hdr)
 #define FLAMIA_QL_D(TIN, HD_, WD, NV)                           \
   do {                                                          \
     if (o_bf16) FLAMIA_QL(TIN, __nv_bfloat16, HD_, WD, NV);     \
