@@ -33,9 +33,15 @@ namespace flamia {
 
 // Compute warps 0-7 (two per TMEM lane quarter: warp w owns query rows
 // 32(w%4)..+31 and key blocks 2(w/4), 2(w/4)+1), producer warp 8, MMA warp 9.
+// Warpgroups: 0-1 compute (warps 0-7), 2 dQ drain (warps 8-11, one per TMEM
+// lane quarter), 3 producer (12), MMA issuer (13), dQ reducer (14), idle (15).
+// Registers are rebalanced per warpgroup after launch (512 x 128 in total):
+// 2 x 128 x 176 + 128 x 80 + 128 x 80 = 65536.
 constexpr int kBwdCompute = 256;
-constexpr int kBwdThreads = kBwdCompute + 96;
-constexpr int kWarpProd = 8, kWarpMma = 9, kWarpRed = 10;
+constexpr int kBwdThreads = 512;
+constexpr int kWarpDrain0 = 8, kWarpProd = 12, kWarpMma = 13, kWarpRed = 14;
+constexpr uint32_t kRegCompute = 176, kRegDrain = 80, kRegCtl = 80;
+static_assert(2 * 128 * kRegCompute + 128 * kRegDrain + 128 * kRegCtl <= 65536, "register split");
 constexpr uint32_t kColDV = 0, kColDK = 128, kColX0 = 256, kColX1 = 384;
 constexpr uint32_t kColSfDV = kColX0 + 0, kColSfDK = kColX0 + 4, kColSfDQ = kColX0 + 8, kColSfOne = kColX0 + 12;
 
@@ -284,11 +290,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&c.dp_full, 1);
     mbar_init(&c.ds_full, kBwdCompute);
     mbar_init(&c.mm_done, 1);
-    mbar_init(&c.x1_free, kBwdCompute);
+    mbar_init(&c.x1_free, DQ ? 128 : kBwdCompute);  // drain warps (DQ) or compute warps read X1 last
     mbar_init(&c.acc_full, 1);
-    mbar_init(&c.acc_free, kBwdCompute);
+    mbar_init(&c.acc_free, 128);  // the drain warpgroup stores dK / dV
     mbar_init(&c.xch_bar, kBwdCompute);
-    mbar_init(&c.dqs_full, kBwdCompute);
+    mbar_init(&c.dqs_full, 128);
     mbar_init(&c.dqs_free, 1);
     c.abort_flag = 0;
     fence_mbar_init();
@@ -306,7 +312,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tb = c.tmem_base;
 
-  if (warp == kWarpProd) {
+  if (warp >= kWarpProd) {
+   // Warpgroup 3: producer, MMA issuer, dQ reducer (and one idle warp).
+   setmaxnreg_dec<kRegCtl>();
+   if (warp == kWarpProd) {
     // ------------------------------------------------------------ producer
     uint32_t ic = 0, ii = 0;
     bool ok = true;
@@ -415,7 +424,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kWarpRed) {
+   } else if (warp == kWarpRed) {
     // ------------------------------------------------------------ dQ reducer
     if (DQ && lane == 0) {
       uint32_t ii = 0;
@@ -441,17 +450,72 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bulk_wait_group0();
     }
     __syncwarp();
+   }
+  } else if (warp >= kWarpDrain0) {
+    setmaxnreg_dec<kRegDrain>();
+    // ------------------------------------------------------------ drain
+    // Warp 8 + qq reads TMEM lane quarter qq.  Per query tile (DQ): rows
+    // 32qq..32qq+31 of the finished dQ tile are staged for the reducer, 32
+    // columns at a time, into the 128B-swizzled [128 rows][32 fp32] boxes.
+    // Rows outside the document hold exact zeros (their dS row is zero), so
+    // whole boxes are added.  Per work item: keys 32qq..32qq+31 of dK and dV
+    // go to global memory, so the compute warps start the next item at once.
+    const int qq = warp - kWarpDrain0, r = 32 * qq + lane;
+    const float sm_scale = p.softmax_scale;
+    uint32_t ic = 0, ii = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++ic) {
+      const int pair = w / p.Hkv, hk = w - pair * p.Hkv;
+      const int2 it = p.bwd_items[pair];
+      const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
+      const int n_t = (len + kTile - 1) / kTile, q_first = p.causal ? it.y : 0;
+      const int n_iter = G * (n_t - q_first);
+      if constexpr (DQ) {
+        for (int t = 0; ok && t < n_iter; ++t, ++ii) {
+          if (!(ok = mbar_wait_warp(&c.mm_done, ii & 1, abort_flag, hdr, 0x341))) break;
+          if (!(ok = mbar_wait_warp(&c.dqs_free, (ii & 1) ^ 1, abort_flag, hdr, 0x342))) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int cb = 0; cb < HD / 32; ++cb) {
+            uint32_t rq[32];
+            tmem_ld32(taddr(tb, qq * 32, kColX1 + 32 * cb), rq);
+            tmem_ld_wait_regs(rq);
+            store_row_box(tl.dqs + cb * (kTile * 32), r, rq);
+          }
+          tc_fence_before();
+          mbar_arrive(&c.x1_free);
+          fence_proxy_async_smem();
+          mbar_arrive(&c.dqs_full);
+        }
+        if (!ok) break;
+      }
+      // ---- dK, dV of this key tile (TMEM lane = key)
+      if (!(ok = mbar_wait_warp(&c.acc_full, ic & 1, abort_flag, hdr, 0x325))) break;
+      tc_fence_after();
+      const int j_loc = kTile * it.y + r;
+      const bool key_ok = j_loc < len;
+      const size_t koff = ((size_t)(ds + j_loc) * p.Hkv + hk) * HD;
+#pragma unroll 1
+      for (int cc = 0; cc < 2 * (HD / 32); ++cc) {
+        const int which = cc / (HD / 32), cb = cc % (HD / 32);  // which: 0 = dK, 1 = dV
+        uint32_t rr[32];
+        tmem_ld32(taddr(tb, qq * 32, (which == 0 ? kColDK : kColDV) + 32 * cb), rr);
+        tmem_ld_wait_regs(rr);
+        if (key_ok) store_row32<OUT_BF16>(which == 0 ? p.dK : p.dV, koff + 32 * cb, rr, which == 0 ? sm_scale : 1.0f);
+      }
+      tc_fence_before();
+      mbar_arrive(&c.acc_free);
+    }
   } else {
+    setmaxnreg_inc<kRegCompute>();
     // ------------------------------------------------------------ compute warps
     const int q = warp & 3, hf = warp >> 2;  // lane quarter (query rows), key-block half
     const int r = 32 * q + lane;             // query row of the tile = TMEM lane
     const int b0 = 2 * hf;                   // first of this thread's two key blocks
-    constexpr int HC = HD / 2;               // output columns drained by this thread
     uint8_t* const dbg_c = hdr->dbg_phat;
     int32_t* const dbg_e = hdr->dbg_eb;
     uint32_t ic = 0, ii = 0;
     bool ok = true;
-    const float sm_scale = p.softmax_scale;
     for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++ic) {
       const int pair = w / p.Hkv, hk = w - pair * p.Hkv;
       const int2 it = p.bwd_items[pair];
@@ -553,54 +617,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(&c.ds_full);
-          if constexpr (DQ) {
-            // ---- dQ tile -> staging boxes (this thread: its row, half of the
-            // columns).  Rows outside the document hold exact zeros (their dS
-            // row is zero), so the whole 128-row box is added.
-            if (!(ok = mbar_wait_warp(&c.mm_done, ii & 1, abort_flag, hdr, 0x324))) break;
-            tc_fence_after();
-            uint32_t rq[2][32];
-            tmem_ld32(taddr(tb, q * 32, kColX1 + hf * HC), rq[0]);
-            if constexpr (HC == 64) {
-              tmem_ld32(taddr(tb, q * 32, kColX1 + hf * HC + 32), rq[1]);
-              tmem_ld_wait_regs(rq[0], rq[1]);
-            } else {
-              tmem_ld_wait_regs(rq[0]);
-            }
-            tc_fence_before();
-            mbar_arrive(&c.x1_free);
-            if (!(ok = mbar_wait_warp(&c.dqs_free, (ii & 1) ^ 1, abort_flag, hdr, 0x329))) break;
-#pragma unroll
-            for (int cbl = 0; cbl < HC / 32; ++cbl)
-              store_row_box(tl.dqs + (hf * (HC / 32) + cbl) * (kTile * 32), r, rq[cbl]);
-            fence_proxy_async_smem();
-            mbar_arrive(&c.dqs_full);
-          }
         }
       }
       if (!ok) break;
       mbar_arrive(&c.kv_empty);  // key vectors no longer read
-      // ---- dK, dV of this key tile (TMEM lane = key; this thread: half of the columns)
-      if (!(ok = mbar_wait_warp(&c.acc_full, ic & 1, abort_flag, hdr, 0x325))) break;
-      tc_fence_after();
-      const int j_loc = key0 + r;
-      const bool key_ok = j_loc < len;
-      const size_t koff = ((size_t)(ds + j_loc) * p.Hkv + hk) * HD + hf * HC;
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const float f = which == 0 ? sm_scale : 1.0f;
-        void* outp = which == 0 ? p.dK : p.dV;
-        const uint32_t col = (which == 0 ? kColDK : kColDV) + hf * HC;
-#pragma unroll
-        for (int cb = 0; cb < HC / 32; ++cb) {
-          uint32_t rr[32];
-          tmem_ld32(taddr(tb, q * 32, col + 32 * cb), rr);
-          tmem_ld_wait_regs(rr);
-          if (key_ok) store_row32<OUT_BF16>(outp, koff + 32 * cb, rr, f);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&c.acc_free);
     }
   }
   tc_fence_before();
@@ -617,6 +637,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ============================================================================
 constexpr int kDqStages = 2;
 constexpr int kDqThreads = kBwdCompute + 64;  // compute warps 0-7, producer 8, MMA 9
+constexpr int kDqWarpProd = 8, kDqWarpMma = 9;
 constexpr uint32_t kDqColAcc = 0, kDqColX0 = 128, kDqColX1 = 256;
 constexpr uint32_t kDqColSf = kDqColX0 + 0, kDqColSfOne = kDqColX0 + 4;
 
@@ -675,13 +696,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     c.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpMma) tmem_alloc(&c.tmem_base, 512);
+  if (warp == kDqWarpMma) tmem_alloc(&c.tmem_base, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = c.tmem_base;
 
-  if (warp == kWarpProd) {
+  if (warp == kDqWarpProd) {
     uint32_t ic = 0, kv = 0;
     bool ok = true;
     for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++ic) {
@@ -721,7 +742,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
       }
     }
-  } else if (warp == kWarpMma) {
+  } else if (warp == kDqWarpMma) {
     if (elect_one()) {
       uint32_t ic = 0, kv = 0, ii = 0;
       bool ok = true;
@@ -845,7 +866,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   tc_fence_before();
   __syncthreads();
   drain_after_abort(abort_flag);
-  if (warp == kWarpMma) tmem_dealloc(tb, 512);
+  if (warp == kDqWarpMma) tmem_dealloc(tb, 512);
 }
 
 // dQ buffer (fp32 sums of dS^ K^) times the softmax scale -> output dtype.
