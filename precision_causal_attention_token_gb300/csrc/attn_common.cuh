@@ -71,6 +71,18 @@ __device__ __forceinline__ void phat_block_codes(const float (&y)[32], int E, ui
   }
 }
 
+// One 32-key block of logits for one row, read from tensor memory.
+template <bool EXACT, bool NEED_MASK>
+__device__ __forceinline__ int phat_logits1(uint32_t t_s, float (&y)[32], float rowc, const float* kf,
+                                            const float* vf, int i_loc, int key, int len, int causal) {
+  uint32_t rr[32];
+  tmem_ld32(t_s, rr);
+  tmem_ld_wait_regs(rr);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(rr[j]);
+  return phat_block_logits<EXACT, NEED_MASK>(y, rowc, kf, vf, i_loc, key, len, causal);
+}
+
 // Two 32-key blocks of logits for one row: both S blocks are read from
 // tensor memory with one wait, then turned into logits and exponents.
 template <bool EXACT, bool NEED_MASK>

@@ -215,15 +215,20 @@ struct RowVals {
   int eq, edo, mi;
   float li, Di, rowc, hdo;
 };
-__device__ __forceinline__ RowVals load_row(const AttnParams& p, int h, int tok, bool row_ok) {
+// `tok_valid` is any token index inside the array (the loads are issued
+// unconditionally, so several rows' loads can be in flight at once).
+__device__ __forceinline__ RowVals load_row(const AttnParams& p, int h, int tok, bool row_ok, int tok_valid) {
+  const size_t mt = (size_t)h * p.T + (row_ok ? tok : tok_valid);
+  const int eq = (int)__ldg(p.q_sc + mt) - 127, edo = (int)__ldg(p.do_sc + mt) - 127;
+  const int mi = __ldg(p.m + mt);
+  const float li = __ldg(p.l + mt), Di = __ldg(p.D + mt);
   RowVals v{0, 0, 0, 1.f, 0.f, 0.f, 1.f};
   if (row_ok) {
-    const size_t mt = (size_t)h * p.T + tok;
-    v.eq = (int)__ldg(p.q_sc + mt) - 127;
-    v.edo = (int)__ldg(p.do_sc + mt) - 127;
-    v.mi = __ldg(p.m + mt);
-    v.li = __ldg(p.l + mt);
-    v.Di = __ldg(p.D + mt);
+    v.eq = eq;
+    v.edo = edo;
+    v.mi = mi;
+    v.li = li;
+    v.Di = Di;
   }
   v.rowc = p.c_log2 * pow2_127(v.eq);
   v.hdo = pow2_127(v.edo);
@@ -351,19 +356,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int qt = q_first; qt < n_t; ++qt, ++ii) {
           const int qs = ii & 1;
           if (!(ok = mbar_wait_warp(&c.qd_empty[qs], ((ii >> 1) & 1) ^ 1, abort_flag, hdr, 0x302))) break;
-#pragma unroll
-          for (int rr4 = 0; rr4 < 4; ++rr4) {
-            const int row = lane * 4 + rr4, i_loc = kTile * qt + row;
-            const RowVals v = load_row(p, h, ds + i_loc, i_loc < len);
-            c.rows[qs][row] = RowStage{v.rowc, v.hdo, 1.0f / v.li, v.Di, v.mi, v.eq};
-          }
+          // the tiles first, then the per-row values (their loads overlap the copies)
           if (lane == 0) {
-            mbar_arrive_expect_tx(&c.qd_full[qs], 2 * kTile * HD);
+            mbar_expect_tx(&c.qd_full[qs], 2 * kTile * HD);
             tma_load_3d(tl.q[qs], &map_q, &c.qd_full[qs], 0, h, ds + kTile * qt);
             tma_load_3d(tl.dO[qs], &map_do, &c.qd_full[qs], 0, h, ds + kTile * qt);
-          } else {
-            mbar_arrive(&c.qd_full[qs]);
           }
+          RowVals v[4];
+#pragma unroll
+          for (int rr4 = 0; rr4 < 4; ++rr4) {
+            const int i_loc = kTile * qt + lane * 4 + rr4;
+            v[rr4] = load_row(p, h, ds + i_loc, i_loc < len, ds);
+          }
+#pragma unroll
+          for (int rr4 = 0; rr4 < 4; ++rr4)
+            c.rows[qs][lane * 4 + rr4] = RowStage{v[rr4].rowc, v[rr4].hdo, 1.0f / v[rr4].li, v[rr4].Di, v[rr4].mi,
+                                                  v[rr4].eq};
+          mbar_arrive(&c.qd_full[qs]);
         }
       }
     }
@@ -800,7 +809,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
       const int i_loc = kTile * it.y + r;
       const bool row_ok = i_loc < len;
-      const RowVals rv = load_row(p, h, ds + i_loc, row_ok);
+      const RowVals rv = load_row(p, h, ds + i_loc, row_ok, ds);
       const float inv_l = 1.0f / rv.li;
       for (int kt = 0; ok && kt < n_kt; ++kt, ++kv, ++ii) {
         const int st = kv % kDqStages;

@@ -45,6 +45,18 @@ __device__ __forceinline__ void dbg_dump_phat2(uint8_t* dc, int32_t* de, int T, 
     if (k0 + 32 * b < T) de[row + k0 + 32 * b] = Eb[b];
 }
 
+// Test hook: one row's P^ codes and exponent for one 32-key block.
+__device__ __forceinline__ void dbg_dump_phat1(uint8_t* dc, int32_t* de, int T, int h, int tok, int key_tok0,
+                                               int blk, const uint32_t (&codes)[8], int Eb) {
+  if (dc == nullptr) return;
+  const size_t row = ((size_t)h * T + tok) * (size_t)T;
+  const int k0 = key_tok0 + 32 * blk;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (k0 + j < T) dc[row + k0 + j] = (uint8_t)(codes[j >> 2] >> (8 * (j & 3)));
+  if (k0 < T) de[row + k0] = Eb;
+}
+
 struct WsLayout {
   size_t header, tile_prefix, blk32_prefix, fwd_items, bwd_items, keys_a, keys_b, dq_acc, total;
   int32_t max_items;       // upper bound of tiles: ceil(T/128) + n_seq
@@ -149,6 +161,11 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes) : "memory");
+}
+// Announce `bytes` of asynchronous copies on `bar` without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
 }
 // One poll.  The suspend-time hint lets the hardware park the warp until the
 // phase completes (or 1 ms passes) instead of spinning on issue slots that
@@ -368,6 +385,32 @@ __device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&a)[32]) {
         "+r"(a[24]), "+r"(a[25]), "+r"(a[26]), "+r"(a[27]), "+r"(a[28]), "+r"(a[29]), "+r"(a[30]), "+r"(a[31])
       :
       : "memory");
+}
+// 32 lanes x 16 columns of 32-bit.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&a)[16]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+        "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15])
+      :
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t a) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(a) : "memory");
 }
 __device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t a, uint32_t b) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(a), "r"(b) : "memory");

@@ -6,18 +6,18 @@
 //
 // Persistent grid over the longest-first work list (document, 128-query tile)
 // x query heads.  Warp roles:
-//   warps 0-7  softmax: two warps per TMEM lane quarter; thread (warp w, lane)
-//              owns query row 32(w%4)+lane of the tile (= its TMEM lane) and
-//              key blocks 2(w/4), 2(w/4)+1 of each 128-key tile.
+//   warps 0-15 softmax: four warps per TMEM lane quarter; thread (warp w,
+//              lane) owns query row 32(w%4)+lane of the tile (= its TMEM
+//              lane) and key block w/4 of each 128-key tile.
 //              Reads S from TMEM, forms y = x + eV(j) (the per-key V factor
 //              folded into P along the contraction axis), quantizes P^ with
 //              one no-clamp exponent per (row, 32-key block), keeps the
 //              row's integer reference m and normaliser l, writes P^ codes to
 //              shared memory and the block exponents (relative to m) to TMEM
 //              as the A-operand scale factors of the P^V MMA.
-//   warp 8     producer: TMA loads of Q, K, V code tiles (128 x d, swizzled)
+//   warp 16    producer: TMA loads of Q, K, V code tiles (128 x d, swizzled)
 //              and the per-key scale vectors of each K/V stage.
-//   warp 9     MMA issuer: S = Q^ K^T (kind::f8f6f4, fp32 in TMEM, double
+//   warp 17    MMA issuer: S = Q^ K^T (kind::f8f6f4, fp32 in TMEM, double
 //              buffered) and O += P^ V^ (kind::mxf8f6f4 block-scaled, scale A
 //              = P^ block exponents, scale B = 1: V's own scale is folded).
 // The next tile's S is issued before the current tile's P^V so the tensor
@@ -28,9 +28,9 @@
 namespace flamia {
 
 constexpr int kFwdStages = 3;
-constexpr int kFwdSoftmax = 256;
+constexpr int kFwdSoftmax = 512;
 constexpr int kFwdThreads = kFwdSoftmax + 64;
-constexpr int kFwdWarpProd = 8, kFwdWarpMma = 9;
+constexpr int kFwdWarpProd = 16, kFwdWarpMma = 17;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColSFA0 = 384, kColSFA1 = 392, kColSFB = 400;
 
 template <int HD>
@@ -48,9 +48,9 @@ struct FwdCtl {
   uint64_t q_full, q_empty;
   uint64_t k_full[kFwdStages], k_empty[kFwdStages], v_full[kFwdStages], v_empty[kFwdStages];
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2], o_full, o_free;
-  uint64_t eb_bar[4], l_bar[4];  // per TMEM lane quarter: the two warps that share its rows
-  int ebx[2][kTile][4];  // [tile parity][row][key block] P^ block exponents, shared by a row's two threads
-  float lx[kTile][2];    // [row][half] partial normalisers for the epilogue
+  uint64_t eb_bar[4], l_bar[4];  // per TMEM lane quarter: the four warps that share its rows
+  int ebx[2][kTile][4];  // [tile parity][row][key block] P^ block exponents, shared by a row's four threads
+  float lx[kTile][4];    // [row][key block] partial normalisers for the epilogue
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -101,8 +101,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     mbar_init(&c.o_full, 1);
     mbar_init(&c.o_free, kFwdSoftmax);
     for (int qq = 0; qq < 4; ++qq) {
-      mbar_init(&c.eb_bar[qq], 64);
-      mbar_init(&c.l_bar[qq], 64);
+      mbar_init(&c.eb_bar[qq], 128);
+      mbar_init(&c.l_bar[qq], 128);
     }
     c.abort_flag = 0;
     fence_mbar_init();
@@ -228,10 +228,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int q = warp & 3, hf = warp >> 2;  // lane quarter, key-block half
-    const int r = 32 * q + lane;             // query row of the tile = TMEM lane
-    const int b0 = 2 * hf;                   // first of this thread's two key blocks
-    constexpr int HC = HD / 2;               // O columns handled by this thread
+    const int q = warp & 3, blk = warp >> 2;  // lane quarter, key block
+    const int r = 32 * q + lane;              // query row of the tile = TMEM lane
+    constexpr int OC = HD / 4;                // O columns handled by this thread
     uint8_t* const dbg_c = hdr->dbg_phat;
     int32_t* const dbg_e = hdr->dbg_eb;
     uint32_t kv = 0, sc = 0, pc = 0, ic = 0;
@@ -247,7 +246,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int eq = row_ok ? (int)__ldg(p.q_sc + (size_t)h * p.T + q0 + r) - 127 : 0;
       const float rowc = p.c_log2 * pow2_127(eq);
       int m_ref = kEmptyBlock;
-      float l_run = 0.f;  // this thread's share of the normaliser (its two key blocks)
+      float l_run = 0.f;  // this thread's share of the normaliser (its key block)
       for (int kt = 0; ok && kt < n_kt; ++kt, ++kv, ++sc, ++pc) {
         const int st = kv % kFwdStages;
         const uint32_t kph = (kv / kFwdStages) & 1;
@@ -256,80 +255,79 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (!(ok = mbar_wait_warp(&c.s_full[sb], sph, abort_flag, hdr, 0x222))) break;
         tc_fence_after();
         const int key0 = kTile * kt;
-        const bool need_mask = (kt == n_kt - 1);  // diagonal tile, or a document's last tile
-        int Eb[2];
-        float lb[2];
-        uint32_t codes[2][8];
+        int Eb;
+        float lb;
+        uint32_t codes[8];
         {
-          float y[2][32];
-          const uint32_t t0 = taddr(tb, q * 32, (sb ? kColS1 : kColS0) + 32 * b0), t1 = t0 + 32;
-          const float* kfb = c.kf[st] + 32 * b0;
-          const float* vfb = c.vf[st] + 32 * b0;
-          if (need_mask)
-            phat_logits2<EXACT, true>(t0, t1, y, Eb, rowc, kfb, vfb, i_loc, key0 + 32 * b0, len, p.causal);
+          float y[32];
+          const uint32_t t_s = taddr(tb, q * 32, (sb ? kColS1 : kColS0) + 32 * blk);
+          const float* kfb = c.kf[st] + 32 * blk;
+          const float* vfb = c.vf[st] + 32 * blk;
+          // the diagonal tile (or a document's last tile) is the only one with masked keys
+          if (kt == n_kt - 1)
+            Eb = phat_logits1<EXACT, true>(t_s, y, rowc, kfb, vfb, i_loc, key0 + 32 * blk, len, p.causal);
           else
-            phat_logits2<EXACT, false>(t0, t1, y, Eb, rowc, kfb, vfb, i_loc, key0 + 32 * b0, len, p.causal);
+            Eb = phat_logits1<EXACT, false>(t_s, y, rowc, kfb, vfb, i_loc, key0 + 32 * blk, len, p.causal);
+          const float* vi = c.vinv[st] + 32 * blk;
+          float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int bb = 0; bb < 2; ++bb) {
-            const float* vi = c.vinv[st] + 32 * (b0 + bb);
-            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 v4 = *reinterpret_cast<const float4*>(vi + 4 * q4);
+            const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+            float pv[4];
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              const float4 v4 = *reinterpret_cast<const float4*>(vi + 4 * q4);
-              const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
-              float pv[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                pv[e] = (Eb[bb] == kEmptyBlock) ? 0.f : phat_value(y[bb][4 * q4 + e], Eb[bb]);
-                l4[e] = fmaf(pv[e], vv[e], l4[e]);
-              }
-              codes[bb][q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
+            for (int e = 0; e < 4; ++e) {
+              pv[e] = (Eb == kEmptyBlock) ? 0.f : phat_value(y[4 * q4 + e], Eb);
+              l4[e] = fmaf(pv[e], vv[e], l4[e]);
             }
-            lb[bb] = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+            codes[q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
           }
+          lb = (l4[0] + l4[1]) + (l4[2] + l4[3]);
         }
         tc_fence_before();
         mbar_arrive(&c.s_free[sb]);
         // the row's reference needs all four block exponents: exchange with
-        // the row's other thread (an mbarrier with a bounded wait)
+        // the row's other three threads (an mbarrier with a bounded wait)
         const int par = sc & 1;
-        c.ebx[par][r][b0] = Eb[0];
-        c.ebx[par][r][b0 + 1] = Eb[1];
+        c.ebx[par][r][blk] = Eb;
         mbar_arrive(&c.eb_bar[q]);
         if (!(ok = mbar_wait_warp(&c.eb_bar[q], sc & 1, abort_flag, hdr, 0x226))) break;
-        int Eall[4];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) Eall[b] = c.ebx[par][r][b];
+        const int4 e4 = *reinterpret_cast<const int4*>(c.ebx[par][r]);
+        const int Eall[4] = {e4.x, e4.y, e4.z, e4.w};
         const int Emax = max(max(Eall[0], Eall[1]), max(Eall[2], Eall[3]));
         int m_new = m_ref;
         if (Emax != kEmptyBlock && (m_ref == kEmptyBlock || Emax > m_ref + 8)) m_new = Emax;
-        float lsum = 0.f;
-#pragma unroll
-        for (int bb = 0; bb < 2; ++bb)
-          if (Eb[bb] != kEmptyBlock) lsum += ldexp_f(lb[bb], Eb[bb] - m_new);
+        const float lsum = (Eb != kEmptyBlock) ? ldexp_f(lb, Eb - m_new) : 0.f;
         uint32_t word = 0;
 #pragma unroll
         for (int b = 0; b < 4; ++b)
           if (Eall[b] != kEmptyBlock) word |= (uint32_t)min(max(Eall[b] - m_new + 127, 0), 254) << (8 * b);
         mbar_arrive(&c.k_empty[st]);
-        if (row_ok) dbg_dump_phat2(dbg_c, dbg_e, p.T, h, q0 + r, ds + key0, b0, codes, Eb);
+        if (row_ok) dbg_dump_phat1(dbg_c, dbg_e, p.T, h, q0 + r, ds + key0, blk, codes, Eb);
         l_run = (m_ref == kEmptyBlock) ? lsum : ldexp_f(l_run, m_ref - m_new) + lsum;
-        // rescale this thread's half of the O accumulator row once the previous
-        // P^V has landed (warp-uniform: tcgen05.ld/st are warp-collective; lanes
-        // whose reference did not move scale by 1)
+        // rescale this thread's quarter of the O accumulator row once the
+        // previous P^V has landed (warp-uniform: tcgen05.ld/st are
+        // warp-collective; lanes whose reference did not move scale by 1)
         if (__any_sync(0xffffffffu, kt > 0 && m_new != m_ref)) {
           const uint32_t pp = pc - 1;
           if (!(ok = mbar_wait_warp(&c.p_free[pp & 1], (pp >> 1) & 1, abort_flag, hdr, 0x223))) break;
           tc_fence_after();
           const float f = (m_new != m_ref) ? ldexp_f(1.0f, m_ref - m_new) : 1.0f;
-#pragma unroll
-          for (int cb = 0; cb < HC / 32; ++cb) {
+          const uint32_t t_o = taddr(tb, q * 32, kColO + blk * OC);
+          if constexpr (OC == 32) {
             uint32_t rr[32];
-            tmem_ld32(taddr(tb, q * 32, kColO + hf * HC + 32 * cb), rr);
+            tmem_ld32(t_o, rr);
             tmem_ld_wait_regs(rr);
 #pragma unroll
             for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * f);
-            tmem_st32(taddr(tb, q * 32, kColO + hf * HC + 32 * cb), rr);
+            tmem_st32(t_o, rr);
+          } else {
+            uint32_t rr[16];
+            tmem_ld16(t_o, rr);
+            tmem_ld_wait_regs(rr);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * f);
+            tmem_st16(t_o, rr);
           }
           tmem_st_wait();
         }
@@ -337,49 +335,43 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t pb = pc & 1;
         if (!(ok = mbar_wait_warp(&c.p_free[pb], ((pc >> 1) & 1) ^ 1, abort_flag, hdr, 0x224))) break;
         uint8_t* prow = tl.p[pb];
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint4 v4 = make_uint4(codes[ch >> 1][4 * (ch & 1)], codes[ch >> 1][4 * (ch & 1) + 1],
-                                codes[ch >> 1][4 * (ch & 1) + 2], codes[ch >> 1][4 * (ch & 1) + 3]);
-          *reinterpret_cast<uint4*>(prow + sw128_off(r, 4 * hf + ch)) = v4;
-        }
-        // the row's scale word goes to all four columns (two per thread)
-        tmem_st2(taddr(tb, q * 32, (pb ? kColSFA1 : kColSFA0) + 2 * hf), word, word);
+        *reinterpret_cast<uint4*>(prow + sw128_off(r, 2 * blk)) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+        *reinterpret_cast<uint4*>(prow + sw128_off(r, 2 * blk + 1)) =
+            make_uint4(codes[4], codes[5], codes[6], codes[7]);
+        // the row's scale word goes to all four columns (one per thread)
+        tmem_st1(taddr(tb, q * 32, (pb ? kColSFA1 : kColSFA0) + blk), word);
         fence_proxy_async_smem();
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&c.p_full[pb]);
       }
       if (!ok) break;
-      // epilogue: O = acc / l (this thread: half of the row)
-      if (!(ok = mbar_wait_warp(&c.o_full, ic & 1, abort_flag, hdr, 0x225))) break;
-      tc_fence_after();
-      float o[HC];
-#pragma unroll
-      for (int cb = 0; cb < HC / 32; ++cb) {
-        uint32_t rr[32];
-        tmem_ld32(taddr(tb, q * 32, kColO + hf * HC + 32 * cb), rr);
-        tmem_ld_wait_regs(rr);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) o[32 * cb + j] = __uint_as_float(rr[j]);
-      }
-      tc_fence_before();
-      mbar_arrive(&c.o_free);
-      c.lx[r][hf] = l_run;
+      // epilogue: O = acc / l (this thread: a quarter of the row)
+      c.lx[r][blk] = l_run;
       mbar_arrive(&c.l_bar[q]);
       if (!(ok = mbar_wait_warp(&c.l_bar[q], ic & 1, abort_flag, hdr, 0x227))) break;
-      const float l_tot = c.lx[r][0] + c.lx[r][1];
+      const float4 l4 = *reinterpret_cast<const float4*>(c.lx[r]);
+      const float l_tot = (l4.x + l4.y) + (l4.z + l4.w);
+      const float inv = 1.0f / l_tot;
+      if (!(ok = mbar_wait_warp(&c.o_full, ic & 1, abort_flag, hdr, 0x225))) break;
+      tc_fence_after();
+      uint32_t rr[OC];
+      if constexpr (OC == 32) tmem_ld32(taddr(tb, q * 32, kColO + blk * OC), rr);
+      else tmem_ld16(taddr(tb, q * 32, kColO + blk * OC), rr);
+      tmem_ld_wait_regs(rr);
+      tc_fence_before();
+      mbar_arrive(&c.o_free);
       if (row_ok) {
-        const float inv = 1.0f / l_tot;
-        const size_t off = ((size_t)(q0 + r) * p.H + h) * HD + hf * HC;
+        const size_t off = ((size_t)(q0 + r) * p.H + h) * HD + blk * OC;
         if constexpr (OUT_BF16) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O) + off);
 #pragma unroll
-          for (int c8 = 0; c8 < HC / 8; ++c8) {
+          for (int c8 = 0; c8 < OC / 8; ++c8) {
             uint32_t wv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(o[8 * c8 + 2 * e] * inv, o[8 * c8 + 2 * e + 1] * inv);
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(rr[8 * c8 + 2 * e]) * inv,
+                                                        __uint_as_float(rr[8 * c8 + 2 * e + 1]) * inv);
               wv[e] = *reinterpret_cast<uint32_t*>(&b2);
             }
             dst[c8] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
@@ -387,10 +379,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         } else {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.O) + off);
 #pragma unroll
-          for (int c4 = 0; c4 < HC / 4; ++c4)
-            dst[c4] = make_float4(o[4 * c4] * inv, o[4 * c4 + 1] * inv, o[4 * c4 + 2] * inv, o[4 * c4 + 3] * inv);
+          for (int c4 = 0; c4 < OC / 4; ++c4)
+            dst[c4] = make_float4(__uint_as_float(rr[4 * c4]) * inv, __uint_as_float(rr[4 * c4 + 1]) * inv,
+                                  __uint_as_float(rr[4 * c4 + 2]) * inv, __uint_as_float(rr[4 * c4 + 3]) * inv);
         }
-        if (hf == 0) {
+        if (blk == 0) {
           p.m[(size_t)h * p.T + q0 + r] = m_ref;
           p.l[(size_t)h * p.T + q0 + r] = l_tot;
         }
