@@ -22,6 +22,7 @@ flamia_status_t validate(const flamia_problem_t* p) {
   if ((int64_t)p->T * p->H * p->d >= (int64_t)1 << 40) return FLAMIA_ERR_UNSUPPORTED;
   if (p->T > (1 << 30) || p->n_seq > p->T + 1) return FLAMIA_ERR_INVALID_ARG;
   if (p->path != FLAMIA_PATH_MXFP8 && p->path != FLAMIA_PATH_NVFP4_FP8) return FLAMIA_ERR_UNSUPPORTED;
+  if (p->path == FLAMIA_PATH_NVFP4_FP8 && p->exact) return FLAMIA_ERR_UNSUPPORTED;
   if ((p->in_dtype != FLAMIA_F32 && p->in_dtype != FLAMIA_BF16) ||
       (p->out_dtype != FLAMIA_F32 && p->out_dtype != FLAMIA_BF16))
     return FLAMIA_ERR_UNSUPPORTED;
@@ -80,6 +81,21 @@ bool make_dq_map(CUtensorMap* m, float* ptr, int d, int heads, int T) {
   cuuint32_t box[3] = {32, 1, 128};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 3-D map over the mixed path's bf16 score operands [T][heads][d]: box = 128
+// tokens x 1 head x 64 values (128 bytes, 128B swizzle).
+bool make_nv_map(CUtensorMap* m, const void* ptr, int d, int heads, int T) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -151,6 +167,7 @@ flamia_status_t flamia_quantize(const flamia_problem_t* p, int32_t role, const v
         a.codes4 = static_cast<uint8_t*>(out[i].codes4);
         a.scales4 = static_cast<uint8_t*>(out[i].scales4);
         a.gscale4 = static_cast<float*>(out[i].gscale4);
+        a.xnv = reinterpret_cast<__nv_bfloat16*>(w + (i == 0 ? L.nv_q : L.nv_k));
       }
       units += max_blk * a.heads;
     }
@@ -198,6 +215,7 @@ static flamia_status_t fill_params(const flamia_problem_t* p, const WsLayout& L,
   a->bwd_items = reinterpret_cast<const int2*>(w + L.bwd_items);
   a->hdr = reinterpret_cast<WsHeader*>(w + L.header);
   a->dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
+  a->nvfp4 = p->path == FLAMIA_PATH_NVFP4_FP8 ? 1 : 0;
   return FLAMIA_OK;
 }
 
@@ -213,7 +231,6 @@ flamia_status_t flamia_fwd(const flamia_problem_t* p, const flamia_operand_t* q,
   if (p->path == FLAMIA_PATH_NVFP4_FP8 && (!q->codes4 || !q->scales4 || !q->gscale4 || !k->codes4 ||
                                            !k->scales4 || !k->gscale4))
     return FLAMIA_ERR_INVALID_ARG;
-  if (p->path == FLAMIA_PATH_NVFP4_FP8) return FLAMIA_ERR_UNSUPPORTED;  // scores in NVFP4: not built yet
   AttnParams a;
   fill_params(p, L, ws, &a);
   a.q_sc = static_cast<const uint8_t*>(q->scales);
@@ -226,6 +243,15 @@ flamia_status_t flamia_fwd(const flamia_problem_t* p, const flamia_operand_t* q,
     return FLAMIA_ERR_CUDA;
   maps.dO = maps.q;
   maps.dq = maps.q;
+  maps.qn = maps.q;
+  maps.kn = maps.k;
+  if (a.nvfp4) {
+    a.q_g = static_cast<const float*>(q->gscale4);
+    a.k_g = static_cast<const float*>(k->gscale4);
+    if (!make_nv_map(&maps.qn, static_cast<uint8_t*>(ws) + L.nv_q, p->d, p->H, p->T) ||
+        !make_nv_map(&maps.kn, static_cast<uint8_t*>(ws) + L.nv_k, p->d, p->Hkv, p->T))
+      return FLAMIA_ERR_CUDA;
+  }
   return launch_fwd(a, maps, stream) == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
 }
 
@@ -240,7 +266,7 @@ flamia_status_t flamia_bwd(const flamia_problem_t* p, const flamia_operand_t* q,
   if (!operand_ok(q) || !operand_ok(k) || !operand_ok(v) || !operand_ok(dO) || !D || !m || !l || !dQ || !dK ||
       !dV || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
     return FLAMIA_ERR_INVALID_ARG;
-  if (p->path == FLAMIA_PATH_NVFP4_FP8) return FLAMIA_ERR_UNSUPPORTED;
+  if (p->path == FLAMIA_PATH_NVFP4_FP8 && (!q->gscale4 || !k->gscale4)) return FLAMIA_ERR_INVALID_ARG;
   AttnParams a;
   fill_params(p, L, ws, &a);
   a.q_sc = static_cast<const uint8_t*>(q->scales);
@@ -256,6 +282,15 @@ flamia_status_t flamia_bwd(const flamia_problem_t* p, const flamia_operand_t* q,
       !make_codes_map(&maps.v, v->codes, p->d, p->Hkv, p->T) || !make_codes_map(&maps.dO, dO->codes, p->d, p->H, p->T) ||
       !make_dq_map(&maps.dq, a.dq_acc, p->d, p->H, p->T))
     return FLAMIA_ERR_CUDA;
+  maps.qn = maps.q;
+  maps.kn = maps.k;
+  if (a.nvfp4) {
+    a.q_g = static_cast<const float*>(q->gscale4);
+    a.k_g = static_cast<const float*>(k->gscale4);
+    if (!make_nv_map(&maps.qn, static_cast<uint8_t*>(ws) + L.nv_q, p->d, p->H, p->T) ||
+        !make_nv_map(&maps.kn, static_cast<uint8_t*>(ws) + L.nv_k, p->d, p->Hkv, p->T))
+      return FLAMIA_ERR_CUDA;
+  }
   return launch_bwd(a, maps, stream) == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
 }
 

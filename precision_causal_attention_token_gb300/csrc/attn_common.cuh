@@ -102,6 +102,51 @@ __device__ __forceinline__ void phat_logits2(uint32_t t_s0, uint32_t t_s1, float
   }
 }
 
+// Bytes of one 128-token score-operand tile: E4M3 codes (MXFP8 path) or
+// bf16 NVFP4 values (mixed path).
+template <int HD, bool NV4>
+constexpr int score_tile_bytes() {
+  return NV4 ? 2 * kTile * HD : kTile * HD;
+}
+
+// S = Q K^T for one 128 x 128 tile into TMEM column d_s.
+//  MXFP8: E4M3 tiles with rows of HD bytes (swizzle = HD bytes), kind::f8f6f4,
+//         32 K-elements per instruction.
+//  Mixed: bf16 tiles stored as HD/64 boxes of [128 rows][64 values] (128B
+//         swizzle), kind::f16, 16 K-elements per instruction; the products of
+//         E2M1 values and E4M3 block scales are exact in bf16, so this is the
+//         block-scaled NVFP4 product, accumulated in fp32.
+template <int HD, bool NV4>
+__device__ __forceinline__ void issue_scores(uint32_t d_s, const uint8_t* qt, const uint8_t* kt) {
+  const uint32_t qa = smem_u32(qt), ka = smem_u32(kt);
+  if constexpr (NV4) {
+    const uint32_t id = idesc_bf16(128, 128);
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      const uint32_t off = (uint32_t)(kk >> 2) * (kTile * 128) + (uint32_t)(kk & 3) * 32;
+      mma_bf16(d_s, smem_desc(qa + off, 16, 1024, kSwz128), smem_desc(ka + off, 16, 1024, kSwz128), id, kk > 0);
+    }
+  } else {
+    const uint32_t id = idesc_f8(128, 128, 0, 0);
+    constexpr uint32_t swz = HD == 128 ? kSwz128 : kSwz64;
+#pragma unroll
+    for (int kk = 0; kk < HD / 32; ++kk)
+      mma_f8(d_s, smem_desc(qa + 32 * kk, 16, 8 * HD, swz), smem_desc(ka + 32 * kk, 16, 8 * HD, swz), id, kk > 0);
+  }
+}
+
+// TMA of one 128-token score-operand tile (row `tok0`, head `head`).
+template <int HD, bool NV4>
+__device__ __forceinline__ void load_score_tile(uint8_t* dst, const CUtensorMap* map8, const CUtensorMap* mapn,
+                                                uint64_t* bar, int head, int tok0) {
+  if constexpr (NV4) {
+#pragma unroll
+    for (int bx = 0; bx < HD / 64; ++bx) tma_load_3d(dst + bx * (kTile * 128), mapn, bar, 64 * bx, head, tok0);
+  } else {
+    tma_load_3d(dst, map8, bar, 0, head, tok0);
+  }
+}
+
 // x * 2^e for any integer e (exact while the result stays normal).
 __device__ __forceinline__ float ldexp_f(float x, int e) {
   if (e >= -126 && e <= 127) return x * exp2i(e);

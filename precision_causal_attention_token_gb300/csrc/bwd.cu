@@ -45,9 +45,12 @@ static_assert(2 * 128 * kRegCompute + 128 * kRegDrain + 128 * kRegCtl <= 65536, 
 constexpr uint32_t kColDV = 0, kColDK = 128, kColX0 = 256, kColX1 = 384;
 constexpr uint32_t kColSfDV = kColX0 + 0, kColSfDK = kColX0 + 4, kColSfDQ = kColX0 + 8, kColSfOne = kColX0 + 12;
 
-template <int HD, bool EXACT, bool DQ>
+// NV4 (mixed path): the scores' operands are bf16 NVFP4 values (k holds K's,
+// qn Q's); dK still contracts with the E4M3 Q codes.  dQ then comes from the
+// dQ kernel (no DQ variant).
+template <int HD, bool EXACT, bool DQ, bool NV4>
 struct __align__(1024) BwdTiles {
-  uint8_t k[kTile * HD];
+  uint8_t k[score_tile_bytes<HD, NV4>()];
   uint8_t v[kTile * HD];
   uint8_t q[2][kTile * HD];
   uint8_t dO[2][kTile * HD];
@@ -56,6 +59,7 @@ struct __align__(1024) BwdTiles {
   uint8_t dsk[EXACT ? kTile * kTile : 1024];  // exact option: dK payload
   // dQ tile staged for the bulk reduce-add: HD/32 boxes of [128 rows][32 fp32], 128B-swizzled
   float dqs[DQ ? kTile * HD : 256];
+  uint8_t qn[2][NV4 ? score_tile_bytes<HD, NV4>() : 1024];  // mixed path: Q's score operand
 };
 
 // Per-row values of one query tile, staged in shared memory by the producer
@@ -79,9 +83,9 @@ struct BwdCtl {
   int abort_flag;
 };
 
-template <int HD, bool EXACT, bool DQ>
+template <int HD, bool EXACT, bool DQ, bool NV4>
 constexpr size_t bwd_smem_bytes() {
-  return sizeof(BwdTiles<HD, EXACT, DQ>) + sizeof(BwdCtl) + 1024;
+  return sizeof(BwdTiles<HD, EXACT, DQ, NV4>) + sizeof(BwdCtl) + 1024;
 }
 
 __device__ __forceinline__ uint64_t bdesc_k(const uint8_t* t, uint32_t off, uint32_t rb) {
@@ -217,11 +221,14 @@ struct RowVals {
 };
 // `tok_valid` is any token index inside the array (the loads are issued
 // unconditionally, so several rows' loads can be in flight at once).
+// NV4: the score's row factor is Q's per-token NVFP4 scale instead of 2^eQ.
+template <bool NV4>
 __device__ __forceinline__ RowVals load_row(const AttnParams& p, int h, int tok, bool row_ok, int tok_valid) {
   const size_t mt = (size_t)h * p.T + (row_ok ? tok : tok_valid);
   const int eq = (int)__ldg(p.q_sc + mt) - 127, edo = (int)__ldg(p.do_sc + mt) - 127;
   const int mi = __ldg(p.m + mt);
   const float li = __ldg(p.l + mt), Di = __ldg(p.D + mt);
+  const float gq = NV4 ? __ldg(p.q_g + mt) : 1.f;
   RowVals v{0, 0, 0, 1.f, 0.f, 0.f, 1.f};
   if (row_ok) {
     v.eq = eq;
@@ -230,7 +237,7 @@ __device__ __forceinline__ RowVals load_row(const AttnParams& p, int h, int tok,
     v.li = li;
     v.Di = Di;
   }
-  v.rowc = p.c_log2 * pow2_127(v.eq);
+  v.rowc = p.c_log2 * (NV4 ? (row_ok ? gq : 1.f) : pow2_127(v.eq));
   v.hdo = pow2_127(v.edo);
   return v;
 }
@@ -268,14 +275,18 @@ __device__ __forceinline__ uint32_t dq_operand(const float (&dsv)[32], float ama
 // warps and added to the fp32 dQ buffer by the reducer warp with bulk tensor
 // reduce-adds (whole 128-byte lines, the addition done in L2).
 // ============================================================================
-template <int HD, bool OUT_BF16, bool EXACT, bool DQ>
+template <int HD, bool OUT_BF16, bool EXACT, bool DQ, bool NV4>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
-               const __grid_constant__ CUtensorMap map_dq) {
+               const __grid_constant__ CUtensorMap map_dq, const __grid_constant__ CUtensorMap map_qn,
+               const __grid_constant__ CUtensorMap map_kn) {
+  static_assert(!(NV4 && DQ), "the mixed path takes dQ from the dQ kernel");
+  constexpr bool PERKEY = EXACT || NV4;
+  constexpr int kQKBytes = score_tile_bytes<HD, NV4>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  using Tiles = BwdTiles<HD, EXACT, DQ>;
+  using Tiles = BwdTiles<HD, EXACT, DQ, NV4>;
   Tiles& tl = *reinterpret_cast<Tiles*>(base);
   BwdCtl& c = *reinterpret_cast<BwdCtl*>(base + sizeof(Tiles));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -311,6 +322,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     prefetch_tensormap(&map_v);
     prefetch_tensormap(&map_do);
     if (DQ) prefetch_tensormap(&map_dq);
+    if (NV4) {
+      prefetch_tensormap(&map_qn);
+      prefetch_tensormap(&map_kn);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -335,18 +350,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int jj = 0; jj < 4; ++jj) {
         const int j = lane * 4 + jj, key = kTile * it.y + j;
         int ek = 0, ev = 0;
+        float gk = 1.f;
         if (key < len) {
           ek = (int)__ldg(p.k_sc + (size_t)hk * p.T + ds + key) - 127;
           ev = (int)__ldg(p.v_sc + (size_t)hk * p.T + ds + key) - 127;
+          if (NV4) gk = __ldg(p.k_g + (size_t)hk * p.T + ds + key);
         }
-        c.kf[j] = pow2_127(ek);
+        c.kf[j] = NV4 ? gk : pow2_127(ek);
         c.vf[j] = (float)ev;
         c.vinv[j] = pow2_127(-ev);
         if ((j & 31) == 0) c.ekb[j >> 5] = ek;
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(&c.kv_full, 2 * kTile * HD);
-        tma_load_3d(tl.k, &map_k, &c.kv_full, 0, hk, k0);
+        mbar_arrive_expect_tx(&c.kv_full, kQKBytes + kTile * HD);
+        load_score_tile<HD, NV4>(tl.k, &map_k, &map_kn, &c.kv_full, hk, k0);
         tma_load_3d(tl.v, &map_v, &c.kv_full, 0, hk, k0);
       } else {
         mbar_arrive(&c.kv_full);
@@ -358,15 +375,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!(ok = mbar_wait_warp(&c.qd_empty[qs], ((ii >> 1) & 1) ^ 1, abort_flag, hdr, 0x302))) break;
           // the tiles first, then the per-row values (their loads overlap the copies)
           if (lane == 0) {
-            mbar_expect_tx(&c.qd_full[qs], 2 * kTile * HD);
+            mbar_expect_tx(&c.qd_full[qs], 2 * kTile * HD + (NV4 ? kQKBytes : 0));
             tma_load_3d(tl.q[qs], &map_q, &c.qd_full[qs], 0, h, ds + kTile * qt);
             tma_load_3d(tl.dO[qs], &map_do, &c.qd_full[qs], 0, h, ds + kTile * qt);
+            if (NV4) load_score_tile<HD, NV4>(tl.qn[qs], &map_q, &map_qn, &c.qd_full[qs], h, ds + kTile * qt);
           }
           RowVals v[4];
 #pragma unroll
           for (int rr4 = 0; rr4 < 4; ++rr4) {
             const int i_loc = kTile * qt + lane * 4 + rr4;
-            v[rr4] = load_row(p, h, ds + i_loc, i_loc < len, ds);
+            v[rr4] = load_row<NV4>(p, h, ds + i_loc, i_loc < len, ds);
           }
 #pragma unroll
           for (int rr4 = 0; rr4 < 4; ++rr4)
@@ -395,9 +413,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // X0 holds the previous iteration's scale factors until its MMAs finish
           if (ii > 0 && !(ok = mbar_wait(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x313))) break;
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < HD / 32; ++kk)
-            mma_f8(tb + kColX0, bdesc_k(tl.q[qs], 32 * kk, HD), bdesc_k(tl.k, 32 * kk, HD), id_sp, kk > 0);
+          issue_scores<HD, NV4>(tb + kColX0, NV4 ? tl.qn[qs] : tl.q[qs], tl.k);
           tc_commit(&c.s_full);
           if (!(ok = mbar_wait(&c.x1_free, (ii & 1) ^ 1, abort_flag, hdr, 0x314))) break;
           tc_fence_after();
@@ -546,7 +562,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           int Eb[2];
           // the diagonal tile (and a document's last key tile) needs the mask
           const bool need_mask = p.causal ? (qt == it.y) : (it.y == n_t - 1);
-          recompute_phat<EXACT>(taddr(tb, q * 32, kColX0), b0, rv.rowc, c.kf, c.vf, i_loc, key0, len, p.causal,
+          recompute_phat<PERKEY>(taddr(tb, q * 32, kColX0), b0, rv.rowc, c.kf, c.vf, i_loc, key0, len, p.causal,
                                 need_mask, row_ok, pcode, Eb);
           if (row_ok) dbg_dump_phat2(dbg_c, dbg_e, p.T, h, ds + i_loc, ds + key0, b0, pcode, Eb);
           if (!(ok = mbar_wait_warp(&c.dp_full, ii & 1, abort_flag, hdr, 0x323))) break;
@@ -650,17 +666,21 @@ constexpr int kDqWarpProd = 8, kDqWarpMma = 9;
 constexpr uint32_t kDqColAcc = 0, kDqColX0 = 128, kDqColX1 = 256;
 constexpr uint32_t kDqColSf = kDqColX0 + 0, kDqColSfOne = kDqColX0 + 4;
 
-template <int HD>
+// q and k hold the scores' operands (E4M3 codes, or bf16 NVFP4 values on the
+// mixed path, where k8 holds K's E4M3 codes for the dQ MMA).
+template <int HD, bool NV4>
 struct __align__(1024) DqTiles {
-  uint8_t q[kTile * HD];
+  uint8_t q[score_tile_bytes<HD, NV4>()];
   uint8_t dO[kTile * HD];
-  uint8_t k[kDqStages][kTile * HD];
+  uint8_t k[kDqStages][score_tile_bytes<HD, NV4>()];
   uint8_t v[kDqStages][kTile * HD];
   uint8_t ds[kTile * kTile];
+  uint8_t k8[kDqStages][NV4 ? kTile * HD : 1024];
 };
 
 struct DqCtl {
   float kf[kDqStages][kTile], vf[kDqStages][kTile], vinv[kDqStages][kTile];
+  float kfold[kDqStages][kTile];  // 2^eK(j): the exact option's dQ-operand fold
   int ekb[kDqStages][4];
   uint8_t xdq[2][kTile][4];  // [parity][query row][key block] dQ scale bytes
   uint64_t qd_full, qd_empty, kv_full[kDqStages], kv_empty[kDqStages];
@@ -669,19 +689,22 @@ struct DqCtl {
   int abort_flag;
 };
 
-template <int HD>
+template <int HD, bool NV4>
 constexpr size_t dq_smem_bytes() {
-  return sizeof(DqTiles<HD>) + sizeof(DqCtl) + 1024;
+  return sizeof(DqTiles<HD, NV4>) + sizeof(DqCtl) + 1024;
 }
 
-template <int HD, bool OUT_BF16, bool EXACT>
+template <int HD, bool OUT_BF16, bool EXACT, bool NV4>
 __global__ void __launch_bounds__(kDqThreads, 1)
     dq_kernel(const AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-              const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do) {
+              const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+              const __grid_constant__ CUtensorMap map_qn, const __grid_constant__ CUtensorMap map_kn) {
+  constexpr bool PERKEY = EXACT || NV4;
+  constexpr int kQKBytes = score_tile_bytes<HD, NV4>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  DqTiles<HD>& tl = *reinterpret_cast<DqTiles<HD>*>(base);
-  DqCtl& c = *reinterpret_cast<DqCtl*>(base + sizeof(DqTiles<HD>));
+  DqTiles<HD, NV4>& tl = *reinterpret_cast<DqTiles<HD, NV4>*>(base);
+  DqCtl& c = *reinterpret_cast<DqCtl*>(base + sizeof(DqTiles<HD, NV4>));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.H / p.Hkv;
   const int n_work = p.hdr->n_items * p.H;
@@ -721,8 +744,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
       if (!(ok = mbar_wait_warp(&c.qd_empty, (ic & 1) ^ 1, abort_flag, hdr, 0x401))) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&c.qd_full, 2 * kTile * HD);
-        tma_load_3d(tl.q, &map_q, &c.qd_full, 0, h, ds + kTile * it.y);
+        mbar_arrive_expect_tx(&c.qd_full, kQKBytes + kTile * HD);
+        load_score_tile<HD, NV4>(tl.q, &map_q, &map_qn, &c.qd_full, h, ds + kTile * it.y);
         tma_load_3d(tl.dO, &map_do, &c.qd_full, 0, h, ds + kTile * it.y);
       }
       for (int kt = 0; kt < n_kt; ++kt, ++kv) {
@@ -733,19 +756,23 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         for (int jj = 0; jj < 4; ++jj) {
           const int j = lane * 4 + jj, key = kTile * kt + j;
           int ek = 0, ev = 0;
+          float gk = 1.f;
           if (key < len) {
             ek = (int)__ldg(p.k_sc + (size_t)hk * p.T + ds + key) - 127;
             ev = (int)__ldg(p.v_sc + (size_t)hk * p.T + ds + key) - 127;
+            if (NV4) gk = __ldg(p.k_g + (size_t)hk * p.T + ds + key);
           }
-          c.kf[st][j] = pow2_127(ek);
+          c.kf[st][j] = NV4 ? gk : pow2_127(ek);
+          c.kfold[st][j] = pow2_127(ek);
           c.vf[st][j] = (float)ev;
           c.vinv[st][j] = pow2_127(-ev);
           if ((j & 31) == 0) c.ekb[st][j >> 5] = ek;
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&c.kv_full[st], 2 * kTile * HD);
-          tma_load_3d(tl.k[st], &map_k, &c.kv_full[st], 0, hk, ds + kTile * kt);
+          mbar_arrive_expect_tx(&c.kv_full[st], kQKBytes + kTile * HD + (NV4 ? kTile * HD : 0));
+          load_score_tile<HD, NV4>(tl.k[st], &map_k, &map_kn, &c.kv_full[st], hk, ds + kTile * kt);
           tma_load_3d(tl.v[st], &map_v, &c.kv_full[st], 0, hk, ds + kTile * kt);
+          if (NV4) tma_load_3d(tl.k8[st], &map_k, &c.kv_full[st], 0, hk, ds + kTile * kt);
         } else {
           mbar_arrive(&c.kv_full[st]);
         }
@@ -768,9 +795,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           if (!(ok = mbar_wait(&c.kv_full[st], ph, abort_flag, hdr, 0x412))) break;
           if (ii > 0 && !(ok = mbar_wait(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x413))) break;
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < HD / 32; ++kk)
-            mma_f8(tb + kDqColX0, bdesc_k(tl.q, 32 * kk, HD), bdesc_k(tl.k[st], 32 * kk, HD), id_sp, kk > 0);
+          issue_scores<HD, NV4>(tb + kDqColX0, tl.q, tl.k[st]);
           tc_commit(&c.s_full);
           if (!(ok = mbar_wait(&c.dp_free, (ii & 1) ^ 1, abort_flag, hdr, 0x414))) break;
           tc_fence_after();
@@ -783,7 +808,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_mxf8(tb + kDqColAcc, bdesc_k(tl.ds, 32 * kk, 128), bdesc_mn(tl.k[st], kk * 32 * HD, HD),
+            mma_mxf8(tb + kDqColAcc, bdesc_k(tl.ds, 32 * kk, 128), bdesc_mn(NV4 ? tl.k8[st] : tl.k[st], kk * 32 * HD, HD),
                      idesc_mxf8(128, HD, 0, 1, kk, kk), tb + kDqColSf, tb + kDqColSfOne, (kt > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&c.mm_done);
           tc_commit(&c.kv_empty[st]);
@@ -809,7 +834,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
       const int i_loc = kTile * it.y + r;
       const bool row_ok = i_loc < len;
-      const RowVals rv = load_row(p, h, ds + i_loc, row_ok, ds);
+      const RowVals rv = load_row<NV4>(p, h, ds + i_loc, row_ok, ds);
       const float inv_l = 1.0f / rv.li;
       for (int kt = 0; ok && kt < n_kt; ++kt, ++kv, ++ii) {
         const int st = kv % kDqStages;
@@ -819,7 +844,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         tc_fence_after();
         uint32_t pcode[2][8];
         int Eb[2];
-        recompute_phat<EXACT>(taddr(tb, q * 32, kDqColX0), b0, rv.rowc, c.kf[st], c.vf[st], i_loc, kTile * kt, len,
+        recompute_phat<PERKEY>(taddr(tb, q * 32, kDqColX0), b0, rv.rowc, c.kf[st], c.vf[st], i_loc, kTile * kt, len,
                               p.causal, kt == n_kt - 1, row_ok, pcode, Eb);
         if (!(ok = mbar_wait_warp(&c.dp_full, ii & 1, abort_flag, hdr, 0x423))) break;
         if (ii > 0 && !(ok = mbar_wait_warp(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x424))) break;
@@ -839,7 +864,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           uint32_t codes[8];
           int e_blk;
           c.xdq[par][r][b] =
-              (uint8_t)dq_operand<EXACT>(dsv, amax_ds, c.kf[st] + 32 * b, c.ekb[st][b], codes, e_blk);
+              (uint8_t)dq_operand<EXACT>(dsv, amax_ds, c.kfold[st] + 32 * b, c.ekb[st][b], codes, e_blk);
           store_row_block(tl.ds, r, b, codes);
         }
         tc_fence_before();
@@ -904,46 +929,61 @@ static cudaError_t set_smem(K kernel, size_t smem) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
-template <int HD, bool OB, bool EX>
+template <int HD, bool OB, bool EX, bool NV4>
 static cudaError_t launch_bwd_t(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
-  const bool det = p.exact || p.deterministic;
+  const bool det = p.exact || p.deterministic || NV4;
   const int nsm = sm_count();
   long work = (long)p.max_items * p.Hkv;
   int grid = (int)(work < nsm ? work : nsm);
   cudaError_t e;
-  if (!det) {
-    const size_t smem = bwd_smem_bytes<HD, EX, true>();
-    if ((e = set_smem(bwd_kernel<HD, OB, EX, true>, smem)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(p.dq_acc, 0, sizeof(float) * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
-    bwd_kernel<HD, OB, EX, true><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.dq);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const size_t n4 = (size_t)p.T * p.H * HD / 4;
-    int cg = (int)((n4 + 255) / 256);
-    if (cg > nsm * 8) cg = nsm * 8;
-    if (OB) dq_convert_kernel<true><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4, p.softmax_scale);
-    else dq_convert_kernel<false><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4, p.softmax_scale);
-    return cudaGetLastError();
+  if constexpr (!NV4) {
+    if (!det) {
+      const size_t smem = bwd_smem_bytes<HD, EX, true, false>();
+      static_assert(bwd_smem_bytes<HD, EX, true, false>() <= 232448, "shared memory");
+      if ((e = set_smem(bwd_kernel<HD, OB, EX, true, false>, smem)) != cudaSuccess) return e;
+      if ((e = cudaMemsetAsync(p.dq_acc, 0, sizeof(float) * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
+      bwd_kernel<HD, OB, EX, true, false><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.dq, m.q, m.q);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      const size_t n4 = (size_t)p.T * p.H * HD / 4;
+      int cg = (int)((n4 + 255) / 256);
+      if (cg > nsm * 8) cg = nsm * 8;
+      if (OB) dq_convert_kernel<true><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4, p.softmax_scale);
+      else dq_convert_kernel<false><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4, p.softmax_scale);
+      return cudaGetLastError();
+    }
   }
-  const size_t smem = bwd_smem_bytes<HD, EX, false>();
-  if ((e = set_smem(bwd_kernel<HD, OB, EX, false>, smem)) != cudaSuccess) return e;
+  const size_t smem = bwd_smem_bytes<HD, EX, false, NV4>();
+  static_assert(bwd_smem_bytes<HD, EX, false, NV4>() <= 232448, "shared memory");
+  static_assert(dq_smem_bytes<HD, NV4>() <= 232448, "shared memory");
+  if ((e = set_smem(bwd_kernel<HD, OB, EX, false, NV4>, smem)) != cudaSuccess) return e;
   // without DQ the dQ map is not read (the q map stands in for the argument)
-  bwd_kernel<HD, OB, EX, false><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.q);
+  bwd_kernel<HD, OB, EX, false, NV4><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.q, m.qn, m.kn);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const size_t dsm = dq_smem_bytes<HD>();
-  if ((e = set_smem(dq_kernel<HD, OB, EX>, dsm)) != cudaSuccess) return e;
+  const size_t dsm = dq_smem_bytes<HD, NV4>();
+  if ((e = set_smem(dq_kernel<HD, OB, EX, NV4>, dsm)) != cudaSuccess) return e;
   long dwork = (long)p.max_items * p.H;
   int dgrid = (int)(dwork < nsm ? dwork : nsm);
-  dq_kernel<HD, OB, EX><<<dgrid, kDqThreads, dsm, st>>>(p, m.q, m.k, m.v, m.dO);
+  dq_kernel<HD, OB, EX, NV4><<<dgrid, kDqThreads, dsm, st>>>(p, m.q, m.k, m.v, m.dO, m.qn, m.kn);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
-  if (p.d == 128) {
-    if (p.exact) return p.out_bf16 ? launch_bwd_t<128, true, true>(p, m, st) : launch_bwd_t<128, false, true>(p, m, st);
-    return p.out_bf16 ? launch_bwd_t<128, true, false>(p, m, st) : launch_bwd_t<128, false, false>(p, m, st);
+template <int HD, bool OB, bool EX>
+static cudaError_t launch_bwd_n(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
+  if constexpr (EX) {  // the exact option is not offered on the mixed path (the host rejects it)
+    return p.nvfp4 ? cudaErrorNotSupported : launch_bwd_t<HD, OB, EX, false>(p, m, st);
+  } else {
+    return p.nvfp4 ? launch_bwd_t<HD, OB, EX, true>(p, m, st) : launch_bwd_t<HD, OB, EX, false>(p, m, st);
   }
-  if (p.exact) return p.out_bf16 ? launch_bwd_t<64, true, true>(p, m, st) : launch_bwd_t<64, false, true>(p, m, st);
-  return p.out_bf16 ? launch_bwd_t<64, true, false>(p, m, st) : launch_bwd_t<64, false, false>(p, m, st);
+}
+
+template <int HD, bool OB>
+static cudaError_t launch_bwd_e(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
+  return p.exact ? launch_bwd_n<HD, OB, true>(p, m, st) : launch_bwd_n<HD, OB, false>(p, m, st);
+}
+
+cudaError_t launch_bwd(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
+  if (p.d == 128) return p.out_bf16 ? launch_bwd_e<128, true>(p, m, st) : launch_bwd_e<128, false>(p, m, st);
+  return p.out_bf16 ? launch_bwd_e<64, true>(p, m, st) : launch_bwd_e<64, false>(p, m, st);
 }
 
 }  // namespace flamia

@@ -58,7 +58,9 @@ __device__ __forceinline__ void dbg_dump_phat1(uint8_t* dc, int32_t* de, int T, 
 }
 
 struct WsLayout {
-  size_t header, tile_prefix, blk32_prefix, fwd_items, bwd_items, keys_a, keys_b, dq_acc, total;
+  size_t header, tile_prefix, blk32_prefix, fwd_items, bwd_items, keys_a, keys_b, dq_acc;
+  size_t nv_q, nv_k;       // mixed path: bf16 [T][H][d] / [T][Hkv][d], NVFP4 values without the token scale
+  size_t total;
   int32_t max_items;       // upper bound of tiles: ceil(T/128) + n_seq
   int32_t sort_n;          // max_items rounded up to the block-sort size
 };
@@ -80,6 +82,11 @@ inline WsLayout ws_layout(const flamia_problem_t& p) {
   L.keys_a = o; o = align256(o + sizeof(uint64_t) * L.sort_n * 2);
   L.keys_b = o; o = align256(o + sizeof(uint64_t) * L.sort_n * 2);
   L.dq_acc = o; o = align256(o + sizeof(float) * (size_t)p.T * p.H * p.d);
+  L.nv_q = L.nv_k = 0;
+  if (p.path == FLAMIA_PATH_NVFP4_FP8) {
+    L.nv_q = o; o = align256(o + 2 * (size_t)p.T * p.H * p.d);
+    L.nv_k = o; o = align256(o + 2 * (size_t)p.T * p.Hkv * p.d);
+  }
   L.total = o;
   return L;
 }
@@ -317,6 +324,22 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, uint32
                                                   uint32_t a_sf_id, uint32_t b_sf_id) {
   return (b_sf_id << 4) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
          (a_sf_id << 29);
+}
+
+// Instruction descriptor, kind::f16 with bf16 A and B, fp32 accumulate:
+// c_format(4-5)=1 (F32), a_format(7-9)=1 (BF16), b_format(10-12)=1 (BF16),
+// K-major A and B, N>>3 in 17-22, M>>4 in 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem], bf16 inputs (16 K-elements), fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem], E4M3 inputs, fp32 accumulate.

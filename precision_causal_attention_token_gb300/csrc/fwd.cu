@@ -33,10 +33,10 @@ constexpr int kFwdThreads = kFwdSoftmax + 64;
 constexpr int kFwdWarpProd = 16, kFwdWarpMma = 17;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColSFA0 = 384, kColSFA1 = 392, kColSFB = 400;
 
-template <int HD>
+template <int HD, bool NV4>
 struct __align__(1024) FwdTiles {
-  uint8_t q[kTile * HD];
-  uint8_t k[kFwdStages][kTile * HD];
+  uint8_t q[score_tile_bytes<HD, NV4>()];
+  uint8_t k[kFwdStages][score_tile_bytes<HD, NV4>()];
   uint8_t v[kFwdStages][kTile * HD];
   uint8_t p[2][kTile * kTile];
 };
@@ -55,9 +55,9 @@ struct FwdCtl {
   int abort_flag;
 };
 
-template <int HD>
+template <int HD, bool NV4>
 constexpr size_t fwd_smem_bytes() {
-  return sizeof(FwdTiles<HD>) + sizeof(FwdCtl) + 1024;
+  return sizeof(FwdTiles<HD, NV4>) + sizeof(FwdCtl) + 1024;
 }
 
 // K-major operand with rows of `row_bytes` (128 or 64), swizzle = row size.
@@ -69,14 +69,19 @@ __device__ __forceinline__ uint64_t desc_mnmajor(const uint8_t* tile, uint32_t b
   return smem_desc(smem_u32(tile) + byte_off, 8 * row_bytes, 8 * row_bytes, row_bytes == 128 ? kSwz128 : kSwz64);
 }
 
-template <int HD, bool OUT_BF16, bool EXACT>
+// NV4: the mixed path (scores from the NVFP4 payload, bf16 operand tiles,
+// per-token fp32 factors g_Q(i) g_K(j) applied with the softmax scale).
+template <int HD, bool OUT_BF16, bool EXACT, bool NV4>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-               const __grid_constant__ CUtensorMap map_v) {
+               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_qn,
+               const __grid_constant__ CUtensorMap map_kn) {
+  constexpr bool PERKEY = EXACT || NV4;  // the key factor varies within a 32-key block
+  constexpr int kQKBytes = score_tile_bytes<HD, NV4>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  FwdTiles<HD>& tl = *reinterpret_cast<FwdTiles<HD>*>(base);
-  FwdCtl& c = *reinterpret_cast<FwdCtl*>(base + sizeof(FwdTiles<HD>));
+  FwdTiles<HD, NV4>& tl = *reinterpret_cast<FwdTiles<HD, NV4>*>(base);
+  FwdCtl& c = *reinterpret_cast<FwdCtl*>(base + sizeof(FwdTiles<HD, NV4>));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.H / p.Hkv;
   const int n_work = p.hdr->n_items * p.H;
@@ -112,6 +117,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     prefetch_tensormap(&map_q);
     prefetch_tensormap(&map_k);
     prefetch_tensormap(&map_v);
+    if (NV4) {
+      prefetch_tensormap(&map_qn);
+      prefetch_tensormap(&map_kn);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -137,8 +146,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
       if (!(ok = mbar_wait_warp(&c.q_empty, (qc & 1) ^ 1, abort_flag, hdr, 0x201))) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&c.q_full, kTile * HD);
-        tma_load_3d(tl.q, &map_q, &c.q_full, 0, h, q0);
+        mbar_arrive_expect_tx(&c.q_full, kQKBytes);
+        load_score_tile<HD, NV4>(tl.q, &map_q, &map_qn, &c.q_full, h, q0);
       }
       ++qc;
       for (int kt = 0; kt < n_kt; ++kt, ++kv) {
@@ -149,17 +158,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int jj = 0; jj < 4; ++jj) {
           const int j = lane * 4 + jj, key = kTile * kt + j;
           int ek = 0, ev = 0;
+          float gk = 1.f;
           if (key < len) {
             ek = (int)__ldg(p.k_sc + (size_t)hk * p.T + ds + key) - 127;
             ev = (int)__ldg(p.v_sc + (size_t)hk * p.T + ds + key) - 127;
+            if (NV4) gk = __ldg(p.k_g + (size_t)hk * p.T + ds + key);
           }
-          c.kf[st][j] = pow2_127(ek);
+          c.kf[st][j] = NV4 ? gk : pow2_127(ek);
           c.vf[st][j] = (float)ev;
           c.vinv[st][j] = pow2_127(-ev);
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&c.k_full[st], kTile * HD);
-          tma_load_3d(tl.k[st], &map_k, &c.k_full[st], 0, hk, ds + kTile * kt);
+          mbar_arrive_expect_tx(&c.k_full[st], kQKBytes);
+          load_score_tile<HD, NV4>(tl.k[st], &map_k, &map_kn, &c.k_full[st], hk, ds + kTile * kt);
         } else {
           mbar_arrive(&c.k_full[st]);
         }
@@ -175,7 +186,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (elect_one()) {
       uint32_t kv = 0, qc = 0, sc = 0, pc = 0, ic = 0;
       bool ok = true;
-      const uint32_t id_s = idesc_f8(128, 128, 0, 0);
       for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
         const int pair = w / p.H;
         const int2 it = p.fwd_items[pair];
@@ -191,10 +201,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!(ok = mbar_wait(&c.k_full[st], ph, abort_flag, hdr, 0x212))) break;
             if (!(ok = mbar_wait(&c.s_free[sb], sph ^ 1, abort_flag, hdr, 0x213))) break;
             tc_fence_after();
-            const uint32_t d_s = tb + (sb ? kColS1 : kColS0);
-#pragma unroll
-            for (int kk = 0; kk < HD / 32; ++kk)
-              mma_f8(d_s, desc_kmajor(tl.q, 32 * kk, HD), desc_kmajor(tl.k[st], 32 * kk, HD), id_s, kk > 0);
+            issue_scores<HD, NV4>(tb + (sb ? kColS1 : kColS0), tl.q, tl.k[st]);
             tc_commit(&c.s_full[sb]);
             tc_commit(&c.k_empty[st]);
             if (kt == n_kt - 1) tc_commit(&c.q_empty);
@@ -243,8 +250,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
       const int i_loc = kTile * it.y + r;
       const bool row_ok = i_loc < len;
-      const int eq = row_ok ? (int)__ldg(p.q_sc + (size_t)h * p.T + q0 + r) - 127 : 0;
-      const float rowc = p.c_log2 * pow2_127(eq);
+      float rowc;
+      if constexpr (NV4) {
+        rowc = p.c_log2 * (row_ok ? __ldg(p.q_g + (size_t)h * p.T + q0 + r) : 1.f);
+      } else {
+        const int eq = row_ok ? (int)__ldg(p.q_sc + (size_t)h * p.T + q0 + r) - 127 : 0;
+        rowc = p.c_log2 * pow2_127(eq);
+      }
       int m_ref = kEmptyBlock;
       float l_run = 0.f;  // this thread's share of the normaliser (its key block)
       for (int kt = 0; ok && kt < n_kt; ++kt, ++kv, ++sc, ++pc) {
@@ -265,9 +277,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const float* vfb = c.vf[st] + 32 * blk;
           // the diagonal tile (or a document's last tile) is the only one with masked keys
           if (kt == n_kt - 1)
-            Eb = phat_logits1<EXACT, true>(t_s, y, rowc, kfb, vfb, i_loc, key0 + 32 * blk, len, p.causal);
+            Eb = phat_logits1<PERKEY, true>(t_s, y, rowc, kfb, vfb, i_loc, key0 + 32 * blk, len, p.causal);
           else
-            Eb = phat_logits1<EXACT, false>(t_s, y, rowc, kfb, vfb, i_loc, key0 + 32 * blk, len, p.causal);
+            Eb = phat_logits1<PERKEY, false>(t_s, y, rowc, kfb, vfb, i_loc, key0 + 32 * blk, len, p.causal);
           const float* vi = c.vinv[st] + 32 * blk;
           float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -408,25 +420,35 @@ static int num_sms() {
   return n;
 }
 
-template <int HD, bool OB, bool EX>
+template <int HD, bool OB, bool EX, bool NV4>
 static cudaError_t launch_fwd_t(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
-  const size_t smem = fwd_smem_bytes<HD>();
+  const size_t smem = fwd_smem_bytes<HD, NV4>();
+  static_assert(fwd_smem_bytes<HD, NV4>() <= 232448, "shared memory");
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(fwd_kernel<HD, OB, EX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(fwd_kernel<HD, OB, EX, NV4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   long work = (long)p.max_items * p.H;
   int grid = (int)(work < num_sms() ? work : num_sms());
-  fwd_kernel<HD, OB, EX><<<grid, kFwdThreads, smem, st>>>(p, m.q, m.k, m.v);
+  fwd_kernel<HD, OB, EX, NV4><<<grid, kFwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.qn, m.kn);
   return cudaGetLastError();
+}
+
+template <int HD, bool OB, bool EX>
+static cudaError_t launch_fwd_n(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
+  if constexpr (EX) {  // the exact option is not offered on the mixed path (the host rejects it)
+    return p.nvfp4 ? cudaErrorNotSupported : launch_fwd_t<HD, OB, EX, false>(p, m, st);
+  } else {
+    return p.nvfp4 ? launch_fwd_t<HD, OB, EX, true>(p, m, st) : launch_fwd_t<HD, OB, EX, false>(p, m, st);
+  }
 }
 
 template <int HD, bool OB>
 static cudaError_t launch_fwd_e(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
-  return p.exact ? launch_fwd_t<HD, OB, true>(p, m, st) : launch_fwd_t<HD, OB, false>(p, m, st);
+  return p.exact ? launch_fwd_n<HD, OB, true>(p, m, st) : launch_fwd_n<HD, OB, false>(p, m, st);
 }
 
 cudaError_t launch_fwd(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {

@@ -11,6 +11,7 @@ struct QuantArgs {
   uint8_t* codes4;   // [T][heads][d/2]   (NVFP4 operand)
   uint8_t* scales4;  // [T][heads][d/16]
   float* gscale4;    // [heads][T]
+  __nv_bfloat16* xnv;  // [T][heads][d] NVFP4 value e2m1 * block scale (exact in bf16), no token scale
   const void* O;     // [T][heads][d]     (dO role)
   float* D;          // [heads][T]
   int T, heads;
@@ -43,6 +44,9 @@ struct AttnParams {
   const uint8_t* k_sc;  // [Hkv][T]
   const uint8_t* v_sc;  // [Hkv][T]
   const uint8_t* do_sc; // [H][T]
+  const float* q_g;     // mixed path: per-token fp32 scale of Q's NVFP4 payload [H][T]
+  const float* k_g;     // mixed path: of K's [Hkv][T]
+  int nvfp4;            // 1: scores from the NVFP4 payload (bf16 operands in the workspace)
   const float* D;       // [H][T]
   int32_t* m;           // [H][T]
   float* l;             // [H][T]
@@ -55,6 +59,7 @@ struct AttnParams {
 
 struct AttnMaps {
   CUtensorMap q, k, v, dO;
+  CUtensorMap qn, kn;  // mixed path: bf16 NVFP4 values, boxes of 128 tokens x 64 values (128B swizzle)
   CUtensorMap dq;  // fp32 dQ accumulator [T][H][d], boxes of 128 rows x 32 values (reduce-add target)
 };
 

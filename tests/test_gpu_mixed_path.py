@@ -1,0 +1,116 @@
+"""Mixed NVFP4/FP8 path on the GPU against the oracle's mixed path: QK^T from
+the NVFP4 payload (E2M1 codes, E4M3 16-element block scales, fp32 per-token
+scale), everything else MXFP8.  Same bar as the MXFP8 path: O, dQ, dK, dV
+within 2e-2 of the row max-abs with cosine >= 0.9999 against the oracle's
+result of the same quantization; the recomputed P^ equals the forward's."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import precision_causal_attention_token_gb300 as fl
+import synth
+from gpu_helpers import compare, cosine, np_of, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+NV = dict(path=fl.PATH_NVFP4_FP8)
+NV_ORC = dict(path=oracle.PATH_NVFP4_FP8)
+
+
+def _check(tc, ref, noise=None):
+    for name in ("O", "dQ", "dK", "dV"):
+        compare(f"mixed {name}", getattr(tc, name), ref[name], noise=None if noise is None else noise.get(name))
+    lse = np_of(tc.m) + np.log2(np_of(tc.l))
+    assert np.abs(lse - ref["lse2"]).max() < 1e-3
+
+
+CASES = [
+    ("ragged packed bf16", synth.custom([300, 45, 129, 1, 600], H=2, d=128, seed=701), {}),
+    ("GQA H=4 Hkv=2", synth.custom([257, 130, 64], H=4, Hkv=2, d=128, seed=702), {}),
+    ("non-causal", synth.custom([200, 77, 129], H=2, d=128, seed=703), {"causal": False}),
+    ("d=64", synth.custom([190, 66, 300], H=2, d=64, seed=704), {}),
+    ("tiny fp32 d=64", synth.workload(1), {}),
+]
+
+
+@pytest.mark.parametrize("name,w,kw", CASES, ids=[c[0] for c in CASES])
+def test_mixed_parity_small(name, w, kw):
+    tc = run_gpu(w, **kw, **NV)
+    ref = run_oracle(w, **kw, **NV_ORC)
+    # the NVFP4 payload and the MXFP8 codes both match the oracle bit for bit
+    rc, rb, rg = oracle.quantize_nvfp4(w.tensor("q"))
+    packed = tc.q4[0].cpu().numpy()
+    got = np.stack([packed & 0xF, packed >> 4], axis=-1).reshape(rc.shape)
+    assert (got == rc).all()
+    assert (tc.q4[1].cpu().numpy() == rb).all()
+    assert (tc.q4[2].cpu().numpy() == rg).all()
+    assert (tc.q_codes.cpu().numpy() == ref["q_codes"]).all()
+    _check(tc, ref)
+
+
+def test_mixed_outlier_channels():
+    # x20 channels in Q and K: near one-hot softmax, dS cancels down to O's
+    # rounding; compare against the oracle within its own O-rounding sensitivity
+    w = synth.custom([180, 300], H=2, d=128, seed=705, outlier_channels=2)
+    tc = run_gpu(w, **NV)
+    q, k, v, do = (w.tensor(n) for n in ("q", "k", "v", "do"))
+    ref = oracle.train_call(q, k, v, do, w.cu_seqlens, path=oracle.PATH_NVFP4_FP8, out_dtype="bf16")
+    r64 = oracle.train_call(q, k, v, do, w.cu_seqlens, path=oracle.PATH_NVFP4_FP8, out_dtype="f64")
+    _check(tc, ref, noise={n: ref[n] - r64[n] for n in ("dQ", "dK", "dV")})
+
+
+def test_mixed_cosine_to_unquantized_reference():
+    # the pages' band for the mixed path: O about 0.992, dQ about 0.991
+    w = synth.custom([512, 300], H=2, d=128, seed=706)
+    tc = run_gpu(w, **NV)
+    q, k, v, do = (w.tensor(n) for n in ("q", "k", "v", "do"))
+    ref = oracle.train_call(q, k, v, do, w.cu_seqlens, quantize=False)
+    c = {n: cosine(np_of(getattr(tc, n)), ref[n]) for n in ("O", "dQ", "dK", "dV")}
+    assert c["O"] >= 0.99 and c["dQ"] >= 0.985 and c["dK"] >= 0.985 and c["dV"] >= 0.99, c
+
+
+def test_mixed_forward_and_backward_phat_bit_identical():
+    """The backward rebuilds the forward's P^ codes and block exponents bit for
+    bit on the mixed path too (same NVFP4 scores, same per-key factors)."""
+    w = synth.custom([200, 70, 129], H=2, d=128, seed=707)
+    dev = torch.device("cuda")
+    q, k, v, do = (torch.from_numpy(w.tensor(n)).to(dev, torch.bfloat16) for n in ("q", "k", "v", "do"))
+    cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
+    tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu, path=fl.PATH_NVFP4_FP8)
+    tc.plan()
+    buf = lambda: (torch.zeros(w.H, w.T, w.T, dtype=torch.uint8, device=dev),
+                   torch.full((w.H, w.T, w.T), -7777, dtype=torch.int32, device=dev))
+    cf, ef = buf()
+    fl.flamia_debug_set_phat_dump(tc.ws, cf, ef)
+    tc.forward(q, k, v)
+    cb, eb = buf()
+    fl.flamia_debug_set_phat_dump(tc.ws, cb, eb)
+    tc.backward(do)
+    fl.flamia_debug_set_phat_dump(tc.ws, None, None)
+    torch.cuda.synchronize()
+    assert fl.flamia_get_device_status(tc.ws) == fl.OK
+    assert (ef != -7777).sum().item() > 0
+    assert torch.equal(ef, eb)
+    assert torch.equal(cf, cb)
+    assert (cf != 0).float().mean().item() > 0.01
+
+
+def test_mixed_full_size_sampled_against_oracle():
+    """The mixed-path workload (4 x 32768 packed, log-normal documents, x20
+    outlier channels) in full; the oracle recomputes one (document, head)
+    slice, which equals the full call's outputs there."""
+    w = synth.workload(4)
+    q, k, v, do = (w.tensor(n) for n in ("q", "k", "v", "do"))
+    tc = run_gpu(w, inputs=(q, k, v, do), **NV)
+    lens = np.diff(w.cu_seqlens)
+    doc = int(np.argsort(lens)[len(lens) // 2])
+    head = 9
+    s, e = int(w.cu_seqlens[doc]), int(w.cu_seqlens[doc + 1])
+    sl = lambda a: np.ascontiguousarray(a[s:e, head:head + 1])
+    cu1 = np.array([0, e - s], np.int32)
+    ref = oracle.train_call(sl(q), sl(k), sl(v), sl(do), cu1, path=oracle.PATH_NVFP4_FP8, out_dtype="bf16")
+    r64 = oracle.train_call(sl(q), sl(k), sl(v), sl(do), cu1, path=oracle.PATH_NVFP4_FP8, out_dtype="f64")
+    for name in ("O", "dQ", "dK", "dV"):
+        compare(f"mixed {name} doc {doc} head {head}", getattr(tc, name)[s:e, head:head + 1], ref[name],
+                noise=None if name == "O" else ref[name] - r64[name])
