@@ -95,10 +95,11 @@ __device__ __forceinline__ uint64_t bdesc_mn(const uint8_t* t, uint32_t off, uin
   return smem_desc(smem_u32(t) + off, 8 * rb, 8 * rb, rb == 128 ? kSwz128 : kSwz64);
 }
 
+// Max over the warp of a non-negative float (no NaN): with the sign bit
+// cleared (a -0 counts as 0) the bit patterns order like unsigned integers,
+// so one integer warp reduction replaces a five-step shuffle chain.
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int s = 16; s >= 1; s >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, s));
-  return v;
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7FFFFFFFu));
 }
 
 __device__ __forceinline__ uint32_t sf_byte(int e) { return (uint32_t)min(max(e + 127, 0), 254); }

@@ -108,6 +108,16 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
     if (t < ntok) raw[t].load(x + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL);
     else raw[t].zero();
   }
+  // dO role: O's rows are loaded up front as well, so their latency overlaps
+  // the exponent work instead of stalling each token's dot product
+  RawRow<TO, WITH_D ? EPL : 2> orow[WITH_D ? 32 : 1];
+  if constexpr (WITH_D) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      if (t < ntok) orow[t].load(static_cast<const TO*>(a.O) + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL);
+      else orow[t].zero();
+    }
+  }
   // per-token maxima (lane t <- token t) also feed the NVFP4 token scale
   float pmax[32];
 #pragma unroll
@@ -151,14 +161,12 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
         *reinterpret_cast<uint16_t*>(dst) = (uint16_t)cw;
       }
       if constexpr (WITH_D) {
-        RawRow<TO, EPL> o;
-        o.load(static_cast<const TO*>(a.O) + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL);
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < EPL; e += 2) {
           const float2 d2 = unpack_e4m3x2((uint16_t)(cw >> (8 * e)));
-          acc = fmaf(mul_pow2(d2.x, e_t), o.at(e), acc);
-          acc = fmaf(mul_pow2(d2.y, e_t), o.at(e + 1), acc);
+          acc = fmaf(mul_pow2(d2.x, e_t), orow[t].at(e), acc);
+          acc = fmaf(mul_pow2(d2.y, e_t), orow[t].at(e + 1), acc);
         }
         dpart[t] = acc;
       }
@@ -214,7 +222,7 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
 
 // Grid-stride over the units of up to three tensors (Q, K, V share a launch).
 template <typename TIn, typename TO, int HD, bool WITH_D, bool NVFP4>
-__global__ void __launch_bounds__(128, 3) quantize_kernel(const __grid_constant__ QuantBatch qb,
+__global__ void __launch_bounds__(128, WITH_D ? 2 : 3) quantize_kernel(const __grid_constant__ QuantBatch qb,
                                                           const int32_t* __restrict__ cu,
                                                           const int32_t* __restrict__ blk_prefix, int n_seq,
                                                           WsHeader* hdr) {
@@ -239,8 +247,8 @@ __global__ void __launch_bounds__(128, 3) quantize_kernel(const __grid_constant_
 cudaError_t launch_quantize(const QuantBatch& qb, int d, int in_bf16, int o_bf16, bool with_D, bool nvfp4,
                             const int32_t* cu, const int32_t* blk_prefix, int n_seq, WsHeader* hdr,
                             int max_units, int n_sms, cudaStream_t st) {
-  int blocks = (max_units + 3) / 4;  // four warps per block, one unit per warp
-  const int cap = 3 * n_sms * 4;      // three resident blocks per SM, four waves of grid stride
+  int blocks = (max_units + 3) / 4;                 // four warps per block, one unit per warp
+  const int cap = (with_D ? 2 : 3) * n_sms * 4;     // resident blocks per SM x four waves of grid stride
   blocks = blocks < 1 ? 1 : (blocks > cap ? cap : blocks);
 #define FLAMIA_QL(TIN, TO_, HD_, WD, NV) \
   quantize_kernel<TIN, TO_, HD_, WD, NV><<<blocks, 128, 0, st>>>(qb, cu, blk_prefix, n_seq, hdr)
