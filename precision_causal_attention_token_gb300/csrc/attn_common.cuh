@@ -45,28 +45,42 @@ __device__ __forceinline__ int phat_block_logits(float (&a)[32], float rowc, con
   float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
   const float sb = __fmul_rn(rowc, kf[0]);
 #pragma unroll
-  for (int jj = 0; jj < 32; ++jj) {
-    const float sc = EXACT ? __fmul_rn(rowc, kf[jj]) : sb;
-    float y = score_to_y(a[jj], sc, vf[jj]);
-    if (NEED_MASK && !visible(i_loc, key + jj, len, causal)) y = -INFINITY;
-    a[jj] = y;
-    m4[jj & 3] = fmaxf(m4[jj & 3], y);
+  for (int j4 = 0; j4 < 8; ++j4) {
+    const float4 v4 = *reinterpret_cast<const float4*>(vf + 4 * j4);  // 16-byte aligned factor vectors
+    const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+    float kk[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (EXACT) {
+      const float4 k4 = *reinterpret_cast<const float4*>(kf + 4 * j4);
+      kk[0] = k4.x; kk[1] = k4.y; kk[2] = k4.z; kk[3] = k4.w;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int jj = 4 * j4 + e;
+      const float sc = EXACT ? __fmul_rn(rowc, kk[e]) : sb;
+      float y = score_to_y(a[jj], sc, vv[e]);
+      if (NEED_MASK && !visible(i_loc, key + jj, len, causal)) y = -INFINITY;
+      a[jj] = y;
+      m4[e] = fmaxf(m4[e], y);
+    }
   }
   const float M = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
   return (M == -INFINITY) ? kEmptyBlock : phat_block_exp(M);
 }
 
 // p = 2^(y - E) (<= 448 up to the approximation of ex2; the cvt saturates).
+// An empty block (E = kEmptyBlock) has y = -inf everywhere, so p = 0 with no
+// test; a caller that wants zeros for finite y passes E = kZeroCodes.
 __device__ __forceinline__ float phat_value(float y, int E) { return ex2_approx(__fsub_rn(y, (float)E)); }
+constexpr int kZeroCodes = 1 << 30;  // 2^(y - 2^30) = 0 for every finite logit
 
-// P^ codes of one 32-key block from its logits and exponent (all zero for an
-// empty block), as 8 words of 4 E4M3 bytes.
+// P^ codes of one 32-key block from its logits and exponent, as 8 words of
+// 4 E4M3 bytes.
 __device__ __forceinline__ void phat_block_codes(const float (&y)[32], int E, uint32_t (&codes)[8]) {
 #pragma unroll
   for (int q4 = 0; q4 < 8; ++q4) {
     float pv[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) pv[e] = (E == kEmptyBlock) ? 0.f : phat_value(y[4 * q4 + e], E);
+    for (int e = 0; e < 4; ++e) pv[e] = phat_value(y[4 * q4 + e], E);
     codes[q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
   }
 }
@@ -146,6 +160,10 @@ __device__ __forceinline__ void load_score_tile(uint8_t* dst, const CUtensorMap*
     tma_load_3d(dst, map8, bar, 0, head, tok0);
   }
 }
+
+// x * 2^e for e <= 127, flushed to 0 below 2^-126 (for normaliser terms and
+// rescale factors, where such terms are far below fp32 resolution).
+__device__ __forceinline__ float ldexp_fast(float x, int e) { return e >= -126 ? x * exp2i(min(e, 127)) : 0.f; }
 
 // x * 2^e for any integer e (exact while the result stays normal).
 __device__ __forceinline__ float ldexp_f(float x, int e) {

@@ -119,8 +119,9 @@ __device__ __forceinline__ void recompute_phat(uint32_t t_s, int b0, float rowc,
   else
     phat_logits2<EXACT, false>(t0, t1, y, Eb, rowc, kf + 32 * b0, vf + 32 * b0, i_loc, key0 + 32 * b0, len, causal);
   if (!row_ok) Eb[0] = Eb[1] = kEmptyBlock;
-  phat_block_codes(y[0], Eb[0], pcode[0]);
-  phat_block_codes(y[1], Eb[1], pcode[1]);
+  // rows outside the document: finite logits, zero codes
+  phat_block_codes(y[0], row_ok ? Eb[0] : kZeroCodes, pcode[0]);
+  phat_block_codes(y[1], row_ok ? Eb[1] : kZeroCodes, pcode[1]);
 }
 
 // Per-(row, key block) factors of dS and P~: with gb = 2^(Eb - m) / l (0 for

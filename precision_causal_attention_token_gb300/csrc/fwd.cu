@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             float pv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              pv[e] = (Eb == kEmptyBlock) ? 0.f : phat_value(y[4 * q4 + e], Eb);
+              pv[e] = phat_value(y[4 * q4 + e], Eb);  // 0 on an empty block (y = -inf)
               l4[e] = fmaf(pv[e], vv[e], l4[e]);
             }
             codes[q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
@@ -309,14 +309,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int Emax = max(max(Eall[0], Eall[1]), max(Eall[2], Eall[3]));
         int m_new = m_ref;
         if (Emax != kEmptyBlock && (m_ref == kEmptyBlock || Emax > m_ref + 8)) m_new = Emax;
-        const float lsum = (Eb != kEmptyBlock) ? ldexp_f(lb, Eb - m_new) : 0.f;
+        const float lsum = (Eb != kEmptyBlock) ? ldexp_fast(lb, Eb - m_new) : 0.f;
         uint32_t word = 0;
 #pragma unroll
         for (int b = 0; b < 4; ++b)
           if (Eall[b] != kEmptyBlock) word |= (uint32_t)min(max(Eall[b] - m_new + 127, 0), 254) << (8 * b);
         mbar_arrive(&c.k_empty[st]);
         if (row_ok) dbg_dump_phat1(dbg_c, dbg_e, p.T, h, q0 + r, ds + key0, blk, codes, Eb);
-        l_run = (m_ref == kEmptyBlock) ? lsum : ldexp_f(l_run, m_ref - m_new) + lsum;
+        l_run = (m_ref == kEmptyBlock) ? lsum : ldexp_fast(l_run, m_ref - m_new) + lsum;
         // rescale this thread's quarter of the O accumulator row once the
         // previous P^V has landed (warp-uniform: tcgen05.ld/st are
         // warp-collective; lanes whose reference did not move scale by 1)
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const uint32_t pp = pc - 1;
           if (!(ok = mbar_wait_warp(&c.p_free[pp & 1], (pp >> 1) & 1, abort_flag, hdr, 0x223))) break;
           tc_fence_after();
-          const float f = (m_new != m_ref) ? ldexp_f(1.0f, m_ref - m_new) : 1.0f;
+          const float f = (m_new != m_ref) ? ldexp_fast(1.0f, m_ref - m_new) : 1.0f;
           const uint32_t t_o = taddr(tb, q * 32, kColO + blk * OC);
           if constexpr (OC == 32) {
             uint32_t rr[32];
