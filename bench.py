@@ -58,6 +58,25 @@ def _dist():
     return rank, world, local
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest of every rank's `x` (the job's time is its slowest rank's);
+    `x` itself with one process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(flops_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job TFLOP/s: every rank runs the same workload (independent
+    replicas, weak scaling), so the job does world x the work in the slowest
+    rank's time."""
+    return flops_per_rank * world / (ms * 1e-3) / 1e12
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -273,11 +292,8 @@ def run_ours(a):
     ms = t_start.elapsed_time(t_end) / a.steps
     ph = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])  # ms
     quant_ms, fwd_ms, dquant_ms, bwd_ms = ph.mean(axis=0)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = flops * world / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(ms, dev)
+    value = job_rate(flops, world, ms)
 
     # e2e: host (pinned) inputs copied in, results (O, dQ, dK, dV) copied out, every step
     hq, hk, hv, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
@@ -303,8 +319,8 @@ def run_ours(a):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    e2e_val = flops * world / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+    e2e_val = job_rate(flops, world, e2e_ms)
 
     if rank != 0:
         if world > 1:
