@@ -42,8 +42,12 @@ constexpr int kBwdThreads = 512;
 constexpr int kWarpDrain0 = 8, kWarpProd = 12, kWarpMma = 13, kWarpRed = 14;
 constexpr uint32_t kRegCompute = 176, kRegDrain = 80, kRegCtl = 80;
 static_assert(2 * 128 * kRegCompute + 128 * kRegDrain + 128 * kRegCtl <= 65536, "register split");
+// TMEM: dV, dK accumulators; X0 = S; X1 = dP, then (once dP is read) the
+// scale factors at X1 + 64.. and the dQ tile, 64 columns at a time, at X1 + 0.
+// Keeping the scale factors out of X0 lets the next tile's S start as soon as
+// the compute warps have read this tile's S.
 constexpr uint32_t kColDV = 0, kColDK = 128, kColX0 = 256, kColX1 = 384;
-constexpr uint32_t kColSfDV = kColX0 + 0, kColSfDK = kColX0 + 4, kColSfDQ = kColX0 + 8, kColSfOne = kColX0 + 12;
+constexpr uint32_t kColSfDV = kColX1 + 64, kColSfDK = kColX1 + 68, kColSfDQ = kColX1 + 72, kColSfOne = kColX1 + 76;
 
 // NV4 (mixed path): the scores' operands are bf16 NVFP4 values (k holds K's,
 // qn Q's); dK still contracts with the E4M3 Q codes.  dQ then comes from the
@@ -79,6 +83,8 @@ struct BwdCtl {
   uint8_t xdq[2][kTile][4];  // [parity][query row][key block] dQ scale bytes
   uint64_t kv_full, kv_empty, qd_full[2], qd_empty[2];
   uint64_t s_full, dp_full, ds_full, mm_done, x1_free, acc_full, acc_free, xch_bar, dqs_full, dqs_free;
+  uint64_t x0_free, dq_lo_full, dq_lo_free;
+  ItemRing ring;  // this CTA's work items, in the order all roles process them
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -308,12 +314,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&c.dp_full, 1);
     mbar_init(&c.ds_full, kBwdCompute);
     mbar_init(&c.mm_done, 1);
-    mbar_init(&c.x1_free, DQ ? 128 : kBwdCompute);  // drain warps (DQ) or compute warps read X1 last
+    mbar_init(&c.x1_free, 128);     // drain warps: the dQ tile has left X1
+    mbar_init(&c.x0_free, kBwdCompute);  // compute warps: S has been read
+    mbar_init(&c.dq_lo_full, 1);
+    mbar_init(&c.dq_lo_free, 128);
     mbar_init(&c.acc_full, 1);
     mbar_init(&c.acc_free, 128);  // the drain warpgroup stores dK / dV
     mbar_init(&c.xch_bar, kBwdCompute);
     mbar_init(&c.dqs_full, 128);
     mbar_init(&c.dqs_free, 1);
+    // readers: the MMA thread, the dQ reducer (DQ), four drain and eight compute warps
+    item_ring_init(c.ring, 1 + (DQ ? 1 : 0) + 4 + kBwdCompute / 32);
     c.abort_flag = 0;
     fence_mbar_init();
   }
@@ -341,7 +352,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ producer
     uint32_t ic = 0, ii = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++ic) {
+    for (uint32_t n_it = 0; ok; ++n_it, ++ic) {
+      const int w = item_publish(c.ring, n_it, &hdr->bwd_counter, n_work, lane, abort_flag, hdr, 0x304, ok);
+      if (w < 0) break;
       const int pair = w / p.Hkv, hk = w - pair * p.Hkv;
       const int2 it = p.bwd_items[pair];
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
@@ -402,27 +415,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t ic = 0, ii = 0;
       bool ok = true;
       const uint32_t id_sp = idesc_f8(128, 128, 0, 0);
-      for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++ic) {
+      for (uint32_t n_it = 0; ok; ++n_it, ++ic) {
+        const int w = item_get(c.ring, n_it, abort_flag, hdr, 0x318, ok);
+        if (w < 0) break;
         const int pair = w / p.Hkv;
         const int2 it = p.bwd_items[pair];
         const int len = __ldg(p.cu + it.x + 1) - __ldg(p.cu + it.x);
         const int n_t = (len + kTile - 1) / kTile, q_first = p.causal ? it.y : 0;
         const int n_iter = G * (n_t - q_first);
         if (!(ok = mbar_wait(&c.kv_full, ic & 1, abort_flag, hdr, 0x311))) break;
-        for (int t = 0; ok && t < n_iter; ++t, ++ii) {
-          const int qs = ii & 1;
-          if (!(ok = mbar_wait(&c.qd_full[qs], (ii >> 1) & 1, abort_flag, hdr, 0x312))) break;
-          // X0 holds the previous iteration's scale factors until its MMAs finish
-          if (ii > 0 && !(ok = mbar_wait(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x313))) break;
+        // S of query tile ii into X0 (Q^ of stage ii & 1, K^ of this item)
+        auto issue_s = [&](uint32_t i_s) -> bool {
+          const int qs_s = i_s & 1;
+          if (!mbar_wait(&c.qd_full[qs_s], (i_s >> 1) & 1, abort_flag, hdr, 0x312)) return false;
+          // X0 is free once the compute warps have read the previous S
+          if (!mbar_wait(&c.x0_free, (i_s & 1) ^ 1, abort_flag, hdr, 0x313)) return false;
           tc_fence_after();
-          issue_scores<HD, NV4>(tb + kColX0, NV4 ? tl.qn[qs] : tl.q[qs], tl.k);
+          issue_scores<HD, NV4>(tb + kColX0, NV4 ? tl.qn[qs_s] : tl.q[qs_s], tl.k);
           tc_commit(&c.s_full);
-          if (!(ok = mbar_wait(&c.x1_free, (ii & 1) ^ 1, abort_flag, hdr, 0x314))) break;
+          return true;
+        };
+        // dP of query tile ii into X1
+        auto issue_dp = [&](uint32_t i_p) -> bool {
+          // X1 is free once the previous tile's MMAs have read their scale
+          // factors there and (DQ) its dQ tile has been drained
+          if constexpr (DQ) {
+            if (!mbar_wait(&c.x1_free, (i_p & 1) ^ 1, abort_flag, hdr, 0x314)) return false;
+          } else {
+            if (i_p > 0 && !mbar_wait(&c.mm_done, (i_p - 1) & 1, abort_flag, hdr, 0x314)) return false;
+          }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < HD / 32; ++kk)
-            mma_f8(tb + kColX1, bdesc_k(tl.dO[qs], 32 * kk, HD), bdesc_k(tl.v, 32 * kk, HD), id_sp, kk > 0);
+            mma_f8(tb + kColX1, bdesc_k(tl.dO[i_p & 1], 32 * kk, HD), bdesc_k(tl.v, 32 * kk, HD), id_sp, kk > 0);
           tc_commit(&c.dp_full);
+          return true;
+        };
+        // the first tile of the item: S and dP; later tiles' S and dP are
+        // issued one tile ahead (S as soon as X0 is read, dP once X1 is free)
+        if (!(ok = issue_s(ii) && issue_dp(ii))) break;
+        for (int t = 0; ok && t < n_iter; ++t, ++ii) {
+          const int qs = ii & 1;
+          if (t + 1 < n_iter && !(ok = issue_s(ii + 1))) break;
           if (!(ok = mbar_wait(&c.ds_full, ii & 1, abort_flag, hdr, 0x315))) break;
           if (t == 0 && !(ok = mbar_wait(&c.acc_free, (ic & 1) ^ 1, abort_flag, hdr, 0x316))) break;
           tc_fence_after();
@@ -436,13 +470,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                      idesc_mxf8(128, HD, 1, 1, kk, kk), tb + kColSfDK, tb + kColSfOne, acc);
           }
           if constexpr (DQ) {
+            // dQ = dS^ K^ in halves of 64 columns through X1[0, 64): the
+            // drain warps empty the first half while the second is computed
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)  // contraction over the 128 keys
-              mma_mxf8(tb + kColX1, bdesc_k(tl.ds, 32 * kk, 128), bdesc_mn(tl.k, kk * 32 * HD, HD),
-                       idesc_mxf8(128, HD, 0, 1, kk, kk), tb + kColSfDQ, tb + kColSfOne, kk > 0 ? 1u : 0u);
+            for (int half = 0; half < HD / 64; ++half) {
+              if (half == 1) {
+                tc_commit(&c.dq_lo_full);
+                if (!(ok = mbar_wait(&c.dq_lo_free, ii & 1, abort_flag, hdr, 0x317))) break;
+                tc_fence_after();
+              }
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)  // contraction over the 128 keys
+                mma_mxf8(tb + kColX1, bdesc_k(tl.ds, 32 * kk, 128), bdesc_mn(tl.k, kk * 32 * HD + 64 * half, HD),
+                         idesc_mxf8(128, 64, 0, 1, kk, kk), tb + kColSfDQ, tb + kColSfOne, kk > 0 ? 1u : 0u);
+            }
+            if (!ok) break;
           }
           tc_commit(&c.mm_done);
           tc_commit(&c.qd_empty[qs]);
+          if (t + 1 < n_iter && !(ok = issue_dp(ii + 1))) break;
           if (t == n_iter - 1) {
             tc_commit(&c.acc_full);
             tc_commit(&c.kv_empty);
@@ -456,7 +502,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (DQ && lane == 0) {
       uint32_t ii = 0;
       bool ok = true;
-      for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+      for (uint32_t n_it = 0; ok; ++n_it) {
+        const int w = item_get(c.ring, n_it, abort_flag, hdr, 0x332, ok);
+        if (w < 0) break;
         const int pair = w / p.Hkv, hk = w - pair * p.Hkv;
         const int2 it = p.bwd_items[pair];
         const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
@@ -491,7 +539,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float sm_scale = p.softmax_scale;
     uint32_t ic = 0, ii = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++ic) {
+    for (uint32_t n_it = 0; ok; ++n_it, ++ic) {
+      const int w = item_get_warp(c.ring, n_it, lane, abort_flag, hdr, 0x344, ok);
+      if (w < 0) break;
       const int pair = w / p.Hkv, hk = w - pair * p.Hkv;
       const int2 it = p.bwd_items[pair];
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
@@ -499,17 +549,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int n_iter = G * (n_t - q_first);
       if constexpr (DQ) {
         for (int t = 0; ok && t < n_iter; ++t, ++ii) {
-          if (!(ok = mbar_wait_warp(&c.mm_done, ii & 1, abort_flag, hdr, 0x341))) break;
-          if (!(ok = mbar_wait_warp(&c.dqs_free, (ii & 1) ^ 1, abort_flag, hdr, 0x342))) break;
-          tc_fence_after();
+          // the dQ tile arrives in X1[0, 64) in halves of 64 columns (d = 128)
+          // or whole (d = 64); each half goes to two staging boxes
+#pragma unroll
+          for (int half = 0; half < HD / 64; ++half) {
+            if (half == 0 && HD == 128) {
+              if (!(ok = mbar_wait_warp(&c.dq_lo_full, ii & 1, abort_flag, hdr, 0x343))) break;
+            } else {
+              if (!(ok = mbar_wait_warp(&c.mm_done, ii & 1, abort_flag, hdr, 0x341))) break;
+            }
+            if (half == 0 && !(ok = mbar_wait_warp(&c.dqs_free, (ii & 1) ^ 1, abort_flag, hdr, 0x342))) break;
+            tc_fence_after();
 #pragma unroll 1
-          for (int cb = 0; cb < HD / 32; ++cb) {
-            uint32_t rq[32];
-            tmem_ld32(taddr(tb, qq * 32, kColX1 + 32 * cb), rq);
-            tmem_ld_wait_regs(rq);
-            store_row_box(tl.dqs + cb * (kTile * 32), r, rq);
+            for (int cb = 0; cb < 2; ++cb) {
+              uint32_t rq[32];
+              tmem_ld32(taddr(tb, qq * 32, kColX1 + 32 * cb), rq);
+              tmem_ld_wait_regs(rq);
+              store_row_box(tl.dqs + (2 * half + cb) * (kTile * 32), r, rq);
+            }
+            tc_fence_before();
+            if (half == 0 && HD == 128) mbar_arrive(&c.dq_lo_free);
           }
-          tc_fence_before();
+          if (!ok) break;
           mbar_arrive(&c.x1_free);
           fence_proxy_async_smem();
           mbar_arrive(&c.dqs_full);
@@ -543,7 +604,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int32_t* const dbg_e = hdr->dbg_eb;
     uint32_t ic = 0, ii = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++ic) {
+    for (uint32_t n_it = 0; ok; ++n_it, ++ic) {
+      const int w = item_get_warp(c.ring, n_it, lane, abort_flag, hdr, 0x329, ok);
+      if (w < 0) break;
       const int pair = w / p.Hkv, hk = w - pair * p.Hkv;
       const int2 it = p.bwd_items[pair];
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
@@ -566,6 +629,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const bool need_mask = p.causal ? (qt == it.y) : (it.y == n_t - 1);
           recompute_phat<PERKEY>(taddr(tb, q * 32, kColX0), b0, rv.rowc, c.kf, c.vf, i_loc, key0, len, p.causal,
                                 need_mask, row_ok, pcode, Eb);
+          tc_fence_before();
+          mbar_arrive(&c.x0_free);  // S has been read: X0 may take the next S
           if (row_ok) dbg_dump_phat2(dbg_c, dbg_e, p.T, h, ds + i_loc, ds + key0, b0, pcode, Eb);
           if (!(ok = mbar_wait_warp(&c.dp_full, ii & 1, abort_flag, hdr, 0x323))) break;
           // the previous iteration's MMAs must be done with the P~ / dS tiles
@@ -576,10 +641,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld32(taddr(tb, q * 32, kColX1 + 32 * b0), dp[0]);
           tmem_ld32(taddr(tb, q * 32, kColX1 + 32 * (b0 + 1)), dp[1]);
           tmem_ld_wait_regs(dp[0], dp[1]);
-          if constexpr (!DQ) {  // dP has been read: X1 may take the next dP
-            tc_fence_before();
-            mbar_arrive(&c.x1_free);
-          }
 #pragma unroll
           for (int bb = 0; bb < 2; ++bb) {
             const int b = b0 + bb;
@@ -687,6 +748,7 @@ struct DqCtl {
   uint8_t xdq[2][kTile][4];  // [parity][query row][key block] dQ scale bytes
   uint64_t qd_full, qd_empty, kv_full[kDqStages], kv_empty[kDqStages];
   uint64_t s_full, dp_full, dp_free, ds_full, mm_done, dq_full, dq_free, xch_bar;
+  ItemRing ring;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -727,6 +789,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&c.dq_full, 1);
     mbar_init(&c.dq_free, kBwdCompute);
     mbar_init(&c.xch_bar, kBwdCompute);
+    item_ring_init(c.ring, 1 + kBwdCompute / 32);  // the MMA thread and the compute warps
     c.abort_flag = 0;
     fence_mbar_init();
   }
@@ -739,7 +802,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   if (warp == kDqWarpProd) {
     uint32_t ic = 0, kv = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++ic) {
+    for (uint32_t n_it = 0; ok; ++n_it, ++ic) {
+      const int w = item_publish(c.ring, n_it, &hdr->dq_counter, n_work, lane, abort_flag, hdr, 0x404, ok);
+      if (w < 0) break;
       const int pair = w / p.H, h = w - pair * p.H, hk = h / G;
       const int2 it = p.fwd_items[pair];
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
@@ -785,7 +850,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       uint32_t ic = 0, kv = 0, ii = 0;
       bool ok = true;
       const uint32_t id_sp = idesc_f8(128, 128, 0, 0);
-      for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++ic) {
+      for (uint32_t n_it = 0; ok; ++n_it, ++ic) {
+        const int w = item_get(c.ring, n_it, abort_flag, hdr, 0x418, ok);
+        if (w < 0) break;
         const int pair = w / p.H;
         const int2 it = p.fwd_items[pair];
         const int len = __ldg(p.cu + it.x + 1) - __ldg(p.cu + it.x);
@@ -829,7 +896,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     constexpr int HC = HD / 2;
     uint32_t ic = 0, kv = 0, ii = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++ic) {
+    for (uint32_t n_it = 0; ok; ++n_it, ++ic) {
+      const int w = item_get_warp(c.ring, n_it, lane, abort_flag, hdr, 0x428, ok);
+      if (w < 0) break;
       const int pair = w / p.H, h = w - pair * p.H;
       const int2 it = p.fwd_items[pair];
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
@@ -944,6 +1013,7 @@ static cudaError_t launch_bwd_t(const AttnParams& p, const AttnMaps& m, cudaStre
       static_assert(bwd_smem_bytes<HD, EX, true, false>() <= 232448, "shared memory");
       if ((e = set_smem(bwd_kernel<HD, OB, EX, true, false>, smem)) != cudaSuccess) return e;
       if ((e = cudaMemsetAsync(p.dq_acc, 0, sizeof(float) * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
+      if ((e = cudaMemsetAsync(&p.hdr->bwd_counter, 0, sizeof(uint32_t), st)) != cudaSuccess) return e;
       bwd_kernel<HD, OB, EX, true, false><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.dq, m.q, m.q);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
       const size_t n4 = (size_t)p.T * p.H * HD / 4;
@@ -958,6 +1028,8 @@ static cudaError_t launch_bwd_t(const AttnParams& p, const AttnMaps& m, cudaStre
   static_assert(bwd_smem_bytes<HD, EX, false, NV4>() <= 232448, "shared memory");
   static_assert(dq_smem_bytes<HD, NV4>() <= 232448, "shared memory");
   if ((e = set_smem(bwd_kernel<HD, OB, EX, false, NV4>, smem)) != cudaSuccess) return e;
+  // work counters of the two launches below
+  if ((e = cudaMemsetAsync(&p.hdr->bwd_counter, 0, 2 * sizeof(uint32_t), st)) != cudaSuccess) return e;
   // without DQ the dQ map is not read (the q map stands in for the argument)
   bwd_kernel<HD, OB, EX, false, NV4><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.q, m.qn, m.kn);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -224,6 +224,62 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, v
   return __all_sync(0xffffffffu, ok);
 }
 
+// ---------------------------------------------------------------------------
+// Dynamic work distribution of the persistent kernels: the producer warp takes
+// the next item of the longest-first list from a global counter and publishes
+// it in a small shared-memory ring; every other warp role reads the items in
+// the same order from the ring, so all roles of a CTA agree on its items.
+// -1 marks the end.  Slots are released as soon as they are read.
+// ---------------------------------------------------------------------------
+constexpr int kItemRing = 4;
+struct ItemRing {
+  int item[kItemRing];
+  uint64_t full[kItemRing], empty[kItemRing];
+};
+
+__device__ __forceinline__ void item_ring_init(ItemRing& r, uint32_t consumers) {
+  for (int s = 0; s < kItemRing; ++s) {
+    mbar_init(&r.full[s], 1);
+    mbar_init(&r.empty[s], consumers);
+  }
+}
+
+// Producer warp (all lanes): fetch the n-th item of this CTA; -1 when none is left.
+__device__ __forceinline__ int item_publish(ItemRing& r, uint32_t n, uint32_t* counter, int n_work, int lane,
+                                            volatile int* abort_flag, WsHeader* hdr, uint32_t where, bool& ok) {
+  const int s = (int)(n % kItemRing);
+  if (!(ok = mbar_wait_warp(&r.empty[s], ((n / kItemRing) & 1) ^ 1, abort_flag, hdr, where))) return -1;
+  int w = 0;
+  if (lane == 0) {
+    w = (int)atomicAdd(counter, 1u);
+    if (w >= n_work) w = -1;
+    r.item[s] = w;
+    mbar_arrive(&r.full[s]);
+  }
+  return __shfl_sync(0xffffffffu, w, 0);
+}
+
+// Consumer, one thread: the n-th item (its slot released at once).
+__device__ __forceinline__ int item_get(ItemRing& r, uint32_t n, volatile int* abort_flag, WsHeader* hdr,
+                                        uint32_t where, bool& ok) {
+  const int s = (int)(n % kItemRing);
+  if (!(ok = mbar_wait(&r.full[s], (n / kItemRing) & 1, abort_flag, hdr, where))) return -1;
+  const int w = *reinterpret_cast<volatile int*>(&r.item[s]);
+  mbar_arrive(&r.empty[s]);
+  return w;
+}
+
+// Consumer, whole warp: the n-th item (lane 0 releases the slot).
+__device__ __forceinline__ int item_get_warp(ItemRing& r, uint32_t n, int lane, volatile int* abort_flag,
+                                             WsHeader* hdr, uint32_t where, bool& ok) {
+  const int s = (int)(n % kItemRing);
+  if (!(ok = mbar_wait_warp(&r.full[s], (n / kItemRing) & 1, abort_flag, hdr, where))) return -1;
+  const int w = *reinterpret_cast<volatile int*>(&r.item[s]);
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&r.empty[s]);
+  return w;
+}
+
 // After an abort, give TMA copies already issued by this CTA time to land
 // before the CTA exits (bounded: about 50 microseconds).
 __device__ __forceinline__ void drain_after_abort(volatile int* abort_flag) {

@@ -51,6 +51,7 @@ struct FwdCtl {
   uint64_t eb_bar[4], l_bar[4];  // per TMEM lane quarter: the four warps that share its rows
   int ebx[2][kTile][4];  // [tile parity][row][key block] P^ block exponents, shared by a row's four threads
   float lx[kTile][4];    // [row][key block] partial normalisers for the epilogue
+  ItemRing ring;  // this CTA's work items, in the order all roles process them
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -109,6 +110,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&c.eb_bar[qq], 128);
       mbar_init(&c.l_bar[qq], 128);
     }
+    item_ring_init(c.ring, 1 + kFwdSoftmax / 32);  // the MMA thread and each softmax warp
     c.abort_flag = 0;
     fence_mbar_init();
   }
@@ -138,7 +140,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // ------------------------------------------------------------ producer
     uint32_t kv = 0, qc = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+    for (uint32_t n_it = 0; ok; ++n_it) {
+      const int w = item_publish(c.ring, n_it, &hdr->fwd_counter, n_work, lane, abort_flag, hdr, 0x204, ok);
+      if (w < 0) break;
       const int pair = w / p.H, h = w - pair * p.H, hk = h / G;
       const int2 it = p.fwd_items[pair];
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
@@ -186,7 +190,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (elect_one()) {
       uint32_t kv = 0, qc = 0, sc = 0, pc = 0, ic = 0;
       bool ok = true;
-      for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+      for (uint32_t n_it = 0; ok; ++n_it) {
+        const int w = item_get(c.ring, n_it, abort_flag, hdr, 0x217, ok);
+        if (w < 0) break;
         const int pair = w / p.H;
         const int2 it = p.fwd_items[pair];
         const int len = __ldg(p.cu + it.x + 1) - __ldg(p.cu + it.x);
@@ -242,7 +248,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     int32_t* const dbg_e = hdr->dbg_eb;
     uint32_t kv = 0, sc = 0, pc = 0, ic = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+    for (uint32_t n_it = 0; ok; ++n_it) {
+      const int w = item_get_warp(c.ring, n_it, lane, abort_flag, hdr, 0x228, ok);
+      if (w < 0) break;
       const int pair = w / p.H, h = w - pair * p.H;
       const int2 it = p.fwd_items[pair];
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
@@ -433,6 +441,8 @@ static cudaError_t launch_fwd_t(const AttnParams& p, const AttnMaps& m, cudaStre
   }
   long work = (long)p.max_items * p.H;
   int grid = (int)(work < num_sms() ? work : num_sms());
+  cudaError_t e = cudaMemsetAsync(&p.hdr->fwd_counter, 0, sizeof(uint32_t), st);  // work counter of this launch
+  if (e != cudaSuccess) return e;
   fwd_kernel<HD, OB, EX, NV4><<<grid, kFwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.qn, m.kn);
   return cudaGetLastError();
 }
