@@ -441,6 +441,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // factors there and (DQ) its dQ tile has been drained
           if constexpr (DQ) {
             if (!mbar_wait(&c.x1_free, (i_p & 1) ^ 1, abort_flag, hdr, 0x314)) return false;
+            // d = 64: the single dQ tile may drain before dV / dK have read the scale factors
+            if (HD == 64 && i_p > 0 && !mbar_wait(&c.mm_done, (i_p - 1) & 1, abort_flag, hdr, 0x319)) return false;
           } else {
             if (i_p > 0 && !mbar_wait(&c.mm_done, (i_p - 1) & 1, abort_flag, hdr, 0x314)) return false;
           }
@@ -461,6 +463,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (t == 0 && !(ok = mbar_wait(&c.acc_free, (ic & 1) ^ 1, abort_flag, hdr, 0x316))) break;
           tc_fence_after();
           const uint8_t* dsk = EXACT ? tl.dsk : tl.ds;
+          // dQ = dS^ K^ in halves of 64 columns through X1[0, 64); the first
+          // half goes first so that its drain overlaps the dV / dK MMAs
+          auto issue_dq = [&](int half) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // contraction over the 128 keys
+              mma_mxf8(tb + kColX1, bdesc_k(tl.ds, 32 * kk, 128), bdesc_mn(tl.k, kk * 32 * HD + 64 * half, HD),
+                       idesc_mxf8(128, 64, 0, 1, kk, kk), tb + kColSfDQ, tb + kColSfOne, kk > 0 ? 1u : 0u);
+          };
+          if constexpr (DQ) {
+            issue_dq(0);
+            tc_commit(&c.dq_lo_full);
+          }
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {  // contraction over the 128 queries
             const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
@@ -469,22 +483,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_mxf8(tb + kColDK, bdesc_mn(dsk, kk * 32 * 128, 128), bdesc_mn(tl.q[qs], kk * 32 * HD, HD),
                      idesc_mxf8(128, HD, 1, 1, kk, kk), tb + kColSfDK, tb + kColSfOne, acc);
           }
-          if constexpr (DQ) {
-            // dQ = dS^ K^ in halves of 64 columns through X1[0, 64): the
-            // drain warps empty the first half while the second is computed
-#pragma unroll
-            for (int half = 0; half < HD / 64; ++half) {
-              if (half == 1) {
-                tc_commit(&c.dq_lo_full);
-                if (!(ok = mbar_wait(&c.dq_lo_free, ii & 1, abort_flag, hdr, 0x317))) break;
-                tc_fence_after();
-              }
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)  // contraction over the 128 keys
-                mma_mxf8(tb + kColX1, bdesc_k(tl.ds, 32 * kk, 128), bdesc_mn(tl.k, kk * 32 * HD + 64 * half, HD),
-                         idesc_mxf8(128, 64, 0, 1, kk, kk), tb + kColSfDQ, tb + kColSfOne, kk > 0 ? 1u : 0u);
-            }
-            if (!ok) break;
+          if constexpr (DQ && HD == 128) {
+            if (!(ok = mbar_wait(&c.dq_lo_free, ii & 1, abort_flag, hdr, 0x317))) break;
+            tc_fence_after();
+            issue_dq(1);
           }
           tc_commit(&c.mm_done);
           tc_commit(&c.qd_empty[qs]);
@@ -550,10 +552,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if constexpr (DQ) {
         for (int t = 0; ok && t < n_iter; ++t, ++ii) {
           // the dQ tile arrives in X1[0, 64) in halves of 64 columns (d = 128)
-          // or whole (d = 64); each half goes to two staging boxes
+          // or whole (d = 64); each half goes to two staging boxes.  The first
+          // half is committed before the dV / dK MMAs, the second with them.
 #pragma unroll
           for (int half = 0; half < HD / 64; ++half) {
-            if (half == 0 && HD == 128) {
+            if (half == 0) {  // the first (d = 64: only) half is committed on its own
               if (!(ok = mbar_wait_warp(&c.dq_lo_full, ii & 1, abort_flag, hdr, 0x343))) break;
             } else {
               if (!(ok = mbar_wait_warp(&c.mm_done, ii & 1, abort_flag, hdr, 0x341))) break;
