@@ -36,11 +36,11 @@ namespace flamia {
 // Warpgroups: 0-1 compute (warps 0-7), 2 dQ drain (warps 8-11, one per TMEM
 // lane quarter), 3 producer (12), MMA issuer (13), dQ reducer (14), idle (15).
 // Registers are rebalanced per warpgroup after launch (512 x 128 in total):
-// 2 x 128 x 176 + 128 x 80 + 128 x 80 = 65536.
+// 2 x 128 x 168 + 128 x 96 + 128 x 80 = 65536.
 constexpr int kBwdCompute = 256;
 constexpr int kBwdThreads = 512;
 constexpr int kWarpDrain0 = 8, kWarpProd = 12, kWarpMma = 13, kWarpRed = 14;
-constexpr uint32_t kRegCompute = 176, kRegDrain = 80, kRegCtl = 80;
+constexpr uint32_t kRegCompute = 168, kRegDrain = 96, kRegCtl = 80;
 static_assert(2 * 128 * kRegCompute + 128 * kRegDrain + 128 * kRegCtl <= 65536, "register split");
 // TMEM: dV, dK accumulators; X0 = S; X1 = dP, then (once dP is read) the
 // scale factors at X1 + 64.. and the dQ tile, 64 columns at a time, at X1 + 0.
@@ -563,12 +563,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             if (half == 0 && !(ok = mbar_wait_warp(&c.dqs_free, (ii & 1) ^ 1, abort_flag, hdr, 0x342))) break;
             tc_fence_after();
-#pragma unroll 1
-            for (int cb = 0; cb < 2; ++cb) {
-              uint32_t rq[32];
-              tmem_ld32(taddr(tb, qq * 32, kColX1 + 32 * cb), rq);
-              tmem_ld_wait_regs(rq);
-              store_row_box(tl.dqs + (2 * half + cb) * (kTile * 32), r, rq);
+            {
+              uint32_t rq[2][32];  // both 32-column blocks with one wait
+              tmem_ld32(taddr(tb, qq * 32, kColX1), rq[0]);
+              tmem_ld32(taddr(tb, qq * 32, kColX1 + 32), rq[1]);
+              tmem_ld_wait_regs(rq[0], rq[1]);
+              store_row_box(tl.dqs + (2 * half) * (kTile * 32), r, rq[0]);
+              store_row_box(tl.dqs + (2 * half + 1) * (kTile * 32), r, rq[1]);
             }
             tc_fence_before();
             if (half == 0 && HD == 128) mbar_arrive(&c.dq_lo_free);
