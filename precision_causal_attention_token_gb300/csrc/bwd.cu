@@ -36,11 +36,11 @@ namespace flamia {
 // Warpgroups: 0-1 compute (warps 0-7), 2 dQ drain (warps 8-11, one per TMEM
 // lane quarter), 3 producer (12), MMA issuer (13), dQ reducer (14), idle (15).
 // Registers are rebalanced per warpgroup after launch (512 x 128 in total):
-// 2 x 128 x 168 + 128 x 96 + 128 x 80 = 65536.
+// 2 x 128 x 160 + 128 x 112 + 128 x 80 = 65536.
 constexpr int kBwdCompute = 256;
 constexpr int kBwdThreads = 512;
 constexpr int kWarpDrain0 = 8, kWarpProd = 12, kWarpMma = 13, kWarpRed = 14;
-constexpr uint32_t kRegCompute = 168, kRegDrain = 96, kRegCtl = 80;
+constexpr uint32_t kRegCompute = 160, kRegDrain = 112, kRegCtl = 80;
 static_assert(2 * 128 * kRegCompute + 128 * kRegDrain + 128 * kRegCtl <= 65536, "register split");
 // TMEM: dV, dK accumulators; X0 = S; X1 = dP, then (once dP is read) the
 // scale factors at X1 + 64.. and the dQ tile, 64 columns at a time, at X1 + 0.
@@ -52,18 +52,27 @@ constexpr uint32_t kColSfDV = kColX1 + 64, kColSfDK = kColX1 + 68, kColSfDQ = kC
 // NV4 (mixed path): the scores' operands are bf16 NVFP4 values (k holds K's,
 // qn Q's); dK still contracts with the E4M3 Q codes.  dQ then comes from the
 // dQ kernel (no DQ variant).
+// K/V tiles of consecutive work items are double-buffered so the next item's
+// copies land while this one is processed (one buffer on the mixed path,
+// whose bf16 score tiles leave no room for a second).
+template <bool NV4>
+constexpr int bwd_kv_stages() {
+  return NV4 ? 1 : 2;
+}
+
 template <int HD, bool EXACT, bool DQ, bool NV4>
 struct __align__(1024) BwdTiles {
-  uint8_t k[score_tile_bytes<HD, NV4>()];
-  uint8_t v[kTile * HD];
+  uint8_t k[bwd_kv_stages<NV4>()][score_tile_bytes<HD, NV4>()];
+  uint8_t v[bwd_kv_stages<NV4>()][kTile * HD];
   uint8_t q[2][kTile * HD];
   uint8_t dO[2][kTile * HD];
   uint8_t pt[kTile * kTile];   // P~ codes   [query][key]
   uint8_t ds[kTile * kTile];   // dS^ codes  [query][key] (dQ payload; also dK's in the default option)
   uint8_t dsk[EXACT ? kTile * kTile : 1024];  // exact option: dK payload
-  // dQ tile staged for the bulk reduce-add: HD/32 boxes of [128 rows][32 fp32], 128B-swizzled
-  float dqs[DQ ? kTile * HD : 256];
-  uint8_t qn[2][NV4 ? score_tile_bytes<HD, NV4>() : 1024];  // mixed path: Q's score operand
+  // one half (64 columns) of a dQ tile staged for the bulk reduce-add: two
+  // boxes of [128 rows][32 fp32], 128B-swizzled
+  float dqs[DQ ? kTile * 64 : 256];
+  uint8_t qn[2][NV4 ? score_tile_bytes<HD, NV4>() : 16];  // mixed path: Q's score operand
 };
 
 // Per-row values of one query tile, staged in shared memory by the producer
@@ -75,13 +84,13 @@ struct RowStage {
 
 struct BwdCtl {
   RowStage rows[2][kTile];  // [Q/dO stage][query row]
-  float kf[kTile];     // 2^eK(j)
-  float vf[kTile];     // eV(j)
-  float vinv[kTile];   // 2^-eV(j)
-  int ekb[4];          // eK of each 32-key block (default option)
+  float kf[2][kTile];    // [K/V stage] 2^eK(j) (mixed path: g_K(j))
+  float vf[2][kTile];    // eV(j)
+  float vinv[2][kTile];  // 2^-eV(j)
+  int ekb[2][4];         // eK of each 32-key block (default option)
   uint8_t xch[2][2][4][4];   // [parity][dV, dK][query block][key block] scale bytes
   uint8_t xdq[2][kTile][4];  // [parity][query row][key block] dQ scale bytes
-  uint64_t kv_full, kv_empty, qd_full[2], qd_empty[2];
+  uint64_t kv_full[2], kv_empty[2], qd_full[2], qd_empty[2];
   uint64_t s_full, dp_full, ds_full, mm_done, x1_free, acc_full, acc_free, xch_bar, dqs_full, dqs_free;
   uint64_t x0_free, dq_lo_full, dq_lo_free;
   ItemRing ring;  // this CTA's work items, in the order all roles process them
@@ -290,6 +299,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                const __grid_constant__ CUtensorMap map_dq, const __grid_constant__ CUtensorMap map_qn,
                const __grid_constant__ CUtensorMap map_kn) {
   static_assert(!(NV4 && DQ), "the mixed path takes dQ from the dQ kernel");
+  constexpr int kKvStages = bwd_kv_stages<NV4>();
   constexpr bool PERKEY = EXACT || NV4;
   constexpr int kQKBytes = score_tile_bytes<HD, NV4>();
   extern __shared__ uint8_t smem_raw[];
@@ -304,8 +314,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   WsHeader* hdr = p.hdr;
 
   if (tid == 0) {
-    mbar_init(&c.kv_full, 32);
-    mbar_init(&c.kv_empty, 1 + kBwdCompute);
+    for (int s2 = 0; s2 < 2; ++s2) {
+      mbar_init(&c.kv_full[s2], 32);
+      mbar_init(&c.kv_empty[s2], 1 + kBwdCompute);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&c.qd_full[s], 32);
       mbar_init(&c.qd_empty[s], 1);
@@ -360,7 +372,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
       const int k0 = ds + kTile * it.y;
       const int n_t = (len + kTile - 1) / kTile, q_first = p.causal ? it.y : 0;
-      if (!(ok = mbar_wait_warp(&c.kv_empty, (ic & 1) ^ 1, abort_flag, hdr, 0x301))) break;
+      const int kvs = ic % kKvStages;
+      if (!(ok = mbar_wait_warp(&c.kv_empty[kvs], ((ic / kKvStages) & 1) ^ 1, abort_flag, hdr, 0x301))) break;
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
         const int j = lane * 4 + jj, key = kTile * it.y + j;
@@ -371,17 +384,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ev = (int)__ldg(p.v_sc + (size_t)hk * p.T + ds + key) - 127;
           if (NV4) gk = __ldg(p.k_g + (size_t)hk * p.T + ds + key);
         }
-        c.kf[j] = NV4 ? gk : pow2_127(ek);
-        c.vf[j] = (float)ev;
-        c.vinv[j] = pow2_127(-ev);
-        if ((j & 31) == 0) c.ekb[j >> 5] = ek;
+        c.kf[kvs][j] = NV4 ? gk : pow2_127(ek);
+        c.vf[kvs][j] = (float)ev;
+        c.vinv[kvs][j] = pow2_127(-ev);
+        if ((j & 31) == 0) c.ekb[kvs][j >> 5] = ek;
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(&c.kv_full, kQKBytes + kTile * HD);
-        load_score_tile<HD, NV4>(tl.k, &map_k, &map_kn, &c.kv_full, hk, k0);
-        tma_load_3d(tl.v, &map_v, &c.kv_full, 0, hk, k0);
+        mbar_arrive_expect_tx(&c.kv_full[kvs], kQKBytes + kTile * HD);
+        load_score_tile<HD, NV4>(tl.k[kvs], &map_k, &map_kn, &c.kv_full[kvs], hk, k0);
+        tma_load_3d(tl.v[kvs], &map_v, &c.kv_full[kvs], 0, hk, k0);
       } else {
-        mbar_arrive(&c.kv_full);
+        mbar_arrive(&c.kv_full[kvs]);
       }
       for (int g = 0; ok && g < G; ++g) {
         const int h = hk * G + g;
@@ -423,7 +436,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int len = __ldg(p.cu + it.x + 1) - __ldg(p.cu + it.x);
         const int n_t = (len + kTile - 1) / kTile, q_first = p.causal ? it.y : 0;
         const int n_iter = G * (n_t - q_first);
-        if (!(ok = mbar_wait(&c.kv_full, ic & 1, abort_flag, hdr, 0x311))) break;
+        const int kvs = ic % kKvStages;
+        if (!(ok = mbar_wait(&c.kv_full[kvs], (ic / kKvStages) & 1, abort_flag, hdr, 0x311))) break;
         // S of query tile ii into X0 (Q^ of stage ii & 1, K^ of this item)
         auto issue_s = [&](uint32_t i_s) -> bool {
           const int qs_s = i_s & 1;
@@ -431,7 +445,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // X0 is free once the compute warps have read the previous S
           if (!mbar_wait(&c.x0_free, (i_s & 1) ^ 1, abort_flag, hdr, 0x313)) return false;
           tc_fence_after();
-          issue_scores<HD, NV4>(tb + kColX0, NV4 ? tl.qn[qs_s] : tl.q[qs_s], tl.k);
+          issue_scores<HD, NV4>(tb + kColX0, NV4 ? tl.qn[qs_s] : tl.q[qs_s], tl.k[kvs]);
           tc_commit(&c.s_full);
           return true;
         };
@@ -449,7 +463,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < HD / 32; ++kk)
-            mma_f8(tb + kColX1, bdesc_k(tl.dO[i_p & 1], 32 * kk, HD), bdesc_k(tl.v, 32 * kk, HD), id_sp, kk > 0);
+            mma_f8(tb + kColX1, bdesc_k(tl.dO[i_p & 1], 32 * kk, HD), bdesc_k(tl.v[kvs], 32 * kk, HD), id_sp, kk > 0);
           tc_commit(&c.dp_full);
           return true;
         };
@@ -468,7 +482,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           auto issue_dq = [&](int half) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)  // contraction over the 128 keys
-              mma_mxf8(tb + kColX1, bdesc_k(tl.ds, 32 * kk, 128), bdesc_mn(tl.k, kk * 32 * HD + 64 * half, HD),
+              mma_mxf8(tb + kColX1, bdesc_k(tl.ds, 32 * kk, 128), bdesc_mn(tl.k[kvs], kk * 32 * HD + 64 * half, HD),
                        idesc_mxf8(128, 64, 0, 1, kk, kk), tb + kColSfDQ, tb + kColSfOne, kk > 0 ? 1u : 0u);
           };
           if constexpr (DQ) {
@@ -493,7 +507,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (t + 1 < n_iter && !(ok = issue_dp(ii + 1))) break;
           if (t == n_iter - 1) {
             tc_commit(&c.acc_full);
-            tc_commit(&c.kv_empty);
+            tc_commit(&c.kv_empty[kvs]);
           }
         }
       }
@@ -502,7 +516,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
    } else if (warp == kWarpRed) {
     // ------------------------------------------------------------ dQ reducer
     if (DQ && lane == 0) {
-      uint32_t ii = 0;
+      uint32_t ii = 0, hc = 0;  // hc: staged halves
       bool ok = true;
       for (uint32_t n_it = 0; ok; ++n_it) {
         const int w = item_get(c.ring, n_it, abort_flag, hdr, 0x332, ok);
@@ -514,13 +528,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int g = 0; ok && g < G; ++g) {
           const int h = hk * G + g;
           for (int qt = q_first; qt < n_t; ++qt, ++ii) {
-            if (!(ok = mbar_wait(&c.dqs_full, ii & 1, abort_flag, hdr, 0x331))) break;
+            // one staged half (64 columns) at a time
+            for (int half = 0; ok && half < HD / 64; ++half, ++hc) {
+              if (!(ok = mbar_wait(&c.dqs_full, hc & 1, abort_flag, hdr, 0x331))) break;
 #pragma unroll
-            for (int cb = 0; cb < HD / 32; ++cb)
-              tma_reduce_add_3d(&map_dq, tl.dqs + cb * (kTile * 32), 32 * cb, h, ds + kTile * qt);
-            bulk_commit_group();
-            bulk_wait_group_read0();
-            mbar_arrive(&c.dqs_free);
+              for (int cb = 0; cb < 2; ++cb)
+                tma_reduce_add_3d(&map_dq, tl.dqs + cb * (kTile * 32), 64 * half + 32 * cb, h, ds + kTile * qt);
+              bulk_commit_group();
+              bulk_wait_group_read0();
+              mbar_arrive(&c.dqs_free);
+            }
           }
         }
       }
@@ -539,7 +556,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // go to global memory, so the compute warps start the next item at once.
     const int qq = warp - kWarpDrain0, r = 32 * qq + lane;
     const float sm_scale = p.softmax_scale;
-    uint32_t ic = 0, ii = 0;
+    uint32_t ic = 0, ii = 0, hc = 0;  // hc: staged dQ halves
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it, ++ic) {
       const int w = item_get_warp(c.ring, n_it, lane, abort_flag, hdr, 0x344, ok);
@@ -561,23 +578,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             } else {
               if (!(ok = mbar_wait_warp(&c.mm_done, ii & 1, abort_flag, hdr, 0x341))) break;
             }
-            if (half == 0 && !(ok = mbar_wait_warp(&c.dqs_free, (ii & 1) ^ 1, abort_flag, hdr, 0x342))) break;
             tc_fence_after();
-            {
-              uint32_t rq[2][32];  // both 32-column blocks with one wait
-              tmem_ld32(taddr(tb, qq * 32, kColX1), rq[0]);
-              tmem_ld32(taddr(tb, qq * 32, kColX1 + 32), rq[1]);
-              tmem_ld_wait_regs(rq[0], rq[1]);
-              store_row_box(tl.dqs + (2 * half) * (kTile * 32), r, rq[0]);
-              store_row_box(tl.dqs + (2 * half + 1) * (kTile * 32), r, rq[1]);
-            }
+            uint32_t rq[2][32];  // both 32-column blocks with one wait
+            tmem_ld32(taddr(tb, qq * 32, kColX1), rq[0]);
+            tmem_ld32(taddr(tb, qq * 32, kColX1 + 32), rq[1]);
+            tmem_ld_wait_regs(rq[0], rq[1]);
             tc_fence_before();
-            if (half == 0 && HD == 128) mbar_arrive(&c.dq_lo_free);
+            if (half == 0 && HD == 128) mbar_arrive(&c.dq_lo_free);  // X1[0, 64) may take the second half
+            if (half == HD / 64 - 1) mbar_arrive(&c.x1_free);         // the dQ tile has left X1
+            // the staging half is free once the reducer has read the previous one
+            if (!(ok = mbar_wait_warp(&c.dqs_free, (hc & 1) ^ 1, abort_flag, hdr, 0x342))) break;
+            store_row_box(tl.dqs, r, rq[0]);
+            store_row_box(tl.dqs + kTile * 32, r, rq[1]);
+            fence_proxy_async_smem();
+            mbar_arrive(&c.dqs_full);
+            ++hc;
           }
           if (!ok) break;
-          mbar_arrive(&c.x1_free);
-          fence_proxy_async_smem();
-          mbar_arrive(&c.dqs_full);
         }
         if (!ok) break;
       }
@@ -615,7 +632,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int2 it = p.bwd_items[pair];
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
       const int n_t = (len + kTile - 1) / kTile, q_first = p.causal ? it.y : 0;
-      if (!(ok = mbar_wait_warp(&c.kv_full, ic & 1, abort_flag, hdr, 0x321))) break;
+      const int kvs = ic % kKvStages;
+      if (!(ok = mbar_wait_warp(&c.kv_full[kvs], (ic / kKvStages) & 1, abort_flag, hdr, 0x321))) break;
       const int key0 = kTile * it.y;
       for (int g = 0; ok && g < G; ++g) {
         const int h = hk * G + g;
@@ -631,7 +649,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           int Eb[2];
           // the diagonal tile (and a document's last key tile) needs the mask
           const bool need_mask = p.causal ? (qt == it.y) : (it.y == n_t - 1);
-          recompute_phat<PERKEY>(taddr(tb, q * 32, kColX0), b0, rv.rowc, c.kf, c.vf, i_loc, key0, len, p.causal,
+          recompute_phat<PERKEY>(taddr(tb, q * 32, kColX0), b0, rv.rowc, c.kf[kvs], c.vf[kvs], i_loc, key0, len, p.causal,
                                 need_mask, row_ok, pcode, Eb);
           tc_fence_before();
           mbar_arrive(&c.x0_free);  // S has been read: X0 may take the next S
@@ -650,7 +668,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int b = b0 + bb;
             float dsv[32], ptv[32];
             float amax_ds, amax_pt;
-            ds_block(dp[bb], pcode[bb], ds_factors(Eb[bb], rv.mi, rv.inv_l, rv.hdo, rv.Di), c.vinv + 32 * b, dsv,
+            ds_block(dp[bb], pcode[bb], ds_factors(Eb[bb], rv.mi, rv.inv_l, rv.hdo, rv.Di), c.vinv[kvs] + 32 * b, dsv,
                      ptv, amax_ds, amax_pt);
             // P~: 32 x 32 block (this warp's 32 queries x key block b)
             const int e_pt = noclamp_exp_clamped(warp_max(amax_pt));
@@ -660,13 +678,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             uint32_t kbyte, qbyte = 0;
             if constexpr (!EXACT) {
               int e_ds;
-              qbyte = dq_operand<false>(dsv, amax_ds, c.kf + 32 * b, c.ekb[b], codes, e_ds);
+              qbyte = dq_operand<false>(dsv, amax_ds, c.kf[kvs] + 32 * b, c.ekb[kvs][b], codes, e_ds);
               store_row_block(tl.ds, r, b, codes);
               kbyte = sf_byte(e_ds + rv.eq);  // dK operand: the same codes, Q's block exponent folded in
             } else {
               if constexpr (DQ) {
                 int unused;
-                qbyte = dq_operand<true>(dsv, amax_ds, c.kf + 32 * b, c.ekb[b], codes, unused);
+                qbyte = dq_operand<true>(dsv, amax_ds, c.kf[kvs] + 32 * b, c.ekb[kvs][b], codes, unused);
                 store_row_block(tl.ds, r, b, codes);
               }
               // dK operand: 32 x 32 block of dS * 2^eQ(i)
@@ -712,7 +730,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       if (!ok) break;
-      mbar_arrive(&c.kv_empty);  // key vectors no longer read
+      mbar_arrive(&c.kv_empty[kvs]);  // key vectors no longer read
     }
   }
   tc_fence_before();
