@@ -107,21 +107,30 @@ __global__ void plan_keys_kernel(const int32_t* __restrict__ tile_prefix, int n_
   keys[sort_n + g] = kb;
 }
 
-// Bitonic sort of kSortBlock keys per CTA (ascending).
-__global__ void __launch_bounds__(1024) block_sort_kernel(uint64_t* keys) {
+// Bitonic sort of kSortBlock keys per CTA (ascending).  Keys past the real
+// items are padding (all bits set), so a block whose real keys fit in the
+// first P = 2^k slots only runs the network up to size P: the padding above
+// stays in place and the block ends sorted.
+__global__ void __launch_bounds__(1024) block_sort_kernel(uint64_t* keys, int sort_n, const WsHeader* hdr) {
   __shared__ uint64_t s[kSortBlock];
   uint64_t* k = keys + (size_t)blockIdx.x * kSortBlock;
   const int tid = threadIdx.x;
+  const int per_list = sort_n / kSortBlock;
+  const int n_real = min(kSortBlock, max(0, hdr->n_items - (int)(blockIdx.x % per_list) * kSortBlock));
+  int P = 2;
+  while (P < n_real) P <<= 1;
   s[tid] = k[tid];
   s[tid + 1024] = k[tid + 1024];
   __syncthreads();
-  for (int size = 2; size <= kSortBlock; size <<= 1) {
+  for (int size = 2; size <= P; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       const int i = 2 * tid - (tid & (stride - 1));  // lower index of the pair
       const int j = i + stride;
-      const bool up = ((i & size) == 0);
-      const uint64_t a = s[i], b = s[j];
-      if ((a > b) == up) { s[i] = b; s[j] = a; }
+      if (j < P) {
+        const bool up = ((i & size) == 0);
+        const uint64_t a = s[i], b = s[j];
+        if ((a > b) == up) { s[i] = b; s[j] = a; }
+      }
       __syncthreads();
     }
   }
@@ -179,7 +188,7 @@ cudaError_t launch_plan(const flamia_problem_t& p, const WsLayout& L, uint8_t* w
   plan_prefix_kernel<<<1, 1024, 0, st>>>(p.cu_seqlens, p.n_seq, p.T, tile_prefix, blk_prefix, hdr);
   const int n = L.sort_n;
   plan_keys_kernel<<<(n + 255) / 256, 256, 0, st>>>(tile_prefix, p.n_seq, p.causal, n, hdr, ka);
-  block_sort_kernel<<<2 * n / kSortBlock, 1024, 0, st>>>(ka);
+  block_sort_kernel<<<2 * n / kSortBlock, 1024, 0, st>>>(ka, n, hdr);
   uint64_t *src = ka, *dst = kb;
   for (int w = kSortBlock; w < n; w *= 2) {
     merge_pass_kernel<<<(2 * n + 255) / 256, 256, 0, st>>>(src, dst, n, w);
@@ -261,7 +270,7 @@ extern "C" flamia_status_t flamia_plan_noalloc(const flamia_problem_t* p, int2* 
                                             &sc->hdr);
   plan_keys_kernel<<<(n + 255) / 256, 256, 0, stream>>>(sc->tile_prefix, p->n_seq, p->causal, n, &sc->hdr,
                                                         sc->keys_a);
-  block_sort_kernel<<<2 * n / kSortBlock, 1024, 0, stream>>>(sc->keys_a);
+  block_sort_kernel<<<2 * n / kSortBlock, 1024, 0, stream>>>(sc->keys_a, n, &sc->hdr);
   uint64_t *src = sc->keys_a, *dst = sc->keys_b;
   for (int w = kSortBlock; w < n; w *= 2) {
     merge_pass_kernel<<<(2 * n + 255) / 256, 256, 0, stream>>>(src, dst, n, w);
