@@ -653,7 +653,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 need_mask, row_ok, pcode, Eb);
           tc_fence_before();
           mbar_arrive(&c.x0_free);  // S has been read: X0 may take the next S
-          if (row_ok) dbg_dump_phat2(dbg_c, dbg_e, p.T, h, ds + i_loc, ds + key0, b0, pcode, Eb);
+          if (dbg_c != nullptr && row_ok) {
+            PhatDump d;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) d.w[k] = pcode[k >> 3][k & 7];
+            d.e[0] = Eb[0];
+            d.e[1] = Eb[1];
+            dbg_dump_phat(dbg_c, dbg_e, p.T, h, ds + i_loc, ds + key0, b0, 2, d);
+          }
           if (!(ok = mbar_wait_warp(&c.dp_full, ii & 1, abort_flag, hdr, 0x323))) break;
           // the previous iteration's MMAs must be done with the P~ / dS tiles
           if (ii > 0 && !(ok = mbar_wait_warp(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x326))) break;

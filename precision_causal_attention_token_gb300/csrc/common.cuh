@@ -29,32 +29,25 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "header");
 
-// Test hook: record one row's P^ codes and block exponents for two 32-key
-// blocks (b0, b0 + 1) of a 128-key tile.  `dc`/`de` are the header's hook
-// pointers, read once per kernel (null: off).
-__device__ __forceinline__ void dbg_dump_phat2(uint8_t* dc, int32_t* de, int T, int h, int tok, int key_tok0,
-                                               int b0, const uint32_t (&codes)[2][8], const int (&Eb)[2]) {
-  if (dc == nullptr) return;
+// Test hook: record one row's P^ codes and block exponents for `nb` 32-key
+// blocks starting at block b0 of a 128-key tile (w[8 * i + k] = word k of
+// block i).  Out of line, not unrolled and taking its data by value: it runs
+// only when the hook is set, and the hot loops keep their registers and a
+// small code footprint.  Callers test `dc` first.
+struct PhatDump {
+  uint32_t w[16];
+  int e[2];
+};
+static __device__ __noinline__ void dbg_dump_phat(uint8_t* dc, int32_t* de, int T, int h, int tok, int key_tok0, int b0,
+                                          int nb, const PhatDump d) {
   const size_t row = ((size_t)h * T + tok) * (size_t)T;
   const int k0 = key_tok0 + 32 * b0;
-#pragma unroll
-  for (int j = 0; j < 64; ++j)
-    if (k0 + j < T) dc[row + k0 + j] = (uint8_t)(codes[j >> 5][(j >> 2) & 7] >> (8 * (j & 3)));
-#pragma unroll
-  for (int b = 0; b < 2; ++b)
-    if (k0 + 32 * b < T) de[row + k0 + 32 * b] = Eb[b];
-}
-
-// Test hook: one row's P^ codes and exponent for one 32-key block.
-__device__ __forceinline__ void dbg_dump_phat1(uint8_t* dc, int32_t* de, int T, int h, int tok, int key_tok0,
-                                               int blk, const uint32_t (&codes)[8], int Eb) {
-  if (dc == nullptr) return;
-  const size_t row = ((size_t)h * T + tok) * (size_t)T;
-  const int k0 = key_tok0 + 32 * blk;
-#pragma unroll
-  for (int j = 0; j < 32; ++j)
-    if (k0 + j < T) dc[row + k0 + j] = (uint8_t)(codes[j >> 2] >> (8 * (j & 3)));
-  if (k0 < T) de[row + k0] = Eb;
+#pragma unroll 1
+  for (int j = 0; j < 32 * nb; ++j)
+    if (k0 + j < T) dc[row + k0 + j] = (uint8_t)(d.w[j >> 2] >> (8 * (j & 3)));
+#pragma unroll 1
+  for (int b = 0; b < nb; ++b)
+    if (k0 + 32 * b < T) de[row + k0 + 32 * b] = d.e[b];
 }
 
 struct WsLayout {

@@ -323,7 +323,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int b = 0; b < 4; ++b)
           if (Eall[b] != kEmptyBlock) word |= (uint32_t)min(max(Eall[b] - m_new + 127, 0), 254) << (8 * b);
         mbar_arrive(&c.k_empty[st]);
-        if (row_ok) dbg_dump_phat1(dbg_c, dbg_e, p.T, h, q0 + r, ds + key0, blk, codes, Eb);
+        if (dbg_c != nullptr && row_ok) {
+          PhatDump d;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) d.w[k] = k < 8 ? codes[k & 7] : 0u;
+          d.e[0] = Eb;
+          d.e[1] = 0;
+          dbg_dump_phat(dbg_c, dbg_e, p.T, h, q0 + r, ds + key0, blk, 1, d);
+        }
         l_run = (m_ref == kEmptyBlock) ? lsum : ldexp_fast(l_run, m_ref - m_new) + lsum;
         // rescale this thread's quarter of the O accumulator row once the
         // previous P^V has landed (warp-uniform: tcgen05.ld/st are
