@@ -20,9 +20,11 @@
 
 namespace flamia {
 
-// x * 2^e for e in [-127, 127] (exact unless the result is subnormal).
-__device__ __forceinline__ float mul_pow2(float x, int e) {
-  return (e >= -126) ? x * exp2i(e) : (x * exp2i(e + 64)) * exp2i(-64);
+// 2^e for e in [-127, 127] as a product of two normal factors (one multiply
+// each, no branch): x * 2^e is exact unless the result is subnormal.
+__device__ __forceinline__ float2 pow2_pair(int e) {
+  const int e1 = e >> 1;
+  return make_float2(exp2i(e1), exp2i(e - e1));
 }
 
 // Reduce v[0..31] (one partial per token, per lane) across the warp so that
@@ -148,9 +150,12 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
     dpart[t] = 0.f;
     const int e_t = __shfl_sync(0xffffffffu, my_e, t);
     if (t < ntok) {
+      // 2^-e_t is a normal fp32 for every exponent of finite data (e_t <= 120),
+      // so one multiply per element is exact down to the E4M3 range
+      const float inv_s = exp2i(max(-e_t, -126));
       float q[EPL];
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) q[e] = mul_pow2(raw[t].at(e), -e_t);
+      for (int e = 0; e < EPL; ++e) q[e] = raw[t].at(e) * inv_s;
       uint8_t* dst = a.codes + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL;
       uint32_t cw;
       if constexpr (EPL == 4) {
@@ -161,14 +166,17 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
         *reinterpret_cast<uint16_t*>(dst) = (uint16_t)cw;
       }
       if constexpr (WITH_D) {
+        // D's terms are code * O (products exact in fp32); the token's 2^e_t
+        // is applied once to the lane's partial sum
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < EPL; e += 2) {
           const float2 d2 = unpack_e4m3x2((uint16_t)(cw >> (8 * e)));
-          acc = fmaf(mul_pow2(d2.x, e_t), orow[t].at(e), acc);
-          acc = fmaf(mul_pow2(d2.y, e_t), orow[t].at(e + 1), acc);
+          acc = fmaf(d2.x, orow[t].at(e), acc);
+          acc = fmaf(d2.y, orow[t].at(e + 1), acc);
         }
-        dpart[t] = acc;
+        const float2 s2 = pow2_pair(e_t);
+        dpart[t] = (acc * s2.x) * s2.y;
       }
     }
   }
