@@ -1024,9 +1024,17 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, void* out, size
 
 int sm_count();
 
-template <typename K>
-static cudaError_t set_smem(K kernel, size_t smem) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+// Raise a kernel's dynamic shared-memory limit once per kernel (not a stream
+// operation, so it is kept out of launches that may be captured in a graph).
+template <auto Kernel>
+static cudaError_t set_smem(size_t smem) {
+  static bool done[64] = {};  // one flag per kernel and device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (done[dev]) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  done[dev] = e == cudaSuccess;
+  return e;
 }
 
 template <int HD, bool OB, bool EX, bool NV4>
@@ -1040,7 +1048,7 @@ static cudaError_t launch_bwd_t(const AttnParams& p, const AttnMaps& m, cudaStre
     if (!det) {
       const size_t smem = bwd_smem_bytes<HD, EX, true, false>();
       static_assert(bwd_smem_bytes<HD, EX, true, false>() <= 232448, "shared memory");
-      if ((e = set_smem(bwd_kernel<HD, OB, EX, true, false>, smem)) != cudaSuccess) return e;
+      if ((e = set_smem<bwd_kernel<HD, OB, EX, true, false>>(smem)) != cudaSuccess) return e;
       if ((e = cudaMemsetAsync(p.dq_acc, 0, sizeof(float) * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
       if ((e = cudaMemsetAsync(&p.hdr->bwd_counter, 0, sizeof(uint32_t), st)) != cudaSuccess) return e;
       bwd_kernel<HD, OB, EX, true, false><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.dq, m.q, m.q);
@@ -1056,14 +1064,14 @@ static cudaError_t launch_bwd_t(const AttnParams& p, const AttnMaps& m, cudaStre
   const size_t smem = bwd_smem_bytes<HD, EX, false, NV4>();
   static_assert(bwd_smem_bytes<HD, EX, false, NV4>() <= 232448, "shared memory");
   static_assert(dq_smem_bytes<HD, NV4>() <= 232448, "shared memory");
-  if ((e = set_smem(bwd_kernel<HD, OB, EX, false, NV4>, smem)) != cudaSuccess) return e;
+  if ((e = set_smem<bwd_kernel<HD, OB, EX, false, NV4>>(smem)) != cudaSuccess) return e;
   // work counters of the two launches below
   if ((e = cudaMemsetAsync(&p.hdr->bwd_counter, 0, 2 * sizeof(uint32_t), st)) != cudaSuccess) return e;
   // without DQ the dQ map is not read (the q map stands in for the argument)
   bwd_kernel<HD, OB, EX, false, NV4><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.q, m.qn, m.kn);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t dsm = dq_smem_bytes<HD, NV4>();
-  if ((e = set_smem(dq_kernel<HD, OB, EX, NV4>, dsm)) != cudaSuccess) return e;
+  if ((e = set_smem<dq_kernel<HD, OB, EX, NV4>>(dsm)) != cudaSuccess) return e;
   long dwork = (long)p.max_items * p.H;
   int dgrid = (int)(dwork < nsm ? dwork : nsm);
   dq_kernel<HD, OB, EX, NV4><<<dgrid, kDqThreads, dsm, st>>>(p, m.q, m.k, m.v, m.dO, m.qn, m.kn);

@@ -439,12 +439,14 @@ template <int HD, bool OB, bool EX, bool NV4>
 static cudaError_t launch_fwd_t(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
   const size_t smem = fwd_smem_bytes<HD, NV4>();
   static_assert(fwd_smem_bytes<HD, NV4>() <= 232448, "shared memory");
-  static bool attr_set = false;
-  if (!attr_set) {
+  static bool attr_set[64] = {};  // per device: raised once, outside any graph capture
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (!attr_set[dev]) {
     cudaError_t e =
         cudaFuncSetAttribute(fwd_kernel<HD, OB, EX, NV4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   long work = (long)p.max_items * p.H;
   int grid = (int)(work < num_sms() ? work : num_sms());
