@@ -400,19 +400,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int h = hk * G + g;
         for (int qt = q_first; qt < n_t; ++qt, ++ii) {
           const int qs = ii & 1;
-          if (!(ok = mbar_wait_warp(&c.qd_empty[qs], ((ii >> 1) & 1) ^ 1, abort_flag, hdr, 0x302))) break;
-          // the tiles first, then the per-row values (their loads overlap the copies)
-          if (lane == 0) {
-            mbar_expect_tx(&c.qd_full[qs], 2 * kTile * HD + (NV4 ? kQKBytes : 0));
-            tma_load_3d(tl.q[qs], &map_q, &c.qd_full[qs], 0, h, ds + kTile * qt);
-            tma_load_3d(tl.dO[qs], &map_do, &c.qd_full[qs], 0, h, ds + kTile * qt);
-            if (NV4) load_score_tile<HD, NV4>(tl.qn[qs], &map_q, &map_qn, &c.qd_full[qs], h, ds + kTile * qt);
-          }
+          // the per-row values are read from global memory before waiting for
+          // the stage, so their latency overlaps the wait
           RowVals v[4];
 #pragma unroll
           for (int rr4 = 0; rr4 < 4; ++rr4) {
             const int i_loc = kTile * qt + lane * 4 + rr4;
             v[rr4] = load_row<NV4>(p, h, ds + i_loc, i_loc < len, ds);
+          }
+          if (!(ok = mbar_wait_warp(&c.qd_empty[qs], ((ii >> 1) & 1) ^ 1, abort_flag, hdr, 0x302))) break;
+          if (lane == 0) {
+            mbar_expect_tx(&c.qd_full[qs], 2 * kTile * HD + (NV4 ? kQKBytes : 0));
+            tma_load_3d(tl.q[qs], &map_q, &c.qd_full[qs], 0, h, ds + kTile * qt);
+            tma_load_3d(tl.dO[qs], &map_do, &c.qd_full[qs], 0, h, ds + kTile * qt);
+            if (NV4) load_score_tile<HD, NV4>(tl.qn[qs], &map_q, &map_qn, &c.qd_full[qs], h, ds + kTile * qt);
           }
 #pragma unroll
           for (int rr4 = 0; rr4 < 4; ++rr4)
