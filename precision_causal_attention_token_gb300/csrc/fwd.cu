@@ -318,10 +318,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         int m_new = m_ref;
         if (Emax != kEmptyBlock && (m_ref == kEmptyBlock || Emax > m_ref + 8)) m_new = Emax;
         const float lsum = (Eb != kEmptyBlock) ? ldexp_fast(lb, Eb - m_new) : 0.f;
+        // the row's scale word (one byte per key block, relative to m) is
+        // built and stored by the row's block-0 thread (warp-uniform)
         uint32_t word = 0;
+        if (blk == 0) {
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
-          if (Eall[b] != kEmptyBlock) word |= (uint32_t)min(max(Eall[b] - m_new + 127, 0), 254) << (8 * b);
+          for (int b = 0; b < 4; ++b)
+            if (Eall[b] != kEmptyBlock) word |= (uint32_t)min(max(Eall[b] - m_new + 127, 0), 254) << (8 * b);
+        }
         mbar_arrive(&c.k_empty[st]);
         if (dbg_c != nullptr && row_ok) {
           PhatDump d;
@@ -365,10 +369,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         *reinterpret_cast<uint4*>(prow + sw128_off(r, 2 * blk)) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
         *reinterpret_cast<uint4*>(prow + sw128_off(r, 2 * blk + 1)) =
             make_uint4(codes[4], codes[5], codes[6], codes[7]);
-        // the row's scale word goes to all four columns (one per thread)
-        tmem_st1(taddr(tb, q * 32, (pb ? kColSFA1 : kColSFA0) + blk), word);
+        // the row's scale word goes to all four columns
+        if (blk == 0) tmem_st4(taddr(tb, q * 32, pb ? kColSFA1 : kColSFA0), word, word, word, word);
         fence_proxy_async_smem();
-        tmem_st_wait();
+        if (blk == 0) tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&c.p_full[pb]);
       }
