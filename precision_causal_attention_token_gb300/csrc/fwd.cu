@@ -29,8 +29,13 @@ namespace flamia {
 
 constexpr int kFwdStages = 3;
 constexpr int kFwdSoftmax = 512;
-constexpr int kFwdThreads = kFwdSoftmax + 64;
+// Warpgroups 0-3 softmax, warpgroup 4: producer (warp 16), MMA issuer (17),
+// two idle warps.  Registers are rebalanced after launch (640 x 96 in total):
+// 4 x 128 x 104 + 128 x 64 = 61440.
+constexpr int kFwdThreads = kFwdSoftmax + 128;
 constexpr int kFwdWarpProd = 16, kFwdWarpMma = 17;
+constexpr uint32_t kFwdRegSoftmax = 104, kFwdRegCtl = 64;
+static_assert(4 * 128 * kFwdRegSoftmax + 128 * kFwdRegCtl <= kFwdThreads * 96, "register split");
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColSFA0 = 384, kColSFA1 = 392, kColSFB = 400;
 
 template <int HD, bool NV4>
@@ -136,7 +141,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after();
 
-  if (warp == kFwdWarpProd) {
+  if (warp >= kFwdWarpProd) {
+   setmaxnreg_dec<kFwdRegCtl>();
+   if (warp == kFwdWarpProd) {
     // ------------------------------------------------------------ producer
     uint32_t kv = 0, qc = 0;
     bool ok = true;
@@ -239,7 +246,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
     }
     __syncwarp();
+   }
   } else {
+    setmaxnreg_inc<kFwdRegSoftmax>();
     // ------------------------------------------------------------ softmax
     const int q = warp & 3, blk = warp >> 2;  // lane quarter, key block
     const int r = 32 * q + lane;              // query row of the tile = TMEM lane
