@@ -108,6 +108,13 @@ __device__ __forceinline__ int noclamp_exp_clamped(float amax) {
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
+// Max over the warp of a non-negative float (no NaN): with the sign bit
+// cleared (a -0 counts as 0) the bit patterns order like unsigned integers,
+// so one integer warp reduction replaces a five-step shuffle chain.
+__device__ __forceinline__ float warp_max(float v) {
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7FFFFFFFu));
+}
+
 // Two fp32 -> two E4M3FN codes (RNE, saturating), `lo` in the low byte.
 __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
   uint16_t r;

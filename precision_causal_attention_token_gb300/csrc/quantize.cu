@@ -120,71 +120,107 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
       else orow[t].zero();
     }
   }
-  // per-token maxima (lane t <- token t) also feed the NVFP4 token scale
-  float pmax[32];
+  if constexpr (!NVFP4) {
+    // MXFP8 codes.  Token-block units: one exponent from the lane maxima and a
+    // single warp reduction.  Per-token units (V, exact option): one warp
+    // reduction per token, so every lane holds that token's exponent.
+    int e_blk = 0;
+    if (!a.per_token) {
+      float lm = 0.f;
 #pragma unroll
-  for (int t = 0; t < 32; ++t) {
-    float m = 0.f;
+      for (int t = 0; t < 32; ++t)
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) m = fmaxf(m, fabsf(raw[t].at(e)));
-    pmax[t] = m;
-  }
-  float tok_amax_arr[32];
+        for (int e = 0; e < EPL; ++e) lm = fmaxf(lm, fabsf(raw[t].at(e)));
+      e_blk = noclamp_exp_clamped(warp_max(lm));
+    }
+    int my_e = e_blk;  // exponent of token `lane`
+    float dpart[WITH_D ? 32 : 1];
 #pragma unroll
-  for (int t = 0; t < 32; ++t) tok_amax_arr[t] = pmax[t];
-  const float my_tok_amax = transpose_reduce<true>(tok_amax_arr, lane);
-  int my_e;  // exponent of token `lane`
-  if (a.per_token) {
-    my_e = noclamp_exp_clamped(my_tok_amax);
-  } else {
-    float bmax = my_tok_amax;
+    for (int t = 0; t < 32; ++t) {
+      int e_t = e_blk;
+      if (a.per_token) {
+        float lm = 0.f;
 #pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, s));
-    my_e = noclamp_exp_clamped(bmax);
-  }
-  if (lane < ntok) a.scales[(size_t)h * a.T + t0 + lane] = (uint8_t)(my_e + 127);
-
-  float dpart[32];
-#pragma unroll
-  for (int t = 0; t < 32; ++t) {
-    dpart[t] = 0.f;
-    const int e_t = __shfl_sync(0xffffffffu, my_e, t);
-    if (t < ntok) {
-      // 2^-e_t is a normal fp32 for every exponent of finite data (e_t <= 120),
-      // so one multiply per element is exact down to the E4M3 range
-      const float inv_s = exp2i(max(-e_t, -126));
-      float q[EPL];
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) q[e] = raw[t].at(e) * inv_s;
-      uint8_t* dst = a.codes + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL;
-      uint32_t cw;
-      if constexpr (EPL == 4) {
-        cw = pack_e4m3x4(q[0], q[1], q[2], q[3]);
-        *reinterpret_cast<uint32_t*>(dst) = cw;
-      } else {
-        cw = pack_e4m3x2(q[0], q[1]);
-        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)cw;
+        for (int e = 0; e < EPL; ++e) lm = fmaxf(lm, fabsf(raw[t].at(e)));
+        e_t = noclamp_exp_clamped(warp_max(lm));
+        if (lane == t) my_e = e_t;
       }
-      if constexpr (WITH_D) {
-        // D's terms are code * O (products exact in fp32); the token's 2^e_t
-        // is applied once to the lane's partial sum
-        float acc = 0.f;
+      if constexpr (WITH_D) dpart[t] = 0.f;
+      if (t < ntok) {
+        // 2^-e_t is a normal fp32 for every exponent of finite data (e_t <= 120),
+        // so one multiply per element is exact down to the E4M3 range
+        const float inv_s = exp2i(max(-e_t, -126));
+        float qv[EPL];
 #pragma unroll
-        for (int e = 0; e < EPL; e += 2) {
-          const float2 d2 = unpack_e4m3x2((uint16_t)(cw >> (8 * e)));
-          acc = fmaf(d2.x, orow[t].at(e), acc);
-          acc = fmaf(d2.y, orow[t].at(e + 1), acc);
+        for (int e = 0; e < EPL; ++e) qv[e] = raw[t].at(e) * inv_s;
+        uint8_t* dst = a.codes + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL;
+        uint32_t cw;
+        if constexpr (EPL == 4) {
+          cw = pack_e4m3x4(qv[0], qv[1], qv[2], qv[3]);
+          *reinterpret_cast<uint32_t*>(dst) = cw;
+        } else {
+          cw = pack_e4m3x2(qv[0], qv[1]);
+          *reinterpret_cast<uint16_t*>(dst) = (uint16_t)cw;
         }
-        const float2 s2 = pow2_pair(e_t);
-        dpart[t] = (acc * s2.x) * s2.y;
+        if constexpr (WITH_D) {
+          // D's terms are code * O (products exact in fp32); the exponent is
+          // applied to the lane's partial sum (per token) or to the token's
+          // sum (token block)
+          float acc = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; e += 2) {
+            const float2 d2 = unpack_e4m3x2((uint16_t)(cw >> (8 * e)));
+            acc = fmaf(d2.x, orow[t].at(e), acc);
+            acc = fmaf(d2.y, orow[t].at(e + 1), acc);
+          }
+          if (a.per_token) {
+            const float2 s2 = pow2_pair(e_t);
+            acc = (acc * s2.x) * s2.y;
+          }
+          dpart[t] = acc;
+        }
       }
     }
-  }
-  if constexpr (WITH_D) {
-    const float dsum = transpose_reduce<false>(dpart, lane);
-    if (lane < ntok) a.D[(size_t)h * a.T + t0 + lane] = dsum;
-  }
-  if constexpr (NVFP4) {
+    if (lane < ntok) a.scales[(size_t)h * a.T + t0 + lane] = (uint8_t)(my_e + 127);
+    if constexpr (WITH_D) {
+      float dsum = transpose_reduce<false>(dpart, lane);
+      if (!a.per_token) {
+        const float2 s2 = pow2_pair(e_blk);
+        dsum = (dsum * s2.x) * s2.y;
+      }
+      if (lane < ntok) a.D[(size_t)h * a.T + t0 + lane] = dsum;
+    }
+    return;
+  } else {
+    // The mixed path's quantizer: MXFP8 codes as above from per-token maxima
+    // (lane t <- token t), which also feed the NVFP4 token scale.
+    float pmax[32];
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      float m = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) m = fmaxf(m, fabsf(raw[t].at(e)));
+      pmax[t] = m;
+    }
+    float tok_amax_arr[32];
+#pragma unroll
+    for (int t = 0; t < 32; ++t) tok_amax_arr[t] = pmax[t];
+    const float my_tok_amax = transpose_reduce<true>(tok_amax_arr, lane);
+    const int my_e = noclamp_exp_clamped(a.per_token ? my_tok_amax : warp_max(my_tok_amax));
+    if (lane < ntok) a.scales[(size_t)h * a.T + t0 + lane] = (uint8_t)(my_e + 127);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      const int e_t = __shfl_sync(0xffffffffu, my_e, t);
+      if (t < ntok) {
+        const float inv_s = exp2i(max(-e_t, -126));
+        float qv[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) qv[e] = raw[t].at(e) * inv_s;
+        uint8_t* dst = a.codes + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL;
+        if constexpr (EPL == 4) *reinterpret_cast<uint32_t*>(dst) = pack_e4m3x4(qv[0], qv[1], qv[2], qv[3]);
+        else *reinterpret_cast<uint16_t*>(dst) = pack_e4m3x2(qv[0], qv[1]);
+      }
+    }
     if (a.codes4 == nullptr) return;  // V has no NVFP4 operand
     // NVFP4 operand for the mixed path's QK^T (FLAMIA summary §3.4, §3.2):
     // per-token fp32 scale g = amax / (6 * 448), 16-element E4M3 block
@@ -228,9 +264,19 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
   }
 }
 
+// Resident 128-thread blocks per SM for each variant: the register
+// footprint is set by the unit held in registers (bf16 pairs packed; with D
+// also O's rows; the mixed path also the per-token maxima).
+template <typename TIn, typename TO, bool WITH_D, bool NVFP4>
+constexpr int quant_blocks_per_sm() {
+  if constexpr (NVFP4) return 3;
+  else if constexpr (WITH_D) return (sizeof(TIn) == 2 && sizeof(TO) == 2) ? 3 : 2;
+  else return sizeof(TIn) == 2 ? 5 : 3;
+}
+
 // Grid-stride over the units of up to three tensors (Q, K, V share a launch).
 template <typename TIn, typename TO, int HD, bool WITH_D, bool NVFP4>
-__global__ void __launch_bounds__(128, WITH_D ? 2 : 3) quantize_kernel(const __grid_constant__ QuantBatch qb,
+__global__ void __launch_bounds__(128, (quant_blocks_per_sm<TIn, TO, WITH_D, NVFP4>())) quantize_kernel(const __grid_constant__ QuantBatch qb,
                                                           const int32_t* __restrict__ cu,
                                                           const int32_t* __restrict__ blk_prefix, int n_seq,
                                                           WsHeader* hdr) {
@@ -255,11 +301,14 @@ __global__ void __launch_bounds__(128, WITH_D ? 2 : 3) quantize_kernel(const __g
 cudaError_t launch_quantize(const QuantBatch& qb, int d, int in_bf16, int o_bf16, bool with_D, bool nvfp4,
                             const int32_t* cu, const int32_t* blk_prefix, int n_seq, WsHeader* hdr,
                             int max_units, int n_sms, cudaStream_t st) {
-  int blocks = (max_units + 3) / 4;                 // four warps per block, one unit per warp
-  const int cap = (with_D ? 2 : 3) * n_sms * 4;     // resident blocks per SM x four waves of grid stride
-  blocks = blocks < 1 ? 1 : (blocks > cap ? cap : blocks);
-#define FLAMIA_QL(TIN, TO_, HD_, WD, NV) \
-  quantize_kernel<TIN, TO_, HD_, WD, NV><<<blocks, 128, 0, st>>>(qb, cu, blk_prefix, n_seq, hdr)
+  const int want = (max_units + 3) / 4;  // four warps per block, one unit per warp
+  // at most four waves of resident blocks; the warps stride over the rest
+#define FLAMIA_QL(TIN, TO_, HD_, WD, NV)                                                      \
+  do {                                                                                        \
+    const int cap = quant_blocks_per_sm<TIN, TO_, WD, NV>() * n_sms * 4;                      \
+    const int blocks = want < 1 ? 1 : (want > cap ? cap : want);                              \
+    quantize_kernel<TIN, TO_, HD_, WD, NV><<<blocks, 128, 0, st>>>(qb, cu, blk_prefix, n_seq, hdr); \
+  } while (0)
 #define FLAMIA_QL_D(TIN, HD_, WD, NV)                           \
   do {                                                          \
     if (o_bf16) FLAMIA_QL(TIN, __nv_bfloat16, HD_, WD, NV);     \
