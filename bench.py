@@ -252,19 +252,21 @@ def run_ours(a):
         if evs:
             evs[0].record(stream)
         tc.plan(stream)
-        fl.flamia_quantize(tc.prob, fl.ROLE_QKV, [q, k, v], None, [tc.opq, tc.opk, tc.opv], None, tc.ws, stream)
         if evs:
             evs[1].record(stream)
-        fl.flamia_fwd(tc.prob, tc.opq, tc.opk, tc.opv, tc.O, tc.m, tc.l, tc.ws, stream)
+        fl.flamia_quantize(tc.prob, fl.ROLE_QKV, [q, k, v], None, [tc.opq, tc.opk, tc.opv], None, tc.ws, stream)
         if evs:
             evs[2].record(stream)
-        fl.flamia_quantize(tc.prob, fl.ROLE_DO, [do], tc.O, [tc.opdo], tc.D, tc.ws, stream)
+        fl.flamia_fwd(tc.prob, tc.opq, tc.opk, tc.opv, tc.O, tc.m, tc.l, tc.ws, stream)
         if evs:
             evs[3].record(stream)
+        fl.flamia_quantize(tc.prob, fl.ROLE_DO, [do], tc.O, [tc.opdo], tc.D, tc.ws, stream)
+        if evs:
+            evs[4].record(stream)
         fl.flamia_bwd(tc.prob, tc.opq, tc.opk, tc.opv, tc.opdo, tc.D, tc.m, tc.l, tc.dQ, tc.dK, tc.dV, tc.ws,
                       stream)
         if evs:
-            evs[4].record(stream)
+            evs[5].record(stream)
 
     for _ in range(max(3, a.warmup)):
         step()
@@ -275,12 +277,12 @@ def run_ours(a):
 
     # per-phase breakdown (and the backward kernel's time for the roofline):
     # launched eagerly with events between the phases
-    evs = [[ev() for _ in range(5)] for _ in range(a.steps)]
+    evs = [[ev() for _ in range(6)] for _ in range(a.steps)]
     for i in range(a.steps):
         step(evs[i], stream)
     torch.cuda.synchronize()
-    ph = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])  # ms
-    quant_ms, fwd_ms, dquant_ms, bwd_ms = ph.mean(axis=0)
+    ph = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in evs])  # ms
+    plan_ms, quant_ms, fwd_ms, dquant_ms, bwd_ms = ph.mean(axis=0)
 
     # timed region: the training call captured once as a CUDA graph (the API
     # neither allocates nor synchronises) and replayed K times
@@ -346,6 +348,11 @@ def run_ours(a):
     peaks, kind = _peaks()
     fp8_sustained = 2.0 * float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     bwd_tflops = bwd_flops / (bwd_ms * 1e-3) / 1e12
+    # the quantizers' algorithmic bytes per token-head: Q/K/V read 2d, write
+    # d codes + 1 scale byte; dO reads dO and O (4d), writes d + 1 + 4 (D)
+    hbm = float(peaks["hbm_gbs"])
+    qkv_gbs = float(w.T) * (w.H + 2 * w.Hkv) * (3 * w.d + 1) / (quant_ms * 1e-3) / 1e9
+    do_gbs = float(w.T) * w.H * (5 * w.d + 5) / (dquant_ms * 1e-3) / 1e9
     n_items = int(sum((l + 127) // 128 for l in w.seqlens))
     launches_per_step = 4 + 1 + 1 + 1 + 2  # plan(4) quantize(Q,K,V in one) fwd dO-quantize bwd dq-convert
     cpu = None
@@ -364,8 +371,11 @@ def run_ours(a):
                    "flops_per_step": flops, "l2": "inputs larger than L2 (256 MiB of bf16 Q/K/V/dO)",
                    "fraction_of_fp8_peak": value / world / fp8_sustained,
                    "timing": "CUDA graph of one training call, replayed; phases from an eager pass with events",
-                   "phase_ms": {"plan+quantize_qkv": quant_ms, "fwd": fwd_ms, "quantize_do": dquant_ms,
+                   "phase_ms": {"plan": plan_ms, "quantize_qkv": quant_ms, "fwd": fwd_ms, "quantize_do": dquant_ms,
                                 "bwd+dq_convert": bwd_ms, "eager_step": float(ph.sum(axis=1).mean())},
+                   "quantizer_hbm": {"qkv_gbs": qkv_gbs, "do_gbs": do_gbs, "peak_gbs": hbm,
+                                     "frac_qkv": qkv_gbs / hbm, "frac_do": do_gbs / hbm,
+                                     "peak_source": f"{kind} hbm_gbs (copy bandwidth)"},
                    "fwd_tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": bwd_tflops},
         "roofline": {"bound": "tensor", "kernel": "bwd_kernel (+dq convert)", "achieved": bwd_tflops,
                      "peak": fp8_sustained, "unit": "TFLOP/s", "frac": bwd_tflops / fp8_sustained,

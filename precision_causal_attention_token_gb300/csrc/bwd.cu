@@ -78,7 +78,7 @@ struct __align__(1024) BwdTiles {
 // Per-row values of one query tile, staged in shared memory by the producer
 // next to the tile's Q / dO codes (off the compute warps' critical path).
 struct RowStage {
-  float rowc, hdo, inv_l, Di;
+  float rowc, hdo, inv_l, nDp;  // nDp = -D 2^-edO
   int mi, eq;
 };
 
@@ -110,13 +110,6 @@ __device__ __forceinline__ uint64_t bdesc_mn(const uint8_t* t, uint32_t off, uin
   return smem_desc(smem_u32(t) + off, 8 * rb, 8 * rb, rb == 128 ? kSwz128 : kSwz64);
 }
 
-// Max over the warp of a non-negative float (no NaN): with the sign bit
-// cleared (a -0 counts as 0) the bit patterns order like unsigned integers,
-// so one integer warp reduction replaces a five-step shuffle chain.
-__device__ __forceinline__ float warp_max(float v) {
-  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7FFFFFFFu));
-}
-
 __device__ __forceinline__ uint32_t sf_byte(int e) { return (uint32_t)min(max(e + 127, 0), 254); }
 
 // Recompute this thread's P^ codes for its two 32-key blocks (b0, b0 + 1) of a
@@ -139,26 +132,23 @@ __device__ __forceinline__ void recompute_phat(uint32_t t_s, int b0, float rowc,
   phat_block_codes(y[1], row_ok ? Eb[1] : kZeroCodes, pcode[1]);
 }
 
-// Per-(row, key block) factors of dS and P~: with gb = 2^(Eb - m) / l (0 for
+// Per-(row, key block) factor of dS and P~: with gb = 2^(Eb - m) / l (0 for
 // an empty block or a row outside the document), Pn = P^ 2^-eV / l =
-// code * gb * 2^-eV, so
-//   dS  = Pn (dP - D) = code * (accdP * gb 2^edO - gb D * 2^-eV(j))
-//   P~ input = Pn 2^edO = code * (gb 2^edO) * 2^-eV(j)   (the dO factor folded in).
-struct DsFactors {
-  float gbh;  // gb * 2^edO
-  float gbD;  // gb * D
-};
-__device__ __forceinline__ DsFactors ds_factors(int Eb_b, int mi, float inv_l, float hdo, float Di) {
-  const float gb = (Eb_b == kEmptyBlock) ? 0.f : ldexp_f(inv_l, Eb_b - mi);
-  return DsFactors{gb * hdo, gb * Di};
+// code * gb * 2^-eV, so with gbh = gb 2^edO and nDp = -D 2^-edO
+//   dS  = Pn (dP - D) = gbh * code * (accdP + nDp 2^-eV(j))      = gbh * w
+//   P~ input = Pn 2^edO = gbh * code * 2^-eV(j)                    = gbh * u
+// (the dO factor folded in).  gbh is a row constant of the block, so it is
+// applied once per block: to the max-abs and to the encoding scale.
+__device__ __forceinline__ float ds_gbh(int Eb_b, int mi, float inv_l, float hdo) {
+  return (Eb_b == kEmptyBlock) ? 0.f : ldexp_f(inv_l, Eb_b - mi) * hdo;
 }
 
-// dS and the P~ input of one 32-key block of this thread's row from the dP
+// w and u (above) of one 32-key block of this thread's row from the dP
 // accumulator values `acc` (fp32 bits), and their max-abs.
-__device__ __forceinline__ void ds_block(const uint32_t (&acc)[32], const uint32_t (&pcode_b)[8], DsFactors f,
-                                         const float* vinv_b, float (&dsv)[32], float (&ptv)[32], float& amax_ds,
-                                         float& amax_pt) {
-  float a_ds = 0.f, a_pt = 0.f;
+__device__ __forceinline__ void ds_block(const uint32_t (&acc)[32], const uint32_t (&pcode_b)[8], float nDp,
+                                         const float* vinv_b, float (&wv)[32], float (&uv)[32], float& amax_w,
+                                         float& amax_u) {
+  float a_w = 0.f, a_u = 0.f;
 #pragma unroll
   for (int q4 = 0; q4 < 8; ++q4) {
     const uint32_t cw = pcode_b[q4];
@@ -170,15 +160,14 @@ __device__ __forceinline__ void ds_block(const uint32_t (&acc)[32], const uint32
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int jj = 4 * q4 + e;
-      const float z = fmaf(__uint_as_float(acc[jj]), f.gbh, -(f.gbD * vv[e]));
-      dsv[jj] = pd[e] * z;
-      ptv[jj] = pd[e] * (f.gbh * vv[e]);
-      a_ds = fmaxf(a_ds, fabsf(dsv[jj]));
-      a_pt = fmaxf(a_pt, ptv[jj]);
+      wv[jj] = pd[e] * fmaf(nDp, vv[e], __uint_as_float(acc[jj]));
+      uv[jj] = pd[e] * vv[e];
+      a_w = fmaxf(a_w, fabsf(wv[jj]));
+      a_u = fmaxf(a_u, uv[jj]);
     }
   }
-  amax_ds = a_ds;
-  amax_pt = a_pt;
+  amax_w = a_w;
+  amax_u = a_u;
 }
 
 // 2^-e for a block exponent e (e <= 120 for any finite max-abs, so the
@@ -259,23 +248,24 @@ __device__ __forceinline__ RowVals load_row(const AttnParams& p, int h, int tok,
   return v;
 }
 
-// The dQ operand of key block b.  Default option: one exponent per 32x32
-// block (reduced over the warp's 32 rows) and scale byte e + eK(block).  Exact
-// option: one exponent per (row, 32 keys) of dS * 2^eK(j), scale byte e.
-// Returns the default option's block exponent (reused for dK) in e_blk.
+// The dQ operand of key block b from dS = gbh * w.  Default option: one
+// exponent per 32x32 block (reduced over the warp's 32 rows) and scale byte
+// e + eK(block).  Exact option: one exponent per (row, 32 keys) of
+// dS * 2^eK(j), scale byte e.  Returns the default option's block exponent
+// (reused for dK) in e_blk.
 template <bool EXACT>
-__device__ __forceinline__ uint32_t dq_operand(const float (&dsv)[32], float amax_ds, const float* kf_b, int ekb,
-                                               uint32_t (&codes)[8], int& e_blk) {
+__device__ __forceinline__ uint32_t dq_operand(const float (&wv)[32], float amax_w, float gbh, const float* kf_b,
+                                               int ekb, uint32_t (&codes)[8], int& e_blk) {
   if constexpr (!EXACT) {
-    e_blk = noclamp_exp_clamped(warp_max(amax_ds));
-    encode32(dsv, inv_pow2(e_blk), codes);
+    e_blk = noclamp_exp_clamped(warp_max(amax_w * gbh));
+    encode32(wv, gbh * inv_pow2(e_blk), codes);
     return sf_byte(e_blk + ekb);
   } else {
     float f[32];
     float am = 0.f;
 #pragma unroll
     for (int jj = 0; jj < 32; ++jj) {
-      f[jj] = dsv[jj] * kf_b[jj];
+      f[jj] = wv[jj] * (gbh * kf_b[jj]);
       am = fmaxf(am, fabsf(f[jj]));
     }
     const int e = noclamp_exp_clamped(am);
@@ -417,8 +407,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
 #pragma unroll
           for (int rr4 = 0; rr4 < 4; ++rr4)
-            c.rows[qs][lane * 4 + rr4] = RowStage{v[rr4].rowc, v[rr4].hdo, 1.0f / v[rr4].li, v[rr4].Di, v[rr4].mi,
-                                                  v[rr4].eq};
+            c.rows[qs][lane * 4 + rr4] = RowStage{v[rr4].rowc, v[rr4].hdo, 1.0f / v[rr4].li,
+                                                  ldexp_f(-v[rr4].Di, -v[rr4].edo), v[rr4].mi, v[rr4].eq};
           mbar_arrive(&c.qd_full[qs]);
         }
       }
@@ -674,33 +664,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int bb = 0; bb < 2; ++bb) {
             const int b = b0 + bb;
-            float dsv[32], ptv[32];
-            float amax_ds, amax_pt;
-            ds_block(dp[bb], pcode[bb], ds_factors(Eb[bb], rv.mi, rv.inv_l, rv.hdo, rv.Di), c.vinv[kvs] + 32 * b, dsv,
-                     ptv, amax_ds, amax_pt);
+            float wv[32], uv[32];
+            float amax_w, amax_u;
+            const float gbh = ds_gbh(Eb[bb], rv.mi, rv.inv_l, rv.hdo);
+            ds_block(dp[bb], pcode[bb], rv.nDp, c.vinv[kvs] + 32 * b, wv, uv, amax_w, amax_u);
             // P~: 32 x 32 block (this warp's 32 queries x key block b)
-            const int e_pt = noclamp_exp_clamped(warp_max(amax_pt));
+            const int e_pt = noclamp_exp_clamped(warp_max(amax_u * gbh));
             uint32_t codes[8];
-            encode32(ptv, inv_pow2(e_pt), codes);
+            encode32(uv, gbh * inv_pow2(e_pt), codes);
             store_row_block(tl.pt, r, b, codes);
             uint32_t kbyte, qbyte = 0;
             if constexpr (!EXACT) {
               int e_ds;
-              qbyte = dq_operand<false>(dsv, amax_ds, c.kf[kvs] + 32 * b, c.ekb[kvs][b], codes, e_ds);
+              qbyte = dq_operand<false>(wv, amax_w, gbh, c.kf[kvs] + 32 * b, c.ekb[kvs][b], codes, e_ds);
               store_row_block(tl.ds, r, b, codes);
               kbyte = sf_byte(e_ds + rv.eq);  // dK operand: the same codes, Q's block exponent folded in
             } else {
               if constexpr (DQ) {
                 int unused;
-                qbyte = dq_operand<true>(dsv, amax_ds, c.kf[kvs] + 32 * b, c.ekb[kvs][b], codes, unused);
+                qbyte = dq_operand<true>(wv, amax_w, gbh, c.kf[kvs] + 32 * b, c.ekb[kvs][b], codes, unused);
                 store_row_block(tl.ds, r, b, codes);
               }
               // dK operand: 32 x 32 block of dS * 2^eQ(i)
-              const float feq = pow2_127(rv.eq);
+              const float gq = gbh * pow2_127(rv.eq);
               float f[32];
 #pragma unroll
-              for (int jj = 0; jj < 32; ++jj) f[jj] = dsv[jj] * feq;
-              const int e_k = noclamp_exp_clamped(warp_max(amax_ds * feq));
+              for (int jj = 0; jj < 32; ++jj) f[jj] = wv[jj] * gq;
+              const int e_k = noclamp_exp_clamped(warp_max(amax_w * gq));
               encode32(f, inv_pow2(e_k), codes);
               store_row_block(tl.dsk, r, b, codes);
               kbyte = sf_byte(e_k);
@@ -937,6 +927,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const bool row_ok = i_loc < len;
       const RowVals rv = load_row<NV4>(p, h, ds + i_loc, row_ok, ds);
       const float inv_l = 1.0f / rv.li;
+      const float nDp = ldexp_f(-rv.Di, -rv.edo);
       for (int kt = 0; ok && kt < n_kt; ++kt, ++kv, ++ii) {
         const int st = kv % kDqStages;
         const uint32_t ph = (kv / kDqStages) & 1;
@@ -958,14 +949,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
         for (int bb = 0; bb < 2; ++bb) {
           const int b = b0 + bb;
-          float dsv[32], ptv[32];
-          float amax_ds, amax_pt;
-          ds_block(dp[bb], pcode[bb], ds_factors(Eb[bb], rv.mi, inv_l, rv.hdo, rv.Di), c.vinv[st] + 32 * b, dsv, ptv,
-                   amax_ds, amax_pt);
+          float wv[32], uv[32];
+          float amax_w, amax_u;
+          const float gbh = ds_gbh(Eb[bb], rv.mi, inv_l, rv.hdo);
+          ds_block(dp[bb], pcode[bb], nDp, c.vinv[st] + 32 * b, wv, uv, amax_w, amax_u);
           uint32_t codes[8];
           int e_blk;
           c.xdq[par][r][b] =
-              (uint8_t)dq_operand<EXACT>(dsv, amax_ds, c.kfold[st] + 32 * b, c.ekb[st][b], codes, e_blk);
+              (uint8_t)dq_operand<EXACT>(wv, amax_w, gbh, c.kfold[st] + 32 * b, c.ekb[st][b], codes, e_blk);
           store_row_block(tl.ds, r, b, codes);
         }
         tc_fence_before();
