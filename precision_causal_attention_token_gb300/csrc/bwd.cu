@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr bool PERKEY = EXACT || NV4;
   constexpr int kQKBytes = score_tile_bytes<HD, NV4>();
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* base = smem_base_1k(smem_raw);
   using Tiles = BwdTiles<HD, EXACT, DQ, NV4>;
   Tiles& tl = *reinterpret_cast<Tiles*>(base);
   BwdCtl& c = *reinterpret_cast<BwdCtl*>(base + sizeof(Tiles));
@@ -786,7 +786,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   constexpr bool PERKEY = EXACT || NV4;
   constexpr int kQKBytes = score_tile_bytes<HD, NV4>();
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* base = smem_base_1k(smem_raw);
   DqTiles<HD, NV4>& tl = *reinterpret_cast<DqTiles<HD, NV4>*>(base);
   DqCtl& c = *reinterpret_cast<DqCtl*>(base + sizeof(DqTiles<HD, NV4>));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

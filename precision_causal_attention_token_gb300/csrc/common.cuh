@@ -156,6 +156,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared-memory buffer rounded up to a 1024-byte boundary (the
+// 128-byte swizzle pattern repeats every 1024 bytes).  The array pointer is
+// offset, rather than an integer copy of its address rounded, so the result
+// stays in the shared address space and every access through it compiles to
+// a shared-memory instruction instead of a generic one.
+__device__ __forceinline__ uint8_t* smem_base_1k(uint8_t* raw) {
+  return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
 }

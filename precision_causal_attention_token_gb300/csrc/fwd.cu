@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   constexpr bool PERKEY = EXACT || NV4;  // the key factor varies within a 32-key block
   constexpr int kQKBytes = score_tile_bytes<HD, NV4>();
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* base = smem_base_1k(smem_raw);
   FwdTiles<HD, NV4>& tl = *reinterpret_cast<FwdTiles<HD, NV4>*>(base);
   FwdCtl& c = *reinterpret_cast<FwdCtl*>(base + sizeof(FwdTiles<HD, NV4>));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
