@@ -42,45 +42,62 @@ constexpr int kEmptyBlock = -(1 << 30);
 template <bool EXACT, bool NEED_MASK>
 __device__ __forceinline__ int phat_block_logits(float (&a)[32], float rowc, const float* kf, const float* vf,
                                                  int i_loc, int key, int len, int causal) {
-  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  // pairs of keys go through the packed fp32 FMA (same rounding as fmaf)
+  float m2[2] = {-INFINITY, -INFINITY};
   const float sb = __fmul_rn(rowc, kf[0]);
+  const uint64_t sb2 = f2_pack(sb, sb);
 #pragma unroll
   for (int j4 = 0; j4 < 8; ++j4) {
     const float4 v4 = *reinterpret_cast<const float4*>(vf + 4 * j4);  // 16-byte aligned factor vectors
-    const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
-    float kk[4] = {0.f, 0.f, 0.f, 0.f};
+    uint64_t sc2[2] = {sb2, sb2};
     if constexpr (EXACT) {
       const float4 k4 = *reinterpret_cast<const float4*>(kf + 4 * j4);
-      kk[0] = k4.x; kk[1] = k4.y; kk[2] = k4.z; kk[3] = k4.w;
+      const uint64_t r2 = f2_pack(rowc, rowc);
+      sc2[0] = f2_mul(r2, f2_pack(k4.x, k4.y));
+      sc2[1] = f2_mul(r2, f2_pack(k4.z, k4.w));
     }
+    const uint64_t vv2[2] = {f2_pack(v4.x, v4.y), f2_pack(v4.z, v4.w)};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int jj = 4 * j4 + e;
-      const float sc = EXACT ? __fmul_rn(rowc, kk[e]) : sb;
-      float y = score_to_y(a[jj], sc, vv[e]);
-      if (NEED_MASK && !visible(i_loc, key + jj, len, causal)) y = -INFINITY;
-      a[jj] = y;
-      m4[e] = fmaxf(m4[e], y);
+    for (int h = 0; h < 2; ++h) {
+      const int jj = 4 * j4 + 2 * h;
+      float y0, y1;
+      f2_unpack(f2_fma(f2_pack(a[jj], a[jj + 1]), sc2[h], vv2[h]), y0, y1);
+      if (NEED_MASK && !visible(i_loc, key + jj, len, causal)) y0 = -INFINITY;
+      if (NEED_MASK && !visible(i_loc, key + jj + 1, len, causal)) y1 = -INFINITY;
+      a[jj] = y0;
+      a[jj + 1] = y1;
+      m2[h] = fmax3(m2[h], y0, y1);
     }
   }
-  const float M = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+  const float M = fmaxf(m2[0], m2[1]);
   return (M == -INFINITY) ? kEmptyBlock : phat_block_exp(M);
 }
 
-// p = 2^(y - E) (<= 448 up to the approximation of ex2; the cvt saturates).
-// An empty block (E = kEmptyBlock) has y = -inf everywhere, so p = 0 with no
-// test; a caller that wants zeros for finite y passes E = kZeroCodes.
-__device__ __forceinline__ float phat_value(float y, int E) { return ex2_approx(__fsub_rn(y, (float)E)); }
+// p = 2^(y - E) for two keys (<= 448 up to the approximation of ex2; the cvt
+// saturates), with nE2 = phat_neg_exp(E).  An empty block (E = kEmptyBlock)
+// has y = -inf everywhere, so p = 0 with no test; a caller that wants zeros
+// for finite y passes E = kZeroCodes.  y + (-E) is the IEEE difference y - E.
+__device__ __forceinline__ uint64_t phat_neg_exp(int E) {
+  const float nE = -(float)E;
+  return f2_pack(nE, nE);
+}
+__device__ __forceinline__ void phat_values2(float y0, float y1, uint64_t nE2, float& p0, float& p1) {
+  float d0, d1;
+  f2_unpack(f2_add(f2_pack(y0, y1), nE2), d0, d1);
+  p0 = ex2_approx(d0);
+  p1 = ex2_approx(d1);
+}
 constexpr int kZeroCodes = 1 << 30;  // 2^(y - 2^30) = 0 for every finite logit
 
 // P^ codes of one 32-key block from its logits and exponent, as 8 words of
 // 4 E4M3 bytes.
 __device__ __forceinline__ void phat_block_codes(const float (&y)[32], int E, uint32_t (&codes)[8]) {
+  const uint64_t nE2 = phat_neg_exp(E);
 #pragma unroll
   for (int q4 = 0; q4 < 8; ++q4) {
     float pv[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) pv[e] = phat_value(y[4 * q4 + e], E);
+    phat_values2(y[4 * q4], y[4 * q4 + 1], nE2, pv[0], pv[1]);
+    phat_values2(y[4 * q4 + 2], y[4 * q4 + 3], nE2, pv[2], pv[3]);
     codes[q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
   }
 }

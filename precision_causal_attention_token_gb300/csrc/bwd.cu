@@ -114,7 +114,7 @@ __device__ __forceinline__ uint32_t sf_byte(int e) { return (uint32_t)min(max(e 
 
 // Recompute this thread's P^ codes for its two 32-key blocks (b0, b0 + 1) of a
 // 128-key tile from S in TMEM, with the forward's arithmetic
-// (phat_block_logits, phat_value): the same inputs give the same codes and
+// (phat_block_logits, phat_values2): the same inputs give the same codes and
 // block exponents.  Rows outside the document give empty blocks (codes 0).
 template <bool EXACT>
 __device__ __forceinline__ void recompute_phat(uint32_t t_s, int b0, float rowc, const float* kf, const float* vf,
@@ -148,26 +148,31 @@ __device__ __forceinline__ float ds_gbh(int Eb_b, int mi, float inv_l, float hdo
 __device__ __forceinline__ void ds_block(const uint32_t (&acc)[32], const uint32_t (&pcode_b)[8], float nDp,
                                          const float* vinv_b, float (&wv)[32], float (&uv)[32], float& amax_w,
                                          float& amax_u) {
-  float a_w = 0.f, a_u = 0.f;
+  // key pairs through the packed fp32 instructions; max |w| as the larger of
+  // max w and -min w, each in two partial chains of three-input max / min
+  float w_hi[2] = {0.f, 0.f}, w_lo[2] = {0.f, 0.f}, a_u[2] = {0.f, 0.f};
+  const uint64_t nD2 = f2_pack(nDp, nDp);
 #pragma unroll
   for (int q4 = 0; q4 < 8; ++q4) {
     const uint32_t cw = pcode_b[q4];
     const float2 p01 = unpack_e4m3x2((uint16_t)(cw & 0xFFFFu));
     const float2 p23 = unpack_e4m3x2((uint16_t)(cw >> 16));
-    const float pd[4] = {p01.x, p01.y, p23.x, p23.y};
     const float4 vi = *reinterpret_cast<const float4*>(vinv_b + 4 * q4);
-    const float vv[4] = {vi.x, vi.y, vi.z, vi.w};
+    const uint64_t pd2[2] = {f2_pack(p01.x, p01.y), f2_pack(p23.x, p23.y)};
+    const uint64_t vv2[2] = {f2_pack(vi.x, vi.y), f2_pack(vi.z, vi.w)};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int jj = 4 * q4 + e;
-      wv[jj] = pd[e] * fmaf(nDp, vv[e], __uint_as_float(acc[jj]));
-      uv[jj] = pd[e] * vv[e];
-      a_w = fmaxf(a_w, fabsf(wv[jj]));
-      a_u = fmaxf(a_u, uv[jj]);
+    for (int h = 0; h < 2; ++h) {
+      const int jj = 4 * q4 + 2 * h;
+      const uint64_t y2 = f2_fma(nD2, vv2[h], f2_pack(__uint_as_float(acc[jj]), __uint_as_float(acc[jj + 1])));
+      f2_unpack(f2_mul(pd2[h], y2), wv[jj], wv[jj + 1]);
+      f2_unpack(f2_mul(pd2[h], vv2[h]), uv[jj], uv[jj + 1]);
+      w_hi[h] = fmax3(w_hi[h], wv[jj], wv[jj + 1]);
+      w_lo[h] = fmin3(w_lo[h], wv[jj], wv[jj + 1]);
+      a_u[h] = fmax3(a_u[h], uv[jj], uv[jj + 1]);
     }
   }
-  amax_w = a_w;
-  amax_u = a_u;
+  amax_w = fmaxf(fmaxf(w_hi[0], w_hi[1]), -fminf(w_lo[0], w_lo[1]));
+  amax_u = fmaxf(a_u[0], a_u[1]);
 }
 
 // 2^-e for a block exponent e (e <= 120 for any finite max-abs, so the
@@ -176,9 +181,14 @@ __device__ __forceinline__ float inv_pow2(int e) { return exp2i(-min(e, 126)); }
 
 // Codes of 32 values times s (a power of two), as 8 words of 4 E4M3 bytes.
 __device__ __forceinline__ void encode32(const float (&v)[32], float s, uint32_t (&out)[8]) {
+  const uint64_t s2 = f2_pack(s, s);
 #pragma unroll
-  for (int q4 = 0; q4 < 8; ++q4)
-    out[q4] = pack_e4m3x4(v[4 * q4] * s, v[4 * q4 + 1] * s, v[4 * q4 + 2] * s, v[4 * q4 + 3] * s);
+  for (int q4 = 0; q4 < 8; ++q4) {
+    float x[4];
+    f2_unpack(f2_mul(f2_pack(v[4 * q4], v[4 * q4 + 1]), s2), x[0], x[1]);
+    f2_unpack(f2_mul(f2_pack(v[4 * q4 + 2], v[4 * q4 + 3]), s2), x[2], x[3]);
+    out[q4] = pack_e4m3x4(x[0], x[1], x[2], x[3]);
+  }
 }
 
 // Store 32 codes (keys 32b..32b+31) of row r into a 128B-swizzled [128][128] tile.

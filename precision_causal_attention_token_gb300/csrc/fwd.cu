@@ -298,19 +298,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           else
             Eb = phat_logits1<PERKEY, false>(t_s, y, rowc, kfb, vfb, i_loc, key0 + 32 * blk, len, p.causal);
           const float* vi = c.vinv[st] + 32 * blk;
-          float l4[4] = {0.f, 0.f, 0.f, 0.f};
+          const uint64_t nE2 = phat_neg_exp(Eb);
+          uint64_t l2[2] = {0ull, 0ull};  // four partial sums, two per packed pair
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
             const float4 v4 = *reinterpret_cast<const float4*>(vi + 4 * q4);
-            const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
-            float pv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              pv[e] = phat_value(y[4 * q4 + e], Eb);  // 0 on an empty block (y = -inf)
-              l4[e] = fmaf(pv[e], vv[e], l4[e]);
-            }
+            float pv[4];  // 0 on an empty block (y = -inf)
+            phat_values2(y[4 * q4], y[4 * q4 + 1], nE2, pv[0], pv[1]);
+            phat_values2(y[4 * q4 + 2], y[4 * q4 + 3], nE2, pv[2], pv[3]);
+            l2[0] = f2_fma(f2_pack(pv[0], pv[1]), f2_pack(v4.x, v4.y), l2[0]);
+            l2[1] = f2_fma(f2_pack(pv[2], pv[3]), f2_pack(v4.z, v4.w), l2[1]);
             codes[q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
           }
+          float l4[4];
+          f2_unpack(l2[0], l4[0], l4[1]);
+          f2_unpack(l2[1], l4[2], l4[3]);
           lb = (l4[0] + l4[1]) + (l4[2] + l4[3]);
         }
         tc_fence_before();
