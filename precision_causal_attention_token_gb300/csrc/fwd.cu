@@ -205,42 +205,48 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int len = __ldg(p.cu + it.x + 1) - __ldg(p.cu + it.x);
         const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
         if (!(ok = mbar_wait(&c.q_full, qc & 1, abort_flag, hdr, 0x211))) break;
-        const uint32_t kv_base = kv;
-        for (int kt = 0; ok && kt <= n_kt; ++kt) {
-          if (kt < n_kt) {
-            const int st = kv % kFwdStages;
-            const uint32_t ph = (kv / kFwdStages) & 1;
-            const uint32_t sb = sc & 1, sph = (sc >> 1) & 1;
-            if (!(ok = mbar_wait(&c.k_full[st], ph, abort_flag, hdr, 0x212))) break;
-            if (!(ok = mbar_wait(&c.s_free[sb], sph ^ 1, abort_flag, hdr, 0x213))) break;
-            tc_fence_after();
-            issue_scores<HD, NV4>(tb + (sb ? kColS1 : kColS0), tl.q, tl.k[st]);
-            tc_commit(&c.s_full[sb]);
-            tc_commit(&c.k_empty[st]);
-            if (kt == n_kt - 1) tc_commit(&c.q_empty);
-            ++sc;
-            ++kv;
-          }
-          if (kt >= 1) {
-            const uint32_t j = kt - 1, vidx = kv_base + j;
-            const int vst = vidx % kFwdStages;
-            const uint32_t vph = (vidx / kFwdStages) & 1;
-            const uint32_t pb = pc & 1, pph = (pc >> 1) & 1;
-            if (!(ok = mbar_wait(&c.p_full[pb], pph, abort_flag, hdr, 0x214))) break;
-            if (!(ok = mbar_wait(&c.v_full[vst], vph, abort_flag, hdr, 0x215))) break;
-            if (j == 0 && !(ok = mbar_wait(&c.o_free, (ic & 1) ^ 1, abort_flag, hdr, 0x216))) break;
-            tc_fence_after();
-            const uint32_t sfa = tb + (pb ? kColSFA1 : kColSFA0);
+        // S runs two tiles ahead of P^V: the softmax warps release S(t)'s
+        // buffer a full tile before they hand over P^(t), so S(t + 2) can be
+        // issued as soon as P^V(t - 1) is, and is ready a tile later.
+        auto issue_s = [&](int t) -> bool {
+          const uint32_t kvt = kv + t, sct = sc + t;
+          const int st = kvt % kFwdStages;
+          const uint32_t ph = (kvt / kFwdStages) & 1;
+          const uint32_t sb = sct & 1, sph = (sct >> 1) & 1;
+          if (!mbar_wait(&c.k_full[st], ph, abort_flag, hdr, 0x212)) return false;
+          if (!mbar_wait(&c.s_free[sb], sph ^ 1, abort_flag, hdr, 0x213)) return false;
+          tc_fence_after();
+          issue_scores<HD, NV4>(tb + (sb ? kColS1 : kColS0), tl.q, tl.k[st]);
+          tc_commit(&c.s_full[sb]);
+          tc_commit(&c.k_empty[st]);
+          if (t == n_kt - 1) tc_commit(&c.q_empty);
+          return true;
+        };
+        if (!(ok = issue_s(0))) break;
+        if (n_kt > 1 && !(ok = issue_s(1))) break;
+        for (int j = 0; ok && j < n_kt; ++j) {
+          if (j + 2 < n_kt && !(ok = issue_s(j + 2))) break;
+          const uint32_t vidx = kv + j, pct = pc + j;
+          const int vst = vidx % kFwdStages;
+          const uint32_t vph = (vidx / kFwdStages) & 1;
+          const uint32_t pb = pct & 1, pph = (pct >> 1) & 1;
+          if (!(ok = mbar_wait(&c.p_full[pb], pph, abort_flag, hdr, 0x214))) break;
+          if (!(ok = mbar_wait(&c.v_full[vst], vph, abort_flag, hdr, 0x215))) break;
+          if (j == 0 && !(ok = mbar_wait(&c.o_free, (ic & 1) ^ 1, abort_flag, hdr, 0x216))) break;
+          tc_fence_after();
+          const uint32_t sfa = tb + (pb ? kColSFA1 : kColSFA0);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_mxf8(tb + kColO, desc_kmajor(tl.p[pb], 32 * kk, 128), desc_mnmajor(tl.v[vst], 32 * kk * HD, HD),
-                       idesc_mxf8(128, HD, 0, 1, kk, kk), sfa, tb + kColSFB, (j > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(&c.p_free[pb]);
-            tc_commit(&c.v_empty[vst]);
-            if ((int)j == n_kt - 1) tc_commit(&c.o_full);
-            ++pc;
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            mma_mxf8(tb + kColO, desc_kmajor(tl.p[pb], 32 * kk, 128), desc_mnmajor(tl.v[vst], 32 * kk * HD, HD),
+                     idesc_mxf8(128, HD, 0, 1, kk, kk), sfa, tb + kColSFB, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&c.p_free[pb]);
+          tc_commit(&c.v_empty[vst]);
+          if (j == n_kt - 1) tc_commit(&c.o_full);
         }
+        if (!ok) break;
+        kv += n_kt;
+        sc += n_kt;
+        pc += n_kt;
         ++qc;
         ++ic;
       }
@@ -276,53 +282,70 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       int m_ref = kEmptyBlock;
       float l_run = 0.f;  // this thread's share of the normaliser (its key block)
-      for (int kt = 0; ok && kt < n_kt; ++kt, ++kv, ++sc, ++pc) {
-        const int st = kv % kFwdStages;
-        const uint32_t kph = (kv / kFwdStages) & 1;
-        const uint32_t sb = sc & 1, sph = (sc >> 1) & 1;
-        if (!(ok = mbar_wait_warp(&c.k_full[st], kph, abort_flag, hdr, 0x221))) break;
-        if (!(ok = mbar_wait_warp(&c.s_full[sb], sph, abort_flag, hdr, 0x222))) break;
+      // Software pipeline over the key tiles: the logits, P^ codes and block
+      // exponent of tile t + 1 are computed while the exponents of tile t
+      // are being exchanged among the row's four threads, so the exchange
+      // latency overlaps work.  Tile t uses counters kv + t, sc + t, pc + t.
+      // Part A (tile t): S and the per-key vectors in, codes / Eb / partial
+      // normaliser out, S buffer and key vectors released.
+      auto part_a = [&](int t, uint32_t (&codes)[8], int& Eb, float& lb) -> bool {
+        const uint32_t kvt = kv + t, sct = sc + t;
+        const int st = kvt % kFwdStages;
+        const uint32_t kph = (kvt / kFwdStages) & 1;
+        const uint32_t sb = sct & 1, sph = (sct >> 1) & 1;
+        if (!mbar_wait_warp(&c.k_full[st], kph, abort_flag, hdr, 0x221)) return false;
+        if (!mbar_wait_warp(&c.s_full[sb], sph, abort_flag, hdr, 0x222)) return false;
         tc_fence_after();
-        const int key0 = kTile * kt;
-        int Eb;
-        float lb;
-        uint32_t codes[8];
-        {
-          float y[32];
-          const uint32_t t_s = taddr(tb, q * 32, (sb ? kColS1 : kColS0) + 32 * blk);
-          const float* kfb = c.kf[st] + 32 * blk;
-          const float* vfb = c.vf[st] + 32 * blk;
-          // the diagonal tile (or a document's last tile) is the only one with masked keys
-          if (kt == n_kt - 1)
-            Eb = phat_logits1<PERKEY, true>(t_s, y, rowc, kfb, vfb, i_loc, key0 + 32 * blk, len, p.causal);
-          else
-            Eb = phat_logits1<PERKEY, false>(t_s, y, rowc, kfb, vfb, i_loc, key0 + 32 * blk, len, p.causal);
-          const float* vi = c.vinv[st] + 32 * blk;
-          const uint64_t nE2 = phat_neg_exp(Eb);
-          uint64_t l2[2] = {0ull, 0ull};  // four partial sums, two per packed pair
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            const float4 v4 = *reinterpret_cast<const float4*>(vi + 4 * q4);
-            float pv[4];  // 0 on an empty block (y = -inf)
-            phat_values2(y[4 * q4], y[4 * q4 + 1], nE2, pv[0], pv[1]);
-            phat_values2(y[4 * q4 + 2], y[4 * q4 + 3], nE2, pv[2], pv[3]);
-            l2[0] = f2_fma(f2_pack(pv[0], pv[1]), f2_pack(v4.x, v4.y), l2[0]);
-            l2[1] = f2_fma(f2_pack(pv[2], pv[3]), f2_pack(v4.z, v4.w), l2[1]);
-            codes[q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
-          }
-          float l4[4];
-          f2_unpack(l2[0], l4[0], l4[1]);
-          f2_unpack(l2[1], l4[2], l4[3]);
-          lb = (l4[0] + l4[1]) + (l4[2] + l4[3]);
-        }
+        const int key0 = kTile * t;
+        float y[32];
+        const uint32_t t_s = taddr(tb, q * 32, (sb ? kColS1 : kColS0) + 32 * blk);
+        const float* kfb = c.kf[st] + 32 * blk;
+        const float* vfb = c.vf[st] + 32 * blk;
+        // the diagonal tile (or a document's last tile) is the only one with masked keys
+        if (t == n_kt - 1)
+          Eb = phat_logits1<PERKEY, true>(t_s, y, rowc, kfb, vfb, i_loc, key0 + 32 * blk, len, p.causal);
+        else
+          Eb = phat_logits1<PERKEY, false>(t_s, y, rowc, kfb, vfb, i_loc, key0 + 32 * blk, len, p.causal);
         tc_fence_before();
         mbar_arrive(&c.s_free[sb]);
-        // the row's reference needs all four block exponents: exchange with
-        // the row's other three threads (an mbarrier with a bounded wait)
-        const int par = sc & 1;
-        c.ebx[par][r][blk] = Eb;
+        const float* vi = c.vinv[st] + 32 * blk;
+        const uint64_t nE2 = phat_neg_exp(Eb);
+        uint64_t l2[2] = {0ull, 0ull};  // four partial sums, two per packed pair
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 v4 = *reinterpret_cast<const float4*>(vi + 4 * q4);
+          float pv[4];  // 0 on an empty block (y = -inf)
+          phat_values2(y[4 * q4], y[4 * q4 + 1], nE2, pv[0], pv[1]);
+          phat_values2(y[4 * q4 + 2], y[4 * q4 + 3], nE2, pv[2], pv[3]);
+          l2[0] = f2_fma(f2_pack(pv[0], pv[1]), f2_pack(v4.x, v4.y), l2[0]);
+          l2[1] = f2_fma(f2_pack(pv[2], pv[3]), f2_pack(v4.z, v4.w), l2[1]);
+          codes[q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
+        }
+        mbar_arrive(&c.k_empty[st]);  // key vectors no longer read
+        float l4[4];
+        f2_unpack(l2[0], l4[0], l4[1]);
+        f2_unpack(l2[1], l4[2], l4[3]);
+        lb = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        return true;
+      };
+      // the row's reference needs all four block exponents: each thread
+      // publishes its own to the row's other three (an mbarrier per lane
+      // quarter, one phase per tile, with a bounded wait)
+      auto publish = [&](int t, int Eb) {
+        c.ebx[(sc + t) & 1][r][blk] = Eb;
         mbar_arrive(&c.eb_bar[q]);
-        if (!(ok = mbar_wait_warp(&c.eb_bar[q], sc & 1, abort_flag, hdr, 0x226))) break;
+      };
+      uint32_t codes[8], codes_n[8];
+      int Eb = 0, Eb_n = 0;
+      float lb = 0.f, lb_n = 0.f;
+      if (!(ok = part_a(0, codes, Eb, lb))) break;
+      publish(0, Eb);
+      for (int kt = 0; ok && kt < n_kt; ++kt) {
+        const bool more = kt + 1 < n_kt;
+        if (more && !(ok = part_a(kt + 1, codes_n, Eb_n, lb_n))) break;
+        const uint32_t sct = sc + kt, pct = pc + kt;
+        const int par = sct & 1;
+        if (!(ok = mbar_wait_warp(&c.eb_bar[q], sct & 1, abort_flag, hdr, 0x226))) break;
         const int4 e4 = *reinterpret_cast<const int4*>(c.ebx[par][r]);
         const int Eall[4] = {e4.x, e4.y, e4.z, e4.w};
         const int Emax = max(max(Eall[0], Eall[1]), max(Eall[2], Eall[3]));
@@ -330,28 +353,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (Emax != kEmptyBlock && (m_ref == kEmptyBlock || Emax > m_ref + 8)) m_new = Emax;
         const float lsum = (Eb != kEmptyBlock) ? ldexp_fast(lb, Eb - m_new) : 0.f;
         // the row's scale word (one byte per key block, relative to m) is
-        // built and stored by the row's block-0 thread (warp-uniform)
+        // built and stored by the row's block-0 thread
         uint32_t word = 0;
         if (blk == 0) {
 #pragma unroll
           for (int b = 0; b < 4; ++b)
             if (Eall[b] != kEmptyBlock) word |= (uint32_t)min(max(Eall[b] - m_new + 127, 0), 254) << (8 * b);
         }
-        mbar_arrive(&c.k_empty[st]);
         if (dbg_c != nullptr && row_ok) {
           PhatDump d;
 #pragma unroll
           for (int k = 0; k < 16; ++k) d.w[k] = k < 8 ? codes[k & 7] : 0u;
           d.e[0] = Eb;
           d.e[1] = 0;
-          dbg_dump_phat(dbg_c, dbg_e, p.T, h, q0 + r, ds + key0, blk, 1, d);
+          dbg_dump_phat(dbg_c, dbg_e, p.T, h, q0 + r, ds + kTile * kt, blk, 1, d);
         }
         l_run = (m_ref == kEmptyBlock) ? lsum : ldexp_fast(l_run, m_ref - m_new) + lsum;
         // rescale this thread's quarter of the O accumulator row once the
         // previous P^V has landed (warp-uniform: tcgen05.ld/st are
         // warp-collective; lanes whose reference did not move scale by 1)
         if (__any_sync(0xffffffffu, kt > 0 && m_new != m_ref)) {
-          const uint32_t pp = pc - 1;
+          const uint32_t pp = pct - 1;
           if (!(ok = mbar_wait_warp(&c.p_free[pp & 1], (pp >> 1) & 1, abort_flag, hdr, 0x223))) break;
           tc_fence_after();
           const float f = (m_new != m_ref) ? ldexp_fast(1.0f, m_ref - m_new) : 1.0f;
@@ -374,8 +396,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tmem_st_wait();
         }
         m_ref = m_new;
-        const uint32_t pb = pc & 1;
-        if (!(ok = mbar_wait_warp(&c.p_free[pb], ((pc >> 1) & 1) ^ 1, abort_flag, hdr, 0x224))) break;
+        const uint32_t pb = pct & 1;
+        if (!(ok = mbar_wait_warp(&c.p_free[pb], ((pct >> 1) & 1) ^ 1, abort_flag, hdr, 0x224))) break;
         uint8_t* prow = tl.p[pb];
         *reinterpret_cast<uint4*>(prow + sw128_off(r, 2 * blk)) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
         *reinterpret_cast<uint4*>(prow + sw128_off(r, 2 * blk + 1)) =
@@ -386,7 +408,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (blk == 0) tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&c.p_full[pb]);
+        if (more) {
+          publish(kt + 1, Eb_n);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) codes[k] = codes_n[k];
+          Eb = Eb_n;
+          lb = lb_n;
+        }
       }
+      kv += n_kt;
+      sc += n_kt;
+      pc += n_kt;
       if (!ok) break;
       // epilogue: O = acc / l (this thread: a quarter of the row)
       c.lx[r][blk] = l_run;

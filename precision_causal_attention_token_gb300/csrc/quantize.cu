@@ -126,12 +126,14 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
     // reduction per token, so every lane holds that token's exponent.
     int e_blk = 0;
     if (!a.per_token) {
-      float lm = 0.f;
+      // four partial maxima (short dependency chains), three-input max
+      float lm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int t = 0; t < 32; ++t)
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) lm = fmaxf(lm, fabsf(raw[t].at(e)));
-      e_blk = noclamp_exp_clamped(warp_max(lm));
+        for (int e = 0; e < EPL; e += 2)
+          lm[t & 3] = fmax3(lm[t & 3], fabsf(raw[t].at(e)), fabsf(raw[t].at(e + 1)));
+      e_blk = noclamp_exp_clamped(warp_max(fmaxf(fmaxf(lm[0], lm[1]), fmaxf(lm[2], lm[3]))));
     }
     int my_e = e_blk;  // exponent of token `lane`
     float dpart[WITH_D ? 32 : 1];
