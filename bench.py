@@ -45,6 +45,9 @@ def _args():
     ap.add_argument("--ref-sample-tokens", type=int, default=1024,
                     help="causal prefix length per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5],
+                    help="2: batched 4x4096 (the benchmark workload); 3: packed 8x16384 log-normal documents; "
+                         "4: mixed NVFP4/FP8 path, packed 4x32768; 5: long GQA 2x65536, H=32, Hkv=8")
     ap.add_argument("--rows", type=int, default=4,
                     help="4096-token rows of the batched workload (4 = the benchmark workload; fewer rows give "
                          "a smaller case of the same kernels for profiler captures)")
@@ -169,8 +172,10 @@ def _profiled_traffic(kernel: str):
     return float(mb.group(1))
 
 
-def _workload(rows: int = 4):
+def _workload(rows: int = 4, idx: int = 2):
     import synth
+    if idx != 2:
+        return synth.workload(idx)
     w = synth.workload(2)
     if rows != 4:
         w = synth.custom([4096] * rows, H=16, d=128, seed=w.seed, name=f"batched {rows}x4096 H=16 d=128 bf16")
@@ -236,10 +241,11 @@ def run_ours(a):
     dev = torch.device("cuda", local)
     __graft_entry__.build()
 
-    w = _workload(a.rows)
+    w = _workload(a.rows, a.workload)
+    mixed = a.workload == 4
     q, k, v, do = (torch.from_numpy(w.tensor(n)).to(dev, torch.bfloat16) for n in ("q", "k", "v", "do"))
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
-    tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu)
+    tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu, path=fl.PATH_NVFP4_FP8 if mixed else fl.PATH_MXFP8)
     flops = w.flops()
     pairs = w.causal_pairs
     fwd_flops, bwd_flops = 4.0 * w.d * w.H * pairs, 10.0 * w.d * w.H * pairs
@@ -366,16 +372,18 @@ def run_ours(a):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 (MXFP8 operands, fp32 accumulate)", "data": "synthetic",
-        "config": {"workload": WORKLOAD.format(rows=a.rows), "tokens": w.T, "heads": w.H, "head_dim": w.d, "documents": len(w.seqlens),
+        "dtype": ("e2m1/e4m3 scores (NVFP4), e4m3 elsewhere, fp32 accumulate" if mixed
+                  else "e4m3 (MXFP8 operands, fp32 accumulate)"), "data": "synthetic",
+        "config": {"workload": WORKLOAD.format(rows=a.rows) if a.workload == 2 else w.name, "tokens": w.T, "heads": w.H, "head_dim": w.d, "documents": len(w.seqlens),
                    "flops_per_step": flops, "l2": "inputs larger than L2 (256 MiB of bf16 Q/K/V/dO)",
                    "fraction_of_fp8_peak": value / world / fp8_sustained,
                    "timing": "CUDA graph of one training call, replayed; phases from an eager pass with events",
                    "phase_ms": {"plan": plan_ms, "quantize_qkv": quant_ms, "fwd": fwd_ms, "quantize_do": dquant_ms,
                                 "bwd+dq_convert": bwd_ms, "eager_step": float(ph.sum(axis=1).mean())},
-                   "quantizer_hbm": {"qkv_gbs": qkv_gbs, "do_gbs": do_gbs, "peak_gbs": hbm,
-                                     "frac_qkv": qkv_gbs / hbm, "frac_do": do_gbs / hbm,
-                                     "peak_source": f"{kind} hbm_gbs (copy bandwidth)"},
+                   "quantizer_hbm": None if mixed else {
+                       "qkv_gbs": qkv_gbs, "do_gbs": do_gbs, "peak_gbs": hbm,
+                       "frac_qkv": qkv_gbs / hbm, "frac_do": do_gbs / hbm,
+                       "peak_source": f"{kind} hbm_gbs (copy bandwidth)"},
                    "fwd_tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": bwd_tflops},
         "roofline": {"bound": "tensor", "kernel": "bwd_kernel (+dq convert)", "achieved": bwd_tflops,
                      "peak": fp8_sustained, "unit": "TFLOP/s", "frac": bwd_tflops / fp8_sustained,
