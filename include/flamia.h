@@ -23,7 +23,8 @@
  *     plan/quantize/fwd/bwd, so the sequence can be captured in a CUDA graph.
  *   - Packed token-major layouts: activations [T][heads][d] (row-major, d
  *     contiguous); per-token metadata [heads][T].
- *   - All device pointers must be 16-byte aligned; tensors are contiguous.
+ *   - Every device pointer must be 16-byte aligned (cu_seqlens: 4-byte);
+ *     tensors are contiguous.
  *   - Arguments are validated on the host before any launch; a violation
  *     returns FLAMIA_ERR_INVALID_ARG or FLAMIA_ERR_UNSUPPORTED and launches
  *     nothing.  Launch failures return FLAMIA_ERR_CUDA.  Device-side
@@ -181,6 +182,20 @@ flamia_status_t flamia_clear_device_status(void* ws, cudaStream_t stream);
  * hook off.  Must be called after flamia_plan (which does not touch it) and
  * synchronises `stream`. */
 flamia_status_t flamia_debug_set_phat_dump(void* ws, size_t ws_bytes, void* codes, int32_t* exps,
+                                           cudaStream_t stream);
+
+/* Test hook (not for the hot path): make the next flamia_fwd / flamia_bwd
+ * calls on workspace `ws` exercise their bounded waits.  wait_ns != 0
+ * replaces the limit of every wait inside the attention kernels (default
+ * about 2 s; at most 10 s accepted); withhold_first_item != 0 makes each CTA's
+ * producer withhold its first work item, so the other roles' waits for it
+ * run out: the kernel then records FLAMIA_ERR_TIMEOUT in the device status
+ * word, every role leaves its loop and the CTA releases its tensor memory and
+ * exits (nothing was issued, so no copy or MMA is in flight).  The outputs of
+ * such a call are undefined.  flamia_plan switches the hook off.  Synchronises
+ * `stream`.  Returns FLAMIA_ERR_INVALID_ARG for a null or too small
+ * workspace or a limit above 10 s. */
+flamia_status_t flamia_debug_set_wait_test(void* ws, size_t ws_bytes, uint64_t wait_ns, int32_t withhold_first_item,
                                            cudaStream_t stream);
 
 /* Allocation-free work-list builder (this library's own addition; the

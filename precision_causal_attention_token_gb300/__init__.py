@@ -21,7 +21,7 @@ ROLE_QKV, ROLE_DO = 0, 1
 
 EXPORTED = ("flamia_workspace_size", "flamia_plan", "flamia_quantize", "flamia_fwd", "flamia_bwd",
             "flamia_get_device_status", "flamia_clear_device_status", "flamia_status_string",
-            "flamia_debug_set_phat_dump", "flamia_plan_noalloc")
+            "flamia_debug_set_phat_dump", "flamia_debug_set_wait_test", "flamia_plan_noalloc")
 
 
 class FlamiaError(RuntimeError):
@@ -70,6 +70,8 @@ def load_library(path: str = LIB_PATH):
     L.flamia_status_string.restype, L.flamia_status_string.argtypes = ctypes.c_char_p, [i32]
     L.flamia_debug_set_phat_dump.restype = i32
     L.flamia_debug_set_phat_dump.argtypes = [vp, sz, vp, vp, vp]
+    L.flamia_debug_set_wait_test.restype = i32
+    L.flamia_debug_set_wait_test.argtypes = [vp, sz, ctypes.c_uint64, i32, vp]
     L.flamia_plan_noalloc.restype = i32
     L.flamia_plan_noalloc.argtypes = [P, vp, vp, vp, vp]
     _lib = L
@@ -154,6 +156,14 @@ def flamia_debug_set_phat_dump(ws, codes, exps, stream=None):
                                                      _stream(stream)), "flamia_debug_set_phat_dump")
 
 
+def flamia_debug_set_wait_test(ws, wait_ns: int, withhold_first_item: bool, stream=None):
+    """Test hook: shorten the attention kernels' wait limit and/or withhold each
+    CTA's first work item, so that the waits run out (see include/flamia.h)."""
+    _check(load_library().flamia_debug_set_wait_test(_ptr(ws), ws.numel() * ws.element_size(), int(wait_ns),
+                                                     int(bool(withhold_first_item)), _stream(stream)),
+           "flamia_debug_set_wait_test")
+
+
 def flamia_clear_device_status(ws, stream=None):
     _check(load_library().flamia_clear_device_status(_ptr(ws), _stream(stream)), "flamia_clear_device_status")
 
@@ -174,6 +184,7 @@ class TrainCall:
     causal: bool = True
     exact: bool = False
     deterministic: bool = False
+    causal_dq_scale: bool = False
     path: int = PATH_MXFP8
     in_dtype: int = BF16
     out_dtype: int = BF16
@@ -184,6 +195,7 @@ class TrainCall:
         dev = self.cu_seqlens.device
         self.prob = make_problem(self.T, self.H, self.Hkv, self.d, self.cu_seqlens, causal=self.causal,
                                  exact=self.exact, deterministic=self.deterministic,
+                                 causal_dq_scale=self.causal_dq_scale,
                                  softmax_scale=self.softmax_scale, path=self.path, in_dtype=self.in_dtype,
                                  out_dtype=self.out_dtype)
         nbytes = flamia_workspace_size(self.prob)

@@ -101,7 +101,12 @@ bool make_nv_map(CUtensorMap* m, const void* ptr, int d, int heads, int T) {
   return r == CUDA_SUCCESS;
 }
 
-bool operand_ok(const flamia_operand_t* o) { return o && o->codes && o->scales && aligned16(o->codes); }
+// Null members of the NVFP4 payload are allowed here (the MXFP8 path does
+// not use them); every pointer given must be 16-byte aligned.
+bool operand_ok(const flamia_operand_t* o) {
+  return o && o->codes && o->scales && aligned16(o->codes) && aligned16(o->scales) && aligned16(o->codes4) &&
+         aligned16(o->scales4) && aligned16(o->gscale4);
+}
 
 }  // namespace
 
@@ -177,7 +182,7 @@ flamia_status_t flamia_quantize(const flamia_problem_t* p, int32_t role, const v
                : FLAMIA_ERR_CUDA;
   }
   if (role == FLAMIA_ROLE_DO) {
-    if (!in[0] || !aligned16(in[0]) || !O || !aligned16(O) || !D || !operand_ok(&out[0]))
+    if (!in[0] || !aligned16(in[0]) || !O || !aligned16(O) || !D || !aligned16(D) || !operand_ok(&out[0]))
       return FLAMIA_ERR_INVALID_ARG;
     QuantBatch qb{};
     qb.n = 1;
@@ -226,7 +231,8 @@ flamia_status_t flamia_fwd(const flamia_problem_t* p, const flamia_operand_t* q,
   if (s != FLAMIA_OK) return s;
   WsLayout L;
   if ((s = check_ws(p, ws, ws_bytes, &L)) != FLAMIA_OK) return s;
-  if (!operand_ok(q) || !operand_ok(k) || !operand_ok(v) || !O || !aligned16(O) || !m || !l)
+  if (!operand_ok(q) || !operand_ok(k) || !operand_ok(v) || !O || !aligned16(O) || !m || !aligned16(m) || !l ||
+      !aligned16(l))
     return FLAMIA_ERR_INVALID_ARG;
   if (p->path == FLAMIA_PATH_NVFP4_FP8 && (!q->codes4 || !q->scales4 || !q->gscale4 || !k->codes4 ||
                                            !k->scales4 || !k->gscale4))
@@ -264,7 +270,7 @@ flamia_status_t flamia_bwd(const flamia_problem_t* p, const flamia_operand_t* q,
   WsLayout L;
   if ((s = check_ws(p, ws, ws_bytes, &L)) != FLAMIA_OK) return s;
   if (!operand_ok(q) || !operand_ok(k) || !operand_ok(v) || !operand_ok(dO) || !D || !m || !l || !dQ || !dK ||
-      !dV || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
+      !dV || !aligned16(D) || !aligned16(m) || !aligned16(l) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
     return FLAMIA_ERR_INVALID_ARG;
   if (p->path == FLAMIA_PATH_NVFP4_FP8 && (!q->gscale4 || !k->gscale4)) return FLAMIA_ERR_INVALID_ARG;
   AttnParams a;
@@ -311,6 +317,24 @@ flamia_status_t flamia_debug_set_phat_dump(void* ws, size_t ws_bytes, void* code
   ptrs[1] = exps;
   uint8_t* dst = static_cast<uint8_t*>(ws) + offsetof(WsHeader, dbg_phat);
   if (cudaMemcpyAsync(dst, ptrs, sizeof(ptrs), cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return FLAMIA_ERR_CUDA;
+  return FLAMIA_OK;
+}
+
+flamia_status_t flamia_debug_set_wait_test(void* ws, size_t ws_bytes, uint64_t wait_ns, int32_t withhold_first_item,
+                                           cudaStream_t stream) {
+  if (!ws || ws_bytes < sizeof(WsHeader) || wait_ns > 10000000000ull) return FLAMIA_ERR_INVALID_ARG;
+  static thread_local struct {
+    uint32_t withhold, pad;
+    uint64_t wait_ns;
+  } v;
+  static_assert(offsetof(WsHeader, dbg_wait_ns) == offsetof(WsHeader, dbg_withhold) + 8, "hook layout");
+  v.withhold = withhold_first_item ? 1u : 0u;
+  v.pad = 0u;
+  v.wait_ns = wait_ns;
+  uint8_t* dst = static_cast<uint8_t*>(ws) + offsetof(WsHeader, dbg_withhold);
+  if (cudaMemcpyAsync(dst, &v, sizeof(v), cudaMemcpyHostToDevice, stream) != cudaSuccess ||
       cudaStreamSynchronize(stream) != cudaSuccess)
     return FLAMIA_ERR_CUDA;
   return FLAMIA_OK;

@@ -21,8 +21,10 @@
 //     written to TMEM (in X0, free once S is read) as MMA scale factors
 //   dV += P~^T dO^ (A = P~ MN-major, B = dO MN-major)   block-scaled
 //   dK += dS^T Q^  (A = dS MN-major, B = Q MN-major)    block-scaled
-//   dQ  = dS K^    -> TMEM X1 (A = dS K-major, B = K MN-major), added to
-//     an fp32 buffer with vector reductions by the compute warps.
+//   dQ  = dS K^    -> TMEM X1 in two 64-column halves (A = dS K-major,
+//     B = K MN-major); the drain warps stage each half in shared memory and
+//     the reducer warp adds it into the fp32 dQ buffer with bulk tensor
+//     reduce-adds (the addition happens in L2).
 // Every per-token factor that varies along a contraction (2^eQ, 2^eK, 2^edO,
 // 2^-eV) is folded into the other operand before its block quantization, so
 // all B operands run with unit scale factors.
@@ -32,7 +34,7 @@
 namespace flamia {
 
 // Compute warps 0-7 (two per TMEM lane quarter: warp w owns query rows
-// 32(w%4)..+31 and key blocks 2(w/4), 2(w/4)+1), producer warp 8, MMA warp 9.
+// 32(w%4)..+31 and key blocks 2(w/4), 2(w/4)+1).
 // Warpgroups: 0-1 compute (warps 0-7), 2 dQ drain (warps 8-11, one per TMEM
 // lane quarter), 3 producer (12), MMA issuer (13), dQ reducer (14), idle (15).
 // Registers are rebalanced per warpgroup after launch (512 x 128 in total):

@@ -25,7 +25,10 @@ struct WsHeader {
   uint32_t pad0;
   uint8_t* dbg_phat;       // test hook: P^ codes [H][T][T] (null: off)
   int32_t* dbg_eb;         // test hook: P^ block exponents [H][T][T] at each block's first key
-  uint32_t pad[52];
+  uint32_t dbg_withhold;   // test hook: each CTA's producer withholds its first work item
+  uint32_t pad1;
+  uint64_t dbg_wait_ns;    // test hook: bounded-wait limit in ns (0: the default limit)
+  uint32_t pad[48];
 };
 static_assert(sizeof(WsHeader) == 256, "header");
 
@@ -263,10 +266,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   if (mbar_test_wait(bar, parity)) return true;  // already complete: no suspend
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t test_limit = hdr->dbg_wait_ns;  // a test may shorten the limit
+  const uint64_t limit = test_limit ? test_limit : kWaitLimitNs;
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit) {
       *abort_flag = 1;
       report(hdr, FLAMIA_ERR_TIMEOUT, where);
       return false;
@@ -309,6 +314,9 @@ __device__ __forceinline__ int item_publish(ItemRing& r, uint32_t n, uint32_t* c
                                             volatile int* abort_flag, WsHeader* hdr, uint32_t where, bool& ok) {
   const int s = (int)(n % kItemRing);
   if (!(ok = mbar_wait_warp(&r.empty[s], ((n / kItemRing) & 1) ^ 1, abort_flag, hdr, where))) return -1;
+  // test hook: the first item is never published, so every consumer's wait
+  // on it runs out; nothing has been issued yet, so the CTA exits cleanly
+  if (n == 0 && *reinterpret_cast<volatile uint32_t*>(&hdr->dbg_withhold) != 0u) return -1;
   int w = 0;
   if (lane == 0) {
     w = (int)atomicAdd(counter, 1u);

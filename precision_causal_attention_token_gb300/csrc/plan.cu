@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(1024) plan_prefix_kernel(const int32_t* __rest
     hdr->status_where = 0;
     hdr->dbg_phat = nullptr;  // test hooks off unless set after the plan
     hdr->dbg_eb = nullptr;
+    hdr->dbg_withhold = 0u;
+    hdr->dbg_wait_ns = 0ull;
   }
   __syncthreads();
   for (int base = 0; base < n_seq; base += 1024) {
@@ -88,12 +90,16 @@ __device__ __forceinline__ int doc_of_tile(const int32_t* __restrict__ tile_pref
 }
 
 // keys[0 .. sort_n) forward list, keys[sort_n .. 2 sort_n) backward list.
+// A real item's cost is at least 1, so its key's high word is at most
+// 0xFFFFFFFE; a padding slot g gets the high word 0xFFFFFFFF and its own
+// index below, so padding keys are unique too and sort after every real key
+// in slot order.  (Equal padding keys would collide in the merge passes.)
 __global__ void plan_keys_kernel(const int32_t* __restrict__ tile_prefix, int n_seq, int causal, int sort_n,
                                  const WsHeader* hdr, uint64_t* keys) {
   const int g = blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= sort_n) return;
   const int n_items = hdr->n_items;
-  uint64_t kf = ~0ull, kb = ~0ull;
+  uint64_t kf = (0xFFFFFFFFull << 32) | (uint32_t)g, kb = kf;
   if (g < n_items) {
     const int doc = doc_of_tile(tile_prefix, n_seq, g);
     const int tile = g - __ldg(tile_prefix + doc);
@@ -108,9 +114,10 @@ __global__ void plan_keys_kernel(const int32_t* __restrict__ tile_prefix, int n_
 }
 
 // Bitonic sort of kSortBlock keys per CTA (ascending).  Keys past the real
-// items are padding (all bits set), so a block whose real keys fit in the
-// first P = 2^k slots only runs the network up to size P: the padding above
-// stays in place and the block ends sorted.
+// items are padding, larger than every real key and ascending with the slot,
+// so a block whose real keys fit in the first P = 2^k slots only runs the
+// network up to size P: the padding above stays in place and the block ends
+// sorted.
 __global__ void __launch_bounds__(1024) block_sort_kernel(uint64_t* keys, int sort_n, const WsHeader* hdr) {
   __shared__ uint64_t s[kSortBlock];
   uint64_t* k = keys + (size_t)blockIdx.x * kSortBlock;
@@ -140,7 +147,10 @@ __global__ void __launch_bounds__(1024) block_sort_kernel(uint64_t* keys, int so
 
 // One merge pass: sorted runs of `width` keys are merged pairwise.  Each key
 // finds its output slot as (own rank) + (number of smaller keys in the
-// sibling run), by binary search; keys are unique.  Two lists of sort_n keys.
+// sibling run), by binary search.  Keys are unique (padding included), so the
+// slots of a pass are a permutation: every destination word is written, and
+// no pass reads a word that an earlier pass did not write.  Two lists of
+// sort_n keys.
 __global__ void merge_pass_kernel(const uint64_t* __restrict__ src, uint64_t* __restrict__ dst, int sort_n,
                                   int width) {
   const int gi = blockIdx.x * blockDim.x + threadIdx.x;
@@ -263,9 +273,10 @@ extern "C" flamia_status_t flamia_plan_noalloc(const flamia_problem_t* p, int2* 
   NoAllocScratch* sc = noalloc_scratch_for_current_device();
   if (sc == nullptr) return FLAMIA_ERR_CUDA;
   const int n = ((max_items + kSortBlock - 1) / kSortBlock) * kSortBlock;
-  // every scratch word a kernel reads is written earlier in this sequence
-  // (the prefix kernel writes the header and both tables, the key kernel all
-  // 2n keys), so nothing needs clearing between calls
+  // every scratch word a kernel reads is written earlier in this sequence:
+  // the prefix kernel writes the header and both tables, the key kernel all
+  // 2n keys (unique, padding included), and each merge pass writes a
+  // permutation of its source, so nothing needs clearing between calls
   plan_prefix_kernel<<<1, 1024, 0, stream>>>(p->cu_seqlens, p->n_seq, p->T, sc->tile_prefix, sc->blk_prefix,
                                             &sc->hdr);
   plan_keys_kernel<<<(n + 255) / 256, 256, 0, stream>>>(sc->tile_prefix, p->n_seq, p->causal, n, &sc->hdr,

@@ -20,13 +20,13 @@ def to_dev(a: np.ndarray, dtype: str, dev="cuda"):
 
 
 def run_gpu(w, *, causal=True, exact=False, path=fl.PATH_MXFP8, deterministic=False, inputs=None,
-            backward=True):
+            backward=True, causal_dq_scale=False):
     dev = torch.device("cuda:0")
     q, k, v, do = inputs if inputs is not None else (w.tensor(n) for n in ("q", "k", "v", "do"))
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
     dt = fl.BF16 if w.dtype == "bf16" else fl.F32
     tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu, causal=causal, exact=exact, path=path, in_dtype=dt,
-                      out_dtype=dt, deterministic=deterministic)
+                      out_dtype=dt, deterministic=deterministic, causal_dq_scale=causal_dq_scale)
     tc.plan()
     tc.forward(to_dev(q, w.dtype), to_dev(k, w.dtype), to_dev(v, w.dtype))
     if backward:
@@ -48,19 +48,28 @@ def np_of(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
+# Outputs whose oracle value cancels down to the rounding of O before
+# D = <dO^, O> (near one-hot softmax rows, from x20 outlier channels in Q and
+# K) get, on top of ROW_TOL, NOISE_K times the row's largest oracle-only
+# sensitivity to that rounding.  Why 4: the oracle's noise is the change
+# between O rounded to bf16 and O kept exact, at most half a bf16 ulp per
+# element; the GPU rounds an fp32 O whose last bits differ from the oracle's
+# fp64 O, so an element of its stored O can sit one whole ulp from the
+# oracle's stored O (twice the per-element deviation), and the row sum
+# D_i = sum_k dO_ik O_ik can add those deviations with the same sign where the
+# oracle's half-ulp errors partly cancel (another factor of two).
+NOISE_K = 4.0
+
+
 def compare(name, got, want, row_tol=ROW_TOL, cos_tol=COS_TOL, rows=None, noise=None):
     """Per-row (last axis) max-error bound and whole-tensor cosine.
 
     noise: the oracle's own change in this output when only the rounding of
     O before D = <dO, O> changes (O stored in the output dtype vs kept in
-    fp64), same shape as `want`.  Given for workloads with x20 outlier
-    channels in Q and K, where the softmax is nearly one-hot: there
-    dS = P (dP - D) cancels down to O's rounding, any two implementations
-    whose O differs in the last bits disagree row by row, and the oracle
-    itself moves dQ by up to 35x a row's max-abs.  For such outputs the
-    comparison is the cosine, required to stay within four times the
-    oracle's own cosine deficit, plus a bound of 10% of the tensor's
-    max-abs on every element.  All of it comes from the oracle."""
+    fp64), same shape as `want`.  When given, each row may in addition differ
+    by NOISE_K times that row's largest noise, and the cosine bound becomes
+    the oracle's own cosine (want - noise against want) with its deficit
+    multiplied by NOISE_K, if that is lower.  All of it comes from the oracle."""
     g = np_of(got) if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
     r = np.asarray(want, np.float64)
     nz = None if noise is None else np.asarray(noise, np.float64)
@@ -70,22 +79,23 @@ def compare(name, got, want, row_tol=ROW_TOL, cos_tol=COS_TOL, rows=None, noise=
     assert g.shape == r.shape, (name, g.shape, r.shape)
     assert np.isfinite(g).all(), f"{name}: non-finite values"
     err = np.abs(g - r)
+    rowmax = np.abs(r).max(axis=-1, keepdims=True)
+    floor = 1e-6 * max(np.abs(r).max(), 1e-30)
+    allow = row_tol * np.maximum(rowmax, floor)
+    if nz is not None and np.abs(nz).max() > 0:
+        allow = allow + NOISE_K * np.abs(nz).max(axis=-1, keepdims=True)
+        cos_tol = min(cos_tol, 1.0 - NOISE_K * (1.0 - cosine(r - nz, r)))
+    ratio = err / allow
+    worst = float(ratio.max()) if err.size else 0.0
     gg, rr = g.ravel(), r.ravel()
     denom = np.sqrt((gg @ gg) * (rr @ rr))
     cos = float(gg @ rr / denom) if denom > 0 else 1.0
-    if nz is not None and np.abs(nz).max() > 0:
-        own = cosine(r - nz, r)
-        tol = min(cos_tol, 1.0 - 4.0 * (1.0 - own))
-        worst = float(err.max() / max(np.abs(r).max(), 1e-30))
-        print(f"{name}: cosine {cos:.6f} (oracle's own {own:.6f}), max |err| / max |ref| {worst:.3e}")
-        assert cos >= tol, f"{name}: cosine {cos:.7f} < {tol:.7f}"
-        assert worst <= 0.1, f"{name}: max |err| = {worst:.3e} of the tensor's max-abs"
-        return worst, cos
-    rowmax = np.abs(r).max(axis=-1, keepdims=True)
-    floor = 1e-6 * max(np.abs(r).max(), 1e-30)
-    worst = float((err / np.maximum(rowmax, floor)).max()) if err.size else 0.0
-    assert worst <= row_tol, f"{name}: max |err| / row max-abs = {worst:.3e} > {row_tol}"
-    assert cos >= cos_tol, f"{name}: cosine {cos:.7f} < {cos_tol}"
+    if worst > 1.0:
+        flat = np.argsort(ratio.reshape(-1, ratio.shape[-1]).max(axis=-1))[::-1][:5]
+        print(f"{name}: worst rows (flattened index, err / allowance):",
+              [(int(i), float(ratio.reshape(-1, ratio.shape[-1])[i].max())) for i in flat])
+    assert worst <= 1.0, f"{name}: max |err| exceeds the per-row allowance by {worst:.3f}x"
+    assert cos >= cos_tol, f"{name}: cosine {cos:.7f} < {cos_tol:.7f}"
     return worst, cos
 
 

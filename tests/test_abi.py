@@ -89,6 +89,32 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.flamia_get_device_status(None, None) == fl.ERR_INVALID_ARG
 
 
+def test_misaligned_pointers_rejected_before_launch(lib):
+    """Every device pointer must be 16-byte aligned (cu_seqlens 4-byte): the
+    host rejects a misaligned scale vector, D, m or l without touching the
+    device (the pointers below are never dereferenced)."""
+    p, _ = _prob()
+    big = 1 << 40
+    ws = 1 << 20
+    good = lambda: fl.Operand(0x10000, 0x20000, None, None, None)
+    for field in ("codes", "scales"):
+        bad = good()
+        setattr(bad, field, getattr(bad, field) + 1)
+        assert lib.flamia_fwd(p, bad, good(), good(), 0x30000, 0x40000, 0x50000, ws, big, None) == fl.ERR_INVALID_ARG
+    for m, l in ((0x40004, 0x50000), (0x40000, 0x50008)):
+        assert lib.flamia_fwd(p, good(), good(), good(), 0x30000, m, l, ws, big, None) == fl.ERR_INVALID_ARG
+    ops = [good() for _ in range(4)]
+    for D, m, l in ((0x60004, 0x40000, 0x50000), (0x60000, 0x40008, 0x50000), (0x60000, 0x40000, 0x5000c)):
+        st = lib.flamia_bwd(p, ops[0], ops[1], ops[2], ops[3], D, m, l, 0x70000, 0x80000, 0x90000, ws, big, None)
+        assert st == fl.ERR_INVALID_ARG
+
+
+def test_wait_test_hook_rejects_bad_arguments(lib):
+    assert lib.flamia_debug_set_wait_test(None, 1 << 20, 1000, 1, None) == fl.ERR_INVALID_ARG
+    assert lib.flamia_debug_set_wait_test(1 << 20, 16, 1000, 1, None) == fl.ERR_INVALID_ARG
+    assert lib.flamia_debug_set_wait_test(1 << 20, 1 << 20, 20_000_000_000, 1, None) == fl.ERR_INVALID_ARG
+
+
 def test_binding_raises_without_library(tmp_path):
     import importlib
     mod = importlib.import_module("precision_causal_attention_token_gb300")

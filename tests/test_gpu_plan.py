@@ -77,6 +77,35 @@ def test_worklist_matches_host_sort(wl, causal):
     assert fl.flamia_get_device_status(ws) == fl.OK
 
 
+@pytest.mark.parametrize("fill", [0x00, 0xA5])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("n_docs", [3837, 9000])
+def test_worklist_multi_pass_with_padding(n_docs, causal, fill):
+    """Several merge passes (sort_n = 8192 and 18432) over lists that are
+    mostly padding: ceil(T/128) + n_seq bounds the item count at twice the real
+    items.  The workspace starts as all 0x00 or all 0xA5 bytes, so a pass that
+    left a slot unwritten would hand stale words to the next pass."""
+    lens = [128] * n_docs
+    T = int(sum(lens))
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32), device="cuda")
+    prob = fl.make_problem(T, 1, 1, 128, cu, causal=causal)
+    ws = torch.full((fl.flamia_workspace_size(prob),), fill, dtype=torch.uint8, device="cuda")
+
+    class _TC:
+        pass
+
+    tc = _TC()
+    tc.ws = ws
+    fl.flamia_plan(prob, ws)
+    torch.cuda.synchronize()
+    n_items, _, f, b, _, _ = _read_lists(tc, T, len(lens))
+    hf, hb = _host_lists(lens, causal)
+    assert n_items == len(hf) == n_docs
+    assert [tuple(x) for x in f] == hf
+    assert [tuple(x) for x in b] == hb
+    assert fl.flamia_get_device_status(ws) == fl.OK
+
+
 def test_bad_seqlens_reported_on_device():
     cu = torch.tensor([0, 50, 40, 100], dtype=torch.int32, device="cuda")  # decreasing
     prob = fl.make_problem(100, 1, 1, 128, cu)

@@ -36,13 +36,24 @@ def _lists_from_workspace(ws, T, n_seq):
     return n, f, b
 
 
-def _check(lens, causal):
+def _host_lists(lens, causal):
+    """The longest-first order by definition: cost descending, ties in item order."""
+    items = [(d, t) for d, l in enumerate(lens) for t in range((l + 127) // 128)]
+    nt = {d: (l + 127) // 128 for d, l in enumerate(lens)}
+    fc = lambda it: (it[1] + 1) if causal else nt[it[0]]
+    bc = lambda it: (nt[it[0]] - it[1]) if causal else nt[it[0]]
+    f = sorted(range(len(items)), key=lambda i: (-fc(items[i]), i))
+    b = sorted(range(len(items)), key=lambda i: (-bc(items[i]), i))
+    return np.array([items[i] for i in f], np.int32), np.array([items[i] for i in b], np.int32)
+
+
+def _check(lens, causal, heads=(4, 2)):
     import __graft_entry__
     __graft_entry__.build()
     T = int(sum(lens))
     cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32), device="cuda")
-    prob = fl.make_problem(T, 4, 2, 128, cu, causal=causal)
-    ws = torch.zeros(fl.flamia_workspace_size(prob), dtype=torch.uint8, device="cuda")
+    prob = fl.make_problem(T, heads[0], heads[1], 128, cu, causal=causal)
+    ws = torch.full((fl.flamia_workspace_size(prob),), 0xA5, dtype=torch.uint8, device="cuda")
     fl.flamia_plan(prob, ws)
     max_items = (T + 127) // 128 + len(lens)
     fwd = torch.full((max_items, 2), -1, dtype=torch.int32, device="cuda")
@@ -54,13 +65,25 @@ def _check(lens, causal):
     assert int(n.item()) == n_ref > 0
     assert np.array_equal(fwd[:n_ref].cpu().numpy(), f_ref)
     assert np.array_equal(bwd[:n_ref].cpu().numpy(), b_ref)
+    hf, hb = _host_lists(lens, causal)
+    assert np.array_equal(f_ref, hf) and np.array_equal(b_ref, hb)
 
 
 def test_noalloc_plan_matches_workspace_plan_twice():
-    # two calls in a row, different problems: the shared scratch keeps no stale state
+    # calls in a row, different problems: the shared scratch keeps no stale state
     _check(synth.workload(3).seqlens, causal=True)
     _check([1, 300, 0, 129, 128, 4000, 31] + [1] * 2000, causal=False)
     _check(synth.workload(3).seqlens, causal=True)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_noalloc_plan_multi_pass_after_larger_problem(causal):
+    # several merge passes over lists that are mostly padding, right after a
+    # larger problem: the shared scratch then holds that problem's keys, some
+    # smaller than this problem's padding keys
+    _check([128] * 9000, causal=causal, heads=(1, 1))
+    _check([128] * 3837, causal=causal, heads=(1, 1))
+    _check([128] * 3837, causal=not causal, heads=(1, 1))
 
 
 def test_noalloc_plan_rejects_oversized_problems():
