@@ -45,6 +45,12 @@ def _args():
     ap.add_argument("--ref-sample-tokens", type=int, default=1024,
                     help="causal prefix length per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-procs", type=int, default=min(16, os.cpu_count() or 1),
+                    help="processes of the all-core oracle sample (one single-threaded oracle per head)")
+    ap.add_argument("--cpu-sample-tokens-all", type=int, default=1024,
+                    help="causal prefix length of each process of the all-core oracle sample")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the packed / long-GQA workloads and the option overheads")
     ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5],
                     help="2: batched 4x4096 (the benchmark workload); 3: packed 8x16384 log-normal documents; "
                          "4: mixed NVFP4/FP8 path, packed 4x32768; 5: long GQA 2x65536, H=32, Hkv=8")
@@ -200,6 +206,59 @@ def _oracle_sample(w, n_tokens: int):
     return flops, dt
 
 
+def cpu_info() -> dict:
+    """Host core count and CPU model (for the CPU-baseline record)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.split(":")[0].strip() in ("Model name", "Model"):
+                model = ln.split(":", 1)[1].strip()
+                if not model.isdigit():
+                    break
+    except Exception:
+        pass
+    return {"nproc": os.cpu_count(), "cpu_model": model}
+
+
+def _oracle_worker(args):
+    """One single-threaded oracle instance on the causal prefix of document 0
+    for one head (a process of its own; inputs drawn from the same seeded
+    generator as the workload)."""
+    head, n_tokens, seed = args
+    import synth
+    import oracle
+    w = synth.workload(2)
+    nh = w.H
+    # the head's slice of the first n_tokens tokens: draws are indexed by
+    # (token, head, channel), so the slice is generated without the rest
+    def draw(stream):
+        x = np.empty((n_tokens, 1, w.d), np.float32)
+        for t in range(n_tokens):
+            x[t, 0] = synth.normal(w.seed, stream, w.d, start=(t * nh + head) * w.d).astype(np.float32)
+        return synth.round_to_bf16(x)
+    q, k, v, do = (draw(s) for s in (synth.STREAM_Q, synth.STREAM_K, synth.STREAM_V, synth.STREAM_DO))
+    cu = np.array([0, n_tokens], np.int32)
+    t0 = time.perf_counter()
+    oracle.train_call(q, k, v, do, cu, out_dtype="bf16")
+    return time.perf_counter() - t0
+
+
+def oracle_all_cores(n_tokens: int, procs: int):
+    """Wall time of `procs` independent single-threaded oracle instances (one
+    per head, spawned processes), and the FLOPs they cover together."""
+    import multiprocessing as mp
+    import oracle
+    oracle.build()
+    ctx = mp.get_context("spawn")
+    t0 = time.perf_counter()
+    with ctx.Pool(procs) as pool:
+        per = pool.map(_oracle_worker, [(h % 16, n_tokens, 0) for h in range(procs)])
+    wall = time.perf_counter() - t0
+    flops = 14.0 * 128 * procs * n_tokens * (n_tokens + 1) / 2
+    return flops, wall, max(per)
+
+
 def run_reference(a):
     rank, world, _ = _dist()
     if rank != 0:
@@ -228,12 +287,130 @@ def run_reference(a):
     return 0
 
 
+def _step_fn(fl, tc, inputs):
+    """One training call (plan, quantize Q/K/V, forward, quantize dO + D,
+    backward) on `stream`, with optional events between the phases."""
+    q, k, v, do = inputs
+
+    def step(evs=None, stream=None):
+        import torch
+        stream = stream or torch.cuda.current_stream()
+        rec = (lambda i: evs[i].record(stream)) if evs else (lambda i: None)
+        rec(0)
+        tc.plan(stream)
+        rec(1)
+        fl.flamia_quantize(tc.prob, fl.ROLE_QKV, [q, k, v], None, [tc.opq, tc.opk, tc.opv], None, tc.ws, stream)
+        rec(2)
+        fl.flamia_fwd(tc.prob, tc.opq, tc.opk, tc.opv, tc.O, tc.m, tc.l, tc.ws, stream)
+        rec(3)
+        fl.flamia_quantize(tc.prob, fl.ROLE_DO, [do], tc.O, [tc.opdo], tc.D, tc.ws, stream)
+        rec(4)
+        fl.flamia_bwd(tc.prob, tc.opq, tc.opk, tc.opv, tc.opdo, tc.D, tc.m, tc.l, tc.dQ, tc.dK, tc.dV, tc.ws,
+                      stream)
+        rec(5)
+
+    return step
+
+
+def _phases(step, steps, stream):
+    """Mean ms of each phase over `steps` eager calls timed with events."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    for i in range(steps):
+        step(evs[i], stream)
+    torch.cuda.synchronize()
+    ph = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in evs])
+    return ph.mean(axis=0), float(ph.sum(axis=1).mean())
+
+
+def _graph_ms(step, steps, stream):
+    """ms per call of the training call captured once as a CUDA graph (the API
+    neither allocates nor synchronises) and replayed `steps` times."""
+    import torch
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    graph.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return graph, t0.elapsed_time(t1) / steps
+
+
+def _device_inputs(w, dev):
+    """Seeded normal Q/K/V/dO drawn on the device (the secondary workloads,
+    timed only), with the workload's outlier channels x20 in Q and K."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    out = []
+    for name, heads in (("q", w.H), ("k", w.Hkv), ("v", w.Hkv), ("do", w.H)):
+        x = torch.randn(w.T, heads, w.d, generator=g, device=dev, dtype=torch.float32)
+        if w.outlier_channels and name in ("q", "k"):
+            for h, chans in enumerate(w.outliers()[:heads] if name == "q" else w.outliers_kv()):
+                x[:, h, chans] *= 20.0
+        out.append(x.to(torch.bfloat16))
+    return out
+
+
+def _secondary(fl, idx, dev, stream, steps):
+    """Step time and TFLOP/s of another workload of the pages' kind."""
+    import torch
+    w = _workload(4, idx)
+    inputs = _device_inputs(w, dev)
+    cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
+    tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu)
+    step = _step_fn(fl, tc, inputs)
+    for _ in range(2):
+        step()
+    (pl, qk, fw, qd, bw), eager = _phases(step, 2, stream)
+    graph, ms = _graph_ms(step, steps, stream)
+    st = fl.flamia_get_device_status(tc.ws)
+    if st != fl.OK:
+        raise RuntimeError(f"workload {idx}: {fl.status_string(st)}")
+    pairs = w.causal_pairs
+    res = {"workload": w.name, "ms_per_step": ms, "tflops": w.flops() / (ms * 1e-3) / 1e12,
+           "fwd_tflops": 4.0 * w.d * w.H * pairs / (fw * 1e-3) / 1e12,
+           "bwd_tflops": 10.0 * w.d * w.H * pairs / (bw * 1e-3) / 1e12,
+           "phase_ms": {"quantize_qkv": qk, "fwd": fw, "quantize_do": qd, "bwd+dq_convert": bw}}
+    del graph, tc, inputs
+    torch.cuda.empty_cache()
+    return res
+
+
+def _option_overheads(fl, w, inputs, dev, stream, base_bwd_ms, steps):
+    """Backward time of the deterministic and the exact options on the same
+    workload, relative to the default backward."""
+    import torch
+    cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
+    out = {}
+    for name, kw in (("deterministic", {"deterministic": True}), ("exact", {"exact": True})):
+        tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu, **kw)
+        step = _step_fn(fl, tc, inputs)
+        for _ in range(2):
+            step()
+        (pl, qk, fw, qd, bw), _ = _phases(step, steps, stream)
+        out[name] = {"bwd_ms": bw, "fwd_ms": fw, "bwd_overhead": bw / base_bwd_ms - 1.0}
+        del tc
+    return out
+
+
 def run_ours(a):
     import torch
     import precision_causal_attention_token_gb300 as fl
     import __graft_entry__
 
     rank, world, local = _dist()
+    cpu_all = None
+    if rank == 0 and not a.no_cpu_baseline and a.cpu_procs > 0:
+        # the all-core oracle runs in spawned processes before this process
+        # touches the GPU
+        f_all, wall_all, slowest = oracle_all_cores(a.cpu_sample_tokens_all, a.cpu_procs)
+        cpu_all = (f_all, wall_all, slowest)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
@@ -250,29 +427,7 @@ def run_ours(a):
     pairs = w.causal_pairs
     fwd_flops, bwd_flops = 4.0 * w.d * w.H * pairs, 10.0 * w.d * w.H * pairs
     stream = torch.cuda.current_stream()
-
-    ev = lambda: torch.cuda.Event(enable_timing=True)
-
-    def step(evs=None, stream=None):
-        stream = stream or torch.cuda.current_stream()
-        if evs:
-            evs[0].record(stream)
-        tc.plan(stream)
-        if evs:
-            evs[1].record(stream)
-        fl.flamia_quantize(tc.prob, fl.ROLE_QKV, [q, k, v], None, [tc.opq, tc.opk, tc.opv], None, tc.ws, stream)
-        if evs:
-            evs[2].record(stream)
-        fl.flamia_fwd(tc.prob, tc.opq, tc.opk, tc.opv, tc.O, tc.m, tc.l, tc.ws, stream)
-        if evs:
-            evs[3].record(stream)
-        fl.flamia_quantize(tc.prob, fl.ROLE_DO, [do], tc.O, [tc.opdo], tc.D, tc.ws, stream)
-        if evs:
-            evs[4].record(stream)
-        fl.flamia_bwd(tc.prob, tc.opq, tc.opk, tc.opv, tc.opdo, tc.D, tc.m, tc.l, tc.dQ, tc.dK, tc.dV, tc.ws,
-                      stream)
-        if evs:
-            evs[5].record(stream)
+    step = _step_fn(fl, tc, (q, k, v, do))
 
     for _ in range(max(3, a.warmup)):
         step()
@@ -281,17 +436,12 @@ def run_ours(a):
     if st != fl.OK:
         raise RuntimeError(f"device status after warm-up: {fl.status_string(st)}")
 
-    # per-phase breakdown (and the backward kernel's time for the roofline):
+    # per-phase breakdown (and the backward's time for the roofline):
     # launched eagerly with events between the phases
-    evs = [[ev() for _ in range(6)] for _ in range(a.steps)]
-    for i in range(a.steps):
-        step(evs[i], stream)
-    torch.cuda.synchronize()
-    ph = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in evs])  # ms
-    plan_ms, quant_ms, fwd_ms, dquant_ms, bwd_ms = ph.mean(axis=0)
+    (plan_ms, quant_ms, fwd_ms, dquant_ms, bwd_ms), eager_ms = _phases(step, a.steps, stream)
 
-    # timed region: the training call captured once as a CUDA graph (the API
-    # neither allocates nor synchronises) and replayed K times
+    # timed region: the training call captured once as a CUDA graph and
+    # replayed K times, bracketed by a barrier and a synchronize
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         step()
@@ -304,7 +454,7 @@ def run_ours(a):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    t_start, t_end = ev(), ev()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(a.steps):
         graph.replay()
@@ -338,7 +488,7 @@ def run_ours(a):
 
     e2e_step()
     torch.cuda.synchronize()
-    e0, e1 = ev(), ev()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
         e2e_step()
@@ -347,53 +497,83 @@ def run_ours(a):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
     e2e_val = job_rate(flops, world, e2e_ms)
 
+    # secondary measurements (rank 0 of the default workload only): the packed
+    # and long-GQA workloads, and the cost of the deterministic and exact options
+    extra = {}
+    if rank == 0 and a.workload == 2 and a.rows == 4 and not a.no_secondary:
+        del graph
+        extra["option_overheads"] = _option_overheads(fl, w, (q, k, v, do), dev, stream, bwd_ms, max(3, a.steps // 4))
+        del tc
+        torch.cuda.empty_cache()
+        extra["workloads"] = {f"{i}": _secondary(fl, i, dev, stream, max(3, a.steps // 4)) for i in (3, 5)}
+
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return 0
     peaks, kind = _peaks()
-    fp8_sustained = 2.0 * float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    fp8_burst = 2.0 * float(peaks["bf16_tflops"])
+    fp8_sustained = 2.0 * float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
     bwd_tflops = bwd_flops / (bwd_ms * 1e-3) / 1e12
     # the quantizers' algorithmic bytes per token-head: Q/K/V read 2d, write
     # d codes + 1 scale byte; dO reads dO and O (4d), writes d + 1 + 4 (D)
     hbm = float(peaks["hbm_gbs"])
     qkv_gbs = float(w.T) * (w.H + 2 * w.Hkv) * (3 * w.d + 1) / (quant_ms * 1e-3) / 1e9
     do_gbs = float(w.T) * w.H * (5 * w.d + 5) / (dquant_ms * 1e-3) / 1e9
-    n_items = int(sum((l + 127) // 128 for l in w.seqlens))
     launches_per_step = 4 + 1 + 1 + 1 + 2  # plan(4) quantize(Q,K,V in one) fwd dO-quantize bwd dq-convert
     cpu = None
     if not a.no_cpu_baseline:
         import oracle
         oracle.build()
         f, dt = _oracle_sample(w, a.cpu_sample_tokens)
+        info = cpu_info()
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                "sample": f"causal prefix of {a.cpu_sample_tokens} tokens of document 0, head 0 "
-                         f"(single-threaded fp64 oracle, full quantized call), {dt:.1f} s"}
+                         f"(single-threaded fp64 oracle, full quantized call), {dt:.1f} s",
+               "nproc": info["nproc"], "cpu_model": info["cpu_model"]}
+        if cpu_all is not None:
+            f_all, wall_all, slowest = cpu_all
+            cpu["all_cores"] = {"value": f_all / wall_all / 1e12, "unit": "TFLOP/s", "cores": a.cpu_procs,
+                                "sample": f"{a.cpu_procs} independent single-threaded oracle processes, one per "
+                                          f"head, each on the causal prefix of {a.cpu_sample_tokens_all} tokens "
+                                          f"of document 0; wall {wall_all:.1f} s (slowest {slowest:.1f} s)"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": ("e2m1/e4m3 scores (NVFP4), e4m3 elsewhere, fp32 accumulate" if mixed
                   else "e4m3 (MXFP8 operands, fp32 accumulate)"), "data": "synthetic",
-        "config": {"workload": WORKLOAD.format(rows=a.rows) if a.workload == 2 else w.name, "tokens": w.T, "heads": w.H, "head_dim": w.d, "documents": len(w.seqlens),
+        "config": {"workload": WORKLOAD.format(rows=a.rows) if a.workload == 2 else w.name, "tokens": w.T,
+                   "heads": w.H, "head_dim": w.d, "documents": len(w.seqlens),
                    "flops_per_step": flops, "l2": "inputs larger than L2 (256 MiB of bf16 Q/K/V/dO)",
-                   "fraction_of_fp8_peak": value / world / fp8_sustained,
+                   "fraction_of_fp8_peak": value / world / fp8_burst,
+                   "fraction_of_fp8_peak_sustained": value / world / fp8_sustained,
                    "timing": "CUDA graph of one training call, replayed; phases from an eager pass with events",
                    "phase_ms": {"plan": plan_ms, "quantize_qkv": quant_ms, "fwd": fwd_ms, "quantize_do": dquant_ms,
-                                "bwd+dq_convert": bwd_ms, "eager_step": float(ph.sum(axis=1).mean())},
+                                "bwd+dq_convert": bwd_ms, "eager_step": eager_ms},
                    "quantizer_hbm": None if mixed else {
                        "qkv_gbs": qkv_gbs, "do_gbs": do_gbs, "peak_gbs": hbm,
                        "frac_qkv": qkv_gbs / hbm, "frac_do": do_gbs / hbm,
                        "peak_source": f"{kind} hbm_gbs (copy bandwidth)"},
-                   "fwd_tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": bwd_tflops},
-        "roofline": {"bound": "tensor", "kernel": "bwd_kernel (+dq convert)", "achieved": bwd_tflops,
-                     "peak": fp8_sustained, "unit": "TFLOP/s", "frac": bwd_tflops / fp8_sustained,
+                   "fwd_tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": bwd_tflops,
+                   "fwd_frac_of_fp8_burst": fwd_flops / (fwd_ms * 1e-3) / 1e12 / fp8_burst},
+        "roofline": {"bound": "tensor", "kernel": "bwd_kernel (+dq convert, timed together)", "achieved": bwd_tflops,
+                     "peak": fp8_burst, "unit": "TFLOP/s", "frac": bwd_tflops / fp8_burst,
+                     "frac_of_sustained": bwd_tflops / fp8_sustained,
                      "traffic": _profiled_traffic("bwd_kernel"),
-                     "peak_source": f"{kind}: 2 x bf16_tflops_sustained (dense FP8 = 2x bf16)"},
+                     "peak_source": f"{kind}: 2 x bf16_tflops (burst; dense FP8 = 2x bf16), the backward being "
+                                    f"timed alone in under a millisecond"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * a.steps,
         "clocks": clk,
     }
+    if extra:
+        for r in extra.get("workloads", {}).values():
+            r["frac_of_fp8_burst"] = r["tflops"] / fp8_burst
+        if "option_overheads" in extra:
+            extra["option_overheads"]["pages"] = ("deterministic dQ costs 5-12% (MHA) and 20-34% (GQA); the causal "
+                                                  "dQ scale 8-11% of the backward at 32768 tokens")
+        line["secondary"] = extra
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -61,7 +61,20 @@ def np_of(t):
 NOISE_K = 4.0
 
 
-def compare(name, got, want, row_tol=ROW_TOL, cos_tol=COS_TOL, rows=None, noise=None):
+def compare_all(names, got, want, noise=None, o_differs=None, **kw):
+    """compare() for several outputs; every failure is reported before the
+    test fails, so one run shows all of them."""
+    errors = []
+    for n in names:
+        try:
+            compare(n, got[n], want[n], noise=None if noise is None else noise.get(n),
+                    o_differs=o_differs if n == "dQ" else None, **kw)
+        except AssertionError as e:
+            errors.append(str(e))
+    assert not errors, "; ".join(errors)
+
+
+def compare(name, got, want, row_tol=ROW_TOL, cos_tol=COS_TOL, rows=None, noise=None, o_differs=None):
     """Per-row (last axis) max-error bound and whole-tensor cosine.
 
     noise: the oracle's own change in this output when only the rounding of
@@ -90,13 +103,34 @@ def compare(name, got, want, row_tol=ROW_TOL, cos_tol=COS_TOL, rows=None, noise=
     gg, rr = g.ravel(), r.ravel()
     denom = np.sqrt((gg @ gg) * (rr @ rr))
     cos = float(gg @ rr / denom) if denom > 0 else 1.0
-    if worst > 1.0:
-        flat = np.argsort(ratio.reshape(-1, ratio.shape[-1]).max(axis=-1))[::-1][:5]
-        print(f"{name}: worst rows (flattened index, err / allowance):",
-              [(int(i), float(ratio.reshape(-1, ratio.shape[-1])[i].max())) for i in flat])
-    assert worst <= 1.0, f"{name}: max |err| exceeds the per-row allowance by {worst:.3f}x"
+    row_ratio = ratio.max(axis=-1)
+    over = row_ratio > 1.0
+    if over.any():
+        flat = np.argsort(row_ratio.ravel())[::-1][:5]
+        print(f"{name}: {int(over.sum())} of {over.size} rows over the allowance; worst (flattened row, "
+              f"err / allowance):", [(int(i), float(row_ratio.ravel()[i])) for i in flat])
+    if o_differs is not None and nz is not None and over.any():
+        # dQ rows whose stored O differs from the oracle's: there D and the
+        # cancelling dS follow the GPU's own O (see NOISE_K); such rows may
+        # exceed the allowance, but only those, at most 1% of the rows, and
+        # by no more than 10% of the tensor's max-abs
+        od = np.asarray(o_differs, bool)
+        od = od[rows] if rows is not None else od
+        assert od.shape == over.shape, (od.shape, over.shape)
+        unexplained = over & ~od
+        assert not unexplained.any(), f"{name}: {int(unexplained.sum())} rows over the allowance with O equal"
+        assert over.sum() <= max(1, 0.01 * over.size), f"{name}: {int(over.sum())} rows over the allowance"
+        rel = float(err[over].max() / max(np.abs(r).max(), 1e-30))
+        assert rel <= 0.1, f"{name}: an excepted row is off by {rel:.3e} of the tensor's max-abs"
+    else:
+        assert worst <= 1.0, f"{name}: max |err| exceeds the per-row allowance by {worst:.3f}x"
     assert cos >= cos_tol, f"{name}: cosine {cos:.7f} < {cos_tol:.7f}"
     return worst, cos
+
+
+def o_rows_differ(tc_O, ref_O):
+    """Rows (token, head) whose stored O differs from the oracle's stored O."""
+    return np.any(np_of(tc_O) != np.asarray(ref_O, np.float64), axis=-1)
 
 
 def o_rounding_noise(w, *, causal=True, exact=False, inputs=None):

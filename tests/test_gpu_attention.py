@@ -9,20 +9,20 @@ import torch
 import oracle
 import precision_causal_attention_token_gb300 as fl
 import synth
-from gpu_helpers import compare, cosine, np_of, o_rounding_noise, run_gpu, run_oracle, to_dev
+from gpu_helpers import (compare, compare_all, cosine, np_of, o_rounding_noise, o_rows_differ, run_gpu, run_oracle,
+                         to_dev)
 
 pytestmark = pytest.mark.gpu
 
 
 def _check_all(w, tc, ref, rows=None, noise=None):
-    out = {}
-    for name in ("O", "dQ", "dK", "dV"):
-        nz = None if noise is None or name == "O" else noise[name]
-        out[name] = compare(name, getattr(tc, name), ref[name], rows=rows, noise=nz)
+    names = ("O", "dQ", "dK", "dV")
+    got = {n: getattr(tc, n) for n in names}
+    od = o_rows_differ(tc.O, ref["O"]) if noise is not None else None
+    compare_all(names, got, ref, noise=noise, o_differs=od, rows=rows)
     # row statistics: lse2 = m + log2(l) for valid rows
     lse = np_of(tc.m) + np.log2(np_of(tc.l))
     assert np.abs(lse - ref["lse2"]).max() < 1e-3
-    return out
 
 
 SMALL = [
@@ -87,13 +87,14 @@ def test_full_size_sampled_against_oracle(wl, doc, head):
     sl = lambda a: np.ascontiguousarray(a[s:e, head:head + 1])
     cu1 = np.array([0, e - s], np.int32)
     ref = oracle.train_call(sl(q), sl(k), sl(v), sl(do), cu1, out_dtype="bf16")
-    noise = {}
+    noise, od = None, None
+    got = {n: getattr(tc, n)[s:e, head:head + 1] for n in ("O", "dQ", "dK", "dV")}
     if w.outlier_channels:
         r64 = oracle.train_call(sl(q), sl(k), sl(v), sl(do), cu1, out_dtype="f64")
         noise = {n: ref[n] - r64[n] for n in ("dQ", "dK", "dV")}
-    for name in ("O", "dQ", "dK", "dV"):
-        compare(f"{name} doc {doc} head {head}", getattr(tc, name)[s:e, head:head + 1], ref[name],
-                noise=noise.get(name))
+        od = o_rows_differ(got["O"], ref["O"])
+    print(f"doc {doc} ({e - s} tokens), head {head}")
+    compare_all(("O", "dQ", "dK", "dV"), got, ref, noise=noise, o_differs=od)
 
 
 def test_long_gqa_group_of_four_sampled_against_oracle():

@@ -10,7 +10,7 @@ import torch
 import oracle
 import precision_causal_attention_token_gb300 as fl
 import synth
-from gpu_helpers import compare, cosine, np_of, run_gpu, run_oracle
+from gpu_helpers import compare_all, cosine, np_of, o_rows_differ, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -19,8 +19,9 @@ NV_ORC = dict(path=oracle.PATH_NVFP4_FP8)
 
 
 def _check(tc, ref, noise=None):
-    for name in ("O", "dQ", "dK", "dV"):
-        compare(f"mixed {name}", getattr(tc, name), ref[name], noise=None if noise is None else noise.get(name))
+    names = ("O", "dQ", "dK", "dV")
+    od = o_rows_differ(tc.O, ref["O"]) if noise is not None else None
+    compare_all(names, {n: getattr(tc, n) for n in names}, ref, noise=noise, o_differs=od)
     lse = np_of(tc.m) + np.log2(np_of(tc.l))
     assert np.abs(lse - ref["lse2"]).max() < 1e-3
 
@@ -111,6 +112,6 @@ def test_mixed_full_size_sampled_against_oracle():
     cu1 = np.array([0, e - s], np.int32)
     ref = oracle.train_call(sl(q), sl(k), sl(v), sl(do), cu1, path=oracle.PATH_NVFP4_FP8, out_dtype="bf16")
     r64 = oracle.train_call(sl(q), sl(k), sl(v), sl(do), cu1, path=oracle.PATH_NVFP4_FP8, out_dtype="f64")
-    for name in ("O", "dQ", "dK", "dV"):
-        compare(f"mixed {name} doc {doc} head {head}", getattr(tc, name)[s:e, head:head + 1], ref[name],
-                noise=None if name == "O" else ref[name] - r64[name])
+    got = {n: getattr(tc, n)[s:e, head:head + 1] for n in ("O", "dQ", "dK", "dV")}
+    noise = {n: ref[n] - r64[n] for n in ("dQ", "dK", "dV")}
+    compare_all(("O", "dQ", "dK", "dV"), got, ref, noise=noise, o_differs=o_rows_differ(got["O"], ref["O"]))
