@@ -40,7 +40,8 @@ class _Cfg(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("Hkv", ctypes.c_int), ("d", ctypes.c_int),
                 ("nseq", ctypes.c_int), ("causal", ctypes.c_int), ("softmax_scale", ctypes.c_double),
                 ("quant_p", ctypes.c_int), ("quant_ds", ctypes.c_int), ("quant_pt", ctypes.c_int),
-                ("exact", ctypes.c_int), ("out_round", ctypes.c_int)]
+                ("exact", ctypes.c_int), ("out_round", ctypes.c_int), ("dq_fp16", ctypes.c_int),
+                ("dq_causal_scale", ctypes.c_int)]
 
 
 def lib():
@@ -58,6 +59,11 @@ def lib():
             L.orc_noclamp_exponent.restype, L.orc_noclamp_exponent.argtypes = i, [d]
             L.orc_scale_exponent.restype, L.orc_scale_exponent.argtypes = i, [d]
             L.orc_round_bf16.restype, L.orc_round_bf16.argtypes = d, [d]
+            L.orc_round_f16.restype, L.orc_round_f16.argtypes = d, [d]
+            L.orc_dq_prescale_c0.restype, L.orc_dq_prescale_c0.argtypes = i, [i, d]
+            L.orc_dq_prescale.restype, L.orc_dq_prescale.argtypes = i, [i, i, i, i]
+            L.orc_dq_prescales.restype = None
+            L.orc_dq_prescales.argtypes = [i, i, i, p, i, p, p, p, i, i, i, p]
             for f in ("orc_e4m3_encode_array", "orc_e2m1_encode_array", "orc_noclamp_exponent_array"):
                 getattr(L, f).restype = None
                 getattr(L, f).argtypes = [p, ctypes.c_long, p]
@@ -143,6 +149,32 @@ def round_bf16(x: float) -> float:
     return lib().orc_round_bf16(float(x))
 
 
+def round_f16(x: float) -> float:
+    return lib().orc_round_f16(float(x))
+
+
+def dq_prescale_c0(d: int, softmax_scale: float) -> int:
+    return lib().orc_dq_prescale_c0(int(d), float(softmax_scale))
+
+
+def dq_prescale(c0: int, edo: int, mk: int, mv: int) -> int:
+    return lib().orc_dq_prescale(int(c0), int(edo), int(mk), int(mv))
+
+
+def dq_prescales(cu_seqlens, eK, eV, edO, d, softmax_scale=None, causal=True, causal_scale=False) -> np.ndarray:
+    """Prescale exponents p [H][T] of the FP16 dQ partials from the exponent
+    arrays eK, eV [Hkv][T] and edO [H][T] (scale byte - 127)."""
+    eK, eV, edO = (np.ascontiguousarray(a, dtype=np.int32) for a in (eK, eV, edO))
+    Hkv, T = eK.shape
+    H = edO.shape[0]
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    out = np.zeros((H, T), np.int32)
+    scale = float(softmax_scale if softmax_scale is not None else 1.0 / np.sqrt(d))
+    lib().orc_dq_prescales(T, H, Hkv, _ptr(cu), len(cu) - 1, _ptr(eK), _ptr(eV), _ptr(edO),
+                           dq_prescale_c0(d, scale), int(causal), int(causal_scale), _ptr(out))
+    return out
+
+
 E4M3_TABLE = None
 
 
@@ -208,7 +240,7 @@ def compute_D(dOq, O_stored) -> np.ndarray:
 # --------------------------------------------------------------------------- attention
 def attention(cu_seqlens, Q, K, V, dO=None, *, Qs=None, Ks=None, eQ=None, eK=None, eV=None, edO=None,
               causal=True, softmax_scale=None, quant_p=True, quant_ds=True, quant_pt=True, exact=False,
-              out_round=0):
+              out_round=0, dq_fp16=False, dq_causal_scale=False):
     """Attention forward (+ backward when dO is given) in fp64.
 
     Q [T][H][d], K/V [T][Hkv][d], dO [T][H][d] are operand values (dequantized
@@ -228,7 +260,8 @@ def attention(cu_seqlens, Q, K, V, dO=None, *, Qs=None, Ks=None, eQ=None, eK=Non
     edO = z(H) if edO is None else np.ascontiguousarray(edO, dtype=np.int32)
     cfg = _Cfg(T, H, Hkv, d, len(cu) - 1, int(causal),
                float(softmax_scale if softmax_scale is not None else 1.0 / np.sqrt(d)),
-               int(quant_p), int(quant_ds), int(quant_pt), int(exact), int(out_round))
+               int(quant_p), int(quant_ds), int(quant_pt), int(exact), int(out_round), int(dq_fp16),
+               int(dq_causal_scale))
     O = np.empty((T, H, d), np.float64)
     lse2 = np.empty((H, T), np.float64)
     D = dQ = dK = dV = None
@@ -245,14 +278,21 @@ def attention(cu_seqlens, Q, K, V, dO=None, *, Qs=None, Ks=None, eQ=None, eK=Non
 
 
 def train_call(q, k, v, do, cu_seqlens, *, causal=True, exact=False, path=PATH_MXFP8, out_dtype="bf16",
-               softmax_scale=None, quantize=True):
+               softmax_scale=None, quantize=True, dq_fp16=None, dq_causal_scale=False):
     """The whole training call from raw inputs: quantize Q/K/V, forward, quantize
     dO (+ D), backward.  Inputs are fp32 arrays whose values are the exact inputs
     (bf16-exact for bf16 workloads).  Returns a dict with every intermediate
     payload (codes, scale bytes), O as stored, D, lse2, dQ, dK, dV.
 
     quantize=False gives the unquantized fp64 reference of the same call.
+    dq_fp16: dQ partials per 128-key tile in FP16 with a power-of-two row
+    prescale (the pages' default reduction); None selects it for the default
+    option of the MXFP8 path, whose dQ is reduced across key tiles, and not for
+    the exact option or the mixed path, whose dQ is summed in a fixed order in
+    fp32.  dq_causal_scale: the prescale from keys j <= i only.
     """
+    if dq_fp16 is None:
+        dq_fp16 = (not exact) and path == PATH_MXFP8
     cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do) if do is not None else None
     out_round = {"bf16": 1, "f32": 2, "f64": 0}[out_dtype]
@@ -282,6 +322,7 @@ def train_call(q, k, v, do, cu_seqlens, *, causal=True, exact=False, path=PATH_M
         res.update(do_codes=dc, do_scales=ds)
     r = attention(cu, Qh, Kh, Vh, dOh, Qs=Qs_, Ks=Ks_, eQ=qs.astype(np.int32) - 127,
                   eK=ks.astype(np.int32) - 127, eV=vs.astype(np.int32) - 127, edO=edO, causal=causal,
-                  softmax_scale=softmax_scale, exact=exact, out_round=out_round)
+                  softmax_scale=softmax_scale, exact=exact, out_round=out_round,
+                  dq_fp16=dq_fp16 and do is not None, dq_causal_scale=dq_causal_scale)
     res.update(r)
     return res

@@ -143,6 +143,19 @@ double orc_round_bf16(double x) {
   return (double)f;
 }
 
+// IEEE binary16 round-to-nearest-even of a double: 11 significant bits down
+// to 2^-14, a fixed step of 2^-24 below (subnormals), infinity from 65520 up.
+double orc_round_f16(double x) {
+  if (std::isnan(x)) return x;
+  double a = std::fabs(x);
+  if (a >= 65520.0) return std::copysign(INFINITY, x);
+  int e = 0;
+  std::frexp(a, &e);                       // a = f * 2^e, f in [0.5, 1)
+  int step = (a >= std::ldexp(1.0, -14)) ? e - 11 : -24;
+  double q = std::nearbyint(std::ldexp(a, -step));  // ties to even (default rounding mode)
+  return std::copysign(std::ldexp(q, step), x);
+}
+
 // ---------------------------------------------------------------------------
 // Quantizers.
 // ---------------------------------------------------------------------------
@@ -270,7 +283,58 @@ struct orc_attn_cfg {
   int quant_pt;          // quantize the dV operand P~ in 32x32 blocks
   int exact;             // exact option: per-row dS exponents for dQ ([SUM] §4.5)
   int out_round;         // O as stored: 0 kept in fp64, 1 rounded to bf16, 2 to fp32
+  int dq_fp16;           // dQ partials of each 128-key tile in FP16 with a row prescale
+  int dq_causal_scale;   // the prescale from keys j <= i only (else the whole document)
 };
+
+// The power-of-two dQ prescale of one query row ([READ] 四 4.4: FP16 dQ
+// partials with a data-dependent power-of-two prescale, since a fixed one
+// overflows on outlier K channels; [SUM] §4.5: the optional causal dQ scale).
+// Reading: a bound of |dQ_i| from the exponent bytes alone.  With
+// |dO^_i|_2 <= sqrt(d) 448 2^edO(i), |V^_j|_2 <= sqrt(d) 448 2^eV(j) and
+// |K^_j|_inf <= 448 2^eK(j) (no element clamps), |dP_ij - D_i| stays below
+// 2 (1 + 2^-4) d 448^2 2^(edO + eV) and
+//   |dQ_i| <= 2.5 d 448^3 scale 2^(edO(i) + MK + MV) =: 2^(c0 + edO + MK + MV)
+// with MK, MV the largest eK, eV over the keys the rule looks at: the whole
+// document by default (a sequence-range dependency), keys j <= i with the
+// causal dQ scale.  The prescale 2^p, p = 15 - c0 - (edO + MK + MV) clamped
+// to [-126, 127], keeps every partial sum of 2^p dQ_i within 2^15 < 65504.
+int orc_dq_prescale_c0(int d, double softmax_scale) {
+  int e = 0;
+  double f = std::frexp(2.5 * d * 448.0 * 448.0 * 448.0 * softmax_scale, &e);
+  return f > 0.5 ? e : e - 1;  // ceil(log2(.)), exact
+}
+int orc_dq_prescale(int c0, int edO, int mk, int mv) {
+  int p = 15 - c0 - (edO + mk + mv);
+  return p < -126 ? -126 : (p > 127 ? 127 : p);
+}
+
+// The prescale exponent of every query row: p [H][T] from the exponent bytes
+// eK, eV [Hkv][T] and edO [H][T].  MK, MV run over the row's document, or
+// over keys j <= i when causal and causal_scale are both set.
+void orc_dq_prescales(int T, int H, int Hkv, const int* cu, int nseq, const int* eK, const int* eV,
+                      const int* edO, int c0, int causal, int causal_scale, int* p) {
+  const int G = H / Hkv;
+  for (int doc = 0; doc < nseq; ++doc) {
+    const int s0 = cu[doc], L = cu[doc + 1] - cu[doc];
+    for (int h = 0; h < H; ++h) {
+      const int hk = h / G;
+      int mk_doc = -1000, mv_doc = -1000;
+      for (int j = 0; j < L; ++j) {
+        mk_doc = std::max(mk_doc, eK[(size_t)hk * T + s0 + j]);
+        mv_doc = std::max(mv_doc, eV[(size_t)hk * T + s0 + j]);
+      }
+      int mk = -1000, mv = -1000;
+      for (int i = 0; i < L; ++i) {
+        mk = std::max(mk, eK[(size_t)hk * T + s0 + i]);
+        mv = std::max(mv, eV[(size_t)hk * T + s0 + i]);
+        const bool pre = causal && causal_scale;
+        p[(size_t)h * T + s0 + i] = orc_dq_prescale(c0, edO[(size_t)h * T + s0 + i], pre ? mk : mk_doc,
+                                                    pre ? mv : mv_doc);
+      }
+    }
+  }
+}
 
 // Quantize v (values of one block) to E4M3 codes with the no-clamp exponent of
 // the block's max-abs and return the dequantized values in place.  `clampexp`
@@ -330,6 +394,10 @@ void orc_attention(const orc_attn_cfg* cfg, const int* cu, const double* Qs, con
   const int G = H / Hkv;
   const double LOG2E = 1.4426950408889634073599246810019;
   const bool bwd = (dO != nullptr);
+  std::vector<int> pq((size_t)T * H, 0);  // dQ prescale exponents (FP16 partials)
+  if (bwd && cfg->dq_fp16)
+    orc_dq_prescales(T, H, Hkv, cu, cfg->nseq, eK, eV, edO, orc_dq_prescale_c0(d, cfg->softmax_scale),
+                     cfg->causal, cfg->dq_causal_scale, pq.data());
   if (bwd) {
     std::fill(dQ, dQ + (size_t)T * H * d, 0.0);
     std::fill(dK, dK + (size_t)T * Hkv * d, 0.0);
@@ -469,12 +537,26 @@ void orc_attention(const orc_attn_cfg* cfg, const int* cu, const double* Qs, con
           }
       }
       // 8., 9., 10. gradients
-      for (int i = 0; i < L; ++i)
+      for (int i = 0; i < L; ++i) {
+        const int p = pq[(size_t)h * T + s0 + i];
         for (int k = 0; k < d; ++k) {
           double acc = 0.0;
-          for (int j = 0; j < L; ++j) acc += dSq[(size_t)i * L + j] * kk(j, k);
+          if (!cfg->dq_fp16) {
+            for (int j = 0; j < L; ++j) acc += dSq[(size_t)i * L + j] * kk(j, k);
+          } else {
+            // each 128-key tile's partial sum, scaled by 2^p and rounded to
+            // FP16, is added to an FP16 accumulator (each sum rounded), in
+            // the order of the key tiles
+            for (int j0 = 0; j0 < L; j0 += 128) {
+              double part = 0.0;
+              for (int j = j0; j < std::min(j0 + 128, L); ++j) part += dSq[(size_t)i * L + j] * kk(j, k);
+              acc = orc_round_f16(acc + orc_round_f16(std::ldexp(part, p)));
+            }
+            acc = std::ldexp(acc, -p);
+          }
           dQ[((size_t)(s0 + i) * H + h) * d + k] = cfg->softmax_scale * acc;
         }
+      }
       for (int j = 0; j < L; ++j)
         for (int k = 0; k < d; ++k) {
           double ak = 0.0, av = 0.0;
