@@ -32,8 +32,9 @@
  *     seen by a kernel) set the device status word in the workspace, read
  *     with flamia_get_device_status().
  *   - The workspace `ws` (size from flamia_workspace_size) holds the plan,
- *     the fp32 dQ accumulator and the status word.  It must stay the same
- *     buffer from flamia_plan through flamia_bwd of one call.
+ *     the dQ accumulator (fp32, or FP16 with its prescale exponents), and
+ *     the status word.  It must stay the same buffer from flamia_plan through
+ *     flamia_bwd of one call.
  */
 #ifndef FLAMIA_H_
 #define FLAMIA_H_
@@ -76,8 +77,18 @@ typedef enum { FLAMIA_ROLE_QKV = 0, FLAMIA_ROLE_DO = 1 } flamia_role_t;
  *   exact        1: the exact option ([SUM] §4.5): per-token Q, K and dO
  *                scales, per-(row, 32-key) dS exponents for dQ, deterministic
  *                dQ.  0: token-block scales over 32 document-local tokens.
- *   causal_dq_scale  accepted; with fp32 dQ accumulation it changes nothing
- *                ([SUM] §4.5 introduces it for FP16 accumulators).
+ *   causal_dq_scale  with dq_fp16: 1 takes the power-of-two prescale of
+ *                row i's FP16 dQ partials from keys j <= i only ([SUM] §4.5:
+ *                removes the sequence-range dependency of the dQ
+ *                accumulator); 0 from the whole document.
+ *   dq_fp16      1: the default option's dQ partials (one per 128-key tile)
+ *                are prescaled by a power of two per query row, rounded to
+ *                FP16 and reduced into an FP16 accumulator ([READ] 四 4.4);
+ *                0: fp32 partials into an fp32 accumulator (the default here:
+ *                faster on this kernel, whose backward is bound by its compute
+ *                warps, not by the reduction).  No effect on the exact and
+ *                deterministic options and the mixed path, whose dQ sums in
+ *                fp32 in a fixed order.
  *   deterministic 1: dQ reduced in a fixed order (no atomics).
  *   softmax_scale  0 selects 1/sqrt(d).
  *   path         flamia_path_t.
@@ -90,6 +101,7 @@ typedef struct {
   int32_t causal, exact, causal_dq_scale, deterministic;
   float softmax_scale;
   int32_t path, in_dtype, out_dtype;
+  int32_t dq_fp16;
 } flamia_problem_t;
 
 /* A quantized operand (device pointers, caller-owned).
@@ -156,7 +168,11 @@ flamia_status_t flamia_fwd(const flamia_problem_t* p, const flamia_operand_t* q,
  * with the forward's tiling and exponent evaluation, dP = dO^ V^T,
  * dS = P (dP - D), dS quantized with one exponent per 32x32 block (the exact
  * option: per (row, 32 keys) for dQ), dV += P~^T dO^, dK += dS^T Q^,
- * dQ += dS K^, all accumulated in fp32; GQA sums dK/dV over the group.
+ * dQ += dS K^; dK and dV accumulate in fp32; dQ's per-key-tile partials are
+ * summed by bulk reduce-adds, in fp32, or (dq_fp16) prescaled by a power of
+ * two per query row and summed in FP16 ([READ] 四 4.4); the exact and
+ * deterministic options and the mixed path sum dQ in fp32 in a fixed order.
+ * GQA sums dK/dV over the group.
  *   dQ device [T][H][d], dK/dV device [T][Hkv][d], out_dtype.
  * D, m, l as produced by flamia_quantize(DO) and flamia_fwd. */
 flamia_status_t flamia_bwd(const flamia_problem_t* p, const flamia_operand_t* q, const flamia_operand_t* k,
@@ -184,19 +200,27 @@ flamia_status_t flamia_clear_device_status(void* ws, cudaStream_t stream);
 flamia_status_t flamia_debug_set_phat_dump(void* ws, size_t ws_bytes, void* codes, int32_t* exps,
                                            cudaStream_t stream);
 
-/* Test hook (not for the hot path): make the next flamia_fwd / flamia_bwd
- * calls on workspace `ws` exercise their bounded waits.  wait_ns != 0
- * replaces the limit of every wait inside the attention kernels (default
- * about 2 s; at most 10 s accepted); withhold_first_item != 0 makes each CTA's
- * producer withhold its first work item, so the other roles' waits for it
- * run out: the kernel then records FLAMIA_ERR_TIMEOUT in the device status
- * word, every role leaves its loop and the CTA releases its tensor memory and
- * exits (nothing was issued, so no copy or MMA is in flight).  The outputs of
- * such a call are undefined.  flamia_plan switches the hook off.  Synchronises
- * `stream`.  Returns FLAMIA_ERR_INVALID_ARG for a null or too small
- * workspace or a limit above 10 s. */
-flamia_status_t flamia_debug_set_wait_test(void* ws, size_t ws_bytes, uint64_t wait_ns, int32_t withhold_first_item,
-                                           cudaStream_t stream);
+/* Regions of the workspace that tests read back (flamia_debug_workspace_offset). */
+typedef enum {
+  FLAMIA_WS_FWD_ITEMS = 0,    /* int32 pairs (document, 128-query tile), longest first */
+  FLAMIA_WS_BWD_ITEMS = 1,    /* int32 pairs (document, 128-key tile), longest first */
+  FLAMIA_WS_DQ_PRESCALE = 2   /* int8 [H][T]: exponent p of the FP16 dQ partials' prescale 2^p */
+} flamia_ws_region_t;
+
+/* Test hook: byte offset of a region inside the workspace of problem `p`
+ * (0 for an invalid problem or region).  The dQ prescale exponents are
+ * written by flamia_bwd on the dq_fp16 path. */
+size_t flamia_debug_workspace_offset(const flamia_problem_t* p, int32_t region);
+
+/* Test hook (not for the hot path): exercise the bounded waits.  While on,
+ * each CTA of the next flamia_fwd / flamia_bwd launches withholds its first
+ * work item, so its other roles' waits for that item run out after the
+ * bounded-wait limit (about 2 s): the kernel records FLAMIA_ERR_TIMEOUT in the
+ * device status word, every role leaves its loop and the CTA releases its
+ * tensor memory and exits (nothing was issued, so no copy or MMA is in
+ * flight).  The outputs of such a call are undefined.  Process-wide (not per
+ * workspace); flamia_plan switches it off.  Always returns FLAMIA_OK. */
+flamia_status_t flamia_debug_withhold_first_item(int32_t on);
 
 /* Allocation-free work-list builder (this library's own addition; the
  * method's pages have no counterpart).  For callers that cannot allocate

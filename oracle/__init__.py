@@ -278,7 +278,7 @@ def attention(cu_seqlens, Q, K, V, dO=None, *, Qs=None, Ks=None, eQ=None, eK=Non
 
 
 def train_call(q, k, v, do, cu_seqlens, *, causal=True, exact=False, path=PATH_MXFP8, out_dtype="bf16",
-               softmax_scale=None, quantize=True, dq_fp16=None, dq_causal_scale=False):
+               softmax_scale=None, quantize=True, dq_fp16=False, dq_causal_scale=False):
     """The whole training call from raw inputs: quantize Q/K/V, forward, quantize
     dO (+ D), backward.  Inputs are fp32 arrays whose values are the exact inputs
     (bf16-exact for bf16 workloads).  Returns a dict with every intermediate
@@ -286,13 +286,9 @@ def train_call(q, k, v, do, cu_seqlens, *, causal=True, exact=False, path=PATH_M
 
     quantize=False gives the unquantized fp64 reference of the same call.
     dq_fp16: dQ partials per 128-key tile in FP16 with a power-of-two row
-    prescale (the pages' default reduction); None selects it for the default
-    option of the MXFP8 path, whose dQ is reduced across key tiles, and not for
-    the exact option or the mixed path, whose dQ is summed in a fixed order in
-    fp32.  dq_causal_scale: the prescale from keys j <= i only.
+    prescale (the pages' FP16 reduction); False sums dQ in fp64.
+    dq_causal_scale: the prescale from keys j <= i only.
     """
-    if dq_fp16 is None:
-        dq_fp16 = (not exact) and path == PATH_MXFP8
     cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do) if do is not None else None
     out_round = {"bf16": 1, "f32": 2, "f64": 0}[out_dtype]

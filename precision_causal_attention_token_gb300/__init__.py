@@ -21,7 +21,9 @@ ROLE_QKV, ROLE_DO = 0, 1
 
 EXPORTED = ("flamia_workspace_size", "flamia_plan", "flamia_quantize", "flamia_fwd", "flamia_bwd",
             "flamia_get_device_status", "flamia_clear_device_status", "flamia_status_string",
-            "flamia_debug_set_phat_dump", "flamia_debug_set_wait_test", "flamia_plan_noalloc")
+            "flamia_debug_set_phat_dump", "flamia_debug_withhold_first_item", "flamia_debug_workspace_offset",
+            "flamia_plan_noalloc")
+WS_FWD_ITEMS, WS_BWD_ITEMS, WS_DQ_PRESCALE = range(3)
 
 
 class FlamiaError(RuntimeError):
@@ -35,7 +37,7 @@ class Problem(ctypes.Structure):
                 ("n_seq", ctypes.c_int32), ("cu_seqlens", ctypes.c_void_p), ("causal", ctypes.c_int32),
                 ("exact", ctypes.c_int32), ("causal_dq_scale", ctypes.c_int32), ("deterministic", ctypes.c_int32),
                 ("softmax_scale", ctypes.c_float), ("path", ctypes.c_int32), ("in_dtype", ctypes.c_int32),
-                ("out_dtype", ctypes.c_int32)]
+                ("out_dtype", ctypes.c_int32), ("dq_fp16", ctypes.c_int32)]
 
 
 class Operand(ctypes.Structure):
@@ -70,8 +72,9 @@ def load_library(path: str = LIB_PATH):
     L.flamia_status_string.restype, L.flamia_status_string.argtypes = ctypes.c_char_p, [i32]
     L.flamia_debug_set_phat_dump.restype = i32
     L.flamia_debug_set_phat_dump.argtypes = [vp, sz, vp, vp, vp]
-    L.flamia_debug_set_wait_test.restype = i32
-    L.flamia_debug_set_wait_test.argtypes = [vp, sz, ctypes.c_uint64, i32, vp]
+    L.flamia_debug_workspace_offset.restype, L.flamia_debug_workspace_offset.argtypes = sz, [P, i32]
+    L.flamia_debug_withhold_first_item.restype = i32
+    L.flamia_debug_withhold_first_item.argtypes = [i32]
     L.flamia_plan_noalloc.restype = i32
     L.flamia_plan_noalloc.argtypes = [P, vp, vp, vp, vp]
     _lib = L
@@ -98,11 +101,12 @@ def _stream(stream) -> int | None:
 
 
 def make_problem(T, H, Hkv, d, cu_seqlens, *, causal=True, exact=False, causal_dq_scale=False,
-                 deterministic=False, softmax_scale=0.0, path=PATH_MXFP8, in_dtype=BF16, out_dtype=BF16) -> Problem:
+                 deterministic=False, softmax_scale=0.0, path=PATH_MXFP8, in_dtype=BF16, out_dtype=BF16,
+                 dq_fp16=False) -> Problem:
     """cu_seqlens: int32 device tensor [n_seq + 1] (kept referenced by the caller)."""
     return Problem(int(T), int(H), int(Hkv), int(d), int(cu_seqlens.numel() - 1), cu_seqlens.data_ptr(),
                    int(causal), int(exact), int(causal_dq_scale), int(deterministic), float(softmax_scale),
-                   int(path), int(in_dtype), int(out_dtype))
+                   int(path), int(in_dtype), int(out_dtype), int(dq_fp16))
 
 
 def operand(codes, scales, codes4=None, scales4=None, gscale4=None) -> Operand:
@@ -156,12 +160,15 @@ def flamia_debug_set_phat_dump(ws, codes, exps, stream=None):
                                                      _stream(stream)), "flamia_debug_set_phat_dump")
 
 
-def flamia_debug_set_wait_test(ws, wait_ns: int, withhold_first_item: bool, stream=None):
-    """Test hook: shorten the attention kernels' wait limit and/or withhold each
-    CTA's first work item, so that the waits run out (see include/flamia.h)."""
-    _check(load_library().flamia_debug_set_wait_test(_ptr(ws), ws.numel() * ws.element_size(), int(wait_ns),
-                                                     int(bool(withhold_first_item)), _stream(stream)),
-           "flamia_debug_set_wait_test")
+def flamia_debug_workspace_offset(prob: Problem, region: int) -> int:
+    """Byte offset of a workspace region (WS_FWD_ITEMS, WS_BWD_ITEMS, WS_DQ_PRESCALE)."""
+    return int(load_library().flamia_debug_workspace_offset(ctypes.byref(prob), int(region)))
+
+
+def flamia_debug_withhold_first_item(on: bool):
+    """Test hook: the next attention launches withhold each CTA's first work
+    item, so that their bounded waits run out (see include/flamia.h)."""
+    _check(load_library().flamia_debug_withhold_first_item(int(bool(on))), "flamia_debug_withhold_first_item")
 
 
 def flamia_clear_device_status(ws, stream=None):
@@ -185,6 +192,7 @@ class TrainCall:
     exact: bool = False
     deterministic: bool = False
     causal_dq_scale: bool = False
+    dq_fp16: bool = False
     path: int = PATH_MXFP8
     in_dtype: int = BF16
     out_dtype: int = BF16
@@ -195,7 +203,7 @@ class TrainCall:
         dev = self.cu_seqlens.device
         self.prob = make_problem(self.T, self.H, self.Hkv, self.d, self.cu_seqlens, causal=self.causal,
                                  exact=self.exact, deterministic=self.deterministic,
-                                 causal_dq_scale=self.causal_dq_scale,
+                                 causal_dq_scale=self.causal_dq_scale, dq_fp16=self.dq_fp16,
                                  softmax_scale=self.softmax_scale, path=self.path, in_dtype=self.in_dtype,
                                  out_dtype=self.out_dtype)
         nbytes = flamia_workspace_size(self.prob)

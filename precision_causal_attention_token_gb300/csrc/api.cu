@@ -3,6 +3,7 @@
 // synchronisation on the plan/quantize/fwd/bwd paths.
 #include <cmath>
 #include <cstddef>
+#include <atomic>
 #include <cstring>
 #include <cudaTypedefs.h>
 
@@ -11,6 +12,10 @@
 using namespace flamia;
 
 namespace {
+
+// Test hook (flamia_debug_withhold_first_item): process-wide, copied into the
+// parameters of the next attention launches, cleared by flamia_plan.
+std::atomic<int> g_dbg_withhold{0};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -42,6 +47,16 @@ float softmax_scale_of(const flamia_problem_t* p) {
   return p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / std::sqrt((float)p->d);
 }
 
+// The constant of the FP16 dQ prescale: c0 = ceil(log2(2.5 d 448^3 scale)),
+// so that |dQ_i| <= 2^(c0 + edO(i) + max eK + max eV) (close reading, 4.4: a
+// data-dependent power-of-two prescale of the FP16 dQ partials).  frexp keeps
+// it exact: x = f 2^e with f in [0.5, 1), ceil(log2 x) = e unless f = 0.5.
+int dq_prescale_c0(int d, float scale) {
+  int e = 0;
+  const double f = std::frexp(2.5 * d * 448.0 * 448.0 * 448.0 * (double)scale, &e);
+  return f > 0.5 ? e : e - 1;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -71,16 +86,19 @@ bool make_codes_map(CUtensorMap* m, const void* ptr, int d, int heads, int T) {
   return r == CUDA_SUCCESS;
 }
 
-// 3-D map over the fp32 dQ accumulator [T][heads][d]: box = 128 tokens x 1
-// head x 32 values (128 bytes, 128B swizzle), the target of bulk reduce-adds.
-bool make_dq_map(CUtensorMap* m, float* ptr, int d, int heads, int T) {
+// 3-D map over the dQ accumulator [T][heads][d], the target of bulk
+// reduce-adds: box = 128 tokens x 1 head x 128 bytes of values (32 fp32, or
+// 64 FP16 with dq_fp16), 128B swizzle.
+bool make_dq_map(CUtensorMap* m, void* ptr, int d, int heads, int T, bool fp16) {
   auto enc = encode_fn();
   if (!enc) return false;
+  const cuuint64_t es = fp16 ? 2 : 4;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)T};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)heads * d * 4};
-  cuuint32_t box[3] = {32, 1, 128};
+  cuuint64_t strides[2] = {(cuuint64_t)d * es, (cuuint64_t)heads * d * es};
+  cuuint32_t box[3] = {fp16 ? 64u : 32u, 1, 128};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+  CUresult r = enc(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims,
+                   strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -135,6 +153,7 @@ flamia_status_t flamia_plan(const flamia_problem_t* p, void* ws, size_t ws_bytes
   if (s != FLAMIA_OK) return s;
   WsLayout L;
   if ((s = check_ws(p, ws, ws_bytes, &L)) != FLAMIA_OK) return s;
+  g_dbg_withhold.store(0);
   return launch_plan(*p, L, static_cast<uint8_t*>(ws), stream) == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
 }
 
@@ -220,7 +239,13 @@ static flamia_status_t fill_params(const flamia_problem_t* p, const WsLayout& L,
   a->bwd_items = reinterpret_cast<const int2*>(w + L.bwd_items);
   a->hdr = reinterpret_cast<WsHeader*>(w + L.header);
   a->dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
+  a->dq16 = reinterpret_cast<__half*>(w + L.dq_acc);
+  a->dq_fp16 = p->dq_fp16 ? 1 : 0;
+  a->pexp = reinterpret_cast<int8_t*>(w + L.pexp);
+  a->c0 = dq_prescale_c0(p->d, a->softmax_scale);
+  a->causal_dq_scale = p->causal_dq_scale ? 1 : 0;
   a->nvfp4 = p->path == FLAMIA_PATH_NVFP4_FP8 ? 1 : 0;
+  a->dbg_withhold = g_dbg_withhold.load();
   return FLAMIA_OK;
 }
 
@@ -286,7 +311,7 @@ flamia_status_t flamia_bwd(const flamia_problem_t* p, const flamia_operand_t* q,
   AttnMaps maps;
   if (!make_codes_map(&maps.q, q->codes, p->d, p->H, p->T) || !make_codes_map(&maps.k, k->codes, p->d, p->Hkv, p->T) ||
       !make_codes_map(&maps.v, v->codes, p->d, p->Hkv, p->T) || !make_codes_map(&maps.dO, dO->codes, p->d, p->H, p->T) ||
-      !make_dq_map(&maps.dq, a.dq_acc, p->d, p->H, p->T))
+      !make_dq_map(&maps.dq, a.dq_acc, p->d, p->H, p->T, a.dq_fp16 != 0))
     return FLAMIA_ERR_CUDA;
   maps.qn = maps.q;
   maps.kn = maps.k;
@@ -322,21 +347,19 @@ flamia_status_t flamia_debug_set_phat_dump(void* ws, size_t ws_bytes, void* code
   return FLAMIA_OK;
 }
 
-flamia_status_t flamia_debug_set_wait_test(void* ws, size_t ws_bytes, uint64_t wait_ns, int32_t withhold_first_item,
-                                           cudaStream_t stream) {
-  if (!ws || ws_bytes < sizeof(WsHeader) || wait_ns > 10000000000ull) return FLAMIA_ERR_INVALID_ARG;
-  static thread_local struct {
-    uint32_t withhold, pad;
-    uint64_t wait_ns;
-  } v;
-  static_assert(offsetof(WsHeader, dbg_wait_ns) == offsetof(WsHeader, dbg_withhold) + 8, "hook layout");
-  v.withhold = withhold_first_item ? 1u : 0u;
-  v.pad = 0u;
-  v.wait_ns = wait_ns;
-  uint8_t* dst = static_cast<uint8_t*>(ws) + offsetof(WsHeader, dbg_withhold);
-  if (cudaMemcpyAsync(dst, &v, sizeof(v), cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-      cudaStreamSynchronize(stream) != cudaSuccess)
-    return FLAMIA_ERR_CUDA;
+size_t flamia_debug_workspace_offset(const flamia_problem_t* p, int32_t region) {
+  if (validate(p) != FLAMIA_OK) return 0;
+  const WsLayout L = ws_layout(*p);
+  switch (region) {
+    case FLAMIA_WS_FWD_ITEMS: return L.fwd_items;
+    case FLAMIA_WS_BWD_ITEMS: return L.bwd_items;
+    case FLAMIA_WS_DQ_PRESCALE: return L.pexp;
+  }
+  return 0;
+}
+
+flamia_status_t flamia_debug_withhold_first_item(int32_t on) {
+  g_dbg_withhold.store(on ? 1 : 0);
   return FLAMIA_OK;
 }
 

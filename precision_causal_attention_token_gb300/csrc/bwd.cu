@@ -22,9 +22,12 @@
 //   dV += P~^T dO^ (A = P~ MN-major, B = dO MN-major)   block-scaled
 //   dK += dS^T Q^  (A = dS MN-major, B = Q MN-major)    block-scaled
 //   dQ  = dS K^    -> TMEM X1 in two 64-column halves (A = dS K-major,
-//     B = K MN-major); the drain warps stage each half in shared memory and
-//     the reducer warp adds it into the fp32 dQ buffer with bulk tensor
-//     reduce-adds (the addition happens in L2).
+//     B = K MN-major); the drain warps stage each half in 128B-swizzled boxes
+//     and the reducer warp adds them into the dQ accumulator with bulk tensor
+//     reduce-adds (the addition happens in L2): fp32 partials by default, or
+//     (DQ16) each row scaled by its power-of-two prescale and rounded to FP16
+//     (close reading 4.4: FP16 dQ partials with a data-dependent
+//     power-of-two prescale).
 // Every per-token factor that varies along a contraction (2^eQ, 2^eK, 2^edO,
 // 2^-eV) is folded into the other operand before its block quantization, so
 // all B operands run with unit scale factors.
@@ -71,9 +74,10 @@ struct __align__(1024) BwdTiles {
   uint8_t pt[kTile * kTile];   // P~ codes   [query][key]
   uint8_t ds[kTile * kTile];   // dS^ codes  [query][key] (dQ payload; also dK's in the default option)
   uint8_t dsk[EXACT ? kTile * kTile : 1024];  // exact option: dK payload
-  // one half (64 columns) of a dQ tile staged for the bulk reduce-add: two
-  // boxes of [128 rows][32 fp32], 128B-swizzled
-  float dqs[DQ ? kTile * 64 : 256];
+  // one half (64 columns) of a dQ tile staged for the bulk reduce-adds: two
+  // boxes of [128 rows][32 fp32], or one of [128 rows][64 FP16] (DQ16);
+  // 128B-swizzled
+  uint8_t dqs[DQ ? kTile * 256 : 1024];
   uint8_t qn[2][NV4 ? score_tile_bytes<HD, NV4>() : 16];  // mixed path: Q's score operand
 };
 
@@ -225,11 +229,26 @@ __device__ __forceinline__ void store_row32(void* out, size_t off, const uint32_
 }
 
 // Store 32 fp32 values of row r into one 128B-swizzled [128 rows][32 fp32] box.
-__device__ __forceinline__ void store_row_box(float* box, int r, const uint32_t (&rr)[32]) {
-  uint8_t* b = reinterpret_cast<uint8_t*>(box);
+__device__ __forceinline__ void store_row_box(uint8_t* box, int r, const uint32_t (&rr)[32]) {
 #pragma unroll
   for (int c = 0; c < 8; ++c)
-    *reinterpret_cast<uint4*>(b + sw128_off(r, c)) = make_uint4(rr[4 * c], rr[4 * c + 1], rr[4 * c + 2], rr[4 * c + 3]);
+    *reinterpret_cast<uint4*>(box + sw128_off(r, c)) = make_uint4(rr[4 * c], rr[4 * c + 1], rr[4 * c + 2], rr[4 * c + 3]);
+}
+
+// 32 fp32 values times s, rounded to FP16 (RNE), as 16-byte chunks c0..c0+3
+// of row r of a 128B-swizzled [128 rows][64 FP16] box.
+__device__ __forceinline__ void store_row_f16(uint8_t* box, int r, int c0, const uint32_t (&rr)[32], float s) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __half2 h2 = __floats2half2_rn(__uint_as_float(rr[8 * c + 2 * e]) * s,
+                                           __uint_as_float(rr[8 * c + 2 * e + 1]) * s);
+      w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint4*>(box + sw128_off(r, c0 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
 }
 
 // Per-row values the backward needs for query row i of head h.
@@ -288,19 +307,20 @@ __device__ __forceinline__ uint32_t dq_operand(const float (&wv)[32], float amax
 }
 
 // ============================================================================
-// dK/dV kernel (and dQ when DQ): one CTA per (document, 128-key tile, KV
-// head), looping over the group's query heads and tiles.  With DQ, each query
+// dK/dV kernel (and dQ when DQ; DQ16: FP16 partials): one CTA per (document,
+// 128-key tile, KV head), looping over the group's query heads and tiles.  With DQ, each query
 // tile's dQ = dS^ K^ lands in TMEM, is staged in shared memory by the compute
 // warps and added to the fp32 dQ buffer by the reducer warp with bulk tensor
 // reduce-adds (whole 128-byte lines, the addition done in L2).
 // ============================================================================
-template <int HD, bool OUT_BF16, bool EXACT, bool DQ, bool NV4>
+template <int HD, bool OUT_BF16, bool EXACT, bool DQ, bool NV4, bool DQ16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                const __grid_constant__ CUtensorMap map_dq, const __grid_constant__ CUtensorMap map_qn,
                const __grid_constant__ CUtensorMap map_kn) {
   static_assert(!(NV4 && DQ), "the mixed path takes dQ from the dQ kernel");
+  static_assert(DQ || !DQ16, "FP16 partials belong to the dQ path");
   constexpr int kKvStages = bwd_kv_stages<NV4>();
   constexpr bool PERKEY = EXACT || NV4;
   constexpr int kQKBytes = score_tile_bytes<HD, NV4>();
@@ -367,7 +387,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint32_t ic = 0, ii = 0;
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it, ++ic) {
-      const int w = item_publish(c.ring, n_it, &hdr->bwd_counter, n_work, lane, abort_flag, hdr, 0x304, ok);
+      const int w = item_publish(c.ring, n_it, &hdr->bwd_counter, n_work, lane, abort_flag, hdr, 0x304, ok, p.dbg_withhold);
       if (w < 0) break;
       const int pair = w / p.Hkv, hk = w - pair * p.Hkv;
       const int2 it = p.bwd_items[pair];
@@ -518,6 +538,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
    } else if (warp == kWarpRed) {
     // ------------------------------------------------------------ dQ reducer
+    // Each staged half is added into the accumulator by bulk tensor
+    // reduce-adds (rows past the document's end hold zeros; rows past T are
+    // clipped by the copy).
     if (DQ && lane == 0) {
       uint32_t ii = 0, hc = 0;  // hc: staged halves
       bool ok = true;
@@ -530,13 +553,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int n_t = (len + kTile - 1) / kTile, q_first = p.causal ? it.y : 0;
         for (int g = 0; ok && g < G; ++g) {
           const int h = hk * G + g;
-          for (int qt = q_first; qt < n_t; ++qt, ++ii) {
+          for (int qt = q_first; ok && qt < n_t; ++qt, ++ii) {
             // one staged half (64 columns) at a time
             for (int half = 0; ok && half < HD / 64; ++half, ++hc) {
               if (!(ok = mbar_wait(&c.dqs_full, hc & 1, abort_flag, hdr, 0x331))) break;
+              if constexpr (DQ16) {
+                tma_reduce_add_3d(&map_dq, tl.dqs, 64 * half, h, ds + kTile * qt);
+              } else {
 #pragma unroll
-              for (int cb = 0; cb < 2; ++cb)
-                tma_reduce_add_3d(&map_dq, tl.dqs + cb * (kTile * 32), 64 * half + 32 * cb, h, ds + kTile * qt);
+                for (int cb = 0; cb < 2; ++cb)
+                  tma_reduce_add_3d(&map_dq, tl.dqs + cb * (kTile * 128), 64 * half + 32 * cb, h, ds + kTile * qt);
+              }
               bulk_commit_group();
               bulk_wait_group_read0();
               mbar_arrive(&c.dqs_free);
@@ -570,10 +597,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int n_t = (len + kTile - 1) / kTile, q_first = p.causal ? it.y : 0;
       const int n_iter = G * (n_t - q_first);
       if constexpr (DQ) {
+        const int per_g = n_t - q_first;
         for (int t = 0; ok && t < n_iter; ++t, ++ii) {
+          // this iteration's query tile and head (the order of every role)
+          const int g = t / per_g, qt = q_first + (t - g * per_g);
+          const int i_loc = kTile * qt + r;
+          // DQ16: the row's power-of-two prescale (rows past the document: zeros)
+          float sp = 0.f;
+          if constexpr (DQ16)
+            if (i_loc < len) sp = exp2i((int)__ldg(p.pexp + (size_t)(hk * G + g) * p.T + ds + i_loc));
           // the dQ tile arrives in X1[0, 64) in halves of 64 columns (d = 128)
-          // or whole (d = 64); each half goes to two staging boxes.  The first
-          // half is committed before the dV / dK MMAs, the second with them.
+          // or whole (d = 64); each half is staged as FP16.  The first half is
+          // committed before the dV / dK MMAs, the second with them.
 #pragma unroll
           for (int half = 0; half < HD / 64; ++half) {
             if (half == 0) {  // the first (d = 64: only) half is committed on its own
@@ -591,8 +626,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (half == HD / 64 - 1) mbar_arrive(&c.x1_free);         // the dQ tile has left X1
             // the staging half is free once the reducer has read the previous one
             if (!(ok = mbar_wait_warp(&c.dqs_free, (hc & 1) ^ 1, abort_flag, hdr, 0x342))) break;
-            store_row_box(tl.dqs, r, rq[0]);
-            store_row_box(tl.dqs + kTile * 32, r, rq[1]);
+            if constexpr (DQ16) {
+              store_row_f16(tl.dqs, r, 0, rq[0], sp);
+              store_row_f16(tl.dqs, r, 4, rq[1], sp);
+            } else {
+              store_row_box(tl.dqs, r, rq[0]);
+              store_row_box(tl.dqs + kTile * 128, r, rq[1]);
+            }
             fence_proxy_async_smem();
             mbar_arrive(&c.dqs_full);
             ++hc;
@@ -835,7 +875,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     uint32_t ic = 0, kv = 0;
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it, ++ic) {
-      const int w = item_publish(c.ring, n_it, &hdr->dq_counter, n_work, lane, abort_flag, hdr, 0x404, ok);
+      const int w = item_publish(c.ring, n_it, &hdr->dq_counter, n_work, lane, abort_flag, hdr, 0x404, ok, p.dbg_withhold);
       if (w < 0) break;
       const int pair = w / p.H, h = w - pair * p.H, hk = h / G;
       const int2 it = p.fwd_items[pair];
@@ -1007,7 +1047,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   if (warp == kDqWarpMma) tmem_dealloc(tb, 512);
 }
 
-// dQ buffer (fp32 sums of dS^ K^) times the softmax scale -> output dtype.
+// The fp32 dQ accumulator (sums of dS^ K^ over key tiles) times the softmax
+// scale -> output dtype.
 template <bool OUT_BF16>
 __global__ void dq_convert_kernel(const float* __restrict__ acc, void* out, size_t n4, float scale) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
@@ -1018,11 +1059,114 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, void* out, size
     v.w *= scale;
     if constexpr (OUT_BF16) {
       __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
-      uint2 u = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
-      reinterpret_cast<uint2*>(out)[i] = u;
+      reinterpret_cast<uint2*>(out)[i] = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
     } else {
       reinterpret_cast<float4*>(out)[i] = v;
     }
+  }
+}
+
+// The FP16 dQ accumulator (sums of 2^p dS^ K^ over key tiles) times the
+// softmax scale and 2^-p of its row -> output dtype.  Four values a thread.
+template <bool OUT_BF16>
+__global__ void dq16_convert_kernel(const __half* __restrict__ acc, const int8_t* __restrict__ pexp, void* out,
+                                  size_t n4, float scale, int T, int H, int d4) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t row = i / (size_t)d4;  // (token, head) = (row / H, row % H)
+    const int t = (int)(row / (size_t)H), h = (int)(row - (size_t)t * H);
+    const float f = scale * pow2_127(-(int)__ldg(pexp + (size_t)h * T + t));
+    const uint2 u = reinterpret_cast<const uint2*>(acc)[i];
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    const float4 v = make_float4(a.x * f, a.y * f, b.x * f, b.y * f);
+    if constexpr (OUT_BF16) {
+      __nv_bfloat162 x = __floats2bfloat162_rn(v.x, v.y), y = __floats2bfloat162_rn(v.z, v.w);
+      reinterpret_cast<uint2*>(out)[i] = make_uint2(*reinterpret_cast<uint32_t*>(&x), *reinterpret_cast<uint32_t*>(&y));
+    } else {
+      reinterpret_cast<float4*>(out)[i] = v;
+    }
+  }
+}
+
+// The prescale exponent of every query row's FP16 dQ partials, pexp [H][T]:
+// p_i = 15 - c0 - (edO(i) + MK + MV), clamped to [-126, 127], with MK, MV
+// the largest key and value exponents over the row's document, or over keys
+// j <= i (a running maximum) with the causal dQ scale.  Then every partial
+// sum of 2^p_i dQ_i stays within 2^15 (close reading 4.4; FLAMIA summary §4.5).
+// One CTA per (document, KV head); 256 tokens at a time.
+__global__ void __launch_bounds__(256) dq_prescale_kernel(const AttnParams p) {
+  __shared__ int s_k[8], s_v[8];
+  __shared__ int carry_k, carry_v;
+  const int doc = blockIdx.x, hk = blockIdx.y, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int s0 = __ldg(p.cu + doc), len = __ldg(p.cu + doc + 1) - s0;
+  // an inconsistent cu_seqlens (reported by the plan) touches nothing here
+  if (s0 < 0 || len <= 0 || s0 + len > p.T || p.hdr->n_items == 0) return;
+  const int G = p.H / p.Hkv;
+  const bool prefix = p.causal && p.causal_dq_scale;
+  const uint8_t* ksc = p.k_sc + (size_t)hk * p.T + s0;
+  const uint8_t* vsc = p.v_sc + (size_t)hk * p.T + s0;
+  if (tid == 0) {
+    carry_k = -1000;
+    carry_v = -1000;
+  }
+  __syncthreads();
+  if (!prefix) {  // the document's maxima
+    int mk = -1000, mv = -1000;
+    for (int j = tid; j < len; j += 256) {
+      mk = max(mk, (int)__ldg(ksc + j) - 127);
+      mv = max(mv, (int)__ldg(vsc + j) - 127);
+    }
+    mk = __reduce_max_sync(0xffffffffu, mk);
+    mv = __reduce_max_sync(0xffffffffu, mv);
+    if (lane == 0) {
+      atomicMax(&carry_k, mk);
+      atomicMax(&carry_v, mv);
+    }
+    __syncthreads();
+  }
+  for (int c = 0; c < len; c += 256) {
+    const int j = c + tid;
+    int mk = j < len ? (int)__ldg(ksc + j) - 127 : -1000;
+    int mv = j < len ? (int)__ldg(vsc + j) - 127 : -1000;
+    if (prefix) {  // running maxima: inclusive scan in the warp, then across warps
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int uk = __shfl_up_sync(0xffffffffu, mk, o), uv = __shfl_up_sync(0xffffffffu, mv, o);
+        if (lane >= o) {
+          mk = max(mk, uk);
+          mv = max(mv, uv);
+        }
+      }
+      if (lane == 31) {
+        s_k[wid] = mk;
+        s_v[wid] = mv;
+      }
+      __syncthreads();
+      int pk = carry_k, pv = carry_v;
+      for (int w2 = 0; w2 < wid; ++w2) {
+        pk = max(pk, s_k[w2]);
+        pv = max(pv, s_v[w2]);
+      }
+      mk = max(mk, pk);
+      mv = max(mv, pv);
+      __syncthreads();
+      if (tid == 255) {  // the chunk's last token carries the running maxima on
+        carry_k = mk;
+        carry_v = mv;
+      }
+    } else {
+      mk = carry_k;
+      mv = carry_v;
+    }
+    if (j < len) {
+      for (int g = 0; g < G; ++g) {
+        const int h = hk * G + g;
+        const int edo = (int)__ldg(p.do_sc + (size_t)h * p.T + s0 + j) - 127;
+        const int e = 15 - p.c0 - (edo + mk + mv);
+        p.pexp[(size_t)h * p.T + s0 + j] = (int8_t)(e < -126 ? -126 : (e > 127 ? 127 : e));
+      }
+    }
+    __syncthreads();
   }
 }
 
@@ -1052,27 +1196,42 @@ static cudaError_t launch_bwd_t(const AttnParams& p, const AttnMaps& m, cudaStre
     if (!det) {
       const size_t smem = bwd_smem_bytes<HD, EX, true, false>();
       static_assert(bwd_smem_bytes<HD, EX, true, false>() <= 232448, "shared memory");
-      if ((e = set_smem<bwd_kernel<HD, OB, EX, true, false>>(smem)) != cudaSuccess) return e;
-      if ((e = cudaMemsetAsync(p.dq_acc, 0, sizeof(float) * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
-      if ((e = cudaMemsetAsync(&p.hdr->bwd_counter, 0, sizeof(uint32_t), st)) != cudaSuccess) return e;
-      bwd_kernel<HD, OB, EX, true, false><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.dq, m.q, m.q);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
       const size_t n4 = (size_t)p.T * p.H * HD / 4;
       int cg = (int)((n4 + 255) / 256);
       if (cg > nsm * 8) cg = nsm * 8;
-      if (OB) dq_convert_kernel<true><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4, p.softmax_scale);
-      else dq_convert_kernel<false><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4, p.softmax_scale);
+      if ((e = cudaMemsetAsync(&p.hdr->bwd_counter, 0, sizeof(uint32_t), st)) != cudaSuccess) return e;
+      if (p.dq_fp16) {
+        if ((e = set_smem<bwd_kernel<HD, OB, EX, true, false, true>>(smem)) != cudaSuccess) return e;
+        if ((e = cudaMemsetAsync(p.dq16, 0, 2 * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
+        if (p.n_seq > 0) dq_prescale_kernel<<<dim3(p.n_seq, p.Hkv), 256, 0, st>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        bwd_kernel<HD, OB, EX, true, false, true><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.dq, m.q,
+                                                                                  m.q);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (OB)
+          dq16_convert_kernel<true><<<cg, 256, 0, st>>>(p.dq16, p.pexp, p.dQ, n4, p.softmax_scale, p.T, p.H, HD / 4);
+        else
+          dq16_convert_kernel<false><<<cg, 256, 0, st>>>(p.dq16, p.pexp, p.dQ, n4, p.softmax_scale, p.T, p.H, HD / 4);
+      } else {
+        if ((e = set_smem<bwd_kernel<HD, OB, EX, true, false, false>>(smem)) != cudaSuccess) return e;
+        if ((e = cudaMemsetAsync(p.dq_acc, 0, 4 * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
+        bwd_kernel<HD, OB, EX, true, false, false><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.dq, m.q,
+                                                                                   m.q);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (OB) dq_convert_kernel<true><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4, p.softmax_scale);
+        else dq_convert_kernel<false><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4, p.softmax_scale);
+      }
       return cudaGetLastError();
     }
   }
   const size_t smem = bwd_smem_bytes<HD, EX, false, NV4>();
   static_assert(bwd_smem_bytes<HD, EX, false, NV4>() <= 232448, "shared memory");
   static_assert(dq_smem_bytes<HD, NV4>() <= 232448, "shared memory");
-  if ((e = set_smem<bwd_kernel<HD, OB, EX, false, NV4>>(smem)) != cudaSuccess) return e;
+  if ((e = set_smem<bwd_kernel<HD, OB, EX, false, NV4, false>>(smem)) != cudaSuccess) return e;
   // work counters of the two launches below
   if ((e = cudaMemsetAsync(&p.hdr->bwd_counter, 0, 2 * sizeof(uint32_t), st)) != cudaSuccess) return e;
   // without DQ the dQ map is not read (the q map stands in for the argument)
-  bwd_kernel<HD, OB, EX, false, NV4><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.q, m.qn, m.kn);
+  bwd_kernel<HD, OB, EX, false, NV4, false><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.q, m.qn, m.kn);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t dsm = dq_smem_bytes<HD, NV4>();
   if ((e = set_smem<dq_kernel<HD, OB, EX, NV4>>(dsm)) != cudaSuccess) return e;

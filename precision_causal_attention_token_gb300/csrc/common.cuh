@@ -25,10 +25,7 @@ struct WsHeader {
   uint32_t pad0;
   uint8_t* dbg_phat;       // test hook: P^ codes [H][T][T] (null: off)
   int32_t* dbg_eb;         // test hook: P^ block exponents [H][T][T] at each block's first key
-  uint32_t dbg_withhold;   // test hook: each CTA's producer withholds its first work item
-  uint32_t pad1;
-  uint64_t dbg_wait_ns;    // test hook: bounded-wait limit in ns (0: the default limit)
-  uint32_t pad[48];
+  uint32_t pad[52];
 };
 static_assert(sizeof(WsHeader) == 256, "header");
 
@@ -54,7 +51,9 @@ static __device__ __noinline__ void dbg_dump_phat(uint8_t* dc, int32_t* de, int 
 }
 
 struct WsLayout {
-  size_t header, tile_prefix, blk32_prefix, fwd_items, bwd_items, keys_a, keys_b, dq_acc;
+  size_t header, tile_prefix, blk32_prefix, fwd_items, bwd_items, keys_a, keys_b;
+  size_t dq_acc;           // [T][H][d] dQ accumulator: fp32, or binary16 with dq_fp16
+  size_t pexp;             // int8 [H][T]: the dQ prescale exponent of each query row
   size_t nv_q, nv_k;       // mixed path: bf16 [T][H][d] / [T][Hkv][d], NVFP4 values without the token scale
   size_t total;
   int32_t max_items;       // upper bound of tiles: ceil(T/128) + n_seq
@@ -77,7 +76,8 @@ inline WsLayout ws_layout(const flamia_problem_t& p) {
   L.bwd_items = o; o = align256(o + sizeof(int2) * L.max_items);
   L.keys_a = o; o = align256(o + sizeof(uint64_t) * L.sort_n * 2);
   L.keys_b = o; o = align256(o + sizeof(uint64_t) * L.sort_n * 2);
-  L.dq_acc = o; o = align256(o + sizeof(float) * (size_t)p.T * p.H * p.d);
+  L.dq_acc = o; o = align256(o + (p.dq_fp16 ? 2 : 4) * (size_t)p.T * p.H * p.d);
+  L.pexp = o; o = align256(o + (size_t)p.T * p.H);
   L.nv_q = L.nv_k = 0;
   if (p.path == FLAMIA_PATH_NVFP4_FP8) {
     L.nv_q = o; o = align256(o + 2 * (size_t)p.T * p.H * p.d);
@@ -266,12 +266,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   if (mbar_test_wait(bar, parity)) return true;  // already complete: no suspend
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  const uint64_t test_limit = hdr->dbg_wait_ns;  // a test may shorten the limit
-  const uint64_t limit = test_limit ? test_limit : kWaitLimitNs;
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > limit) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;
       report(hdr, FLAMIA_ERR_TIMEOUT, where);
       return false;
@@ -310,13 +308,16 @@ __device__ __forceinline__ void item_ring_init(ItemRing& r, uint32_t consumers) 
 }
 
 // Producer warp (all lanes): fetch the n-th item of this CTA; -1 when none is left.
+// withhold_first (a test hook, a kernel parameter): the first item is never
+// published, so every consumer's wait for it runs out.
 __device__ __forceinline__ int item_publish(ItemRing& r, uint32_t n, uint32_t* counter, int n_work, int lane,
-                                            volatile int* abort_flag, WsHeader* hdr, uint32_t where, bool& ok) {
+                                            volatile int* abort_flag, WsHeader* hdr, uint32_t where, bool& ok,
+                                            int withhold_first) {
   const int s = (int)(n % kItemRing);
   if (!(ok = mbar_wait_warp(&r.empty[s], ((n / kItemRing) & 1) ^ 1, abort_flag, hdr, where))) return -1;
-  // test hook: the first item is never published, so every consumer's wait
-  // on it runs out; nothing has been issued yet, so the CTA exits cleanly
-  if (n == 0 && *reinterpret_cast<volatile uint32_t*>(&hdr->dbg_withhold) != 0u) return -1;
+  // nothing has been issued yet when the first item is withheld, so the CTA
+  // exits cleanly after its consumers' waits run out
+  if (n == 0 && withhold_first) return -1;
   int w = 0;
   if (lane == 0) {
     w = (int)atomicAdd(counter, 1u);
@@ -365,7 +366,8 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 // Element-wise add of a shared-memory box into global memory through a tensor
-// map (the reduction happens in L2); completion is tracked by bulk groups.
+// map (the element type is the map's; the reduction happens in L2, rows past
+// the tensor's end are clipped); completion is tracked by bulk groups.
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* smem_src, int c0, int c1,
                                                   int c2) {
   asm volatile(

@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     uint32_t kv = 0, qc = 0;
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it) {
-      const int w = item_publish(c.ring, n_it, &hdr->fwd_counter, n_work, lane, abort_flag, hdr, 0x204, ok);
+      const int w = item_publish(c.ring, n_it, &hdr->fwd_counter, n_work, lane, abort_flag, hdr, 0x204, ok, p.dbg_withhold);
       if (w < 0) break;
       const int pair = w / p.H, h = w - pair * p.H, hk = h / G;
       const int2 it = p.fwd_items[pair];

@@ -33,6 +33,7 @@ cudaError_t launch_plan(const flamia_problem_t& p, const WsLayout& L, uint8_t* w
 // Everything the attention kernels need for one call (host-built).
 struct AttnParams {
   int T, H, Hkv, d, n_seq, causal, exact, deterministic, out_bf16, max_items;
+  int dbg_withhold;     // test hook: each CTA's producer withholds its first work item
   float softmax_scale;  // c' (scores)
   float c_log2;         // softmax_scale * log2(e)
   const int32_t* cu;
@@ -51,7 +52,12 @@ struct AttnParams {
   int32_t* m;           // [H][T]
   float* l;             // [H][T]
   void* O;              // [T][H][d]
-  float* dq_acc;        // [T][H][d] fp32
+  float* dq_acc;        // [T][H][d] fp32 dQ accumulator (dq_fp16 = 0)
+  __half* dq16;         // [T][H][d] binary16 dQ accumulator, prescaled FP16 partials (dq_fp16 = 1)
+  int dq_fp16;
+  int8_t* pexp;         // [H][T] dQ prescale exponent of each query row
+  int c0;               // ceil(log2(2.5 d 448^3 softmax_scale)): the constant of the prescale bound
+  int causal_dq_scale;  // 1: the prescale from keys j <= i only (causal); 0: the whole document
   void* dQ;             // [T][H][d]
   void* dK;             // [T][Hkv][d]
   void* dV;             // [T][Hkv][d]
@@ -60,7 +66,8 @@ struct AttnParams {
 struct AttnMaps {
   CUtensorMap q, k, v, dO;
   CUtensorMap qn, kn;  // mixed path: bf16 NVFP4 values, boxes of 128 tokens x 64 values (128B swizzle)
-  CUtensorMap dq;  // fp32 dQ accumulator [T][H][d], boxes of 128 rows x 32 values (reduce-add target)
+  CUtensorMap dq;      // dQ accumulator [T][H][d], the reduce-add target: fp32 boxes of 128 rows x 32
+                       // values, or (dq_fp16) FP16 boxes of 128 rows x 64 values; 128B swizzle
 };
 
 cudaError_t launch_fwd(const AttnParams& p, const AttnMaps& maps, cudaStream_t st);

@@ -35,8 +35,6 @@ __global__ void __launch_bounds__(1024) plan_prefix_kernel(const int32_t* __rest
     hdr->status_where = 0;
     hdr->dbg_phat = nullptr;  // test hooks off unless set after the plan
     hdr->dbg_eb = nullptr;
-    hdr->dbg_withhold = 0u;
-    hdr->dbg_wait_ns = 0ull;
   }
   __syncthreads();
   for (int base = 0; base < n_seq; base += 1024) {

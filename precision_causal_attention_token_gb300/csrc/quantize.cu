@@ -110,16 +110,6 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
     if (t < ntok) raw[t].load(x + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL);
     else raw[t].zero();
   }
-  // dO role: O's rows are loaded up front as well, so their latency overlaps
-  // the exponent work instead of stalling each token's dot product
-  RawRow<TO, WITH_D ? EPL : 2> orow[WITH_D ? 32 : 1];
-  if constexpr (WITH_D) {
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      if (t < ntok) orow[t].load(static_cast<const TO*>(a.O) + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL);
-      else orow[t].zero();
-    }
-  }
   if constexpr (!NVFP4) {
     // MXFP8 codes.  Token-block units: one exponent from the lane maxima and a
     // single warp reduction.  Per-token units (V, exact option): one warp
@@ -136,7 +126,10 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
       e_blk = noclamp_exp_clamped(warp_max(fmaxf(fmaxf(lm[0], lm[1]), fmaxf(lm[2], lm[3]))));
     }
     int my_e = e_blk;  // exponent of token `lane`
-    float dpart[WITH_D ? 32 : 1];
+    // dO role: each token's code word is kept for D, and the dO values die
+    // as the codes are made, so O's rows are read afterwards (below) without
+    // both blocks held in registers at once
+    uint32_t cws[WITH_D ? 32 : 1];
 #pragma unroll
     for (int t = 0; t < 32; ++t) {
       int e_t = e_blk;
@@ -147,7 +140,7 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
         e_t = noclamp_exp_clamped(warp_max(lm));
         if (lane == t) my_e = e_t;
       }
-      if constexpr (WITH_D) dpart[t] = 0.f;
+      if constexpr (WITH_D) cws[t] = 0u;
       if (t < ntok) {
         // 2^-e_t is a normal fp32 for every exponent of finite data (e_t <= 120),
         // so one multiply per element is exact down to the E4M3 range
@@ -164,27 +157,42 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
           cw = pack_e4m3x2(qv[0], qv[1]);
           *reinterpret_cast<uint16_t*>(dst) = (uint16_t)cw;
         }
-        if constexpr (WITH_D) {
-          // D's terms are code * O (products exact in fp32); the exponent is
-          // applied to the lane's partial sum (per token) or to the token's
-          // sum (token block)
+        if constexpr (WITH_D) cws[t] = cw;
+      }
+    }
+    if (lane < ntok) a.scales[(size_t)h * a.T + t0 + lane] = (uint8_t)(my_e + 127);
+    if constexpr (WITH_D) {
+      // D's terms are code * O (products exact in fp32); the exponent is
+      // applied to the lane's partial sum (per token) or to the token's sum
+      // (token block).  O is read eight rows at a time.
+      float dpart[32];
+      const TO* __restrict__ Ob = static_cast<const TO*>(a.O) + (size_t)t0 * row + (size_t)h * HD + lane * EPL;
+#pragma unroll
+      for (int c8 = 0; c8 < 32; c8 += 8) {
+        RawRow<TO, EPL> orow[8];
+#pragma unroll
+        for (int t8 = 0; t8 < 8; ++t8) {
+          if (c8 + t8 < ntok) orow[t8].load(Ob + (size_t)(c8 + t8) * row);
+          else orow[t8].zero();
+        }
+#pragma unroll
+        for (int t8 = 0; t8 < 8; ++t8) {
+          const int t = c8 + t8;
+          const uint32_t cw = cws[t];
           float acc = 0.f;
 #pragma unroll
           for (int e = 0; e < EPL; e += 2) {
             const float2 d2 = unpack_e4m3x2((uint16_t)(cw >> (8 * e)));
-            acc = fmaf(d2.x, orow[t].at(e), acc);
-            acc = fmaf(d2.y, orow[t].at(e + 1), acc);
+            acc = fmaf(d2.x, orow[t8].at(e), acc);
+            acc = fmaf(d2.y, orow[t8].at(e + 1), acc);
           }
           if (a.per_token) {
-            const float2 s2 = pow2_pair(e_t);
+            const float2 s2 = pow2_pair(__shfl_sync(0xffffffffu, my_e, t));
             acc = (acc * s2.x) * s2.y;
           }
           dpart[t] = acc;
         }
       }
-    }
-    if (lane < ntok) a.scales[(size_t)h * a.T + t0 + lane] = (uint8_t)(my_e + 127);
-    if constexpr (WITH_D) {
       float dsum = transpose_reduce<false>(dpart, lane);
       if (!a.per_token) {
         const float2 s2 = pow2_pair(e_blk);
@@ -272,7 +280,7 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
 template <typename TIn, typename TO, bool WITH_D, bool NVFP4>
 constexpr int quant_blocks_per_sm() {
   if constexpr (NVFP4) return 3;
-  else if constexpr (WITH_D) return (sizeof(TIn) == 2 && sizeof(TO) == 2) ? 3 : 2;
+  else if constexpr (WITH_D) return (sizeof(TIn) == 2 && sizeof(TO) == 2) ? 4 : 2;
   else return sizeof(TIn) == 2 ? 5 : 3;
 }
 

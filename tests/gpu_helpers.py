@@ -20,13 +20,13 @@ def to_dev(a: np.ndarray, dtype: str, dev="cuda"):
 
 
 def run_gpu(w, *, causal=True, exact=False, path=fl.PATH_MXFP8, deterministic=False, inputs=None,
-            backward=True, causal_dq_scale=False):
+            backward=True, causal_dq_scale=False, dq_fp16=False):
     dev = torch.device("cuda:0")
     q, k, v, do = inputs if inputs is not None else (w.tensor(n) for n in ("q", "k", "v", "do"))
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
     dt = fl.BF16 if w.dtype == "bf16" else fl.F32
     tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu, causal=causal, exact=exact, path=path, in_dtype=dt,
-                      out_dtype=dt, deterministic=deterministic, causal_dq_scale=causal_dq_scale)
+                      out_dtype=dt, deterministic=deterministic, causal_dq_scale=causal_dq_scale, dq_fp16=dq_fp16)
     tc.plan()
     tc.forward(to_dev(q, w.dtype), to_dev(k, w.dtype), to_dev(v, w.dtype))
     if backward:
@@ -38,10 +38,13 @@ def run_gpu(w, *, causal=True, exact=False, path=fl.PATH_MXFP8, deterministic=Fa
     return tc
 
 
-def run_oracle(w, *, causal=True, exact=False, path=oracle.PATH_MXFP8, inputs=None, backward=True):
+def run_oracle(w, *, causal=True, exact=False, path=oracle.PATH_MXFP8, inputs=None, backward=True,
+               dq_fp16=False, dq_causal_scale=False):
+    """The oracle's call on the same inputs (dq_fp16: FP16 dQ partials with the
+    power-of-two prescale, as the GPU's dq_fp16 option)."""
     q, k, v, do = inputs if inputs is not None else (w.tensor(n) for n in ("q", "k", "v", "do"))
     return oracle.train_call(q, k, v, do if backward else None, w.cu_seqlens, causal=causal, exact=exact,
-                             path=path, out_dtype=w.dtype)
+                             path=path, out_dtype=w.dtype, dq_fp16=dq_fp16, dq_causal_scale=dq_causal_scale)
 
 
 def np_of(t):

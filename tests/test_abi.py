@@ -46,7 +46,11 @@ def _prob(**kw):
 def test_workspace_size_valid_and_invalid(lib):
     p, _ = _prob()
     n = fl.flamia_workspace_size(p)
-    assert n > 228 * 4 * 128 * 4  # holds the fp32 dQ accumulator
+    assert n > 228 * 4 * 128 * 2 + 228 * 4  # holds the FP16 dQ accumulator and the row prescales
+    # the offsets tests read back lie inside the workspace, in layout order
+    offs = [fl.flamia_debug_workspace_offset(p, r) for r in (fl.WS_FWD_ITEMS, fl.WS_BWD_ITEMS, fl.WS_DQ_PRESCALE)]
+    assert 0 < offs[0] < offs[1] < offs[2] and offs[2] + 228 * 4 <= n
+    assert fl.flamia_debug_workspace_offset(p, 99) == 0
     for bad in (dict(d=96), dict(H=3), dict(T=0), dict(Hkv=0)):
         q, _ = _prob(**bad)
         assert fl.flamia_workspace_size(q) == 0, bad
@@ -109,10 +113,10 @@ def test_misaligned_pointers_rejected_before_launch(lib):
         assert st == fl.ERR_INVALID_ARG
 
 
-def test_wait_test_hook_rejects_bad_arguments(lib):
-    assert lib.flamia_debug_set_wait_test(None, 1 << 20, 1000, 1, None) == fl.ERR_INVALID_ARG
-    assert lib.flamia_debug_set_wait_test(1 << 20, 16, 1000, 1, None) == fl.ERR_INVALID_ARG
-    assert lib.flamia_debug_set_wait_test(1 << 20, 1 << 20, 20_000_000_000, 1, None) == fl.ERR_INVALID_ARG
+def test_withhold_hook_is_host_side(lib):
+    # the hook only sets a host-side flag for the next launches (no device call)
+    assert lib.flamia_debug_withhold_first_item(1) == fl.OK
+    assert lib.flamia_debug_withhold_first_item(0) == fl.OK
 
 
 def test_binding_raises_without_library(tmp_path):

@@ -120,13 +120,35 @@ def test_long_gqa_group_of_four_sampled_against_oracle():
         compare(f"{name} doc {doc} kv head {hk}", got, ref[name])
     got = {n: getattr(a, n).clone() for n in ("O", "dQ", "dK", "dV")}
     del a
-    b = run_gpu(w, inputs=(q, k, v, do), causal_dq_scale=True)
-    # with fp32 dQ accumulation the flag changes nothing: O, dK and dV are
-    # bit-identical (fixed-order sums); dQ is summed by reduce-adds whose order
-    # varies from run to run, so it is held to the same oracle bar
+    # FP16 dQ partials with the causal dQ scale: only dQ's reduction changes,
+    # so O, dK and dV stay bit-identical (fixed-order sums); dQ is held to the
+    # oracle's result with the same FP16 partials and prescale rule
+    b = run_gpu(w, inputs=(q, k, v, do), dq_fp16=True, causal_dq_scale=True)
     for n in ("O", "dK", "dV"):
         assert torch.equal(got[n], getattr(b, n)), n
-    compare(f"dQ (causal dQ scale) doc {doc} kv head {hk}", b.dQ[s:e, hk * G:(hk + 1) * G], ref["dQ"])
+    ref_c = oracle.train_call(qs, kv(k), kv(v), dos, np.array([0, e - s], np.int32), out_dtype="bf16",
+                              dq_fp16=True, dq_causal_scale=True)
+    compare(f"dQ (FP16 partials, causal dQ scale) doc {doc} kv head {hk}", b.dQ[s:e, hk * G:(hk + 1) * G],
+            ref_c["dQ"])
+
+
+@pytest.mark.parametrize("causal_dq_scale", [False, True])
+def test_dq_prescale_exponents_bit_exact(causal_dq_scale):
+    """FP16 dQ partials (dq_fp16): the prescale exponent of every query row (an
+    integer from the exponent bytes) equals the oracle's, document-range and
+    causal, and dQ meets the parity bar against the oracle's FP16 reduction."""
+    w = synth.custom([300, 45, 129, 1, 600], H=4, Hkv=2, d=128, seed=715)
+    tc = run_gpu(w, dq_fp16=True, causal_dq_scale=causal_dq_scale)
+    off = fl.flamia_debug_workspace_offset(tc.prob, fl.WS_DQ_PRESCALE)
+    got = tc.ws[off:off + w.H * w.T].view(torch.int8).cpu().numpy().astype(np.int32).reshape(w.H, w.T)
+    ref = run_oracle(w, dq_fp16=True, dq_causal_scale=causal_dq_scale)
+    e = lambda a: a.astype(np.int32) - 127
+    want = oracle.dq_prescales(w.cu_seqlens, e(ref["k_scales"]), e(ref["v_scales"]), e(ref["do_scales"]), w.d,
+                               causal=True, causal_scale=causal_dq_scale)
+    assert np.array_equal(got, want)
+    if causal_dq_scale:  # the running maxima make the exponents vary along a document
+        assert len(np.unique(want[0, :300])) > 1
+    compare("dQ", tc.dQ, ref["dQ"])
 
 
 def _dump_buffers(w):

@@ -1,10 +1,9 @@
 """Failure detection without a GPU fault: every wait inside the attention
-kernels is bounded.  A test hook shortens the limit and makes each CTA's
-producer withhold its first work item, so the other roles' waits for it run
-out.  The kernel must then record FLAMIA_ERR_TIMEOUT in the workspace's
-status word and exit cleanly (tensor memory released, nothing in flight), and
-the context must stay usable: the next normal call returns OK and matches the
-oracle."""
+kernels is bounded (about 2 s).  A test hook makes each CTA's producer
+withhold its first work item, so the other roles' waits for it run out.  The
+kernel must then record FLAMIA_ERR_TIMEOUT in the workspace's status word and
+exit cleanly (tensor memory released, nothing in flight), and the context
+must stay usable: the next normal call returns OK and matches the oracle."""
 import pytest
 import torch
 
@@ -13,8 +12,6 @@ import synth
 from gpu_helpers import compare, run_gpu, run_oracle, to_dev
 
 pytestmark = pytest.mark.gpu
-
-LIMIT_NS = 20_000_000  # 20 ms
 
 
 def _call(w):
@@ -31,9 +28,12 @@ def test_forward_wait_runs_out_and_reports_timeout():
     tc, (q, k, v, do) = _call(w)
     tc.plan()
     fl.flamia_quantize(tc.prob, fl.ROLE_QKV, [q, k, v], None, [tc.opq, tc.opk, tc.opv], None, tc.ws)
-    fl.flamia_debug_set_wait_test(tc.ws, LIMIT_NS, True)
-    fl.flamia_fwd(tc.prob, tc.opq, tc.opk, tc.opv, tc.O, tc.m, tc.l, tc.ws)
-    torch.cuda.synchronize()
+    fl.flamia_debug_withhold_first_item(True)
+    try:
+        fl.flamia_fwd(tc.prob, tc.opq, tc.opk, tc.opv, tc.O, tc.m, tc.l, tc.ws)
+        torch.cuda.synchronize()
+    finally:
+        fl.flamia_debug_withhold_first_item(False)
     assert fl.flamia_get_device_status(tc.ws) == fl.ERR_TIMEOUT
     # the plan clears the status word and the hook; the same workspace then works
     tc.run(q, k, v, do)
@@ -49,24 +49,15 @@ def test_backward_wait_runs_out_and_reports_timeout():
     tc, (q, k, v, do) = _call(w)
     tc.plan()
     tc.forward(q, k, v)
-    fl.flamia_debug_set_wait_test(tc.ws, LIMIT_NS, True)
-    tc.backward(do)
-    torch.cuda.synchronize()
+    fl.flamia_debug_withhold_first_item(True)
+    try:
+        tc.backward(do)
+        torch.cuda.synchronize()
+    finally:
+        fl.flamia_debug_withhold_first_item(False)
     assert fl.flamia_get_device_status(tc.ws) == fl.ERR_TIMEOUT
     # a fresh workspace and call on the same context
     tc2 = run_gpu(w)
     ref = run_oracle(w)
     for name in ("O", "dQ", "dK", "dV"):
         compare(name, getattr(tc2, name), ref[name])
-
-
-def test_short_limit_alone_does_not_fire():
-    """A shortened limit with nothing withheld: a normal call stays OK."""
-    w = synth.custom([300, 45], H=2, d=128, seed=813)
-    tc, (q, k, v, do) = _call(w)
-    tc.plan()
-    fl.flamia_debug_set_wait_test(tc.ws, 200_000_000, False)
-    tc.forward(q, k, v)
-    tc.backward(do)
-    torch.cuda.synchronize()
-    assert fl.flamia_get_device_status(tc.ws) == fl.OK

@@ -278,8 +278,8 @@ def test_leakage_probe_default_option_leaks_within_block():
     q, k, v, do = (w.tensor(n).astype(np.float64) for n in ("q", "k", "v", "do"))
     half = 130
     pert = [_perturb_future(x, half, 8) for x in (q, k, v, do)]
-    a = oracle.train_call(q, k, v, do, w.cu_seqlens, dq_causal_scale=True)
-    b = oracle.train_call(*pert, w.cu_seqlens, dq_causal_scale=True)
+    a = oracle.train_call(q, k, v, do, w.cu_seqlens, dq_fp16=True, dq_causal_scale=True)
+    b = oracle.train_call(*pert, w.cu_seqlens, dq_fp16=True, dq_causal_scale=True)
     diff = np.abs(a["O"][:half + 1] - b["O"][:half + 1]).max()
     assert diff > 0
     # rows before the block that holds the perturbed tokens are untouched
@@ -288,7 +288,7 @@ def test_leakage_probe_default_option_leaks_within_block():
     # without the causal dQ scale the FP16 dQ accumulator's prescale covers the
     # whole document ([SUM] §4.5: the default keeps a sequence-range
     # dependency of the dQ accumulator), so earlier dQ rows change too
-    c = oracle.train_call(q, k, v, do, w.cu_seqlens)
-    d = oracle.train_call(*pert, w.cu_seqlens)
+    c = oracle.train_call(q, k, v, do, w.cu_seqlens, dq_fp16=True)
+    d = oracle.train_call(*pert, w.cu_seqlens, dq_fp16=True)
     assert (c["O"][:128] == d["O"][:128]).all()
     assert not (c["dQ"][:128] == d["dQ"][:128]).all()
