@@ -40,7 +40,8 @@ class _Cfg(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("Hkv", ctypes.c_int), ("d", ctypes.c_int),
                 ("nseq", ctypes.c_int), ("causal", ctypes.c_int), ("softmax_scale", ctypes.c_double),
                 ("quant_p", ctypes.c_int), ("quant_ds", ctypes.c_int), ("quant_pt", ctypes.c_int),
-                ("exact", ctypes.c_int), ("out_round", ctypes.c_int), ("dq_fp16", ctypes.c_int),
+                ("exact", ctypes.c_int), ("out_round", ctypes.c_int), ("bitexp", ctypes.c_int),
+                ("dq_fp16", ctypes.c_int),
                 ("dq_causal_scale", ctypes.c_int)]
 
 
@@ -60,6 +61,7 @@ def lib():
             L.orc_scale_exponent.restype, L.orc_scale_exponent.argtypes = i, [d]
             L.orc_round_bf16.restype, L.orc_round_bf16.argtypes = d, [d]
             L.orc_round_f16.restype, L.orc_round_f16.argtypes = d, [d]
+            L.orc_bitexp2.restype, L.orc_bitexp2.argtypes = d, [d]
             L.orc_dq_prescale_c0.restype, L.orc_dq_prescale_c0.argtypes = i, [i, d]
             L.orc_dq_prescale.restype, L.orc_dq_prescale.argtypes = i, [i, i, i, i]
             L.orc_dq_prescales.restype = None
@@ -147,6 +149,11 @@ def scale_exponent(amax: float) -> int:
 
 def round_bf16(x: float) -> float:
     return lib().orc_round_bf16(float(x))
+
+
+def bitexp2(z: float) -> float:
+    """The bit-level approximation of 2^z (bf16 bit field, zero-mean shift)."""
+    return lib().orc_bitexp2(float(z))
 
 
 def round_f16(x: float) -> float:
@@ -240,7 +247,7 @@ def compute_D(dOq, O_stored) -> np.ndarray:
 # --------------------------------------------------------------------------- attention
 def attention(cu_seqlens, Q, K, V, dO=None, *, Qs=None, Ks=None, eQ=None, eK=None, eV=None, edO=None,
               causal=True, softmax_scale=None, quant_p=True, quant_ds=True, quant_pt=True, exact=False,
-              out_round=0, dq_fp16=False, dq_causal_scale=False):
+              out_round=0, dq_fp16=False, dq_causal_scale=False, bitexp=False):
     """Attention forward (+ backward when dO is given) in fp64.
 
     Q [T][H][d], K/V [T][Hkv][d], dO [T][H][d] are operand values (dequantized
@@ -260,7 +267,7 @@ def attention(cu_seqlens, Q, K, V, dO=None, *, Qs=None, Ks=None, eQ=None, eK=Non
     edO = z(H) if edO is None else np.ascontiguousarray(edO, dtype=np.int32)
     cfg = _Cfg(T, H, Hkv, d, len(cu) - 1, int(causal),
                float(softmax_scale if softmax_scale is not None else 1.0 / np.sqrt(d)),
-               int(quant_p), int(quant_ds), int(quant_pt), int(exact), int(out_round), int(dq_fp16),
+               int(quant_p), int(quant_ds), int(quant_pt), int(exact), int(out_round), int(bitexp), int(dq_fp16),
                int(dq_causal_scale))
     O = np.empty((T, H, d), np.float64)
     lse2 = np.empty((H, T), np.float64)
@@ -278,7 +285,7 @@ def attention(cu_seqlens, Q, K, V, dO=None, *, Qs=None, Ks=None, eQ=None, eK=Non
 
 
 def train_call(q, k, v, do, cu_seqlens, *, causal=True, exact=False, path=PATH_MXFP8, out_dtype="bf16",
-               softmax_scale=None, quantize=True, dq_fp16=False, dq_causal_scale=False):
+               softmax_scale=None, quantize=True, dq_fp16=False, dq_causal_scale=False, bitexp=False):
     """The whole training call from raw inputs: quantize Q/K/V, forward, quantize
     dO (+ D), backward.  Inputs are fp32 arrays whose values are the exact inputs
     (bf16-exact for bf16 workloads).  Returns a dict with every intermediate
@@ -288,7 +295,10 @@ def train_call(q, k, v, do, cu_seqlens, *, causal=True, exact=False, path=PATH_M
     dq_fp16: dQ partials per 128-key tile in FP16 with a power-of-two row
     prescale (the pages' FP16 reduction); False sums dQ in fp64.
     dq_causal_scale: the prescale from keys j <= i only.
+    bitexp: the inference forward with bit-level exponentials (no backward).
     """
+    if bitexp and do is not None:
+        raise ValueError("the bit-level exponential forward is for inference: no backward")
     cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do) if do is not None else None
     out_round = {"bf16": 1, "f32": 2, "f64": 0}[out_dtype]
@@ -319,6 +329,6 @@ def train_call(q, k, v, do, cu_seqlens, *, causal=True, exact=False, path=PATH_M
     r = attention(cu, Qh, Kh, Vh, dOh, Qs=Qs_, Ks=Ks_, eQ=qs.astype(np.int32) - 127,
                   eK=ks.astype(np.int32) - 127, eV=vs.astype(np.int32) - 127, edO=edO, causal=causal,
                   softmax_scale=softmax_scale, exact=exact, out_round=out_round,
-                  dq_fp16=dq_fp16 and do is not None, dq_causal_scale=dq_causal_scale)
+                  dq_fp16=dq_fp16 and do is not None, dq_causal_scale=dq_causal_scale, bitexp=bitexp)
     res.update(r)
     return res

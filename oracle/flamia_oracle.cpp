@@ -156,6 +156,24 @@ double orc_round_f16(double x) {
   return std::copysign(std::ldexp(q, step), x);
 }
 
+// Bit-level exponential for inference ([SUM] §3.7 and §4.4; [READ] 4.5: the
+// Schraudolph variant for the 8-bit P^ evaluates the piecewise-linear
+// 2^floor(z) (1 + frac(z)) in the bf16 bit field, written there by a fused
+// multiply-add as a fixed-point number, with a shift that makes its error
+// zero-mean).  Reading: the bf16 pattern is n = RNE(128 z) + 128 * 127 - 7,
+// i.e. the fraction rounded to 7 bits and moved down by 7 units of the last
+// place: the mean of log2((1 + f) / 2^f) over f in [0, 1) is
+// 2 - 1/ln 2 - 1/2 = 0.0573, or 7.3 such units.  z is first raised to
+// z_lo = -126.9453125, where n = 0, so z <= z_lo gives exactly 0 and n never
+// goes negative.
+double orc_bitexp2(double z) {
+  const double z_lo = -126.9453125;
+  if (!(z > z_lo)) z = z_lo;  // also -inf and NaN
+  const long n = (long)std::nearbyint(128.0 * z) + 128L * 127 - 7;  // RNE: the default mode
+  const int e = (int)(n >> 7), mant = (int)(n & 127);
+  return e == 0 ? std::ldexp((double)mant, -133) : std::ldexp(128.0 + mant, e - 134);
+}
+
 // ---------------------------------------------------------------------------
 // Quantizers.
 // ---------------------------------------------------------------------------
@@ -283,6 +301,7 @@ struct orc_attn_cfg {
   int quant_pt;          // quantize the dV operand P~ in 32x32 blocks
   int exact;             // exact option: per-row dS exponents for dQ ([SUM] §4.5)
   int out_round;         // O as stored: 0 kept in fp64, 1 rounded to bf16, 2 to fp32
+  int bitexp;            // inference: 2^z by the bit-level approximation on 5 of every 8 key pairs
   int dq_fp16;           // dQ partials of each 128-key tile in FP16 with a row prescale
   int dq_causal_scale;   // the prescale from keys j <= i only (else the whole document)
 };
@@ -436,8 +455,34 @@ void orc_attention(const orc_attn_cfg* cfg, const int* cu, const double* Qs, con
         double li = 0.0;
         for (int j = 0; j < L; ++j)
           if (vis[(size_t)i * L + j]) li += std::exp2(x[(size_t)i * L + j] - m[i]);
+        if (cfg->bitexp) {
+          // Inference forward with bit-level exponentials ([SUM] §3.7): in
+          // each (row, 32-key block), z = y - E with E = ceil(max y - log2 448)
+          // (the block's P^ exponent); keys of pairs 0-4 of every 8 pairs take
+          // orc_bitexp2(z), pairs 5-7 the exact 2^z (reading of "five of every
+          // eight pairs").  P^ codes come from these values and the normaliser
+          // is their sum, l = sum_j p~_ij 2^(E - eV(j) - m).
+          li = 0.0;
+          for (int b = 0; b < L; b += 32) {
+            double ymax = -INFINITY;
+            for (int j = b; j < std::min(b + 32, L); ++j)
+              if (vis[(size_t)i * L + j])
+                ymax = std::max(ymax, x[(size_t)i * L + j] + eV[(size_t)hk * T + s0 + j]);
+            const int E = (int)std::ceil(ymax - std::log2(448.0));
+            for (int j = b; j < std::min(b + 32, L); ++j) {
+              double& p = P[(size_t)i * L + j];
+              if (!vis[(size_t)i * L + j]) { p = 0.0; continue; }
+              const int ev = eV[(size_t)hk * T + s0 + j];
+              const double z = x[(size_t)i * L + j] + ev - E;
+              const double pt = (((j - b) / 2) % 8 < 5) ? orc_bitexp2(z) : std::exp2(z);
+              li += std::ldexp(pt, E - ev - m[i]);
+              const double q = cfg->quant_p ? orc_e4m3_decode(orc_e4m3_encode(pt)) : pt;
+              p = std::ldexp(q, E - m[i]);
+            }
+          }
+        }
         l[i] = li;
-        for (int b = 0; b < L; b += 32) {
+        for (int b = 0; !cfg->bitexp && b < L; b += 32) {
           std::vector<double*> blk;
           for (int j = b; j < std::min(b + 32, L); ++j) {
             double& p = P[(size_t)i * L + j];
