@@ -402,6 +402,35 @@ def _option_overheads(fl, w, inputs, dev, stream, base_bwd_ms, steps):
     return out
 
 
+def _bitexp_forward(fl, w, inputs, dev, stream, steps):
+    """Forward kernel time of the inference forward with bit-level
+    exponentials against the default forward, both launched back to back on
+    the same quantized operands (the quantizer is not timed)."""
+    import torch
+    q, k, v, _ = inputs
+    cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
+    out = {}
+    for name, kw in (("default", {}), ("bitexp", {"bitexp": True})):
+        tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu, **kw)
+        tc.plan(stream)
+        tc.forward(q, k, v, stream)
+        for _ in range(2):
+            fl.flamia_fwd(tc.prob, tc.opq, tc.opk, tc.opv, tc.O, tc.m, tc.l, tc.ws, stream)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record(stream)
+        for i in range(steps):
+            fl.flamia_fwd(tc.prob, tc.opq, tc.opk, tc.opv, tc.O, tc.m, tc.l, tc.ws, stream)
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        st = fl.flamia_get_device_status(tc.ws)
+        if st != fl.OK:
+            raise RuntimeError(f"{name} forward: {fl.status_string(st)}")
+        out[name] = {"fwd_ms": float(np.mean([ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]))}
+        del tc
+    out["speedup"] = out["default"]["fwd_ms"] / out["bitexp"]["fwd_ms"]
+    return out
+
+
 def run_ours(a):
     import torch
     import precision_causal_attention_token_gb300 as fl
@@ -506,6 +535,7 @@ def run_ours(a):
     if rank == 0 and a.workload == 2 and a.rows == 4 and not a.no_secondary:
         del graph
         extra["option_overheads"] = _option_overheads(fl, w, (q, k, v, do), dev, stream, bwd_ms, max(3, a.steps // 4))
+        extra["bitexp_inference_forward"] = _bitexp_forward(fl, w, (q, k, v, do), dev, stream, max(3, a.steps // 4))
         del tc
         torch.cuda.empty_cache()
         extra["workloads"] = {f"{i}": _secondary(fl, i, dev, stream, max(3, a.steps // 4)) for i in (3, 5)}

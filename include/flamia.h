@@ -94,6 +94,17 @@ typedef enum { FLAMIA_ROLE_QKV = 0, FLAMIA_ROLE_DO = 1 } flamia_role_t;
  *   path         flamia_path_t.
  *   in_dtype     dtype of Q, K, V, dO, O inputs (FLAMIA_BF16 or FLAMIA_F32).
  *   out_dtype    dtype of O, dQ, dK, dV outputs.
+ *   bitexp       1: inference forward with bit-level exponentials ([SUM] §3.7
+ *                Bit-Level Exponentials for Inference, §4.4): on key pairs 0-4
+ *                of every 8 in each 32-key block, 2^z is the bf16 bit-field
+ *                approximation 2^floor(z) (1 + frac z), fraction rounded to 7
+ *                bits, with a zero-mean shift of 7 units (pattern
+ *                RNE(128 z) + 16249, 0 for z <= -126.9453125); the other
+ *                pairs use the hardware exponential.  l sums the same values.
+ *                MXFP8 path, default option only (else
+ *                FLAMIA_ERR_UNSUPPORTED); flamia_bwd rejects it
+ *                (FLAMIA_ERR_UNSUPPORTED): the backward must rebuild the
+ *                forward's P^ exactly.
  */
 typedef struct {
   int32_t T, H, Hkv, d, n_seq;
@@ -102,6 +113,7 @@ typedef struct {
   float softmax_scale;
   int32_t path, in_dtype, out_dtype;
   int32_t dq_fp16;
+  int32_t bitexp;
 } flamia_problem_t;
 
 /* A quantized operand (device pointers, caller-owned).

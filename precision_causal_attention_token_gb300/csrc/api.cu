@@ -28,6 +28,7 @@ flamia_status_t validate(const flamia_problem_t* p) {
   if (p->T > (1 << 30) || p->n_seq > p->T + 1) return FLAMIA_ERR_INVALID_ARG;
   if (p->path != FLAMIA_PATH_MXFP8 && p->path != FLAMIA_PATH_NVFP4_FP8) return FLAMIA_ERR_UNSUPPORTED;
   if (p->path == FLAMIA_PATH_NVFP4_FP8 && p->exact) return FLAMIA_ERR_UNSUPPORTED;
+  if (p->bitexp && (p->path != FLAMIA_PATH_MXFP8 || p->exact)) return FLAMIA_ERR_UNSUPPORTED;
   if ((p->in_dtype != FLAMIA_F32 && p->in_dtype != FLAMIA_BF16) ||
       (p->out_dtype != FLAMIA_F32 && p->out_dtype != FLAMIA_BF16))
     return FLAMIA_ERR_UNSUPPORTED;
@@ -245,6 +246,7 @@ static flamia_status_t fill_params(const flamia_problem_t* p, const WsLayout& L,
   a->c0 = dq_prescale_c0(p->d, a->softmax_scale);
   a->causal_dq_scale = p->causal_dq_scale ? 1 : 0;
   a->nvfp4 = p->path == FLAMIA_PATH_NVFP4_FP8 ? 1 : 0;
+  a->bitexp = p->bitexp ? 1 : 0;
   a->dbg_withhold = g_dbg_withhold.load();
   return FLAMIA_OK;
 }
@@ -292,6 +294,9 @@ flamia_status_t flamia_bwd(const flamia_problem_t* p, const flamia_operand_t* q,
                            cudaStream_t stream) {
   flamia_status_t s = validate(p);
   if (s != FLAMIA_OK) return s;
+  // the bit-level exponential forward is for inference: the backward cannot
+  // rebuild its P^ ([SUM] §3.7)
+  if (p->bitexp) return FLAMIA_ERR_UNSUPPORTED;
   WsLayout L;
   if ((s = check_ws(p, ws, ws_bytes, &L)) != FLAMIA_OK) return s;
   if (!operand_ok(q) || !operand_ok(k) || !operand_ok(v) || !operand_ok(dO) || !D || !m || !l || !dQ || !dK ||

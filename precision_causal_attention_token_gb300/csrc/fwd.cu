@@ -75,9 +75,33 @@ __device__ __forceinline__ uint64_t desc_mnmajor(const uint8_t* tile, uint32_t b
   return smem_desc(smem_u32(tile) + byte_off, 8 * row_bytes, 8 * row_bytes, row_bytes == 128 ? kSwz128 : kSwz64);
 }
 
+// 2^z by the bit-level approximation (FLAMIA summary, §3.7 Bit-Level
+// Exponentials for Inference): one fused multiply-add writes 128 z + 16249
+// as an integer n into the low mantissa bits of a float in [2^23, 2^24)
+// (1.5 * 2^23 + 16249 = 12599161; the float's bits are 0x4B400000 + n and
+// the ulp there is 1, so n is 128 z + 16249 rounded to nearest even), and a
+// 16-bit shift moves n into the bf16 half of an fp32: exponent n >> 7,
+// mantissa n & 127, i.e. 2^floor(z) (1 + frac z) with the fraction rounded to
+// 7 bits and taken 7 units down (zero mean error).  z is first raised to
+// -126.9453125, where n = 0, so n stays in [0, 17376] (z <= log2 448 in a
+// P^ block) and -inf, NaN and the underflow give +0.
+__device__ __forceinline__ float bitexp2(float z) {
+  const float f = __fmaf_rn(fmaxf(z, -126.9453125f), 128.f, 12599161.f);
+  return __uint_as_float(__float_as_uint(f) << 16);
+}
+// phat_values2 with the bit-level exponential: p = bitexp2(y - E).
+__device__ __forceinline__ void phat_bitexp2(float y0, float y1, uint64_t nE2, float& p0, float& p1) {
+  float d0, d1;
+  f2_unpack(f2_add(f2_pack(y0, y1), nE2), d0, d1);
+  p0 = bitexp2(d0);
+  p1 = bitexp2(d1);
+}
+
 // NV4: the mixed path (scores from the NVFP4 payload, bf16 operand tiles,
 // per-token fp32 factors g_Q(i) g_K(j) applied with the softmax scale).
-template <int HD, bool OUT_BF16, bool EXACT, bool NV4>
+// BX: the inference forward with bit-level exponentials on key pairs 0-4 of
+// every 8 in a 32-key block (the other pairs keep ex2); MXFP8 default option.
+template <int HD, bool OUT_BF16, bool EXACT, bool NV4, bool BX>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_qn,
@@ -315,8 +339,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int q4 = 0; q4 < 8; ++q4) {
           const float4 v4 = *reinterpret_cast<const float4*>(vi + 4 * q4);
           float pv[4];  // 0 on an empty block (y = -inf)
-          phat_values2(y[4 * q4], y[4 * q4 + 1], nE2, pv[0], pv[1]);
-          phat_values2(y[4 * q4 + 2], y[4 * q4 + 3], nE2, pv[2], pv[3]);
+          // key pairs 2 q4 and 2 q4 + 1 of the block; with BX the pairs
+          // whose index mod 8 is below 5 take the bit-level exponential
+          if (BX && (2 * q4) % 8 < 5)
+            phat_bitexp2(y[4 * q4], y[4 * q4 + 1], nE2, pv[0], pv[1]);
+          else
+            phat_values2(y[4 * q4], y[4 * q4 + 1], nE2, pv[0], pv[1]);
+          if (BX && (2 * q4 + 1) % 8 < 5)
+            phat_bitexp2(y[4 * q4 + 2], y[4 * q4 + 3], nE2, pv[2], pv[3]);
+          else
+            phat_values2(y[4 * q4 + 2], y[4 * q4 + 3], nE2, pv[2], pv[3]);
           l2[0] = f2_fma(f2_pack(pv[0], pv[1]), f2_pack(v4.x, v4.y), l2[0]);
           l2[1] = f2_fma(f2_pack(pv[2], pv[3]), f2_pack(v4.z, v4.w), l2[1]);
           codes[q4] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
@@ -482,7 +514,7 @@ static int num_sms() {
   return n;
 }
 
-template <int HD, bool OB, bool EX, bool NV4>
+template <int HD, bool OB, bool EX, bool NV4, bool BX = false>
 static cudaError_t launch_fwd_t(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
   const size_t smem = fwd_smem_bytes<HD, NV4>();
   static_assert(fwd_smem_bytes<HD, NV4>() <= 232448, "shared memory");
@@ -491,7 +523,7 @@ static cudaError_t launch_fwd_t(const AttnParams& p, const AttnMaps& m, cudaStre
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   if (!attr_set[dev]) {
     cudaError_t e =
-        cudaFuncSetAttribute(fwd_kernel<HD, OB, EX, NV4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(fwd_kernel<HD, OB, EX, NV4, BX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -499,15 +531,17 @@ static cudaError_t launch_fwd_t(const AttnParams& p, const AttnMaps& m, cudaStre
   int grid = (int)(work < num_sms() ? work : num_sms());
   cudaError_t e = cudaMemsetAsync(&p.hdr->fwd_counter, 0, sizeof(uint32_t), st);  // work counter of this launch
   if (e != cudaSuccess) return e;
-  fwd_kernel<HD, OB, EX, NV4><<<grid, kFwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.qn, m.kn);
+  fwd_kernel<HD, OB, EX, NV4, BX><<<grid, kFwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.qn, m.kn);
   return cudaGetLastError();
 }
 
 template <int HD, bool OB, bool EX>
 static cudaError_t launch_fwd_n(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
-  if constexpr (EX) {  // the exact option is not offered on the mixed path (the host rejects it)
-    return p.nvfp4 ? cudaErrorNotSupported : launch_fwd_t<HD, OB, EX, false>(p, m, st);
+  if constexpr (EX) {  // neither the mixed path nor bitexp has the exact option (the host rejects both)
+    return (p.nvfp4 || p.bitexp) ? cudaErrorNotSupported : launch_fwd_t<HD, OB, EX, false>(p, m, st);
   } else {
+    if (p.bitexp)  // MXFP8 only (the host rejects it on the mixed path)
+      return p.nvfp4 ? cudaErrorNotSupported : launch_fwd_t<HD, OB, EX, false, true>(p, m, st);
     return p.nvfp4 ? launch_fwd_t<HD, OB, EX, true>(p, m, st) : launch_fwd_t<HD, OB, EX, false>(p, m, st);
   }
 }

@@ -48,6 +48,7 @@ struct AttnParams {
   const float* q_g;     // mixed path: per-token fp32 scale of Q's NVFP4 payload [H][T]
   const float* k_g;     // mixed path: of K's [Hkv][T]
   int nvfp4;            // 1: scores from the NVFP4 payload (bf16 operands in the workspace)
+  int bitexp;           // 1: forward with bit-level exponentials (inference only)
   const float* D;       // [H][T]
   int32_t* m;           // [H][T]
   float* l;             // [H][T]

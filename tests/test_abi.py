@@ -129,3 +129,22 @@ def test_binding_raises_without_library(tmp_path):
             mod.load_library(str(tmp_path / "missing.so"))
     finally:
         mod._lib = saved
+
+
+def test_bitexp_is_inference_only(lib):
+    """The bit-level exponential forward ([SUM] §3.7) is offered on the MXFP8
+    default option only, and flamia_bwd refuses it on the host (its P^ cannot
+    be rebuilt by the backward).  No pointer below is dereferenced."""
+    p, _ = _prob()
+    p.bitexp = 1
+    assert fl.flamia_workspace_size(p) > 0
+    for field, val in (("exact", 1), ("path", fl.PATH_NVFP4_FP8)):
+        q, _ = _prob()
+        q.bitexp = 1
+        setattr(q, field, val)
+        assert fl.flamia_workspace_size(q) == 0, field
+    good = lambda: fl.Operand(0x10000, 0x20000, None, None, None)
+    ops = [good() for _ in range(4)]
+    st = lib.flamia_bwd(p, ops[0], ops[1], ops[2], ops[3], 0x60000, 0x40000, 0x50000, 0x70000, 0x80000, 0x90000,
+                        1 << 20, 1 << 40, None)
+    assert st == fl.ERR_UNSUPPORTED
