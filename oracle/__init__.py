@@ -62,6 +62,7 @@ def lib():
             L.orc_round_bf16.restype, L.orc_round_bf16.argtypes = d, [d]
             L.orc_round_f16.restype, L.orc_round_f16.argtypes = d, [d]
             L.orc_bitexp2.restype, L.orc_bitexp2.argtypes = d, [d]
+            L.orc_fwht_f32.restype, L.orc_fwht_f32.argtypes = None, [ctypes.c_void_p, i, i]
             L.orc_dq_prescale_c0.restype, L.orc_dq_prescale_c0.argtypes = i, [i, d]
             L.orc_dq_prescale.restype, L.orc_dq_prescale.argtypes = i, [i, i, i, i]
             L.orc_dq_prescales.restype = None
@@ -154,6 +155,24 @@ def round_bf16(x: float) -> float:
 def bitexp2(z: float) -> float:
     """The bit-level approximation of 2^z (bf16 bit field, zero-mean shift)."""
     return lib().orc_bitexp2(float(z))
+
+
+def fwht_f32(x) -> np.ndarray:
+    """Hadamard rotation x -> x H_d of every d-vector along the last axis, in
+    fp32 by the fast Walsh-Hadamard transform (unnormalised).  Returns the
+    fp32 results as float64."""
+    a = np.ascontiguousarray(x, dtype=np.float32).copy()
+    d = a.shape[-1]
+    lib().orc_fwht_f32(a.ctypes.data, int(a.size // d), int(d))
+    return a.astype(np.float64)
+
+
+def sylvester(d: int) -> np.ndarray:
+    """The Sylvester Hadamard matrix H_d (entries +-1) from its recursion."""
+    h = np.ones((1, 1))
+    while h.shape[0] < d:
+        h = np.block([[h, h], [h, -h]])
+    return h
 
 
 def round_f16(x: float) -> float:
@@ -285,7 +304,8 @@ def attention(cu_seqlens, Q, K, V, dO=None, *, Qs=None, Ks=None, eQ=None, eK=Non
 
 
 def train_call(q, k, v, do, cu_seqlens, *, causal=True, exact=False, path=PATH_MXFP8, out_dtype="bf16",
-               softmax_scale=None, quantize=True, dq_fp16=False, dq_causal_scale=False, bitexp=False):
+               softmax_scale=None, quantize=True, dq_fp16=False, dq_causal_scale=False, bitexp=False,
+               hadamard=False):
     """The whole training call from raw inputs: quantize Q/K/V, forward, quantize
     dO (+ D), backward.  Inputs are fp32 arrays whose values are the exact inputs
     (bf16-exact for bf16 workloads).  Returns a dict with every intermediate
@@ -296,6 +316,8 @@ def train_call(q, k, v, do, cu_seqlens, *, causal=True, exact=False, path=PATH_M
     prescale (the pages' FP16 reduction); False sums dQ in fp64.
     dq_causal_scale: the prescale from keys j <= i only.
     bitexp: the inference forward with bit-level exponentials (no backward).
+    hadamard: Q and K rotated by H_d before quantization (fwht_f32), the
+    softmax scale divided by d, and dQ, dK rotated back (x H_d, fp64).
     """
     if bitexp and do is not None:
         raise ValueError("the bit-level exponential forward is for inference: no backward")
@@ -303,10 +325,22 @@ def train_call(q, k, v, do, cu_seqlens, *, causal=True, exact=False, path=PATH_M
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do) if do is not None else None
     out_round = {"bf16": 1, "f32": 2, "f64": 0}[out_dtype]
     res: dict = {}
+    Hd = None
+    if hadamard:
+        if path == PATH_NVFP4_FP8:
+            raise ValueError("the Hadamard rotation is offered on the MXFP8 path")
+        d = q.shape[-1]
+        Hd = sylvester(d)
+        softmax_scale = (softmax_scale if softmax_scale else 1.0 / np.sqrt(d)) / d
+        # unquantized: the plain definition in fp64; quantized: the fp32
+        # rotation the codes are decided from
+        q, k = (q @ Hd, k @ Hd) if not quantize else (fwht_f32(q), fwht_f32(k))
     if not quantize:
         r = attention(cu, q, k, v, do, causal=causal, softmax_scale=softmax_scale, quant_p=False,
                       quant_ds=False, quant_pt=False, exact=exact, out_round=0)
         res.update(r)
+        if Hd is not None and do is not None:
+            res["dQ"], res["dK"] = r["dQ"] @ Hd, r["dK"] @ Hd
         return res
     blk = 1 if exact else 32
     qc, qs = quantize_blocks(q, cu, blk)
@@ -331,4 +365,6 @@ def train_call(q, k, v, do, cu_seqlens, *, causal=True, exact=False, path=PATH_M
                   softmax_scale=softmax_scale, exact=exact, out_round=out_round,
                   dq_fp16=dq_fp16 and do is not None, dq_causal_scale=dq_causal_scale, bitexp=bitexp)
     res.update(r)
+    if Hd is not None and do is not None:
+        res["dQ"], res["dK"] = r["dQ"] @ Hd, r["dK"] @ Hd
     return res

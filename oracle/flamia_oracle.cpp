@@ -174,6 +174,31 @@ double orc_bitexp2(double z) {
   return e == 0 ? std::ldexp((double)mant, -133) : std::ldexp(128.0 + mant, e - 134);
 }
 
+// Hadamard rotation of Q and K before quantization ([SUM] abstract and §4.3
+// Ablation Study: the fused quantizer applies a Hadamard rotation; [READ] 四
+// 4.4, fused quantization: QuIP-style incoherence processing mixes the
+// head-dimension channels to spread outliers, and an orthogonal transform
+// keeps the dot products).  Reading: the Sylvester matrix H_d (entries +-1,
+// H_2n = [[H_n, H_n], [H_n, -H_n]]), unnormalised, applied to each token's
+// d-vector (x -> x H_d); the 1/d of H_d H_d = d I goes into the softmax scale.
+// The rotated values are what gets quantized, so they are formed in fp32, the
+// precision the kernel decides the codes in, by the fast Walsh-Hadamard
+// transform: stages h = 1, 2, 4, ..., d/2, each replacing the pair
+// (x[i], x[i + h]) (i with bit h clear) by (x[i] + x[i + h], x[i] - x[i + h]),
+// every sum rounded to fp32.  x: n rows of d floats, in place.
+void orc_fwht_f32(float* x, int n, int d) {
+  for (int r = 0; r < n; ++r) {
+    float* v = x + (size_t)r * d;
+    for (int h = 1; h < d; h <<= 1)
+      for (int i = 0; i < d; ++i)
+        if ((i & h) == 0) {
+          const float a = v[i], b = v[i + h];
+          v[i] = a + b;
+          v[i + h] = a - b;
+        }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Quantizers.
 // ---------------------------------------------------------------------------
