@@ -105,6 +105,18 @@ typedef enum { FLAMIA_ROLE_QKV = 0, FLAMIA_ROLE_DO = 1 } flamia_role_t;
  *                FLAMIA_ERR_UNSUPPORTED); flamia_bwd rejects it
  *                (FLAMIA_ERR_UNSUPPORTED): the backward must rebuild the
  *                forward's P^ exactly.
+ *   hadamard     1: Q and K are rotated by the Sylvester Hadamard matrix H_d
+ *                (entries +-1) before quantization ([SUM] §4.3 Ablation Study
+ *                and abstract: the fused quantizer's Hadamard rotation;
+ *                [READ] 四 4.4: it spreads outlier channels and keeps dot
+ *                products).  The rotated values are formed in fp32 by the
+ *                fast Walsh-Hadamard transform (stages h = 1, 2, ..., d/2)
+ *                inside flamia_quantize, the 1/d of H_d H_d = d I is folded
+ *                into the softmax scale, and flamia_bwd rotates dQ and dK
+ *                back, so O, dQ, dK, dV keep their meaning.  The Q/K payloads
+ *                hold rotated codes.  MXFP8 path only (else
+ *                FLAMIA_ERR_UNSUPPORTED); the workspace grows by
+ *                4 T Hkv d bytes.
  */
 typedef struct {
   int32_t T, H, Hkv, d, n_seq;
@@ -114,6 +126,7 @@ typedef struct {
   int32_t path, in_dtype, out_dtype;
   int32_t dq_fp16;
   int32_t bitexp;
+  int32_t hadamard;
 } flamia_problem_t;
 
 /* A quantized operand (device pointers, caller-owned).

@@ -29,6 +29,7 @@ flamia_status_t validate(const flamia_problem_t* p) {
   if (p->path != FLAMIA_PATH_MXFP8 && p->path != FLAMIA_PATH_NVFP4_FP8) return FLAMIA_ERR_UNSUPPORTED;
   if (p->path == FLAMIA_PATH_NVFP4_FP8 && p->exact) return FLAMIA_ERR_UNSUPPORTED;
   if (p->bitexp && (p->path != FLAMIA_PATH_MXFP8 || p->exact)) return FLAMIA_ERR_UNSUPPORTED;
+  if (p->hadamard && p->path != FLAMIA_PATH_MXFP8) return FLAMIA_ERR_UNSUPPORTED;
   if ((p->in_dtype != FLAMIA_F32 && p->in_dtype != FLAMIA_BF16) ||
       (p->out_dtype != FLAMIA_F32 && p->out_dtype != FLAMIA_BF16))
     return FLAMIA_ERR_UNSUPPORTED;
@@ -44,8 +45,12 @@ flamia_status_t check_ws(const flamia_problem_t* p, void* ws, size_t ws_bytes, W
   return FLAMIA_OK;
 }
 
+// The scale the kernels apply to the scores: with the Hadamard rotation the
+// rotated dot products are d times the originals (H_d H_d = d I), so 1/d
+// (a power of two) joins the softmax scale.
 float softmax_scale_of(const flamia_problem_t* p) {
-  return p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / std::sqrt((float)p->d);
+  const float s = p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / std::sqrt((float)p->d);
+  return p->hadamard ? s / (float)p->d : s;
 }
 
 // The constant of the FP16 dQ prescale: c0 = ceil(log2(2.5 d 448^3 scale)),
@@ -187,6 +192,7 @@ flamia_status_t flamia_quantize(const flamia_problem_t* p, int32_t role, const v
       a.heads = i == 0 ? p->H : p->Hkv;
       a.T = p->T;
       a.per_token = (i == 2 || p->exact) ? 1 : 0;
+      a.rotate = (i < 2 && p->hadamard) ? 1 : 0;
       if (nv && i < 2) {
         if (!out[i].codes4 || !out[i].scales4 || !out[i].gscale4) return FLAMIA_ERR_INVALID_ARG;
         a.codes4 = static_cast<uint8_t*>(out[i].codes4);
@@ -247,6 +253,8 @@ static flamia_status_t fill_params(const flamia_problem_t* p, const WsLayout& L,
   a->causal_dq_scale = p->causal_dq_scale ? 1 : 0;
   a->nvfp4 = p->path == FLAMIA_PATH_NVFP4_FP8 ? 1 : 0;
   a->bitexp = p->bitexp ? 1 : 0;
+  a->hadamard = p->hadamard ? 1 : 0;
+  a->rot_dk = p->hadamard ? reinterpret_cast<float*>(w + L.rot_dk) : nullptr;
   a->dbg_withhold = g_dbg_withhold.load();
   return FLAMIA_OK;
 }

@@ -653,7 +653,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t rr[32];
         tmem_ld32(taddr(tb, qq * 32, (which == 0 ? kColDK : kColDV) + 32 * cb), rr);
         tmem_ld_wait_regs(rr);
-        if (key_ok) store_row32<OUT_BF16>(which == 0 ? p.dK : p.dV, koff + 32 * cb, rr, which == 0 ? sm_scale : 1.0f);
+        if (!key_ok) continue;
+        if (which == 0 && p.hadamard)  // dK of the rotated Q, in fp32 until the back-rotation
+          store_row32<false>(p.rot_dk, koff + 32 * cb, rr, sm_scale);
+        else
+          store_row32<OUT_BF16>(which == 0 ? p.dK : p.dV, koff + 32 * cb, rr, which == 0 ? sm_scale : 1.0f);
       }
       tc_fence_before();
       mbar_arrive(&c.acc_free);
@@ -1035,7 +1039,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         uint32_t rr[32];
         tmem_ld32(taddr(tb, q * 32, kDqColAcc + hf * HC + 32 * cb), rr);
         tmem_ld_wait_regs(rr);
-        if (row_ok) store_row32<OUT_BF16>(p.dQ, off + 32 * cb, rr, p.softmax_scale);
+        if (!row_ok) continue;
+        if (p.hadamard)  // dQ of the rotated Q, in fp32 until the back-rotation
+          store_row32<false>(p.dq_acc, off + 32 * cb, rr, p.softmax_scale);
+        else
+          store_row32<OUT_BF16>(p.dQ, off + 32 * cb, rr, p.softmax_scale);
       }
       tc_fence_before();
       mbar_arrive(&c.dq_free);
@@ -1086,6 +1094,86 @@ __global__ void dq16_convert_kernel(const __half* __restrict__ acc, const int8_t
       reinterpret_cast<float4*>(out)[i] = v;
     }
   }
+}
+
+// Back-rotation of the gradients of rotated operands (Hadamard option):
+// with Q_r = Q H_d, dL/dQ = (dL/dQ_r) H_d (H_d symmetric), likewise for K.
+// One warp per row of `rows` d-vectors: the row (fp32, or FP16 with the
+// row's prescale 2^-pexp when F16) times f, the fast Walsh-Hadamard transform
+// in fp32, then the output dtype.  Lane l holds elements [l EPL, l EPL + EPL).
+template <bool OUT_BF16, int HD, bool F16>
+__global__ void __launch_bounds__(256) rot_back_kernel(const void* __restrict__ src, const int8_t* __restrict__ pexp,
+                                                       void* out, size_t rows, float f, int T, int heads) {
+  constexpr int EPL = HD / 32;
+  const int lane = threadIdx.x & 31;
+  const size_t warps = (size_t)gridDim.x * (blockDim.x >> 5);
+  for (size_t r = blockIdx.x * (size_t)(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+    const size_t o = r * HD + (size_t)lane * EPL;
+    float v[EPL];
+    float fr = f;
+    if constexpr (F16) {
+      const int t = (int)(r / (size_t)heads), h = (int)(r - (size_t)t * heads);
+      fr = f * pow2_127(-(int)__ldg(pexp + (size_t)h * T + t));
+      const __half* s16 = static_cast<const __half*>(src) + o;
+#pragma unroll
+      for (int e = 0; e < EPL; e += 2) {
+        const float2 x = __half22float2(*reinterpret_cast<const __half2*>(s16 + e));
+        v[e] = x.x;
+        v[e + 1] = x.y;
+      }
+    } else {
+      const float* s32 = static_cast<const float*>(src) + o;
+      if constexpr (EPL == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(s32);
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(s32);
+        v[0] = x.x; v[1] = x.y;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) v[e] *= fr;
+#pragma unroll
+    for (int h = 1; h < EPL; h <<= 1)
+#pragma unroll
+      for (int e = 0; e < EPL; ++e)
+        if ((e & h) == 0) {
+          const float a = v[e], b = v[e + h];
+          v[e] = a + b;
+          v[e + h] = a - b;
+        }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const bool upper = (lane & m) != 0;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        const float x = __shfl_xor_sync(0xffffffffu, v[e], m);
+        v[e] = upper ? x - v[e] : v[e] + x;
+      }
+    }
+    if constexpr (OUT_BF16) {
+      uint32_t w[EPL / 2];
+#pragma unroll
+      for (int e = 0; e < EPL; e += 2) {
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[e], v[e + 1]);
+        w[e / 2] = *reinterpret_cast<const uint32_t*>(&b2);
+      }
+      if constexpr (EPL == 4) *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + o) = make_uint2(w[0], w[1]);
+      else *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(out) + o) = w[0];
+    } else {
+      if constexpr (EPL == 4) *reinterpret_cast<float4*>(static_cast<float*>(out) + o) = make_float4(v[0], v[1], v[2], v[3]);
+      else *reinterpret_cast<float2*>(static_cast<float*>(out) + o) = make_float2(v[0], v[1]);
+    }
+  }
+}
+
+template <bool OB, int HD, bool F16>
+static cudaError_t launch_rot_back(const void* src, const int8_t* pexp, void* out, size_t rows, float f, int T,
+                                   int heads, int nsm, cudaStream_t st) {
+  const size_t want = (rows + 7) / 8;  // eight warps a block, a row a warp
+  const int blocks = (int)(want < (size_t)nsm * 8 ? (want < 1 ? 1 : want) : (size_t)nsm * 8);
+  rot_back_kernel<OB, HD, F16><<<blocks, 256, 0, st>>>(src, pexp, out, rows, f, T, heads);
+  return cudaGetLastError();
 }
 
 // The prescale exponent of every query row's FP16 dQ partials, pexp [H][T]:
@@ -1208,6 +1296,13 @@ static cudaError_t launch_bwd_t(const AttnParams& p, const AttnMaps& m, cudaStre
         bwd_kernel<HD, OB, EX, true, false, true><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.dq, m.q,
                                                                                   m.q);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (p.hadamard) {
+          if ((e = launch_rot_back<OB, HD, true>(p.dq16, p.pexp, p.dQ, (size_t)p.T * p.H, p.softmax_scale, p.T, p.H,
+                                                 nsm, st)) != cudaSuccess)
+            return e;
+          return launch_rot_back<OB, HD, false>(p.rot_dk, nullptr, p.dK, (size_t)p.T * p.Hkv, 1.f, p.T, p.Hkv, nsm,
+                                                st);
+        }
         if (OB)
           dq16_convert_kernel<true><<<cg, 256, 0, st>>>(p.dq16, p.pexp, p.dQ, n4, p.softmax_scale, p.T, p.H, HD / 4);
         else
@@ -1218,6 +1313,13 @@ static cudaError_t launch_bwd_t(const AttnParams& p, const AttnMaps& m, cudaStre
         bwd_kernel<HD, OB, EX, true, false, false><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.dq, m.q,
                                                                                    m.q);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (p.hadamard) {
+          if ((e = launch_rot_back<OB, HD, false>(p.dq_acc, nullptr, p.dQ, (size_t)p.T * p.H, p.softmax_scale, p.T,
+                                                  p.H, nsm, st)) != cudaSuccess)
+            return e;
+          return launch_rot_back<OB, HD, false>(p.rot_dk, nullptr, p.dK, (size_t)p.T * p.Hkv, 1.f, p.T, p.Hkv, nsm,
+                                                st);
+        }
         if (OB) dq_convert_kernel<true><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4, p.softmax_scale);
         else dq_convert_kernel<false><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4, p.softmax_scale);
       }
@@ -1238,6 +1340,13 @@ static cudaError_t launch_bwd_t(const AttnParams& p, const AttnMaps& m, cudaStre
   long dwork = (long)p.max_items * p.H;
   int dgrid = (int)(dwork < nsm ? dwork : nsm);
   dq_kernel<HD, OB, EX, NV4><<<dgrid, kDqThreads, dsm, st>>>(p, m.q, m.k, m.v, m.dO, m.qn, m.kn);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (!NV4 && p.hadamard) {  // both kernels left fp32 gradients of the rotated operands
+    if ((e = launch_rot_back<OB, HD, false>(p.dq_acc, nullptr, p.dQ, (size_t)p.T * p.H, 1.f, p.T, p.H, nsm, st)) !=
+        cudaSuccess)
+      return e;
+    return launch_rot_back<OB, HD, false>(p.rot_dk, nullptr, p.dK, (size_t)p.T * p.Hkv, 1.f, p.T, p.Hkv, nsm, st);
+  }
   return cudaGetLastError();
 }
 

@@ -54,6 +54,7 @@ struct WsLayout {
   size_t header, tile_prefix, blk32_prefix, fwd_items, bwd_items, keys_a, keys_b;
   size_t dq_acc;           // [T][H][d] dQ accumulator: fp32, or binary16 with dq_fp16
   size_t pexp;             // int8 [H][T]: the dQ prescale exponent of each query row
+  size_t rot_dk;           // hadamard: fp32 [T][Hkv][d] dK before the back-rotation
   size_t nv_q, nv_k;       // mixed path: bf16 [T][H][d] / [T][Hkv][d], NVFP4 values without the token scale
   size_t total;
   int32_t max_items;       // upper bound of tiles: ceil(T/128) + n_seq
@@ -76,8 +77,14 @@ inline WsLayout ws_layout(const flamia_problem_t& p) {
   L.bwd_items = o; o = align256(o + sizeof(int2) * L.max_items);
   L.keys_a = o; o = align256(o + sizeof(uint64_t) * L.sort_n * 2);
   L.keys_b = o; o = align256(o + sizeof(uint64_t) * L.sort_n * 2);
-  L.dq_acc = o; o = align256(o + (p.dq_fp16 ? 2 : 4) * (size_t)p.T * p.H * p.d);
+  // fp32 unless the FP16 partials alone use it (the rotation's back-transform
+  // reads every dQ path's result from here in fp32)
+  L.dq_acc = o; o = align256(o + (p.dq_fp16 && !p.hadamard ? 2 : 4) * (size_t)p.T * p.H * p.d);
   L.pexp = o; o = align256(o + (size_t)p.T * p.H);
+  L.rot_dk = 0;
+  if (p.hadamard) {  // dK in the rotated basis, fp32, before the back-rotation
+    L.rot_dk = o; o = align256(o + 4 * (size_t)p.T * p.Hkv * p.d);
+  }
   L.nv_q = L.nv_k = 0;
   if (p.path == FLAMIA_PATH_NVFP4_FP8) {
     L.nv_q = o; o = align256(o + 2 * (size_t)p.T * p.H * p.d);

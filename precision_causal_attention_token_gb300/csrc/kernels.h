@@ -16,6 +16,7 @@ struct QuantArgs {
   float* D;          // [heads][T]
   int T, heads;
   int per_token;
+  int rotate;        // Hadamard rotation of each token's d-vector before quantization
 };
 
 // Up to three tensors quantized by one launch (Q, K, V; or dO alone).
@@ -49,6 +50,8 @@ struct AttnParams {
   const float* k_g;     // mixed path: of K's [Hkv][T]
   int nvfp4;            // 1: scores from the NVFP4 payload (bf16 operands in the workspace)
   int bitexp;           // 1: forward with bit-level exponentials (inference only)
+  int hadamard;         // 1: Q, K rotated; dQ, dK go through fp32 buffers and are rotated back
+  float* rot_dk;        // hadamard: fp32 [T][Hkv][d] dK (times the softmax scale), rotated basis
   const float* D;       // [H][T]
   int32_t* m;           // [H][T]
   float* l;             // [H][T]

@@ -87,8 +87,42 @@ struct RawRow {
   }
 };
 
-// Quantize one (32-token block g, head h) unit of one tensor.
-template <typename TIn, typename TO, int HD, bool WITH_D, bool NVFP4>
+// Hadamard rotation of one token's d-vector across the warp (FLAMIA summary
+// §4.3 and close reading 四 4.4: the fused quantizer rotates Q and K to
+// spread outlier channels): x -> x H_d with the Sylvester matrix (entries
+// +-1), by the fast Walsh-Hadamard transform in fp32 with stages h = 1, 2,
+// ..., d/2 in that order; each stage turns the pair (x[i], x[i + h]) (bit h
+// of i clear) into (x[i] + x[i + h], x[i] - x[i + h]).  Lane l holds
+// elements [l EPL, l EPL + EPL): the stages below EPL are in-lane, the
+// others pair lane l with lane l ^ m (one shuffle per element and stage).
+template <int EPL>
+__device__ __forceinline__ void fwht_warp(float (&v)[EPL], int lane) {
+#pragma unroll
+  for (int h = 1; h < EPL; h <<= 1)
+#pragma unroll
+    for (int e = 0; e < EPL; ++e)
+      if ((e & h) == 0) {
+        const float a = v[e], b = v[e + h];
+        v[e] = a + b;
+        v[e + h] = a - b;
+      }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[e], m);
+      v[e] = upper ? o - v[e] : v[e] + o;  // lower: x[i] + x[i + h]; upper: x[i] - x[i + h]
+    }
+  }
+}
+
+// Quantize one (32-token block g, head h) unit of one tensor.  ROT: the
+// launch holds a rotated tensor; units with a.rotate quantize x H_d (fp32)
+// instead of x.  The rotation is recomputed from the packed input words for
+// the exponent pass and again for the code pass (the same operations give
+// the same fp32 values), which keeps 32 rotated rows out of registers.
+template <typename TIn, typename TO, int HD, bool WITH_D, bool NVFP4, bool ROT>
 __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, const int32_t* __restrict__ cu,
                                               const int32_t* __restrict__ blk_prefix, int n_seq, int lane) {
   constexpr int EPL = HD / 32;  // elements per lane: 4 (d=128) or 2 (d=64)
@@ -110,6 +144,15 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
     if (t < ntok) raw[t].load(x + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL);
     else raw[t].zero();
   }
+  static_assert(!ROT || (!WITH_D && !NVFP4), "only Q/K/V launches of the MXFP8 path rotate");
+  // token t's EPL values of this lane (rotated when the unit rotates; a zero
+  // row stays zero)
+  auto row_vals = [&](int t, float (&v)[EPL]) {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) v[e] = raw[t].at(e);
+    if constexpr (ROT)
+      if (a.rotate) fwht_warp<EPL>(v, lane);
+  };
   if constexpr (!NVFP4) {
     // MXFP8 codes.  Token-block units: one exponent from the lane maxima and a
     // single warp reduction.  Per-token units (V, exact option): one warp
@@ -119,10 +162,12 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
       // four partial maxima (short dependency chains), three-input max
       float lm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int t = 0; t < 32; ++t)
+      for (int t = 0; t < 32; ++t) {
+        float v[EPL];
+        row_vals(t, v);
 #pragma unroll
-        for (int e = 0; e < EPL; e += 2)
-          lm[t & 3] = fmax3(lm[t & 3], fabsf(raw[t].at(e)), fabsf(raw[t].at(e + 1)));
+        for (int e = 0; e < EPL; e += 2) lm[t & 3] = fmax3(lm[t & 3], fabsf(v[e]), fabsf(v[e + 1]));
+      }
       e_blk = noclamp_exp_clamped(warp_max(fmaxf(fmaxf(lm[0], lm[1]), fmaxf(lm[2], lm[3]))));
     }
     int my_e = e_blk;  // exponent of token `lane`
@@ -133,10 +178,12 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
 #pragma unroll
     for (int t = 0; t < 32; ++t) {
       int e_t = e_blk;
+      float v[EPL];
+      row_vals(t, v);
       if (a.per_token) {
         float lm = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) lm = fmaxf(lm, fabsf(raw[t].at(e)));
+        for (int e = 0; e < EPL; ++e) lm = fmaxf(lm, fabsf(v[e]));
         e_t = noclamp_exp_clamped(warp_max(lm));
         if (lane == t) my_e = e_t;
       }
@@ -147,7 +194,7 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
         const float inv_s = exp2i(max(-e_t, -126));
         float qv[EPL];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) qv[e] = raw[t].at(e) * inv_s;
+        for (int e = 0; e < EPL; ++e) qv[e] = v[e] * inv_s;
         uint8_t* dst = a.codes + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL;
         uint32_t cw;
         if constexpr (EPL == 4) {
@@ -277,7 +324,7 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
 // Resident 128-thread blocks per SM for each variant: the register
 // footprint is set by the unit held in registers (bf16 pairs packed; with D
 // also O's rows; the mixed path also the per-token maxima).
-template <typename TIn, typename TO, bool WITH_D, bool NVFP4>
+template <typename TIn, typename TO, bool WITH_D, bool NVFP4, bool ROT>
 constexpr int quant_blocks_per_sm() {
   if constexpr (NVFP4) return 3;
   else if constexpr (WITH_D) return (sizeof(TIn) == 2 && sizeof(TO) == 2) ? 4 : 2;
@@ -285,8 +332,8 @@ constexpr int quant_blocks_per_sm() {
 }
 
 // Grid-stride over the units of up to three tensors (Q, K, V share a launch).
-template <typename TIn, typename TO, int HD, bool WITH_D, bool NVFP4>
-__global__ void __launch_bounds__(128, (quant_blocks_per_sm<TIn, TO, WITH_D, NVFP4>())) quantize_kernel(const __grid_constant__ QuantBatch qb,
+template <typename TIn, typename TO, int HD, bool WITH_D, bool NVFP4, bool ROT>
+__global__ void __launch_bounds__(128, (quant_blocks_per_sm<TIn, TO, WITH_D, NVFP4, ROT>())) quantize_kernel(const __grid_constant__ QuantBatch qb,
                                                           const int32_t* __restrict__ cu,
                                                           const int32_t* __restrict__ blk_prefix, int n_seq,
                                                           WsHeader* hdr) {
@@ -303,7 +350,7 @@ __global__ void __launch_bounds__(128, (quant_blocks_per_sm<TIn, TO, WITH_D, NVF
     }
     const QuantArgs& a = qb.a[r];
     const int g = u / a.heads, h = u - g * a.heads;
-    quantize_unit<TIn, TO, HD, WITH_D, NVFP4>(a, g, h, cu, blk_prefix, n_seq, lane);
+    quantize_unit<TIn, TO, HD, WITH_D, NVFP4, ROT>(a, g, h, cu, blk_prefix, n_seq, lane);
   }
 }
 
@@ -312,13 +359,16 @@ cudaError_t launch_quantize(const QuantBatch& qb, int d, int in_bf16, int o_bf16
                             const int32_t* cu, const int32_t* blk_prefix, int n_seq, WsHeader* hdr,
                             int max_units, int n_sms, cudaStream_t st) {
   const int want = (max_units + 3) / 4;  // four warps per block, one unit per warp
+  bool rot = false;
+  for (int i = 0; i < qb.n; ++i) rot = rot || qb.a[i].rotate;
   // at most four waves of resident blocks; the warps stride over the rest
-#define FLAMIA_QL(TIN, TO_, HD_, WD, NV)                                                      \
-  do {                                                                                        \
-    const int cap = quant_blocks_per_sm<TIN, TO_, WD, NV>() * n_sms * 4;                      \
-    const int blocks = want < 1 ? 1 : (want > cap ? cap : want);                              \
-    quantize_kernel<TIN, TO_, HD_, WD, NV><<<blocks, 128, 0, st>>>(qb, cu, blk_prefix, n_seq, hdr); \
+#define FLAMIA_QL_R(TIN, TO_, HD_, WD, NV, RT)                                                         \
+  do {                                                                                                 \
+    const int cap = quant_blocks_per_sm<TIN, TO_, WD, NV, RT>() * n_sms * 4;                           \
+    const int blocks = want < 1 ? 1 : (want > cap ? cap : want);                                       \
+    quantize_kernel<TIN, TO_, HD_, WD, NV, RT><<<blocks, 128, 0, st>>>(qb, cu, blk_prefix, n_seq, hdr); \
   } while (0)
+#define FLAMIA_QL(TIN, TO_, HD_, WD, NV) FLAMIA_QL_R(TIN, TO_, HD_, WD, NV, false)
 #define FLAMIA_QL_D(TIN, HD_, WD, NV)                           \
   do {                                                          \
     if (o_bf16) FLAMIA_QL(TIN, __nv_bfloat16, HD_, WD, NV);     \
@@ -328,6 +378,7 @@ cudaError_t launch_quantize(const QuantBatch& qb, int d, int in_bf16, int o_bf16
   do {                                                          \
     if (with_D) FLAMIA_QL_D(TIN, HD_, true, false);             \
     else if (nvfp4) FLAMIA_QL(TIN, float, HD_, false, true);    \
+    else if (rot) FLAMIA_QL_R(TIN, float, HD_, false, false, true); \
     else FLAMIA_QL(TIN, float, HD_, false, false);              \
   } while (0)
   if (in_bf16) {
@@ -338,6 +389,7 @@ cudaError_t launch_quantize(const QuantBatch& qb, int d, int in_bf16, int o_bf16
 #undef FLAMIA_QL_V
 #undef FLAMIA_QL_D
 #undef FLAMIA_QL
+#undef FLAMIA_QL_R
   return cudaGetLastError();
 }
 

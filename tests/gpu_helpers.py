@@ -20,13 +20,14 @@ def to_dev(a: np.ndarray, dtype: str, dev="cuda"):
 
 
 def run_gpu(w, *, causal=True, exact=False, path=fl.PATH_MXFP8, deterministic=False, inputs=None,
-            backward=True, causal_dq_scale=False, dq_fp16=False):
+            backward=True, causal_dq_scale=False, dq_fp16=False, hadamard=False):
     dev = torch.device("cuda:0")
     q, k, v, do = inputs if inputs is not None else (w.tensor(n) for n in ("q", "k", "v", "do"))
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
     dt = fl.BF16 if w.dtype == "bf16" else fl.F32
     tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu, causal=causal, exact=exact, path=path, in_dtype=dt,
-                      out_dtype=dt, deterministic=deterministic, causal_dq_scale=causal_dq_scale, dq_fp16=dq_fp16)
+                      out_dtype=dt, deterministic=deterministic, causal_dq_scale=causal_dq_scale, dq_fp16=dq_fp16,
+                      hadamard=hadamard)
     tc.plan()
     tc.forward(to_dev(q, w.dtype), to_dev(k, w.dtype), to_dev(v, w.dtype))
     if backward:
@@ -39,12 +40,13 @@ def run_gpu(w, *, causal=True, exact=False, path=fl.PATH_MXFP8, deterministic=Fa
 
 
 def run_oracle(w, *, causal=True, exact=False, path=oracle.PATH_MXFP8, inputs=None, backward=True,
-               dq_fp16=False, dq_causal_scale=False):
+               dq_fp16=False, dq_causal_scale=False, hadamard=False):
     """The oracle's call on the same inputs (dq_fp16: FP16 dQ partials with the
     power-of-two prescale, as the GPU's dq_fp16 option)."""
     q, k, v, do = inputs if inputs is not None else (w.tensor(n) for n in ("q", "k", "v", "do"))
     return oracle.train_call(q, k, v, do if backward else None, w.cu_seqlens, causal=causal, exact=exact,
-                             path=path, out_dtype=w.dtype, dq_fp16=dq_fp16, dq_causal_scale=dq_causal_scale)
+                             path=path, out_dtype=w.dtype, dq_fp16=dq_fp16, dq_causal_scale=dq_causal_scale,
+                             hadamard=hadamard)
 
 
 def np_of(t):
@@ -136,11 +138,11 @@ def o_rows_differ(tc_O, ref_O):
     return np.any(np_of(tc_O) != np.asarray(ref_O, np.float64), axis=-1)
 
 
-def o_rounding_noise(w, *, causal=True, exact=False, inputs=None):
+def o_rounding_noise(w, *, causal=True, exact=False, inputs=None, hadamard=False):
     """Oracle-only sensitivity of dQ/dK/dV to rounding O before D."""
-    a = run_oracle(w, causal=causal, exact=exact, inputs=inputs)
+    a = run_oracle(w, causal=causal, exact=exact, inputs=inputs, hadamard=hadamard)
     q, k, v, do = inputs if inputs is not None else (w.tensor(n) for n in ("q", "k", "v", "do"))
-    b = oracle.train_call(q, k, v, do, w.cu_seqlens, causal=causal, exact=exact, out_dtype="f64")
+    b = oracle.train_call(q, k, v, do, w.cu_seqlens, causal=causal, exact=exact, out_dtype="f64", hadamard=hadamard)
     return a, {n: a[n] - b[n] for n in ("dQ", "dK", "dV")}
 
 

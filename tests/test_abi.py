@@ -148,3 +148,21 @@ def test_bitexp_is_inference_only(lib):
     st = lib.flamia_bwd(p, ops[0], ops[1], ops[2], ops[3], 0x60000, 0x40000, 0x50000, 0x70000, 0x80000, 0x90000,
                         1 << 20, 1 << 40, None)
     assert st == fl.ERR_UNSUPPORTED
+
+
+def test_hadamard_option_host_rules(lib):
+    """The Hadamard option runs on the MXFP8 path only and adds the fp32 dK
+    buffer of the back-rotation (4 T Hkv d bytes) to the workspace."""
+    p, _ = _prob()
+    n = fl.flamia_workspace_size(p)
+    p.hadamard = 1
+    assert fl.flamia_workspace_size(p) >= n + 4 * 228 * 2 * 128
+    q, _ = _prob()
+    q.hadamard, q.path = 1, fl.PATH_NVFP4_FP8
+    assert fl.flamia_workspace_size(q) == 0
+    # with FP16 dQ partials the dQ buffer stays fp32 (the back-rotation reads it)
+    r, _ = _prob()
+    r.dq_fp16 = 1
+    n16 = fl.flamia_workspace_size(r)
+    r.hadamard = 1
+    assert fl.flamia_workspace_size(r) >= n16 + 2 * 228 * 4 * 128 + 4 * 228 * 2 * 128
