@@ -383,21 +383,23 @@ def _secondary(fl, idx, dev, stream, steps):
 
 
 def _option_overheads(fl, w, inputs, dev, stream, base_bwd_ms, steps):
-    """Backward time of the deterministic and exact options and of the FP16
-    dQ partials (document-range and causal prescale) on the same workload,
-    relative to the default backward."""
+    """Backward time of the deterministic and exact options, of the FP16 dQ
+    partials (document-range and causal prescale) and of the Hadamard option
+    (whose cost is mostly in the Q/K/V quantizer and the back-rotation) on
+    the same workload, relative to the default backward."""
     import torch
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
     out = {}
     for name, kw in (("deterministic", {"deterministic": True}), ("exact", {"exact": True}),
                      ("fp16_dq_partials", {"dq_fp16": True}),
-                     ("fp16_dq_partials_causal_scale", {"dq_fp16": True, "causal_dq_scale": True})):
+                     ("fp16_dq_partials_causal_scale", {"dq_fp16": True, "causal_dq_scale": True}),
+                     ("hadamard", {"hadamard": True})):
         tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu, **kw)
         step = _step_fn(fl, tc, inputs)
         for _ in range(2):
             step()
         (pl, qk, fw, qd, bw), _ = _phases(step, steps, stream)
-        out[name] = {"bwd_ms": bw, "fwd_ms": fw, "bwd_overhead": bw / base_bwd_ms - 1.0}
+        out[name] = {"bwd_ms": bw, "fwd_ms": fw, "quantize_qkv_ms": qk, "bwd_overhead": bw / base_bwd_ms - 1.0}
         del tc
     return out
 

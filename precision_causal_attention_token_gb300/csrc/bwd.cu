@@ -1143,13 +1143,10 @@ __global__ void __launch_bounds__(256) rot_back_kernel(const void* __restrict__ 
           v[e + h] = a - b;
         }
 #pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-      const bool upper = (lane & m) != 0;
+    for (int m = 1; m < 32; m <<= 1) {  // lower lane: x + v; upper lane: x - v
+      const float sgn = (lane & m) ? -1.f : 1.f;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        const float x = __shfl_xor_sync(0xffffffffu, v[e], m);
-        v[e] = upper ? x - v[e] : v[e] + x;
-      }
+      for (int e = 0; e < EPL; ++e) v[e] = fmaf(sgn, v[e], __shfl_xor_sync(0xffffffffu, v[e], m));
     }
     if constexpr (OUT_BF16) {
       uint32_t w[EPL / 2];

@@ -106,25 +106,26 @@ __device__ __forceinline__ void fwht_warp(float (&v)[EPL], int lane) {
         v[e] = a + b;
         v[e + h] = a - b;
       }
+  // lower lane: o + v = x[i] + x[i + h]; upper lane: o - v = x[i] - x[i + h]
+  // (one fused multiply-add by +-1: the product is exact, the sum rounds once)
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1) {
-    const bool upper = (lane & m) != 0;
+    const float sgn = (lane & m) ? -1.f : 1.f;
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      const float o = __shfl_xor_sync(0xffffffffu, v[e], m);
-      v[e] = upper ? o - v[e] : v[e] + o;  // lower: x[i] + x[i + h]; upper: x[i] - x[i + h]
-    }
+    for (int e = 0; e < EPL; ++e) v[e] = fmaf(sgn, v[e], __shfl_xor_sync(0xffffffffu, v[e], m));
   }
 }
 
 // Quantize one (32-token block g, head h) unit of one tensor.  ROT: the
 // launch holds a rotated tensor; units with a.rotate quantize x H_d (fp32)
-// instead of x.  The rotation is recomputed from the packed input words for
-// the exponent pass and again for the code pass (the same operations give
-// the same fp32 values), which keeps 32 rotated rows out of registers.
+// instead of x.  The exponent pass stages each token's values (rotated or
+// not) in the warp's shared-memory slice `stage` ([32 tokens][32 lanes][EPL]
+// fp32, each lane reading back only what it wrote), and the code pass reads
+// them from there, so 32 rotated rows never sit in registers.
 template <typename TIn, typename TO, int HD, bool WITH_D, bool NVFP4, bool ROT>
 __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, const int32_t* __restrict__ cu,
-                                              const int32_t* __restrict__ blk_prefix, int n_seq, int lane) {
+                                              const int32_t* __restrict__ blk_prefix, int n_seq, int lane,
+                                              float* stage) {
   constexpr int EPL = HD / 32;  // elements per lane: 4 (d=128) or 2 (d=64)
   const TIn* __restrict__ x = static_cast<const TIn*>(a.x);
   const size_t row = (size_t)a.heads * HD;  // elements between consecutive tokens
@@ -146,12 +147,30 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
   }
   static_assert(!ROT || (!WITH_D && !NVFP4), "only Q/K/V launches of the MXFP8 path rotate");
   // token t's EPL values of this lane (rotated when the unit rotates; a zero
-  // row stays zero)
-  auto row_vals = [&](int t, float (&v)[EPL]) {
+  // row stays zero).  ROT: `fresh` computes and stages them, else they are
+  // read back from the stage.
+  auto row_vals = [&](int t, float (&v)[EPL], bool fresh) {
+    if constexpr (ROT) {
+      float* s = stage + (t * 32 + lane) * EPL;
+      if (fresh) {
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) v[e] = raw[t].at(e);
-    if constexpr (ROT)
-      if (a.rotate) fwht_warp<EPL>(v, lane);
+        for (int e = 0; e < EPL; ++e) v[e] = raw[t].at(e);
+        if (a.rotate) fwht_warp<EPL>(v, lane);
+        if constexpr (EPL == 4) *reinterpret_cast<float4*>(s) = make_float4(v[0], v[1], v[2], v[3]);
+        else *reinterpret_cast<float2*>(s) = make_float2(v[0], v[1]);
+      } else {
+        if constexpr (EPL == 4) {
+          const float4 u = *reinterpret_cast<const float4*>(s);
+          v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+        } else {
+          const float2 u = *reinterpret_cast<const float2*>(s);
+          v[0] = u.x; v[1] = u.y;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) v[e] = raw[t].at(e);
+    }
   };
   if constexpr (!NVFP4) {
     // MXFP8 codes.  Token-block units: one exponent from the lane maxima and a
@@ -164,7 +183,7 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
 #pragma unroll
       for (int t = 0; t < 32; ++t) {
         float v[EPL];
-        row_vals(t, v);
+        row_vals(t, v, true);
 #pragma unroll
         for (int e = 0; e < EPL; e += 2) lm[t & 3] = fmax3(lm[t & 3], fabsf(v[e]), fabsf(v[e + 1]));
       }
@@ -179,7 +198,7 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
     for (int t = 0; t < 32; ++t) {
       int e_t = e_blk;
       float v[EPL];
-      row_vals(t, v);
+      row_vals(t, v, a.per_token != 0);  // token-block units staged them in the exponent pass
       if (a.per_token) {
         float lm = 0.f;
 #pragma unroll
@@ -326,7 +345,7 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
 // also O's rows; the mixed path also the per-token maxima).
 template <typename TIn, typename TO, bool WITH_D, bool NVFP4, bool ROT>
 constexpr int quant_blocks_per_sm() {
-  if constexpr (NVFP4) return 3;
+  if constexpr (NVFP4 || ROT) return 3;
   else if constexpr (WITH_D) return (sizeof(TIn) == 2 && sizeof(TO) == 2) ? 4 : 2;
   else return sizeof(TIn) == 2 ? 5 : 3;
 }
@@ -337,6 +356,8 @@ __global__ void __launch_bounds__(128, (quant_blocks_per_sm<TIn, TO, WITH_D, NVF
                                                           const int32_t* __restrict__ cu,
                                                           const int32_t* __restrict__ blk_prefix, int n_seq,
                                                           WsHeader* hdr) {
+  extern __shared__ float4 quant_stage[];  // ROT: 32 * HD fp32 per warp
+  float* const stage = ROT ? reinterpret_cast<float*>(quant_stage) + (threadIdx.x >> 5) * (32 * HD) : nullptr;
   const int lane = threadIdx.x & 31;
   const int warps_total = gridDim.x * (blockDim.x >> 5);
   const int n_blk = hdr->n_blk32;
@@ -350,8 +371,21 @@ __global__ void __launch_bounds__(128, (quant_blocks_per_sm<TIn, TO, WITH_D, NVF
     }
     const QuantArgs& a = qb.a[r];
     const int g = u / a.heads, h = u - g * a.heads;
-    quantize_unit<TIn, TO, HD, WITH_D, NVFP4, ROT>(a, g, h, cu, blk_prefix, n_seq, lane);
+    quantize_unit<TIn, TO, HD, WITH_D, NVFP4, ROT>(a, g, h, cu, blk_prefix, n_seq, lane, stage);
   }
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device (a function
+// attribute, not a stream operation).
+template <auto Kernel>
+static cudaError_t raise_smem_once(int smem) {
+  static bool done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (done[dev]) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  done[dev] = e == cudaSuccess;
+  return e;
 }
 
 // Host-side launcher (called by api.cu).
@@ -362,11 +396,17 @@ cudaError_t launch_quantize(const QuantBatch& qb, int d, int in_bf16, int o_bf16
   bool rot = false;
   for (int i = 0; i < qb.n; ++i) rot = rot || qb.a[i].rotate;
   // at most four waves of resident blocks; the warps stride over the rest
-#define FLAMIA_QL_R(TIN, TO_, HD_, WD, NV, RT)                                                         \
-  do {                                                                                                 \
-    const int cap = quant_blocks_per_sm<TIN, TO_, WD, NV, RT>() * n_sms * 4;                           \
-    const int blocks = want < 1 ? 1 : (want > cap ? cap : want);                                       \
-    quantize_kernel<TIN, TO_, HD_, WD, NV, RT><<<blocks, 128, 0, st>>>(qb, cu, blk_prefix, n_seq, hdr); \
+#define FLAMIA_QL_R(TIN, TO_, HD_, WD, NV, RT)                                                            \
+  do {                                                                                                    \
+    const int cap = quant_blocks_per_sm<TIN, TO_, WD, NV, RT>() * n_sms * 4;                              \
+    const int blocks = want < 1 ? 1 : (want > cap ? cap : want);                                          \
+    const int smem = RT ? 4 * 32 * HD_ * (int)sizeof(float) : 0;                                          \
+    if (RT) {                                                                                             \
+      const cudaError_t ea =                                                                              \
+          raise_smem_once<quantize_kernel<TIN, TO_, HD_, WD, NV, RT>>(smem);                              \
+      if (ea != cudaSuccess) return ea;                                                                   \
+    }                                                                                                     \
+    quantize_kernel<TIN, TO_, HD_, WD, NV, RT><<<blocks, 128, smem, st>>>(qb, cu, blk_prefix, n_seq, hdr); \
   } while (0)
 #define FLAMIA_QL(TIN, TO_, HD_, WD, NV) FLAMIA_QL_R(TIN, TO_, HD_, WD, NV, false)
 #define FLAMIA_QL_D(TIN, HD_, WD, NV)                           \
