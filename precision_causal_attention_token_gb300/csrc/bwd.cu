@@ -713,17 +713,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (ii > 0 && !(ok = mbar_wait_warp(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x326))) break;
           tc_fence_after();
           const int par = ii & 1;
-          uint32_t dp[2][32];
-          tmem_ld32(taddr(tb, q * 32, kColX1 + 32 * b0), dp[0]);
-          tmem_ld32(taddr(tb, q * 32, kColX1 + 32 * (b0 + 1)), dp[1]);
-          tmem_ld_wait_regs(dp[0], dp[1]);
-#pragma unroll
+          // The two key blocks go through one copy of the block code (a loop
+          // that is not unrolled): unrolled, the backward's hot loop no longer
+          // fit the instruction cache.
+#pragma unroll 1
           for (int bb = 0; bb < 2; ++bb) {
             const int b = b0 + bb;
+            uint32_t dp[32], pc[8];
+            tmem_ld32(taddr(tb, q * 32, kColX1 + 32 * b), dp);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) pc[k] = bb ? pcode[1][k] : pcode[0][k];
+            const int eb = bb ? Eb[1] : Eb[0];
+            tmem_ld_wait_regs(dp);
             float wv[32], uv[32];
             float amax_w, amax_u;
-            const float gbh = ds_gbh(Eb[bb], rv.mi, rv.inv_l, rv.hdo);
-            ds_block(dp[bb], pcode[bb], rv.nDp, c.vinv[kvs] + 32 * b, wv, uv, amax_w, amax_u);
+            const float gbh = ds_gbh(eb, rv.mi, rv.inv_l, rv.hdo);
+            ds_block(dp, pc, rv.nDp, c.vinv[kvs] + 32 * b, wv, uv, amax_w, amax_u);
             // P~: 32 x 32 block (this warp's 32 queries x key block b)
             const int e_pt = noclamp_exp_clamped(warp_max(amax_u * gbh));
             uint32_t codes[8];
