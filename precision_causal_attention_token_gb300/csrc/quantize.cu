@@ -45,6 +45,17 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[32], int lane) {
   return v[0];
 }
 
+// Largest magnitude among a lane's packed bf16 words (max of |x| taken on the
+// bf16 pairs, exact), as fp32.
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t m, uint32_t w) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(w & 0x7FFF7FFFu));
+  return r;
+}
+__device__ __forceinline__ float bf16x2_hmax_f32(uint32_t m) {
+  return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+}
+
 // Smallest E4M3FN code whose value is >= r (r > 0), saturating at 448.
 __device__ __forceinline__ uint32_t e4m3_roundup(float r) {
   uint32_t c = pack_e4m3x2(r, 0.f) & 0xFFu;
@@ -176,16 +187,28 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
     // MXFP8 codes.  Token-block units: one exponent from the lane maxima and a
     // single warp reduction.  Per-token units (V, exact option): one warp
     // reduction per token, so every lane holds that token's exponent.
+    // bf16 input, no rotation: maxima taken on the packed bf16 pairs
+    constexpr bool kPackedMax = sizeof(TIn) == 2 && !ROT;
     int e_blk = 0;
     if (!a.per_token) {
       // four partial maxima (short dependency chains), three-input max
       float lm[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (kPackedMax) {
+        uint32_t m2[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-      for (int t = 0; t < 32; ++t) {
-        float v[EPL];
-        row_vals(t, v, true);
+        for (int t = 0; t < 32; ++t)
 #pragma unroll
-        for (int e = 0; e < EPL; e += 2) lm[t & 3] = fmax3(lm[t & 3], fabsf(v[e]), fabsf(v[e + 1]));
+          for (int k = 0; k < RawRow<TIn, EPL>::kWords; ++k) m2[t & 3] = bf16x2_absmax(m2[t & 3], raw[t].w[k]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) lm[k] = bf16x2_hmax_f32(m2[k]);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          float v[EPL];
+          row_vals(t, v, true);
+#pragma unroll
+          for (int e = 0; e < EPL; e += 2) lm[t & 3] = fmax3(lm[t & 3], fabsf(v[e]), fabsf(v[e + 1]));
+        }
       }
       e_blk = noclamp_exp_clamped(warp_max(fmaxf(fmaxf(lm[0], lm[1]), fmaxf(lm[2], lm[3]))));
     }
@@ -201,8 +224,15 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
       row_vals(t, v, a.per_token != 0);  // token-block units staged them in the exponent pass
       if (a.per_token) {
         float lm = 0.f;
+        if constexpr (kPackedMax) {
+          uint32_t m2 = 0u;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) lm = fmaxf(lm, fabsf(v[e]));
+          for (int k = 0; k < RawRow<TIn, EPL>::kWords; ++k) m2 = bf16x2_absmax(m2, raw[t].w[k]);
+          lm = bf16x2_hmax_f32(m2);
+        } else {
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) lm = fmaxf(lm, fabsf(v[e]));
+        }
         e_t = noclamp_exp_clamped(warp_max(lm));
         if (lane == t) my_e = e_t;
       }
@@ -211,9 +241,10 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
         // 2^-e_t is a normal fp32 for every exponent of finite data (e_t <= 120),
         // so one multiply per element is exact down to the E4M3 range
         const float inv_s = exp2i(max(-e_t, -126));
+        const uint64_t s2 = f2_pack(inv_s, inv_s);
         float qv[EPL];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) qv[e] = v[e] * inv_s;
+        for (int e = 0; e < EPL; e += 2) f2_unpack(f2_mul(f2_pack(v[e], v[e + 1]), s2), qv[e], qv[e + 1]);
         uint8_t* dst = a.codes + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL;
         uint32_t cw;
         if constexpr (EPL == 4) {
