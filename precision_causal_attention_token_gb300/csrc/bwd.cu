@@ -696,8 +696,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           int Eb[2];
           // the diagonal tile (and a document's last key tile) needs the mask
           const bool need_mask = p.causal ? (qt == it.y) : (it.y == n_t - 1);
-          recompute_phat<PERKEY>(taddr(tb, q * 32, kColX0), b0, rv.rowc, c.kf[kvs], c.vf[kvs], i_loc, key0, len, p.causal,
-                                need_mask, row_ok, pcode, Eb);
+          // P^ of the two key blocks, one block at a time through one copy of
+          // the code (as the dS blocks below)
+#pragma unroll 1
+          for (int bb = 0; bb < 2; ++bb) {
+            const int b = b0 + bb;
+            uint32_t sr[32], cw[8];
+            tmem_ld32(taddr(tb, q * 32, kColX0 + 32 * b), sr);
+            tmem_ld_wait_regs(sr);
+            float y[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(sr[j]);
+            int e;
+            if (need_mask)
+              e = phat_block_logits<PERKEY, true>(y, rv.rowc, c.kf[kvs] + 32 * b, c.vf[kvs] + 32 * b, i_loc,
+                                                  key0 + 32 * b, len, p.causal);
+            else
+              e = phat_block_logits<PERKEY, false>(y, rv.rowc, c.kf[kvs] + 32 * b, c.vf[kvs] + 32 * b, i_loc,
+                                                   key0 + 32 * b, len, p.causal);
+            if (!row_ok) e = kEmptyBlock;
+            // rows outside the document: finite logits, zero codes
+            phat_block_codes(y, row_ok ? e : kZeroCodes, cw);
+            if (bb == 0) {
+              Eb[0] = e;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) pcode[0][k] = cw[k];
+            } else {
+              Eb[1] = e;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) pcode[1][k] = cw[k];
+            }
+          }
           tc_fence_before();
           mbar_arrive(&c.x0_free);  // S has been read: X0 may take the next S
           if (dbg_c != nullptr && row_ok) {
