@@ -127,28 +127,44 @@ __device__ __forceinline__ void fwht_warp(float (&v)[EPL], int lane) {
   }
 }
 
+// First token and token count of document-local 32-token block g: the
+// document is the last one with blk_prefix[doc] <= g.  A 32-way search:
+// every lane probes one position of the current range (blk_prefix is
+// non-decreasing, so the probes at or below g form a prefix of the lanes),
+// so a pass costs one load round trip and up to 32 documents take one pass.
+__device__ __forceinline__ int2 block_tokens(int g, const int32_t* __restrict__ cu,
+                                             const int32_t* __restrict__ blk_prefix, int n_seq, int lane) {
+  int lo = 0, hi = n_seq;  // blk_prefix[lo] <= g < blk_prefix[hi]
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) >> 5;
+    const int pidx = lo + (lane + 1) * step;
+    const bool le = pidx < hi && __ldg(blk_prefix + pidx) <= g;
+    const int k = __popc(__ballot_sync(0xffffffffu, le));
+    hi = min(hi, lo + (k + 1) * step);
+    lo += k * step;
+  }
+  const int doc_start = __ldg(cu + lo), doc_end = __ldg(cu + lo + 1);
+  const int t0 = doc_start + 32 * (g - __ldg(blk_prefix + lo));
+  return make_int2(t0, min(32, doc_end - t0));
+}
+
 // Quantize one (32-token block g, head h) unit of one tensor.  ROT: the
 // launch holds a rotated tensor; units with a.rotate quantize x H_d (fp32)
 // instead of x.  The exponent pass stages each token's values (rotated or
 // not) in the warp's shared-memory slice `stage` ([32 tokens][32 lanes][EPL]
 // fp32, each lane reading back only what it wrote), and the code pass reads
 // them from there, so 32 rotated rows never sit in registers.
+// `loc` is the unit's (first token, token count); the next unit's block
+// `g_next` (or -1) is located while this unit's rows are in flight.
 template <typename TIn, typename TO, int HD, bool WITH_D, bool NVFP4, bool ROT>
-__device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, const int32_t* __restrict__ cu,
+__device__ __forceinline__ void quantize_unit(const QuantArgs& a, int2 loc, int h, int g_next,
+                                              int2& loc_next, const int32_t* __restrict__ cu,
                                               const int32_t* __restrict__ blk_prefix, int n_seq, int lane,
                                               float* stage) {
   constexpr int EPL = HD / 32;  // elements per lane: 4 (d=128) or 2 (d=64)
   const TIn* __restrict__ x = static_cast<const TIn*>(a.x);
   const size_t row = (size_t)a.heads * HD;  // elements between consecutive tokens
-  // document of block g: last doc with blk_prefix[doc] <= g
-  int lo = 0, hi = n_seq;  // blk_prefix[lo] <= g < blk_prefix[hi]
-  while (hi - lo > 1) {
-    int mid = (lo + hi) >> 1;
-    if (__ldg(blk_prefix + mid) <= g) lo = mid; else hi = mid;
-  }
-  const int doc_start = __ldg(cu + lo), doc_end = __ldg(cu + lo + 1);
-  const int t0 = doc_start + 32 * (g - __ldg(blk_prefix + lo));
-  const int ntok = min(32, doc_end - t0);
+  const int t0 = loc.x, ntok = loc.y;
 
   RawRow<TIn, EPL> raw[32];
 #pragma unroll
@@ -156,6 +172,7 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int g, int h, 
     if (t < ntok) raw[t].load(x + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL);
     else raw[t].zero();
   }
+  if (g_next >= 0) loc_next = block_tokens(g_next, cu, blk_prefix, n_seq, lane);
   static_assert(!ROT || (!WITH_D && !NVFP4), "only Q/K/V launches of the MXFP8 path rotate");
   // token t's EPL values of this lane (rotated when the unit rotates; a zero
   // row stays zero).  ROT: `fresh` computes and stages them, else they are
@@ -394,15 +411,31 @@ __global__ void __launch_bounds__(128, (quant_blocks_per_sm<TIn, TO, WITH_D, NVF
   const int n_blk = hdr->n_blk32;
   int total = 0;
   for (int r = 0; r < qb.n; ++r) total += n_blk * qb.a[r].heads;
-  for (int unit = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); unit < total; unit += warps_total) {
-    int r = 0, u = unit;
+  // unit -> (tensor r, block g, head h)
+  auto split = [&](int unit, int& r, int& g, int& h) {
+    int u = unit;
+    r = 0;
     while (r + 1 < qb.n && u >= n_blk * qb.a[r].heads) {
       u -= n_blk * qb.a[r].heads;
       ++r;
     }
-    const QuantArgs& a = qb.a[r];
-    const int g = u / a.heads, h = u - g * a.heads;
-    quantize_unit<TIn, TO, HD, WITH_D, NVFP4, ROT>(a, g, h, cu, blk_prefix, n_seq, lane, stage);
+    g = u / qb.a[r].heads;
+    h = u - g * qb.a[r].heads;
+  };
+  int unit = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (unit >= total) return;
+  int r, g, h;
+  split(unit, r, g, h);
+  int2 loc = block_tokens(g, cu, blk_prefix, n_seq, lane);
+  for (; unit < total; unit += warps_total) {
+    const int nxt = unit + warps_total;
+    int r2 = 0, g2 = -1, h2 = 0;
+    if (nxt < total) split(nxt, r2, g2, h2);
+    int2 loc2 = loc;
+    quantize_unit<TIn, TO, HD, WITH_D, NVFP4, ROT>(qb.a[r], loc, h, g2, loc2, cu, blk_prefix, n_seq, lane, stage);
+    r = r2;
+    h = h2;
+    loc = loc2;
   }
 }
 
