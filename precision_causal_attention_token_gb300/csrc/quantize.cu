@@ -56,6 +56,27 @@ __device__ __forceinline__ float bf16x2_hmax_f32(uint32_t m) {
   return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
 }
 
+// transpose_reduce<true> on 32 non-negative bf16 values packed in pairs
+// (w[j] holds tokens 2j, 2j+1): four stages move whole registers (both
+// tokens of a pair at once), the last splits the pair.  Lane t ends with the
+// maximum of token t over all lanes (16 shuffles).
+__device__ __forceinline__ float transpose_max_bf16x2(uint32_t (&w)[16], int lane) {
+#pragma unroll
+  for (int s = 8; s >= 1; s >>= 1) {  // token stride 2s
+    const bool upper = (lane & (2 * s)) != 0;
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      const uint32_t send = upper ? w[i] : w[i + s];
+      const uint32_t keep = upper ? w[i + s] : w[i];
+      w[i] = bf16x2_absmax(keep, __shfl_xor_sync(0xffffffffu, send, 2 * s));
+    }
+  }
+  const bool odd = (lane & 1) != 0;  // lane 2k + 1 keeps token 2k + 1 (the high half)
+  const float keep = __uint_as_float(odd ? (w[0] & 0xFFFF0000u) : (w[0] << 16));
+  const float send = __uint_as_float(odd ? (w[0] << 16) : (w[0] & 0xFFFF0000u));
+  return fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+}
+
 // Smallest E4M3FN code whose value is >= r (r > 0), saturating at 448.
 __device__ __forceinline__ uint32_t e4m3_roundup(float r) {
   uint32_t c = pack_e4m3x2(r, 0.f) & 0xFFu;
@@ -230,34 +251,55 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int2 loc, int 
       e_blk = noclamp_exp_clamped(warp_max(fmaxf(fmaxf(lm[0], lm[1]), fmaxf(lm[2], lm[3]))));
     }
     int my_e = e_blk;  // exponent of token `lane`
+    if (a.per_token) {
+      // per-token maxima: each lane's maximum of every token, then one
+      // transpose-reduce leaves token `lane`'s maximum in lane `lane` (31
+      // shuffles for the unit instead of a warp reduction per token)
+      if constexpr (kPackedMax) {
+        // a token's lane maximum is a bf16 value: two tokens per register
+        uint32_t pm2[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          uint32_t m0 = 0u, m1 = 0u;
+#pragma unroll
+          for (int k = 0; k < RawRow<TIn, EPL>::kWords; ++k) {
+            m0 = bf16x2_absmax(m0, raw[2 * j].w[k]);
+            m1 = bf16x2_absmax(m1, raw[2 * j + 1].w[k]);
+          }
+          // fold each token's pair of halves, then pack token 2j low, 2j+1 high
+          const uint32_t f0 = bf16x2_absmax(m0, (m0 >> 16) | (m0 << 16));
+          const uint32_t f1 = bf16x2_absmax(m1, (m1 >> 16) | (m1 << 16));
+          pm2[j] = (f0 & 0xFFFFu) | (f1 << 16);
+        }
+        my_e = noclamp_exp_clamped(transpose_max_bf16x2(pm2, lane));
+      } else {
+        float pm[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          float v[EPL];
+          row_vals(t, v, true);
+          float lm = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) lm = fmaxf(lm, fabsf(v[e]));
+          pm[t] = lm;
+        }
+        my_e = noclamp_exp_clamped(transpose_reduce<true>(pm, lane));
+      }
+    }
+    const float my_inv = exp2i(max(-my_e, -126));
     // dO role: each token's code word is kept for D, and the dO values die
     // as the codes are made, so O's rows are read afterwards (below) without
     // both blocks held in registers at once
     uint32_t cws[WITH_D ? 32 : 1];
 #pragma unroll
     for (int t = 0; t < 32; ++t) {
-      int e_t = e_blk;
       float v[EPL];
-      row_vals(t, v, a.per_token != 0);  // token-block units staged them in the exponent pass
-      if (a.per_token) {
-        float lm = 0.f;
-        if constexpr (kPackedMax) {
-          uint32_t m2 = 0u;
-#pragma unroll
-          for (int k = 0; k < RawRow<TIn, EPL>::kWords; ++k) m2 = bf16x2_absmax(m2, raw[t].w[k]);
-          lm = bf16x2_hmax_f32(m2);
-        } else {
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) lm = fmaxf(lm, fabsf(v[e]));
-        }
-        e_t = noclamp_exp_clamped(warp_max(lm));
-        if (lane == t) my_e = e_t;
-      }
+      row_vals(t, v, false);  // staged by the exponent pass (rotated units)
+      // 2^-e is a normal fp32 for every exponent of finite data (e <= 120),
+      // so one multiply per element is exact down to the E4M3 range
+      const float inv_s = __shfl_sync(0xffffffffu, my_inv, a.per_token ? t : 0);
       if constexpr (WITH_D) cws[t] = 0u;
       if (t < ntok) {
-        // 2^-e_t is a normal fp32 for every exponent of finite data (e_t <= 120),
-        // so one multiply per element is exact down to the E4M3 range
-        const float inv_s = exp2i(max(-e_t, -126));
         const uint64_t s2 = f2_pack(inv_s, inv_s);
         float qv[EPL];
 #pragma unroll
