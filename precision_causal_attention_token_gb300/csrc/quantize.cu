@@ -320,19 +320,20 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int2 loc, int 
     if constexpr (WITH_D) {
       // D's terms are code * O (products exact in fp32); the exponent is
       // applied to the lane's partial sum (per token) or to the token's sum
-      // (token block).  O is read eight rows at a time.
+      // (token block).  O is read kOChunk rows at a time.
+      constexpr int kOChunk = sizeof(TO) == 2 ? 16 : 8;
       float dpart[32];
       const TO* __restrict__ Ob = static_cast<const TO*>(a.O) + (size_t)t0 * row + (size_t)h * HD + lane * EPL;
 #pragma unroll
-      for (int c8 = 0; c8 < 32; c8 += 8) {
-        RawRow<TO, EPL> orow[8];
+      for (int c8 = 0; c8 < 32; c8 += kOChunk) {
+        RawRow<TO, EPL> orow[kOChunk];
 #pragma unroll
-        for (int t8 = 0; t8 < 8; ++t8) {
+        for (int t8 = 0; t8 < kOChunk; ++t8) {
           if (c8 + t8 < ntok) orow[t8].load(Ob + (size_t)(c8 + t8) * row);
           else orow[t8].zero();
         }
 #pragma unroll
-        for (int t8 = 0; t8 < 8; ++t8) {
+        for (int t8 = 0; t8 < kOChunk; ++t8) {
           const int t = c8 + t8;
           const uint32_t cw = cws[t];
           float acc = 0.f;
