@@ -383,16 +383,16 @@ def _secondary(fl, idx, dev, stream, steps):
 
 
 def _option_overheads(fl, w, inputs, dev, stream, base_bwd_ms, steps):
-    """Backward time of the deterministic and exact options, of the FP16 dQ
-    partials (document-range and causal prescale) and of the Hadamard option
-    (whose cost is mostly in the Q/K/V quantizer and the back-rotation) on
-    the same workload, relative to the default backward."""
+    """Backward time of the deterministic and exact options, of fp32 dQ
+    partials instead of the default FP16 ones, of the causal dQ scale and of
+    the Hadamard option (whose cost is mostly in the Q/K/V quantizer and the
+    back-rotation) on the same workload, relative to the default backward."""
     import torch
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
     out = {}
     for name, kw in (("deterministic", {"deterministic": True}), ("exact", {"exact": True}),
-                     ("fp16_dq_partials", {"dq_fp16": True}),
-                     ("fp16_dq_partials_causal_scale", {"dq_fp16": True, "causal_dq_scale": True}),
+                     ("fp32_dq_partials", {"dq_fp16": False}),
+                     ("causal_dq_scale", {"causal_dq_scale": True}),
                      ("hadamard", {"hadamard": True})):
         tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu, **kw)
         step = _step_fn(fl, tc, inputs)
@@ -461,6 +461,7 @@ def run_ours(a):
     pairs = w.causal_pairs
     fwd_flops, bwd_flops = 4.0 * w.d * w.H * pairs, 10.0 * w.d * w.H * pairs
     stream = torch.cuda.current_stream()
+    dq16 = tc.dq_fp16
     step = _step_fn(fl, tc, (q, k, v, do))
 
     for _ in range(max(3, a.warmup)):
@@ -605,6 +606,7 @@ def run_ours(a):
         "config": {"workload": WORKLOAD.format(rows=a.rows) if a.workload == 2 else w.name, "tokens": w.T,
                    "heads": w.H, "head_dim": w.d, "documents": len(w.seqlens),
                    "flops_per_step": flops, "l2": "inputs larger than L2 (256 MiB of bf16 Q/K/V/dO)",
+                   "dq_partials": "fp16, power-of-two row prescale" if dq16 else "fp32",
                    "fraction_of_fp8_peak": value / world / fp8_burst,
                    "fraction_of_fp8_peak_sustained": value / world / fp8_sustained,
                    "timing": "CUDA graph of one training call, replayed; phases from an eager pass with events",

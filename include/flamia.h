@@ -83,12 +83,13 @@ typedef enum { FLAMIA_ROLE_QKV = 0, FLAMIA_ROLE_DO = 1 } flamia_role_t;
  *                accumulator); 0 from the whole document.
  *   dq_fp16      1: the default option's dQ partials (one per 128-key tile)
  *                are prescaled by a power of two per query row, rounded to
- *                FP16 and reduced into an FP16 accumulator ([READ] 四 4.4);
- *                0: fp32 partials into an fp32 accumulator (the default here:
- *                faster on this kernel, whose backward is bound by its compute
- *                warps, not by the reduction).  No effect on the exact and
- *                deterministic options and the mixed path, whose dQ sums in
- *                fp32 in a fixed order.
+ *                FP16 and reduced into an FP16 accumulator ([READ] 四 4.4;
+ *                the setting the Python training call uses by default: as
+ *                fast as fp32 on short documents, faster on long and packed
+ *                ones, where it halves the accumulator's traffic);
+ *                0: fp32 partials into an fp32 accumulator.  No effect on the
+ *                exact and deterministic options and the mixed path, whose
+ *                dQ sums in fp32 in a fixed order.
  *   deterministic 1: dQ reduced in a fixed order (no atomics).
  *   softmax_scale  0 selects 1/sqrt(d).
  *   path         flamia_path_t.

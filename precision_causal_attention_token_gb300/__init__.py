@@ -194,7 +194,7 @@ class TrainCall:
     exact: bool = False
     deterministic: bool = False
     causal_dq_scale: bool = False
-    dq_fp16: bool = False
+    dq_fp16: bool = True  # FP16 dQ partials with the power-of-two prescale (the pages' default)
     bitexp: bool = False  # inference forward only: backward() raises
     hadamard: bool = False  # Q and K rotated before quantization; gradients rotated back
     path: int = PATH_MXFP8

@@ -72,25 +72,27 @@ def test_empty_and_single_token_documents():
     assert np.abs(o[0] - vh[0]).max() <= (2.0 ** -4 + 2.0 ** -8) * np.abs(vh[0]).max()
 
 
-@pytest.mark.parametrize("wl,doc,head", [(2, 2, 5), (3, None, 7)])
-def test_full_size_sampled_against_oracle(wl, doc, head):
-    """Full-size workload in the launch configuration the benchmark times; the
-    oracle recomputes one (document, head) slice: attention never crosses
-    documents or heads, so the slice's outputs are the full call's."""
+@pytest.mark.parametrize("wl,doc,head,dq_fp16", [(2, 2, 5, True), (2, 1, 9, False), (3, None, 7, True)])
+def test_full_size_sampled_against_oracle(wl, doc, head, dq_fp16):
+    """Full-size workload in the launch configuration the benchmark times (FP16
+    dQ partials, the training call's default; fp32 partials too); the oracle
+    recomputes one (document, head) slice: attention never crosses documents
+    or heads, and the dQ prescale is per document and head, so the slice's
+    outputs are the full call's."""
     w = synth.workload(wl)
     q, k, v, do = (w.tensor(n) for n in ("q", "k", "v", "do"))
-    tc = run_gpu(w, inputs=(q, k, v, do))
+    tc = run_gpu(w, inputs=(q, k, v, do), dq_fp16=dq_fp16)
     lens = np.diff(w.cu_seqlens)
     if doc is None:  # a mid-sized document of the packed workload
         doc = int(np.argsort(lens)[len(lens) // 2])
     s, e = int(w.cu_seqlens[doc]), int(w.cu_seqlens[doc + 1])
     sl = lambda a: np.ascontiguousarray(a[s:e, head:head + 1])
     cu1 = np.array([0, e - s], np.int32)
-    ref = oracle.train_call(sl(q), sl(k), sl(v), sl(do), cu1, out_dtype="bf16")
+    ref = oracle.train_call(sl(q), sl(k), sl(v), sl(do), cu1, out_dtype="bf16", dq_fp16=dq_fp16)
     noise, od = None, None
     got = {n: getattr(tc, n)[s:e, head:head + 1] for n in ("O", "dQ", "dK", "dV")}
     if w.outlier_channels:
-        r64 = oracle.train_call(sl(q), sl(k), sl(v), sl(do), cu1, out_dtype="f64")
+        r64 = oracle.train_call(sl(q), sl(k), sl(v), sl(do), cu1, out_dtype="f64", dq_fp16=dq_fp16)
         noise = {n: ref[n] - r64[n] for n in ("dQ", "dK", "dV")}
         od = o_rows_differ(got["O"], ref["O"])
     print(f"doc {doc} ({e - s} tokens), head {head}")

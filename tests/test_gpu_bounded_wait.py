@@ -39,7 +39,7 @@ def test_forward_wait_runs_out_and_reports_timeout():
     tc.run(q, k, v, do)
     torch.cuda.synchronize()
     assert fl.flamia_get_device_status(tc.ws) == fl.OK
-    ref = run_oracle(w)
+    ref = run_oracle(w, dq_fp16=tc.dq_fp16)
     for name in ("O", "dQ", "dK", "dV"):
         compare(name, getattr(tc, name), ref[name])
 
