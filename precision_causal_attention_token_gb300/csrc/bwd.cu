@@ -1109,23 +1109,43 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, void* out, size
 }
 
 // The FP16 dQ accumulator (sums of 2^p dS^ K^ over key tiles) times the
-// softmax scale and 2^-p of its row -> output dtype.  Four values a thread.
-template <bool OUT_BF16>
-__global__ void dq16_convert_kernel(const __half* __restrict__ acc, const int8_t* __restrict__ pexp, void* out,
-                                  size_t n4, float scale, int T, int H, int d4) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-    const size_t row = i / (size_t)d4;  // (token, head) = (row / H, row % H)
-    const int t = (int)(row / (size_t)H), h = (int)(row - (size_t)t * H);
+// softmax scale and 2^-p of its row -> output dtype.  One warp per (token,
+// head) row: the row's prescale is read once, lane l converts elements
+// [l HD/32, (l + 1) HD/32).
+template <bool OUT_BF16, int HD>
+__global__ void __launch_bounds__(256) dq16_convert_kernel(const __half* __restrict__ acc,
+                                                           const int8_t* __restrict__ pexp, void* out, size_t rows,
+                                                           float scale, int T, int H) {
+  constexpr int EPL = HD / 32;
+  const int lane = threadIdx.x & 31;
+  const size_t warps = (size_t)gridDim.x * (blockDim.x >> 5);
+  for (size_t r = blockIdx.x * (size_t)(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+    const int t = (int)(r / (size_t)H), h = (int)(r - (size_t)t * H);
     const float f = scale * pow2_127(-(int)__ldg(pexp + (size_t)h * T + t));
-    const uint2 u = reinterpret_cast<const uint2*>(acc)[i];
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-    const float4 v = make_float4(a.x * f, a.y * f, b.x * f, b.y * f);
-    if constexpr (OUT_BF16) {
-      __nv_bfloat162 x = __floats2bfloat162_rn(v.x, v.y), y = __floats2bfloat162_rn(v.z, v.w);
-      reinterpret_cast<uint2*>(out)[i] = make_uint2(*reinterpret_cast<uint32_t*>(&x), *reinterpret_cast<uint32_t*>(&y));
+    const size_t o = r * HD + (size_t)lane * EPL;
+    float v[EPL];
+    if constexpr (EPL == 4) {
+      const uint2 u = *reinterpret_cast<const uint2*>(acc + o);
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+      v[0] = a.x * f; v[1] = a.y * f; v[2] = b.x * f; v[3] = b.y * f;
     } else {
-      reinterpret_cast<float4*>(out)[i] = v;
+      const uint32_t u = *reinterpret_cast<const uint32_t*>(acc + o);
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u));
+      v[0] = a.x * f; v[1] = a.y * f;
+    }
+    if constexpr (OUT_BF16) {
+      uint32_t w[EPL / 2];
+#pragma unroll
+      for (int e = 0; e < EPL; e += 2) {
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[e], v[e + 1]);
+        w[e / 2] = *reinterpret_cast<const uint32_t*>(&b2);
+      }
+      if constexpr (EPL == 4) *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + o) = make_uint2(w[0], w[1]);
+      else *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(out) + o) = w[0];
+    } else {
+      if constexpr (EPL == 4) *reinterpret_cast<float4*>(static_cast<float*>(out) + o) = make_float4(v[0], v[1], v[2], v[3]);
+      else *reinterpret_cast<float2*>(static_cast<float*>(out) + o) = make_float2(v[0], v[1]);
     }
   }
 }
@@ -1212,9 +1232,10 @@ static cudaError_t launch_rot_back(const void* src, const int8_t* pexp, void* ou
 // the largest key and value exponents over the row's document, or over keys
 // j <= i (a running maximum) with the causal dQ scale.  Then every partial
 // sum of 2^p_i dQ_i stays within 2^15 (close reading 4.4; FLAMIA summary §4.5).
-// One CTA per (document, KV head); 256 tokens at a time.
-__global__ void __launch_bounds__(256) dq_prescale_kernel(const AttnParams p) {
-  __shared__ int s_k[8], s_v[8];
+// One CTA per (document, KV head), kPrescaleThreads threads.
+constexpr int kPrescaleThreads = 1024;
+__global__ void __launch_bounds__(kPrescaleThreads) dq_prescale_kernel(const AttnParams p) {
+  __shared__ int s_k[kPrescaleThreads / 32], s_v[kPrescaleThreads / 32];
   __shared__ int carry_k, carry_v;
   const int doc = blockIdx.x, hk = blockIdx.y, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int s0 = __ldg(p.cu + doc), len = __ldg(p.cu + doc + 1) - s0;
@@ -1231,7 +1252,7 @@ __global__ void __launch_bounds__(256) dq_prescale_kernel(const AttnParams p) {
   __syncthreads();
   if (!prefix) {  // the document's maxima
     int mk = -1000, mv = -1000;
-    for (int j = tid; j < len; j += 256) {
+    for (int j = tid; j < len; j += kPrescaleThreads) {
       mk = max(mk, (int)__ldg(ksc + j) - 127);
       mv = max(mv, (int)__ldg(vsc + j) - 127);
     }
@@ -1242,41 +1263,65 @@ __global__ void __launch_bounds__(256) dq_prescale_kernel(const AttnParams p) {
       atomicMax(&carry_v, mv);
     }
     __syncthreads();
+    mk = carry_k;
+    mv = carry_v;
+    // every token independently (no chunk barriers): the loads of all of a
+    // thread's tokens and heads can be in flight together
+    for (int j = tid; j < len; j += kPrescaleThreads)
+      for (int g = 0; g < G; ++g) {
+        const int h = hk * G + g;
+        const int edo = (int)__ldg(p.do_sc + (size_t)h * p.T + s0 + j) - 127;
+        const int e = 15 - p.c0 - (edo + mk + mv);
+        p.pexp[(size_t)h * p.T + s0 + j] = (int8_t)(e < -126 ? -126 : (e > 127 ? 127 : e));
+      }
+    return;
   }
-  for (int c = 0; c < len; c += 256) {
+  // causal dQ scale: running maxima over keys j <= i, kPrescaleThreads tokens
+  // at a time (inclusive scan in each warp, then across the warps' totals)
+  for (int c = 0; c < len; c += kPrescaleThreads) {
     const int j = c + tid;
     int mk = j < len ? (int)__ldg(ksc + j) - 127 : -1000;
     int mv = j < len ? (int)__ldg(vsc + j) - 127 : -1000;
-    if (prefix) {  // running maxima: inclusive scan in the warp, then across warps
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int uk = __shfl_up_sync(0xffffffffu, mk, o), uv = __shfl_up_sync(0xffffffffu, mv, o);
+      if (lane >= o) {
+        mk = max(mk, uk);
+        mv = max(mv, uv);
+      }
+    }
+    if (lane == 31) {
+      s_k[wid] = mk;
+      s_v[wid] = mv;
+    }
+    __syncthreads();
+    if (wid == 0) {  // exclusive scan of the warps' totals, with the carry of earlier chunks
+      int tk = lane < kPrescaleThreads / 32 ? s_k[lane] : -1000;
+      int tv = lane < kPrescaleThreads / 32 ? s_v[lane] : -1000;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int uk = __shfl_up_sync(0xffffffffu, mk, o), uv = __shfl_up_sync(0xffffffffu, mv, o);
+        const int uk = __shfl_up_sync(0xffffffffu, tk, o), uv = __shfl_up_sync(0xffffffffu, tv, o);
         if (lane >= o) {
-          mk = max(mk, uk);
-          mv = max(mv, uv);
+          tk = max(tk, uk);
+          tv = max(tv, uv);
         }
       }
+      int ek = __shfl_up_sync(0xffffffffu, tk, 1), ev = __shfl_up_sync(0xffffffffu, tv, 1);
+      if (lane == 0) ek = ev = -1000;
+      const int ck = carry_k, cv = carry_v;
+      __syncwarp();
+      if (lane < kPrescaleThreads / 32) {
+        s_k[lane] = max(ek, ck);
+        s_v[lane] = max(ev, cv);
+      }
       if (lane == 31) {
-        s_k[wid] = mk;
-        s_v[wid] = mv;
+        carry_k = max(ck, tk);
+        carry_v = max(cv, tv);
       }
-      __syncthreads();
-      int pk = carry_k, pv = carry_v;
-      for (int w2 = 0; w2 < wid; ++w2) {
-        pk = max(pk, s_k[w2]);
-        pv = max(pv, s_v[w2]);
-      }
-      mk = max(mk, pk);
-      mv = max(mv, pv);
-      __syncthreads();
-      if (tid == 255) {  // the chunk's last token carries the running maxima on
-        carry_k = mk;
-        carry_v = mv;
-      }
-    } else {
-      mk = carry_k;
-      mv = carry_v;
     }
+    __syncthreads();
+    mk = max(mk, s_k[wid]);
+    mv = max(mv, s_v[wid]);
     if (j < len) {
       for (int g = 0; g < G; ++g) {
         const int h = hk * G + g;
@@ -1322,7 +1367,7 @@ static cudaError_t launch_bwd_t(const AttnParams& p, const AttnMaps& m, cudaStre
       if (p.dq_fp16) {
         if ((e = set_smem<bwd_kernel<HD, OB, EX, true, false, true>>(smem)) != cudaSuccess) return e;
         if ((e = cudaMemsetAsync(p.dq16, 0, 2 * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
-        if (p.n_seq > 0) dq_prescale_kernel<<<dim3(p.n_seq, p.Hkv), 256, 0, st>>>(p);
+        if (p.n_seq > 0) dq_prescale_kernel<<<dim3(p.n_seq, p.Hkv), kPrescaleThreads, 0, st>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         bwd_kernel<HD, OB, EX, true, false, true><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.dq, m.q,
                                                                                   m.q);
@@ -1334,10 +1379,12 @@ static cudaError_t launch_bwd_t(const AttnParams& p, const AttnMaps& m, cudaStre
           return launch_rot_back<OB, HD, false>(p.rot_dk, nullptr, p.dK, (size_t)p.T * p.Hkv, 1.f, p.T, p.Hkv, nsm,
                                                 st);
         }
-        if (OB)
-          dq16_convert_kernel<true><<<cg, 256, 0, st>>>(p.dq16, p.pexp, p.dQ, n4, p.softmax_scale, p.T, p.H, HD / 4);
-        else
-          dq16_convert_kernel<false><<<cg, 256, 0, st>>>(p.dq16, p.pexp, p.dQ, n4, p.softmax_scale, p.T, p.H, HD / 4);
+        {
+          const size_t rows = (size_t)p.T * p.H;
+          const size_t want = (rows + 7) / 8;  // eight warps a block, a row a warp
+          const int blocks = (int)(want < (size_t)nsm * 16 ? (want < 1 ? 1 : want) : (size_t)nsm * 16);
+          dq16_convert_kernel<OB, HD><<<blocks, 256, 0, st>>>(p.dq16, p.pexp, p.dQ, rows, p.softmax_scale, p.T, p.H);
+        }
       } else {
         if ((e = set_smem<bwd_kernel<HD, OB, EX, true, false, false>>(smem)) != cudaSuccess) return e;
         if ((e = cudaMemsetAsync(p.dq_acc, 0, 4 * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
