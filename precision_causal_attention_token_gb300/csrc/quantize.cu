@@ -495,6 +495,10 @@ static cudaError_t raise_smem_once(int smem) {
   return e;
 }
 
+// Grid size in waves of resident blocks (one, four and eight measured within
+// 3% of each other on the batched workload; four kept).
+constexpr int kQuantWaves = 4;
+
 // Host-side launcher (called by api.cu).
 cudaError_t launch_quantize(const QuantBatch& qb, int d, int in_bf16, int o_bf16, bool with_D, bool nvfp4,
                             const int32_t* cu, const int32_t* blk_prefix, int n_seq, WsHeader* hdr,
@@ -502,10 +506,10 @@ cudaError_t launch_quantize(const QuantBatch& qb, int d, int in_bf16, int o_bf16
   const int want = (max_units + 3) / 4;  // four warps per block, one unit per warp
   bool rot = false;
   for (int i = 0; i < qb.n; ++i) rot = rot || qb.a[i].rotate;
-  // at most four waves of resident blocks; the warps stride over the rest
+  // at most kQuantWaves waves of resident blocks; the warps stride over the rest
 #define FLAMIA_QL_R(TIN, TO_, HD_, WD, NV, RT)                                                            \
   do {                                                                                                    \
-    const int cap = quant_blocks_per_sm<TIN, TO_, WD, NV, RT>() * n_sms * 4;                              \
+    const int cap = quant_blocks_per_sm<TIN, TO_, WD, NV, RT>() * n_sms * kQuantWaves;                    \
     const int blocks = want < 1 ? 1 : (want > cap ? cap : want);                                          \
     const int smem = RT ? 4 * 32 * HD_ * (int)sizeof(float) : 0;                                          \
     if (RT) {                                                                                             \
