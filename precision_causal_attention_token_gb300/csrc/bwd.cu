@@ -154,9 +154,9 @@ __device__ __forceinline__ float ds_gbh(int Eb_b, int mi, float inv_l, float hdo
 __device__ __forceinline__ void ds_block(const uint32_t (&acc)[32], const uint32_t (&pcode_b)[8], float nDp,
                                          const float* vinv_b, float (&wv)[32], float (&uv)[32], float& amax_w,
                                          float& amax_u) {
-  // key pairs through the packed fp32 instructions; max |w| as the larger of
-  // max w and -min w, each in two partial chains of three-input max / min
-  float w_hi[2] = {0.f, 0.f}, w_lo[2] = {0.f, 0.f}, a_u[2] = {0.f, 0.f};
+  // key pairs through the packed fp32 instructions; max |w| in two partial
+  // chains of three-input max (the absolute values fold into its operands)
+  float a_w[2] = {0.f, 0.f}, a_u[2] = {0.f, 0.f};
   const uint64_t nD2 = f2_pack(nDp, nDp);
 #pragma unroll
   for (int q4 = 0; q4 < 8; ++q4) {
@@ -172,12 +172,11 @@ __device__ __forceinline__ void ds_block(const uint32_t (&acc)[32], const uint32
       const uint64_t y2 = f2_fma(nD2, vv2[h], f2_pack(__uint_as_float(acc[jj]), __uint_as_float(acc[jj + 1])));
       f2_unpack(f2_mul(pd2[h], y2), wv[jj], wv[jj + 1]);
       f2_unpack(f2_mul(pd2[h], vv2[h]), uv[jj], uv[jj + 1]);
-      w_hi[h] = fmax3(w_hi[h], wv[jj], wv[jj + 1]);
-      w_lo[h] = fmin3(w_lo[h], wv[jj], wv[jj + 1]);
+      a_w[h] = fmax3(a_w[h], fabsf(wv[jj]), fabsf(wv[jj + 1]));
       a_u[h] = fmax3(a_u[h], uv[jj], uv[jj + 1]);
     }
   }
-  amax_w = fmaxf(fmaxf(w_hi[0], w_hi[1]), -fminf(w_lo[0], w_lo[1]));
+  amax_w = fmaxf(a_w[0], a_w[1]);
   amax_u = fmaxf(a_u[0], a_u[1]);
 }
 
