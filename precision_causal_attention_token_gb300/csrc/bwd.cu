@@ -539,10 +539,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ dQ reducer
     // Each staged half is added into the accumulator by bulk tensor
     // reduce-adds (rows past the document's end hold zeros; rows past T are
-    // clipped by the copy).
+    // clipped by the copy).  Ordered (deterministic and exact options): the
+    // partials of a (query tile, head) go in key-tile order.  A counter per
+    // (query tile, head) holds how many have been added; this CTA (key tile
+    // kt) waits for it to read kt, and sets it to kt + 1 once its adds have
+    // completed, which it checks when its next tile's first half is staged
+    // (or at the item's end), so the wait for completion overlaps that
+    // tile's work.  Every wait points at a key tile with more query tiles,
+    // which the longest-first list hands out earlier: no cycle.
     if (DQ && lane == 0) {
       uint32_t ii = 0, hc = 0;  // hc: staged halves
       bool ok = true;
+      uint32_t* pend = nullptr;  // counter to release once the adds issued so far completed
+      uint32_t pend_val = 0;
+      auto release = [&]() {
+        if (pend != nullptr) {
+          bulk_wait_group0();          // this CTA's reduce-adds are performed
+          fence_proxy_async_global();  // ... before the counter is written
+          st_release_gpu(pend, pend_val);
+          pend = nullptr;
+        }
+      };
       for (uint32_t n_it = 0; ok; ++n_it) {
         const int w = item_get(c.ring, n_it, abort_flag, hdr, 0x332, ok);
         if (w < 0) break;
@@ -550,12 +567,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int2 it = p.bwd_items[pair];
         const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
         const int n_t = (len + kTile - 1) / kTile, q_first = p.causal ? it.y : 0;
+        const int tile0 = p.dq_ordered ? __ldg(p.tile_prefix + it.x) : 0;
         for (int g = 0; ok && g < G; ++g) {
           const int h = hk * G + g;
           for (int qt = q_first; ok && qt < n_t; ++qt, ++ii) {
             // one staged half (64 columns) at a time
             for (int half = 0; ok && half < HD / 64; ++half, ++hc) {
               if (!(ok = mbar_wait(&c.dqs_full, hc & 1, abort_flag, hdr, 0x331))) break;
+              if (p.dq_ordered && half == 0) {
+                release();
+                uint32_t* ctr = p.dq_order + (size_t)(tile0 + qt) * p.H + h;
+                // key tiles 0, 1, ... add in turn (causal: those <= qt; else all)
+                if (!(ok = counter_wait(ctr, (uint32_t)it.y, abort_flag, hdr, 0x333))) break;
+                fence_proxy_async_global();  // the reduce-adds below come after the acquire
+                pend = ctr;
+                pend_val = (uint32_t)it.y + 1u;
+              }
               if constexpr (DQ16) {
                 tma_reduce_add_3d(&map_dq, tl.dqs, 64 * half, h, ds + kTile * qt);
               } else {
@@ -569,8 +596,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
           }
         }
+        if (ok) release();  // before the next item: its waits may depend on this one
       }
       bulk_wait_group0();
+      if (ok) release();
     }
     __syncwarp();
    }
@@ -1349,8 +1378,13 @@ static cudaError_t set_smem(size_t smem) {
 }
 
 template <int HD, bool OB, bool EX, bool NV4>
-static cudaError_t launch_bwd_t(const AttnParams& p, const AttnMaps& m, cudaStream_t st) {
-  const bool det = p.exact || p.deterministic || NV4;
+static cudaError_t launch_bwd_t(const AttnParams& p_in, const AttnMaps& m, cudaStream_t st) {
+  // the deterministic and exact options add the dQ partials in key-tile
+  // order (fixed-order sums); only the mixed path keeps the separate dQ
+  // kernel, whose shared memory the bf16 score tiles leave no room for
+  AttnParams p = p_in;
+  p.dq_ordered = (!NV4 && (p.exact || p.deterministic)) ? 1 : 0;
+  const bool det = NV4;
   const int nsm = sm_count();
   long work = (long)p.max_items * p.Hkv;
   int grid = (int)(work < nsm ? work : nsm);
@@ -1363,7 +1397,10 @@ static cudaError_t launch_bwd_t(const AttnParams& p, const AttnMaps& m, cudaStre
       int cg = (int)((n4 + 255) / 256);
       if (cg > nsm * 8) cg = nsm * 8;
       if ((e = cudaMemsetAsync(&p.hdr->bwd_counter, 0, sizeof(uint32_t), st)) != cudaSuccess) return e;
-      if (p.dq_fp16) {
+      if (p.dq_ordered &&
+          (e = cudaMemsetAsync(p.dq_order, 0, sizeof(uint32_t) * (size_t)p.max_items * p.H, st)) != cudaSuccess)
+        return e;
+      if (p.dq_fp16 && !p.dq_ordered) {  // the exact and deterministic options sum fp32 partials
         if ((e = set_smem<bwd_kernel<HD, OB, EX, true, false, true>>(smem)) != cudaSuccess) return e;
         if ((e = cudaMemsetAsync(p.dq16, 0, 2 * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
         if (p.n_seq > 0) dq_prescale_kernel<<<dim3(p.n_seq, p.Hkv), kPrescaleThreads, 0, st>>>(p);

@@ -55,6 +55,7 @@ struct WsLayout {
   size_t dq_acc;           // [T][H][d] dQ accumulator: fp32, or binary16 with dq_fp16
   size_t pexp;             // int8 [H][T]: the dQ prescale exponent of each query row
   size_t rot_dk;           // hadamard: fp32 [T][Hkv][d] dK before the back-rotation
+  size_t dq_order;         // uint32 [max_items][H]: ordered dQ reduction counters
   size_t nv_q, nv_k;       // mixed path: bf16 [T][H][d] / [T][Hkv][d], NVFP4 values without the token scale
   size_t total;
   int32_t max_items;       // upper bound of tiles: ceil(T/128) + n_seq
@@ -78,9 +79,12 @@ inline WsLayout ws_layout(const flamia_problem_t& p) {
   L.keys_a = o; o = align256(o + sizeof(uint64_t) * L.sort_n * 2);
   L.keys_b = o; o = align256(o + sizeof(uint64_t) * L.sort_n * 2);
   // fp32 unless the FP16 partials alone use it (the rotation's back-transform
-  // reads every dQ path's result from here in fp32)
-  L.dq_acc = o; o = align256(o + (p.dq_fp16 && !p.hadamard ? 2 : 4) * (size_t)p.T * p.H * p.d);
+  // reads every dQ path's result from here in fp32; the exact and
+  // deterministic options sum fp32 partials)
+  const bool acc16 = p.dq_fp16 && !p.hadamard && !p.exact && !p.deterministic;
+  L.dq_acc = o; o = align256(o + (acc16 ? 2 : 4) * (size_t)p.T * p.H * p.d);
   L.pexp = o; o = align256(o + (size_t)p.T * p.H);
+  L.dq_order = o; o = align256(o + sizeof(uint32_t) * (size_t)L.max_items * p.H);
   L.rot_dk = 0;
   if (p.hadamard) {  // dK in the rotated basis, fp32, before the back-rotation
     L.rot_dk = o; o = align256(o + 4 * (size_t)p.T * p.Hkv * p.d);
@@ -271,6 +275,36 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      report(hdr, FLAMIA_ERR_TIMEOUT, where);
+      return false;
+    }
+  }
+}
+
+// Bounded wait (one thread) for a counter in global memory, written by other
+// CTAs, to reach `want` (acquire): the ordered dQ reduction.  Same limit and
+// abort protocol as mbar_wait.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders earlier generic-proxy accesses before later async-proxy (bulk copy)
+// accesses of global memory, and the reverse.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+__device__ __forceinline__ bool counter_wait(const uint32_t* ctr, uint32_t want, volatile int* abort_flag,
+                                             WsHeader* hdr, uint32_t where) {
+  if (ld_acquire_gpu(ctr) == want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(ctr) == want) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;

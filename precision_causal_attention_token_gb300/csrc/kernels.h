@@ -52,6 +52,8 @@ struct AttnParams {
   int bitexp;           // 1: forward with bit-level exponentials (inference only)
   int hadamard;         // 1: Q, K rotated; dQ, dK go through fp32 buffers and are rotated back
   float* rot_dk;        // hadamard: fp32 [T][Hkv][d] dK (times the softmax scale), rotated basis
+  uint32_t* dq_order;   // [tiles][H]: dQ partials already added to each (query tile, head), in key-tile order
+  int dq_ordered;       // 1: the partials are added in key-tile order (deterministic and exact options)
   const float* D;       // [H][T]
   int32_t* m;           // [H][T]
   float* l;             // [H][T]
