@@ -541,23 +541,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // reduce-adds (rows past the document's end hold zeros; rows past T are
     // clipped by the copy).  Ordered (deterministic and exact options): the
     // partials of a (query tile, head) go in key-tile order.  A counter per
-    // (query tile, head) holds how many have been added; this CTA (key tile
-    // kt) waits for it to read kt, and sets it to kt + 1 once its adds have
-    // completed, which it checks when its next tile's first half is staged
-    // (or at the item's end), so the wait for completion overlaps that
-    // tile's work.  Every wait points at a key tile with more query tiles,
-    // which the longest-first list hands out earlier: no cycle.
+    // (query tile, head) holds how many have been added: this CTA (key tile
+    // kt) waits for it to read kt (the load is issued a tile ahead, so in the
+    // steady state it has long returned),
+    // and sets it to kt + 1 once its adds have completed: a tile's counter
+    // is released when the tile after next is staged (or at the item's end),
+    // by then its adds, issued a tile earlier, have completed and the wait
+    // for them costs nothing; releasing never waits on another CTA.  Every
+    // wait points at a key tile with more query tiles, which the
+    // longest-first list hands out earlier: no cycle.
     if (DQ && lane == 0) {
+      constexpr int kHalves = HD / 64;
       uint32_t ii = 0, hc = 0;  // hc: staged halves
       bool ok = true;
-      uint32_t* pend = nullptr;  // counter to release once the adds issued so far completed
-      uint32_t pend_val = 0;
-      auto release = [&]() {
-        if (pend != nullptr) {
-          bulk_wait_group0();          // this CTA's reduce-adds are performed
-          fence_proxy_async_global();  // ... before the counter is written
-          st_release_gpu(pend, pend_val);
-          pend = nullptr;
+      // counters of the two previous tiles, released once their adds completed
+      uint32_t* pend[2] = {nullptr, nullptr};
+      uint32_t pend_val[2] = {0u, 0u};
+      auto release = [&](int k) {
+        if (pend[k] != nullptr) {
+          fence_proxy_async_global();  // the completed reduce-adds before the counter
+          st_release_gpu(pend[k], pend_val[k]);
+          pend[k] = nullptr;
         }
       };
       for (uint32_t n_it = 0; ok; ++n_it) {
@@ -568,20 +572,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
         const int n_t = (len + kTile - 1) / kTile, q_first = p.causal ? it.y : 0;
         const int tile0 = p.dq_ordered ? __ldg(p.tile_prefix + it.x) : 0;
+        // key tiles 0, 1, ... add in turn (causal: those <= qt; else all)
+        const uint32_t want = (uint32_t)it.y;
+        uint32_t seen = p.dq_ordered ? ld_acquire_gpu(p.dq_order + (size_t)(tile0 + q_first) * p.H + hk * G) : 0u;
         for (int g = 0; ok && g < G; ++g) {
           const int h = hk * G + g;
           for (int qt = q_first; ok && qt < n_t; ++qt, ++ii) {
+            uint32_t* const ctr = p.dq_ordered ? p.dq_order + (size_t)(tile0 + qt) * p.H + h : nullptr;
             // one staged half (64 columns) at a time
-            for (int half = 0; ok && half < HD / 64; ++half, ++hc) {
+            for (int half = 0; ok && half < kHalves; ++half, ++hc) {
               if (!(ok = mbar_wait(&c.dqs_full, hc & 1, abort_flag, hdr, 0x331))) break;
               if (p.dq_ordered && half == 0) {
-                release();
-                uint32_t* ctr = p.dq_order + (size_t)(tile0 + qt) * p.H + h;
-                // key tiles 0, 1, ... add in turn (causal: those <= qt; else all)
-                if (!(ok = counter_wait(ctr, (uint32_t)it.y, abort_flag, hdr, 0x333))) break;
+                // the tile before last: every group but the last tile's has completed
+                bulk_wait_group<kHalves>();
+                release(0);
+                if (seen != want && !(ok = counter_wait(ctr, want, abort_flag, hdr, 0x333))) break;
                 fence_proxy_async_global();  // the reduce-adds below come after the acquire
-                pend = ctr;
-                pend_val = (uint32_t)it.y + 1u;
               }
               if constexpr (DQ16) {
                 tma_reduce_add_3d(&map_dq, tl.dqs, 64 * half, h, ds + kTile * qt);
@@ -594,12 +600,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               bulk_wait_group_read0();
               mbar_arrive(&c.dqs_free);
             }
+            if (p.dq_ordered && ok) {
+              pend[0] = pend[1];
+              pend_val[0] = pend_val[1];
+              pend[1] = ctr;
+              pend_val[1] = want + 1u;
+              // the next tile's counter, read now (its value is used a tile later)
+              const int qn = qt + 1 < n_t ? qt + 1 : q_first, hn = qt + 1 < n_t ? h : h + 1;
+              if (qt + 1 < n_t || g + 1 < G) seen = ld_acquire_gpu(p.dq_order + (size_t)(tile0 + qn) * p.H + hn);
+            }
           }
         }
-        if (ok) release();  // before the next item: its waits may depend on this one
+        if (ok) {  // before the next item: its waits may depend on this one
+          bulk_wait_group0();
+          release(0);
+          release(1);
+        }
       }
       bulk_wait_group0();
-      if (ok) release();
+      if (ok) {
+        release(0);
+        release(1);
+      }
     }
     __syncwarp();
    }
