@@ -377,6 +377,18 @@ def _secondary(fl, idx, dev, stream, steps):
            "fwd_tflops": 4.0 * w.d * w.H * pairs / (fw * 1e-3) / 1e12,
            "bwd_tflops": 10.0 * w.d * w.H * pairs / (bw * 1e-3) / 1e12,
            "phase_ms": {"quantize_qkv": qk, "fwd": fw, "quantize_do": qd, "bwd+dq_convert": bw}}
+    del graph, tc
+    # the same step with the work items handed out by cluster launch control
+    tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu, clc=True)
+    step = _step_fn(fl, tc, inputs)
+    for _ in range(2):
+        step()
+    (_, _, fw_c, _, bw_c), _ = _phases(step, 2, stream)
+    graph, ms_c = _graph_ms(step, steps, stream)
+    st = fl.flamia_get_device_status(tc.ws)
+    if st != fl.OK:
+        raise RuntimeError(f"workload {idx} (clc): {fl.status_string(st)}")
+    res["clc"] = {"ms_per_step": ms_c, "fwd_ms": fw_c, "bwd_ms": bw_c, "vs_counter": ms / ms_c}
     del graph, tc, inputs
     torch.cuda.empty_cache()
     return res
@@ -384,16 +396,17 @@ def _secondary(fl, idx, dev, stream, steps):
 
 def _option_overheads(fl, w, inputs, dev, stream, base_bwd_ms, steps):
     """Backward time of the deterministic and exact options, of fp32 dQ
-    partials instead of the default FP16 ones, of the causal dQ scale and of
+    partials instead of the default FP16 ones, of the causal dQ scale, of
     the Hadamard option (whose cost is mostly in the Q/K/V quantizer and the
-    back-rotation) on the same workload, relative to the default backward."""
+    back-rotation) and of cluster launch control instead of the persistent
+    grid's counter, on the same workload, relative to the default backward."""
     import torch
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
     out = {}
     for name, kw in (("deterministic", {"deterministic": True}), ("exact", {"exact": True}),
                      ("fp32_dq_partials", {"dq_fp16": False}),
                      ("causal_dq_scale", {"causal_dq_scale": True}),
-                     ("hadamard", {"hadamard": True})):
+                     ("hadamard", {"hadamard": True}), ("clc", {"clc": True})):
         tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu, **kw)
         step = _step_fn(fl, tc, inputs)
         for _ in range(2):

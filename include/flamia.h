@@ -121,6 +121,21 @@ typedef enum { FLAMIA_ROLE_QKV = 0, FLAMIA_ROLE_DO = 1 } flamia_role_t;
  *                hold rotated codes.  MXFP8 path only (else
  *                FLAMIA_ERR_UNSUPPORTED); the workspace grows by
  *                4 T Hkv d bytes.
+ *   clc          how flamia_fwd and flamia_bwd hand out the longest-first
+ *                work items ([SUM] §3.6.2 Load-Balanced Scheduling and
+ *                [READ] 四 4.4, GPU-side scheduling: cluster launch control
+ *                for skewed and causal calls).  1: the grid has one CTA per
+ *                item (item = blockIdx.x, (ceil(T/128) + n_seq) * heads CTAs,
+ *                those past the plan's item count exit at once); a CTA that
+ *                finishes its item cancels a CTA not yet launched
+ *                (clusterlaunchcontrol.try_cancel) and takes that item, and
+ *                stops when none is left.  0: a persistent grid of one CTA
+ *                per SM takes items from a global counter.  Results are the
+ *                same up to the order of the dQ partials' additions.  Not
+ *                with the exact or deterministic options
+ *                (FLAMIA_ERR_UNSUPPORTED): their ordered dQ reduction waits
+ *                on items earlier in the list, which the counter hands out
+ *                first and cancellation need not.
  */
 typedef struct {
   int32_t T, H, Hkv, d, n_seq;
@@ -131,6 +146,7 @@ typedef struct {
   int32_t dq_fp16;
   int32_t bitexp;
   int32_t hadamard;
+  int32_t clc;
 } flamia_problem_t;
 
 /* A quantized operand (device pointers, caller-owned).

@@ -38,7 +38,7 @@ class Problem(ctypes.Structure):
                 ("exact", ctypes.c_int32), ("causal_dq_scale", ctypes.c_int32), ("deterministic", ctypes.c_int32),
                 ("softmax_scale", ctypes.c_float), ("path", ctypes.c_int32), ("in_dtype", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("dq_fp16", ctypes.c_int32), ("bitexp", ctypes.c_int32),
-                ("hadamard", ctypes.c_int32)]
+                ("hadamard", ctypes.c_int32), ("clc", ctypes.c_int32)]
 
 
 class Operand(ctypes.Structure):
@@ -103,12 +103,12 @@ def _stream(stream) -> int | None:
 
 def make_problem(T, H, Hkv, d, cu_seqlens, *, causal=True, exact=False, causal_dq_scale=False,
                  deterministic=False, softmax_scale=0.0, path=PATH_MXFP8, in_dtype=BF16, out_dtype=BF16,
-                 dq_fp16=False, bitexp=False, hadamard=False) -> Problem:
+                 dq_fp16=False, bitexp=False, hadamard=False, clc=False) -> Problem:
     """cu_seqlens: int32 device tensor [n_seq + 1] (kept referenced by the caller)."""
     return Problem(int(T), int(H), int(Hkv), int(d), int(cu_seqlens.numel() - 1), cu_seqlens.data_ptr(),
                    int(causal), int(exact), int(causal_dq_scale), int(deterministic), float(softmax_scale),
                    int(path), int(in_dtype), int(out_dtype), int(dq_fp16), int(bitexp),
-                   int(hadamard))
+                   int(hadamard), int(clc))
 
 
 def operand(codes, scales, codes4=None, scales4=None, gscale4=None) -> Operand:
@@ -197,6 +197,7 @@ class TrainCall:
     dq_fp16: bool = True  # FP16 dQ partials with the power-of-two prescale (the pages' default)
     bitexp: bool = False  # inference forward only: backward() raises
     hadamard: bool = False  # Q and K rotated before quantization; gradients rotated back
+    clc: bool = False  # work items taken over by cluster launch control (a CTA per item)
     path: int = PATH_MXFP8
     in_dtype: int = BF16
     out_dtype: int = BF16
@@ -208,7 +209,7 @@ class TrainCall:
         self.prob = make_problem(self.T, self.H, self.Hkv, self.d, self.cu_seqlens, causal=self.causal,
                                  exact=self.exact, deterministic=self.deterministic,
                                  causal_dq_scale=self.causal_dq_scale, dq_fp16=self.dq_fp16, bitexp=self.bitexp,
-                                 hadamard=self.hadamard,
+                                 hadamard=self.hadamard, clc=self.clc,
                                  softmax_scale=self.softmax_scale, path=self.path, in_dtype=self.in_dtype,
                                  out_dtype=self.out_dtype)
         nbytes = flamia_workspace_size(self.prob)

@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstddef>
 #include <atomic>
+#include <cstdint>
 #include <cstring>
 #include <cudaTypedefs.h>
 
@@ -30,6 +31,10 @@ flamia_status_t validate(const flamia_problem_t* p) {
   if (p->path == FLAMIA_PATH_NVFP4_FP8 && p->exact) return FLAMIA_ERR_UNSUPPORTED;
   if (p->bitexp && (p->path != FLAMIA_PATH_MXFP8 || p->exact)) return FLAMIA_ERR_UNSUPPORTED;
   if (p->hadamard && p->path != FLAMIA_PATH_MXFP8) return FLAMIA_ERR_UNSUPPORTED;
+  // cluster launch control: not with the ordered dQ reduction (its waits need
+  // the items taken in list order); the grid (a CTA per item) must fit in x
+  if (p->clc && (p->exact || p->deterministic)) return FLAMIA_ERR_UNSUPPORTED;
+  if (p->clc && ((int64_t)(p->T + 127) / 128 + p->n_seq) * p->H > INT32_MAX) return FLAMIA_ERR_UNSUPPORTED;
   if ((p->in_dtype != FLAMIA_F32 && p->in_dtype != FLAMIA_BF16) ||
       (p->out_dtype != FLAMIA_F32 && p->out_dtype != FLAMIA_BF16))
     return FLAMIA_ERR_UNSUPPORTED;
@@ -258,6 +263,7 @@ static flamia_status_t fill_params(const flamia_problem_t* p, const WsLayout& L,
   a->hadamard = p->hadamard ? 1 : 0;
   a->rot_dk = p->hadamard ? reinterpret_cast<float*>(w + L.rot_dk) : nullptr;
   a->dq_order = reinterpret_cast<uint32_t*>(w + L.dq_order);
+  a->clc = p->clc ? 1 : 0;
   a->dbg_withhold = g_dbg_withhold.load();
   return FLAMIA_OK;
 }

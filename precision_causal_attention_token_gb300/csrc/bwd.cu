@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint32_t ic = 0, ii = 0;
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it, ++ic) {
-      const int w = item_publish(c.ring, n_it, &hdr->bwd_counter, n_work, lane, abort_flag, hdr, 0x304, ok, p.dbg_withhold);
+      const int w = item_publish(c.ring, n_it, &hdr->bwd_counter, n_work, lane, abort_flag, hdr, 0x304, ok, p.dbg_withhold, p.clc);
       if (w < 0) break;
       const int pair = w / p.Hkv, hk = w - pair * p.Hkv;
       const int2 it = p.bwd_items[pair];
@@ -963,7 +963,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     uint32_t ic = 0, kv = 0;
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it, ++ic) {
-      const int w = item_publish(c.ring, n_it, &hdr->dq_counter, n_work, lane, abort_flag, hdr, 0x404, ok, p.dbg_withhold);
+      const int w = item_publish(c.ring, n_it, &hdr->dq_counter, n_work, lane, abort_flag, hdr, 0x404, ok, p.dbg_withhold, p.clc);
       if (w < 0) break;
       const int pair = w / p.H, h = w - pair * p.H, hk = h / G;
       const int2 it = p.fwd_items[pair];
@@ -1408,8 +1408,7 @@ static cudaError_t launch_bwd_t(const AttnParams& p_in, const AttnMaps& m, cudaS
   p.dq_ordered = (!NV4 && (p.exact || p.deterministic)) ? 1 : 0;
   const bool det = NV4;
   const int nsm = sm_count();
-  long work = (long)p.max_items * p.Hkv;
-  int grid = (int)(work < nsm ? work : nsm);
+  const int grid = attn_grid((long)p.max_items * p.Hkv, nsm, p.clc);
   cudaError_t e;
   if constexpr (!NV4) {
     if (!det) {
@@ -1423,12 +1422,12 @@ static cudaError_t launch_bwd_t(const AttnParams& p_in, const AttnMaps& m, cudaS
           (e = cudaMemsetAsync(p.dq_order, 0, sizeof(uint32_t) * (size_t)p.max_items * p.H, st)) != cudaSuccess)
         return e;
       if (p.dq_fp16 && !p.dq_ordered) {  // the exact and deterministic options sum fp32 partials
-        if ((e = set_smem<bwd_kernel<HD, OB, EX, true, false, true>>(smem)) != cudaSuccess) return e;
+        if ((e = set_smem<bwd_kernel<HD, OB, EX, true, false, true>>(attn_smem_max(smem))) != cudaSuccess) return e;
         if ((e = cudaMemsetAsync(p.dq16, 0, 2 * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
         if (p.n_seq > 0) dq_prescale_kernel<<<dim3(p.n_seq, p.Hkv), kPrescaleThreads, 0, st>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        bwd_kernel<HD, OB, EX, true, false, true><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.dq, m.q,
-                                                                                  m.q);
+        bwd_kernel<HD, OB, EX, true, false, true><<<grid, kBwdThreads, attn_smem(smem, p.clc), st>>>(
+            p, m.q, m.k, m.v, m.dO, m.dq, m.q, m.q);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if (p.hadamard) {
           if ((e = launch_rot_back<OB, HD, true>(p.dq16, p.pexp, p.dQ, (size_t)p.T * p.H, p.softmax_scale, p.T, p.H,
@@ -1444,10 +1443,10 @@ static cudaError_t launch_bwd_t(const AttnParams& p_in, const AttnMaps& m, cudaS
           dq16_convert_kernel<OB, HD><<<blocks, 256, 0, st>>>(p.dq16, p.pexp, p.dQ, rows, p.softmax_scale, p.T, p.H);
         }
       } else {
-        if ((e = set_smem<bwd_kernel<HD, OB, EX, true, false, false>>(smem)) != cudaSuccess) return e;
+        if ((e = set_smem<bwd_kernel<HD, OB, EX, true, false, false>>(attn_smem_max(smem))) != cudaSuccess) return e;
         if ((e = cudaMemsetAsync(p.dq_acc, 0, 4 * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
-        bwd_kernel<HD, OB, EX, true, false, false><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.dq, m.q,
-                                                                                   m.q);
+        bwd_kernel<HD, OB, EX, true, false, false><<<grid, kBwdThreads, attn_smem(smem, p.clc), st>>>(
+            p, m.q, m.k, m.v, m.dO, m.dq, m.q, m.q);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if (p.hadamard) {
           if ((e = launch_rot_back<OB, HD, false>(p.dq_acc, nullptr, p.dQ, (size_t)p.T * p.H, p.softmax_scale, p.T,
@@ -1465,17 +1464,17 @@ static cudaError_t launch_bwd_t(const AttnParams& p_in, const AttnMaps& m, cudaS
   const size_t smem = bwd_smem_bytes<HD, EX, false, NV4>();
   static_assert(bwd_smem_bytes<HD, EX, false, NV4>() <= 232448, "shared memory");
   static_assert(dq_smem_bytes<HD, NV4>() <= 232448, "shared memory");
-  if ((e = set_smem<bwd_kernel<HD, OB, EX, false, NV4, false>>(smem)) != cudaSuccess) return e;
+  if ((e = set_smem<bwd_kernel<HD, OB, EX, false, NV4, false>>(attn_smem_max(smem))) != cudaSuccess) return e;
   // work counters of the two launches below
   if ((e = cudaMemsetAsync(&p.hdr->bwd_counter, 0, 2 * sizeof(uint32_t), st)) != cudaSuccess) return e;
   // without DQ the dQ map is not read (the q map stands in for the argument)
-  bwd_kernel<HD, OB, EX, false, NV4, false><<<grid, kBwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.dO, m.q, m.qn, m.kn);
+  bwd_kernel<HD, OB, EX, false, NV4, false><<<grid, kBwdThreads, attn_smem(smem, p.clc), st>>>(p, m.q, m.k, m.v, m.dO,
+                                                                                               m.q, m.qn, m.kn);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t dsm = dq_smem_bytes<HD, NV4>();
-  if ((e = set_smem<dq_kernel<HD, OB, EX, NV4>>(dsm)) != cudaSuccess) return e;
-  long dwork = (long)p.max_items * p.H;
-  int dgrid = (int)(dwork < nsm ? dwork : nsm);
-  dq_kernel<HD, OB, EX, NV4><<<dgrid, kDqThreads, dsm, st>>>(p, m.q, m.k, m.v, m.dO, m.qn, m.kn);
+  if ((e = set_smem<dq_kernel<HD, OB, EX, NV4>>(attn_smem_max(dsm))) != cudaSuccess) return e;
+  const int dgrid = attn_grid((long)p.max_items * p.H, nsm, p.clc);
+  dq_kernel<HD, OB, EX, NV4><<<dgrid, kDqThreads, attn_smem(dsm, p.clc), st>>>(p, m.q, m.k, m.v, m.dO, m.qn, m.kn);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (!NV4 && p.hadamard) {  // both kernels left fp32 gradients of the rotated operands
     if ((e = launch_rot_back<OB, HD, false>(p.dq_acc, nullptr, p.dQ, (size_t)p.T * p.H, 1.f, p.T, p.H, nsm, st)) !=

@@ -325,16 +325,25 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, v
 }
 
 // ---------------------------------------------------------------------------
-// Dynamic work distribution of the persistent kernels: the producer warp takes
-// the next item of the longest-first list from a global counter and publishes
-// it in a small shared-memory ring; every other warp role reads the items in
-// the same order from the ring, so all roles of a CTA agree on its items.
-// -1 marks the end.  Slots are released as soon as they are read.
+// Dynamic work distribution: the producer warp takes the next item of the
+// longest-first list and publishes it in a small shared-memory ring; every
+// other warp role reads the items in the same order from the ring, so all
+// roles of a CTA agree on its items.  -1 marks the end.  Slots are released
+// as soon as they are read.  Two ways to take the next item:
+//  * persistent grid (one CTA per SM): a global counter (atomicAdd);
+//  * cluster launch control (one CTA per item, blockIdx.x = the item): the
+//    CTA starts with its own item, then asks the hardware to cancel a CTA of
+//    the grid that has not been launched yet and takes that CTA's item; when
+//    no CTA is left to cancel, the CTA is done.  Every item is processed
+//    once: by its own CTA if that one is launched, else by the CTA that
+//    cancelled it.
 // ---------------------------------------------------------------------------
 constexpr int kItemRing = 4;
 struct ItemRing {
   int item[kItemRing];
   uint64_t full[kItemRing], empty[kItemRing];
+  uint64_t clc_bar;                   // completion of a cancellation request
+  alignas(16) uint32_t clc_resp[4];  // its 16-byte response
 };
 
 __device__ __forceinline__ void item_ring_init(ItemRing& r, uint32_t consumers) {
@@ -342,26 +351,75 @@ __device__ __forceinline__ void item_ring_init(ItemRing& r, uint32_t consumers) 
     mbar_init(&r.full[s], 1);
     mbar_init(&r.empty[s], consumers);
   }
+  mbar_init(&r.clc_bar, 1);
 }
 
-// Producer warp (all lanes): fetch the n-th item of this CTA; -1 when none is left.
+// Cluster launch control (PTX ISA 8.6, sm_100 and later; the grid's clusters
+// are single CTAs here): request the cancellation of a not yet launched CTA;
+// the response lands in `resp` and completes 16 bytes of `bar`'s transaction.
+__device__ __forceinline__ void clc_try_cancel(uint32_t* resp, uint64_t* bar) {
+  asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+               ::"r"(smem_u32(resp)), "r"(smem_u32(bar)) : "memory");
+}
+// The x index of the CTA a completed response cancelled, or -1 if the request
+// found no CTA left to cancel.
+__device__ __forceinline__ int clc_cancelled_x(const uint32_t* resp) {
+  const uint32_t w0 = reinterpret_cast<const volatile uint32_t*>(resp)[0];
+  const uint32_t w1 = reinterpret_cast<const volatile uint32_t*>(resp)[1];
+  const uint32_t w2 = reinterpret_cast<const volatile uint32_t*>(resp)[2];
+  const uint32_t w3 = reinterpret_cast<const volatile uint32_t*>(resp)[3];
+  const uint64_t lo = ((uint64_t)w1 << 32) | w0, hi = ((uint64_t)w3 << 32) | w2;
+  uint32_t cancelled;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "mov.b128 r, {%1, %2};\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(cancelled) : "l"(lo), "l"(hi));
+  if (!cancelled) return -1;
+  uint32_t x;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t"
+      "mov.b128 r, {%1, %2};\n\t"
+      "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, r;\n\t}"
+      : "=r"(x) : "l"(lo), "l"(hi));
+  return (int)x;
+}
+
+// Producer warp (all lanes): fetch the n-th item of this CTA; -1 when none is
+// left.  clc: by cluster launch control (the grid has a CTA per item), else
+// from the global counter.  After a -1 the producer asks for nothing more.
 // withhold_first (a test hook, a kernel parameter): the first item is never
 // published, so every consumer's wait for it runs out.
 __device__ __forceinline__ int item_publish(ItemRing& r, uint32_t n, uint32_t* counter, int n_work, int lane,
                                             volatile int* abort_flag, WsHeader* hdr, uint32_t where, bool& ok,
-                                            int withhold_first) {
+                                            int withhold_first, int clc) {
   const int s = (int)(n % kItemRing);
   if (!(ok = mbar_wait_warp(&r.empty[s], ((n / kItemRing) & 1) ^ 1, abort_flag, hdr, where))) return -1;
   // nothing has been issued yet when the first item is withheld, so the CTA
   // exits cleanly after its consumers' waits run out
   if (n == 0 && withhold_first) return -1;
-  int w = 0;
+  int w = 0, fail = 0;
   if (lane == 0) {
-    w = (int)atomicAdd(counter, 1u);
+    if (!clc) {
+      w = (int)atomicAdd(counter, 1u);
+    } else if (n == 0) {
+      w = (int)blockIdx.x;
+    } else {  // request n - 1 of this CTA: phase (n - 1) & 1
+      mbar_arrive_expect_tx(&r.clc_bar, 16);
+      clc_try_cancel(r.clc_resp, &r.clc_bar);
+      if (mbar_wait(&r.clc_bar, (n - 1) & 1, abort_flag, hdr, where | 0x80)) {
+        w = clc_cancelled_x(r.clc_resp);
+      } else {
+        w = -1;
+        fail = 1;
+      }
+    }
     if (w >= n_work) w = -1;
     r.item[s] = w;
     mbar_arrive(&r.full[s]);
   }
+  if (__shfl_sync(0xffffffffu, fail, 0)) ok = false;
   return __shfl_sync(0xffffffffu, w, 0);
 }
 

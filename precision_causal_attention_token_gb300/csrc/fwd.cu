@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     uint32_t kv = 0, qc = 0;
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it) {
-      const int w = item_publish(c.ring, n_it, &hdr->fwd_counter, n_work, lane, abort_flag, hdr, 0x204, ok, p.dbg_withhold);
+      const int w = item_publish(c.ring, n_it, &hdr->fwd_counter, n_work, lane, abort_flag, hdr, 0x204, ok, p.dbg_withhold, p.clc);
       if (w < 0) break;
       const int pair = w / p.H, h = w - pair * p.H, hk = h / G;
       const int2 it = p.fwd_items[pair];
@@ -522,16 +522,15 @@ static cudaError_t launch_fwd_t(const AttnParams& p, const AttnMaps& m, cudaStre
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   if (!attr_set[dev]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(fwd_kernel<HD, OB, EX, NV4, BX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<HD, OB, EX, NV4, BX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem_max(smem));
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  long work = (long)p.max_items * p.H;
-  int grid = (int)(work < num_sms() ? work : num_sms());
+  const int grid = attn_grid((long)p.max_items * p.H, num_sms(), p.clc);
   cudaError_t e = cudaMemsetAsync(&p.hdr->fwd_counter, 0, sizeof(uint32_t), st);  // work counter of this launch
   if (e != cudaSuccess) return e;
-  fwd_kernel<HD, OB, EX, NV4, BX><<<grid, kFwdThreads, smem, st>>>(p, m.q, m.k, m.v, m.qn, m.kn);
+  fwd_kernel<HD, OB, EX, NV4, BX><<<grid, kFwdThreads, attn_smem(smem, p.clc), st>>>(p, m.q, m.k, m.v, m.qn, m.kn);
   return cudaGetLastError();
 }
 

@@ -29,6 +29,15 @@ cudaError_t launch_quantize(const QuantBatch& qb, int d, int in_bf16, int o_bf16
                             const int32_t* cu, const int32_t* blk_prefix, int n_seq, WsHeader* hdr, int max_units,
                             int n_sms, cudaStream_t st);
 int sm_count();
+
+// Grid of an attention kernel over `work` items: one CTA per SM (persistent,
+// items from a global counter) or, with cluster launch control, one CTA per
+// item.  Such a CTA asks for at least kClcMinSmem bytes of shared memory so
+// that no two share an SM: each holds all of the SM's tensor memory.
+constexpr size_t kClcMinSmem = 116 * 1024;
+inline int attn_grid(long work, int nsm, int clc) { return clc ? (int)work : (int)(work < nsm ? work : nsm); }
+inline size_t attn_smem(size_t smem, int clc) { return clc && smem < kClcMinSmem ? kClcMinSmem : smem; }
+inline size_t attn_smem_max(size_t smem) { return smem < kClcMinSmem ? kClcMinSmem : smem; }
 cudaError_t launch_plan(const flamia_problem_t& p, const WsLayout& L, uint8_t* ws, cudaStream_t st);
 
 // Everything the attention kernels need for one call (host-built).
@@ -54,6 +63,7 @@ struct AttnParams {
   float* rot_dk;        // hadamard: fp32 [T][Hkv][d] dK (times the softmax scale), rotated basis
   uint32_t* dq_order;   // [tiles][H]: dQ partials already added to each (query tile, head), in key-tile order
   int dq_ordered;       // 1: the partials are added in key-tile order (deterministic and exact options)
+  int clc;              // 1: a CTA per work item, items taken over by cluster launch control
   const float* D;       // [H][T]
   int32_t* m;           // [H][T]
   float* l;             // [H][T]

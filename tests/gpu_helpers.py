@@ -20,14 +20,14 @@ def to_dev(a: np.ndarray, dtype: str, dev="cuda"):
 
 
 def run_gpu(w, *, causal=True, exact=False, path=fl.PATH_MXFP8, deterministic=False, inputs=None,
-            backward=True, causal_dq_scale=False, dq_fp16=False, hadamard=False):
+            backward=True, causal_dq_scale=False, dq_fp16=False, hadamard=False, clc=False):
     dev = torch.device("cuda:0")
     q, k, v, do = inputs if inputs is not None else (w.tensor(n) for n in ("q", "k", "v", "do"))
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
     dt = fl.BF16 if w.dtype == "bf16" else fl.F32
     tc = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu, causal=causal, exact=exact, path=path, in_dtype=dt,
                       out_dtype=dt, deterministic=deterministic, causal_dq_scale=causal_dq_scale, dq_fp16=dq_fp16,
-                      hadamard=hadamard)
+                      hadamard=hadamard, clc=clc)
     tc.plan()
     tc.forward(to_dev(q, w.dtype), to_dev(k, w.dtype), to_dev(v, w.dtype))
     if backward:

@@ -166,3 +166,21 @@ def test_hadamard_option_host_rules(lib):
     n16 = fl.flamia_workspace_size(r)
     r.hadamard = 1
     assert fl.flamia_workspace_size(r) >= n16 + 2 * 228 * 4 * 128 + 4 * 228 * 2 * 128
+
+
+def test_clc_option_host_rules(lib):
+    """Cluster launch control hands out the items of every option but the two
+    whose ordered dQ reduction needs them in list order (exact,
+    deterministic); it changes nothing in the workspace."""
+    p, _ = _prob()
+    n = fl.flamia_workspace_size(p)
+    p.clc = 1
+    assert fl.flamia_workspace_size(p) == n
+    for field in ("exact", "deterministic"):
+        q, _ = _prob()
+        q.clc = 1
+        setattr(q, field, 1)
+        assert fl.flamia_workspace_size(q) == 0, field
+    r, _ = _prob()
+    r.clc, r.path = 1, fl.PATH_NVFP4_FP8
+    assert fl.flamia_workspace_size(r) > 0
