@@ -403,7 +403,9 @@ def _option_overheads(fl, w, inputs, dev, stream, base_bwd_ms, steps):
     import torch
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
     out = {}
-    for name, kw in (("deterministic", {"deterministic": True}), ("exact", {"exact": True}),
+    for name, kw in (("deterministic", {"deterministic": True}),
+                     ("deterministic_fp32_partials", {"deterministic": True, "dq_fp16": False}),
+                     ("exact", {"exact": True}),
                      ("fp32_dq_partials", {"dq_fp16": False}),
                      ("causal_dq_scale", {"causal_dq_scale": True}),
                      ("hadamard", {"hadamard": True}), ("clc", {"clc": True})):

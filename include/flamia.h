@@ -88,12 +88,14 @@ typedef enum { FLAMIA_ROLE_QKV = 0, FLAMIA_ROLE_DO = 1 } flamia_role_t;
  *                fast as fp32 on short documents, faster on long and packed
  *                ones, where it halves the accumulator's traffic);
  *                0: fp32 partials into an fp32 accumulator.  No effect on the
- *                exact and deterministic options and the mixed path, whose
- *                dQ sums in fp32 in a fixed order.
+ *                exact option and the mixed path, whose dQ sums in fp32 in
+ *                a fixed order.
  *   deterministic 1: dQ's partials (one per 128-key tile) are added in
  *                key-tile order (a counter per query tile and head orders the
  *                bulk reduce-adds of the CTAs), so dQ is reproducible bit for
- *                bit; fp32 partials.
+ *                bit; FP16 partials with dq_fp16 (then every FP16 addition
+ *                happens in the order the per-tile model of [READ] 四 4.4
+ *                states), else fp32.
  *   softmax_scale  0 selects 1/sqrt(d).
  *   path         flamia_path_t.
  *   in_dtype     dtype of Q, K, V, dO, O inputs (FLAMIA_BF16 or FLAMIA_F32).
@@ -216,8 +218,9 @@ flamia_status_t flamia_fwd(const flamia_problem_t* p, const flamia_operand_t* q,
  * dQ += dS K^; dK and dV accumulate in fp32; dQ's per-key-tile partials are
  * summed by bulk reduce-adds, in fp32, or (dq_fp16) prescaled by a power of
  * two per query row and summed in FP16 ([READ] 四 4.4); the exact and
- * deterministic options add fp32 partials in key-tile order, and the mixed
- * path sums dQ in fp32 in a second kernel, in a fixed order.
+ * deterministic options add the partials in key-tile order (the exact
+ * option's in fp32), and the mixed path sums dQ in fp32 in a second kernel,
+ * in a fixed order.
  * GQA sums dK/dV over the group.
  *   dQ device [T][H][d], dK/dV device [T][Hkv][d], out_dtype.
  * D, m, l as produced by flamia_quantize(DO) and flamia_fwd. */

@@ -252,9 +252,9 @@ static flamia_status_t fill_params(const flamia_problem_t* p, const WsLayout& L,
   a->hdr = reinterpret_cast<WsHeader*>(w + L.header);
   a->dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
   a->dq16 = reinterpret_cast<__half*>(w + L.dq_acc);
-  // FP16 partials belong to the default option's unordered reduction; the
-  // exact and deterministic options add fp32 partials in key-tile order
-  a->dq_fp16 = (p->dq_fp16 && !p->exact && !p->deterministic) ? 1 : 0;
+  // FP16 partials: the default option, unordered or (deterministic) in
+  // key-tile order; the exact option adds fp32 partials in key-tile order
+  a->dq_fp16 = (p->dq_fp16 && !p->exact) ? 1 : 0;
   a->pexp = reinterpret_cast<int8_t*>(w + L.pexp);
   a->c0 = dq_prescale_c0(p->d, a->softmax_scale);
   a->causal_dq_scale = p->causal_dq_scale ? 1 : 0;

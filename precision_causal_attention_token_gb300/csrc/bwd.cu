@@ -1421,7 +1421,7 @@ static cudaError_t launch_bwd_t(const AttnParams& p_in, const AttnMaps& m, cudaS
       if (p.dq_ordered &&
           (e = cudaMemsetAsync(p.dq_order, 0, sizeof(uint32_t) * (size_t)p.max_items * p.H, st)) != cudaSuccess)
         return e;
-      if (p.dq_fp16 && !p.dq_ordered) {  // the exact and deterministic options sum fp32 partials
+      if (p.dq_fp16) {  // FP16 partials (never with the exact option), unordered or in key-tile order
         if ((e = set_smem<bwd_kernel<HD, OB, EX, true, false, true>>(attn_smem_max(smem))) != cudaSuccess) return e;
         if ((e = cudaMemsetAsync(p.dq16, 0, 2 * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
         if (p.n_seq > 0) dq_prescale_kernel<<<dim3(p.n_seq, p.Hkv), kPrescaleThreads, 0, st>>>(p);

@@ -79,9 +79,9 @@ inline WsLayout ws_layout(const flamia_problem_t& p) {
   L.keys_a = o; o = align256(o + sizeof(uint64_t) * L.sort_n * 2);
   L.keys_b = o; o = align256(o + sizeof(uint64_t) * L.sort_n * 2);
   // fp32 unless the FP16 partials alone use it (the rotation's back-transform
-  // reads every dQ path's result from here in fp32; the exact and
-  // deterministic options sum fp32 partials)
-  const bool acc16 = p.dq_fp16 && !p.hadamard && !p.exact && !p.deterministic;
+  // reads every dQ path's result from here in fp32; the exact option sums
+  // fp32 partials)
+  const bool acc16 = p.dq_fp16 && !p.hadamard && !p.exact;
   L.dq_acc = o; o = align256(o + (acc16 ? 2 : 4) * (size_t)p.T * p.H * p.d);
   L.pexp = o; o = align256(o + (size_t)p.T * p.H);
   L.dq_order = o; o = align256(o + sizeof(uint32_t) * (size_t)L.max_items * p.H);

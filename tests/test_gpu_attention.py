@@ -229,11 +229,26 @@ def test_leakage_probe_default_option_residue():
     assert not o_same and o_rel > 0
 
 
-def test_deterministic_dq_is_reproducible():
+@pytest.mark.parametrize("dq_fp16", [False, True])
+def test_deterministic_dq_is_reproducible(dq_fp16):
     w = synth.custom([700, 300], H=2, Hkv=1, d=128, seed=707)
-    a = run_gpu(w, deterministic=True)
-    b = run_gpu(w, deterministic=True)
+    a = run_gpu(w, deterministic=True, dq_fp16=dq_fp16)
+    b = run_gpu(w, deterministic=True, dq_fp16=dq_fp16)
     assert torch.equal(a.dQ, b.dQ) and torch.equal(a.dK, b.dK) and torch.equal(a.dV, b.dV)
-    ref = run_oracle(w)
+    ref = run_oracle(w, dq_fp16=dq_fp16)
     for name in ("O", "dQ", "dK", "dV"):
         compare(name, getattr(a, name), ref[name])
+
+
+@pytest.mark.parametrize("dq_fp16", [False, True])
+def test_deterministic_dq_more_items_than_sms(dq_fp16):
+    # 13 key tiles x 16 heads: CTAs wait on one another's counters across the
+    # whole grid; the result is the same on every run and matches the oracle
+    # (whose FP16 model adds the partials in this same key-tile order)
+    w = synth.custom([1024, 600], H=16, d=128, seed=708)
+    runs = [run_gpu(w, deterministic=True, dq_fp16=dq_fp16) for _ in range(3)]
+    for r in runs[1:]:
+        assert torch.equal(runs[0].dQ, r.dQ) and torch.equal(runs[0].dK, r.dK)
+    ref = run_oracle(w, dq_fp16=dq_fp16)
+    for name in ("O", "dQ", "dK", "dV"):
+        compare(name, getattr(runs[0], name), ref[name])
