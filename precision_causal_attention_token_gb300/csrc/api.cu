@@ -115,18 +115,21 @@ bool make_dq_map(CUtensorMap* m, void* ptr, int d, int heads, int T, bool fp16) 
   return r == CUDA_SUCCESS;
 }
 
-// 3-D map over the mixed path's bf16 score operands [T][heads][d]: box = 128
-// tokens x 1 head x 64 values (128 bytes, 128B swizzle).
+// 3-D map over the mixed path's packed E2M1 codes [T][heads][d/2]: box = 128
+// tokens x 1 head x d/2 bytes, swizzle = d/2 bytes (64B or 32B), out-of-range
+// rows read as zero.
 bool make_nv_map(CUtensorMap* m, const void* ptr, int d, int heads, int T) {
   auto enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)T};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  const cuuint64_t rb = (cuuint64_t)d / 2;
+  cuuint64_t dims[3] = {rb, (cuuint64_t)heads, (cuuint64_t)T};
+  cuuint64_t strides[2] = {rb, (cuuint64_t)heads * rb};
+  cuuint32_t box[3] = {(cuuint32_t)rb, 1, 128};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   d == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -203,7 +206,6 @@ flamia_status_t flamia_quantize(const flamia_problem_t* p, int32_t role, const v
         a.codes4 = static_cast<uint8_t*>(out[i].codes4);
         a.scales4 = static_cast<uint8_t*>(out[i].scales4);
         a.gscale4 = static_cast<float*>(out[i].gscale4);
-        a.xnv = reinterpret_cast<__nv_bfloat16*>(w + (i == 0 ? L.nv_q : L.nv_k));
       }
       units += max_blk * a.heads;
     }
@@ -298,8 +300,9 @@ flamia_status_t flamia_fwd(const flamia_problem_t* p, const flamia_operand_t* q,
   if (a.nvfp4) {
     a.q_g = static_cast<const float*>(q->gscale4);
     a.k_g = static_cast<const float*>(k->gscale4);
-    if (!make_nv_map(&maps.qn, static_cast<uint8_t*>(ws) + L.nv_q, p->d, p->H, p->T) ||
-        !make_nv_map(&maps.kn, static_cast<uint8_t*>(ws) + L.nv_k, p->d, p->Hkv, p->T))
+    a.q_bs = static_cast<const uint8_t*>(q->scales4);
+    a.k_bs = static_cast<const uint8_t*>(k->scales4);
+    if (!make_nv_map(&maps.qn, q->codes4, p->d, p->H, p->T) || !make_nv_map(&maps.kn, k->codes4, p->d, p->Hkv, p->T))
       return FLAMIA_ERR_CUDA;
   }
   return launch_fwd(a, maps, stream) == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
@@ -319,7 +322,9 @@ flamia_status_t flamia_bwd(const flamia_problem_t* p, const flamia_operand_t* q,
   if (!operand_ok(q) || !operand_ok(k) || !operand_ok(v) || !operand_ok(dO) || !D || !m || !l || !dQ || !dK ||
       !dV || !aligned16(D) || !aligned16(m) || !aligned16(l) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
     return FLAMIA_ERR_INVALID_ARG;
-  if (p->path == FLAMIA_PATH_NVFP4_FP8 && (!q->gscale4 || !k->gscale4)) return FLAMIA_ERR_INVALID_ARG;
+  if (p->path == FLAMIA_PATH_NVFP4_FP8 && (!q->codes4 || !q->scales4 || !q->gscale4 || !k->codes4 ||
+                                           !k->scales4 || !k->gscale4))
+    return FLAMIA_ERR_INVALID_ARG;
   AttnParams a;
   fill_params(p, L, ws, &a);
   a.q_sc = static_cast<const uint8_t*>(q->scales);
@@ -340,8 +345,9 @@ flamia_status_t flamia_bwd(const flamia_problem_t* p, const flamia_operand_t* q,
   if (a.nvfp4) {
     a.q_g = static_cast<const float*>(q->gscale4);
     a.k_g = static_cast<const float*>(k->gscale4);
-    if (!make_nv_map(&maps.qn, static_cast<uint8_t*>(ws) + L.nv_q, p->d, p->H, p->T) ||
-        !make_nv_map(&maps.kn, static_cast<uint8_t*>(ws) + L.nv_k, p->d, p->Hkv, p->T))
+    a.q_bs = static_cast<const uint8_t*>(q->scales4);
+    a.k_bs = static_cast<const uint8_t*>(k->scales4);
+    if (!make_nv_map(&maps.qn, q->codes4, p->d, p->H, p->T) || !make_nv_map(&maps.kn, k->codes4, p->d, p->Hkv, p->T))
       return FLAMIA_ERR_CUDA;
   }
   return launch_bwd(a, maps, stream) == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;

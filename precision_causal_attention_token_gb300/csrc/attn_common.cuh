@@ -134,29 +134,67 @@ __device__ __forceinline__ void phat_logits2(uint32_t t_s0, uint32_t t_s1, float
 }
 
 // Bytes of one 128-token score-operand tile: E4M3 codes (MXFP8 path) or
-// bf16 NVFP4 values (mixed path).
+// packed E2M1 codes, two to a byte (mixed path).
 template <int HD, bool NV4>
 constexpr int score_tile_bytes() {
-  return NV4 ? 2 * kTile * HD : kTile * HD;
+  return NV4 ? kTile * HD / 2 : kTile * HD;
+}
+
+// Mixed path: the 16-element block scales of a 128-token tile, staged for
+// copy_scales_x4 in HD/64 blocks of 512 bytes (block s: K-elements
+// 64s..64s+63); row r of a block holds the 4-byte scale words of tokens r,
+// r + 32, r + 64, r + 96.  One warp; tokens at or past T get zero scales (their
+// codes are zero-filled).  The writes are made visible to the tensor core's
+// copies (async proxy) before the caller's arrival.
+template <int HD>
+__device__ __forceinline__ void stage_nv_scales(uint32_t* dst, const uint8_t* bs, int heads, int h, int tok0, int T,
+                                                int lane) {
+  constexpr int NS = HD / 64;  // scale words per token-head
+  uint32_t wv[4][NS];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int tok = tok0 + lane + 32 * c;
+    const uint8_t* src = bs + ((size_t)tok * heads + h) * (HD / 16);
+    if constexpr (NS == 2) {
+      const uint2 v = tok < T ? *reinterpret_cast<const uint2*>(src) : make_uint2(0u, 0u);
+      wv[c][0] = v.x;
+      wv[c][1] = v.y;
+    } else {
+      wv[c][0] = tok < T ? *reinterpret_cast<const uint32_t*>(src) : 0u;
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < NS; ++s)
+    *reinterpret_cast<uint4*>(dst + s * 128 + lane * 4) = make_uint4(wv[0][s], wv[1][s], wv[2][s], wv[3][s]);
+  fence_proxy_async_smem();
+}
+
+// Mixed path: copy a staged tile's scales (stage_nv_scales) to tensor memory
+// columns col..col + 4 HD/64 - 1 (MMA thread).
+template <int HD>
+__device__ __forceinline__ void copy_nv_scales(uint32_t col_tmem, const uint32_t* src) {
+#pragma unroll
+  for (int s = 0; s < HD / 64; ++s) copy_scales_x4(col_tmem + 4 * s, src + s * 128);
 }
 
 // S = Q K^T for one 128 x 128 tile into TMEM column d_s.
 //  MXFP8: E4M3 tiles with rows of HD bytes (swizzle = HD bytes), kind::f8f6f4,
 //         32 K-elements per instruction.
-//  Mixed: bf16 tiles stored as HD/64 boxes of [128 rows][64 values] (128B
-//         swizzle), kind::f16, 16 K-elements per instruction; the products of
-//         E2M1 values and E4M3 block scales are exact in bf16, so this is the
-//         block-scaled NVFP4 product, accumulated in fp32.
+//  Mixed: packed E2M1 tiles with rows of HD/2 bytes (swizzle = HD/2 bytes),
+//         kind::mxf4nvf4 with the E4M3 16-element block scales in tensor
+//         memory (sfa: Q's, sfb: K's, as copy_nv_scales puts them), 64
+//         K-elements per instruction, fp32 accumulation.
 template <int HD, bool NV4>
-__device__ __forceinline__ void issue_scores(uint32_t d_s, const uint8_t* qt, const uint8_t* kt) {
+__device__ __forceinline__ void issue_scores(uint32_t d_s, const uint8_t* qt, const uint8_t* kt, uint32_t sfa = 0,
+                                             uint32_t sfb = 0) {
   const uint32_t qa = smem_u32(qt), ka = smem_u32(kt);
   if constexpr (NV4) {
-    const uint32_t id = idesc_bf16(128, 128);
+    const uint32_t id = idesc_mxf4nvf4(128, 128);
+    constexpr uint32_t rb = HD / 2, swz = HD == 128 ? kSwz64 : kSwz32;
 #pragma unroll
-    for (int kk = 0; kk < HD / 16; ++kk) {
-      const uint32_t off = (uint32_t)(kk >> 2) * (kTile * 128) + (uint32_t)(kk & 3) * 32;
-      mma_bf16(d_s, smem_desc(qa + off, 16, 1024, kSwz128), smem_desc(ka + off, 16, 1024, kSwz128), id, kk > 0);
-    }
+    for (int s = 0; s < HD / 64; ++s)
+      mma_mxf4nvf4(d_s, smem_desc(qa + 32 * s, 16, 8 * rb, swz), smem_desc(ka + 32 * s, 16, 8 * rb, swz), id,
+                   sfa + 4 * s, sfb + 4 * s, s > 0);
   } else {
     const uint32_t id = idesc_f8(128, 128, 0, 0);
     constexpr uint32_t swz = HD == 128 ? kSwz128 : kSwz64;
@@ -171,8 +209,7 @@ template <int HD, bool NV4>
 __device__ __forceinline__ void load_score_tile(uint8_t* dst, const CUtensorMap* map8, const CUtensorMap* mapn,
                                                 uint64_t* bar, int head, int tok0) {
   if constexpr (NV4) {
-#pragma unroll
-    for (int bx = 0; bx < HD / 64; ++bx) tma_load_3d(dst + bx * (kTile * 128), mapn, bar, 64 * bx, head, tok0);
+    tma_load_3d(dst, mapn, bar, 0, head, tok0);
   } else {
     tma_load_3d(dst, map8, bar, 0, head, tok0);
   }

@@ -54,15 +54,14 @@ static_assert(2 * 128 * kRegCompute + 128 * kRegDrain + 128 * kRegCtl <= 65536, 
 constexpr uint32_t kColDV = 0, kColDK = 128, kColX0 = 256, kColX1 = 384;
 constexpr uint32_t kColSfDV = kColX1 + 64, kColSfDK = kColX1 + 68, kColSfDQ = kColX1 + 72, kColSfOne = kColX1 + 76;
 
-// NV4 (mixed path): the scores' operands are bf16 NVFP4 values (k holds K's,
-// qn Q's); dK still contracts with the E4M3 Q codes.  dQ then comes from the
-// dQ kernel (no DQ variant).
+// NV4 (mixed path): the scores' operands are packed E2M1 codes (k holds K's,
+// qn Q's) with their block scales staged in ksf / qsf; dK still contracts
+// with the E4M3 Q codes.  dQ then comes from the dQ kernel (no DQ variant).
 // K/V tiles of consecutive work items are double-buffered so the next item's
-// copies land while this one is processed (one buffer on the mixed path,
-// whose bf16 score tiles leave no room for a second).
+// copies land while this one is processed.
 template <bool NV4>
 constexpr int bwd_kv_stages() {
-  return NV4 ? 1 : 2;
+  return 2;
 }
 
 template <int HD, bool EXACT, bool DQ, bool NV4>
@@ -79,6 +78,8 @@ struct __align__(1024) BwdTiles {
   // 128B-swizzled
   uint8_t dqs[DQ ? kTile * 256 : 1024];
   uint8_t qn[2][NV4 ? score_tile_bytes<HD, NV4>() : 16];  // mixed path: Q's score operand
+  uint32_t qsf[2][NV4 ? 256 : 4];                          // mixed path: its block scales
+  uint32_t ksf[bwd_kv_stages<NV4>()][NV4 ? 256 : 4];       // and K's
 };
 
 // Per-row values of one query tile, staged in shared memory by the producer
@@ -410,6 +411,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         c.vinv[kvs][j] = pow2_127(-ev);
         if ((j & 31) == 0) c.ekb[kvs][j >> 5] = ek;
       }
+      if constexpr (NV4) stage_nv_scales<HD>(tl.ksf[kvs], p.k_bs, p.Hkv, hk, k0, p.T, lane);
       if (lane == 0) {
         mbar_arrive_expect_tx(&c.kv_full[kvs], kQKBytes + kTile * HD);
         load_score_tile<HD, NV4>(tl.k[kvs], &map_k, &map_kn, &c.kv_full[kvs], hk, k0);
@@ -430,6 +432,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             v[rr4] = load_row<NV4>(p, h, ds + i_loc, i_loc < len, ds);
           }
           if (!(ok = mbar_wait_warp(&c.qd_empty[qs], ((ii >> 1) & 1) ^ 1, abort_flag, hdr, 0x302))) break;
+          if constexpr (NV4) stage_nv_scales<HD>(tl.qsf[qs], p.q_bs, p.H, h, ds + kTile * qt, p.T, lane);
           if (lane == 0) {
             mbar_expect_tx(&c.qd_full[qs], 2 * kTile * HD + (NV4 ? kQKBytes : 0));
             tma_load_3d(tl.q[qs], &map_q, &c.qd_full[qs], 0, h, ds + kTile * qt);
@@ -467,7 +470,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // X0 is free once the compute warps have read the previous S
           if (!mbar_wait(&c.x0_free, (i_s & 1) ^ 1, abort_flag, hdr, 0x313)) return false;
           tc_fence_after();
-          issue_scores<HD, NV4>(tb + kColX0, NV4 ? tl.qn[qs_s] : tl.q[qs_s], tl.k[kvs]);
+          if constexpr (NV4) {  // the block scales go to X1's last 16 columns (see below)
+            copy_nv_scales<HD>(tb + kColX1 + 112, tl.qsf[qs_s]);
+            copy_nv_scales<HD>(tb + kColX1 + 120, tl.ksf[kvs]);
+          }
+          issue_scores<HD, NV4>(tb + kColX0, NV4 ? tl.qn[qs_s] : tl.q[qs_s], tl.k[kvs], tb + kColX1 + 112,
+                                tb + kColX1 + 120);
           tc_commit(&c.s_full);
           return true;
         };
@@ -481,6 +489,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (HD == 64 && i_p > 0 && !mbar_wait(&c.mm_done, (i_p - 1) & 1, abort_flag, hdr, 0x319)) return false;
           } else {
             if (i_p > 0 && !mbar_wait(&c.mm_done, (i_p - 1) & 1, abort_flag, hdr, 0x314)) return false;
+            // mixed path: S(i_p) has read its scale factors in X1
+            if (NV4 && !mbar_wait(&c.s_full, i_p & 1, abort_flag, hdr, 0x31a)) return false;
           }
           tc_fence_after();
 #pragma unroll
@@ -490,12 +500,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           return true;
         };
         // the first tile of the item: S and dP; later tiles' S and dP are
-        // issued one tile ahead (S as soon as X0 is read, dP once X1 is free)
+        // issued one tile ahead (S as soon as X0 is read, dP once X1 is free).
+        // Mixed path: S's block scales sit in X1, so S(t + 1) waits until
+        // dS(t) is done (dP(t) read); it is needed only after dS(t + 1)'s
+        // inputs anyway, and dP(t + 1) follows the MMAs that precede it.
         if (!(ok = issue_s(ii) && issue_dp(ii))) break;
         for (int t = 0; ok && t < n_iter; ++t, ++ii) {
           const int qs = ii & 1;
-          if (t + 1 < n_iter && !(ok = issue_s(ii + 1))) break;
+          if (!NV4 && t + 1 < n_iter && !(ok = issue_s(ii + 1))) break;
           if (!(ok = mbar_wait(&c.ds_full, ii & 1, abort_flag, hdr, 0x315))) break;
+          if (NV4 && t + 1 < n_iter && !(ok = issue_s(ii + 1))) break;
           if (t == 0 && !(ok = mbar_wait(&c.acc_free, (ic & 1) ^ 1, abort_flag, hdr, 0x316))) break;
           tc_fence_after();
           const uint8_t* dsk = EXACT ? tl.dsk : tl.ds;
@@ -888,9 +902,12 @@ constexpr int kDqThreads = kBwdCompute + 64;  // compute warps 0-7, producer 8, 
 constexpr int kDqWarpProd = 8, kDqWarpMma = 9;
 constexpr uint32_t kDqColAcc = 0, kDqColX0 = 128, kDqColX1 = 256;
 constexpr uint32_t kDqColSf = kDqColX0 + 0, kDqColSfOne = kDqColX0 + 4;
+// mixed path: the scores' block scales (Q's, then K's)
+constexpr uint32_t kDqColQSF = 384, kDqColKSF = 392;
 
-// q and k hold the scores' operands (E4M3 codes, or bf16 NVFP4 values on the
-// mixed path, where k8 holds K's E4M3 codes for the dQ MMA).
+// q and k hold the scores' operands (E4M3 codes, or packed E2M1 codes on the
+// mixed path, with their block scales in qsf / ksf, where k8 holds K's E4M3
+// codes for the dQ MMA).
 template <int HD, bool NV4>
 struct __align__(1024) DqTiles {
   uint8_t q[score_tile_bytes<HD, NV4>()];
@@ -899,6 +916,8 @@ struct __align__(1024) DqTiles {
   uint8_t v[kDqStages][kTile * HD];
   uint8_t ds[kTile * kTile];
   uint8_t k8[kDqStages][NV4 ? kTile * HD : 1024];
+  uint32_t qsf[NV4 ? 256 : 4];
+  uint32_t ksf[kDqStages][NV4 ? 256 : 4];
 };
 
 struct DqCtl {
@@ -935,7 +954,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   volatile int* abort_flag = &c.abort_flag;
   WsHeader* hdr = p.hdr;
   if (tid == 0) {
-    mbar_init(&c.qd_full, 1);
+    mbar_init(&c.qd_full, NV4 ? 32 : 1);  // mixed path: every producer lane stages Q's scales
     mbar_init(&c.qd_empty, 1);
     for (int s = 0; s < kDqStages; ++s) {
       mbar_init(&c.kv_full[s], 32);
@@ -970,10 +989,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
       const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
       if (!(ok = mbar_wait_warp(&c.qd_empty, (ic & 1) ^ 1, abort_flag, hdr, 0x401))) break;
+      if constexpr (NV4) stage_nv_scales<HD>(tl.qsf, p.q_bs, p.H, h, ds + kTile * it.y, p.T, lane);
       if (lane == 0) {
         mbar_arrive_expect_tx(&c.qd_full, kQKBytes + kTile * HD);
         load_score_tile<HD, NV4>(tl.q, &map_q, &map_qn, &c.qd_full, h, ds + kTile * it.y);
         tma_load_3d(tl.dO, &map_do, &c.qd_full, 0, h, ds + kTile * it.y);
+      } else if (NV4) {
+        mbar_arrive(&c.qd_full);
       }
       for (int kt = 0; kt < n_kt; ++kt, ++kv) {
         const int st = kv % kDqStages;
@@ -995,6 +1017,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           c.vinv[st][j] = pow2_127(-ev);
           if ((j & 31) == 0) c.ekb[st][j >> 5] = ek;
         }
+        if constexpr (NV4) stage_nv_scales<HD>(tl.ksf[st], p.k_bs, p.Hkv, hk, ds + kTile * kt, p.T, lane);
         if (lane == 0) {
           mbar_arrive_expect_tx(&c.kv_full[st], kQKBytes + kTile * HD + (NV4 ? kTile * HD : 0));
           load_score_tile<HD, NV4>(tl.k[st], &map_k, &map_kn, &c.kv_full[st], hk, ds + kTile * kt);
@@ -1024,7 +1047,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           if (!(ok = mbar_wait(&c.kv_full[st], ph, abort_flag, hdr, 0x412))) break;
           if (ii > 0 && !(ok = mbar_wait(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x413))) break;
           tc_fence_after();
-          issue_scores<HD, NV4>(tb + kDqColX0, tl.q, tl.k[st]);
+          if constexpr (NV4) {  // every earlier MMA has completed: one set of scale columns serves
+            if (kt == 0) copy_nv_scales<HD>(tb + kDqColQSF, tl.qsf);
+            copy_nv_scales<HD>(tb + kDqColKSF, tl.ksf[st]);
+          }
+          issue_scores<HD, NV4>(tb + kDqColX0, tl.q, tl.k[st], tb + kDqColQSF, tb + kDqColKSF);
           tc_commit(&c.s_full);
           if (!(ok = mbar_wait(&c.dp_free, (ii & 1) ^ 1, abort_flag, hdr, 0x414))) break;
           tc_fence_after();

@@ -56,7 +56,6 @@ struct WsLayout {
   size_t pexp;             // int8 [H][T]: the dQ prescale exponent of each query row
   size_t rot_dk;           // hadamard: fp32 [T][Hkv][d] dK before the back-rotation
   size_t dq_order;         // uint32 [max_items][H]: ordered dQ reduction counters
-  size_t nv_q, nv_k;       // mixed path: bf16 [T][H][d] / [T][Hkv][d], NVFP4 values without the token scale
   size_t total;
   int32_t max_items;       // upper bound of tiles: ceil(T/128) + n_seq
   int32_t sort_n;          // max_items rounded up to the block-sort size
@@ -88,11 +87,6 @@ inline WsLayout ws_layout(const flamia_problem_t& p) {
   L.rot_dk = 0;
   if (p.hadamard) {  // dK in the rotated basis, fp32, before the back-rotation
     L.rot_dk = o; o = align256(o + 4 * (size_t)p.T * p.Hkv * p.d);
-  }
-  L.nv_q = L.nv_k = 0;
-  if (p.path == FLAMIA_PATH_NVFP4_FP8) {
-    L.nv_q = o; o = align256(o + 2 * (size_t)p.T * p.H * p.d);
-    L.nv_k = o; o = align256(o + 2 * (size_t)p.T * p.Hkv * p.d);
   }
   L.total = o;
   return L;
@@ -535,7 +529,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   d |= (uint64_t)(swz & 7u) << 61;
   return d;
 }
-constexpr uint32_t kSwz128 = 2, kSwz64 = 4;
+constexpr uint32_t kSwz128 = 2, kSwz64 = 4, kSwz32 = 6;
 
 // Instruction descriptor, kind::f8f6f4 (E4M3 x E4M3 -> fp32):
 // c_format(4-5)=1 (F32), a_format(7-9)=0 (E4M3), b_format(10-12)=0,
@@ -550,6 +544,14 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, uint32
                                                   uint32_t a_sf_id, uint32_t b_sf_id) {
   return (b_sf_id << 4) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
          (a_sf_id << 29);
+}
+
+// Instruction descriptor, kind::mxf4nvf4 block-scaled (E2M1 A and B packed
+// two to a byte, UE4M3 scales, one per 16 K-elements, scale_vec::4X):
+// a_format (7-9) = b_format (10-12) = 1 (E2M1), K-major A and B, N>>3 in
+// 17-22, scale_format (bit 23) = 0 (UE4M3), M>>4 in 24-28, scale ids 0.
+__host__ __device__ constexpr uint32_t idesc_mxf4nvf4(uint32_t M, uint32_t N) {
+  return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // Instruction descriptor, kind::f16 with bf16 A and B, fp32 accumulate:
@@ -585,6 +587,27 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64
       "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
       ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
+}
+
+// NVFP4 form: 64 K-elements per instruction; scale words (four UE4M3 bytes,
+// byte k for K-elements 16k..16k+15) in tensor memory: row m of A at lane m,
+// column sfa + m / 32; column n of B, for the output rows of lane quarter q,
+// at lane 32 q + n % 32, column sfb + n / 32 (as copy_scales_x4 lays them out).
+__device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Shared memory -> tensor memory, 32 rows x 16 bytes (512 contiguous bytes,
+// row r at 16 r) copied to lanes r, 32 + r, 64 + r, 96 + r, columns
+// col..col+3 (the same words in every lane quarter).  Issued by the MMA
+// thread; ordered with its MMAs and tracked by its commits.
+__device__ __forceinline__ void copy_scales_x4(uint32_t col_tmem, const void* src) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(col_tmem),
+               "l"(smem_desc(smem_u32(src), 128, 128, 0)) : "memory");
 }
 
 // 32 lanes x 32 columns of 32-bit: thread t of the warp gets lane (quarter*32+t).

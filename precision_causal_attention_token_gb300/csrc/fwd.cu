@@ -37,6 +37,9 @@ constexpr int kFwdWarpProd = 16, kFwdWarpMma = 17;
 constexpr uint32_t kFwdRegSoftmax = 104, kFwdRegCtl = 64;
 static_assert(4 * 128 * kFwdRegSoftmax + 128 * kFwdRegCtl <= kFwdThreads * 96, "register split");
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColSFA0 = 384, kColSFA1 = 392, kColSFB = 400;
+// mixed path: the scores' block scales, Q's per item and K's per S buffer,
+// each double-buffered (8 columns a buffer: two 64-element steps at d = 128)
+constexpr uint32_t kColQSF = 416, kColKSF = 432;
 
 template <int HD, bool NV4>
 struct __align__(1024) FwdTiles {
@@ -44,6 +47,10 @@ struct __align__(1024) FwdTiles {
   uint8_t k[kFwdStages][score_tile_bytes<HD, NV4>()];
   uint8_t v[kFwdStages][kTile * HD];
   uint8_t p[2][kTile * kTile];
+  // mixed path: Q's and each K stage's block scales staged for the copy to
+  // tensor memory (stage_nv_scales)
+  uint32_t qsf[NV4 ? 256 : 4];
+  uint32_t ksf[kFwdStages][NV4 ? 256 : 4];
 };
 
 struct FwdCtl {
@@ -119,7 +126,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   WsHeader* hdr = p.hdr;
 
   if (tid == 0) {
-    mbar_init(&c.q_full, 1);
+    mbar_init(&c.q_full, NV4 ? 32 : 1);  // mixed path: every producer lane stages Q's scales
     mbar_init(&c.q_empty, 1);
     for (int s = 0; s < kFwdStages; ++s) {
       mbar_init(&c.k_full[s], 32);
@@ -180,9 +187,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int q0 = ds + kTile * it.y;
       const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
       if (!(ok = mbar_wait_warp(&c.q_empty, (qc & 1) ^ 1, abort_flag, hdr, 0x201))) break;
+      if constexpr (NV4) stage_nv_scales<HD>(tl.qsf, p.q_bs, p.H, h, q0, p.T, lane);
       if (lane == 0) {
         mbar_arrive_expect_tx(&c.q_full, kQKBytes);
         load_score_tile<HD, NV4>(tl.q, &map_q, &map_qn, &c.q_full, h, q0);
+      } else if (NV4) {
+        mbar_arrive(&c.q_full);
       }
       ++qc;
       for (int kt = 0; kt < n_kt; ++kt, ++kv) {
@@ -203,6 +213,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           c.vf[st][j] = (float)ev;
           c.vinv[st][j] = pow2_127(-ev);
         }
+        if constexpr (NV4) stage_nv_scales<HD>(tl.ksf[st], p.k_bs, p.Hkv, hk, ds + kTile * kt, p.T, lane);
         if (lane == 0) {
           mbar_arrive_expect_tx(&c.k_full[st], kQKBytes);
           load_score_tile<HD, NV4>(tl.k[st], &map_k, &map_kn, &c.k_full[st], hk, ds + kTile * kt);
@@ -229,6 +240,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int len = __ldg(p.cu + it.x + 1) - __ldg(p.cu + it.x);
         const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
         if (!(ok = mbar_wait(&c.q_full, qc & 1, abort_flag, hdr, 0x211))) break;
+        const uint32_t qsf = tb + kColQSF + 8 * (qc & 1);
+        if constexpr (NV4) {
+          tc_fence_after();
+          copy_nv_scales<HD>(qsf, tl.qsf);
+        }
         // S runs two tiles ahead of P^V: the softmax warps release S(t)'s
         // buffer a full tile before they hand over P^(t), so S(t + 2) can be
         // issued as soon as P^V(t - 1) is, and is ready a tile later.
@@ -240,7 +256,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (!mbar_wait(&c.k_full[st], ph, abort_flag, hdr, 0x212)) return false;
           if (!mbar_wait(&c.s_free[sb], sph ^ 1, abort_flag, hdr, 0x213)) return false;
           tc_fence_after();
-          issue_scores<HD, NV4>(tb + (sb ? kColS1 : kColS0), tl.q, tl.k[st]);
+          const uint32_t ksf = tb + kColKSF + 8 * sb;
+          if constexpr (NV4) copy_nv_scales<HD>(ksf, tl.ksf[st]);
+          issue_scores<HD, NV4>(tb + (sb ? kColS1 : kColS0), tl.q, tl.k[st], qsf, ksf);
           tc_commit(&c.s_full[sb]);
           tc_commit(&c.k_empty[st]);
           if (t == n_kt - 1) tc_commit(&c.q_empty);

@@ -11,7 +11,6 @@ struct QuantArgs {
   uint8_t* codes4;   // [T][heads][d/2]   (NVFP4 operand)
   uint8_t* scales4;  // [T][heads][d/16]
   float* gscale4;    // [heads][T]
-  __nv_bfloat16* xnv;  // [T][heads][d] NVFP4 value e2m1 * block scale (exact in bf16), no token scale
   const void* O;     // [T][heads][d]     (dO role)
   float* D;          // [heads][T]
   int T, heads;
@@ -57,7 +56,9 @@ struct AttnParams {
   const uint8_t* do_sc; // [H][T]
   const float* q_g;     // mixed path: per-token fp32 scale of Q's NVFP4 payload [H][T]
   const float* k_g;     // mixed path: of K's [Hkv][T]
-  int nvfp4;            // 1: scores from the NVFP4 payload (bf16 operands in the workspace)
+  int nvfp4;            // 1: scores from the NVFP4 payload (block-scaled E2M1 MMAs)
+  const uint8_t* q_bs;  // mixed path: Q's E4M3 16-element block scales [T][H][d/16]
+  const uint8_t* k_bs;  // mixed path: K's [T][Hkv][d/16]
   int bitexp;           // 1: forward with bit-level exponentials (inference only)
   int hadamard;         // 1: Q, K rotated; dQ, dK go through fp32 buffers and are rotated back
   float* rot_dk;        // hadamard: fp32 [T][Hkv][d] dK (times the softmax scale), rotated basis

@@ -407,19 +407,11 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int2 loc, int 
         const float sv = unpack_e4m3x2((uint16_t)sc).x;
         const float sg = __fmul_rn(sv, gs);
         uint32_t packed = 0u;
-        uint32_t xb[EPL / 2];  // bf16 pairs of e2m1 * block scale (exact), the score operand
 #pragma unroll
         for (int e = 0; e < EPL; e += 2) {
           uint32_t byte = (sc == 0u) ? 0u
                                      : pack_e2m1x2(__fdiv_rn(raw[t].at(e), sg), __fdiv_rn(raw[t].at(e + 1), sg));
           packed |= byte << (8 * (e / 2));
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(e2m1_value(byte & 0xFu) * sv, e2m1_value(byte >> 4) * sv);
-          xb[e / 2] = *reinterpret_cast<uint32_t*>(&b2);
-        }
-        if (a.xnv != nullptr) {
-          __nv_bfloat16* dstb = a.xnv + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL;
-          if constexpr (EPL == 4) *reinterpret_cast<uint2*>(dstb) = make_uint2(xb[0], xb[1]);
-          else *reinterpret_cast<uint32_t*>(dstb) = xb[0];
         }
         uint8_t* dst4 = a.codes4 + (size_t)(t0 + t) * a.heads * (HD / 2) + (size_t)h * (HD / 2) + lane * (EPL / 2);
         if constexpr (EPL == 4) *reinterpret_cast<uint16_t*>(dst4) = (uint16_t)packed;
