@@ -161,6 +161,10 @@ typedef struct {
  *            per byte, element 2k in the low nibble.
  *   scales4  mixed path, Q and K only: uint8 [T][heads][d/16] E4M3 block scales.
  *   gscale4  mixed path, Q and K only: float [heads][T] per-token fp32 scale.
+ *   On the mixed path flamia_fwd and flamia_bwd read codes4 and scales4 of Q
+ *   and K directly as the operands of the block-scaled NVFP4 score MMA
+ *   ([SUM] §3.4: QK^T and its recompute in NVFP4, one E4M3 scale per 16
+ *   head-dimension elements), so they must stay unchanged between the calls.
  * Unused members may be NULL. */
 typedef struct {
   void* codes;
@@ -199,8 +203,9 @@ flamia_status_t flamia_quantize(const flamia_problem_t* p, int32_t role, const v
                                 const flamia_operand_t* out, float* D, void* ws, size_t ws_bytes,
                                 cudaStream_t stream);
 
-/* Forward ([SUM] §3.1–§3.3; [READ] 4.1–4.4): S = Q^ K^T, online softmax over
- * key tiles with an integer row reference, P^ quantized to E4M3 with one
+/* Forward ([SUM] §3.1–§3.3; [READ] 4.1–4.4): S = Q^ K^T (mixed path:
+ * g_Q(i) g_K(j) sum_d (e2m1 s)_Q (e2m1 s)_K from the NVFP4 payload, [SUM]
+ * §3.4), online softmax over key tiles with an integer row reference, P^ quantized to E4M3 with one
  * exponent per (row, 32-key block) after the per-key V factor is folded in,
  * O += P^ V^ by a block-scaled MMA, O = acc / l.
  *   O  device [T][H][d] out_dtype

@@ -16,10 +16,13 @@
 //              shared memory and the block exponents (relative to m) to TMEM
 //              as the A-operand scale factors of the P^V MMA.
 //   warp 16    producer: TMA loads of Q, K, V code tiles (128 x d, swizzled)
-//              and the per-key scale vectors of each K/V stage.
-//   warp 17    MMA issuer: S = Q^ K^T (kind::f8f6f4, fp32 in TMEM, double
-//              buffered) and O += P^ V^ (kind::mxf8f6f4 block-scaled, scale A
-//              = P^ block exponents, scale B = 1: V's own scale is folded).
+//              and the per-key scale vectors of each K/V stage (mixed path:
+//              also Q's and K's NVFP4 block scales, staged for tcgen05.cp).
+//   warp 17    MMA issuer: S = Q^ K^T (kind::f8f6f4, or on the mixed path
+//              kind::mxf4nvf4 with the block scales copied to TMEM; fp32 in
+//              TMEM, double buffered) and O += P^ V^ (kind::mxf8f6f4
+//              block-scaled, scale A = P^ block exponents, scale B = 1: V's
+//              own scale is folded).
 // The next tile's S is issued before the current tile's P^V so the tensor
 // core works while the softmax warps quantize.
 #include "kernels.h"
@@ -104,8 +107,9 @@ __device__ __forceinline__ void phat_bitexp2(float y0, float y1, uint64_t nE2, f
   p1 = bitexp2(d1);
 }
 
-// NV4: the mixed path (scores from the NVFP4 payload, bf16 operand tiles,
-// per-token fp32 factors g_Q(i) g_K(j) applied with the softmax scale).
+// NV4: the mixed path (scores from the NVFP4 payload: packed E2M1 tiles and
+// E4M3 block scales in a block-scaled MMA; per-token fp32 factors
+// g_Q(i) g_K(j) applied with the softmax scale).
 // BX: the inference forward with bit-level exponentials on key pairs 0-4 of
 // every 8 in a 32-key block (the other pairs keep ex2); MXFP8 default option.
 template <int HD, bool OUT_BF16, bool EXACT, bool NV4, bool BX>
