@@ -224,8 +224,7 @@ flamia_status_t flamia_fwd(const flamia_problem_t* p, const flamia_operand_t* q,
  * summed by bulk reduce-adds, in fp32, or (dq_fp16) prescaled by a power of
  * two per query row and summed in FP16 ([READ] 四 4.4); the exact and
  * deterministic options add the partials in key-tile order (the exact
- * option's in fp32), and the mixed path sums dQ in fp32 in a second kernel,
- * in a fixed order.
+ * option's in fp32); the mixed path takes the same route.
  * GQA sums dK/dV over the group.
  *   dQ device [T][H][d], dK/dV device [T][Hkv][d], out_dtype.
  * D, m, l as produced by flamia_quantize(DO) and flamia_fwd. */

@@ -114,25 +114,6 @@ __device__ __forceinline__ int phat_logits1(uint32_t t_s, float (&y)[32], float 
   return phat_block_logits<EXACT, NEED_MASK>(y, rowc, kf, vf, i_loc, key, len, causal);
 }
 
-// Two 32-key blocks of logits for one row: both S blocks are read from
-// tensor memory with one wait, then turned into logits and exponents.
-template <bool EXACT, bool NEED_MASK>
-__device__ __forceinline__ void phat_logits2(uint32_t t_s0, uint32_t t_s1, float (&y)[2][32], int (&Eb)[2],
-                                             float rowc, const float* kf, const float* vf, int i_loc, int key0,
-                                             int len, int causal) {
-  uint32_t rr[2][32];
-  tmem_ld32(t_s0, rr[0]);
-  tmem_ld32(t_s1, rr[1]);
-  tmem_ld_wait_regs(rr[0], rr[1]);
-#pragma unroll
-  for (int bb = 0; bb < 2; ++bb) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) y[bb][j] = __uint_as_float(rr[bb][j]);
-    Eb[bb] = phat_block_logits<EXACT, NEED_MASK>(y[bb], rowc, kf + 32 * bb, vf + 32 * bb, i_loc, key0 + 32 * bb,
-                                                 len, causal);
-  }
-}
-
 // Bytes of one 128-token score-operand tile: E4M3 codes (MXFP8 path) or
 // packed E2M1 codes, two to a byte (mixed path).
 template <int HD, bool NV4>

@@ -55,19 +55,20 @@ constexpr uint32_t kColDV = 0, kColDK = 128, kColX0 = 256, kColX1 = 384;
 constexpr uint32_t kColSfDV = kColX1 + 64, kColSfDK = kColX1 + 68, kColSfDQ = kColX1 + 72, kColSfOne = kColX1 + 76;
 
 // NV4 (mixed path): the scores' operands are packed E2M1 codes (k holds K's,
-// qn Q's) with their block scales staged in ksf / qsf; dK still contracts
-// with the E4M3 Q codes.  dQ then comes from the dQ kernel (no DQ variant).
+// qn Q's) with their block scales staged in ksf / qsf; dK and dQ still
+// contract with the E4M3 Q and K codes (q, k8).
 // K/V tiles of consecutive work items are double-buffered so the next item's
-// copies land while this one is processed.
-template <bool NV4>
+// copies land while this one is processed (one buffer on the mixed path with
+// dQ, whose extra E4M3 K tile leaves no room for a second).
+template <bool NV4, bool DQ>
 constexpr int bwd_kv_stages() {
-  return 2;
+  return NV4 && DQ ? 1 : 2;
 }
 
 template <int HD, bool EXACT, bool DQ, bool NV4>
 struct __align__(1024) BwdTiles {
-  uint8_t k[bwd_kv_stages<NV4>()][score_tile_bytes<HD, NV4>()];
-  uint8_t v[bwd_kv_stages<NV4>()][kTile * HD];
+  uint8_t k[bwd_kv_stages<NV4, DQ>()][score_tile_bytes<HD, NV4>()];
+  uint8_t v[bwd_kv_stages<NV4, DQ>()][kTile * HD];
   uint8_t q[2][kTile * HD];
   uint8_t dO[2][kTile * HD];
   uint8_t pt[kTile * kTile];   // P~ codes   [query][key]
@@ -79,8 +80,22 @@ struct __align__(1024) BwdTiles {
   uint8_t dqs[DQ ? kTile * 256 : 1024];
   uint8_t qn[2][NV4 ? score_tile_bytes<HD, NV4>() : 16];  // mixed path: Q's score operand
   uint32_t qsf[2][NV4 ? 256 : 4];                          // mixed path: its block scales
-  uint32_t ksf[bwd_kv_stages<NV4>()][NV4 ? 256 : 4];       // and K's
+  uint32_t ksf[bwd_kv_stages<NV4, DQ>()][NV4 ? 256 : 4];   // and K's
+  // mixed path with dQ: K's E4M3 codes for the dQ MMA.  Last, after members
+  // that are whole KB on the mixed path: every tile above must stay at a
+  // 1024-byte boundary (swizzled TMA destinations, MMA operands)
+  uint8_t k8[NV4 && DQ ? bwd_kv_stages<NV4, DQ>() : 1][NV4 && DQ ? kTile * HD : 16];
 };
+// every tile's offset is a multiple of 1024 bytes on every variant used
+template <int HD, bool EXACT, bool DQ, bool NV4>
+constexpr bool bwd_tiles_aligned() {
+  using T = BwdTiles<HD, EXACT, DQ, NV4>;
+  return offsetof(T, q) % 1024 == 0 && offsetof(T, dO) % 1024 == 0 && offsetof(T, pt) % 1024 == 0 &&
+         offsetof(T, ds) % 1024 == 0 && offsetof(T, dsk) % 1024 == 0 && offsetof(T, dqs) % 1024 == 0 &&
+         offsetof(T, v) % 1024 == 0 && (!NV4 || (offsetof(T, qn) % 1024 == 0 && offsetof(T, qsf) % 1024 == 0 &&
+                                                 offsetof(T, ksf) % 1024 == 0)) &&
+         (!(NV4 && DQ) || offsetof(T, k8) % 1024 == 0);
+}
 
 // Per-row values of one query tile, staged in shared memory by the producer
 // next to the tile's Q / dO codes (off the compute warps' critical path).
@@ -118,26 +133,6 @@ __device__ __forceinline__ uint64_t bdesc_mn(const uint8_t* t, uint32_t off, uin
 }
 
 __device__ __forceinline__ uint32_t sf_byte(int e) { return (uint32_t)min(max(e + 127, 0), 254); }
-
-// Recompute this thread's P^ codes for its two 32-key blocks (b0, b0 + 1) of a
-// 128-key tile from S in TMEM, with the forward's arithmetic
-// (phat_block_logits, phat_values2): the same inputs give the same codes and
-// block exponents.  Rows outside the document give empty blocks (codes 0).
-template <bool EXACT>
-__device__ __forceinline__ void recompute_phat(uint32_t t_s, int b0, float rowc, const float* kf, const float* vf,
-                                               int i_loc, int key0, int len, int causal, bool need_mask, bool row_ok,
-                                               uint32_t (&pcode)[2][8], int (&Eb)[2]) {
-  float y[2][32];
-  const uint32_t t0 = t_s + 32 * b0, t1 = t0 + 32;
-  if (need_mask)
-    phat_logits2<EXACT, true>(t0, t1, y, Eb, rowc, kf + 32 * b0, vf + 32 * b0, i_loc, key0 + 32 * b0, len, causal);
-  else
-    phat_logits2<EXACT, false>(t0, t1, y, Eb, rowc, kf + 32 * b0, vf + 32 * b0, i_loc, key0 + 32 * b0, len, causal);
-  if (!row_ok) Eb[0] = Eb[1] = kEmptyBlock;
-  // rows outside the document: finite logits, zero codes
-  phat_block_codes(y[0], row_ok ? Eb[0] : kZeroCodes, pcode[0]);
-  phat_block_codes(y[1], row_ok ? Eb[1] : kZeroCodes, pcode[1]);
-}
 
 // Per-(row, key block) factor of dS and P~: with gb = 2^(Eb - m) / l (0 for
 // an empty block or a row outside the document), Pn = P^ 2^-eV / l =
@@ -319,9 +314,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                const __grid_constant__ CUtensorMap map_dq, const __grid_constant__ CUtensorMap map_qn,
                const __grid_constant__ CUtensorMap map_kn) {
-  static_assert(!(NV4 && DQ), "the mixed path takes dQ from the dQ kernel");
   static_assert(DQ || !DQ16, "FP16 partials belong to the dQ path");
-  constexpr int kKvStages = bwd_kv_stages<NV4>();
+  static_assert(bwd_tiles_aligned<HD, EXACT, DQ, NV4>(), "tile alignment");
+  constexpr int kKvStages = bwd_kv_stages<NV4, DQ>();
   constexpr bool PERKEY = EXACT || NV4;
   constexpr int kQKBytes = score_tile_bytes<HD, NV4>();
   extern __shared__ uint8_t smem_raw[];
@@ -413,9 +408,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if constexpr (NV4) stage_nv_scales<HD>(tl.ksf[kvs], p.k_bs, p.Hkv, hk, k0, p.T, lane);
       if (lane == 0) {
-        mbar_arrive_expect_tx(&c.kv_full[kvs], kQKBytes + kTile * HD);
+        mbar_arrive_expect_tx(&c.kv_full[kvs], kQKBytes + kTile * HD + (NV4 && DQ ? kTile * HD : 0));
         load_score_tile<HD, NV4>(tl.k[kvs], &map_k, &map_kn, &c.kv_full[kvs], hk, k0);
         tma_load_3d(tl.v[kvs], &map_v, &c.kv_full[kvs], 0, hk, k0);
+        if (NV4 && DQ) tma_load_3d(tl.k8[kvs], &map_k, &c.kv_full[kvs], 0, hk, k0);
       } else {
         mbar_arrive(&c.kv_full[kvs]);
       }
@@ -489,9 +485,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (HD == 64 && i_p > 0 && !mbar_wait(&c.mm_done, (i_p - 1) & 1, abort_flag, hdr, 0x319)) return false;
           } else {
             if (i_p > 0 && !mbar_wait(&c.mm_done, (i_p - 1) & 1, abort_flag, hdr, 0x314)) return false;
-            // mixed path: S(i_p) has read its scale factors in X1
-            if (NV4 && !mbar_wait(&c.s_full, i_p & 1, abort_flag, hdr, 0x31a)) return false;
           }
+          // mixed path: S(i_p) has read its scale factors in X1
+          if (NV4 && !mbar_wait(&c.s_full, i_p & 1, abort_flag, hdr, 0x31a)) return false;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < HD / 32; ++kk)
@@ -518,7 +514,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           auto issue_dq = [&](int half) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)  // contraction over the 128 keys
-              mma_mxf8(tb + kColX1, bdesc_k(tl.ds, 32 * kk, 128), bdesc_mn(tl.k[kvs], kk * 32 * HD + 64 * half, HD),
+              mma_mxf8(tb + kColX1, bdesc_k(tl.ds, 32 * kk, 128),
+                       bdesc_mn(NV4 ? tl.k8[kvs] : tl.k[kvs], kk * 32 * HD + 64 * half, HD),
                        idesc_mxf8(128, 64, 0, 1, kk, kk), tb + kColSfDQ, tb + kColSfOne, kk > 0 ? 1u : 0u);
           };
           if constexpr (DQ) {
@@ -891,281 +888,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == kWarpMma) tmem_dealloc(tb, 512);
 }
 
-// ============================================================================
-// Deterministic dQ kernel: one CTA per (document, 128-query tile, head) from
-// the forward's work list; dQ accumulates in TMEM over the key tiles in a
-// fixed order and is written once (no atomics).  Recomputes S, P^, dP and dS
-// with the same functions as the dK/dV kernel.
-// ============================================================================
-constexpr int kDqStages = 2;
-constexpr int kDqThreads = kBwdCompute + 64;  // compute warps 0-7, producer 8, MMA 9
-constexpr int kDqWarpProd = 8, kDqWarpMma = 9;
-constexpr uint32_t kDqColAcc = 0, kDqColX0 = 128, kDqColX1 = 256;
-constexpr uint32_t kDqColSf = kDqColX0 + 0, kDqColSfOne = kDqColX0 + 4;
-// mixed path: the scores' block scales (Q's, then K's)
-constexpr uint32_t kDqColQSF = 384, kDqColKSF = 392;
-
-// q and k hold the scores' operands (E4M3 codes, or packed E2M1 codes on the
-// mixed path, with their block scales in qsf / ksf, where k8 holds K's E4M3
-// codes for the dQ MMA).
-template <int HD, bool NV4>
-struct __align__(1024) DqTiles {
-  uint8_t q[score_tile_bytes<HD, NV4>()];
-  uint8_t dO[kTile * HD];
-  uint8_t k[kDqStages][score_tile_bytes<HD, NV4>()];
-  uint8_t v[kDqStages][kTile * HD];
-  uint8_t ds[kTile * kTile];
-  uint8_t k8[kDqStages][NV4 ? kTile * HD : 1024];
-  uint32_t qsf[NV4 ? 256 : 4];
-  uint32_t ksf[kDqStages][NV4 ? 256 : 4];
-};
-
-struct DqCtl {
-  float kf[kDqStages][kTile], vf[kDqStages][kTile], vinv[kDqStages][kTile];
-  float kfold[kDqStages][kTile];  // 2^eK(j): the exact option's dQ-operand fold
-  int ekb[kDqStages][4];
-  uint8_t xdq[2][kTile][4];  // [parity][query row][key block] dQ scale bytes
-  uint64_t qd_full, qd_empty, kv_full[kDqStages], kv_empty[kDqStages];
-  uint64_t s_full, dp_full, dp_free, ds_full, mm_done, dq_full, dq_free, xch_bar;
-  ItemRing ring;
-  uint32_t tmem_base;
-  int abort_flag;
-};
-
-template <int HD, bool NV4>
-constexpr size_t dq_smem_bytes() {
-  return sizeof(DqTiles<HD, NV4>) + sizeof(DqCtl) + 1024;
-}
-
-template <int HD, bool OUT_BF16, bool EXACT, bool NV4>
-__global__ void __launch_bounds__(kDqThreads, 1)
-    dq_kernel(const AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-              const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
-              const __grid_constant__ CUtensorMap map_qn, const __grid_constant__ CUtensorMap map_kn) {
-  constexpr bool PERKEY = EXACT || NV4;
-  constexpr int kQKBytes = score_tile_bytes<HD, NV4>();
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = smem_base_1k(smem_raw);
-  DqTiles<HD, NV4>& tl = *reinterpret_cast<DqTiles<HD, NV4>*>(base);
-  DqCtl& c = *reinterpret_cast<DqCtl*>(base + sizeof(DqTiles<HD, NV4>));
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = p.H / p.Hkv;
-  const int n_work = p.hdr->n_items * p.H;
-  volatile int* abort_flag = &c.abort_flag;
-  WsHeader* hdr = p.hdr;
-  if (tid == 0) {
-    mbar_init(&c.qd_full, NV4 ? 32 : 1);  // mixed path: every producer lane stages Q's scales
-    mbar_init(&c.qd_empty, 1);
-    for (int s = 0; s < kDqStages; ++s) {
-      mbar_init(&c.kv_full[s], 32);
-      mbar_init(&c.kv_empty[s], 1 + kBwdCompute);
-    }
-    mbar_init(&c.s_full, 1);
-    mbar_init(&c.dp_full, 1);
-    mbar_init(&c.dp_free, kBwdCompute);
-    mbar_init(&c.ds_full, kBwdCompute);
-    mbar_init(&c.mm_done, 1);
-    mbar_init(&c.dq_full, 1);
-    mbar_init(&c.dq_free, kBwdCompute);
-    mbar_init(&c.xch_bar, kBwdCompute);
-    item_ring_init(c.ring, 1 + kBwdCompute / 32);  // the MMA thread and the compute warps
-    c.abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == kDqWarpMma) tmem_alloc(&c.tmem_base, 512);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tb = c.tmem_base;
-
-  if (warp == kDqWarpProd) {
-    uint32_t ic = 0, kv = 0;
-    bool ok = true;
-    for (uint32_t n_it = 0; ok; ++n_it, ++ic) {
-      const int w = item_publish(c.ring, n_it, &hdr->dq_counter, n_work, lane, abort_flag, hdr, 0x404, ok, p.dbg_withhold, p.clc);
-      if (w < 0) break;
-      const int pair = w / p.H, h = w - pair * p.H, hk = h / G;
-      const int2 it = p.fwd_items[pair];
-      const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
-      const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
-      if (!(ok = mbar_wait_warp(&c.qd_empty, (ic & 1) ^ 1, abort_flag, hdr, 0x401))) break;
-      if constexpr (NV4) stage_nv_scales<HD>(tl.qsf, p.q_bs, p.H, h, ds + kTile * it.y, p.T, lane);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&c.qd_full, kQKBytes + kTile * HD);
-        load_score_tile<HD, NV4>(tl.q, &map_q, &map_qn, &c.qd_full, h, ds + kTile * it.y);
-        tma_load_3d(tl.dO, &map_do, &c.qd_full, 0, h, ds + kTile * it.y);
-      } else if (NV4) {
-        mbar_arrive(&c.qd_full);
-      }
-      for (int kt = 0; kt < n_kt; ++kt, ++kv) {
-        const int st = kv % kDqStages;
-        const uint32_t ph = (kv / kDqStages) & 1;
-        if (!(ok = mbar_wait_warp(&c.kv_empty[st], ph ^ 1, abort_flag, hdr, 0x402))) break;
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int j = lane * 4 + jj, key = kTile * kt + j;
-          int ek = 0, ev = 0;
-          float gk = 1.f;
-          if (key < len) {
-            ek = (int)__ldg(p.k_sc + (size_t)hk * p.T + ds + key) - 127;
-            ev = (int)__ldg(p.v_sc + (size_t)hk * p.T + ds + key) - 127;
-            if (NV4) gk = __ldg(p.k_g + (size_t)hk * p.T + ds + key);
-          }
-          c.kf[st][j] = NV4 ? gk : pow2_127(ek);
-          c.kfold[st][j] = pow2_127(ek);
-          c.vf[st][j] = (float)ev;
-          c.vinv[st][j] = pow2_127(-ev);
-          if ((j & 31) == 0) c.ekb[st][j >> 5] = ek;
-        }
-        if constexpr (NV4) stage_nv_scales<HD>(tl.ksf[st], p.k_bs, p.Hkv, hk, ds + kTile * kt, p.T, lane);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&c.kv_full[st], kQKBytes + kTile * HD + (NV4 ? kTile * HD : 0));
-          load_score_tile<HD, NV4>(tl.k[st], &map_k, &map_kn, &c.kv_full[st], hk, ds + kTile * kt);
-          tma_load_3d(tl.v[st], &map_v, &c.kv_full[st], 0, hk, ds + kTile * kt);
-          if (NV4) tma_load_3d(tl.k8[st], &map_k, &c.kv_full[st], 0, hk, ds + kTile * kt);
-        } else {
-          mbar_arrive(&c.kv_full[st]);
-        }
-      }
-    }
-  } else if (warp == kDqWarpMma) {
-    if (elect_one()) {
-      uint32_t ic = 0, kv = 0, ii = 0;
-      bool ok = true;
-      const uint32_t id_sp = idesc_f8(128, 128, 0, 0);
-      for (uint32_t n_it = 0; ok; ++n_it, ++ic) {
-        const int w = item_get(c.ring, n_it, abort_flag, hdr, 0x418, ok);
-        if (w < 0) break;
-        const int pair = w / p.H;
-        const int2 it = p.fwd_items[pair];
-        const int len = __ldg(p.cu + it.x + 1) - __ldg(p.cu + it.x);
-        const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
-        if (!(ok = mbar_wait(&c.qd_full, ic & 1, abort_flag, hdr, 0x411))) break;
-        for (int kt = 0; ok && kt < n_kt; ++kt, ++kv, ++ii) {
-          const int st = kv % kDqStages;
-          const uint32_t ph = (kv / kDqStages) & 1;
-          if (!(ok = mbar_wait(&c.kv_full[st], ph, abort_flag, hdr, 0x412))) break;
-          if (ii > 0 && !(ok = mbar_wait(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x413))) break;
-          tc_fence_after();
-          if constexpr (NV4) {  // every earlier MMA has completed: one set of scale columns serves
-            if (kt == 0) copy_nv_scales<HD>(tb + kDqColQSF, tl.qsf);
-            copy_nv_scales<HD>(tb + kDqColKSF, tl.ksf[st]);
-          }
-          issue_scores<HD, NV4>(tb + kDqColX0, tl.q, tl.k[st], tb + kDqColQSF, tb + kDqColKSF);
-          tc_commit(&c.s_full);
-          if (!(ok = mbar_wait(&c.dp_free, (ii & 1) ^ 1, abort_flag, hdr, 0x414))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < HD / 32; ++kk)
-            mma_f8(tb + kDqColX1, bdesc_k(tl.dO, 32 * kk, HD), bdesc_k(tl.v[st], 32 * kk, HD), id_sp, kk > 0);
-          tc_commit(&c.dp_full);
-          if (!(ok = mbar_wait(&c.ds_full, ii & 1, abort_flag, hdr, 0x415))) break;
-          if (kt == 0 && !(ok = mbar_wait(&c.dq_free, (ic & 1) ^ 1, abort_flag, hdr, 0x416))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_mxf8(tb + kDqColAcc, bdesc_k(tl.ds, 32 * kk, 128), bdesc_mn(NV4 ? tl.k8[st] : tl.k[st], kk * 32 * HD, HD),
-                     idesc_mxf8(128, HD, 0, 1, kk, kk), tb + kDqColSf, tb + kDqColSfOne, (kt > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&c.mm_done);
-          tc_commit(&c.kv_empty[st]);
-          if (kt == n_kt - 1) {
-            tc_commit(&c.dq_full);
-            tc_commit(&c.qd_empty);
-          }
-        }
-      }
-    }
-    __syncwarp();
-  } else {
-    const int q = warp & 3, hf = warp >> 2;  // lane quarter (query rows), key-block half
-    const int r = 32 * q + lane;
-    const int b0 = 2 * hf;
-    constexpr int HC = HD / 2;
-    uint32_t ic = 0, kv = 0, ii = 0;
-    bool ok = true;
-    for (uint32_t n_it = 0; ok; ++n_it, ++ic) {
-      const int w = item_get_warp(c.ring, n_it, lane, abort_flag, hdr, 0x428, ok);
-      if (w < 0) break;
-      const int pair = w / p.H, h = w - pair * p.H;
-      const int2 it = p.fwd_items[pair];
-      const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
-      const int n_kt = p.causal ? it.y + 1 : (len + kTile - 1) / kTile;
-      const int i_loc = kTile * it.y + r;
-      const bool row_ok = i_loc < len;
-      const RowVals rv = load_row<NV4>(p, h, ds + i_loc, row_ok, ds);
-      const float inv_l = 1.0f / rv.li;
-      const float nDp = ldexp_f(-rv.Di, -rv.edo);
-      for (int kt = 0; ok && kt < n_kt; ++kt, ++kv, ++ii) {
-        const int st = kv % kDqStages;
-        const uint32_t ph = (kv / kDqStages) & 1;
-        if (!(ok = mbar_wait_warp(&c.kv_full[st], ph, abort_flag, hdr, 0x421))) break;
-        if (!(ok = mbar_wait_warp(&c.s_full, ii & 1, abort_flag, hdr, 0x422))) break;
-        tc_fence_after();
-        uint32_t pcode[2][8];
-        int Eb[2];
-        recompute_phat<PERKEY>(taddr(tb, q * 32, kDqColX0), b0, rv.rowc, c.kf[st], c.vf[st], i_loc, kTile * kt, len,
-                              p.causal, kt == n_kt - 1, row_ok, pcode, Eb);
-        if (!(ok = mbar_wait_warp(&c.dp_full, ii & 1, abort_flag, hdr, 0x423))) break;
-        if (ii > 0 && !(ok = mbar_wait_warp(&c.mm_done, (ii - 1) & 1, abort_flag, hdr, 0x424))) break;
-        tc_fence_after();
-        const int par = ii & 1;
-        uint32_t dp[2][32];
-        tmem_ld32(taddr(tb, q * 32, kDqColX1 + 32 * b0), dp[0]);
-        tmem_ld32(taddr(tb, q * 32, kDqColX1 + 32 * (b0 + 1)), dp[1]);
-        tmem_ld_wait_regs(dp[0], dp[1]);
-#pragma unroll
-        for (int bb = 0; bb < 2; ++bb) {
-          const int b = b0 + bb;
-          float wv[32], uv[32];
-          float amax_w, amax_u;
-          const float gbh = ds_gbh(Eb[bb], rv.mi, inv_l, rv.hdo);
-          ds_block(dp[bb], pcode[bb], nDp, c.vinv[st] + 32 * b, wv, uv, amax_w, amax_u);
-          uint32_t codes[8];
-          int e_blk;
-          c.xdq[par][r][b] =
-              (uint8_t)dq_operand<EXACT>(wv, amax_w, gbh, c.kfold[st] + 32 * b, c.ekb[st][b], codes, e_blk);
-          store_row_block(tl.ds, r, b, codes);
-        }
-        tc_fence_before();
-        mbar_arrive(&c.dp_free);
-        mbar_arrive(&c.xch_bar);
-        if (!(ok = mbar_wait_warp(&c.xch_bar, ii & 1, abort_flag, hdr, 0x426))) break;
-        if (hf == 0) {
-          const uint32_t wdq = *reinterpret_cast<const uint32_t*>(c.xdq[par][r]);
-          tmem_st4(taddr(tb, q * 32, kDqColSf), wdq, wdq, wdq, wdq);
-          tmem_st4(taddr(tb, q * 32, kDqColSfOne), 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-        }
-        fence_proxy_async_smem();
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&c.ds_full);
-        mbar_arrive(&c.kv_empty[st]);
-      }
-      if (!ok) break;
-      if (!(ok = mbar_wait_warp(&c.dq_full, ic & 1, abort_flag, hdr, 0x425))) break;
-      tc_fence_after();
-      const size_t off = ((size_t)(ds + i_loc) * p.H + h) * HD + hf * HC;
-#pragma unroll
-      for (int cb = 0; cb < HC / 32; ++cb) {
-        uint32_t rr[32];
-        tmem_ld32(taddr(tb, q * 32, kDqColAcc + hf * HC + 32 * cb), rr);
-        tmem_ld_wait_regs(rr);
-        if (!row_ok) continue;
-        if (p.hadamard)  // dQ of the rotated Q, in fp32 until the back-rotation
-          store_row32<false>(p.dq_acc, off + 32 * cb, rr, p.softmax_scale);
-        else
-          store_row32<OUT_BF16>(p.dQ, off + 32 * cb, rr, p.softmax_scale);
-      }
-      tc_fence_before();
-      mbar_arrive(&c.dq_free);
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  drain_after_abort(abort_flag);
-  if (warp == kDqWarpMma) tmem_dealloc(tb, 512);
-}
-
 // The fp32 dQ accumulator (sums of dS^ K^ over key tiles) times the softmax
 // scale -> output dtype.
 template <bool OUT_BF16>
@@ -1429,86 +1151,55 @@ static cudaError_t set_smem(size_t smem) {
 template <int HD, bool OB, bool EX, bool NV4>
 static cudaError_t launch_bwd_t(const AttnParams& p_in, const AttnMaps& m, cudaStream_t st) {
   // the deterministic and exact options add the dQ partials in key-tile
-  // order (fixed-order sums); only the mixed path keeps the separate dQ
-  // kernel, whose shared memory the bf16 score tiles leave no room for
+  // order (fixed-order sums)
   AttnParams p = p_in;
-  p.dq_ordered = (!NV4 && (p.exact || p.deterministic)) ? 1 : 0;
-  const bool det = NV4;
+  p.dq_ordered = (p.exact || p.deterministic) ? 1 : 0;
   const int nsm = sm_count();
   const int grid = attn_grid((long)p.max_items * p.Hkv, nsm, p.clc);
   cudaError_t e;
-  if constexpr (!NV4) {
-    if (!det) {
-      const size_t smem = bwd_smem_bytes<HD, EX, true, false>();
-      static_assert(bwd_smem_bytes<HD, EX, true, false>() <= 232448, "shared memory");
-      const size_t n4 = (size_t)p.T * p.H * HD / 4;
-      int cg = (int)((n4 + 255) / 256);
-      if (cg > nsm * 8) cg = nsm * 8;
-      if ((e = cudaMemsetAsync(&p.hdr->bwd_counter, 0, sizeof(uint32_t), st)) != cudaSuccess) return e;
-      if (p.dq_ordered &&
-          (e = cudaMemsetAsync(p.dq_order, 0, sizeof(uint32_t) * (size_t)p.max_items * p.H, st)) != cudaSuccess)
+  const size_t smem = bwd_smem_bytes<HD, EX, true, NV4>();
+  static_assert(bwd_smem_bytes<HD, EX, true, NV4>() <= 232448, "shared memory");
+  const size_t n4 = (size_t)p.T * p.H * HD / 4;
+  int cg = (int)((n4 + 255) / 256);
+  if (cg > nsm * 8) cg = nsm * 8;
+  if ((e = cudaMemsetAsync(&p.hdr->bwd_counter, 0, sizeof(uint32_t), st)) != cudaSuccess) return e;
+  if (p.dq_ordered &&
+      (e = cudaMemsetAsync(p.dq_order, 0, sizeof(uint32_t) * (size_t)p.max_items * p.H, st)) != cudaSuccess)
+    return e;
+  if (p.dq_fp16) {  // FP16 partials (never with the exact option), unordered or in key-tile order
+    if ((e = set_smem<bwd_kernel<HD, OB, EX, true, NV4, true>>(attn_smem_max(smem))) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(p.dq16, 0, 2 * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
+    if (p.n_seq > 0) dq_prescale_kernel<<<dim3(p.n_seq, p.Hkv), kPrescaleThreads, 0, st>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_kernel<HD, OB, EX, true, NV4, true><<<grid, kBwdThreads, attn_smem(smem, p.clc), st>>>(
+        p, m.q, m.k, m.v, m.dO, m.dq, m.qn, m.kn);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (!NV4 && p.hadamard) {
+      if ((e = launch_rot_back<OB, HD, true>(p.dq16, p.pexp, p.dQ, (size_t)p.T * p.H, p.softmax_scale, p.T, p.H,
+                                             nsm, st)) != cudaSuccess)
         return e;
-      if (p.dq_fp16) {  // FP16 partials (never with the exact option), unordered or in key-tile order
-        if ((e = set_smem<bwd_kernel<HD, OB, EX, true, false, true>>(attn_smem_max(smem))) != cudaSuccess) return e;
-        if ((e = cudaMemsetAsync(p.dq16, 0, 2 * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
-        if (p.n_seq > 0) dq_prescale_kernel<<<dim3(p.n_seq, p.Hkv), kPrescaleThreads, 0, st>>>(p);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        bwd_kernel<HD, OB, EX, true, false, true><<<grid, kBwdThreads, attn_smem(smem, p.clc), st>>>(
-            p, m.q, m.k, m.v, m.dO, m.dq, m.q, m.q);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        if (p.hadamard) {
-          if ((e = launch_rot_back<OB, HD, true>(p.dq16, p.pexp, p.dQ, (size_t)p.T * p.H, p.softmax_scale, p.T, p.H,
-                                                 nsm, st)) != cudaSuccess)
-            return e;
-          return launch_rot_back<OB, HD, false>(p.rot_dk, nullptr, p.dK, (size_t)p.T * p.Hkv, 1.f, p.T, p.Hkv, nsm,
-                                                st);
-        }
-        {
-          const size_t rows = (size_t)p.T * p.H;
-          const size_t want = (rows + 7) / 8;  // eight warps a block, a row a warp
-          const int blocks = (int)(want < (size_t)nsm * 16 ? (want < 1 ? 1 : want) : (size_t)nsm * 16);
-          dq16_convert_kernel<OB, HD><<<blocks, 256, 0, st>>>(p.dq16, p.pexp, p.dQ, rows, p.softmax_scale, p.T, p.H);
-        }
-      } else {
-        if ((e = set_smem<bwd_kernel<HD, OB, EX, true, false, false>>(attn_smem_max(smem))) != cudaSuccess) return e;
-        if ((e = cudaMemsetAsync(p.dq_acc, 0, 4 * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
-        bwd_kernel<HD, OB, EX, true, false, false><<<grid, kBwdThreads, attn_smem(smem, p.clc), st>>>(
-            p, m.q, m.k, m.v, m.dO, m.dq, m.q, m.q);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        if (p.hadamard) {
-          if ((e = launch_rot_back<OB, HD, false>(p.dq_acc, nullptr, p.dQ, (size_t)p.T * p.H, p.softmax_scale, p.T,
-                                                  p.H, nsm, st)) != cudaSuccess)
-            return e;
-          return launch_rot_back<OB, HD, false>(p.rot_dk, nullptr, p.dK, (size_t)p.T * p.Hkv, 1.f, p.T, p.Hkv, nsm,
-                                                st);
-        }
-        if (OB) dq_convert_kernel<true><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4, p.softmax_scale);
-        else dq_convert_kernel<false><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4, p.softmax_scale);
-      }
-      return cudaGetLastError();
+      return launch_rot_back<OB, HD, false>(p.rot_dk, nullptr, p.dK, (size_t)p.T * p.Hkv, 1.f, p.T, p.Hkv, nsm,
+                                            st);
     }
+    const size_t rows = (size_t)p.T * p.H;
+    const size_t want = (rows + 7) / 8;  // eight warps a block, a row a warp
+    const int blocks = (int)(want < (size_t)nsm * 16 ? (want < 1 ? 1 : want) : (size_t)nsm * 16);
+    dq16_convert_kernel<OB, HD><<<blocks, 256, 0, st>>>(p.dq16, p.pexp, p.dQ, rows, p.softmax_scale, p.T, p.H);
+    return cudaGetLastError();
   }
-  const size_t smem = bwd_smem_bytes<HD, EX, false, NV4>();
-  static_assert(bwd_smem_bytes<HD, EX, false, NV4>() <= 232448, "shared memory");
-  static_assert(dq_smem_bytes<HD, NV4>() <= 232448, "shared memory");
-  if ((e = set_smem<bwd_kernel<HD, OB, EX, false, NV4, false>>(attn_smem_max(smem))) != cudaSuccess) return e;
-  // work counters of the two launches below
-  if ((e = cudaMemsetAsync(&p.hdr->bwd_counter, 0, 2 * sizeof(uint32_t), st)) != cudaSuccess) return e;
-  // without DQ the dQ map is not read (the q map stands in for the argument)
-  bwd_kernel<HD, OB, EX, false, NV4, false><<<grid, kBwdThreads, attn_smem(smem, p.clc), st>>>(p, m.q, m.k, m.v, m.dO,
-                                                                                               m.q, m.qn, m.kn);
+  if ((e = set_smem<bwd_kernel<HD, OB, EX, true, NV4, false>>(attn_smem_max(smem))) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(p.dq_acc, 0, 4 * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
+  bwd_kernel<HD, OB, EX, true, NV4, false><<<grid, kBwdThreads, attn_smem(smem, p.clc), st>>>(
+      p, m.q, m.k, m.v, m.dO, m.dq, m.qn, m.kn);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const size_t dsm = dq_smem_bytes<HD, NV4>();
-  if ((e = set_smem<dq_kernel<HD, OB, EX, NV4>>(attn_smem_max(dsm))) != cudaSuccess) return e;
-  const int dgrid = attn_grid((long)p.max_items * p.H, nsm, p.clc);
-  dq_kernel<HD, OB, EX, NV4><<<dgrid, kDqThreads, attn_smem(dsm, p.clc), st>>>(p, m.q, m.k, m.v, m.dO, m.qn, m.kn);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (!NV4 && p.hadamard) {  // both kernels left fp32 gradients of the rotated operands
-    if ((e = launch_rot_back<OB, HD, false>(p.dq_acc, nullptr, p.dQ, (size_t)p.T * p.H, 1.f, p.T, p.H, nsm, st)) !=
-        cudaSuccess)
+  if (!NV4 && p.hadamard) {
+    if ((e = launch_rot_back<OB, HD, false>(p.dq_acc, nullptr, p.dQ, (size_t)p.T * p.H, p.softmax_scale, p.T, p.H,
+                                            nsm, st)) != cudaSuccess)
       return e;
     return launch_rot_back<OB, HD, false>(p.rot_dk, nullptr, p.dK, (size_t)p.T * p.Hkv, 1.f, p.T, p.Hkv, nsm, st);
   }
+  if (OB) dq_convert_kernel<true><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4, p.softmax_scale);
+  else dq_convert_kernel<false><<<cg, 256, 0, st>>>(p.dq_acc, p.dQ, n4, p.softmax_scale);
   return cudaGetLastError();
 }
 

@@ -55,6 +55,13 @@ struct __align__(1024) FwdTiles {
   uint32_t qsf[NV4 ? 256 : 4];
   uint32_t ksf[kFwdStages][NV4 ? 256 : 4];
 };
+// the tiles sit at 1024-byte boundaries (swizzled TMA destinations, MMA operands)
+template <int HD, bool NV4>
+constexpr bool fwd_tiles_aligned() {
+  using T = FwdTiles<HD, NV4>;
+  return offsetof(T, k) % 1024 == 0 && offsetof(T, v) % 1024 == 0 && offsetof(T, p) % 1024 == 0 &&
+         (!NV4 || (offsetof(T, qsf) % 16 == 0 && offsetof(T, ksf) % 16 == 0));
+}
 
 struct FwdCtl {
   float kf[kFwdStages][kTile];    // 2^eK(j)
@@ -119,6 +126,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                const __grid_constant__ CUtensorMap map_kn) {
   constexpr bool PERKEY = EXACT || NV4;  // the key factor varies within a 32-key block
   constexpr int kQKBytes = score_tile_bytes<HD, NV4>();
+  static_assert(fwd_tiles_aligned<HD, NV4>(), "tile alignment");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_base_1k(smem_raw);
   FwdTiles<HD, NV4>& tl = *reinterpret_cast<FwdTiles<HD, NV4>*>(base);

@@ -82,7 +82,7 @@ struct AttnParams {
 
 struct AttnMaps {
   CUtensorMap q, k, v, dO;
-  CUtensorMap qn, kn;  // mixed path: bf16 NVFP4 values, boxes of 128 tokens x 64 values (128B swizzle)
+  CUtensorMap qn, kn;  // mixed path: packed E2M1 codes, boxes of 128 tokens x d/2 bytes
   CUtensorMap dq;      // dQ accumulator [T][H][d], the reduce-add target: fp32 boxes of 128 rows x 32
                        // values, or (dq_fp16) FP16 boxes of 128 rows x 64 values; 128B swizzle
 };

@@ -50,6 +50,19 @@ def test_mixed_parity_small(name, w, kw):
     _check(tc, ref)
 
 
+@pytest.mark.parametrize("dq_fp16,deterministic", [(True, False), (True, True), (False, True)])
+def test_mixed_fused_dq_options(dq_fp16, deterministic):
+    # the mixed path's dQ goes through the fused backward's reduction like the
+    # MXFP8 path's: FP16 or fp32 partials, unordered or in key-tile order
+    w = synth.custom([300, 45, 129, 1, 600], H=4, Hkv=2, d=128, seed=708)
+    tc = run_gpu(w, dq_fp16=dq_fp16, deterministic=deterministic, **NV)
+    ref = run_oracle(w, dq_fp16=dq_fp16, **NV_ORC)
+    _check(tc, ref)
+    if deterministic:
+        again = run_gpu(w, dq_fp16=dq_fp16, deterministic=deterministic, **NV)
+        assert torch.equal(tc.dQ, again.dQ) and torch.equal(tc.dK, again.dK)
+
+
 def test_mixed_outlier_channels():
     # x20 channels in Q and K: near one-hot softmax, dS cancels down to O's
     # rounding; compare against the oracle within its own O-rounding sensitivity
