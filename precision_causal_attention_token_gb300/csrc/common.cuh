@@ -21,8 +21,7 @@ struct WsHeader {
   int32_t n_blk32;         // document-local 32-token blocks
   uint32_t fwd_counter;    // persistent-grid work counters (reset per launch)
   uint32_t bwd_counter;
-  uint32_t dq_counter;
-  uint32_t pad0;
+  uint32_t pad0[2];
   uint8_t* dbg_phat;       // test hook: P^ codes [H][T][T] (null: off)
   int32_t* dbg_eb;         // test hook: P^ block exponents [H][T][T] at each block's first key
   uint32_t pad[52];

@@ -30,7 +30,6 @@ __global__ void __launch_bounds__(1024) plan_prefix_kernel(const int32_t* __rest
     bad = (__ldg(cu) != 0 || __ldg(cu + n_seq) != T) ? 1 : 0;
     hdr->fwd_counter = 0;
     hdr->bwd_counter = 0;
-    hdr->dq_counter = 0;
     hdr->status = 0;         // the status word covers one call, plan through backward
     hdr->status_where = 0;
     hdr->dbg_phat = nullptr;  // test hooks off unless set after the plan
