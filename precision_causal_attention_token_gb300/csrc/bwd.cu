@@ -907,44 +907,47 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, void* out, size
   }
 }
 
-// The FP16 dQ accumulator (sums of 2^p dS^ K^ over key tiles) times the
-// softmax scale and 2^-p of its row -> output dtype.  One warp per (token,
-// head) row: the row's prescale is read once, lane l converts elements
-// [l HD/32, (l + 1) HD/32).
+// FP16 dQ accumulator (prescaled partial sums) -> dQ: each element times the
+// softmax scale and 2^-p of its row -> output dtype.  A row of HD FP16 values
+// is HD/8 lanes' 16-byte loads; a warp takes 32/(HD/8) rows at a time and two
+// such groups per loop trip, so each lane keeps 32 bytes of loads in flight.
 template <bool OUT_BF16, int HD>
 __global__ void __launch_bounds__(256) dq16_convert_kernel(const __half* __restrict__ acc,
                                                            const int8_t* __restrict__ pexp, void* out, size_t rows,
                                                            float scale, int T, int H) {
-  constexpr int EPL = HD / 32;
-  const int lane = threadIdx.x & 31;
-  const size_t warps = (size_t)gridDim.x * (blockDim.x >> 5);
-  for (size_t r = blockIdx.x * (size_t)(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+  constexpr int LPR = HD / 8;   // lanes per row
+  constexpr int RPW = 32 / LPR;  // rows per warp and group
+  const int lane = threadIdx.x & 31, sub = lane / LPR, col = (lane % LPR) * 8;
+  const size_t warp = blockIdx.x * (size_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
+  const size_t stride = (size_t)gridDim.x * (blockDim.x >> 5) * RPW;
+#pragma unroll 2
+  for (size_t r0 = warp * RPW; r0 < rows; r0 += stride) {
+    const size_t r = r0 + sub;
+    if (r >= rows) continue;
     const int t = (int)(r / (size_t)H), h = (int)(r - (size_t)t * H);
     const float f = scale * pow2_127(-(int)__ldg(pexp + (size_t)h * T + t));
-    const size_t o = r * HD + (size_t)lane * EPL;
-    float v[EPL];
-    if constexpr (EPL == 4) {
-      const uint2 u = *reinterpret_cast<const uint2*>(acc + o);
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-      v[0] = a.x * f; v[1] = a.y * f; v[2] = b.x * f; v[3] = b.y * f;
-    } else {
-      const uint32_t u = *reinterpret_cast<const uint32_t*>(acc + o);
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u));
-      v[0] = a.x * f; v[1] = a.y * f;
+    const size_t o = r * HD + (size_t)col;
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(acc + o));
+    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&uw[k]));
+      v[2 * k] = x.x * f;
+      v[2 * k + 1] = x.y * f;
     }
     if constexpr (OUT_BF16) {
-      uint32_t w[EPL / 2];
+      uint32_t w[4];
 #pragma unroll
-      for (int e = 0; e < EPL; e += 2) {
-        const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[e], v[e + 1]);
-        w[e / 2] = *reinterpret_cast<const uint32_t*>(&b2);
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+        w[k] = *reinterpret_cast<const uint32_t*>(&b2);
       }
-      if constexpr (EPL == 4) *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + o) = make_uint2(w[0], w[1]);
-      else *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(out) + o) = w[0];
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + o) = make_uint4(w[0], w[1], w[2], w[3]);
     } else {
-      if constexpr (EPL == 4) *reinterpret_cast<float4*>(static_cast<float*>(out) + o) = make_float4(v[0], v[1], v[2], v[3]);
-      else *reinterpret_cast<float2*>(static_cast<float*>(out) + o) = make_float2(v[0], v[1]);
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + o);
+      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
     }
   }
 }
@@ -1182,7 +1185,7 @@ static cudaError_t launch_bwd_t(const AttnParams& p_in, const AttnMaps& m, cudaS
                                             st);
     }
     const size_t rows = (size_t)p.T * p.H;
-    const size_t want = (rows + 7) / 8;  // eight warps a block, a row a warp
+    const size_t want = (rows + 8 * (32 / (HD / 8)) - 1) / (8 * (32 / (HD / 8)));  // eight warps a block
     const int blocks = (int)(want < (size_t)nsm * 16 ? (want < 1 ? 1 : want) : (size_t)nsm * 16);
     dq16_convert_kernel<OB, HD><<<blocks, 256, 0, st>>>(p.dq16, p.pexp, p.dQ, rows, p.softmax_scale, p.T, p.H);
     return cudaGetLastError();

@@ -86,45 +86,41 @@ __device__ __forceinline__ int doc_of_tile(const int32_t* __restrict__ tile_pref
   return lo;
 }
 
-// keys[0 .. sort_n) forward list, keys[sort_n .. 2 sort_n) backward list.
+// Sort key of slot g of list `lst` (0: forward, 1: backward).
 // A real item's cost is at least 1, so its key's high word is at most
 // 0xFFFFFFFE; a padding slot g gets the high word 0xFFFFFFFF and its own
 // index below, so padding keys are unique too and sort after every real key
 // in slot order.  (Equal padding keys would collide in the merge passes.)
-__global__ void plan_keys_kernel(const int32_t* __restrict__ tile_prefix, int n_seq, int causal, int sort_n,
-                                 const WsHeader* hdr, uint64_t* keys) {
-  const int g = blockIdx.x * blockDim.x + threadIdx.x;
-  if (g >= sort_n) return;
-  const int n_items = hdr->n_items;
-  uint64_t kf = (0xFFFFFFFFull << 32) | (uint32_t)g, kb = kf;
-  if (g < n_items) {
-    const int doc = doc_of_tile(tile_prefix, n_seq, g);
-    const int tile = g - __ldg(tile_prefix + doc);
-    const int nt = __ldg(tile_prefix + doc + 1) - __ldg(tile_prefix + doc);
-    const uint32_t cf = causal ? (uint32_t)(tile + 1) : (uint32_t)nt;
-    const uint32_t cb = causal ? (uint32_t)(nt - tile) : (uint32_t)nt;
-    kf = ((uint64_t)(0xFFFFFFFFu - cf) << 32) | (uint32_t)g;
-    kb = ((uint64_t)(0xFFFFFFFFu - cb) << 32) | (uint32_t)g;
-  }
-  keys[g] = kf;
-  keys[sort_n + g] = kb;
+__device__ __forceinline__ uint64_t plan_key(const int32_t* __restrict__ tile_prefix, int n_seq, int causal,
+                                             int n_items, int lst, int g) {
+  if (g >= n_items) return (0xFFFFFFFFull << 32) | (uint32_t)g;
+  const int doc = doc_of_tile(tile_prefix, n_seq, g);
+  const int tile = g - __ldg(tile_prefix + doc);
+  const int nt = __ldg(tile_prefix + doc + 1) - __ldg(tile_prefix + doc);
+  const uint32_t cost = causal ? (uint32_t)(lst == 0 ? tile + 1 : nt - tile) : (uint32_t)nt;
+  return ((uint64_t)(0xFFFFFFFFu - cost) << 32) | (uint32_t)g;
 }
 
-// Bitonic sort of kSortBlock keys per CTA (ascending).  Keys past the real
-// items are padding, larger than every real key and ascending with the slot,
-// so a block whose real keys fit in the first P = 2^k slots only runs the
-// network up to size P: the padding above stays in place and the block ends
-// sorted.
-__global__ void __launch_bounds__(1024) block_sort_kernel(uint64_t* keys, int sort_n, const WsHeader* hdr) {
+// Builds and sorts (bitonic, ascending) kSortBlock keys per CTA: keys[0 ..
+// sort_n) hold the forward list, keys[sort_n .. 2 sort_n) the backward list.
+// Keys past the real items are padding, larger than every real key and
+// ascending with the slot, so a block whose real keys fit in the first
+// P = 2^k slots only runs the network up to size P: the padding above stays in
+// place and the block ends sorted.
+__global__ void __launch_bounds__(1024) block_sort_kernel(const int32_t* __restrict__ tile_prefix, int n_seq,
+                                                          int causal, uint64_t* keys, int sort_n,
+                                                          const WsHeader* hdr) {
   __shared__ uint64_t s[kSortBlock];
   uint64_t* k = keys + (size_t)blockIdx.x * kSortBlock;
   const int tid = threadIdx.x;
   const int per_list = sort_n / kSortBlock;
-  const int n_real = min(kSortBlock, max(0, hdr->n_items - (int)(blockIdx.x % per_list) * kSortBlock));
+  const int lst = (int)blockIdx.x / per_list, g0 = ((int)blockIdx.x % per_list) * kSortBlock;
+  const int n_items = hdr->n_items;
+  const int n_real = min(kSortBlock, max(0, n_items - g0));
   int P = 2;
   while (P < n_real) P <<= 1;
-  s[tid] = k[tid];
-  s[tid + 1024] = k[tid + 1024];
+  s[tid] = plan_key(tile_prefix, n_seq, causal, n_items, lst, g0 + tid);
+  s[tid + 1024] = plan_key(tile_prefix, n_seq, causal, n_items, lst, g0 + tid + 1024);
   __syncthreads();
   for (int size = 2; size <= P; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
@@ -194,8 +190,7 @@ cudaError_t launch_plan(const flamia_problem_t& p, const WsLayout& L, uint8_t* w
   uint64_t* kb = reinterpret_cast<uint64_t*>(ws + L.keys_b);
   plan_prefix_kernel<<<1, 1024, 0, st>>>(p.cu_seqlens, p.n_seq, p.T, tile_prefix, blk_prefix, hdr);
   const int n = L.sort_n;
-  plan_keys_kernel<<<(n + 255) / 256, 256, 0, st>>>(tile_prefix, p.n_seq, p.causal, n, hdr, ka);
-  block_sort_kernel<<<2 * n / kSortBlock, 1024, 0, st>>>(ka, n, hdr);
+  block_sort_kernel<<<2 * n / kSortBlock, 1024, 0, st>>>(tile_prefix, p.n_seq, p.causal, ka, n, hdr);
   uint64_t *src = ka, *dst = kb;
   for (int w = kSortBlock; w < n; w *= 2) {
     merge_pass_kernel<<<(2 * n + 255) / 256, 256, 0, st>>>(src, dst, n, w);
@@ -271,14 +266,13 @@ extern "C" flamia_status_t flamia_plan_noalloc(const flamia_problem_t* p, int2* 
   if (sc == nullptr) return FLAMIA_ERR_CUDA;
   const int n = ((max_items + kSortBlock - 1) / kSortBlock) * kSortBlock;
   // every scratch word a kernel reads is written earlier in this sequence:
-  // the prefix kernel writes the header and both tables, the key kernel all
+  // the prefix kernel writes the header and both tables, the sort kernel all
   // 2n keys (unique, padding included), and each merge pass writes a
   // permutation of its source, so nothing needs clearing between calls
   plan_prefix_kernel<<<1, 1024, 0, stream>>>(p->cu_seqlens, p->n_seq, p->T, sc->tile_prefix, sc->blk_prefix,
                                             &sc->hdr);
-  plan_keys_kernel<<<(n + 255) / 256, 256, 0, stream>>>(sc->tile_prefix, p->n_seq, p->causal, n, &sc->hdr,
-                                                        sc->keys_a);
-  block_sort_kernel<<<2 * n / kSortBlock, 1024, 0, stream>>>(sc->keys_a, n, &sc->hdr);
+  block_sort_kernel<<<2 * n / kSortBlock, 1024, 0, stream>>>(sc->tile_prefix, p->n_seq, p->causal, sc->keys_a, n,
+                                                             &sc->hdr);
   uint64_t *src = sc->keys_a, *dst = sc->keys_b;
   for (int w = kSortBlock; w < n; w *= 2) {
     merge_pass_kernel<<<(2 * n + 255) / 256, 256, 0, stream>>>(src, dst, n, w);
