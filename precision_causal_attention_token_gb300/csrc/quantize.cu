@@ -193,6 +193,18 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int2 loc, int 
     if (t < ntok) raw[t].load(x + (size_t)(t0 + t) * row + (size_t)h * HD + lane * EPL);
     else raw[t].zero();
   }
+  // dO role: O's rows are read in two chunks; the first is requested now, so
+  // its latency overlaps the exponent and code passes
+  constexpr int kOChunk = 16;
+  const TO* __restrict__ Ob = static_cast<const TO*>(a.O) + (size_t)t0 * row + (size_t)h * HD + lane * EPL;
+  RawRow<TO, EPL> oa[WITH_D ? kOChunk : 1];
+  if constexpr (WITH_D) {
+#pragma unroll
+    for (int t8 = 0; t8 < kOChunk; ++t8) {
+      if (t8 < ntok) oa[t8].load(Ob + (size_t)t8 * row);
+      else oa[t8].zero();
+    }
+  }
   if (g_next >= 0) loc_next = block_tokens(g_next, cu, blk_prefix, n_seq, lane);
   static_assert(!ROT || (!WITH_D && !NVFP4), "only Q/K/V launches of the MXFP8 path rotate");
   // token t's EPL values of this lane (rotated when the unit rotates; a zero
@@ -320,36 +332,34 @@ __device__ __forceinline__ void quantize_unit(const QuantArgs& a, int2 loc, int 
     if constexpr (WITH_D) {
       // D's terms are code * O (products exact in fp32); the exponent is
       // applied to the lane's partial sum (per token) or to the token's sum
-      // (token block).  O is read kOChunk rows at a time.
-      constexpr int kOChunk = sizeof(TO) == 2 ? 16 : 8;
+      // (token block).  The second chunk of O's rows is requested before the
+      // first chunk's sums.
       float dpart[32];
-      const TO* __restrict__ Ob = static_cast<const TO*>(a.O) + (size_t)t0 * row + (size_t)h * HD + lane * EPL;
+      RawRow<TO, EPL> ob[kOChunk];
 #pragma unroll
-      for (int c8 = 0; c8 < 32; c8 += kOChunk) {
-        RawRow<TO, EPL> orow[kOChunk];
-#pragma unroll
-        for (int t8 = 0; t8 < kOChunk; ++t8) {
-          if (c8 + t8 < ntok) orow[t8].load(Ob + (size_t)(c8 + t8) * row);
-          else orow[t8].zero();
-        }
-#pragma unroll
-        for (int t8 = 0; t8 < kOChunk; ++t8) {
-          const int t = c8 + t8;
-          const uint32_t cw = cws[t];
-          float acc = 0.f;
-#pragma unroll
-          for (int e = 0; e < EPL; e += 2) {
-            const float2 d2 = unpack_e4m3x2((uint16_t)(cw >> (8 * e)));
-            acc = fmaf(d2.x, orow[t8].at(e), acc);
-            acc = fmaf(d2.y, orow[t8].at(e + 1), acc);
-          }
-          if (a.per_token) {
-            const float2 s2 = pow2_pair(__shfl_sync(0xffffffffu, my_e, t));
-            acc = (acc * s2.x) * s2.y;
-          }
-          dpart[t] = acc;
-        }
+      for (int t8 = 0; t8 < kOChunk; ++t8) {
+        if (kOChunk + t8 < ntok) ob[t8].load(Ob + (size_t)(kOChunk + t8) * row);
+        else ob[t8].zero();
       }
+      auto d_term = [&](int t, const RawRow<TO, EPL>& orow) {
+        const uint32_t cw = cws[t];
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; e += 2) {
+          const float2 d2 = unpack_e4m3x2((uint16_t)(cw >> (8 * e)));
+          acc = fmaf(d2.x, orow.at(e), acc);
+          acc = fmaf(d2.y, orow.at(e + 1), acc);
+        }
+        if (a.per_token) {
+          const float2 s2 = pow2_pair(__shfl_sync(0xffffffffu, my_e, t));
+          acc = (acc * s2.x) * s2.y;
+        }
+        dpart[t] = acc;
+      };
+#pragma unroll
+      for (int t8 = 0; t8 < kOChunk; ++t8) d_term(t8, oa[t8]);
+#pragma unroll
+      for (int t8 = 0; t8 < kOChunk; ++t8) d_term(kOChunk + t8, ob[t8]);
       float dsum = transpose_reduce<false>(dpart, lane);
       if (!a.per_token) {
         const float2 s2 = pow2_pair(e_blk);
