@@ -58,17 +58,17 @@ constexpr uint32_t kColSfDV = kColX1 + 64, kColSfDK = kColX1 + 68, kColSfDQ = kC
 // qn Q's) with their block scales staged in ksf / qsf; dK and dQ still
 // contract with the E4M3 Q and K codes (q, k8).
 // K/V tiles of consecutive work items are double-buffered so the next item's
-// copies land while this one is processed (one buffer on the mixed path with
-// dQ, whose extra E4M3 K tile leaves no room for a second).
-template <bool NV4, bool DQ>
+// copies land while this one is processed (one buffer on the mixed path,
+// whose extra E4M3 K tile leaves no room for a second).
+template <bool NV4>
 constexpr int bwd_kv_stages() {
-  return NV4 && DQ ? 1 : 2;
+  return NV4 ? 1 : 2;
 }
 
-template <int HD, bool EXACT, bool DQ, bool NV4>
+template <int HD, bool EXACT, bool NV4>
 struct __align__(1024) BwdTiles {
-  uint8_t k[bwd_kv_stages<NV4, DQ>()][score_tile_bytes<HD, NV4>()];
-  uint8_t v[bwd_kv_stages<NV4, DQ>()][kTile * HD];
+  uint8_t k[bwd_kv_stages<NV4>()][score_tile_bytes<HD, NV4>()];
+  uint8_t v[bwd_kv_stages<NV4>()][kTile * HD];
   uint8_t q[2][kTile * HD];
   uint8_t dO[2][kTile * HD];
   uint8_t pt[kTile * kTile];   // P~ codes   [query][key]
@@ -77,24 +77,24 @@ struct __align__(1024) BwdTiles {
   // one half (64 columns) of a dQ tile staged for the bulk reduce-adds: two
   // boxes of [128 rows][32 fp32], or one of [128 rows][64 FP16] (DQ16);
   // 128B-swizzled
-  uint8_t dqs[DQ ? kTile * 256 : 1024];
+  uint8_t dqs[kTile * 256];
   uint8_t qn[2][NV4 ? score_tile_bytes<HD, NV4>() : 16];  // mixed path: Q's score operand
   uint32_t qsf[2][NV4 ? 256 : 4];                          // mixed path: its block scales
-  uint32_t ksf[bwd_kv_stages<NV4, DQ>()][NV4 ? 256 : 4];   // and K's
-  // mixed path with dQ: K's E4M3 codes for the dQ MMA.  Last, after members
-  // that are whole KB on the mixed path: every tile above must stay at a
+  uint32_t ksf[bwd_kv_stages<NV4>()][NV4 ? 256 : 4];       // and K's
+  // mixed path: K's E4M3 codes for the dQ MMA.  Last, after members that
+  // are whole KB on the mixed path: every tile above must stay at a
   // 1024-byte boundary (swizzled TMA destinations, MMA operands)
-  uint8_t k8[NV4 && DQ ? bwd_kv_stages<NV4, DQ>() : 1][NV4 && DQ ? kTile * HD : 16];
+  uint8_t k8[NV4 ? bwd_kv_stages<NV4>() : 1][NV4 ? kTile * HD : 16];
 };
 // every tile's offset is a multiple of 1024 bytes on every variant used
-template <int HD, bool EXACT, bool DQ, bool NV4>
+template <int HD, bool EXACT, bool NV4>
 constexpr bool bwd_tiles_aligned() {
-  using T = BwdTiles<HD, EXACT, DQ, NV4>;
+  using T = BwdTiles<HD, EXACT, NV4>;
   return offsetof(T, q) % 1024 == 0 && offsetof(T, dO) % 1024 == 0 && offsetof(T, pt) % 1024 == 0 &&
          offsetof(T, ds) % 1024 == 0 && offsetof(T, dsk) % 1024 == 0 && offsetof(T, dqs) % 1024 == 0 &&
          offsetof(T, v) % 1024 == 0 && (!NV4 || (offsetof(T, qn) % 1024 == 0 && offsetof(T, qsf) % 1024 == 0 &&
                                                  offsetof(T, ksf) % 1024 == 0)) &&
-         (!(NV4 && DQ) || offsetof(T, k8) % 1024 == 0);
+         (!NV4 || offsetof(T, k8) % 1024 == 0);
 }
 
 // Per-row values of one query tile, staged in shared memory by the producer
@@ -120,9 +120,9 @@ struct BwdCtl {
   int abort_flag;
 };
 
-template <int HD, bool EXACT, bool DQ, bool NV4>
+template <int HD, bool EXACT, bool NV4>
 constexpr size_t bwd_smem_bytes() {
-  return sizeof(BwdTiles<HD, EXACT, DQ, NV4>) + sizeof(BwdCtl) + 1024;
+  return sizeof(BwdTiles<HD, EXACT, NV4>) + sizeof(BwdCtl) + 1024;
 }
 
 __device__ __forceinline__ uint64_t bdesc_k(const uint8_t* t, uint32_t off, uint32_t rb) {
@@ -302,26 +302,26 @@ __device__ __forceinline__ uint32_t dq_operand(const float (&wv)[32], float amax
 }
 
 // ============================================================================
-// dK/dV kernel (and dQ when DQ; DQ16: FP16 partials): one CTA per (document,
-// 128-key tile, KV head), looping over the group's query heads and tiles.  With DQ, each query
-// tile's dQ = dS^ K^ lands in TMEM, is staged in shared memory by the compute
-// warps and added to the fp32 dQ buffer by the reducer warp with bulk tensor
-// reduce-adds (whole 128-byte lines, the addition done in L2).
+// Backward kernel (DQ16: FP16 dQ partials): one CTA per (document, 128-key
+// tile, KV head), looping over the group's query heads and tiles.  dK and dV
+// accumulate in TMEM; each query tile's dQ = dS^ K^ lands in TMEM, is staged
+// in shared memory by the drain warps and added to the dQ buffer by the
+// reducer warp with bulk tensor reduce-adds (whole 128-byte lines, the
+// addition done in L2).
 // ============================================================================
-template <int HD, bool OUT_BF16, bool EXACT, bool DQ, bool NV4, bool DQ16>
+template <int HD, bool OUT_BF16, bool EXACT, bool NV4, bool DQ16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const AttnParams p, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                const __grid_constant__ CUtensorMap map_dq, const __grid_constant__ CUtensorMap map_qn,
                const __grid_constant__ CUtensorMap map_kn) {
-  static_assert(DQ || !DQ16, "FP16 partials belong to the dQ path");
-  static_assert(bwd_tiles_aligned<HD, EXACT, DQ, NV4>(), "tile alignment");
-  constexpr int kKvStages = bwd_kv_stages<NV4, DQ>();
+  static_assert(bwd_tiles_aligned<HD, EXACT, NV4>(), "tile alignment");
+  constexpr int kKvStages = bwd_kv_stages<NV4>();
   constexpr bool PERKEY = EXACT || NV4;
   constexpr int kQKBytes = score_tile_bytes<HD, NV4>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_base_1k(smem_raw);
-  using Tiles = BwdTiles<HD, EXACT, DQ, NV4>;
+  using Tiles = BwdTiles<HD, EXACT, NV4>;
   Tiles& tl = *reinterpret_cast<Tiles*>(base);
   BwdCtl& c = *reinterpret_cast<BwdCtl*>(base + sizeof(Tiles));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -352,8 +352,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&c.xch_bar, kBwdCompute);
     mbar_init(&c.dqs_full, 128);
     mbar_init(&c.dqs_free, 1);
-    // readers: the MMA thread, the dQ reducer (DQ), four drain and eight compute warps
-    item_ring_init(c.ring, 1 + (DQ ? 1 : 0) + 4 + kBwdCompute / 32);
+    // readers: the MMA thread, the dQ reducer, four drain and eight compute warps
+    item_ring_init(c.ring, 1 + 1 + 4 + kBwdCompute / 32);
     c.abort_flag = 0;
     fence_mbar_init();
   }
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     prefetch_tensormap(&map_k);
     prefetch_tensormap(&map_v);
     prefetch_tensormap(&map_do);
-    if (DQ) prefetch_tensormap(&map_dq);
+    prefetch_tensormap(&map_dq);
     if (NV4) {
       prefetch_tensormap(&map_qn);
       prefetch_tensormap(&map_kn);
@@ -408,10 +408,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if constexpr (NV4) stage_nv_scales<HD>(tl.ksf[kvs], p.k_bs, p.Hkv, hk, k0, p.T, lane);
       if (lane == 0) {
-        mbar_arrive_expect_tx(&c.kv_full[kvs], kQKBytes + kTile * HD + (NV4 && DQ ? kTile * HD : 0));
+        mbar_arrive_expect_tx(&c.kv_full[kvs], kQKBytes + kTile * HD + (NV4 ? kTile * HD : 0));
         load_score_tile<HD, NV4>(tl.k[kvs], &map_k, &map_kn, &c.kv_full[kvs], hk, k0);
         tma_load_3d(tl.v[kvs], &map_v, &c.kv_full[kvs], 0, hk, k0);
-        if (NV4 && DQ) tma_load_3d(tl.k8[kvs], &map_k, &c.kv_full[kvs], 0, hk, k0);
+        if (NV4) tma_load_3d(tl.k8[kvs], &map_k, &c.kv_full[kvs], 0, hk, k0);
       } else {
         mbar_arrive(&c.kv_full[kvs]);
       }
@@ -478,14 +478,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // dP of query tile ii into X1
         auto issue_dp = [&](uint32_t i_p) -> bool {
           // X1 is free once the previous tile's MMAs have read their scale
-          // factors there and (DQ) its dQ tile has been drained
-          if constexpr (DQ) {
-            if (!mbar_wait(&c.x1_free, (i_p & 1) ^ 1, abort_flag, hdr, 0x314)) return false;
-            // d = 64: the single dQ tile may drain before dV / dK have read the scale factors
-            if (HD == 64 && i_p > 0 && !mbar_wait(&c.mm_done, (i_p - 1) & 1, abort_flag, hdr, 0x319)) return false;
-          } else {
-            if (i_p > 0 && !mbar_wait(&c.mm_done, (i_p - 1) & 1, abort_flag, hdr, 0x314)) return false;
-          }
+          // factors there and its dQ tile has been drained
+          if (!mbar_wait(&c.x1_free, (i_p & 1) ^ 1, abort_flag, hdr, 0x314)) return false;
+          // d = 64: the single dQ tile may drain before dV / dK have read the scale factors
+          if (HD == 64 && i_p > 0 && !mbar_wait(&c.mm_done, (i_p - 1) & 1, abort_flag, hdr, 0x319)) return false;
           // mixed path: S(i_p) has read its scale factors in X1
           if (NV4 && !mbar_wait(&c.s_full, i_p & 1, abort_flag, hdr, 0x31a)) return false;
           tc_fence_after();
@@ -518,10 +514,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        bdesc_mn(NV4 ? tl.k8[kvs] : tl.k[kvs], kk * 32 * HD + 64 * half, HD),
                        idesc_mxf8(128, 64, 0, 1, kk, kk), tb + kColSfDQ, tb + kColSfOne, kk > 0 ? 1u : 0u);
           };
-          if constexpr (DQ) {
-            issue_dq(0);
-            tc_commit(&c.dq_lo_full);
-          }
+          issue_dq(0);
+          tc_commit(&c.dq_lo_full);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {  // contraction over the 128 queries
             const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
@@ -530,7 +524,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_mxf8(tb + kColDK, bdesc_mn(dsk, kk * 32 * 128, 128), bdesc_mn(tl.q[qs], kk * 32 * HD, HD),
                      idesc_mxf8(128, HD, 1, 1, kk, kk), tb + kColSfDK, tb + kColSfOne, acc);
           }
-          if constexpr (DQ && HD == 128) {
+          if constexpr (HD == 128) {
             if (!(ok = mbar_wait(&c.dq_lo_free, ii & 1, abort_flag, hdr, 0x317))) break;
             tc_fence_after();
             issue_dq(1);
@@ -561,7 +555,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // for them costs nothing; releasing never waits on another CTA.  Every
     // wait points at a key tile with more query tiles, which the
     // longest-first list hands out earlier: no cycle.
-    if (DQ && lane == 0) {
+    if (lane == 0) {
       constexpr int kHalves = HD / 64;
       uint32_t ii = 0, hc = 0;  // hc: staged halves
       bool ok = true;
@@ -639,7 +633,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp >= kWarpDrain0) {
     setmaxnreg_dec<kRegDrain>();
     // ------------------------------------------------------------ drain
-    // Warp 8 + qq reads TMEM lane quarter qq.  Per query tile (DQ): rows
+    // Warp 8 + qq reads TMEM lane quarter qq.  Per query tile: rows
     // 32qq..32qq+31 of the finished dQ tile are staged for the reducer, 32
     // columns at a time, into the 128B-swizzled [128 rows][32 fp32] boxes.
     // Rows outside the document hold exact zeros (their dS row is zero), so
@@ -657,7 +651,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int ds = __ldg(p.cu + it.x), len = __ldg(p.cu + it.x + 1) - ds;
       const int n_t = (len + kTile - 1) / kTile, q_first = p.causal ? it.y : 0;
       const int n_iter = G * (n_t - q_first);
-      if constexpr (DQ) {
+      {  // the dQ tiles of this item
         const int per_g = n_t - q_first;
         for (int t = 0; ok && t < n_iter; ++t, ++ii) {
           // this iteration's query tile and head (the order of every role)
@@ -831,11 +825,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               store_row_block(tl.ds, r, b, codes);
               kbyte = sf_byte(e_ds + rv.eq);  // dK operand: the same codes, Q's block exponent folded in
             } else {
-              if constexpr (DQ) {
-                int unused;
-                qbyte = dq_operand<true>(wv, amax_w, gbh, c.kf[kvs] + 32 * b, c.ekb[kvs][b], codes, unused);
-                store_row_block(tl.ds, r, b, codes);
-              }
+              int unused;
+              qbyte = dq_operand<true>(wv, amax_w, gbh, c.kf[kvs] + 32 * b, c.ekb[kvs][b], codes, unused);
+              store_row_block(tl.ds, r, b, codes);
               // dK operand: 32 x 32 block of dS * 2^eQ(i)
               const float gq = gbh * pow2_127(rv.eq);
               float f[32];
@@ -1160,8 +1152,8 @@ static cudaError_t launch_bwd_t(const AttnParams& p_in, const AttnMaps& m, cudaS
   const int nsm = sm_count();
   const int grid = attn_grid((long)p.max_items * p.Hkv, nsm, p.clc);
   cudaError_t e;
-  const size_t smem = bwd_smem_bytes<HD, EX, true, NV4>();
-  static_assert(bwd_smem_bytes<HD, EX, true, NV4>() <= 232448, "shared memory");
+  const size_t smem = bwd_smem_bytes<HD, EX, NV4>();
+  static_assert(bwd_smem_bytes<HD, EX, NV4>() <= 232448, "shared memory");
   const size_t n4 = (size_t)p.T * p.H * HD / 4;
   int cg = (int)((n4 + 255) / 256);
   if (cg > nsm * 8) cg = nsm * 8;
@@ -1170,11 +1162,11 @@ static cudaError_t launch_bwd_t(const AttnParams& p_in, const AttnMaps& m, cudaS
       (e = cudaMemsetAsync(p.dq_order, 0, sizeof(uint32_t) * (size_t)p.max_items * p.H, st)) != cudaSuccess)
     return e;
   if (p.dq_fp16) {  // FP16 partials (never with the exact option), unordered or in key-tile order
-    if ((e = set_smem<bwd_kernel<HD, OB, EX, true, NV4, true>>(attn_smem_max(smem))) != cudaSuccess) return e;
+    if ((e = set_smem<bwd_kernel<HD, OB, EX, NV4, true>>(attn_smem_max(smem))) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(p.dq16, 0, 2 * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
     if (p.n_seq > 0) dq_prescale_kernel<<<dim3(p.n_seq, p.Hkv), kPrescaleThreads, 0, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_kernel<HD, OB, EX, true, NV4, true><<<grid, kBwdThreads, attn_smem(smem, p.clc), st>>>(
+    bwd_kernel<HD, OB, EX, NV4, true><<<grid, kBwdThreads, attn_smem(smem, p.clc), st>>>(
         p, m.q, m.k, m.v, m.dO, m.dq, m.qn, m.kn);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (!NV4 && p.hadamard) {
@@ -1190,9 +1182,9 @@ static cudaError_t launch_bwd_t(const AttnParams& p_in, const AttnMaps& m, cudaS
     dq16_convert_kernel<OB, HD><<<blocks, 256, 0, st>>>(p.dq16, p.pexp, p.dQ, rows, p.softmax_scale, p.T, p.H);
     return cudaGetLastError();
   }
-  if ((e = set_smem<bwd_kernel<HD, OB, EX, true, NV4, false>>(attn_smem_max(smem))) != cudaSuccess) return e;
+  if ((e = set_smem<bwd_kernel<HD, OB, EX, NV4, false>>(attn_smem_max(smem))) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(p.dq_acc, 0, 4 * (size_t)p.T * p.H * HD, st)) != cudaSuccess) return e;
-  bwd_kernel<HD, OB, EX, true, NV4, false><<<grid, kBwdThreads, attn_smem(smem, p.clc), st>>>(
+  bwd_kernel<HD, OB, EX, NV4, false><<<grid, kBwdThreads, attn_smem(smem, p.clc), st>>>(
       p, m.q, m.k, m.v, m.dO, m.dq, m.qn, m.kn);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (!NV4 && p.hadamard) {
