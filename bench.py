@@ -49,6 +49,8 @@ def _args():
                     help="processes of the all-core oracle sample (one single-threaded oracle per head)")
     ap.add_argument("--cpu-sample-tokens-all", type=int, default=1024,
                     help="causal prefix length of each process of the all-core oracle sample")
+    ap.add_argument("--e2e-sets", type=int, default=2,
+                    help="input/output buffer sets in flight in the end-to-end pipeline")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the packed / long-GQA workloads and the option overheads")
     ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5],
@@ -531,17 +533,18 @@ def run_ours(a):
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
     d2h = sum(x.numel() * x.element_size() for x in outs)
     e2e_steps = max(3, a.steps // 2)
-    tc2 = fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu, path=tc.path)
-    ins = [(q, k, v, do), tuple(torch.empty_like(x) for x in (q, k, v, do))]
-    calls = [(tc, step), (tc2, _step_fn(fl, tc2, ins[1]))]
+    nset = max(2, a.e2e_sets)
+    ins = [(q, k, v, do)] + [tuple(torch.empty_like(x) for x in (q, k, v, do)) for _ in range(nset - 1)]
+    extra_calls = [fl.TrainCall(w.T, w.H, w.Hkv, w.d, cu, path=tc.path) for _ in range(nset - 1)]
+    calls = [(tc, step)] + [(c2, _step_fn(fl, c2, ins[n + 1])) for n, c2 in enumerate(extra_calls)]
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev = {n: [torch.cuda.Event(), torch.cuda.Event()] for n in ("in", "done", "out")}
+    ev = {n: [torch.cuda.Event() for _ in range(nset)] for n in ("in", "done", "out")}
     for n in ("done", "out"):  # nothing to wait for on the first use of each set
         for e in ev[n]:
             e.record(stream)
 
     def e2e_step(i):
-        j = i & 1
+        j = i % nset
         with torch.cuda.stream(s_in):
             s_in.wait_event(ev["done"][j])  # the set's previous step has read its inputs
             for dst, src in zip(ins[j], (hq, hk, hv, hdo)):
@@ -557,7 +560,7 @@ def run_ours(a):
                 o.copy_(src, non_blocking=True)
             ev["out"][j].record(s_out)
 
-    for i in range(2):
+    for i in range(nset):
         e2e_step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -565,12 +568,12 @@ def run_ours(a):
     s_in.wait_event(e0)
     for i in range(e2e_steps):
         e2e_step(i)
-    stream.wait_event(ev["out"][(e2e_steps - 1) & 1])
+    stream.wait_event(ev["out"][(e2e_steps - 1) % nset])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
     e2e_val = job_rate(flops, world, e2e_ms)
-    del tc2
+    del extra_calls, calls
 
     # secondary measurements (rank 0 of the default workload only): the packed
     # and long-GQA workloads, and the cost of the deterministic and exact options
@@ -643,8 +646,9 @@ def run_ours(a):
                                     f"timed alone in under a millisecond"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "timing": "every step copies its inputs in and its results out; the copies of the next step's "
-                          "inputs and the previous step's results run on two copy streams during compute"},
+                "timing": "every step copies its inputs in and its results out; the copies of later steps' "
+                          "inputs and earlier steps' results run on two copy streams during compute",
+                "buffer_sets": nset, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * a.steps,
         "clocks": clk,
     }
