@@ -63,6 +63,33 @@ def test_mixed_fused_dq_options(dq_fp16, deterministic):
         assert torch.equal(tc.dQ, again.dQ) and torch.equal(tc.dK, again.dK)
 
 
+def test_nvfp4_payload_on_rounding_midpoints():
+    # Each 16-element block holds the E2M1 rounding midpoints (0.25, 0.75,
+    # ..., 5) and the largest value 6, scaled by a power of two per token, so
+    # the block scale comes out at about 2^k and many quotients x / (s g) sit
+    # within a few ulps of a step of the E2M1 rounding: the product with the
+    # reciprocal cannot decide those and the exact quotient must.  The payload
+    # still equals the oracle's byte for byte.
+    T, H, d = 96, 2, 128
+    mids = np.array([6, 5, 3.5, 2.5, 1.75, 1.25, 0.75, 0.25, -5, -3.5, -2.5, -1.75, -1.25, -0.75, -0.25, 4],
+                    np.float32)
+    rng = np.random.default_rng(9)
+    x = np.empty((T, H, d), np.float32)
+    for t in range(T):
+        for h in range(H):
+            row = np.concatenate([rng.permutation(mids) for _ in range(d // 16)])
+            x[t, h] = row * np.float32(2.0 ** int(rng.integers(-6, 7)))
+    w = synth.custom([T], H=H, d=d, seed=710)
+    v = w.tensor("v")
+    tc = run_gpu(w, inputs=(x, x.copy(), v, w.tensor("do")), backward=False, **NV)
+    rc, rb, rg = oracle.quantize_nvfp4(x)
+    packed = tc.q4[0].cpu().numpy()
+    got = np.stack([packed & 0xF, packed >> 4], axis=-1).reshape(rc.shape)
+    assert (got == rc).all()
+    assert (tc.q4[1].cpu().numpy() == rb).all()
+    assert (tc.q4[2].cpu().numpy() == rg).all()
+
+
 def test_mixed_outlier_channels():
     # x20 channels in Q and K: near one-hot softmax, dS cancels down to O's
     # rounding; compare against the oracle within its own O-rounding sensitivity
