@@ -54,6 +54,19 @@ def test_clc_mixed_path_parity_and_identity():
         assert torch.equal(getattr(a, n), getattr(b, n)), n
 
 
+@pytest.mark.parametrize("kw,okw", [({"hadamard": True}, {"hadamard": True}),
+                                      ({"path": fl.PATH_NVFP4_FP8}, {"path": oracle.PATH_NVFP4_FP8})],
+                         ids=["hadamard", "mixed d=64"])
+def test_clc_with_other_options(kw, okw):
+    # the scheduler under the rotated-operand option and the mixed path at d = 64
+    d = 128 if "hadamard" in kw else 64
+    w = synth.custom([300, 45, 129, 1, 600], H=2, d=d, seed=807)
+    tc = run_gpu(w, clc=True, **kw)
+    ref = run_oracle(w, **okw)
+    names = ("O", "dQ", "dK", "dV")
+    compare_all(names, {n: getattr(tc, n) for n in names}, ref)
+
+
 def _same_up_to_dq_order(a, b, dq16):
     for n in ("O", "m", "l", "dK", "dV"):
         assert torch.equal(getattr(a, n), getattr(b, n)), n
