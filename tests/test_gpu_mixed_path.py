@@ -50,11 +50,12 @@ def test_mixed_parity_small(name, w, kw):
     _check(tc, ref)
 
 
-@pytest.mark.parametrize("dq_fp16,deterministic", [(True, False), (True, True), (False, True)])
-def test_mixed_fused_dq_options(dq_fp16, deterministic):
+@pytest.mark.parametrize("dq_fp16,deterministic,d", [(True, False, 128), (True, True, 128), (False, True, 128),
+                                                    (True, False, 64), (True, True, 64)])
+def test_mixed_fused_dq_options(dq_fp16, deterministic, d):
     # the mixed path's dQ goes through the fused backward's reduction like the
     # MXFP8 path's: FP16 or fp32 partials, unordered or in key-tile order
-    w = synth.custom([300, 45, 129, 1, 600], H=4, Hkv=2, d=128, seed=708)
+    w = synth.custom([300, 45, 129, 1, 600], H=4, Hkv=2, d=d, seed=708)
     tc = run_gpu(w, dq_fp16=dq_fp16, deterministic=deterministic, **NV)
     ref = run_oracle(w, dq_fp16=dq_fp16, **NV_ORC)
     _check(tc, ref)
