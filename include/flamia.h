@@ -292,7 +292,9 @@ flamia_status_t flamia_debug_withhold_first_item(int32_t on);
  * Limits: ceil(T/128) + n_seq <= 65536 and n_seq <= 65536, else
  * FLAMIA_ERR_UNSUPPORTED.  The first call on each device looks up the array's
  * device address with that device current (make that first call before any
- * stream capture).  All calls share the array and it keeps the last call's
+ * stream capture) and keeps it for the life of the process, so the entry
+ * point must not be used on a device after cudaDeviceReset.  All calls share
+ * the array and it keeps the last call's
  * contents: calls whose kernels may overlap on the GPU race with each other
  * and must be serialised by the caller. */
 flamia_status_t flamia_plan_noalloc(const flamia_problem_t* p, int2* fwd_items, int2* bwd_items, int32_t* n_items,
