@@ -106,10 +106,13 @@ __device__ __forceinline__ uint64_t plan_key(const int32_t* __restrict__ tile_pr
 // Keys past the real items are padding, larger than every real key and
 // ascending with the slot, so a block whose real keys fit in the first
 // P = 2^k slots only runs the network up to size P: the padding above stays in
-// place and the block ends sorted.
+// place and the block ends sorted.  When a list is a single block (no merge
+// pass follows), fwd_items / bwd_items are given and the CTA writes the work
+// items of its list directly instead of the sorted keys.
 __global__ void __launch_bounds__(1024) block_sort_kernel(const int32_t* __restrict__ tile_prefix, int n_seq,
                                                           int causal, uint64_t* keys, int sort_n,
-                                                          const WsHeader* hdr) {
+                                                          const WsHeader* hdr, int2* fwd_items,
+                                                          int2* bwd_items) {
   __shared__ uint64_t s[kSortBlock];
   uint64_t* k = keys + (size_t)blockIdx.x * kSortBlock;
   const int tid = threadIdx.x;
@@ -133,6 +136,19 @@ __global__ void __launch_bounds__(1024) block_sort_kernel(const int32_t* __restr
       }
       __syncthreads();
     }
+  }
+  if (fwd_items != nullptr) {  // per_list == 1: slot i of the block is position i of the list
+    int2* items = lst == 0 ? fwd_items : bwd_items;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = tid + 1024 * h;
+      if (i < n_items) {
+        const int g = (int)(uint32_t)(s[i] & 0xFFFFFFFFull);
+        const int doc = doc_of_tile(tile_prefix, n_seq, g);
+        items[i] = make_int2(doc, g - __ldg(tile_prefix + doc));
+      }
+    }
+    return;
   }
   k[tid] = s[tid];
   k[tid + 1024] = s[tid + 1024];
@@ -190,15 +206,19 @@ cudaError_t launch_plan(const flamia_problem_t& p, const WsLayout& L, uint8_t* w
   uint64_t* kb = reinterpret_cast<uint64_t*>(ws + L.keys_b);
   plan_prefix_kernel<<<1, 1024, 0, st>>>(p.cu_seqlens, p.n_seq, p.T, tile_prefix, blk_prefix, hdr);
   const int n = L.sort_n;
-  block_sort_kernel<<<2 * n / kSortBlock, 1024, 0, st>>>(tile_prefix, p.n_seq, p.causal, ka, n, hdr);
+  int2* fwd_items = reinterpret_cast<int2*>(ws + L.fwd_items);
+  int2* bwd_items = reinterpret_cast<int2*>(ws + L.bwd_items);
+  const bool one_block = n == kSortBlock;  // no merge pass: the sort writes the items
+  block_sort_kernel<<<2 * n / kSortBlock, 1024, 0, st>>>(tile_prefix, p.n_seq, p.causal, ka, n, hdr,
+                                                         one_block ? fwd_items : nullptr,
+                                                         one_block ? bwd_items : nullptr);
+  if (one_block) return cudaGetLastError();
   uint64_t *src = ka, *dst = kb;
   for (int w = kSortBlock; w < n; w *= 2) {
     merge_pass_kernel<<<(2 * n + 255) / 256, 256, 0, st>>>(src, dst, n, w);
     uint64_t* t = src; src = dst; dst = t;
   }
-  plan_items_kernel<<<(2 * n + 255) / 256, 256, 0, st>>>(src, tile_prefix, p.n_seq, n, hdr,
-                                                         reinterpret_cast<int2*>(ws + L.fwd_items),
-                                                         reinterpret_cast<int2*>(ws + L.bwd_items));
+  plan_items_kernel<<<(2 * n + 255) / 256, 256, 0, st>>>(src, tile_prefix, p.n_seq, n, hdr, fwd_items, bwd_items);
   return cudaGetLastError();
 }
 
@@ -267,21 +287,27 @@ extern "C" flamia_status_t flamia_plan_noalloc(const flamia_problem_t* p, int2* 
   const int n = ((max_items + kSortBlock - 1) / kSortBlock) * kSortBlock;
   // every scratch word a kernel reads is written earlier in this sequence:
   // the prefix kernel writes the header and both tables, the sort kernel all
-  // 2n keys (unique, padding included), and each merge pass writes a
-  // permutation of its source, so nothing needs clearing between calls
+  // 2n keys (unique, padding included) unless it writes the items itself
+  // (one block per list, nothing reads the keys then), and each merge pass
+  // writes a permutation of its source, so nothing needs clearing between
+  // calls
   plan_prefix_kernel<<<1, 1024, 0, stream>>>(p->cu_seqlens, p->n_seq, p->T, sc->tile_prefix, sc->blk_prefix,
                                             &sc->hdr);
+  const bool one_block = n == kSortBlock;  // no merge pass: the sort writes the items
   block_sort_kernel<<<2 * n / kSortBlock, 1024, 0, stream>>>(sc->tile_prefix, p->n_seq, p->causal, sc->keys_a, n,
-                                                             &sc->hdr);
-  uint64_t *src = sc->keys_a, *dst = sc->keys_b;
-  for (int w = kSortBlock; w < n; w *= 2) {
-    merge_pass_kernel<<<(2 * n + 255) / 256, 256, 0, stream>>>(src, dst, n, w);
-    uint64_t* t = src;
-    src = dst;
-    dst = t;
+                                                             &sc->hdr, one_block ? fwd_items : nullptr,
+                                                             one_block ? bwd_items : nullptr);
+  if (!one_block) {
+    uint64_t *src = sc->keys_a, *dst = sc->keys_b;
+    for (int w = kSortBlock; w < n; w *= 2) {
+      merge_pass_kernel<<<(2 * n + 255) / 256, 256, 0, stream>>>(src, dst, n, w);
+      uint64_t* t = src;
+      src = dst;
+      dst = t;
+    }
+    plan_items_kernel<<<(2 * n + 255) / 256, 256, 0, stream>>>(src, sc->tile_prefix, p->n_seq, n, &sc->hdr,
+                                                               fwd_items, bwd_items);
   }
-  plan_items_kernel<<<(2 * n + 255) / 256, 256, 0, stream>>>(src, sc->tile_prefix, p->n_seq, n, &sc->hdr,
-                                                             fwd_items, bwd_items);
   if (cudaMemcpyAsync(n_items, &sc->hdr.n_items, sizeof(int32_t), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
     return FLAMIA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
