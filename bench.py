@@ -606,9 +606,9 @@ def run_ours(a):
     hbm = float(peaks["hbm_gbs"])
     qkv_gbs = float(w.T) * (w.H + 2 * w.Hkv) * (3 * w.d + 1) / (quant_ms * 1e-3) / 1e9
     do_gbs = float(w.T) * w.H * (5 * w.d + 5) / (dquant_ms * 1e-3) / 1e9
-    # plan (prefix, block sort that writes the items: up to 2048 items no merge pass), quantize (Q, K, V in
-    # one), fwd, dO quantize, dQ prescale, bwd, dQ convert
-    launches_per_step = 2 + 1 + 1 + 1 + 1 + 1 + 1
+    # plan (one launch up to 2048 work items), quantize (Q, K, V in one), fwd, dO quantize, dQ prescale,
+    # bwd, dQ convert
+    launches_per_step = 1 + 1 + 1 + 1 + 1 + 1 + 1
     cpu = None
     if not a.no_cpu_baseline:
         import oracle
