@@ -180,7 +180,9 @@ size_t flamia_workspace_size(const flamia_problem_t* p);
 
 /* Builds, on the GPU, the document tables and the longest-first work lists
  * ([SUM] §3.6.2 and [READ] 4.4: a fixed-pass merge sort on the GPU, once per
- * microbatch, items issued to a persistent grid in descending cost).
+ * microbatch, items issued in descending cost to a persistent grid or, with
+ * clc, by cluster launch control).  One launch when each list fits one sort
+ * block (ceil(T/128) + n_seq <= 2048).
  * Forward items are (document, 128-query tile) with cost = key tiles visited;
  * backward items are (document, 128-key tile) with cost = query tiles
  * visited; ties keep document order.  Reads cu_seqlens on the device only.
