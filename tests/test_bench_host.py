@@ -22,6 +22,20 @@ def test_workload_selection():
     assert (w5.T, w5.H, w5.Hkv) == (2 * 65536, 32, 8)
     w3 = bench._workload(4, 3)
     assert w3.T == 8 * 16384 and sum(w3.seqlens) == w3.T and w3.outlier_channels == 2
+    # the mixed-path workload and its one-row case for profiler captures: the
+    # same documents as the full workload's first 32768-token row
+    w4 = bench._workload(4, 4)
+    one = bench._workload(1, 4)
+    assert w4.T == 4 * 32768 and one.T == 32768 and sum(one.seqlens) == one.T
+    n = 0
+    for i, length in enumerate(w4.seqlens):
+        n += length
+        if n == 32768:
+            assert one.seqlens == w4.seqlens[:i + 1]
+            break
+    else:
+        raise AssertionError("no row boundary at 32768 tokens")
+    assert (one.H, one.Hkv, one.d, one.outlier_channels, one.seed) == (16, 16, 128, 2, w4.seed)
 
 
 def _fake_profile(tmp_path, kernel, source_hash, full_bytes):
