@@ -277,6 +277,36 @@ size_t flamia_debug_workspace_offset(const flamia_problem_t* p, int32_t region);
  * workspace); flamia_plan switches it off.  Always returns FLAMIA_OK. */
 flamia_status_t flamia_debug_withhold_first_item(int32_t on);
 
+/* Test hooks (no device call): the tensor-core descriptors the kernels issue,
+ * as the library's own builders encode them, so that a host test can check
+ * each bit field against the field tables of the PTX ISA's tcgen05
+ * "Instruction descriptor" and "Shared memory descriptor" sections.
+ *
+ * flamia_debug_mma_idesc: the 32-bit instruction descriptor of one
+ *   tcgen05.mma of kind
+ *     FLAMIA_MMA_F8F6F4   kind::f8f6f4, E4M3 x E4M3, fp32 accumulator;
+ *     FLAMIA_MMA_MXF8F6F4 kind::mxf8f6f4.block_scale.scale_vec::1X, E4M3
+ *                         operands, UE8M0 scales (one per 32 K-elements);
+ *     FLAMIA_MMA_MXF4NVF4 kind::mxf4nvf4.block_scale.scale_vec::4X, E2M1
+ *                         operands, UE4M3 scales (one per 16 K-elements);
+ *   for an M x N tile (cta_group::1: M = 64 with N a multiple of 8, or
+ *   M = 128 with N a multiple of 16; 8 or 16 <= N <= 256).  a_mn / b_mn = 1
+ *   selects an MN-major operand (0 or 1; 0 for the E2M1 kind), a_sf_id /
+ *   b_sf_id the scale-factor ids of the block-scaled kinds (0..3; 0 for the
+ *   E2M1 kind, 0 for kind::f8f6f4).  Writes *out and returns FLAMIA_OK;
+ *   FLAMIA_ERR_INVALID_ARG for a NULL out or an argument outside these
+ *   ranges (then *out is untouched).
+ * flamia_debug_smem_desc: the 64-bit shared-memory matrix descriptor for a
+ *   tile at shared address saddr with leading- and stride-dimension byte
+ *   offsets lbo / sbo (all multiples of 16 below 2^18) and swizzle mode
+ *   FLAMIA_SWZ_NONE / _128B / _64B / _32B.  Same return rules. */
+typedef enum { FLAMIA_MMA_F8F6F4 = 0, FLAMIA_MMA_MXF8F6F4 = 1, FLAMIA_MMA_MXF4NVF4 = 2 } flamia_mma_kind_t;
+typedef enum { FLAMIA_SWZ_NONE = 0, FLAMIA_SWZ_128B = 2, FLAMIA_SWZ_64B = 4, FLAMIA_SWZ_32B = 6 } flamia_swizzle_t;
+flamia_status_t flamia_debug_mma_idesc(int32_t kind, uint32_t M, uint32_t N, int32_t a_mn, int32_t b_mn,
+                                       int32_t a_sf_id, int32_t b_sf_id, uint32_t* out);
+flamia_status_t flamia_debug_smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, int32_t swizzle,
+                                       uint64_t* out);
+
 /* Allocation-free work-list builder (this library's own addition; the
  * method's pages have no counterpart).  For callers that cannot allocate
  * device memory: code inside a CUDA graph under capture (cudaMalloc cannot be

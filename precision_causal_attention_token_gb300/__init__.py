@@ -22,8 +22,10 @@ ROLE_QKV, ROLE_DO = 0, 1
 EXPORTED = ("flamia_workspace_size", "flamia_plan", "flamia_quantize", "flamia_fwd", "flamia_bwd",
             "flamia_get_device_status", "flamia_clear_device_status", "flamia_status_string",
             "flamia_debug_set_phat_dump", "flamia_debug_withhold_first_item", "flamia_debug_workspace_offset",
-            "flamia_plan_noalloc")
+            "flamia_plan_noalloc", "flamia_debug_mma_idesc", "flamia_debug_smem_desc")
 WS_FWD_ITEMS, WS_BWD_ITEMS, WS_DQ_PRESCALE = range(3)
+MMA_F8F6F4, MMA_MXF8F6F4, MMA_MXF4NVF4 = range(3)
+SWZ_NONE, SWZ_128B, SWZ_64B, SWZ_32B = 0, 2, 4, 6
 
 
 class FlamiaError(RuntimeError):
@@ -76,6 +78,12 @@ def load_library(path: str = LIB_PATH):
     L.flamia_debug_workspace_offset.restype, L.flamia_debug_workspace_offset.argtypes = sz, [P, i32]
     L.flamia_debug_withhold_first_item.restype = i32
     L.flamia_debug_withhold_first_item.argtypes = [i32]
+    L.flamia_debug_mma_idesc.restype = i32
+    L.flamia_debug_mma_idesc.argtypes = [i32, ctypes.c_uint32, ctypes.c_uint32, i32, i32, i32, i32,
+                                         ctypes.POINTER(ctypes.c_uint32)]
+    L.flamia_debug_smem_desc.restype = i32
+    L.flamia_debug_smem_desc.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, i32,
+                                         ctypes.POINTER(ctypes.c_uint64)]
     L.flamia_plan_noalloc.restype = i32
     L.flamia_plan_noalloc.argtypes = [P, vp, vp, vp, vp]
     _lib = L
@@ -171,6 +179,24 @@ def flamia_debug_withhold_first_item(on: bool):
     """Test hook: the next attention launches withhold each CTA's first work
     item, so that their bounded waits run out (see include/flamia.h)."""
     _check(load_library().flamia_debug_withhold_first_item(int(bool(on))), "flamia_debug_withhold_first_item")
+
+
+def flamia_debug_mma_idesc(kind: int, M: int, N: int, a_mn: int = 0, b_mn: int = 0, a_sf_id: int = 0,
+                           b_sf_id: int = 0) -> int:
+    """Test hook: the tcgen05.mma instruction descriptor the kernels encode
+    for `kind` (MMA_F8F6F4, MMA_MXF8F6F4, MMA_MXF4NVF4) on an M x N tile."""
+    out = ctypes.c_uint32()
+    _check(load_library().flamia_debug_mma_idesc(int(kind), int(M), int(N), int(a_mn), int(b_mn), int(a_sf_id),
+                                                 int(b_sf_id), ctypes.byref(out)), "flamia_debug_mma_idesc")
+    return int(out.value)
+
+
+def flamia_debug_smem_desc(saddr: int, lbo: int, sbo: int, swizzle: int) -> int:
+    """Test hook: the shared-memory matrix descriptor the kernels encode."""
+    out = ctypes.c_uint64()
+    _check(load_library().flamia_debug_smem_desc(int(saddr), int(lbo), int(sbo), int(swizzle), ctypes.byref(out)),
+           "flamia_debug_smem_desc")
+    return int(out.value)
 
 
 def flamia_clear_device_status(ws, stream=None):

@@ -391,6 +391,38 @@ flamia_status_t flamia_debug_withhold_first_item(int32_t on) {
   return FLAMIA_OK;
 }
 
+flamia_status_t flamia_debug_mma_idesc(int32_t kind, uint32_t M, uint32_t N, int32_t a_mn, int32_t b_mn,
+                                       int32_t a_sf_id, int32_t b_sf_id, uint32_t* out) {
+  const uint32_t n_step = M == 64 ? 8u : 16u;
+  if (!out || (M != 64 && M != 128) || N < n_step || N > 256 || N % n_step) return FLAMIA_ERR_INVALID_ARG;
+  if ((a_mn | b_mn) & ~1 || (a_sf_id | b_sf_id) & ~3) return FLAMIA_ERR_INVALID_ARG;
+  switch (kind) {
+    case FLAMIA_MMA_F8F6F4:
+      if (a_sf_id || b_sf_id) return FLAMIA_ERR_INVALID_ARG;
+      *out = idesc_f8(M, N, (uint32_t)a_mn, (uint32_t)b_mn);
+      return FLAMIA_OK;
+    case FLAMIA_MMA_MXF8F6F4:
+      *out = idesc_mxf8(M, N, (uint32_t)a_mn, (uint32_t)b_mn, (uint32_t)a_sf_id, (uint32_t)b_sf_id);
+      return FLAMIA_OK;
+    case FLAMIA_MMA_MXF4NVF4:
+      if (a_mn || b_mn || a_sf_id || b_sf_id) return FLAMIA_ERR_INVALID_ARG;
+      *out = idesc_mxf4nvf4(M, N);
+      return FLAMIA_OK;
+  }
+  return FLAMIA_ERR_INVALID_ARG;
+}
+
+flamia_status_t flamia_debug_smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, int32_t swizzle,
+                                       uint64_t* out) {
+  if (!out || ((saddr | lbo | sbo) & 15u) || saddr >= (1u << 18) || lbo >= (1u << 18) || sbo >= (1u << 18))
+    return FLAMIA_ERR_INVALID_ARG;
+  if (swizzle != FLAMIA_SWZ_NONE && swizzle != FLAMIA_SWZ_128B && swizzle != FLAMIA_SWZ_64B &&
+      swizzle != FLAMIA_SWZ_32B)
+    return FLAMIA_ERR_INVALID_ARG;
+  *out = smem_desc(saddr, lbo, sbo, (uint32_t)swizzle);
+  return FLAMIA_OK;
+}
+
 flamia_status_t flamia_clear_device_status(void* ws, cudaStream_t stream) {
   if (!ws) return FLAMIA_ERR_INVALID_ARG;
   return cudaMemsetAsync(ws, 0, 2 * sizeof(uint32_t), stream) == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;

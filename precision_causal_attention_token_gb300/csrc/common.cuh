@@ -519,7 +519,7 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 // leading-dimension byte offset >> 4 in 16-29, stride-dimension byte offset
 // >> 4 in 32-45, the fixed version value 1 in bits 46-47, base offset 0,
 // swizzle mode in bits 61-63 (2 = 128B, 4 = 64B, 6 = 32B, 0 = none).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
+__host__ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
   d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
@@ -551,22 +551,6 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, uint32
 // 17-22, scale_format (bit 23) = 0 (UE4M3), M>>4 in 24-28, scale ids 0.
 __host__ __device__ constexpr uint32_t idesc_mxf4nvf4(uint32_t M, uint32_t N) {
   return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
-}
-
-// Instruction descriptor, kind::f16 with bf16 A and B, fp32 accumulate:
-// c_format(4-5)=1 (F32), a_format(7-9)=1 (BF16), b_format(10-12)=1 (BF16),
-// K-major A and B, N>>3 in 17-22, M>>4 in 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
-}
-
-// D[tmem] (+)= A[smem] * B[smem], bf16 inputs (16 K-elements), fp32 accumulate.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem], E4M3 inputs, fp32 accumulate.
