@@ -136,3 +136,39 @@ def test_nvfp4_no_clamp_minimal_scale_and_nearest_code():
     xh = oracle.dequantize_nvfp4(codes, bsc, g)
     cos = (xh * x).sum() / np.sqrt((xh * xh).sum() * (x * x).sum())
     assert cos > 0.99
+
+
+def test_scale_byte_clamps_at_the_bottom_of_ue8m0():
+    """A block whose no-clamp exponent lies below UE8M0's range is stored with
+    byte 0 (scale 2^-127, the format's smallest), and its codes are the E4M3
+    roundings of x 2^127; the two format definitions alone fix the values.
+    A block of fp32 inputs (the fp32 input option) of subnormal size with max
+    2^-130 (no-clamp exponent -138):
+    2^-130 -> 2^-3, E4M3 0x20 (exponent field 4, mantissa 0), its negative
+    0xA0; 2^-136 -> 2^-9, E4M3's smallest subnormal, 0x01; 2^-137 -> 2^-10,
+    half of it: a tie, to even, 0x00; 1.5 2^-137 -> 0.75 2^-9: up to 0x01.
+    At the top the clamp is out of reach of finite bf16 or fp32 inputs: the
+    largest bf16, (2 - 2^-7) 2^127, takes e = 120 (byte 247) and scales to
+    255, which rounds to 256 (0x78); the largest fp32 takes e = 120 too."""
+    assert oracle.noclamp_exponent(2.0 ** -130) == -138
+    assert oracle.scale_exponent(2.0 ** -130) == -127
+    assert oracle.scale_exponent(2.0 ** 200) == 127          # reachable in fp64 only
+    big = (2.0 - 2.0 ** -7) * 2.0 ** 127
+    assert float(torch.tensor(big, dtype=torch.bfloat16)) == big
+    assert oracle.scale_exponent(big) == 120
+    assert oracle.scale_exponent(float(np.finfo(np.float32).max)) == 120
+
+    x = np.zeros((64, 1, 64))
+    small = {(0, 0): 2.0 ** -130, (1, 1): -(2.0 ** -130), (2, 2): 2.0 ** -136, (3, 3): 2.0 ** -137,
+             (4, 4): 1.5 * 2.0 ** -137}
+    for (t, c), v in small.items():
+        assert float(np.float32(v)) == v                               # fp32 holds each value
+        x[t, 0, c] = v
+    x[32, 0, 0] = big
+    codes, scales = oracle.quantize_blocks(x, [0, 32, 64], 32)
+    assert (scales[0, :32] == 0).all() and (scales[0, 32:] == 247).all()
+    want = np.zeros((64, 1, 64), np.uint8)
+    for (t, c), code in zip(small, (0x20, 0xA0, 0x01, 0x00, 0x01)):
+        want[t, 0, c] = code
+    want[32, 0, 0] = 0x78
+    assert (codes == want).all()
