@@ -185,3 +185,18 @@ def test_clc_option_host_rules(lib):
     r, _ = _prob()
     r.clc, r.path = 1, fl.PATH_NVFP4_FP8
     assert fl.flamia_workspace_size(r) > 0
+
+
+def test_noalloc_plan_host_rules(lib):
+    """flamia_plan_noalloc checks its arguments on the host before it makes
+    any CUDA call: an invalid problem or a NULL output is rejected, and so is
+    a problem larger than its fixed scratch (more than 65536 tiles plus
+    documents).  No pointer below is dereferenced."""
+    p, _ = _prob()
+    a, b, n = 0x10000, 0x20000, 0x30000
+    for args in ((None, b, n), (a, None, n), (a, b, None)):
+        assert lib.flamia_plan_noalloc(p, *args, None) == fl.ERR_INVALID_ARG, args
+    q, _ = _prob(H=3)
+    assert lib.flamia_plan_noalloc(q, a, b, n, None) == fl.ERR_INVALID_ARG
+    big, _ = _prob(T=128 * 70000)
+    assert lib.flamia_plan_noalloc(big, a, b, n, None) == fl.ERR_UNSUPPORTED
